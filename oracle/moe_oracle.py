@@ -1,0 +1,296 @@
+"""CPU oracle for the forward pass of one top-k-routed Mixture-of-Experts FFN layer.
+
+TEST INFRASTRUCTURE. This module is a plain, slow, float64 statement of what the
+layer computes, used only to check the CUDA library. Only the test suite, the
+package's ``smoke()`` entry and ``bench.py``'s CPU-baseline leg may import it; the
+library itself never does, and it shares no code, table or helper with the CUDA
+path. It does not import the library or its input generator: every function takes
+plain arrays.
+
+Sources (page title, then section):
+
+* [GATE]  "Mixture-of-Experts (MoE) Architecture and Expert Parallelism",
+          section 2 "The Gating Network Formulation": H(x) = x W_g + eps,
+          G(x) = Softmax(KeepTopK(H(x), K)), y = sum_{i in TopK} G_i(x) Expert_i(x);
+          KeepTopK keeps the K largest coordinates and sets the rest to -inf.
+* [EPSH]  "EP Math - Expert Parallelism (MoE)", "What expert parallelism actually
+          shards" and "Placing experts across devices": E experts, each a full FFN,
+          E/D whole experts per device, E divisible by D.
+* [CAP]   same page, "Capacity factor: fixing buffer sizes": C = f * N * k / E,
+          rounded up.
+* [DROP]  same page, "Token drop: what overflow costs": an assignment past the
+          capacity is not processed; it behaves as if the expert output were zero
+          (the token still passes through the residual, which the caller adds).
+* [A2A]   same page, "The dispatch all-to-all" / "The combine all-to-all": each
+          assignment is a d-vector sent to its expert; the combine weights the k
+          returned vectors by the gates and sums them.
+* [MINC]  "MoE Expert Parallelism Sizing: Traffic, Capacity, Fabric",
+          "Cross-framework notes": a minimum capacity per expert regardless of the
+          capacity factor.
+* [SWI]   same page, "Memory residency for the same shape": the gated three-matrix
+          expert form (gate, up, down).
+
+Readings where the pages are silent (each is listed in the design notes too):
+
+* ties in KeepTopK go to the lower expert id, and the kept slots are ordered by
+  descending logit;
+* the optional per-expert router bias is added to H before KeepTopK, so it enters
+  both the selection and the softmax, like the eps term;
+* overflow is dropped in ascending token order: an expert keeps its first C
+  assignments by token index;
+* rows are ordered by (expert, token); the list of dropped assignments is ordered
+  the same way (expert, then token);
+* a dropped slot's gate is not renormalised over the kept slots;
+* SwiGLU expert: silu(x W_gate) * (x W_up) then W_down, silu(z) = z / (1 + e^-z),
+  no biases; ReLU expert: relu(x W_1) W_2.
+
+Every arithmetic step runs in float64 on exact float64 copies of the inputs (bf16
+and fp32 values are exact in float64). ``round_to_bf16`` is only for the optional
+"faithful" diagnostic that rounds at the points where the GPU rounds.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+__all__ = [
+    "router_logits",
+    "keep_topk",
+    "kept_softmax",
+    "expert_capacity",
+    "dispatch",
+    "expert_relu",
+    "expert_swiglu",
+    "silu",
+    "combine",
+    "moe_forward",
+    "near_tie_flags",
+    "round_to_bf16",
+]
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------- router
+def router_logits(x, Wg, bias=None) -> np.ndarray:
+    """H = x . W_g (+ b), [T, E] float64.  [GATE]: H(x) = x W_g + eps with eps = 0.
+
+    ``x`` is [T, d], ``Wg`` is [d, E] (the page's W_g in R^{d x E}); ``bias`` is an
+    optional [E] per-expert term added to every token's logits.
+    """
+    H = _f64(x) @ _f64(Wg)
+    if bias is not None:
+        H = H + _f64(bias)[None, :]
+    return H
+
+
+def keep_topk(H, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, [T, k] int64.  [GATE] KeepTopK.
+
+    Slot j holds the (j+1)-th largest logit. Equal logits rank the lower expert id
+    first: the sort key is (-H[t, e], e), ascending.
+    """
+    H = _f64(H)
+    T, E = H.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    expert_id = np.broadcast_to(np.arange(E), H.shape)
+    order = np.lexsort((expert_id, -H), axis=-1)  # last key is the primary key
+    return order[:, :k].astype(np.int64)
+
+
+def kept_softmax(H, idx) -> np.ndarray:
+    """Gates G = Softmax(KeepTopK(H)), returned at the kept slots, [T, k].  [GATE]
+
+    Written as the definition: every coordinate outside the top k is set to -inf,
+    a softmax runs over all E coordinates (exp(-inf) = 0), and the kept entries are
+    read back in slot order.
+    """
+    H = _f64(H)
+    T, E = H.shape
+    rows = np.arange(T)[:, None]
+    masked = np.full_like(H, -np.inf)
+    masked[rows, idx] = H[rows, idx]
+    shifted = masked - masked.max(axis=1, keepdims=True)
+    p = np.exp(shifted)
+    G = p / p.sum(axis=1, keepdims=True)
+    return G[rows, idx]
+
+
+def near_tie_flags(H, k: int, rel: float = 1e-6):
+    """Tokens whose top-k selection or slot order rests on a near tie.
+
+    Returns (set_tie, order_tie), both [T] bool. ``set_tie``: the k-th and (k+1)-th
+    largest logits differ by less than ``rel`` relative to the larger magnitude, so
+    a different but equally valid rounding could pick another set. ``order_tie``:
+    two adjacent kept logits are that close, so the slot order could differ.
+    """
+    H = _f64(H)
+    T, E = H.shape
+    s = -np.sort(-H, axis=1)
+
+    def close(a, b):
+        scale = np.maximum(np.abs(a), np.abs(b))
+        return (a - b) < rel * scale
+
+    set_tie = np.zeros(T, bool) if k >= E else close(s[:, k - 1], s[:, k])
+    order_tie = np.zeros(T, bool)
+    for j in range(k - 1):
+        order_tie |= close(s[:, j], s[:, j + 1])
+    return set_tie, order_tie
+
+
+# ------------------------------------------------------------------------- dispatch
+def expert_capacity(T: int, k: int, E: int, capacity_factor, min_capacity: int = 0):
+    """Per-expert capacity C = ceil(f * T * k / E), floored at ``min_capacity``.
+
+    [CAP] gives C = f N k / E rounded up (N = the tokens this device holds here);
+    [MINC] adds the floor. ``capacity_factor`` None means dropless (returns None).
+    The factor is taken as an exact rational: a decimal string such as "1.25", a
+    Fraction, or an int; a float is converted by its exact binary value.
+    """
+    if capacity_factor is None:
+        return None
+    f = Fraction(capacity_factor)
+    if f < 0:
+        raise ValueError("capacity factor must be >= 0")
+    C = math.ceil(f * T * k / E)
+    return max(C, int(min_capacity))
+
+
+def dispatch(idx, E: int, capacity=None, D: int = 1) -> dict:
+    """Group the T*k assignments by expert, dropping overflow.  [A2A], [CAP], [DROP]
+
+    Assignment a = t*k + j is token t's j-th slot. For each expert in ascending id
+    the assignments routed to it are listed by ascending token index; the first
+    ``capacity`` of them are kept (all of them when ``capacity`` is None) and the
+    rest are dropped. Kept assignments take consecutive rows in that order, so the
+    row segment of expert e is [offsets[e], offsets[e+1]). With D virtual ranks,
+    rank r owns experts [r E/D, (r+1) E/D) [EPSH], and its rows start at
+    rank_offsets[r].
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    if E % D != 0:
+        raise ValueError("E must be divisible by D")
+    counts_routed = np.zeros(E, np.int64)
+    counts_kept = np.zeros(E, np.int64)
+    kept_ids, dropped_ids = [], []
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)  # row-major scan: ascending token index
+        a = tok * k + slot
+        counts_routed[e] = a.size
+        keep = a if capacity is None else a[:capacity]
+        counts_kept[e] = keep.size
+        kept_ids.append(keep)
+        dropped_ids.append(a[keep.size:])
+    row_src = np.concatenate(kept_ids).astype(np.int64)
+    drop_list = np.concatenate(dropped_ids).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts_kept)]).astype(np.int64)
+    pos = np.full(T * k, -1, np.int64)
+    pos[row_src] = np.arange(row_src.size)
+    rank_offsets = offsets[np.arange(D + 1) * (E // D)]
+    return dict(
+        counts_routed=counts_routed,
+        counts_kept=counts_kept,
+        offsets=offsets,
+        row_src=row_src,
+        pos=pos,
+        drop_list=drop_list,
+        n_dropped=int(drop_list.size),
+        rank_offsets=rank_offsets,
+        capacity=capacity,
+    )
+
+
+# -------------------------------------------------------------------------- experts
+def silu(z):
+    """silu(z) = z / (1 + e^-z)."""
+    z = _f64(z)
+    return z / (1.0 + np.exp(-z))
+
+
+def expert_relu(X, W1, W2) -> np.ndarray:
+    """ReLU FFN expert: relu(X W1) W2, with W1 [d, F] and W2 [F, d]."""
+    return np.maximum(_f64(X) @ _f64(W1), 0.0) @ _f64(W2)
+
+
+def expert_swiglu(X, Wgate, Wup, Wdown, faithful: bool = False) -> np.ndarray:
+    """Gated expert [SWI]: (silu(X Wgate) * (X Wup)) Wdown; Wgate, Wup [d, F], Wdown [F, d].
+
+    ``faithful`` rounds the hidden activation to bf16 before the down projection,
+    where the GPU path stores it (diagnostic only).
+    """
+    X = _f64(X)
+    h = silu(X @ _f64(Wgate)) * (X @ _f64(Wup))
+    if faithful:
+        h = round_to_bf16(h)
+    return h @ _f64(Wdown)
+
+
+# -------------------------------------------------------------------------- combine
+def combine(G, pos, out, T: int, k: int) -> np.ndarray:
+    """y_t = sum over kept slots j of G[t, j] * out[pos[t, j]].  [GATE], [A2A], [DROP]
+
+    A dropped slot (pos = -1) contributes nothing and the remaining gates are not
+    renormalised. Slots are added in slot order.
+    """
+    out = _f64(out)
+    G = _f64(G)
+    pos = np.asarray(pos).reshape(T, k)
+    y = np.zeros((T, out.shape[1]), np.float64)
+    for j in range(k):
+        p = pos[:, j]
+        kept = p >= 0
+        y[kept] += G[kept, j, None] * out[p[kept]]
+    return y
+
+
+def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1) -> dict:
+    """The whole layer: logits, KeepTopK, kept softmax, dispatch, experts, combine.
+
+    ``expert_fn(e, X)`` returns Expert_e applied to the rows X (an [M, d] float64
+    array); for identity experts pass ``lambda e, X: X``. Returns every
+    intermediate the GPU path exposes, in float64 (y is not rounded).
+    """
+    x = _f64(x)
+    T, d = x.shape
+    H = router_logits(x, Wg, bias)
+    E = H.shape[1]
+    idx = keep_topk(H, k)
+    G = kept_softmax(H, idx)
+    disp = dispatch(idx, E, capacity, D)
+    xperm = x[disp["row_src"] // k]
+    out = np.zeros_like(xperm)
+    off = disp["offsets"]
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        if hi > lo:
+            out[lo:hi] = expert_fn(e, xperm[lo:hi])
+    y = combine(G, disp["pos"], out, T, k)
+    res = dict(H=H, idx=idx, G=G, xperm=xperm, out=out, y=y)
+    res.update(disp)
+    return res
+
+
+# ----------------------------------------------------------------------- diagnostics
+def round_to_bf16(a) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even), returned as float64.
+
+    Goes through float32 first (as the GPU does: its values are fp32 before the
+    store). Used only by the faithful diagnostic and by tests that state a
+    result in the bf16 output format.
+    """
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) & 0xFFFF0000).astype(np.uint32)
+    out = r.view(np.float32).astype(np.float64)
+    nan = np.isnan(f)
+    if nan.any():
+        out[nan] = np.nan
+    return out

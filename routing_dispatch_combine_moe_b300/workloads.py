@@ -1,0 +1,142 @@
+"""The five synthetic MoE-layer workloads and their seeded input generator.
+
+This module draws random inputs and nothing else: it holds none of the layer's
+arithmetic, so both the CUDA path and the CPU oracle can be fed from it.
+
+Recipe (every config): x ~ N(0, 1); router weight W_g ~ N(0, 1/d), fp32; expert
+weights ~ N(0, 1/fan_in). Values are drawn in fp32 and then cast to the activation
+dtype. The router-side inputs (x, W_g, the per-expert bias) come from a CPU
+generator so that they are the same whichever device receives them; expert
+weights come from a generator on the target device (seeded from the same seed),
+because the largest workload holds 22.5 GB of them.
+
+Expert weight layout (the usual "linear layer" orientation, K-major for the GEMMs):
+
+* ``W13`` [E, R, d]: for SwiGLU R = 2F, rows [0, F) are W_gate^T and rows [F, 2F)
+  are W_up^T; for ReLU R = F and the rows are W_1^T.
+* ``W2``  [E, d, F]: W_down^T (ReLU: W_2^T).
+
+So the math-layout matrices are W_gate[e] = W13[e, :F].T (d x F) and
+W_down[e] = W2[e].T (F x d).
+
+The imbalanced workload adds a per-expert router bias b_e = -lambda * s * ln(rank_e)
+with Zipf exponent s = 1.2 over a seeded random ranking of the experts (rank 1 is
+the hot expert, whose bias is 0), i.e. b_e = lambda * ln(p_rank / p_1) for Zipf
+probabilities p_r proportional to r^-s. lambda = ZIPF_LAMBDA was found by bisection
+on the oracle's routing of seed 0 so that the hot expert draws 40% of the T*k
+assignments (tests/golden/calibrate_zipf_bias.py reproduces it).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+ZIPF_LAMBDA = 1.059709  # hot expert draws 40.0% of assignments on seed 0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    d: int
+    E: int
+    k: int
+    F: int
+    act: str  # "f32" | "bf16"
+    expert: str  # "relu" | "swiglu" | "identity"
+    capacity_factor: str | None = None  # exact decimal string; None = dropless
+    min_capacity: int = 0
+    D: int = 1  # virtual expert-parallel ranks the dispatch is laid out for
+    zipf_s: float | None = None
+    note: str = field(default="", compare=False)
+
+    @property
+    def torch_act(self) -> torch.dtype:
+        return torch.float32 if self.act == "f32" else torch.bfloat16
+
+    @property
+    def act_bytes(self) -> int:
+        return 4 if self.act == "f32" else 2
+
+    @property
+    def w13_rows(self) -> int:
+        return 2 * self.F if self.expert == "swiglu" else self.F
+
+
+WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("tiny_f32", T=256, d=128, E=8, k=2, F=256, act="f32", expert="relu",
+                 note="tiny fp32 layer, ReLU experts, dropless"),
+        Workload("mixtral_bf16", T=2048, d=4096, E=8, k=2, F=14336, act="bf16",
+                 expert="swiglu", note="Mixtral-shaped layer, SwiGLU experts, dropless"),
+        Workload("dsv3_route_only", T=4096, d=7168, E=256, k=8, F=0, act="bf16",
+                 expert="identity", D=8,
+                 note="DeepSeek-V3-shaped routing+dispatch+combine, identity experts, "
+                      "8 virtual ranks of 32 experts"),
+        Workload("zipf_cf125", T=8192, d=2048, E=64, k=2, F=1408, act="bf16",
+                 expert="swiglu", capacity_factor="1.25", zipf_s=1.2,
+                 note="Zipf(1.2)-biased router, capacity factor 1.25, token-order drops"),
+        Workload("dsv3_full", T=4096, d=7168, E=256, k=8, F=2048, act="bf16",
+                 expert="swiglu", note="DeepSeek-V3-shaped full layer, 22.5 GB of experts"),
+    ]
+}
+
+# Workload order as they are listed: small parity case first, headline second.
+WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full"]
+
+
+def scaled(w: Workload, **changes) -> Workload:
+    """A copy of ``w`` with some sizes changed (for reduced-size parity cases)."""
+    fields = dict(w.__dict__)
+    fields.update(changes)
+    fields.setdefault("name", w.name)
+    return Workload(**fields)
+
+
+def zipf_bias(E: int, s: float, seed: int, lam: float | None = None) -> torch.Tensor:
+    """Per-expert router bias b_e = -lam * s * ln(rank_e) over a seeded ranking."""
+    lam = ZIPF_LAMBDA if lam is None else lam
+    g = torch.Generator().manual_seed(seed * 7919 + 17)
+    rank = torch.randperm(E, generator=g) + 1  # rank_e in 1..E
+    return (-lam * s * torch.log(rank.to(torch.float64))).to(torch.float32)
+
+
+def make_router_inputs(w: Workload, seed: int):
+    """x [T, d] (fp32 values, cast later), W_g [d, E] fp32, bias [E] or None (CPU)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(w.T, w.d, generator=g, dtype=torch.float32)
+    Wg = torch.randn(w.d, w.E, generator=g, dtype=torch.float32) / math.sqrt(w.d)
+    bias = zipf_bias(w.E, w.zipf_s, seed) if w.zipf_s is not None else None
+    return x.to(w.torch_act), Wg, bias
+
+
+def make_expert_weights(w: Workload, seed: int, device="cpu"):
+    """W13 [E, R, d] and W2 [E, d, F] in the activation dtype, drawn expert by expert."""
+    if w.expert == "identity":
+        return None, None
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(seed * 1000003 + 1)
+    W13 = torch.empty(w.E, w.w13_rows, w.d, dtype=w.torch_act, device=dev)
+    W2 = torch.empty(w.E, w.d, w.F, dtype=w.torch_act, device=dev)
+    s13, s2 = 1.0 / math.sqrt(w.d), 1.0 / math.sqrt(w.F)
+    for e in range(w.E):
+        W13[e] = torch.randn(w.w13_rows, w.d, generator=g, device=dev) * s13
+        W2[e] = torch.randn(w.d, w.F, generator=g, device=dev) * s2
+    return W13, W2
+
+
+def make_inputs(w: Workload, seed: int = 0, device="cpu") -> dict:
+    """All inputs of one workload on ``device``: x, Wg, bias, W13, W2."""
+    x, Wg, bias = make_router_inputs(w, seed)
+    W13, W2 = make_expert_weights(w, seed, device)
+    dev = torch.device(device)
+    return dict(
+        x=x.to(dev),
+        Wg=Wg.to(dev),
+        bias=None if bias is None else bias.to(dev),
+        W13=W13,
+        W2=W2,
+    )

@@ -1,0 +1,307 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+The pins come from the gating equations (closed forms, special cases that reduce
+to a library routine), brute force on tiny inputs, invariants the method fixes
+(gates sum to one, counts add up, identity experts return x) and exact small
+constructions. They are chosen so that a dropped term, a flipped sign or index, a
+transposed operand or a wrong ordering rule fails at least one of them.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as Fn
+
+from oracle import moe_oracle as orc
+from routing_dispatch_combine_moe_b300 import workloads as wl
+from tests._harness import expert_fn, f64, run_oracle
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------------- KeepTopK
+@pytest.mark.parametrize("E,k", [(2, 1), (3, 2), (5, 2), (6, 3), (8, 2), (9, 4), (10, 5), (10, 10)])
+def test_topk_matches_brute_force_subsets(E, k):
+    """The kept set is the only k-subset whose minimum beats every excluded value."""
+    r = rng(E * 31 + k)
+    H = r.normal(size=(50, E))
+    idx = orc.keep_topk(H, k)
+    for t in range(H.shape[0]):
+        winners = [
+            S for S in itertools.combinations(range(E), k)
+            if all(min(H[t, list(S)]) > H[t, o] for o in range(E) if o not in S)
+        ]
+        assert len(winners) == 1
+        assert set(idx[t].tolist()) == set(winners[0])
+        vals = H[t, idx[t]]
+        assert np.all(np.diff(vals) < 0), "slots must be in descending logit order"
+
+
+def test_topk_ties_prefer_lower_expert_id():
+    H = np.array([[1.0, 3.0, 3.0, 2.0],
+                  [0.5, 0.5, 0.5, 0.5],
+                  [-1.0, 2.0, -1.0, 2.0]])
+    assert orc.keep_topk(H, 2).tolist() == [[1, 2], [0, 1], [1, 3]]
+    assert orc.keep_topk(H, 3).tolist() == [[1, 2, 3], [0, 1, 2], [1, 3, 0]]
+    assert orc.keep_topk(H, 1).tolist() == [[1], [0], [1]]
+
+
+def test_topk_k_equals_E_is_full_descending_sort():
+    H = rng(1).normal(size=(20, 7))
+    idx = orc.keep_topk(H, 7)
+    np.testing.assert_array_equal(idx, np.argsort(-H, axis=1, kind="stable"))
+
+
+# ----------------------------------------------------------------------- gates
+def test_gates_with_k_equal_E_are_the_full_softmax():
+    H = rng(2).normal(size=(30, 9)) * 3
+    idx = orc.keep_topk(H, 9)
+    G = orc.kept_softmax(H, idx)
+    full = scipy.special.softmax(H, axis=1)
+    np.testing.assert_allclose(G, np.take_along_axis(full, idx, axis=1), rtol=1e-14, atol=0)
+
+
+def test_gates_closed_form_two_kept_of_three():
+    """Kept logits a > b, third logit excluded: G = (1/(1+e^(b-a)), 1/(1+e^(a-b)))."""
+    a, b, c = 1.7, -0.4, 1.2  # c sits between: keep top-2 = {a, c}
+    H = np.array([[a, b, c]])
+    idx = orc.keep_topk(H, 2)
+    assert idx.tolist() == [[0, 2]]
+    G = orc.kept_softmax(H, idx)[0]
+    assert G[0] == pytest.approx(1 / (1 + math.exp(c - a)), rel=1e-15)
+    assert G[1] == pytest.approx(1 / (1 + math.exp(a - c)), rel=1e-15)
+
+
+def test_gates_k1_are_one_and_sum_to_one():
+    H = rng(3).normal(size=(40, 16)) * 5
+    for k in (1, 2, 5, 16):
+        G = orc.kept_softmax(H, orc.keep_topk(H, k))
+        np.testing.assert_allclose(G.sum(axis=1), 1.0, rtol=0, atol=4e-16)
+        assert np.all(np.diff(G, axis=1) <= 0), "gates follow the descending logits"
+    assert np.all(orc.kept_softmax(H, orc.keep_topk(H, 1)) == 1.0)
+
+
+def test_gates_are_shift_invariant_and_large_logits_finite():
+    H = rng(4).normal(size=(10, 8))
+    idx = orc.keep_topk(H, 3)
+    np.testing.assert_allclose(orc.kept_softmax(H + 700.0, idx), orc.kept_softmax(H, idx), rtol=1e-12)
+
+
+def test_router_logits_bias_enters_selection_and_gates():
+    """A large bias on expert 2 puts it first for every token; its gate follows the biased logit."""
+    x = rng(5).normal(size=(6, 4))
+    Wg = rng(6).normal(size=(4, 5))
+    bias = np.array([0.0, 0.0, 50.0, 0.0, 0.0])
+    H = orc.router_logits(x, Wg, bias)
+    np.testing.assert_allclose(H, x @ Wg + bias, rtol=1e-15)
+    idx = orc.keep_topk(H, 2)
+    assert np.all(idx[:, 0] == 2)
+    G = orc.kept_softmax(H, idx)
+    assert np.all(G[:, 0] > 0.999)
+
+
+def test_router_logits_match_torch_matmul():
+    x = rng(7).normal(size=(33, 70))
+    Wg = rng(8).normal(size=(70, 12))
+    ref = torch.from_numpy(x) @ torch.from_numpy(Wg)
+    np.testing.assert_allclose(orc.router_logits(x, Wg), ref.numpy(), rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------- near ties
+def test_near_tie_flags():
+    H = np.array([[3.0, 2.0, 2.0 * (1 - 3e-7), 0.0],   # k=2: 2nd vs 3rd within 1e-6 -> set tie
+                  [3.0, 3.0 * (1 - 1e-7), 1.0, 0.0],   # 1st vs 2nd within 1e-6 -> order tie
+                  [3.0, 2.0, 1.0, 0.0]])
+    s, o = orc.near_tie_flags(H, 2)
+    assert s.tolist() == [True, False, False]
+    assert o.tolist() == [False, True, False]
+    s, o = orc.near_tie_flags(H, 4)
+    assert not s.any()
+
+
+# ----------------------------------------------------------------------- capacity
+def test_capacity_round_up_and_floor():
+    assert orc.expert_capacity(8192, 2, 64, "1.25") == 320
+    assert orc.expert_capacity(10, 1, 3, 1) == 4  # 10/3 rounds up
+    assert orc.expert_capacity(10, 1, 3, "0.9") == 3  # 9/3 exactly
+    assert orc.expert_capacity(10, 1, 3, "0.91") == 4
+    assert orc.expert_capacity(16, 2, 8, "1.0") == 4
+    assert orc.expert_capacity(16, 2, 8, "1.0", min_capacity=6) == 6
+    assert orc.expert_capacity(16, 2, 8, 0) == 0
+    assert orc.expert_capacity(16, 2, 8, None) is None
+
+
+# ----------------------------------------------------------------------- dispatch
+def _brute_dispatch(idx, E, C):
+    """Expected rows from a plain sort of (expert, token, slot) triples."""
+    T, k = idx.shape
+    triples = sorted((int(idx[t, j]), t, j) for t in range(T) for j in range(k))
+    rows, drops, seen = [], [], {}
+    for e, t, j in triples:
+        n = seen.get(e, 0)
+        seen[e] = n + 1
+        (rows if C is None or n < C else drops).append(t * k + j)
+    return rows, drops
+
+
+@pytest.mark.parametrize("C", [None, 0, 1, 3, 7, 1000])
+def test_dispatch_matches_sorted_triples(C):
+    r = rng(11)
+    T, E, k = 37, 6, 3
+    idx = np.stack([r.permutation(E)[:k] for _ in range(T)])
+    disp = orc.dispatch(idx, E, C, D=2)
+    rows, drops = _brute_dispatch(idx, E, C)
+    assert disp["row_src"].tolist() == rows
+    assert disp["drop_list"].tolist() == drops
+    assert disp["n_dropped"] == len(drops)
+    routed = np.bincount(idx.ravel(), minlength=E)
+    np.testing.assert_array_equal(disp["counts_routed"], routed)
+    kept = routed if C is None else np.minimum(routed, C)
+    np.testing.assert_array_equal(disp["counts_kept"], kept)
+    assert disp["counts_routed"].sum() == T * k
+    assert disp["counts_kept"].sum() == T * k - disp["n_dropped"]
+    np.testing.assert_array_equal(disp["offsets"], np.concatenate([[0], np.cumsum(kept)]))
+    # pos and row_src are inverse on kept rows; dropped assignments are -1
+    pos = disp["pos"]
+    assert np.all(pos[disp["row_src"]] == np.arange(len(rows)))
+    assert np.all(pos[disp["drop_list"]] == -1)
+    assert (pos >= 0).sum() == len(rows)
+    # D = 2 virtual ranks own experts [0,3) and [3,6)
+    off = disp["offsets"]
+    assert disp["rank_offsets"].tolist() == [0, off[3], off[6]]
+
+
+def test_dispatch_all_tokens_to_one_expert():
+    T, E, k = 20, 4, 1
+    idx = np.zeros((T, k), np.int64)
+    d = orc.dispatch(idx, E, capacity=5)
+    assert d["counts_routed"].tolist() == [20, 0, 0, 0]
+    assert d["counts_kept"].tolist() == [5, 0, 0, 0]
+    assert d["row_src"].tolist() == [0, 1, 2, 3, 4]
+    assert d["drop_list"].tolist() == list(range(5, 20))
+
+
+# ----------------------------------------------------------------------- experts
+def test_swiglu_closed_form_scalar():
+    """d = F = 1: y = silu(x wg) (x wu) wd with silu(z) = z / (1 + e^-z)."""
+    x, wg, wu, wd = 1.5, 2.0, -3.0, 0.5
+    got = orc.expert_swiglu(np.array([[x]]), np.array([[wg]]), np.array([[wu]]), np.array([[wd]]))
+    z = x * wg
+    assert got[0, 0] == pytest.approx(z / (1 + math.exp(-z)) * (x * wu) * wd, rel=1e-15)
+    # gate and up are not interchangeable
+    swapped = orc.expert_swiglu(np.array([[x]]), np.array([[wu]]), np.array([[wg]]), np.array([[wd]]))
+    assert abs(swapped[0, 0] - got[0, 0]) > 0.1
+
+
+@pytest.mark.parametrize("kind", ["relu", "swiglu"])
+def test_single_expert_k1_layer_is_the_ffn(kind):
+    """E = 1, k = 1: the gate is 1 and the layer reduces to the FFN (torch as witness)."""
+    w = wl.Workload("t", T=19, d=24, E=1, k=1, F=40, act="f32", expert=kind)
+    inp = wl.make_inputs(w, seed=3)
+    res = run_oracle(w, inp)
+    x = inp["x"].double()
+    W13, W2 = inp["W13"][0].double(), inp["W2"][0].double()
+    if kind == "relu":
+        ref = Fn.linear(Fn.relu(Fn.linear(x, W13)), W2)
+    else:
+        g, u = Fn.linear(x, W13[: w.F]), Fn.linear(x, W13[w.F:])
+        ref = Fn.linear(Fn.silu(g) * u, W2)
+    assert np.all(res["G"] == 1.0)
+    np.testing.assert_allclose(res["y"], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_combine_closed_form_with_a_drop():
+    """Both tokens pick expert 0 first; C = 1 drops token 1's slot 0.
+
+    Token 0 routes to (0, 1), token 1 to (0, 2). y_1 must be G[1,1] * Expert_2(x_1)
+    alone: the dropped slot adds nothing and the surviving gate is not renormalised.
+    """
+    x = np.array([[1.0, 2.0], [3.0, -1.0]])
+    Wg = np.array([[1.0, 0.0, 0.5], [0.5, 0.4, 0.0]])  # H0 = (2, .8, .5), H1 = (2.5, -.4, 1.5)
+    scale = {0: 2.0, 1: -1.0, 2: 5.0}
+    res = orc.moe_forward(x, Wg, 2, lambda e, X: scale[e] * X, capacity=1)
+    H = x @ Wg
+    assert res["idx"].tolist() == [[0, 1], [0, 2]]
+    assert res["pos"].tolist() == [0, 1, -1, 2]
+    assert res["drop_list"].tolist() == [2]
+    g0 = (1 / (1 + math.exp(H[0, 1] - H[0, 0])), 1 / (1 + math.exp(H[0, 0] - H[0, 1])))
+    g1 = (1 / (1 + math.exp(H[1, 2] - H[1, 0])), 1 / (1 + math.exp(H[1, 0] - H[1, 2])))
+    np.testing.assert_allclose(res["y"][0], g0[0] * 2.0 * x[0] + g0[1] * -1.0 * x[0], rtol=1e-15)
+    np.testing.assert_allclose(res["y"][1], g1[1] * 5.0 * x[1], rtol=1e-15)
+
+
+def test_identity_experts_return_x_in_bf16():
+    """Identity experts, dropless: y = x * sum(G) = x, exactly once rounded to bf16."""
+    w = wl.Workload("t", T=300, d=64, E=16, k=4, F=0, act="bf16", expert="identity", D=4)
+    inp = wl.make_inputs(w, seed=5)
+    res = run_oracle(w, inp)
+    np.testing.assert_array_equal(orc.round_to_bf16(res["y"]), f64(inp["x"]))
+
+
+def test_zero_capacity_drops_everything_and_y_is_zero():
+    w = wl.Workload("t", T=40, d=16, E=4, k=2, F=24, act="f32", expert="relu", capacity_factor="0")
+    inp = wl.make_inputs(w, seed=6)
+    res = run_oracle(w, inp)
+    assert res["n_dropped"] == w.T * w.k
+    assert np.all(res["y"] == 0.0)
+
+
+def test_large_capacity_equals_dropless():
+    w = wl.Workload("t", T=40, d=16, E=4, k=2, F=24, act="f32", expert="swiglu")
+    inp = wl.make_inputs(w, seed=7)
+    a = run_oracle(w, inp, capacity=None)
+    b = run_oracle(w, inp, capacity=w.T * w.k)
+    np.testing.assert_array_equal(a["y"], b["y"])
+    assert b["n_dropped"] == 0
+
+
+def test_expert_relabelling_leaves_y_unchanged():
+    """Permuting expert ids (router columns and weights together) changes nothing in y."""
+    w = wl.Workload("t", T=64, d=32, E=6, k=2, F=48, act="f32", expert="swiglu")
+    inp = wl.make_inputs(w, seed=8)
+    perm = torch.tensor([3, 0, 5, 1, 4, 2])
+    inp2 = dict(inp, Wg=inp["Wg"][:, perm], W13=inp["W13"][perm], W2=inp["W2"][perm])
+    a, b = run_oracle(w, inp), run_oracle(w, inp2)
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-13, atol=1e-13)
+
+
+def test_dropless_tokens_are_independent():
+    w = wl.Workload("t", T=50, d=32, E=8, k=3, F=40, act="f32", expert="relu")
+    inp = wl.make_inputs(w, seed=9)
+    full = run_oracle(w, inp)["y"]
+    w1 = wl.Workload("t", T=1, d=32, E=8, k=3, F=40, act="f32", expert="relu")
+    for t in (0, 17, 49):
+        one = run_oracle(w1, dict(inp, x=inp["x"][t:t + 1]))["y"]
+        np.testing.assert_allclose(one[0], full[t], rtol=1e-13, atol=1e-14)
+
+
+def test_gates_scale_the_layer_linearly_in_w2():
+    w = wl.Workload("t", T=30, d=16, E=4, k=2, F=24, act="f32", expert="relu")
+    inp = wl.make_inputs(w, seed=10)
+    a = run_oracle(w, inp)["y"]
+    b = run_oracle(w, dict(inp, W2=inp["W2"] * 2))["y"]
+    np.testing.assert_allclose(b, 2 * a, rtol=1e-13, atol=1e-14)
+
+
+# ----------------------------------------------------------------------- bf16 rounding
+def test_round_to_bf16_matches_torch_cast():
+    r = rng(12)
+    v = np.concatenate([r.normal(size=5000) * 10.0 ** r.integers(-6, 6, size=5000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 65504.0, 1e-40]])
+    v32 = v.astype(np.float32)
+    ref = torch.from_numpy(v32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(orc.round_to_bf16(v32), ref)
+
+
+# ----------------------------------------------------------------------- workload recipe
+def test_zipf_workload_hot_expert_draws_forty_percent():
+    w = wl.WORKLOADS["zipf_cf125"]
+    x, Wg, bias = wl.make_router_inputs(w, 0)
+    idx = orc.keep_topk(orc.router_logits(f64(x), f64(Wg), f64(bias)), w.k)
+    share = np.bincount(idx.ravel(), minlength=w.E).max() / idx.size
+    assert abs(share - 0.40) <= 0.01
