@@ -1,0 +1,431 @@
+"""Benchmark of the MoE layer forward (route -> dispatch -> expert FFN -> combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one moe_layer_forward over one batch of the workload (default: the
+Mixtral-shaped bf16 layer, T=2048, d=4096, E=8, k=2, SwiGLU F=14336), inputs and
+weights resident in HBM, timed with CUDA events on the launching stream. Under
+torchrun each rank runs an independent replica on its own GPU (the layer needs no
+cross-GPU exchange on one device; see the design notes), so the job processes
+N * T tokens per step and the step time is the max over ranks.
+
+Prints ONE JSON line on rank 0. `--impl reference` times the float64 CPU oracle on
+a bounded token sample of the same workload on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routing_dispatch_combine_moe_b300 import abi, sizing  # noqa: E402
+from routing_dispatch_combine_moe_b300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mixtral_bf16"
+STAGES = ["route", "dispatch", "expert_up", "expert_down", "combine"]
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, local, backend="nccl"):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max of a float over ranks (identity at world size 1)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * steps * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i",
+                 str(self.gpu_index), "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks / traffic
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def file_sha(path: str) -> str:
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def load_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    rec = d.get(workload, {}).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "routing_dispatch_combine_moe_b300", "csrc", rec["source"])
+    if not os.path.exists(src) or file_sha(src) != rec["source_sha"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
+# ------------------------------------------------------------------ algorithmic work
+def algorithmic(w, rows: int) -> dict:
+    b = w.act_bytes
+    up, down = sizing.expert_gemm_flops(rows, w.d, w.F, w.expert)
+    return dict(
+        route_flops=sizing.router_flops(w.T, w.d, w.E),
+        route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.k * 8,
+        dispatch_bytes=sizing.dispatch_hbm_bytes(w.T, w.d, rows, b),
+        combine_bytes=sizing.combine_hbm_bytes(w.T, w.d, rows, b),
+        up_flops=up, down_flops=down,
+        up_bytes=(w.E * w.w13_rows * w.d + rows * w.d + rows * w.F) * b if w.expert != "identity" else 0,
+        down_bytes=(w.E * w.d * w.F + rows * w.F + rows * w.d) * b if w.expert != "identity" else 0,
+    )
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
+    """Times the float64 oracle on `tokens` tokens of the workload.
+
+    Expert weights are converted to float64 once ("model load", untimed) and kept in
+    `cache` across calls.
+    """
+    from oracle import moe_oracle as orc  # the timed CPU baseline is the oracle, as it stands
+    from oracle.packed import expert_fn, f64
+
+    rng = np.random.default_rng(seed)
+    sel = np.sort(rng.choice(w.T, size=min(tokens, w.T), replace=False))
+    x = f64(inp["x"][torch.as_tensor(sel, device=inp["x"].device)])
+    Wg, bias = f64(inp["Wg"]), f64(inp.get("bias"))
+    cache = {} if cache is None else cache
+    fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, cache=cache)
+    if w.expert != "identity":  # model load: the experts this sample uses, converted once
+        idx = orc.keep_topk(orc.router_logits(x, Wg, bias), w.k)
+        for e in np.unique(idx):
+            fn(int(e), np.zeros((1, w.d)))
+    cap = orc.expert_capacity(len(sel), w.k, w.E, w.capacity_factor, w.min_capacity)
+    t0 = time.perf_counter()
+    orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D)
+    dt = time.perf_counter() - t0
+    threads = cpu_threads()
+    return dict(value=len(sel) / dt, seconds=dt, tokens=len(sel), cores=threads)
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_tokens(w, max_tokens: int = 64, mem_budget: float = 24e9) -> int:
+    """Tokens per oracle sample, bounded so the float64 copies of the experts it touches fit mem_budget."""
+    if w.expert == "identity":
+        return min(w.T, max_tokens)
+    per_expert = (w.w13_rows + w.F) * w.d * 8
+    if w.E * per_expert <= mem_budget:
+        return min(w.T, max_tokens)
+    return max(1, min(w.T, max_tokens, int(mem_budget / per_expert) // w.k))
+
+
+# ------------------------------------------------------------------ arms
+def run_ours(args, w, world, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    inp = wl.make_inputs(w, seed=rank, device=device)
+    cfg = abi.config_for(w)
+    ws = abi.workspace(cfg, device)
+    y = torch.empty(w.T, w.d, dtype=w.torch_act, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(events=None):
+        if events is None:
+            abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"), y, ws)
+        else:
+            abi.moe_layer_forward_traced(cfg, inp["x"], inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"),
+                                         y, ws, events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    view = abi.moe_workspace_get_view(cfg, ws)
+    flags = abi.moe_read_status(view.status)
+    if flags:
+        raise RuntimeError(f"device status flags {flags:#x} after warm-up")
+    base = ws.data_ptr()
+    offs = ws[view.offsets - base:view.offsets - base + 4 * (w.E + 1)].view(torch.int32).cpu().numpy()
+    rank_offs = ws[view.rank_offsets - base:view.rank_offsets - base + 4 * (w.D + 1)].view(torch.int32).cpu().numpy()
+    counts = ws[view.counts_routed - base:view.counts_routed - base + 4 * w.E].view(torch.int32).cpu().numpy()
+    n_dropped = int(ws[view.n_dropped - base:view.n_dropped - base + 4].view(torch.int32).cpu()[0])
+    rows = int(offs[-1])
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for ev in events:  # materialise the event handles before timing
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(events[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = start.elapsed_time(end)
+    stage_ms = {s: float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in events])) for j, s in enumerate(STAGES)}
+    flags = abi.moe_read_status(view.status)
+    max_ms = reduce_max(total_ms, world, device)
+
+    # end to end through the host-buffer entry point: H2D of x, forward, D2H of y each step
+    ws_host = abi.workspace(cfg, device, host=True)
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        abi.moe_layer_forward_host(cfg, x_host, inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"), y_host,
+                                   ws_host)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        abi.moe_layer_forward_host(cfg, x_host, inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"), y_host,
+                                   ws_host)
+    e2e_s = reduce_max(time.perf_counter() - t0, world, device)
+    del ws_host
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_tokens_per_s(w, inp, oracle_sample_tokens(w))
+        cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+               "sample": f"{r['tokens']} random tokens of the workload, float64 numpy oracle "
+                         f"(route, dispatch, experts, combine), {r['seconds']:.2f} s; expert weights converted "
+                         f"to float64 once before timing"}
+
+    if rank != 0:
+        return None
+    work = algorithmic(w, rows)
+    peaks, peak_src = load_peaks()
+    value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
+    dc_bytes = work["dispatch_bytes"] + work["combine_bytes"]
+    dc_ms = stage_ms["dispatch"] + stage_ms["combine"]
+    gemm_ms = stage_ms["expert_up"] + stage_ms["expert_down"]
+    gemm_flops = work["up_flops"] + work["down_flops"]
+    # dominant kernel of the step
+    kernel_work = {
+        "route": ("route_kernel", "alu", work["route_flops"]),
+        "dispatch": ("dispatch (count+scan+scatter+gather)", "hbm", work["dispatch_bytes"]),
+        "expert_up": ("grouped_gemm_kernel<SwiGLU> (up)", "tensor", work["up_flops"]),
+        "expert_down": ("grouped_gemm_kernel<Plain> (down)", "tensor", work["down_flops"]),
+        "combine": ("combine_kernel", "hbm", work["combine_bytes"]),
+    }
+    dom = max(STAGES, key=lambda s: stage_ms[s])
+    kname, bound, amount = kernel_work[dom]
+    dom_s = stage_ms[dom] / 1e3
+    if bound == "tensor":
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": amount / dom_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16 burst"}
+    elif bound == "hbm":
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": amount / dom_s / 1e9, "peak": peak, "unit": "GB/s",
+                "peak_source": f"{peak_src} copy bandwidth"}
+    else:
+        fp32_peak = 148 * 128 * 2 * float(peaks.get("sm_max_mhz", 2032.0)) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": amount / dom_s / 1e12, "peak": fp32_peak, "unit": "TFLOP/s",
+                "peak_source": "148 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = kname
+    roof["traffic"] = load_traffic(w.name, dom)
+    roof["ms_per_launch"] = stage_ms[dom]
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.act, "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "F": w.F, "expert": w.expert,
+                   "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
+                         "dispatched rows" % (w.E * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
+                                              if w.expert != "identity" else 0.0,
+                                              rows * w.d * w.act_bytes / 1e6)},
+        "roofline": roof,
+        "dispatch_combine_gbs": dc_bytes / (dc_ms / 1e3) / 1e9 if dc_ms > 0 else None,
+        "dispatch_combine_frac_hbm": (dc_bytes / (dc_ms / 1e3) / 1e9) / float(peaks["hbm_gbs"]) if dc_ms > 0 else None,
+        "grouped_gemm_tflops": gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 and gemm_flops else None,
+        "grouped_gemm_frac_bf16_peak": (gemm_flops / (gemm_ms / 1e3) / 1e12) / float(peaks["bf16_tflops"])
+        if gemm_ms > 0 and gemm_flops else None,
+        "stage_ms": stage_ms,
+        "routing": {"rows": rows, "dropped": n_dropped, "hist": sizing.histogram_summary(counts),
+                    "rank_imbalance": sizing.imbalance_ratio(np.diff(rank_offs)),
+                    "remote_dispatch_bytes": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),
+                    "pages_dispatch_bytes": sizing.dispatch_bytes_per_direction(w.T, w.k, w.d, w.act_bytes,
+                                                                                w.D if w.D > 1 else None)},
+        "device_status": flags,
+        "clocks": clocks.summary(),
+        "e2e": {"value": job_throughput(w.T, args.steps, world, e2e_s), "unit": UNIT,
+                "h2d_bytes_per_step": w.T * w.d * w.act_bytes, "d2h_bytes_per_step": w.T * w.d * w.act_bytes,
+                "api": "moe_layer_forward_host"},
+        "gpu_launches": abi.moe_kernels_per_forward(cfg) * args.steps,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def run_reference(args, w, world, rank):
+    """The float64 CPU oracle on bounded token samples of the same workload."""
+    if rank != 0:
+        return None
+    inp = wl.make_inputs(w, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    per_step = []
+    cache = {}
+    tokens = min(args.ref_tokens, oracle_sample_tokens(w))
+    for i in range(args.warmup + args.steps):
+        r = oracle_tokens_per_s(w, inp, tokens, seed=i, cache=cache)
+        if i >= args.warmup:
+            per_step.append(r)
+    tokens = sum(r["tokens"] for r in per_step)
+    secs = sum(r["seconds"] for r in per_step)
+    value = tokens / secs
+    cores = per_step[0]["cores"]
+    sample = (f"each step: {tokens} random tokens of the workload through the float64 numpy oracle "
+              f"(route, dispatch, experts, combine); expert weights converted to float64 once, untimed")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / len(per_step) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "F": w.F, "expert": w.expert},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=wl.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        line = run_reference(args, w, world, rank)
+    else:
+        init_dist(world, local)
+        line = run_ours(args, w, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+/*
+ * moe.h - C ABI of the B300 (sm_103a) library for the forward pass of one
+ * top-k-routed Mixture-of-Experts FFN layer on one GPU.
+ *
+ * What the layer computes (sources, by page title and section):
+ *   - "Mixture-of-Experts (MoE) Architecture and Expert Parallelism",
+ *     section 2 "The Gating Network Formulation":
+ *       H(x) = x W_g (+ eps),  G(x) = Softmax(KeepTopK(H(x), k)),
+ *       y = sum over the k kept experts i of G_i(x) * Expert_i(x).
+ *   - "EP Math - Expert Parallelism (MoE)": "The dispatch all-to-all" and
+ *     "The combine all-to-all" (each of the T*k assignments is a d-vector sent to
+ *     its expert and returned), "Capacity factor: fixing buffer sizes"
+ *     (C = f*T*k/E, rounded up) and "Token drop: what overflow costs" (overflow is
+ *     not processed and contributes zero; the caller's residual carries x).
+ *   - "MoE Expert Parallelism Sizing: Traffic, Capacity, Fabric",
+ *     "First-order dispatch and combine bytes": an all-to-all input buffer holds
+ *     one contiguous chunk per destination rank.
+ *
+ * On one GPU the dispatch and combine all-to-alls are on-device permutations:
+ * dispatched rows are grouped by expert, experts ascending, tokens ascending
+ * within an expert, so rank r of D virtual ranks (experts [r*E/D,(r+1)*E/D))
+ * owns one contiguous chunk of rows.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_host are host memory; every other pointer is device
+ *     memory on the current CUDA device, allocated and owned by the caller. The
+ *     library allocates no memory and keeps no per-call state; scratch lives in
+ *     a caller-provided workspace.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) without host synchronisation, so a sequence of calls can be
+ *     captured in a CUDA graph. Exceptions: moe_read_status and
+ *     moe_layer_forward_host (see their comments).
+ *   - Argument errors are returned synchronously as a MOE_ERR_* code before any
+ *     work is enqueued. Errors found on the device (an expert id or row index
+ *     out of range, a bounded wait that gave up) set bits in a device status
+ *     word (MOE_DEV_* flags) instead; read it with moe_read_status.
+ *   - Layouts are row-major. Activation rows (x, dispatched rows, expert
+ *     outputs, y) must start on 16-byte boundaries: d * sizeof(act) % 16 == 0
+ *     and every activation pointer 16-byte aligned. Index arrays are int32.
+ *   - The functions are thread-safe; the same workspace must not be used by two
+ *     calls that may overlap on the GPU.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
+
+/* Return codes. */
+#define MOE_OK 0
+#define MOE_ERR_ARG 1         /* null pointer, non-positive size, k > E, E % D != 0, ... */
+#define MOE_ERR_ALIGN 2       /* pointer or activation row not 16-byte aligned */
+#define MOE_ERR_WORKSPACE 3   /* workspace smaller than the matching *_workspace_bytes */
+#define MOE_ERR_UNSUPPORTED 4 /* valid request this build does not implement (limits below) */
+#define MOE_ERR_CUDA 5        /* a CUDA runtime call failed; moe_last_cuda_error() says which */
+#define MOE_ERR_DEVICE 6      /* moe_read_status found device error flags */
+
+/* Device status flags (bits of the device status word). */
+#define MOE_DEV_ERR_INDEX 0x1   /* an expert id or row index out of range was skipped */
+#define MOE_DEV_ERR_TIMEOUT 0x2 /* a bounded pipeline wait gave up; that kernel's output is incomplete */
+
+/* Activation dtypes and expert kinds. */
+#define MOE_F32 0
+#define MOE_BF16 1
+#define MOE_EXPERT_IDENTITY 0 /* Expert_e(x) = x (routing + dispatch + combine only) */
+#define MOE_EXPERT_RELU 1     /* relu(x W1) W2 */
+#define MOE_EXPERT_SWIGLU 2   /* (silu(x W_gate) * (x W_up)) W_down, silu(z) = z / (1 + e^-z) */
+
+/* Limits of this build. */
+#define MOE_MAX_K 16        /* experts per token */
+#define MOE_MAX_E 256       /* routed experts */
+
+typedef struct moe_config {
+    int32_t T;           /* tokens (rows of x), >= 1 */
+    int32_t d;           /* hidden size, >= 1 */
+    int32_t E;           /* routed experts, 1..MOE_MAX_E */
+    int32_t k;           /* experts kept per token, 1..min(E, MOE_MAX_K) */
+    int32_t F;           /* expert FFN width (ignored for identity experts) */
+    int32_t D;           /* virtual expert-parallel ranks, E % D == 0 (1 = none) */
+    int32_t act_dtype;   /* MOE_F32 or MOE_BF16: x, dispatched rows, h, expert outputs, y */
+    int32_t expert_kind; /* MOE_EXPERT_* */
+    int64_t capacity;    /* tokens each expert keeps; < 0 = dropless (see moe_capacity) */
+} moe_config;
+
+/* Where the dispatch writes its routing map (all device int32 arrays). */
+typedef struct moe_dispatch_map {
+    int32_t* counts_routed; /* [E]   assignments routed to each expert */
+    int32_t* counts_kept;   /* [E]   min(counts_routed, capacity) */
+    int32_t* offsets;       /* [E+1] exclusive scan of counts_kept; rows of expert e are [offsets[e], offsets[e+1]) */
+    int32_t* rank_offsets;  /* [D+1] offsets[r*E/D]: virtual rank r's send chunk is [rank_offsets[r], rank_offsets[r+1]) */
+    int32_t* pos;           /* [T*k] row of assignment t*k+j, or -1 if it was dropped */
+    int32_t* row_src;       /* [T*k] assignment t*k+j held by each row; entries [0, offsets[E]) are written */
+    int32_t* drop_list;     /* [T*k] dropped assignments, ordered by (expert, token); [0, n_dropped) written */
+    int32_t* n_dropped;     /* [1]   number of dropped assignments */
+} moe_dispatch_map;
+
+/* Pointers into a moe_layer_forward workspace (all device memory inside it). */
+typedef struct moe_workspace_view {
+    int32_t* status;     /* device status word (MOE_DEV_* flags) */
+    int32_t* topk_idx;   /* [T*k] */
+    float* topk_gate;    /* [T*k] */
+    moe_dispatch_map map;
+    void* xperm;         /* [T*k, d] act: dispatched rows (the dispatch "send buffer") */
+    void* h;             /* [T*k, F] act: expert hidden activations (NULL for identity) */
+    void* out;           /* [T*k, d] act: expert outputs (aliases xperm for identity) */
+} moe_workspace_view;
+
+/* ------------------------------------------------------------------ sizing */
+
+/* Per-expert capacity ceil(cf_num * T * k / (cf_den * E)), floored at min_capacity,
+ * in exact integer arithmetic ("EP Math", "Capacity factor": C = f T k / E rounded
+ * up; "MoE Expert Parallelism Sizing", "Cross-framework notes": a minimum
+ * capacity). The capacity factor is cf_num / cf_den. Returns -1 on bad arguments
+ * (cf_den <= 0, cf_num < 0, T, k or E <= 0). */
+int64_t moe_capacity(int32_t T, int32_t k, int32_t E, int64_t cf_num, int64_t cf_den, int64_t min_capacity);
+
+/* MOE_OK if the config is valid and supported, else the code the entry points would return. */
+int moe_validate_config(const moe_config* cfg);
+
+/* Workspace bytes each entry point needs (0 when cfg is invalid). */
+size_t moe_dispatch_workspace_bytes(const moe_config* cfg);
+size_t moe_ffn_workspace_bytes(const moe_config* cfg);
+size_t moe_workspace_bytes(const moe_config* cfg);      /* moe_layer_forward */
+size_t moe_workspace_bytes_host(const moe_config* cfg); /* moe_layer_forward_host */
+
+/* Fill `view` with the buffers moe_layer_forward keeps inside `ws`. Pure host
+ * arithmetic on the pointer; touches no memory. */
+int moe_workspace_get_view(const moe_config* cfg, void* ws, size_t ws_bytes, moe_workspace_view* view);
+
+/* Number of kernels one moe_layer_forward enqueues for this config. */
+int moe_kernels_per_forward(const moe_config* cfg);
+
+/* ------------------------------------------------------------ the hot path */
+
+/* Router: logits H = x W_g (+ bias) in fp32, KeepTopK and the softmax over the kept
+ * logits ("Mixture-of-Experts (MoE) Architecture and Expert Parallelism", section 2).
+ *   x         [T, d] act dtype
+ *   Wg        [d, E] fp32 (the page's W_g in R^{d x E})
+ *   bias      [E] fp32 added to every token's logits before KeepTopK, or NULL
+ *   topk_idx  [T, k] int32 out: kept experts, slot 0 = largest logit; equal logits
+ *             rank the lower expert id first
+ *   topk_gate [T, k] fp32 out: G = exp(H_j - H_max) / sum over kept slots
+ * Logits are fp32 sums of fp32 products (x is promoted exactly). */
+int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
+              int32_t* topk_idx, float* topk_gate, moe_stream_t stream);
+
+/* Dispatch: groups the T*k assignments by expert, keeps the first `capacity` of
+ * each expert in token order, and gathers the kept rows of x into `xperm`
+ * ("EP Math": "The dispatch all-to-all", "Capacity factor", "Token drop").
+ *   x        [T, d] act;  topk_idx [T, k] int32 (ids outside [0, E) are skipped
+ *            and flagged MOE_DEV_ERR_INDEX)
+ *   map      output arrays (see moe_dispatch_map)
+ *   xperm    [T*k, d] act out: row r = x[row_src[r] / k]; rows [0, offsets[E]) written
+ *   ws       >= moe_dispatch_workspace_bytes(cfg) bytes; its first 4 bytes are the
+ *            device status word, which this call clears first.
+ * Bit-exact and deterministic: the result does not depend on scheduling. */
+int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                 const moe_dispatch_map* map, void* xperm, void* ws, size_t ws_bytes,
+                 moe_stream_t stream);
+
+/* Grouped expert FFN over the dispatched rows: for each expert e, rows
+ * [offsets[e], offsets[e+1]) of xperm go through Expert_e ("EP Math", "What expert
+ * parallelism actually shards": each expert is a full FFN with its own weights).
+ *   xperm   [T*k, d] act;  offsets [E+1] int32 (from moe_dispatch)
+ *   W13     SwiGLU: [E, 2F, d] act, rows [0,F) = W_gate^T, rows [F,2F) = W_up^T;
+ *           ReLU:   [E, F, d]  act (W1^T).   (The usual linear-layer layout.)
+ *   W2      [E, d, F] act (W_down^T / W2^T)
+ *   h       [T*k, F] act out: hidden activation of each row
+ *   out     [T*k, d] act out: expert output of each row
+ * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation, one
+ * rounding to bf16 for h and for out); fp32 runs on the fp32 FMA units.
+ * Requires F * sizeof(act) % 16 == 0 besides the row rule. ws >=
+ * moe_ffn_workspace_bytes(cfg); its first 4 bytes are the status word (cleared). */
+int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets,
+                   const void* W13, const void* W2, void* h, void* out,
+                   void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine: y[t] = sum over slots j with pos[t*k+j] >= 0 of topk_gate[t*k+j] * out[pos[t*k+j]],
+ * summed in fp32 in slot order and rounded once ("Mixture-of-Experts (MoE)
+ * Architecture and Expert Parallelism", section 2; "EP Math", "The combine
+ * all-to-all"; "Token drop": a dropped slot adds nothing and the gates are not
+ * renormalised). A row index >= T*k is skipped and flagged in `status` if
+ * status is not NULL. Deterministic, no atomics.
+ *   out [T*k, d] act; topk_gate [T, k] fp32; pos [T, k] int32; y [T, d] act out. */
+int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate,
+                const int32_t* pos, void* y, int32_t* status, moe_stream_t stream);
+
+/* The whole layer: route, dispatch, expert FFN, combine. Intermediates live in ws
+ * (layout: moe_workspace_get_view). ws >= moe_workspace_bytes(cfg); the status word
+ * is cleared at the start. W13/W2 may be NULL for identity experts. y [T, d] act. */
+int moe_layer_forward(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
+                      const void* W13, const void* W2, void* y, void* ws, size_t ws_bytes,
+                      moe_stream_t stream);
+
+/* moe_layer_forward that also records CUDA events between its stages, for timing:
+ * events[0] before the router, [1] after it, [2] after the dispatch, [3] after the
+ * expert up-projection, [4] after the down-projection, [5] after the combine
+ * (for identity experts [3] and [4] are recorded right after [2]). `events` holds
+ * cudaEvent_t handles; n_events >= 6 (the first 6 are used). */
+int moe_layer_forward_traced(const moe_config* cfg, const void* x, const float* Wg,
+                             const float* bias, const void* W13, const void* W2, void* y,
+                             void* ws, size_t ws_bytes, moe_stream_t stream,
+                             void* const* events, int32_t n_events);
+
+/* The whole layer from and to host memory: copies x_host into the workspace,
+ * runs moe_layer_forward, copies y back into y_host, all on `stream`, and
+ * synchronises the stream before returning (so y_host is ready). x_host and
+ * y_host should be page-locked for asynchronous copies. ws >=
+ * moe_workspace_bytes_host(cfg). The weights stay device pointers. */
+int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const float* Wg,
+                           const float* bias, const void* W13, const void* W2, void* y_host,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------- diagnostics */
+
+/* Synchronises `stream`, copies the status word at `status_dev` to *flags_host
+ * (may be NULL) and returns MOE_OK if it is zero, MOE_ERR_DEVICE otherwise.
+ * For diagnostics, not for the hot path. */
+int moe_read_status(const int32_t* status_dev, int32_t* flags_host, moe_stream_t stream);
+
+/* Human-readable text of a return code. */
+const char* moe_status_string(int code);
+
+/* Text of the last CUDA error this thread saw inside the library ("" if none). */
+const char* moe_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

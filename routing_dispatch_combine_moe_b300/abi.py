@@ -1,0 +1,271 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h), same names as the C entry points.
+
+Argument marshalling only: tensors become device pointers, the current torch CUDA
+stream becomes the cudaStream_t, non-zero return codes become MoeError. Every step
+of the layer runs in the library's CUDA kernels; there is no fallback, and loading
+fails loudly when the shared library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from fractions import Fraction
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
+
+MOE_OK, MOE_ERR_ARG, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE = 0, 1, 2, 3
+MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = 4, 5, 6
+MOE_DEV_ERR_INDEX, MOE_DEV_ERR_TIMEOUT = 0x1, 0x2
+MOE_F32, MOE_BF16 = 0, 1
+MOE_EXPERT_IDENTITY, MOE_EXPERT_RELU, MOE_EXPERT_SWIGLU = 0, 1, 2
+MOE_MAX_K, MOE_MAX_E = 16, 256
+EXPERT_KINDS = {"identity": MOE_EXPERT_IDENTITY, "relu": MOE_EXPERT_RELU, "swiglu": MOE_EXPERT_SWIGLU}
+ACT_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
+
+_p = ctypes.c_void_p
+_i32, _i64, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        msg = f"{where}: {status_string(code)} (code {code})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("F", _i32), ("D", _i32),
+                ("act_dtype", _i32), ("expert_kind", _i32), ("capacity", _i64)]
+
+
+class moe_dispatch_map(ctypes.Structure):
+    _fields_ = [(n, _p) for n in ("counts_routed", "counts_kept", "offsets", "rank_offsets", "pos",
+                                  "row_src", "drop_list", "n_dropped")]
+
+
+class moe_workspace_view(ctypes.Structure):
+    _fields_ = [("status", _p), ("topk_idx", _p), ("topk_gate", _p), ("map", moe_dispatch_map),
+                ("xperm", _p), ("h", _p), ("out", _p)]
+
+
+_SIGNATURES = {
+    "moe_capacity": (_i64, [_i32, _i32, _i32, _i64, _i64, _i64]),
+    "moe_validate_config": (ctypes.c_int, [ctypes.POINTER(moe_config)]),
+    "moe_dispatch_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_ffn_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_workspace_bytes_host": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_workspace_get_view": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _sz, ctypes.POINTER(moe_workspace_view)]),
+    "moe_kernels_per_forward": (ctypes.c_int, [ctypes.POINTER(moe_config)]),
+    "moe_route": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p]),
+    "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p, _p, _sz, _p]),
+    "moe_expert_ffn": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_combine": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p]),
+    "moe_layer_forward": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_layer_forward_traced": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p,
+                                                ctypes.POINTER(_p), _i32]),
+    "moe_layer_forward_host": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_read_status": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
+    "moe_version": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m routing_dispatch_combine_moe_b300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        detail = lib().moe_last_cuda_error().decode() if code == MOE_ERR_CUDA else ""
+        raise MoeError(code, where, detail)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ------------------------------------------------------------------ config
+def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None) -> moe_config:
+    """A moe_config; ``capacity`` None (dropless) or a non-negative integer."""
+    return moe_config(T=T, d=d, E=E, k=k, F=F, D=D, act_dtype=ACT_DTYPES[act],
+                      expert_kind=EXPERT_KINDS[expert], capacity=-1 if capacity is None else int(capacity))
+
+
+def moe_capacity(T, k, E, capacity_factor, min_capacity=0) -> int:
+    f = Fraction(capacity_factor)
+    c = lib().moe_capacity(T, k, E, f.numerator, f.denominator, min_capacity)
+    if c < 0:
+        raise MoeError(MOE_ERR_ARG, "moe_capacity")
+    return int(c)
+
+
+def config_for(w, capacity="auto") -> moe_config:
+    """moe_config of a workload (see workloads.Workload)."""
+    if capacity == "auto":
+        capacity = None if w.capacity_factor is None else moe_capacity(w.T, w.k, w.E, w.capacity_factor,
+                                                                       w.min_capacity)
+    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity)
+
+
+def moe_validate_config(cfg) -> int:
+    return lib().moe_validate_config(ctypes.byref(cfg))
+
+
+def moe_workspace_bytes(cfg) -> int:
+    return lib().moe_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_workspace_bytes_host(cfg) -> int:
+    return lib().moe_workspace_bytes_host(ctypes.byref(cfg))
+
+
+def moe_dispatch_workspace_bytes(cfg) -> int:
+    return lib().moe_dispatch_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_ffn_workspace_bytes(cfg) -> int:
+    return lib().moe_ffn_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_kernels_per_forward(cfg) -> int:
+    return lib().moe_kernels_per_forward(ctypes.byref(cfg))
+
+
+def workspace(cfg, device="cuda", host=False) -> torch.Tensor:
+    """A uint8 device tensor of the workspace size (memory from torch's allocator)."""
+    n = moe_workspace_bytes_host(cfg) if host else moe_workspace_bytes(cfg)
+    if n == 0:
+        _check(moe_validate_config(cfg), "workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+@dataclass
+class WorkspaceView:
+    status: int
+    topk_idx: int
+    topk_gate: int
+    counts_routed: int
+    counts_kept: int
+    offsets: int
+    rank_offsets: int
+    pos: int
+    row_src: int
+    drop_list: int
+    n_dropped: int
+    xperm: int
+    h: int | None
+    out: int
+
+
+def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
+    v = moe_workspace_view()
+    _check(lib().moe_workspace_get_view(ctypes.byref(cfg), _ptr(ws), ws.numel(), ctypes.byref(v)),
+           "moe_workspace_get_view")
+    m = v.map
+    return WorkspaceView(v.status, v.topk_idx, v.topk_gate, m.counts_routed, m.counts_kept, m.offsets,
+                         m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out)
+
+
+# ------------------------------------------------------------------ hot path
+def moe_route(cfg, x, Wg, bias, topk_idx, topk_gate, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(bias), _ptr(topk_idx), _ptr(topk_gate),
+                           _stream(stream)), "moe_route")
+
+
+def dispatch_map(counts_routed, counts_kept, offsets, rank_offsets, pos, row_src, drop_list, n_dropped):
+    return moe_dispatch_map(*[_ptr(t) for t in (counts_routed, counts_kept, offsets, rank_offsets, pos, row_src,
+                                                drop_list, n_dropped)])
+
+
+def moe_dispatch(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, ws, stream=None):
+    _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xperm),
+                              _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def moe_expert_ffn(cfg, xperm, offsets, W13, W2, h, out, ws, stream=None):
+    _check(lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(xperm), _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h),
+                                _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(cfg, out, topk_gate, pos, y, status=None, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(out), _ptr(topk_gate), _ptr(pos), _ptr(y), _ptr(status),
+                             _stream(stream)), "moe_combine")
+
+
+def moe_layer_forward(cfg, x, Wg, bias, W13, W2, y, ws, stream=None):
+    _check(lib().moe_layer_forward(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(bias), _ptr(W13), _ptr(W2), _ptr(y),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_traced(cfg, x, Wg, bias, W13, W2, y, ws, events, stream=None):
+    """``events``: six torch.cuda.Event(enable_timing=True), recorded between stages."""
+    for ev in events:
+        if ev.cuda_event == 0:  # created lazily by torch; record once to materialise
+            ev.record()
+    arr = (_p * len(events))(*[ev.cuda_event for ev in events])
+    _check(lib().moe_layer_forward_traced(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(bias), _ptr(W13), _ptr(W2),
+                                          _ptr(y), _ptr(ws), ws.numel(), _stream(stream), arr, len(events)),
+           "moe_layer_forward_traced")
+
+
+def moe_layer_forward_host(cfg, x_host, Wg, bias, W13, W2, y_host, ws, stream=None):
+    _check(lib().moe_layer_forward_host(ctypes.byref(cfg), _ptr(x_host), _ptr(Wg), _ptr(bias), _ptr(W13), _ptr(W2),
+                                        _ptr(y_host), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_layer_forward_host")
+
+
+def moe_read_status(status_ptr: int, stream=None) -> int:
+    """Synchronises the stream and returns the device status flags (0 = fine)."""
+    flags = _i32(0)
+    code = lib().moe_read_status(status_ptr, ctypes.byref(flags), _stream(stream))
+    if code not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(code, "moe_read_status")
+    return int(flags.value)
+
+
+def moe_version() -> int:
+    return lib().moe_version()
+
+
+def exported_symbols() -> list[str]:
+    """Function names declared in include/moe.h."""
+    import re
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(", text, flags=re.M)))

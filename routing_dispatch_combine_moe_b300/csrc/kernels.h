@@ -1,0 +1,71 @@
+// Launchers of the CUDA kernels (host side). Each enqueues on `stream` and returns
+// the launch's cudaError_t; argument checks happen in the C ABI layer before these.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Assignments per dispatch block: the histogram, scan and scatter kernels all cut
+// the T*k assignments into blocks of this many, in assignment order.
+constexpr int kDispatchBlock = 256;
+// Rows per tensor-core tile; the scan also emits per-expert tile offsets at this size.
+constexpr int kTileM = 128;
+
+inline int dispatch_blocks(int64_t assignments) {
+    return int((assignments + kDispatchBlock - 1) / kDispatchBlock);
+}
+
+cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
+                         int k, int32_t* topk_idx, float* topk_gate, cudaStream_t stream);
+
+struct DispatchArgs {
+    int T, d, E, k, D;
+    int64_t capacity;  // < 0: dropless
+    int act_bytes;
+    const void* x;
+    const int32_t* topk_idx;
+    int32_t* counts_routed;
+    int32_t* counts_kept;
+    int32_t* offsets;
+    int32_t* rank_offsets;
+    int32_t* pos;
+    int32_t* row_src;
+    int32_t* drop_list;
+    int32_t* n_dropped;
+    void* xperm;
+    // workspace pieces
+    int32_t* status;
+    int32_t* hist;         // [E * nblk]
+    int32_t* drop_offsets; // [E]
+};
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
+
+cudaError_t launch_combine(int act_dtype, const void* out, const float* gate, const int32_t* pos, void* y, int T,
+                           int d, int k, int32_t* status, cudaStream_t stream);
+
+struct FfnArgs {
+    int T, d, E, k, F;
+    int expert_kind;
+    int act_dtype;
+    const void* xperm;
+    const int32_t* offsets;
+    const void* W13;
+    const void* W2;
+    void* h;
+    void* out;
+    int32_t* status;
+};
+
+// bf16 experts on the tensor cores (tcgen05 + TMA).
+cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event);
+// fp32 experts on the FMA units.
+cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event);
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace moe

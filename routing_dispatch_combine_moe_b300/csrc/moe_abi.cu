@@ -1,0 +1,376 @@
+// The C ABI (include/moe.h): argument checks, workspace layout and the launch
+// sequences of the hot path. Every entry point validates on the host, returns a
+// MOE_* code synchronously, and otherwise only enqueues work on the caller's
+// stream.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+thread_local std::string g_last_cuda_error;
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+int fail_cuda(cudaError_t e, const char* where) {
+    g_last_cuda_error = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return MOE_ERR_CUDA;
+}
+
+inline int act_bytes(const moe_config* c) { return c->act_dtype == MOE_F32 ? 4 : 2; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int validate(const moe_config* c) {
+    if (!c) return MOE_ERR_ARG;
+    if (c->T < 1 || c->d < 1 || c->E < 1 || c->k < 1 || c->D < 1) return MOE_ERR_ARG;
+    if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_ARG;
+    if (c->expert_kind != MOE_EXPERT_IDENTITY && c->expert_kind != MOE_EXPERT_RELU &&
+        c->expert_kind != MOE_EXPERT_SWIGLU)
+        return MOE_ERR_ARG;
+    if (c->k > c->E) return MOE_ERR_ARG;
+    if (c->E % c->D != 0) return MOE_ERR_ARG;
+    if (c->expert_kind != MOE_EXPERT_IDENTITY && c->F < 1) return MOE_ERR_ARG;
+    if (c->E > MOE_MAX_E || c->k > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
+    if (int64_t(c->T) * c->k > int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
+    if (c->expert_kind != MOE_EXPERT_IDENTITY && (int64_t(c->F) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+struct Layout {
+    size_t status, hist, drop_offsets, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
+        n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
+    size_t dispatch_end, forward_end, host_end;
+};
+
+Layout layout(const moe_config* c) {
+    Layout L{};
+    const int64_t A = int64_t(c->T) * c->k;
+    const int nblk = dispatch_blocks(A);
+    const size_t b = size_t(act_bytes(c));
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes);
+        return at;
+    };
+    L.status = take(sizeof(int32_t));
+    L.hist = take(sizeof(int32_t) * size_t(c->E) * nblk);
+    L.drop_offsets = take(sizeof(int32_t) * size_t(c->E));
+    L.dispatch_end = o;
+    L.topk_idx = take(sizeof(int32_t) * A);
+    L.topk_gate = take(sizeof(float) * A);
+    L.counts_routed = take(sizeof(int32_t) * size_t(c->E));
+    L.counts_kept = take(sizeof(int32_t) * size_t(c->E));
+    L.offsets = take(sizeof(int32_t) * size_t(c->E + 1));
+    L.rank_offsets = take(sizeof(int32_t) * size_t(c->D + 1));
+    L.n_dropped = take(sizeof(int32_t));
+    L.pos = take(sizeof(int32_t) * A);
+    L.row_src = take(sizeof(int32_t) * A);
+    L.drop_list = take(sizeof(int32_t) * A);
+    L.xperm = take(b * A * size_t(c->d));
+    if (c->expert_kind != MOE_EXPERT_IDENTITY) {
+        L.h = take(b * A * size_t(c->F));
+        L.out = take(b * A * size_t(c->d));
+    } else {
+        L.h = 0;
+        L.out = L.xperm;
+    }
+    L.forward_end = o;
+    L.x_stage = take(b * size_t(c->T) * c->d);
+    L.y_stage = take(b * size_t(c->T) * c->d);
+    L.host_end = o;
+    return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + off);
+}
+
+void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
+    const Layout L = layout(c);
+    v->status = at<int32_t>(ws, L.status);
+    v->topk_idx = at<int32_t>(ws, L.topk_idx);
+    v->topk_gate = at<float>(ws, L.topk_gate);
+    v->map.counts_routed = at<int32_t>(ws, L.counts_routed);
+    v->map.counts_kept = at<int32_t>(ws, L.counts_kept);
+    v->map.offsets = at<int32_t>(ws, L.offsets);
+    v->map.rank_offsets = at<int32_t>(ws, L.rank_offsets);
+    v->map.pos = at<int32_t>(ws, L.pos);
+    v->map.row_src = at<int32_t>(ws, L.row_src);
+    v->map.drop_list = at<int32_t>(ws, L.drop_list);
+    v->map.n_dropped = at<int32_t>(ws, L.n_dropped);
+    v->xperm = at<void>(ws, L.xperm);
+    v->h = c->expert_kind == MOE_EXPERT_IDENTITY ? nullptr : at<void>(ws, L.h);
+    v->out = at<void>(ws, L.out);
+}
+
+int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
+              cudaStream_t s) {
+    const cudaError_t e = launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, idx, gate, s);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
+}
+
+int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const moe_dispatch_map* m, void* xperm,
+                 void* ws, cudaStream_t s) {
+    const Layout L = layout(c);
+    DispatchArgs a{};
+    a.T = c->T; a.d = c->d; a.E = c->E; a.k = c->k; a.D = c->D;
+    a.capacity = c->capacity;
+    a.act_bytes = act_bytes(c);
+    a.x = x;
+    a.topk_idx = idx;
+    a.counts_routed = m->counts_routed;
+    a.counts_kept = m->counts_kept;
+    a.offsets = m->offsets;
+    a.rank_offsets = m->rank_offsets;
+    a.pos = m->pos;
+    a.row_src = m->row_src;
+    a.drop_list = m->drop_list;
+    a.n_dropped = m->n_dropped;
+    a.xperm = xperm;
+    a.status = at<int32_t>(ws, L.status);
+    a.hist = at<int32_t>(ws, L.hist);
+    a.drop_offsets = at<int32_t>(ws, L.drop_offsets);
+    const cudaError_t e = launch_dispatch(a, s);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch");
+}
+
+int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const void* W13, const void* W2, void* h,
+            void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
+    FfnArgs a{};
+    a.T = c->T; a.d = c->d; a.E = c->E; a.k = c->k; a.F = c->F;
+    a.expert_kind = c->expert_kind;
+    a.act_dtype = c->act_dtype;
+    a.xperm = xperm;
+    a.offsets = offsets;
+    a.W13 = W13;
+    a.W2 = W2;
+    a.h = h;
+    a.out = out;
+    a.status = status;
+    const cudaError_t e = c->act_dtype == MOE_BF16 ? launch_ffn_tc(a, s, mid) : launch_ffn_simt(a, s, mid);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_expert_ffn");
+}
+
+int record(void* const* events, int n, int i, cudaStream_t s) {
+    if (!events || i >= n || !events[i]) return MOE_OK;
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "cudaEventRecord");
+}
+
+int forward(const moe_config* c, const void* x, const float* Wg, const float* bias, const void* W13, const void* W2,
+            void* y, void* ws, size_t ws_bytes, cudaStream_t s, void* const* events, int n_events) {
+    int rc = validate(c);
+    if (rc != MOE_OK) return rc;
+    if (!x || !Wg || !y || !ws) return MOE_ERR_ARG;
+    if (c->expert_kind != MOE_EXPERT_IDENTITY && (!W13 || !W2)) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned4(Wg) || (bias && !aligned4(bias)) || !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (W13 && (!aligned16(W13) || !aligned16(W2))) return MOE_ERR_ALIGN;
+    const Layout L = layout(c);
+    if (ws_bytes < L.forward_end) return MOE_ERR_WORKSPACE;
+    moe_workspace_view v{};
+    fill_view(c, ws, &v);
+    cudaError_t e = cudaMemsetAsync(v.status, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    if ((rc = record(events, n_events, 0, s)) != MOE_OK) return rc;
+    if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, s)) != MOE_OK) return rc;
+    if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
+    if ((rc = run_dispatch(c, x, v.topk_idx, &v.map, v.xperm, ws, s)) != MOE_OK) return rc;
+    if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
+    if (c->expert_kind != MOE_EXPERT_IDENTITY) {
+        cudaEvent_t mid = (events && n_events > 3) ? static_cast<cudaEvent_t>(events[3]) : nullptr;
+        if ((rc = run_ffn(c, v.xperm, v.map.offsets, W13, W2, v.h, v.out, v.status, s, mid)) != MOE_OK) return rc;
+    } else if ((rc = record(events, n_events, 3, s)) != MOE_OK) {
+        return rc;
+    }
+    if ((rc = record(events, n_events, 4, s)) != MOE_OK) return rc;
+    e = launch_combine(c->act_dtype, v.out, v.topk_gate, v.map.pos, y, c->T, c->d, c->k, v.status, s);
+    if (e != cudaSuccess) return fail_cuda(e, "moe_combine");
+    return record(events, n_events, 5, s);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int64_t moe_capacity(int32_t T, int32_t k, int32_t E, int64_t cf_num, int64_t cf_den, int64_t min_capacity) {
+    if (T <= 0 || k <= 0 || E <= 0 || cf_den <= 0 || cf_num < 0) return -1;
+    // ceil(cf_num * T * k / (cf_den * E)) without overflow for realistic sizes (128-bit product).
+    const __int128 num = static_cast<__int128>(cf_num) * T * k;
+    const __int128 den = static_cast<__int128>(cf_den) * E;
+    __int128 c = (num + den - 1) / den;
+    if (c < min_capacity) c = min_capacity;
+    if (c > INT64_MAX) c = INT64_MAX;
+    return static_cast<int64_t>(c);
+}
+
+int moe_validate_config(const moe_config* cfg) { return validate(cfg); }
+
+size_t moe_dispatch_workspace_bytes(const moe_config* cfg) {
+    return validate(cfg) == MOE_OK ? layout(cfg).dispatch_end : 0;
+}
+
+size_t moe_ffn_workspace_bytes(const moe_config* cfg) { return validate(cfg) == MOE_OK ? kAlign : 0; }
+
+size_t moe_workspace_bytes(const moe_config* cfg) { return validate(cfg) == MOE_OK ? layout(cfg).forward_end : 0; }
+
+size_t moe_workspace_bytes_host(const moe_config* cfg) {
+    return validate(cfg) == MOE_OK ? layout(cfg).host_end : 0;
+}
+
+int moe_workspace_get_view(const moe_config* cfg, void* ws, size_t ws_bytes, moe_workspace_view* view) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!ws || !view) return MOE_ERR_ARG;
+    if (ws_bytes < layout(cfg).forward_end) return MOE_ERR_WORKSPACE;
+    fill_view(cfg, ws, view);
+    return MOE_OK;
+}
+
+int moe_kernels_per_forward(const moe_config* cfg) {
+    if (validate(cfg) != MOE_OK) return 0;
+    // route + (count, scan, scatter, gather) + (up, down) + combine
+    return 1 + 4 + (cfg->expert_kind == MOE_EXPERT_IDENTITY ? 0 : 2) + 1;
+}
+
+int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias, int32_t* topk_idx,
+              float* topk_gate, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!x || !Wg || !topk_idx || !topk_gate) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned4(Wg) || (bias && !aligned4(bias)) || !aligned4(topk_idx) || !aligned4(topk_gate))
+        return MOE_ERR_ALIGN;
+    return run_route(cfg, x, Wg, bias, topk_idx, topk_gate, stream);
+}
+
+int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const moe_dispatch_map* map,
+                 void* xperm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!x || !topk_idx || !map || !xperm || !ws) return MOE_ERR_ARG;
+    if (!map->counts_routed || !map->counts_kept || !map->offsets || !map->rank_offsets || !map->pos ||
+        !map->row_src || !map->drop_list || !map->n_dropped)
+        return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(xperm) || !aligned16(ws)) return MOE_ERR_ALIGN;
+    if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_dispatch(cfg, x, topk_idx, map, xperm, ws, stream);
+}
+
+int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets, const void* W13, const void* W2,
+                   void* h, void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (cfg->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_ARG;
+    if (!xperm || !offsets || !W13 || !W2 || !h || !out || !ws) return MOE_ERR_ARG;
+    if (!aligned16(xperm) || !aligned16(W13) || !aligned16(W2) || !aligned16(h) || !aligned16(out) ||
+        !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+    int32_t* status = static_cast<int32_t*>(ws);
+    const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_ffn(cfg, xperm, offsets, W13, W2, h, out, status, stream, nullptr);
+}
+
+int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, const int32_t* pos, void* y,
+                int32_t* status, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!out || !topk_gate || !pos || !y) return MOE_ERR_ARG;
+    if (!aligned16(out) || !aligned16(y) || !aligned4(topk_gate) || !aligned4(pos)) return MOE_ERR_ALIGN;
+    const cudaError_t e =
+        launch_combine(cfg->act_dtype, out, topk_gate, pos, y, cfg->T, cfg->d, cfg->k, status, stream);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_combine");
+}
+
+int moe_layer_forward(const moe_config* cfg, const void* x, const float* Wg, const float* bias, const void* W13,
+                      const void* W2, void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return forward(cfg, x, Wg, bias, W13, W2, y, ws, ws_bytes, stream, nullptr, 0);
+}
+
+int moe_layer_forward_traced(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
+                             const void* W13, const void* W2, void* y, void* ws, size_t ws_bytes,
+                             moe_stream_t stream, void* const* events, int32_t n_events) {
+    if (!events || n_events < 6) return MOE_ERR_ARG;
+    return forward(cfg, x, Wg, bias, W13, W2, y, ws, ws_bytes, stream, events, n_events);
+}
+
+int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const float* Wg, const float* bias,
+                           const void* W13, const void* W2, void* y_host, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+    int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!x_host || !y_host || !ws) return MOE_ERR_ARG;
+    const Layout L = layout(cfg);
+    if (ws_bytes < L.host_end) return MOE_ERR_WORKSPACE;
+    const size_t bytes = size_t(act_bytes(cfg)) * cfg->T * cfg->d;
+    void* xs = at<void>(ws, L.x_stage);
+    void* ys = at<void>(ws, L.y_stage);
+    cudaError_t e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(x)");
+    if ((rc = forward(cfg, xs, Wg, bias, W13, W2, ys, ws, ws_bytes, stream, nullptr, 0)) != MOE_OK) return rc;
+    e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(y)");
+    e = cudaStreamSynchronize(stream);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "cudaStreamSynchronize");
+}
+
+int moe_read_status(const int32_t* status_dev, int32_t* flags_host, moe_stream_t stream) {
+    if (!status_dev) return MOE_ERR_ARG;
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, status_dev, sizeof(h), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(status)");
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    if (flags_host) *flags_host = h;
+    return h == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+const char* moe_status_string(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_ARG: return "invalid argument";
+        case MOE_ERR_ALIGN: return "pointer or activation row not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE: return "device reported an error";
+        default: return "unknown status";
+    }
+}
+
+const char* moe_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+int moe_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,57 +1,2 @@
-"""Test-side glue: feeds workload inputs (torch tensors) to the float64 CPU oracle.
-
-Converts tensors to exact float64 numpy arrays and turns the packed expert weights
-(W13 [E, R, d], W2 [E, d, F]) into the math-layout matrices the oracle's expert
-functions take (W_gate = W13[e, :F].T and so on). No arithmetic of the layer lives
-here.
-"""
-from __future__ import annotations
-
-import numpy as np
-import torch
-
-from oracle import moe_oracle as orc
-
-
-def f64(t) -> np.ndarray:
-    if t is None:
-        return None
-    if isinstance(t, np.ndarray):
-        return t.astype(np.float64)
-    return t.detach().to("cpu", torch.float64).numpy()
-
-
-def expert_fn(kind: str, W13, W2, F: int, faithful: bool = False, cache=None):
-    """Expert_e(X) for the oracle, reading expert e's packed weights on demand."""
-    if kind == "identity":
-        return lambda e, X: X
-
-    def weights(e):
-        if cache is not None and e in cache:
-            return cache[e]
-        w13 = f64(W13[e])
-        w2 = f64(W2[e])
-        if cache is not None:
-            cache[e] = (w13, w2)
-        return w13, w2
-
-    if kind == "relu":
-        def fn(e, X):
-            w13, w2 = weights(e)
-            return orc.expert_relu(X, w13.T, w2.T)
-    elif kind == "swiglu":
-        def fn(e, X):
-            w13, w2 = weights(e)
-            return orc.expert_swiglu(X, w13[:F].T, w13[F:].T, w2.T, faithful=faithful)
-    else:
-        raise ValueError(kind)
-    return fn
-
-
-def run_oracle(w, inp: dict, capacity="auto", faithful: bool = False) -> dict:
-    """Oracle forward of workload ``w`` on inputs ``inp`` (tensors on any device)."""
-    if capacity == "auto":
-        capacity = orc.expert_capacity(w.T, w.k, w.E, w.capacity_factor, w.min_capacity)
-    fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, faithful=faithful)
-    return orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), w.k, fn, capacity=capacity,
-                           bias=f64(inp.get("bias")), D=w.D)
+"""Test-side glue: the oracle's adapters for the library's packed tensors."""
+from oracle.packed import expert_fn, f64, run_oracle  # noqa: F401

@@ -1,0 +1,131 @@
+"""The C ABI on the host: the library loads, exports every declared symbol, sizes
+workspaces and rejects bad arguments with the documented codes before touching a GPU.
+
+Nothing here launches a kernel: every call below fails validation (or is pure host
+arithmetic), so the pointers passed are never dereferenced.
+"""
+import ctypes
+
+import pytest
+
+from routing_dispatch_combine_moe_b300 import abi, sizing
+from routing_dispatch_combine_moe_b300 import workloads as wl
+
+A16, MIS = 0x10000, 0x10001  # fake device addresses: 16-byte aligned / misaligned
+
+
+def test_library_exports_every_declared_symbol():
+    lib = abi.lib()
+    names = abi.exported_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+    assert abi.moe_version() >= 100
+
+
+def test_capacity_exact_integer_rounding():
+    assert abi.moe_capacity(8192, 2, 64, "1.25") == 320
+    assert abi.moe_capacity(10, 1, 3, "1") == 4
+    assert abi.moe_capacity(10, 1, 3, "0.9") == 3
+    assert abi.moe_capacity(16, 2, 8, "1", min_capacity=6) == 6
+    for T, k, E, f in [(4096, 8, 256, "1.1"), (1000, 3, 7, "1.33"), (5, 2, 64, "0.5")]:
+        assert abi.moe_capacity(T, k, E, f) == sizing.capacity(T, k, E, f)
+    assert abi.lib().moe_capacity(10, 1, 3, 1, 0, 0) == -1
+    assert abi.lib().moe_capacity(0, 1, 3, 1, 1, 0) == -1
+
+
+def cfg(**kw):
+    base = dict(T=64, d=128, E=8, k=2, F=64, D=1, act="bf16", expert="swiglu", capacity=None)
+    base.update(kw)
+    return abi.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), abi.MOE_OK),
+    (dict(k=9), abi.MOE_ERR_ARG),
+    (dict(k=0), abi.MOE_ERR_ARG),
+    (dict(T=0), abi.MOE_ERR_ARG),
+    (dict(E=8, D=3), abi.MOE_ERR_ARG),
+    (dict(F=0), abi.MOE_ERR_ARG),
+    (dict(F=0, expert="identity"), abi.MOE_OK),
+    (dict(E=300, k=2), abi.MOE_ERR_UNSUPPORTED),
+    (dict(E=64, k=17), abi.MOE_ERR_UNSUPPORTED),
+    (dict(d=100), abi.MOE_ERR_ALIGN),       # 200 bytes per bf16 row
+    (dict(d=100, act="f32"), abi.MOE_OK),   # 400 bytes per fp32 row
+    (dict(F=36), abi.MOE_ERR_ALIGN),
+    (dict(F=36, expert="identity"), abi.MOE_OK),
+])
+def test_validate_config(kw, code):
+    assert abi.moe_validate_config(cfg(**kw)) == code
+
+
+def test_workspace_sizes_and_layout():
+    for name in wl.WORKLOAD_ORDER:
+        w = wl.WORKLOADS[name]
+        c = abi.config_for(w)
+        fwd, host = abi.moe_workspace_bytes(c), abi.moe_workspace_bytes_host(c)
+        disp = abi.moe_dispatch_workspace_bytes(c)
+        A = w.T * w.k
+        assert 0 < disp < fwd < host
+        assert host - fwd >= 2 * w.T * w.d * w.act_bytes
+        assert fwd >= A * w.d * w.act_bytes * (1 if w.expert == "identity" else 2)
+        base = 1 << 40
+        v = abi.lib()
+        view = abi.moe_workspace_view()
+        assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd, ctypes.byref(view)) == abi.MOE_OK
+        ptrs = [view.status, view.topk_idx, view.topk_gate, view.map.counts_routed, view.map.counts_kept,
+                view.map.offsets, view.map.rank_offsets, view.map.n_dropped, view.map.pos, view.map.row_src,
+                view.map.drop_list, view.xperm]
+        assert all(p % 256 == 0 and base <= p < base + fwd for p in ptrs)
+        assert view.status == base
+        if w.expert == "identity":
+            assert view.out == view.xperm and not view.h
+        else:
+            assert view.xperm < view.h < view.out < base + fwd
+            assert view.out + A * w.d * w.act_bytes <= base + fwd
+        assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
+        assert abi.moe_kernels_per_forward(c) == (6 if w.expert == "identity" else 8)
+
+
+def test_entry_points_reject_bad_arguments_on_the_host():
+    lib = abi.lib()
+    c = cfg()
+    bad = cfg(k=9)
+    ref = ctypes.byref
+    # route
+    assert lib.moe_route(ref(bad), A16, A16, None, A16, A16, None) == abi.MOE_ERR_ARG
+    assert lib.moe_route(ref(c), None, A16, None, A16, A16, None) == abi.MOE_ERR_ARG
+    assert lib.moe_route(ref(c), MIS, A16, None, A16, A16, None) == abi.MOE_ERR_ALIGN
+    # dispatch
+    m = abi.moe_dispatch_map(*([A16] * 8))
+    nbytes = abi.moe_dispatch_workspace_bytes(c)
+    assert lib.moe_dispatch(ref(c), A16, A16, ref(m), A16, A16, nbytes - 1, None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_dispatch(ref(c), A16, A16, ref(m), MIS, A16, nbytes, None) == abi.MOE_ERR_ALIGN
+    m0 = abi.moe_dispatch_map(*([A16] * 7 + [None]))
+    assert lib.moe_dispatch(ref(c), A16, A16, ref(m0), A16, A16, nbytes, None) == abi.MOE_ERR_ARG
+    # expert ffn
+    assert lib.moe_expert_ffn(ref(cfg(expert="identity", F=0)), A16, A16, A16, A16, A16, A16, A16, 256,
+                              None) == abi.MOE_ERR_ARG
+    assert lib.moe_expert_ffn(ref(c), A16, A16, A16, A16, MIS, A16, A16, 256, None) == abi.MOE_ERR_ALIGN
+    assert lib.moe_expert_ffn(ref(c), A16, A16, A16, A16, A16, A16, A16, 255, None) == abi.MOE_ERR_WORKSPACE
+    # combine
+    assert lib.moe_combine(ref(c), A16, A16, None, A16, None, None) == abi.MOE_ERR_ARG
+    assert lib.moe_combine(ref(c), A16, A16, A16, MIS, None, None) == abi.MOE_ERR_ALIGN
+    # layer
+    n = abi.moe_workspace_bytes(c)
+    assert lib.moe_layer_forward(ref(c), A16, A16, None, None, A16, A16, A16, n, None) == abi.MOE_ERR_ARG
+    assert lib.moe_layer_forward(ref(c), A16, A16, None, A16, A16, A16, A16, n - 1, None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_layer_forward(ref(c), MIS, A16, None, A16, A16, A16, A16, n, None) == abi.MOE_ERR_ALIGN
+    evs = (ctypes.c_void_p * 6)(*([A16] * 6))
+    assert lib.moe_layer_forward_traced(ref(c), A16, A16, None, A16, A16, A16, A16, n, None, evs,
+                                        5) == abi.MOE_ERR_ARG
+    nh = abi.moe_workspace_bytes_host(c)
+    assert lib.moe_layer_forward_host(ref(c), A16, A16, None, A16, A16, A16, A16, nh - 1,
+                                      None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_read_status(None, None, None) == abi.MOE_ERR_ARG
+
+
+def test_status_strings():
+    for code in range(7):
+        assert abi.status_string(code)
+    assert abi.status_string(99) == "unknown status"
