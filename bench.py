@@ -167,17 +167,19 @@ def load_traffic(workload: str, kernel: str):
 
 
 # ------------------------------------------------------------------ algorithmic work
-def algorithmic(w, rows: int) -> dict:
+def algorithmic(w, rows: int, out_bytes: int, h_cols: int) -> dict:
+    """Algorithmic work per launch: flops of the formulas, bytes each kernel must move at least."""
     b = w.act_bytes
     up, down = sizing.expert_gemm_flops(rows, w.d, w.F, w.expert)
+    ident = w.expert == "identity"
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
         route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.k * 8,
         dispatch_bytes=sizing.dispatch_hbm_bytes(w.T, w.d, rows, b),
-        combine_bytes=sizing.combine_hbm_bytes(w.T, w.d, rows, b),
+        combine_bytes=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
         up_flops=up, down_flops=down,
-        up_bytes=(w.E * w.w13_rows * w.d + rows * w.d + rows * w.F) * b if w.expert != "identity" else 0,
-        down_bytes=(w.E * w.d * w.F + rows * w.F + rows * w.d) * b if w.expert != "identity" else 0,
+        up_bytes=0 if ident else w.E * w.w13_rows * w.d * b + rows * w.d * b + rows * h_cols * b,
+        down_bytes=0 if ident else w.E * w.d * w.F * b + rows * h_cols * b + rows * w.d * out_bytes,
     )
 
 
@@ -304,7 +306,8 @@ def run_ours(args, w, world, rank, local):
 
     if rank != 0:
         return None
-    work = algorithmic(w, rows)
+    out_bytes = torch.tensor([], dtype=abi.out_dtype(cfg)).element_size()
+    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg))
     peaks, peak_src = load_peaks()
     value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
     dc_bytes = work["dispatch_bytes"] + work["combine_bytes"]
@@ -345,6 +348,7 @@ def run_ours(args, w, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.act, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "F": w.F, "expert": w.expert,
                    "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
+                   "precision": w.precision,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
                          "dispatched rows" % (w.E * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9

@@ -72,6 +72,13 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
 #define MOE_EXPERT_RELU 1     /* relu(x W1) W2 */
 #define MOE_EXPERT_SWIGLU 2   /* (silu(x W_gate) * (x W_up)) W_down, silu(z) = z / (1 + e^-z) */
 
+/* Precision of the bf16 expert path (ignored for fp32 activations and identity experts). */
+#define MOE_PRECISION_BF16 0    /* h and the expert outputs are each rounded once to bf16 (fewest bytes) */
+#define MOE_PRECISION_F32_OUT 1 /* h rounded once to bf16, expert outputs kept in fp32 */
+#define MOE_PRECISION_SPLIT_H 2 /* h carried as a bf16 pair (hi = bf16(h), lo = bf16(h - hi)); both halves go
+                                   through the down projection against the same weights; expert outputs in
+                                   fp32: y then carries essentially only its own final rounding */
+
 /* Limits of this build. */
 #define MOE_MAX_K 16        /* experts per token */
 #define MOE_MAX_E 256       /* routed experts */
@@ -85,6 +92,8 @@ typedef struct moe_config {
     int32_t D;           /* virtual expert-parallel ranks, E % D == 0 (1 = none) */
     int32_t act_dtype;   /* MOE_F32 or MOE_BF16: x, dispatched rows, h, expert outputs, y */
     int32_t expert_kind; /* MOE_EXPERT_* */
+    int32_t precision;   /* MOE_PRECISION_*; SPLIT_H needs F % 64 == 0 */
+    int32_t reserved;    /* must be 0 */
     int64_t capacity;    /* tokens each expert keeps; < 0 = dropless (see moe_capacity) */
 } moe_config;
 
@@ -107,8 +116,8 @@ typedef struct moe_workspace_view {
     float* topk_gate;    /* [T*k] */
     moe_dispatch_map map;
     void* xperm;         /* [T*k, d] act: dispatched rows (the dispatch "send buffer") */
-    void* h;             /* [T*k, F] act: expert hidden activations (NULL for identity) */
-    void* out;           /* [T*k, d] act: expert outputs (aliases xperm for identity) */
+    void* h;             /* expert hidden activations, see moe_expert_ffn (NULL for identity) */
+    void* out;           /* expert outputs, see moe_expert_ffn (aliases xperm for identity) */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -166,22 +175,27 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
 
 /* Grouped expert FFN over the dispatched rows: for each expert e, rows
  * [offsets[e], offsets[e+1]) of xperm go through Expert_e ("EP Math", "What expert
- * parallelism actually shards": each expert is a full FFN with its own weights).
+ * parallelism actually shards": every expert is a complete FFN with private weights).
  *   xperm   [T*k, d] act;  offsets [E+1] int32 (from moe_dispatch)
  *   W13     SwiGLU: [E, 2F, d] act, rows [0,F) = W_gate^T, rows [F,2F) = W_up^T;
  *           ReLU:   [E, F, d]  act (W1^T).   (The usual linear-layer layout.)
  *   W2      [E, d, F] act (W_down^T / W2^T)
- *   h       [T*k, F] act out: hidden activation of each row
- *   out     [T*k, d] act out: expert output of each row
- * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation, one
- * rounding to bf16 for h and for out); fp32 runs on the fp32 FMA units.
- * Requires F * sizeof(act) % 16 == 0 besides the row rule. ws >=
- * moe_ffn_workspace_bytes(cfg); its first 4 bytes are the status word (cleared). */
+ *   h       out: hidden activation of each row, [T*k, F] act; under MOE_PRECISION_SPLIT_H
+ *           [T*k, 2F] bf16: for every 64-column block b of h the 64 "hi" values at
+ *           columns [128b, 128b+64) and the 64 "lo" values at [128b+64, 128b+128).
+ *   out     out: expert output of each row, [T*k, d]; fp32 under MOE_PRECISION_F32_OUT
+ *           and MOE_PRECISION_SPLIT_H with bf16 activations, else the act dtype.
+ * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation); fp32
+ * runs on the fp32 FMA units. Requires F * sizeof(act) % 16 == 0 besides the row
+ * rule. ws >= moe_ffn_workspace_bytes(cfg); its first 4 bytes are the status word
+ * (cleared). */
 int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets,
                    const void* W13, const void* W2, void* h, void* out,
                    void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Combine: y[t] = sum over slots j with pos[t*k+j] >= 0 of topk_gate[t*k+j] * out[pos[t*k+j]],
+ * with `out` in the dtype moe_expert_ffn writes (see there; the activation dtype for
+ * identity experts),
  * summed in fp32 in slot order and rounded once ("Mixture-of-Experts (MoE)
  * Architecture and Expert Parallelism", section 2; "EP Math", "The combine
  * all-to-all"; "Token drop": a dropped slot adds nothing and the gates are not

@@ -14,13 +14,14 @@ Sources (page title, then section):
           G(x) = Softmax(KeepTopK(H(x), K)), y = sum_{i in TopK} G_i(x) Expert_i(x);
           KeepTopK keeps the K largest coordinates and sets the rest to -inf.
 * [EPSH]  "EP Math - Expert Parallelism (MoE)", "What expert parallelism actually
-          shards" and "Placing experts across devices": E experts, each a full FFN,
+          shards" and "Placing experts across devices": E experts, each a complete FFN,
           E/D whole experts per device, E divisible by D.
 * [CAP]   same page, "Capacity factor: fixing buffer sizes": C = f * N * k / E,
           rounded up.
 * [DROP]  same page, "Token drop: what overflow costs": an assignment past the
-          capacity is not processed; it behaves as if the expert output were zero
-          (the token still passes through the residual, which the caller adds).
+          capacity is skipped by its expert and adds nothing to y, the same as a
+          zero expert output (the token still passes through the residual, which
+          the caller adds).
 * [A2A]   same page, "The dispatch all-to-all" / "The combine all-to-all": each
           assignment is a d-vector sent to its expert; the combine weights the k
           returned vectors by the gates and sums them.

@@ -23,6 +23,8 @@ MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = 4, 5, 6
 MOE_DEV_ERR_INDEX, MOE_DEV_ERR_TIMEOUT = 0x1, 0x2
 MOE_F32, MOE_BF16 = 0, 1
 MOE_EXPERT_IDENTITY, MOE_EXPERT_RELU, MOE_EXPERT_SWIGLU = 0, 1, 2
+MOE_PRECISION_BF16, MOE_PRECISION_F32_OUT, MOE_PRECISION_SPLIT_H = 0, 1, 2
+PRECISIONS = {"bf16": MOE_PRECISION_BF16, "f32_out": MOE_PRECISION_F32_OUT, "split_h": MOE_PRECISION_SPLIT_H}
 MOE_MAX_K, MOE_MAX_E = 16, 256
 EXPERT_KINDS = {"identity": MOE_EXPERT_IDENTITY, "relu": MOE_EXPERT_RELU, "swiglu": MOE_EXPERT_SWIGLU}
 ACT_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
@@ -42,7 +44,8 @@ class MoeError(RuntimeError):
 
 class moe_config(ctypes.Structure):
     _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("F", _i32), ("D", _i32),
-                ("act_dtype", _i32), ("expert_kind", _i32), ("capacity", _i64)]
+                ("act_dtype", _i32), ("expert_kind", _i32), ("precision", _i32), ("reserved", _i32),
+                ("capacity", _i64)]
 
 
 class moe_dispatch_map(ctypes.Structure):
@@ -122,10 +125,27 @@ def _stream(stream=None):
 
 
 # ------------------------------------------------------------------ config
-def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None) -> moe_config:
+def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None, precision="f32_out") -> moe_config:
     """A moe_config; ``capacity`` None (dropless) or a non-negative integer."""
     return moe_config(T=T, d=d, E=E, k=k, F=F, D=D, act_dtype=ACT_DTYPES[act],
-                      expert_kind=EXPERT_KINDS[expert], capacity=-1 if capacity is None else int(capacity))
+                      expert_kind=EXPERT_KINDS[expert], precision=PRECISIONS[precision], reserved=0,
+                      capacity=-1 if capacity is None else int(capacity))
+
+
+def out_dtype(cfg) -> torch.dtype:
+    """dtype of the expert-output rows moe_expert_ffn writes for this config."""
+    if cfg.act_dtype == MOE_F32:
+        return torch.float32
+    if cfg.expert_kind != MOE_EXPERT_IDENTITY and cfg.precision != MOE_PRECISION_BF16:
+        return torch.float32
+    return torch.bfloat16
+
+
+def hidden_cols(cfg) -> int:
+    """Columns of the h buffer moe_expert_ffn writes (2F in the split-h bf16 mode)."""
+    if cfg.act_dtype == MOE_BF16 and cfg.precision == MOE_PRECISION_SPLIT_H:
+        return 2 * cfg.F
+    return cfg.F
 
 
 def moe_capacity(T, k, E, capacity_factor, min_capacity=0) -> int:
@@ -141,7 +161,7 @@ def config_for(w, capacity="auto") -> moe_config:
     if capacity == "auto":
         capacity = None if w.capacity_factor is None else moe_capacity(w.T, w.k, w.E, w.capacity_factor,
                                                                        w.min_capacity)
-    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity)
+    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision)
 
 
 def moe_validate_config(cfg) -> int:

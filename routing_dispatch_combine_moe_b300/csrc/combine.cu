@@ -8,7 +8,8 @@
 // The reverse all-to-all and the weighted reduction are one gather: one warp per
 // token reads its k expert-output rows (16-byte vector loads, all k issued before
 // the arithmetic), accumulates in fp32 in slot order and rounds once on the store.
-// No atomics, so the result is deterministic.
+// No atomics, so the result is deterministic. Expert outputs are read in their own
+// dtype (bf16 or fp32); a lane handles 8 consecutive elements of the row.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,7 +20,6 @@ template <typename TAct>
 struct Vec16;
 template <>
 struct Vec16<float> {
-    static constexpr int N = 4;
     __device__ static void unpack(const uint4& v, float* f) {
         f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
         f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
@@ -30,7 +30,6 @@ struct Vec16<float> {
 };
 template <>
 struct Vec16<__nv_bfloat16> {
-    static constexpr int N = 8;
     __device__ static void unpack(const uint4& v, float* f) {
         f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
         f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
@@ -41,11 +40,42 @@ struct Vec16<__nv_bfloat16> {
     }
 };
 
-template <typename TAct>
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ out, const float* __restrict__ gate,
-                                                      const int32_t* __restrict__ pos, uint4* __restrict__ y, int T,
-                                                      int k, int vec_per_row, int64_t max_rows, int32_t* status) {
-    using V = Vec16<TAct>;
+// Loads 8 consecutive elements of a row as fp32.
+template <typename T>
+struct Load8;
+template <>
+struct Load8<float> {
+    __device__ static void load(const float* p, float* f) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+        f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+        f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+    }
+};
+template <>
+struct Load8<__nv_bfloat16> {
+    __device__ static void load(const __nv_bfloat16* p, float* f) {
+        Vec16<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4*>(p)), f);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float* f);
+template <>
+__device__ __forceinline__ void store8<float>(float* p, const float* f) {
+    reinterpret_cast<uint4*>(p)[0] = Vec16<float>::pack(f);
+    reinterpret_cast<uint4*>(p)[1] = Vec16<float>::pack(f + 4);
+}
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const float* f) {
+    *reinterpret_cast<uint4*>(p) = Vec16<__nv_bfloat16>::pack(f);
+}
+
+// d must be a multiple of 8 here (16-byte bf16 rows); fp32 rows of d % 8 == 4 use the 4-wide kernel.
+template <typename TOut, typename TY>
+__global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ out, const float* __restrict__ gate,
+                                                      const int32_t* __restrict__ pos, TY* __restrict__ y, int T,
+                                                      int k, int d, int64_t max_rows, int32_t* status) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -66,42 +96,91 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         src[j] = __shfl_sync(0xFFFFFFFFu, p, j);
         gj[j] = __shfl_sync(0xFFFFFFFFu, g, j);
     }
-    for (int v = lane; v < vec_per_row; v += 32) {
-        uint4 raw[MOE_MAX_K];
+    for (int c = lane * 8; c < d; c += 32 * 8) {
+        float acc[8];
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j)
-            if (j < k && src[j] >= 0) raw[j] = __ldg(out + size_t(src[j]) * vec_per_row + v);
-        float acc[V::N];
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
 #pragma unroll
-        for (int q = 0; q < V::N; ++q) acc[q] = 0.f;
+        for (int j0 = 0; j0 < MOE_MAX_K; j0 += 4) {
+            if (j0 >= k) break;
+            float f[4][8];
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j) {
-            if (j < k && src[j] >= 0) {
-                float f[V::N];
-                V::unpack(raw[j], f);
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = j0 + jj;
+                if (j < k && src[j] >= 0) Load8<TOut>::load(out + size_t(src[j]) * d + c, f[jj]);
+            }
 #pragma unroll
-                for (int q = 0; q < V::N; ++q) acc[q] = fmaf(gj[j], f[q], acc[q]);
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = j0 + jj;
+                if (j < k && src[j] >= 0) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] = fmaf(gj[j], f[jj][q], acc[q]);
+                }
             }
         }
-        y[size_t(t) * vec_per_row + v] = V::pack(acc);
+        store8<TY>(y + size_t(t) * d + c, acc);
+    }
+}
+
+// fp32 rows whose length is a multiple of 4 but not of 8.
+__global__ void __launch_bounds__(256) combine_kernel_f32x4(const float* __restrict__ out, const float* __restrict__ gate,
+                                                            const int32_t* __restrict__ pos, float* __restrict__ y,
+                                                            int T, int k, int d, int64_t max_rows, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int p = -1;
+    float g = 0.f;
+    if (lane < k) {
+        p = pos[size_t(t) * k + lane];
+        g = gate[size_t(t) * k + lane];
+        if (p >= max_rows) {
+            set_status(status, MOE_DEV_ERR_INDEX);
+            p = -1;
+        }
+    }
+    int src[MOE_MAX_K];
+    float gj[MOE_MAX_K];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) {
+        src[j] = __shfl_sync(0xFFFFFFFFu, p, j);
+        gj[j] = __shfl_sync(0xFFFFFFFFu, g, j);
+    }
+    for (int c = lane * 4; c < d; c += 32 * 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) {
+            if (j >= k || src[j] < 0) continue;
+            float f[4];
+            Vec16<float>::unpack(__ldg(reinterpret_cast<const uint4*>(out + size_t(src[j]) * d + c)), f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = fmaf(gj[j], f[q], acc[q]);
+        }
+        *reinterpret_cast<uint4*>(y + size_t(t) * d + c) = Vec16<float>::pack(acc);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_combine(int act_dtype, const void* out, const float* gate, const int32_t* pos, void* y, int T,
-                           int d, int k, int32_t* status, cudaStream_t stream) {
-    const int act_bytes = act_dtype == MOE_F32 ? 4 : 2;
-    const int vec_per_row = int(int64_t(d) * act_bytes / 16);
+cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
+                           void* y, int T, int d, int k, int32_t* status, cudaStream_t stream) {
     const int64_t max_rows = int64_t(T) * k;
     const int grid = (T + 7) / 8;
-    if (act_dtype == MOE_F32)
-        combine_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(out), gate, pos,
-                                                        static_cast<uint4*>(y), T, k, vec_per_row, max_rows, status);
-    else
-        combine_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(out), gate, pos,
-                                                                static_cast<uint4*>(y), T, k, vec_per_row,
-                                                                max_rows, status);
+    if (act_dtype == MOE_F32) {
+        if (d % 8 == 0)
+            combine_kernel<float, float><<<grid, 256, 0, stream>>>(static_cast<const float*>(out), gate, pos,
+                                                                   static_cast<float*>(y), T, k, d, max_rows, status);
+        else
+            combine_kernel_f32x4<<<grid, 256, 0, stream>>>(static_cast<const float*>(out), gate, pos,
+                                                           static_cast<float*>(y), T, k, d, max_rows, status);
+    } else if (out_dtype == MOE_F32) {
+        combine_kernel<float, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<const float*>(out), gate, pos, static_cast<__nv_bfloat16*>(y), T, k, d, max_rows, status);
+    } else {
+        combine_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(out), gate, pos, static_cast<__nv_bfloat16*>(y), T, k, d, max_rows,
+            status);
+    }
     return cudaGetLastError();
 }
 

@@ -21,8 +21,8 @@
 //   4. gather  - one warp per token copies x[t] once from HBM into each of its kept
 //                rows with 16-byte vector loads and stores.
 // Because rows are ordered (expert, token), virtual rank r's rows (experts
-// [r E/D, (r+1) E/D)) form one contiguous chunk: the "one chunk per destination"
-// layout of an all-to-all input buffer.
+// [r E/D, (r+1) E/D)) form one contiguous chunk: the layout of an all-to-all input buffer, which
+// holds a separate chunk for every destination rank.
 #include "common.cuh"
 #include "kernels.h"
 

@@ -1,7 +1,7 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05) for bf16
 // experts: the only dense contraction of the layer ("EP Math - Expert Parallelism
-// (MoE)", "What expert parallelism actually shards": each expert is a full FFN with
-// its own weights; the gated three-matrix form is the one in "MoE Expert
+// (MoE)", "What expert parallelism actually shards": every expert is a complete FFN
+// with private weights; the gated three-matrix form is the one in "MoE Expert
 // Parallelism Sizing", "Memory residency for the same shape").
 //
 //   up   : h[r, :]   = act(xperm[r, :] . W13[e]^T)   SwiGLU: silu(g) * u, fused in the epilogue
@@ -27,6 +27,13 @@
 // matching up rows, so each thread's accumulator row has g and u side by side.
 // Every mbarrier wait is bounded; on a timeout the kernel flags MOE_DEV_ERR_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
+//
+// Output kinds (OUT): the up epilogue stores h in bf16 (kOutBF16) or split into
+// hi = bf16(h) and lo = bf16(h - hi) as interleaved 64-column blocks [hi | lo] of a
+// [rows, 2F] matrix (kOutHiLo). In the latter case the down projection runs over 2F
+// columns of A while the producer loads each 64-wide weight K-block twice (once for
+// hi, once for lo), so out = hi.W2 + lo.W2 with exact bf16 products and fp32
+// accumulation. The down epilogue stores bf16 (kOutBF16) or fp32 (kOutF32).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -44,14 +51,16 @@ constexpr int kThreads = 192;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
 
 enum Mode : int { kSwiGLU = 0, kPlain = 1, kReLU = 2 };
+enum Out : int { kOutBF16 = 0, kOutHiLo = 1, kOutF32 = 2 };
 
 struct Params {
     const int32_t* offsets;  // [E+1]
-    __nv_bfloat16* C;        // output, row stride ldc
+    void* C;                 // output, row stride ldc (bf16, or fp32 for a kOutF32 down projection)
     int ldc;                 // elements
     int n_out;               // valid output columns
     int E;
-    int K;                   // reduction length
+    int K;                   // reduction length of A
+    int b_k_shift;           // B's K block = A's K block >> b_k_shift (1 when A holds hi|lo pairs)
     int R;                   // rows per expert in B
     int F;                   // SwiGLU: up rows start at e*R + F
     int n_tiles;             // output column tiles
@@ -95,7 +104,40 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int MODE>
+// Stores 32 consecutive bf16 values (packed in pk[16]) at dst, the first n_valid of them.
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const uint32_t (&pk)[16], int n_valid) {
+    if (n_valid >= 32) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < n_valid) dst[j] = (j & 1) ? uint16_t(pk[j >> 1] >> 16) : uint16_t(pk[j >> 1] & 0xFFFFu);
+    }
+}
+
+// Stores 32 activations: one bf16 rounding (kOutBF16), or the hi/lo pair into the
+// interleaved [hi | lo] 64-column blocks of a [rows, 2F] matrix (kOutHiLo).
+template <int OUT>
+__device__ __forceinline__ void store_hidden(uint16_t* row_ptr, int col0, int n_out, const float (&h)[32]) {
+    uint32_t hi[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) hi[j] = pack_bf16x2(h[2 * j], h[2 * j + 1]);
+    if constexpr (OUT != kOutHiLo) {
+        store_bf16x32(row_ptr + col0, hi, n_out - col0);
+    } else {
+        uint32_t lo[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            lo[j] = pack_bf16x2(h[2 * j] - bf16_lo(hi[j]), h[2 * j + 1] - bf16_hi(hi[j]));
+        const int blk = col0 >> 6, within = col0 & 63;
+        store_bf16x32(row_ptr + 128 * blk + within, hi, n_out - col0);
+        store_bf16x32(row_ptr + 128 * blk + 64 + within, lo, n_out - col0);
+    }
+}
+
+template <int MODE, int OUT>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                                                                    const __grid_constant__ CUtensorMap mapB,
                                                                    const Params p) {
@@ -175,13 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     if (!mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
                     const int k0 = kb * BK;
+                    const int kB = (kb >> p.b_k_shift) * BK;
                     tma_load_2d_hint(sA + s * A_STAGE, &mapA, &S.full[s], k0, m0, pol_a);
                     if (MODE == kSwiGLU) {
                         const int r0 = e * p.R + nt * (MMA_N / 2);
-                        tma_load_2d(sB + s * B_STAGE, &mapB, &S.full[s], k0, r0);
-                        tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &mapB, &S.full[s], k0, r0 + p.F);
+                        tma_load_2d(sB + s * B_STAGE, &mapB, &S.full[s], kB, r0);
+                        tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &mapB, &S.full[s], kB, r0 + p.F);
                     } else {
-                        tma_load_2d(sB + s * B_STAGE, &mapB, &S.full[s], k0, e * p.R + nt * MMA_N);
+                        tma_load_2d(sB + s * B_STAGE, &mapB, &S.full[s], kB, e * p.R + nt * MMA_N);
                     }
                     armed_mask |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -239,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int row = S.off[e] + mt * BM + r_in_tile;
             const bool row_ok = row < S.off[e + 1];
             const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + acc * MMA_N;
-            __nv_bfloat16* crow = p.C + size_t(row) * p.ldc;
             if (MODE == kSwiGLU) {
+                uint16_t* crow = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t g[32], u[32];
@@ -248,25 +291,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     tmem_ld_32x32b_x32(tbase + MMA_N / 2 + c * 32, u);
                     tmem_ld_wait();
                     const int col0 = nt * (MMA_N / 2) + c * 32;
-                    if (row_ok) {
-                        uint32_t pk[16];
+                    if (row_ok && col0 < p.n_out) {
+                        float h[32];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-                            const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-                            pk[j] = pack_bf16x2(h0, h1);
-                        }
-                        if (col0 + 32 <= p.n_out) {
-                            uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+                        for (int j = 0; j < 32; ++j) h[j] = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                        store_hidden<OUT>(crow, col0, p.n_out, h);
+                    }
+                }
+            } else if (MODE == kReLU) {
+                uint16_t* crow = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
+#pragma unroll 1
+                for (int c = 0; c < MMA_N / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col0 = nt * MMA_N + c * 32;
+                    if (row_ok && col0 < p.n_out) {
+                        float h[32];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                        } else {
-                            for (int j = 0; j < 32 && col0 + j < p.n_out; ++j) {
-                                const uint16_t b = (j & 1) ? uint16_t(pk[j >> 1] >> 16) : uint16_t(pk[j >> 1] & 0xFFFFu);
-                                reinterpret_cast<uint16_t*>(crow)[col0 + j] = b;
-                            }
-                        }
+                        for (int j = 0; j < 32; ++j) h[j] = fmaxf(__uint_as_float(v[j]), 0.f);
+                        store_hidden<OUT>(crow, col0, p.n_out, h);
                     }
                 }
             } else {
@@ -277,23 +321,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     tmem_ld_wait();
                     const int col0 = nt * MMA_N + c * 32;
                     if (row_ok && col0 < p.n_out) {
-                        uint32_t pk[16];
+                        if constexpr (OUT == kOutF32) {
+                            float* crow = static_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
+                            if (col0 + 32 <= p.n_out) {
+                                uint4* d4 = reinterpret_cast<uint4*>(crow);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            float a0 = __uint_as_float(v[2 * j]), a1 = __uint_as_float(v[2 * j + 1]);
-                            if (MODE == kReLU) { a0 = fmaxf(a0, 0.f); a1 = fmaxf(a1, 0.f); }
-                            pk[j] = pack_bf16x2(a0, a1);
-                        }
-                        if (col0 + 32 <= p.n_out) {
-                            uint4* dst = reinterpret_cast<uint4*>(crow + col0);
+                                for (int j = 0; j < 8; ++j)
+                                    d4[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                        } else {
-                            for (int j = 0; j < 32 && col0 + j < p.n_out; ++j) {
-                                const uint16_t b = (j & 1) ? uint16_t(pk[j >> 1] >> 16) : uint16_t(pk[j >> 1] & 0xFFFFu);
-                                reinterpret_cast<uint16_t*>(crow)[col0 + j] = b;
+                                for (int j = 0; j < 32; ++j)
+                                    if (col0 + j < p.n_out) crow[j] = __uint_as_float(v[j]);
                             }
+                        } else {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                            store_bf16x32(static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc + col0, pk,
+                                          p.n_out - col0);
                         }
                     }
                 }
@@ -346,10 +392,10 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int MODE>
+template <int MODE, int OUT>
 cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Params& p, int grid,
                         cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<MODE>;
+    auto kern = grouped_gemm_kernel<MODE, OUT>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -370,6 +416,8 @@ int grid_for(int64_t rows_max, int E, int n_tiles) {
 
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event) {
     const int64_t rows_max = int64_t(a.T) * a.k;
+    const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
+    const bool f32_out = a.precision != MOE_PRECISION_BF16;
     CUtensorMap mA, mB;
     cudaError_t err;
     Params p{};
@@ -378,32 +426,42 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.status = a.status;
     p.F = a.F;
 
-    // Up projection: A = xperm [rows, d]; B = W13 [E*R, d].
+    // Up projection: A = xperm [rows, d]; B = W13 [E*R, d]; C = h.
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;
     const int R = swiglu ? 2 * a.F : a.F;
     if ((err = make_map(&mA, a.xperm, a.d, rows_max, BM)) != cudaSuccess) return err;
     if ((err = make_map(&mB, a.W13, a.d, uint64_t(a.E) * R, swiglu ? MMA_N / 2 : MMA_N)) != cudaSuccess) return err;
-    p.C = static_cast<__nv_bfloat16*>(a.h);
-    p.ldc = a.F;
+    p.C = a.h;
+    p.ldc = split_h ? 2 * a.F : a.F;
     p.n_out = a.F;
     p.K = a.d;
+    p.b_k_shift = 0;
     p.R = R;
     p.n_tiles = swiglu ? (a.F + MMA_N / 2 - 1) / (MMA_N / 2) : (a.F + MMA_N - 1) / MMA_N;
-    err = swiglu ? launch_mode<kSwiGLU>(mA, mB, p, grid_for(rows_max, a.E, p.n_tiles), stream)
-                 : launch_mode<kReLU>(mA, mB, p, grid_for(rows_max, a.E, p.n_tiles), stream);
+    const int g_up = grid_for(rows_max, a.E, p.n_tiles);
+    if (swiglu)
+        err = split_h ? launch_mode<kSwiGLU, kOutHiLo>(mA, mB, p, g_up, stream)
+                      : launch_mode<kSwiGLU, kOutBF16>(mA, mB, p, g_up, stream);
+    else
+        err = split_h ? launch_mode<kReLU, kOutHiLo>(mA, mB, p, g_up, stream)
+                      : launch_mode<kReLU, kOutBF16>(mA, mB, p, g_up, stream);
     if (err != cudaSuccess) return err;
     if (mid_event && (err = cudaEventRecord(mid_event, stream)) != cudaSuccess) return err;
 
-    // Down projection: A = h [rows, F]; B = W2 [E*d, F].
-    if ((err = make_map(&mA, a.h, a.F, rows_max, BM)) != cudaSuccess) return err;
+    // Down projection: A = h [rows, F] (split: [rows, 2F] hi|lo blocks); B = W2 [E*d, F].
+    const int kA = split_h ? 2 * a.F : a.F;
+    if ((err = make_map(&mA, a.h, kA, rows_max, BM)) != cudaSuccess) return err;
     if ((err = make_map(&mB, a.W2, a.F, uint64_t(a.E) * a.d, MMA_N)) != cudaSuccess) return err;
-    p.C = static_cast<__nv_bfloat16*>(a.out);
+    p.C = a.out;
     p.ldc = a.d;
     p.n_out = a.d;
-    p.K = a.F;
+    p.K = kA;
+    p.b_k_shift = split_h ? 1 : 0;
     p.R = a.d;
     p.n_tiles = (a.d + MMA_N - 1) / MMA_N;
-    return launch_mode<kPlain>(mA, mB, p, grid_for(rows_max, a.E, p.n_tiles), stream);
+    const int g_dn = grid_for(rows_max, a.E, p.n_tiles);
+    return f32_out ? launch_mode<kPlain, kOutF32>(mA, mB, p, g_dn, stream)
+                   : launch_mode<kPlain, kOutBF16>(mA, mB, p, g_dn, stream);
 }
 
 }  // namespace moe

@@ -44,13 +44,15 @@ struct DispatchArgs {
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 
-cudaError_t launch_combine(int act_dtype, const void* out, const float* gate, const int32_t* pos, void* y, int T,
-                           int d, int k, int32_t* status, cudaStream_t stream);
+// `out_dtype` is the dtype of the expert outputs (MOE_F32 or MOE_BF16), `act_dtype` that of y.
+cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
+                           void* y, int T, int d, int k, int32_t* status, cudaStream_t stream);
 
 struct FfnArgs {
     int T, d, E, k, F;
     int expert_kind;
     int act_dtype;
+    int precision;  // MOE_PRECISION_*
     const void* xperm;
     const int32_t* offsets;
     const void* W13;

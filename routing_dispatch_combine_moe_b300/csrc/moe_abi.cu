@@ -39,6 +39,18 @@ int fail_cuda(cudaError_t e, const char* where) {
 
 inline int act_bytes(const moe_config* c) { return c->act_dtype == MOE_F32 ? 4 : 2; }
 
+inline bool bf16_experts(const moe_config* c) {
+    return c->act_dtype == MOE_BF16 && c->expert_kind != MOE_EXPERT_IDENTITY;
+}
+
+// bf16 experts with h carried as hi|lo pairs.
+inline bool split_h(const moe_config* c) { return bf16_experts(c) && c->precision == MOE_PRECISION_SPLIT_H; }
+
+// dtype of the expert-output rows the combine reads.
+inline int out_dtype(const moe_config* c) {
+    return (bf16_experts(c) && c->precision != MOE_PRECISION_BF16) ? MOE_F32 : c->act_dtype;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -49,6 +61,10 @@ int validate(const moe_config* c) {
     if (c->expert_kind != MOE_EXPERT_IDENTITY && c->expert_kind != MOE_EXPERT_RELU &&
         c->expert_kind != MOE_EXPERT_SWIGLU)
         return MOE_ERR_ARG;
+    if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_F32_OUT &&
+        c->precision != MOE_PRECISION_SPLIT_H)
+        return MOE_ERR_ARG;
+    if (c->reserved != 0) return MOE_ERR_ARG;
     if (c->k > c->E) return MOE_ERR_ARG;
     if (c->E % c->D != 0) return MOE_ERR_ARG;
     if (c->expert_kind != MOE_EXPERT_IDENTITY && c->F < 1) return MOE_ERR_ARG;
@@ -56,6 +72,7 @@ int validate(const moe_config* c) {
     if (int64_t(c->T) * c->k > int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
     if (c->expert_kind != MOE_EXPERT_IDENTITY && (int64_t(c->F) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
+    if (split_h(c) && c->F % 64 != 0) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -92,8 +109,8 @@ Layout layout(const moe_config* c) {
     L.drop_list = take(sizeof(int32_t) * A);
     L.xperm = take(b * A * size_t(c->d));
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
-        L.h = take(b * A * size_t(c->F));
-        L.out = take(b * A * size_t(c->d));
+        L.h = take(split_h(c) ? 2 * 2 * A * size_t(c->F) : b * A * size_t(c->F));
+        L.out = take((out_dtype(c) == MOE_F32 ? 4 : b) * A * size_t(c->d));
     } else {
         L.h = 0;
         L.out = L.xperm;
@@ -165,6 +182,7 @@ int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, cons
     a.T = c->T; a.d = c->d; a.E = c->E; a.k = c->k; a.F = c->F;
     a.expert_kind = c->expert_kind;
     a.act_dtype = c->act_dtype;
+    a.precision = c->precision;
     a.xperm = xperm;
     a.offsets = offsets;
     a.W13 = W13;
@@ -209,7 +227,7 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
         return rc;
     }
     if ((rc = record(events, n_events, 4, s)) != MOE_OK) return rc;
-    e = launch_combine(c->act_dtype, v.out, v.topk_gate, v.map.pos, y, c->T, c->d, c->k, v.status, s);
+    e = launch_combine(c->act_dtype, out_dtype(c), v.out, v.topk_gate, v.map.pos, y, c->T, c->d, c->k, v.status, s);
     if (e != cudaSuccess) return fail_cuda(e, "moe_combine");
     return record(events, n_events, 5, s);
 }
@@ -308,8 +326,8 @@ int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, 
     if (rc != MOE_OK) return rc;
     if (!out || !topk_gate || !pos || !y) return MOE_ERR_ARG;
     if (!aligned16(out) || !aligned16(y) || !aligned4(topk_gate) || !aligned4(pos)) return MOE_ERR_ALIGN;
-    const cudaError_t e =
-        launch_combine(cfg->act_dtype, out, topk_gate, pos, y, cfg->T, cfg->d, cfg->k, status, stream);
+    const cudaError_t e = launch_combine(cfg->act_dtype, out_dtype(cfg), out, topk_gate, pos, y, cfg->T, cfg->d,
+                                         cfg->k, status, stream);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_combine");
 }
 

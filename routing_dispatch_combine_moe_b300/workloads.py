@@ -50,6 +50,9 @@ class Workload:
     min_capacity: int = 0
     D: int = 1  # virtual expert-parallel ranks the dispatch is laid out for
     zipf_s: float | None = None
+    # bf16 experts: "bf16" (h and expert outputs in bf16), "f32_out" (expert outputs in
+    # fp32) or "split_h" (h as a bf16 hi/lo pair too); see the library header.
+    precision: str = "f32_out"
     note: str = field(default="", compare=False)
 
     @property
@@ -77,8 +80,9 @@ WORKLOADS: dict[str, Workload] = {
                  note="DeepSeek-V3-shaped routing+dispatch+combine, identity experts, "
                       "8 virtual ranks of 32 experts"),
         Workload("zipf_cf125", T=8192, d=2048, E=64, k=2, F=1408, act="bf16",
-                 expert="swiglu", capacity_factor="1.25", zipf_s=1.2,
-                 note="Zipf(1.2)-biased router, capacity factor 1.25, token-order drops"),
+                 expert="swiglu", capacity_factor="1.25", zipf_s=1.2, precision="split_h",
+                 note="Zipf(1.2)-biased router, capacity factor 1.25, token-order drops; the drops "
+                      "shrink rms(y), so h is carried as a bf16 hi/lo pair"),
         Workload("dsv3_full", T=4096, d=7168, E=256, k=8, F=2048, act="bf16",
                  expert="swiglu", note="DeepSeek-V3-shaped full layer, 22.5 GB of experts"),
     ]

@@ -75,8 +75,9 @@ class StageBuffers:
         self.drop_list = torch.full((A,), -7, **i32)
         self.n_dropped = torch.full((1,), -7, **i32)
         self.xperm = torch.full((A, w.d), float("nan"), dtype=w.torch_act, device=device)
-        self.h = torch.full((A, max(w.F, 1)), float("nan"), dtype=w.torch_act, device=device)
-        self.out = torch.full((A, w.d), float("nan"), dtype=w.torch_act, device=device)
+        self.h = torch.full((A, max(abi.hidden_cols(cfg), 1)), float("nan"), dtype=w.torch_act, device=device)
+        self.out = torch.full((A, w.d), float("nan"), dtype=abi.out_dtype(cfg), device=device)
+        self.out_act = "f32" if abi.out_dtype(cfg) == torch.float32 else "bf16"
         self.y = torch.full((w.T, w.d), float("nan"), dtype=w.torch_act, device=device)
         self.ws_dispatch = torch.zeros(abi.moe_dispatch_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.ws_ffn = torch.zeros(abi.moe_ffn_workspace_bytes(cfg), dtype=torch.uint8, device=device)
@@ -162,7 +163,8 @@ def check_ffn(w, inp, bufs, rows: int, expert_subset=None) -> float:
             continue
         X = f64(bufs.xperm[lo:hi])
         exact = fn(e, X)
-        worst = max(worst, check_close(bufs.out[lo:hi], exact, w.act, f"expert {e} output"))
+        worst = max(worst, check_close(bufs.out[lo:hi], exact, bufs.out_act, f"expert {e} output",
+                                       tol=TOL[w.act]))
     return worst
 
 

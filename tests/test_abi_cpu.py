@@ -7,6 +7,7 @@ arithmetic), so the pointers passed are never dereferenced.
 import ctypes
 
 import pytest
+import torch
 
 from routing_dispatch_combine_moe_b300 import abi, sizing
 from routing_dispatch_combine_moe_b300 import workloads as wl
@@ -54,9 +55,40 @@ def cfg(**kw):
     (dict(d=100, act="f32"), abi.MOE_OK),   # 400 bytes per fp32 row
     (dict(F=36), abi.MOE_ERR_ALIGN),
     (dict(F=36, expert="identity"), abi.MOE_OK),
+    (dict(precision="split_h"), abi.MOE_OK),
+    (dict(precision="split_h", F=72), abi.MOE_ERR_UNSUPPORTED),  # split h needs F % 64 == 0
+    (dict(precision="split_h", F=72, act="f32"), abi.MOE_OK),      # fp32 ignores the precision mode
+    (dict(precision="f32_out", F=72), abi.MOE_OK),
+    (dict(precision="bf16", F=72), abi.MOE_OK),
 ])
 def test_validate_config(kw, code):
     assert abi.moe_validate_config(cfg(**kw)) == code
+
+
+def test_validate_rejects_unknown_precision_and_reserved():
+    c = cfg()
+    c.precision = 7
+    assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
+    c = cfg()
+    c.reserved = 1
+    assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
+
+
+def test_split_h_workspace_holds_hi_lo_pairs_and_fp32_outputs():
+    fast, acc = cfg(precision="bf16"), cfg(precision="split_h")
+    A = 64 * 2
+    vf, va = abi.moe_workspace_view(), abi.moe_workspace_view()
+    base = 1 << 40
+    lib = abi.lib()
+    assert lib.moe_workspace_get_view(ctypes.byref(fast), base, abi.moe_workspace_bytes(fast), ctypes.byref(vf)) == 0
+    assert lib.moe_workspace_get_view(ctypes.byref(acc), base, abi.moe_workspace_bytes(acc), ctypes.byref(va)) == 0
+    assert vf.out - vf.h >= A * 64 * 2 and va.out - va.h >= A * 2 * 64 * 2
+    assert base + abi.moe_workspace_bytes(acc) - va.out >= A * 128 * 4
+    assert abi.out_dtype(acc) == torch.float32 and abi.out_dtype(fast) == torch.bfloat16
+    assert abi.hidden_cols(acc) == 128 and abi.hidden_cols(fast) == 64
+    mid = cfg(precision="f32_out")
+    assert abi.out_dtype(mid) == torch.float32 and abi.hidden_cols(mid) == 64
+    assert abi.out_dtype(cfg(precision="split_h", expert="identity", F=0)) == torch.bfloat16
 
 
 def test_workspace_sizes_and_layout():
