@@ -231,6 +231,29 @@ int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const floa
                            const float* bias, const void* W13, const void* W2, void* y_host,
                            void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_dispatch without a workspace, for callers that cannot give the library device
+ * memory for scratch: for example a serving loop that must not allocate device
+ * memory once it runs (cudaMalloc can synchronise the device and stall a step), or a
+ * plugin whose host framework owns every device buffer and passes in only the
+ * tensors. The pages have no counterpart of this entry point; it exists for such
+ * callers.
+ *
+ * Same arguments, outputs and results as moe_dispatch, minus ws/ws_bytes. Its
+ * scratch (histogram and drop offsets, 4 * (E * ceil(T*k/256) + E) bytes plus a
+ * small header) lives in one device array of MOE_STATIC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library keeps until the process exits.
+ * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine) and returns MOE_ERR_WORKSPACE when a config needs more scratch than that.
+ * The first call on a device looks up the array's device address on that device
+ * (cudaGetSymbolAddress, with the device current); make that first call before any
+ * stream capture. All calls share the one array: calls that may overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller. Expert
+ * ids outside [0, E) are skipped, as in moe_dispatch, but there is no status word to
+ * report them through. */
+#define MOE_STATIC_SCRATCH_BYTES (1u << 20)
+int moe_dispatch_static(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        const moe_dispatch_map* map, void* xperm, moe_stream_t stream);
+
 /* ----------------------------------------------------------- diagnostics */
 
 /* Synchronises `stream`, copies the status word at `status_dev` to *flags_host

@@ -75,6 +75,8 @@ _SIGNATURES = {
     "moe_layer_forward_traced": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p,
                                                 ctypes.POINTER(_p), _i32]),
     "moe_layer_forward_host": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
+                                           _p]),
     "moe_read_status": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
@@ -237,6 +239,12 @@ def dispatch_map(counts_routed, counts_kept, offsets, rank_offsets, pos, row_src
 def moe_dispatch(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, ws, stream=None):
     _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xperm),
                               _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_static(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, stream=None):
+    """moe_dispatch with the library's built-in scratch array (no workspace argument)."""
+    _check(lib().moe_dispatch_static(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xperm),
+                                     _stream(stream)), "moe_dispatch_static")
 
 
 def moe_expert_ffn(cfg, xperm, offsets, W13, W2, h, out, ws, stream=None):

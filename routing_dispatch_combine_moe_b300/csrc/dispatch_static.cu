@@ -1,0 +1,106 @@
+// moe_dispatch_static: the dispatch of moe_dispatch for callers that cannot give
+// the library any device memory of their own for scratch. Examples: a serving loop
+// that forbids device allocations after start-up (cudaMalloc can synchronise the
+// device and stall a latency-critical step), or a plugin whose host framework owns
+// every device buffer and exposes only the tensors it passes in.
+//
+// The dispatch needs scratch beyond its inputs and outputs: a per-block histogram
+// of E x blocks ints and E drop offsets. Here they live in one file-scope device
+// array (g_dispatch_scratch below), which every GPU that loads this library holds
+// until the process exits. This entry point allocates nothing: it calls no
+// cudaMalloc, cudaFree or allocating library routine.
+//
+// Host code cannot use the array's name as a device address (in host code it
+// names a host-side stand-in), so the device address is looked up once per device
+// with cudaGetSymbolAddress, with that device current, on the first call made on
+// it; that first call should therefore come before any stream capture.
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kStaticScratchInts = MOE_STATIC_SCRATCH_BYTES / sizeof(int32_t);
+
+// [0]: status word, [64, 64 + E*blocks): histogram, then E drop offsets.
+__device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_dispatch_scratch on the current device, looked up once.
+cudaError_t scratch_address(int32_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern thread_local std::string g_last_cuda_error;
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                   const moe_dispatch_map* map, void* xperm, moe_stream_t stream) {
+    const int rc = moe_validate_config(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!x || !topk_idx || !map || !xperm) return MOE_ERR_ARG;
+    if (!map->counts_routed || !map->counts_kept || !map->offsets || !map->rank_offsets || !map->pos ||
+        !map->row_src || !map->drop_list || !map->n_dropped)
+        return MOE_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(xperm) & 15u)) return MOE_ERR_ALIGN;
+    const int64_t A = int64_t(cfg->T) * cfg->k;
+    const size_t hist_ints = size_t(cfg->E) * size_t(dispatch_blocks(A));
+    if (64 + hist_ints + size_t(cfg->E) > kStaticScratchInts) return MOE_ERR_WORKSPACE;
+
+    int32_t* scratch = nullptr;
+    cudaError_t e = scratch_address(&scratch);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = std::string("moe_dispatch_static: ") + cudaGetErrorName(e) + " (" +
+                            cudaGetErrorString(e) + ")";
+        return MOE_ERR_CUDA;
+    }
+    DispatchArgs a{};
+    a.T = cfg->T; a.d = cfg->d; a.E = cfg->E; a.k = cfg->k; a.D = cfg->D;
+    a.capacity = cfg->capacity;
+    a.act_bytes = cfg->act_dtype == MOE_F32 ? 4 : 2;
+    a.x = x;
+    a.topk_idx = topk_idx;
+    a.counts_routed = map->counts_routed;
+    a.counts_kept = map->counts_kept;
+    a.offsets = map->offsets;
+    a.rank_offsets = map->rank_offsets;
+    a.pos = map->pos;
+    a.row_src = map->row_src;
+    a.drop_list = map->drop_list;
+    a.n_dropped = map->n_dropped;
+    a.xperm = xperm;
+    a.status = scratch;
+    a.hist = scratch + 64;
+    a.drop_offsets = scratch + 64 + hist_ints;
+    e = launch_dispatch(a, stream);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = std::string("moe_dispatch_static: ") + cudaGetErrorName(e) + " (" +
+                            cudaGetErrorString(e) + ")";
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
