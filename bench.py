@@ -220,7 +220,7 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_sample_tokens(w, max_tokens: int = 64, mem_budget: float = 24e9) -> int:
+def oracle_sample_tokens(w, max_tokens: int = 2048, mem_budget: float = 24e9) -> int:
     """Tokens per oracle sample, bounded so the float64 copies of the experts it touches fit mem_budget."""
     if w.expert == "identity":
         return min(w.T, max_tokens)
@@ -266,13 +266,31 @@ def run_ours(args, w, world, rank, local):
         for e in ev:
             e.record(stream)
     torch.cuda.synchronize()
+    # The K timed steps are captured once into a CUDA graph and replayed, so small
+    # layers are not timed as CPU launch latency; eager launches if capture fails.
+    graph, launch_mode = None, "eager"
+    if args.graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(args.steps):
+                    step(events[i])
+            graph.replay()  # one untimed replay of the captured steps
+            torch.cuda.synchronize()
+            launch_mode = "cuda_graph"
+        except Exception as exc:  # noqa: BLE001 - report and fall back
+            graph, launch_mode = None, f"eager (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         start.record(stream)
-        for i in range(args.steps):
-            step(events[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                step(events[i])
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -372,6 +390,7 @@ def run_ours(args, w, world, rank, local):
                 "h2d_bytes_per_step": w.T * w.d * w.act_bytes, "d2h_bytes_per_step": w.T * w.d * w.act_bytes,
                 "api": "moe_layer_forward_host"},
         "gpu_launches": abi.moe_kernels_per_forward(cfg) * args.steps,
+        "launch": launch_mode,
         "cpu_baseline": cpu,
     }
     return line
@@ -414,6 +433,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch the timed steps eagerly instead of replaying a CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

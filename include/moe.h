@@ -21,6 +21,12 @@
  * within an expert, so rank r of D virtual ranks (experts [r*E/D,(r+1)*E/D))
  * owns one contiguous chunk of rows.
  *
+ * Shared experts: with S = cfg.n_shared > 0, experts E..E+S-1 are shared: every token
+ * also uses each of them with gate 1, after its k routed slots (the pages' decode
+ * example sends each token to 8 routed experts plus the shared one). Below, "slots"
+ * K = k + S and "experts" N = E + S; capacity limits only the routed experts, and the
+ * D virtual ranks split the routed experts, the shared rows following rank D-1's.
+ *
  * Conventions for every entry point:
  *   - Pointers named *_host are host memory; every other pointer is device
  *     memory on the current CUDA device, allocated and owned by the caller. The
@@ -80,42 +86,42 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
                                    fp32: y then carries essentially only its own final rounding */
 
 /* Limits of this build. */
-#define MOE_MAX_K 16        /* experts per token */
-#define MOE_MAX_E 256       /* routed experts */
+#define MOE_MAX_K 16        /* experts per token, routed plus shared */
+#define MOE_MAX_E 512       /* experts, routed plus shared */
 
 typedef struct moe_config {
     int32_t T;           /* tokens (rows of x), >= 1 */
     int32_t d;           /* hidden size, >= 1 */
-    int32_t E;           /* routed experts, 1..MOE_MAX_E */
-    int32_t k;           /* experts kept per token, 1..min(E, MOE_MAX_K) */
+    int32_t E;           /* routed experts; E + n_shared <= MOE_MAX_E */
+    int32_t k;           /* routed experts kept per token, 1..E; k + n_shared <= MOE_MAX_K */
     int32_t F;           /* expert FFN width (ignored for identity experts) */
-    int32_t D;           /* virtual expert-parallel ranks, E % D == 0 (1 = none) */
+    int32_t D;           /* virtual expert-parallel ranks over the routed experts, E % D == 0 (1 = none) */
     int32_t act_dtype;   /* MOE_F32 or MOE_BF16: x, dispatched rows, h, expert outputs, y */
     int32_t expert_kind; /* MOE_EXPERT_* */
     int32_t precision;   /* MOE_PRECISION_*; SPLIT_H needs F % 64 == 0 */
-    int32_t reserved;    /* must be 0 */
+    int32_t n_shared;    /* shared experts S >= 0: experts E..E+S-1, used by every token with gate 1 */
     int64_t capacity;    /* tokens each expert keeps; < 0 = dropless (see moe_capacity) */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
 typedef struct moe_dispatch_map {
-    int32_t* counts_routed; /* [E]   assignments routed to each expert */
-    int32_t* counts_kept;   /* [E]   min(counts_routed, capacity) */
-    int32_t* offsets;       /* [E+1] exclusive scan of counts_kept; rows of expert e are [offsets[e], offsets[e+1]) */
+    int32_t* counts_routed; /* [N]   assignments routed to each expert */
+    int32_t* counts_kept;   /* [N]   min(counts_routed, capacity) (shared experts: all T) */
+    int32_t* offsets;       /* [N+1] exclusive scan of counts_kept; rows of expert e are [offsets[e], offsets[e+1]) */
     int32_t* rank_offsets;  /* [D+1] offsets[r*E/D]: virtual rank r's send chunk is [rank_offsets[r], rank_offsets[r+1]) */
-    int32_t* pos;           /* [T*k] row of assignment t*k+j, or -1 if it was dropped */
-    int32_t* row_src;       /* [T*k] assignment t*k+j held by each row; entries [0, offsets[E]) are written */
-    int32_t* drop_list;     /* [T*k] dropped assignments, ordered by (expert, token); [0, n_dropped) written */
+    int32_t* pos;           /* [T*K] row of assignment t*K+j, or -1 if it was dropped */
+    int32_t* row_src;       /* [T*K] assignment t*K+j held by each row; entries [0, offsets[N]) are written */
+    int32_t* drop_list;     /* [T*K] dropped assignments, ordered by (expert, token); [0, n_dropped) written */
     int32_t* n_dropped;     /* [1]   number of dropped assignments */
 } moe_dispatch_map;
 
 /* Pointers into a moe_layer_forward workspace (all device memory inside it). */
 typedef struct moe_workspace_view {
     int32_t* status;     /* device status word (MOE_DEV_* flags) */
-    int32_t* topk_idx;   /* [T*k] */
-    float* topk_gate;    /* [T*k] */
+    int32_t* topk_idx;   /* [T*K] */
+    float* topk_gate;    /* [T*K] */
     moe_dispatch_map map;
-    void* xperm;         /* [T*k, d] act: dispatched rows (the dispatch "send buffer") */
+    void* xperm;         /* [T*K, d] act: dispatched rows (the dispatch "send buffer") */
     void* h;             /* expert hidden activations, see moe_expert_ffn (NULL for identity) */
     void* out;           /* expert outputs, see moe_expert_ffn (aliases xperm for identity) */
 } moe_workspace_view;
@@ -133,6 +139,7 @@ int64_t moe_capacity(int32_t T, int32_t k, int32_t E, int64_t cf_num, int64_t cf
 int moe_validate_config(const moe_config* cfg);
 
 /* Workspace bytes each entry point needs (0 when cfg is invalid). */
+size_t moe_route_workspace_bytes(const moe_config* cfg);
 size_t moe_dispatch_workspace_bytes(const moe_config* cfg);
 size_t moe_ffn_workspace_bytes(const moe_config* cfg);
 size_t moe_workspace_bytes(const moe_config* cfg);      /* moe_layer_forward */
@@ -152,20 +159,23 @@ int moe_kernels_per_forward(const moe_config* cfg);
  *   x         [T, d] act dtype
  *   Wg        [d, E] fp32 (the page's W_g in R^{d x E})
  *   bias      [E] fp32 added to every token's logits before KeepTopK, or NULL
- *   topk_idx  [T, k] int32 out: kept experts, slot 0 = largest logit; equal logits
- *             rank the lower expert id first
- *   topk_gate [T, k] fp32 out: G = exp(H_j - H_max) / sum over kept slots
- * Logits are fp32 sums of fp32 products (x is promoted exactly). */
+ *   topk_idx  [T, K] int32 out: kept experts, slot 0 = largest logit; equal logits
+ *             rank the lower expert id first; slots k..K-1 hold the shared experts
+ *   topk_gate [T, K] fp32 out: G = exp(H_j - H_max) / sum over kept slots (1 for shared)
+ *   ws        scratch of moe_route_workspace_bytes(cfg) bytes: the logits are summed
+ *             from split-K partials kept there.
+ * Logits are fp32 sums of fp32 products (x is promoted exactly), summed in a fixed
+ * order, so the result is deterministic. */
 int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
-              int32_t* topk_idx, float* topk_gate, moe_stream_t stream);
+              int32_t* topk_idx, float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Dispatch: groups the T*k assignments by expert, keeps the first `capacity` of
  * each expert in token order, and gathers the kept rows of x into `xperm`
  * ("EP Math": "The dispatch all-to-all", "Capacity factor", "Token drop").
- *   x        [T, d] act;  topk_idx [T, k] int32 (ids outside [0, E) are skipped
+ *   x        [T, d] act;  topk_idx [T, K] int32 (ids outside [0, N) are skipped
  *            and flagged MOE_DEV_ERR_INDEX)
  *   map      output arrays (see moe_dispatch_map)
- *   xperm    [T*k, d] act out: row r = x[row_src[r] / k]; rows [0, offsets[E]) written
+ *   xperm    [T*K, d] act out: row r = x[row_src[r] / K]; rows [0, offsets[N]) written
  *   ws       >= moe_dispatch_workspace_bytes(cfg) bytes; its first 4 bytes are the
  *            device status word, which this call clears first.
  * Bit-exact and deterministic: the result does not depend on scheduling. */
@@ -176,14 +186,14 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
 /* Grouped expert FFN over the dispatched rows: for each expert e, rows
  * [offsets[e], offsets[e+1]) of xperm go through Expert_e ("EP Math", "What expert
  * parallelism actually shards": every expert is a complete FFN with private weights).
- *   xperm   [T*k, d] act;  offsets [E+1] int32 (from moe_dispatch)
- *   W13     SwiGLU: [E, 2F, d] act, rows [0,F) = W_gate^T, rows [F,2F) = W_up^T;
- *           ReLU:   [E, F, d]  act (W1^T).   (The usual linear-layer layout.)
- *   W2      [E, d, F] act (W_down^T / W2^T)
- *   h       out: hidden activation of each row, [T*k, F] act; under MOE_PRECISION_SPLIT_H
- *           [T*k, 2F] bf16: for every 64-column block b of h the 64 "hi" values at
+ *   xperm   [T*K, d] act;  offsets [N+1] int32 (from moe_dispatch)
+ *   W13     SwiGLU: [N, 2F, d] act, rows [0,F) = W_gate^T, rows [F,2F) = W_up^T;
+ *           ReLU:   [N, F, d]  act (W1^T).   (The usual linear-layer layout.)
+ *   W2      [N, d, F] act (W_down^T / W2^T)
+ *   h       out: hidden activation of each row, [T*K, F] act; under MOE_PRECISION_SPLIT_H
+ *           [T*K, 2F] bf16: for every 64-column block b of h the 64 "hi" values at
  *           columns [128b, 128b+64) and the 64 "lo" values at [128b+64, 128b+128).
- *   out     out: expert output of each row, [T*k, d]; fp32 under MOE_PRECISION_F32_OUT
+ *   out     out: expert output of each row, [T*K, d]; fp32 under MOE_PRECISION_F32_OUT
  *           and MOE_PRECISION_SPLIT_H with bf16 activations, else the act dtype.
  * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation); fp32
  * runs on the fp32 FMA units. Requires F * sizeof(act) % 16 == 0 besides the row
@@ -193,15 +203,15 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
                    const void* W13, const void* W2, void* h, void* out,
                    void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Combine: y[t] = sum over slots j with pos[t*k+j] >= 0 of topk_gate[t*k+j] * out[pos[t*k+j]],
+/* Combine: y[t] = sum over slots j < K with pos[t*K+j] >= 0 of topk_gate[t*K+j] * out[pos[t*K+j]],
  * with `out` in the dtype moe_expert_ffn writes (see there; the activation dtype for
  * identity experts),
  * summed in fp32 in slot order and rounded once ("Mixture-of-Experts (MoE)
  * Architecture and Expert Parallelism", section 2; "EP Math", "The combine
  * all-to-all"; "Token drop": a dropped slot adds nothing and the gates are not
- * renormalised). A row index >= T*k is skipped and flagged in `status` if
+ * renormalised). A row index >= T*K is skipped and flagged in `status` if
  * status is not NULL. Deterministic, no atomics.
- *   out [T*k, d] act; topk_gate [T, k] fp32; pos [T, k] int32; y [T, d] act out. */
+ *   out [T*K, d]; topk_gate [T, K] fp32; pos [T, K] int32; y [T, d] act out. */
 int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate,
                 const int32_t* pos, void* y, int32_t* status, moe_stream_t stream);
 
@@ -239,7 +249,7 @@ int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const floa
  * callers.
  *
  * Same arguments, outputs and results as moe_dispatch, minus ws/ws_bytes. Its
- * scratch (histogram and drop offsets, 4 * (E * ceil(T*k/256) + E) bytes plus a
+ * scratch (histogram and drop offsets, 4 * (N * ceil(T*K/256) + N) bytes plus a
  * small header) lives in one device array of MOE_STATIC_SCRATCH_BYTES inside the
  * library, which every GPU that loads the library keeps until the process exits.
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library

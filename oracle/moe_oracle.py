@@ -30,6 +30,10 @@ Sources (page title, then section):
           capacity factor.
 * [SWI]   same page, "Memory residency for the same shape": the gated three-matrix
           expert form (gate, up, down).
+* [SHR]   same page, "Token assignments and the capacity worksheet" and "Training,
+          prefill and decode are different workloads": a shared expert that every
+          token uses; in DeepSeek's decode deployment it is handled like a routed
+          one, so each token sends 9 vectors (8 routed + the shared expert).
 
 Readings where the pages are silent (each is listed in the design notes too):
 
@@ -44,6 +48,9 @@ Readings where the pages are silent (each is listed in the design notes too):
 * a dropped slot's gate is not renormalised over the kept slots;
 * SwiGLU expert: silu(x W_gate) * (x W_up) then W_down, silu(z) = z / (1 + e^-z),
   no biases; ReLU expert: relu(x W_1) W_2.
+* shared experts are experts E .. E+n_shared-1: every token is also dispatched to
+  each of them with gate 1, after its k routed slots; capacity limits only the
+  routed experts.
 
 Every arithmetic step runs in float64 on exact float64 copies of the inputs (bf16
 and fp32 values are exact in float64). ``round_to_bf16`` is only for the optional
@@ -163,7 +170,7 @@ def expert_capacity(T: int, k: int, E: int, capacity_factor, min_capacity: int =
     return max(C, int(min_capacity))
 
 
-def dispatch(idx, E: int, capacity=None, D: int = 1) -> dict:
+def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None) -> dict:
     """Group the T*k assignments by expert, dropping overflow.  [A2A], [CAP], [DROP]
 
     Assignment a = t*k + j is token t's j-th slot. For each expert in ascending id
@@ -172,12 +179,15 @@ def dispatch(idx, E: int, capacity=None, D: int = 1) -> dict:
     rest are dropped. Kept assignments take consecutive rows in that order, so the
     row segment of expert e is [offsets[e], offsets[e+1]). With D virtual ranks,
     rank r owns experts [r E/D, (r+1) E/D) [EPSH], and its rows start at
-    rank_offsets[r].
+    rank_offsets[r]. Only experts with id < ``capped_experts`` (default: all E) are
+    held to the capacity; the ranks then split those experts, and later experts
+    (shared ones) follow after rank_offsets[D].
     """
     idx = np.asarray(idx)
     T, k = idx.shape
-    if E % D != 0:
-        raise ValueError("E must be divisible by D")
+    capped = E if capped_experts is None else capped_experts
+    if capped % D != 0:
+        raise ValueError("the routed experts must divide into D ranks")
     counts_routed = np.zeros(E, np.int64)
     counts_kept = np.zeros(E, np.int64)
     kept_ids, dropped_ids = [], []
@@ -185,7 +195,7 @@ def dispatch(idx, E: int, capacity=None, D: int = 1) -> dict:
         tok, slot = np.nonzero(idx == e)  # row-major scan: ascending token index
         a = tok * k + slot
         counts_routed[e] = a.size
-        keep = a if capacity is None else a[:capacity]
+        keep = a if (capacity is None or e >= capped) else a[:capacity]
         counts_kept[e] = keep.size
         kept_ids.append(keep)
         dropped_ids.append(a[keep.size:])
@@ -194,7 +204,7 @@ def dispatch(idx, E: int, capacity=None, D: int = 1) -> dict:
     offsets = np.concatenate([[0], np.cumsum(counts_kept)]).astype(np.int64)
     pos = np.full(T * k, -1, np.int64)
     pos[row_src] = np.arange(row_src.size)
-    rank_offsets = offsets[np.arange(D + 1) * (E // D)]
+    rank_offsets = offsets[np.arange(D + 1) * (capped // D)]
     return dict(
         counts_routed=counts_routed,
         counts_kept=counts_kept,
@@ -251,12 +261,14 @@ def combine(G, pos, out, T: int, k: int) -> np.ndarray:
     return y
 
 
-def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1) -> dict:
+def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, n_shared: int = 0) -> dict:
     """The whole layer: logits, KeepTopK, kept softmax, dispatch, experts, combine.
 
     ``expert_fn(e, X)`` returns Expert_e applied to the rows X (an [M, d] float64
-    array); for identity experts pass ``lambda e, X: X``. Returns every
-    intermediate the GPU path exposes, in float64 (y is not rounded).
+    array); for identity experts pass ``lambda e, X: X``. With ``n_shared`` shared
+    experts [SHR], every token also uses experts E .. E+n_shared-1 with gate 1 in
+    slots k .. k+n_shared-1. Returns every intermediate the GPU path exposes, in
+    float64 (y is not rounded); ``idx`` and ``G`` then have k + n_shared slots.
     """
     x = _f64(x)
     T, d = x.shape
@@ -264,11 +276,15 @@ def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1) 
     E = H.shape[1]
     idx = keep_topk(H, k)
     G = kept_softmax(H, idx)
-    disp = dispatch(idx, E, capacity, D)
+    if n_shared:
+        idx = np.concatenate([idx, np.broadcast_to(E + np.arange(n_shared), (T, n_shared))], axis=1)
+        G = np.concatenate([G, np.ones((T, n_shared))], axis=1)
+        k = k + n_shared
+    disp = dispatch(idx, E + n_shared, capacity, D, capped_experts=E)
     xperm = x[disp["row_src"] // k]
     out = np.zeros_like(xperm)
     off = disp["offsets"]
-    for e in range(E):
+    for e in range(E + n_shared):
         lo, hi = off[e], off[e + 1]
         if hi > lo:
             out[lo:hi] = expert_fn(e, xperm[lo:hi])

@@ -25,7 +25,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_EXPERT_IDENTITY, MOE_EXPERT_RELU, MOE_EXPERT_SWIGLU = 0, 1, 2
 MOE_PRECISION_BF16, MOE_PRECISION_F32_OUT, MOE_PRECISION_SPLIT_H = 0, 1, 2
 PRECISIONS = {"bf16": MOE_PRECISION_BF16, "f32_out": MOE_PRECISION_F32_OUT, "split_h": MOE_PRECISION_SPLIT_H}
-MOE_MAX_K, MOE_MAX_E = 16, 256
+MOE_MAX_K, MOE_MAX_E = 16, 512
 EXPERT_KINDS = {"identity": MOE_EXPERT_IDENTITY, "relu": MOE_EXPERT_RELU, "swiglu": MOE_EXPERT_SWIGLU}
 ACT_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
 
@@ -44,7 +44,7 @@ class MoeError(RuntimeError):
 
 class moe_config(ctypes.Structure):
     _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("F", _i32), ("D", _i32),
-                ("act_dtype", _i32), ("expert_kind", _i32), ("precision", _i32), ("reserved", _i32),
+                ("act_dtype", _i32), ("expert_kind", _i32), ("precision", _i32), ("n_shared", _i32),
                 ("capacity", _i64)]
 
 
@@ -67,7 +67,8 @@ _SIGNATURES = {
     "moe_workspace_bytes_host": (_sz, [ctypes.POINTER(moe_config)]),
     "moe_workspace_get_view": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _sz, ctypes.POINTER(moe_workspace_view)]),
     "moe_kernels_per_forward": (ctypes.c_int, [ctypes.POINTER(moe_config)]),
-    "moe_route": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p]),
+    "moe_route_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_route": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p, _p, _sz, _p]),
     "moe_expert_ffn": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_combine": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p]),
@@ -127,10 +128,11 @@ def _stream(stream=None):
 
 
 # ------------------------------------------------------------------ config
-def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None, precision="f32_out") -> moe_config:
+def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None, precision="f32_out",
+                n_shared=0) -> moe_config:
     """A moe_config; ``capacity`` None (dropless) or a non-negative integer."""
     return moe_config(T=T, d=d, E=E, k=k, F=F, D=D, act_dtype=ACT_DTYPES[act],
-                      expert_kind=EXPERT_KINDS[expert], precision=PRECISIONS[precision], reserved=0,
+                      expert_kind=EXPERT_KINDS[expert], precision=PRECISIONS[precision], n_shared=n_shared,
                       capacity=-1 if capacity is None else int(capacity))
 
 
@@ -163,7 +165,7 @@ def config_for(w, capacity="auto") -> moe_config:
     if capacity == "auto":
         capacity = None if w.capacity_factor is None else moe_capacity(w.T, w.k, w.E, w.capacity_factor,
                                                                        w.min_capacity)
-    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision)
+    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision, w.n_shared)
 
 
 def moe_validate_config(cfg) -> int:
@@ -226,9 +228,15 @@ def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
 
 
 # ------------------------------------------------------------------ hot path
-def moe_route(cfg, x, Wg, bias, topk_idx, topk_gate, stream=None):
+def moe_route_workspace_bytes(cfg) -> int:
+    return lib().moe_route_workspace_bytes(ctypes.byref(cfg))
+
+
+def moe_route(cfg, x, Wg, bias, topk_idx, topk_gate, ws=None, stream=None):
+    """``ws``: a uint8 device tensor of moe_route_workspace_bytes(cfg) bytes (None when that is 0)."""
+    n = 0 if ws is None else ws.numel()
     _check(lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(bias), _ptr(topk_idx), _ptr(topk_gate),
-                           _stream(stream)), "moe_route")
+                           _ptr(ws), n, _stream(stream)), "moe_route")
 
 
 def dispatch_map(counts_routed, counts_kept, offsets, rank_offsets, pos, row_src, drop_list, n_dropped):

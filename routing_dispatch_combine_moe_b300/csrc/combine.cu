@@ -40,25 +40,6 @@ struct Vec16<__nv_bfloat16> {
     }
 };
 
-// Loads 8 consecutive elements of a row as fp32.
-template <typename T>
-struct Load8;
-template <>
-struct Load8<float> {
-    __device__ static void load(const float* p, float* f) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-        f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
-        f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
-    }
-};
-template <>
-struct Load8<__nv_bfloat16> {
-    __device__ static void load(const __nv_bfloat16* p, float* f) {
-        Vec16<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4*>(p)), f);
-    }
-};
-
 template <typename T>
 __device__ __forceinline__ void store8(T* p, const float* f);
 template <>
@@ -72,10 +53,14 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* p, const fl
 }
 
 // d must be a multiple of 8 here (16-byte bf16 rows); fp32 rows of d % 8 == 4 use the 4-wide kernel.
-template <typename TOut, typename TY>
+// Each step a lane covers 32 bytes of every kept slot's row (16 bf16 or 8 fp32
+// values) and issues all KMAX slots' loads before the first multiply-add, so up
+// to KMAX x 32 bytes per lane are in flight.
+template <typename TOut, typename TY, int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ out, const float* __restrict__ gate,
                                                       const int32_t* __restrict__ pos, TY* __restrict__ y, int T,
                                                       int k, int d, int64_t max_rows, int32_t* status) {
+    constexpr int EPL = 32 / int(sizeof(TOut));  // elements per lane per step
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -89,36 +74,46 @@ __global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ o
             p = -1;
         }
     }
-    int src[MOE_MAX_K];
-    float gj[MOE_MAX_K];
+    int src[KMAX];
+    float gj[KMAX];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_K; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
         src[j] = __shfl_sync(0xFFFFFFFFu, p, j);
         gj[j] = __shfl_sync(0xFFFFFFFFu, g, j);
+        if (j >= k) src[j] = -1;
     }
-    for (int c = lane * 8; c < d; c += 32 * 8) {
-        float acc[8];
+    for (int c0 = lane * EPL; c0 < d; c0 += 32 * EPL) {
+        const bool full = c0 + EPL <= d;
+        uint4 raw[KMAX][2];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-#pragma unroll
-        for (int j0 = 0; j0 < MOE_MAX_K; j0 += 4) {
-            if (j0 >= k) break;
-            float f[4][8];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = j0 + jj;
-                if (j < k && src[j] >= 0) Load8<TOut>::load(out + size_t(src[j]) * d + c, f[jj]);
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = j0 + jj;
-                if (j < k && src[j] >= 0) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[q] = fmaf(gj[j], f[jj][q], acc[q]);
-                }
+        for (int j = 0; j < KMAX; ++j) {
+            if (src[j] >= 0) {
+                const uint4* rp = reinterpret_cast<const uint4*>(out + size_t(src[j]) * d + c0);
+                raw[j][0] = __ldg(rp);
+                raw[j][1] = full ? __ldg(rp + 1) : make_uint4(0, 0, 0, 0);
             }
         }
-        store8<TY>(y + size_t(t) * d + c, acc);
+        float acc[EPL];
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) acc[q] = 0.f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (src[j] >= 0) {
+                float f[EPL];
+                if constexpr (sizeof(TOut) == 2) {
+                    Vec16<__nv_bfloat16>::unpack(raw[j][0], f);
+                    Vec16<__nv_bfloat16>::unpack(raw[j][1], f + 8);
+                } else {
+                    Vec16<float>::unpack(raw[j][0], f);
+                    Vec16<float>::unpack(raw[j][1], f + 4);
+                }
+#pragma unroll
+                for (int q = 0; q < EPL; ++q) acc[q] = fmaf(gj[j], f[q], acc[q]);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < EPL / 8; ++h)
+            if (full || h == 0) store8<TY>(y + size_t(t) * d + c0 + 8 * h, acc + 8 * h);
     }
 }
 
@@ -160,6 +155,17 @@ __global__ void __launch_bounds__(256) combine_kernel_f32x4(const float* __restr
     }
 }
 
+template <typename TOut, typename TY>
+void launch_k(int grid, const void* out, const float* gate, const int32_t* pos, void* y, int T, int k, int d,
+              int64_t max_rows, int32_t* status, cudaStream_t stream) {
+    const TOut* o = static_cast<const TOut*>(out);
+    TY* yy = static_cast<TY*>(y);
+    if (k <= 2) combine_kernel<TOut, TY, 2><<<grid, 256, 0, stream>>>(o, gate, pos, yy, T, k, d, max_rows, status);
+    else if (k <= 4) combine_kernel<TOut, TY, 4><<<grid, 256, 0, stream>>>(o, gate, pos, yy, T, k, d, max_rows, status);
+    else if (k <= 8) combine_kernel<TOut, TY, 8><<<grid, 256, 0, stream>>>(o, gate, pos, yy, T, k, d, max_rows, status);
+    else combine_kernel<TOut, TY, 16><<<grid, 256, 0, stream>>>(o, gate, pos, yy, T, k, d, max_rows, status);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
@@ -168,18 +174,14 @@ cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const 
     const int grid = (T + 7) / 8;
     if (act_dtype == MOE_F32) {
         if (d % 8 == 0)
-            combine_kernel<float, float><<<grid, 256, 0, stream>>>(static_cast<const float*>(out), gate, pos,
-                                                                   static_cast<float*>(y), T, k, d, max_rows, status);
+            launch_k<float, float>(grid, out, gate, pos, y, T, k, d, max_rows, status, stream);
         else
             combine_kernel_f32x4<<<grid, 256, 0, stream>>>(static_cast<const float*>(out), gate, pos,
                                                            static_cast<float*>(y), T, k, d, max_rows, status);
     } else if (out_dtype == MOE_F32) {
-        combine_kernel<float, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-            static_cast<const float*>(out), gate, pos, static_cast<__nv_bfloat16*>(y), T, k, d, max_rows, status);
+        launch_k<float, __nv_bfloat16>(grid, out, gate, pos, y, T, k, d, max_rows, status, stream);
     } else {
-        combine_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(out), gate, pos, static_cast<__nv_bfloat16*>(y), T, k, d, max_rows,
-            status);
+        launch_k<__nv_bfloat16, __nv_bfloat16>(grid, out, gate, pos, y, T, k, d, max_rows, status, stream);
     }
     return cudaGetLastError();
 }

@@ -84,7 +84,7 @@ __device__ int block_excl_scan(int v, int* warp_sums, int* total) {
     return r;
 }
 
-__global__ void __launch_bounds__(1024) scan_kernel(int E, int D, int nblk, int64_t capacity,
+__global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, int nblk, int64_t capacity,
                                                     int32_t* __restrict__ hist, int32_t* __restrict__ counts_routed,
                                                     int32_t* __restrict__ counts_kept, int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ drop_offsets,
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int D, int nblk, int6
     __syncthreads();
 
     const int cr = tid < E ? routed[tid] : 0;
-    const int ck = (capacity < 0 || cr <= capacity) ? cr : int(capacity);
+    const int ck = (capacity < 0 || tid >= E_capped || cr <= capacity) ? cr : int(capacity);
     const int off = block_excl_scan(ck, warp_sums, &totals[0]);
     const int doff = block_excl_scan(cr - ck, warp_sums, &totals[1]);
     if (tid < E) {
@@ -127,11 +127,11 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int D, int nblk, int6
         *n_dropped = totals[1];
     }
     __syncthreads();
-    if (tid <= D) rank_offsets[tid] = offs[tid * (E / D)];
+    if (tid <= D) rank_offsets[tid] = offs[tid * (E_capped / D)];
 }
 
 __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* __restrict__ topk_idx, int64_t A,
-                                                                 int E, int nblk, int64_t capacity,
+                                                                 int E, int E_capped, int nblk, int64_t capacity,
                                                                  const int32_t* __restrict__ hist,
                                                                  const int32_t* __restrict__ offsets,
                                                                  const int32_t* __restrict__ drop_offsets,
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* 
     }
     int rank = hist[size_t(e) * nblk + blockIdx.x] + rank_in_warp;
     for (int w = 0; w < warp; ++w) rank += cnt[w][e];
-    if (capacity < 0 || rank < capacity) {
+    if (capacity < 0 || e >= E_capped || rank < capacity) {
         const int row = offsets[e] + rank;
         pos[a] = row;
         row_src[row] = int32_t(a);
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
 #pragma unroll
     for (int j = 0; j < MOE_MAX_K; ++j) dst[j] = __shfl_sync(0xFFFFFFFFu, p, j);
     const uint4* src = x + size_t(t) * vec_per_row;
-    constexpr int U = 4;
+    constexpr int U = 8;  // 16-byte pieces per lane in flight
     for (int v0 = lane; v0 < vec_per_row; v0 += 32 * U) {
         uint4 buf[U];
 #pragma unroll
@@ -217,10 +217,10 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const int64_t A = int64_t(a.T) * a.k;
     const int nblk = dispatch_blocks(A);
     count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.hist, a.status);
-    scan_kernel<<<1, 1024, 0, stream>>>(a.E, a.D, nblk, a.capacity, a.hist, a.counts_routed, a.counts_kept,
-                                        a.offsets, a.drop_offsets, a.rank_offsets, a.n_dropped);
-    scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.capacity, a.hist, a.offsets,
-                                                        a.drop_offsets, a.pos, a.row_src, a.drop_list);
+    scan_kernel<<<1, 1024, 0, stream>>>(a.E, a.E_capped, a.D, nblk, a.capacity, a.hist, a.counts_routed,
+                                        a.counts_kept, a.offsets, a.drop_offsets, a.rank_offsets, a.n_dropped);
+    scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, a.E_capped, nblk, a.capacity, a.hist,
+                                                        a.offsets, a.drop_offsets, a.pos, a.row_src, a.drop_list);
     const int vec_per_row = int(int64_t(a.d) * a.act_bytes / 16);
     gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
                                                       static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, A);

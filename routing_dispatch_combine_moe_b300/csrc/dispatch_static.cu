@@ -66,9 +66,10 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
         !map->row_src || !map->drop_list || !map->n_dropped)
         return MOE_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(xperm) & 15u)) return MOE_ERR_ALIGN;
-    const int64_t A = int64_t(cfg->T) * cfg->k;
-    const size_t hist_ints = size_t(cfg->E) * size_t(dispatch_blocks(A));
-    if (64 + hist_ints + size_t(cfg->E) > kStaticScratchInts) return MOE_ERR_WORKSPACE;
+    const int N = cfg->E + cfg->n_shared, K = cfg->k + cfg->n_shared;
+    const int64_t A = int64_t(cfg->T) * K;
+    const size_t hist_ints = size_t(N) * size_t(dispatch_blocks(A));
+    if (64 + hist_ints + size_t(N) > kStaticScratchInts) return MOE_ERR_WORKSPACE;
 
     int32_t* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
@@ -79,7 +80,8 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
         return MOE_ERR_CUDA;
     }
     DispatchArgs a{};
-    a.T = cfg->T; a.d = cfg->d; a.E = cfg->E; a.k = cfg->k; a.D = cfg->D;
+    a.T = cfg->T; a.d = cfg->d; a.E = N; a.k = K; a.D = cfg->D;
+    a.E_capped = cfg->E;
     a.capacity = cfg->capacity;
     a.act_bytes = cfg->act_dtype == MOE_F32 ? 4 : 2;
     a.x = x;

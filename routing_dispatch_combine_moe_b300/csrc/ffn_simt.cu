@@ -159,7 +159,13 @@ cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t stream, cudaEvent_t m
     p.n_tiles = (a.F + TN - 1) / TN;
     cudaError_t err = swiglu ? launch_mode<kSwiGLU>(p, rows_max, stream) : launch_mode<kReLU>(p, rows_max, stream);
     if (err != cudaSuccess) return err;
-    if (mid_event && (err = cudaEventRecord(mid_event, stream)) != cudaSuccess) return err;
+    if (mid_event) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((err = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return err;
+        err = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(mid_event, stream, cudaEventRecordExternal)
+                                                  : cudaEventRecord(mid_event, stream);
+        if (err != cudaSuccess) return err;
+    }
     // Down projection.
     p.A = static_cast<const float*>(a.h);
     p.B = static_cast<const float*>(a.W2);

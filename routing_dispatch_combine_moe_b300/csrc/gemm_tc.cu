@@ -8,7 +8,14 @@
 //   down : out[r, :] = h[r, :] . W2[e]^T
 // for every dispatched row r of expert e (rows [offsets[e], offsets[e+1])).
 //
-// Persistent, warp-specialised kernel, one CTA per SM (192 threads):
+// Persistent, warp-specialised kernel, one CTA per SM (192 threads); two variants:
+//   PAIR=false: one SM per 128x256 output tile (tcgen05 cta_group::1, M=128).
+//   PAIR=true : clusters of two SMs share a 256x256 tile (cta_group::2, M=256): each SM
+//               loads its own 128 rows of A and half of the 256 B rows (the gate half or
+//               the up half for SwiGLU), so a stage is 32 KB per SM instead of 48 KB and
+//               six stages fit; one thread of the even CTA issues the pair MMA, which
+//               writes each SM's 128 accumulator rows into its own TMEM.
+// Roles per CTA:
 //   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
 //               swizzle, 4-stage ring of 48 KB stages guarded by full/empty mbarriers.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and one
@@ -37,21 +44,30 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <cstdlib>
 #include <mutex>
 
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BK = 64, MMA_N = 256, STAGES = 4;
-constexpr int A_STAGE = BM * BK * 2;     // 16 KB
-constexpr int B_STAGE = MMA_N * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int BK = 64, MMA_N = 256;
+constexpr int A_STAGE = 128 * BK * 2;  // 16 KB: 128 rows of A per SM
 constexpr int TMEM_COLS = 512;
 constexpr int kThreads = 192;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
 
 enum Mode : int { kSwiGLU = 0, kPlain = 1, kReLU = 2 };
 enum Out : int { kOutBF16 = 0, kOutHiLo = 1, kOutF32 = 2 };
+
+template <bool PAIR>
+struct Cfg {
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int B_ROWS = PAIR ? MMA_N / 2 : MMA_N;  // B rows this SM loads per stage
+    static constexpr int B_STAGE = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;     // bytes landing in this SM per stage
+    static constexpr int TILE_M = PAIR ? 256 : 128;           // rows of one output tile
+    static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_M, MMA_N);
+    static constexpr int EPI_WARPS_TOTAL = PAIR ? 8 : 4;      // arrivals that free an accumulator
+};
 
 struct Params {
     const int32_t* offsets;  // [E+1]
@@ -67,6 +83,7 @@ struct Params {
     int32_t* status;
 };
 
+template <int STAGES>
 struct Smem {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -79,7 +96,11 @@ struct Smem {
     int tile[MOE_MAX_E + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + sizeof(Smem);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+    return 1024 /*alignment slack*/ + size_t(Cfg<PAIR>::STAGES) * Cfg<PAIR>::STAGE_BYTES +
+           sizeof(Smem<Cfg<PAIR>::STAGES>);
+}
 
 __device__ __forceinline__ void decode_tile(int t, const int* tile, int E, int n_tiles, int& e, int& mt, int& nt) {
     int lo = 0, hi = E - 1;
@@ -137,18 +158,89 @@ __device__ __forceinline__ void store_hidden(uint16_t* row_ptr, int col0, int n_
     }
 }
 
+// Epilogue of one accumulator tile for the 32 TMEM lanes (= rows) of this warp.
 template <int MODE, int OUT>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t tbase, int row, bool row_ok, int nt) {
+    if (MODE == kSwiGLU) {
+        uint16_t* crow = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, g);
+            tmem_ld_32x32b_x32(tbase + MMA_N / 2 + c * 32, u);
+            tmem_ld_wait();
+            const int col0 = nt * (MMA_N / 2) + c * 32;
+            if (row_ok && col0 < p.n_out) {
+                float h[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) h[j] = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                store_hidden<OUT>(crow, col0, p.n_out, h);
+            }
+        }
+    } else if (MODE == kReLU) {
+        uint16_t* crow = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
+#pragma unroll 1
+        for (int c = 0; c < MMA_N / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
+            const int col0 = nt * MMA_N + c * 32;
+            if (row_ok && col0 < p.n_out) {
+                float h[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) h[j] = fmaxf(__uint_as_float(v[j]), 0.f);
+                store_hidden<OUT>(crow, col0, p.n_out, h);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < MMA_N / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
+            const int col0 = nt * MMA_N + c * 32;
+            if (row_ok && col0 < p.n_out) {
+                if constexpr (OUT == kOutF32) {
+                    float* crow = static_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
+                    if (col0 + 32 <= p.n_out) {
+                        uint4* d4 = reinterpret_cast<uint4*>(crow);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) d4[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < p.n_out) crow[j] = __uint_as_float(v[j]);
+                    }
+                } else {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    store_bf16x32(static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc + col0, pk, p.n_out - col0);
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, int OUT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                                                                    const __grid_constant__ CUtensorMap mapB,
                                                                    const Params p) {
+    using C = Cfg<PAIR>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = base;
     unsigned char* sB = base + STAGES * A_STAGE;
-    Smem& S = *reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+    Smem<STAGES>& S = *reinterpret_cast<Smem<STAGES>*>(base + STAGES * C::STAGE_BYTES);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = the CTA that issues the MMAs
+    const bool leader = rank == 0;
+    const int unit = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+    const int n_units = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -157,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&S.tmem_full[a], 1);
-            mbar_init(&S.tmem_empty[a], 4);
+            mbar_init(&S.tmem_empty[a], C::EPI_WARPS_TOTAL);
         }
         mbar_init(&S.mma_done, 1);
         S.abort_flag = 0;
@@ -167,8 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tma_prefetch_desc(&mapB);
     }
     if (warp == 1) {
-        tmem_alloc(&S.tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&S.tmem_base, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (warp == 2) {
         for (int e0 = 0; e0 <= E; e0 += 32) {
@@ -179,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         int run = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
             const int e = e0 + lane;
-            const int v = e < E ? (S.off[e + 1] - S.off[e] + BM - 1) / BM : 0;
+            const int v = e < E ? (S.off[e + 1] - S.off[e] + C::TILE_M - 1) / C::TILE_M : 0;
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -191,14 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
         if (lane == 0) S.tile[E] = run;
     }
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync_all(); else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = S.tmem_base;
     const int total = S.tile[E] * p.n_tiles;
     const int nkb = (p.K + BK - 1) / BK;
     volatile int* abort_flag = &S.abort_flag;
+    // Barriers the peer signals live in the even CTA.
+    const uint32_t full_base = PAIR ? mapa_shared(smem_addr(&S.full[0]), 0) : smem_addr(&S.full[0]);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -208,23 +308,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             // The dispatched rows of an expert are re-read by every N tile: keep them in L2.
             // Weight tiles are shared by the CTAs running the same N tile at the same time.
             const uint64_t pol_a = l2_policy_evict_last();
-            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            for (int t = unit; t < total; t += n_units) {
                 int e, mt, nt;
                 decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
-                const int m0 = S.off[e] + mt * BM;
+                const int m0 = S.off[e] + mt * C::TILE_M + int(rank) * 128;
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
                     const int k0 = kb * BK;
                     const int kB = (kb >> p.b_k_shift) * BK;
-                    tma_load_2d_hint(sA + s * A_STAGE, &mapA, &S.full[s], k0, m0, pol_a);
-                    if (MODE == kSwiGLU) {
-                        const int r0 = e * p.R + nt * (MMA_N / 2);
-                        tma_load_2d(sB + s * B_STAGE, &mapB, &S.full[s], kB, r0);
-                        tma_load_2d(sB + s * B_STAGE + B_STAGE / 2, &mapB, &S.full[s], kB, r0 + p.F);
+                    unsigned char* a_dst = sA + s * A_STAGE;
+                    unsigned char* b_dst = sB + s * C::B_STAGE;
+                    if constexpr (PAIR) {
+                        const uint32_t bar = full_base + uint32_t(s) * 8u;
+                        if (leader) mbar_arrive_expect_tx(&S.full[s], 2 * C::STAGE_BYTES);
+                        tma_load_2d_pair_hint(a_dst, &mapA, bar, k0, m0, pol_a);
+                        int r0;
+                        if (MODE == kSwiGLU) r0 = e * p.R + nt * (MMA_N / 2) + (rank ? p.F : 0);
+                        else r0 = e * p.R + nt * MMA_N + int(rank) * (MMA_N / 2);
+                        tma_load_2d_pair(b_dst, &mapB, bar, kB, r0);
                     } else {
-                        tma_load_2d(sB + s * B_STAGE, &mapB, &S.full[s], kB, e * p.R + nt * MMA_N);
+                        mbar_arrive_expect_tx(&S.full[s], C::STAGE_BYTES);
+                        tma_load_2d_hint(a_dst, &mapA, &S.full[s], k0, m0, pol_a);
+                        if (MODE == kSwiGLU) {
+                            const int r0 = e * p.R + nt * (MMA_N / 2);
+                            tma_load_2d(b_dst, &mapB, &S.full[s], kB, r0);
+                            tma_load_2d(b_dst + C::B_STAGE / 2, &mapB, &S.full[s], kB, r0 + p.F);
+                        } else {
+                            tma_load_2d(b_dst, &mapB, &S.full[s], kB, e * p.R + nt * MMA_N);
+                        }
                     }
                     armed_mask |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -232,16 +344,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 if (!ok) break;
             }
-            // Every armed stage must land before the CTA may exit.
-            for (int q = 0; q < STAGES; ++q)
-                if (armed_mask & (1u << q)) drain_wait(&S.full[q], (armed_par >> q) & 1u);
+            // Every armed stage must land before the CTA may exit. The even CTA's full
+            // barriers also count the odd CTA's bytes; the final cluster barrier keeps
+            // the odd CTA alive until this drain is done.
+            if (leader)
+                for (int q = 0; q < STAGES; ++q)
+                    if (armed_mask & (1u << q)) drain_wait(&S.full[q], (armed_par >> q) & 1u);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int s = 0;
             uint32_t ph = 0;
             int i = 0;
-            for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+            for (int t = unit; t < total; t += n_units, ++i) {
                 const int acc = i & 1;
                 const uint32_t aph = (i >> 1) & 1;
                 if (!mbar_wait(&S.tmem_empty[acc], aph ^ 1u, abort_flag, p.status)) break;
@@ -252,25 +367,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     if (!mbar_wait(&S.full[s], ph, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * A_STAGE));
-                    const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * B_STAGE));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * C::B_STAGE));
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks)
-                        umma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, IDESC, (kb | ks) != 0 ? 1u : 0u);
-                    umma_commit(&S.empty[s]);
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        if constexpr (PAIR)
+                            umma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, C::IDESC, (kb | ks) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, C::IDESC, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    if constexpr (PAIR) umma_commit_pair_multicast(&S.empty[s], 0x3);
+                    else umma_commit(&S.empty[s]);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(&S.tmem_full[acc]);
+                if constexpr (PAIR) umma_commit_pair_multicast(&S.tmem_full[acc], 0x3);
+                else umma_commit(&S.tmem_full[acc]);
             }
-            umma_commit(&S.mma_done);
+            if constexpr (PAIR) umma_commit_pair_multicast(&S.mma_done, 0x1);
+            else umma_commit(&S.mma_done);
             drain_wait(&S.mma_done, 0);
         }
     } else {
-        // Epilogue: warps 2..5 own TMEM lane quarters (warp % 4).
+        // Epilogue: warps 2..5 own TMEM lane quarters (warp % 4) = rows of this SM's half.
         const int q = warp & 3;
         const int r_in_tile = q * 32 + lane;
+        const uint32_t empty_base = PAIR ? mapa_shared(smem_addr(&S.tmem_empty[0]), 0) : 0u;
         int i = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+        for (int t = unit; t < total; t += n_units, ++i) {
             int e, mt, nt;
             decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
             const int acc = i & 1;
@@ -279,82 +402,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int row = S.off[e] + mt * BM + r_in_tile;
+            const int row = S.off[e] + mt * C::TILE_M + int(rank) * 128 + r_in_tile;
             const bool row_ok = row < S.off[e + 1];
             const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + acc * MMA_N;
-            if (MODE == kSwiGLU) {
-                uint16_t* crow = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t g[32], u[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, g);
-                    tmem_ld_32x32b_x32(tbase + MMA_N / 2 + c * 32, u);
-                    tmem_ld_wait();
-                    const int col0 = nt * (MMA_N / 2) + c * 32;
-                    if (row_ok && col0 < p.n_out) {
-                        float h[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) h[j] = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-                        store_hidden<OUT>(crow, col0, p.n_out, h);
-                    }
-                }
-            } else if (MODE == kReLU) {
-                uint16_t* crow = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
-#pragma unroll 1
-                for (int c = 0; c < MMA_N / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, v);
-                    tmem_ld_wait();
-                    const int col0 = nt * MMA_N + c * 32;
-                    if (row_ok && col0 < p.n_out) {
-                        float h[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) h[j] = fmaxf(__uint_as_float(v[j]), 0.f);
-                        store_hidden<OUT>(crow, col0, p.n_out, h);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < MMA_N / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, v);
-                    tmem_ld_wait();
-                    const int col0 = nt * MMA_N + c * 32;
-                    if (row_ok && col0 < p.n_out) {
-                        if constexpr (OUT == kOutF32) {
-                            float* crow = static_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
-                            if (col0 + 32 <= p.n_out) {
-                                uint4* d4 = reinterpret_cast<uint4*>(crow);
-#pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    d4[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    if (col0 + j < p.n_out) crow[j] = __uint_as_float(v[j]);
-                            }
-                        } else {
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                            store_bf16x32(static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc + col0, pk,
-                                          p.n_out - col0);
-                        }
-                    }
-                }
-            }
+            epilogue_tile<MODE, OUT>(p, tbase, row, row_ok, nt);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.tmem_empty[acc]);
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(empty_base + uint32_t(acc) * 8u);
+                else mbar_arrive(&S.tmem_empty[acc]);
+            }
         }
     }
 
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync_all(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -392,24 +459,75 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int MODE, int OUT>
-cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Params& p, int grid,
-                        cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<MODE, OUT>;
+template <int MODE, int OUT, bool PAIR>
+cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const Params& p, int grid,
+                          cudaStream_t stream) {
+    auto kern = grouped_gemm_kernel<MODE, OUT, PAIR>;
+    constexpr size_t smem = smem_bytes<PAIR>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mA, mB, p);
-    return cudaGetLastError();
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // The grid is persistent: never launch more pairs than can be resident at once.
+        static int max_clusters = -1;
+        if (max_clusters < 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = device_sm_count() / 2;
+            max_clusters = n;
+        }
+        if (int(cfg.gridDim.x) > 2 * max_clusters) cfg.gridDim.x = unsigned(2 * max_clusters);
+        return cudaLaunchKernelEx(&cfg, kern, mA, mB, p);
+    } else {
+        kern<<<grid, kThreads, smem, stream>>>(mA, mB, p);
+        return cudaGetLastError();
+    }
 }
 
-int grid_for(int64_t rows_max, int E, int n_tiles) {
-    const int64_t upper = ((rows_max + BM - 1) / BM + E) * int64_t(n_tiles);
-    const int sms = device_sm_count();
-    return int(upper < sms ? (upper > 0 ? upper : 1) : sms);
+// Whether a projection runs on SM pairs: MOE_GEMM_PAIR=0/1 forces it. Otherwise pairs
+// are used when experts average at least 1024 rows: a pair keeps the tensor pipe
+// about 88% busy against about 70% for one SM (each SM reads half the B tile from
+// shared memory), but an expert whose rows end inside a 256-row pair tile leaves up
+// to 128 rows of one SM idle, which costs up to ~12% at 512 rows per expert.
+bool use_pairs(int64_t rows_max, int E) {
+    static int forced = [] {
+        const char* v = getenv("MOE_GEMM_PAIR");
+        return v ? atoi(v) : -1;
+    }();
+    if (forced >= 0) return forced != 0;
+    return rows_max >= int64_t(E) * 1024;
+}
+
+int grid_for(int64_t rows_max, int E, int n_tiles, bool pair) {
+    const int tile_m = pair ? 256 : 128;
+    const int64_t upper = ((rows_max + tile_m - 1) / tile_m + E) * int64_t(n_tiles) * (pair ? 2 : 1);
+    int sms = device_sm_count();
+    if (pair) sms &= ~1;
+    int64_t g = upper < sms ? upper : sms;
+    if (pair) g = (g + 1) & ~int64_t(1);
+    return int(g > 0 ? g : (pair ? 2 : 1));
+}
+
+template <int MODE, int OUT>
+cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Params& p, int64_t rows_max, int E,
+                        bool pair, cudaStream_t stream) {
+    const int grid = grid_for(rows_max, E, p.n_tiles, pair);
+    return pair ? launch_kernel<MODE, OUT, true>(mA, mB, p, grid, stream)
+                : launch_kernel<MODE, OUT, false>(mA, mB, p, grid, stream);
 }
 
 }  // namespace
@@ -418,6 +536,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     const int64_t rows_max = int64_t(a.T) * a.k;
     const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
     const bool f32_out = a.precision != MOE_PRECISION_BF16;
+    const bool pair = use_pairs(rows_max, a.E);
+    const uint32_t b_rows = pair ? MMA_N / 2 : MMA_N;  // rows of one B box
     CUtensorMap mA, mB;
     cudaError_t err;
     Params p{};
@@ -429,8 +549,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     // Up projection: A = xperm [rows, d]; B = W13 [E*R, d]; C = h.
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;
     const int R = swiglu ? 2 * a.F : a.F;
-    if ((err = make_map(&mA, a.xperm, a.d, rows_max, BM)) != cudaSuccess) return err;
-    if ((err = make_map(&mB, a.W13, a.d, uint64_t(a.E) * R, swiglu ? MMA_N / 2 : MMA_N)) != cudaSuccess) return err;
+    if ((err = make_map(&mA, a.xperm, a.d, rows_max, 128)) != cudaSuccess) return err;
+    if ((err = make_map(&mB, a.W13, a.d, uint64_t(a.E) * R, swiglu ? MMA_N / 2 : b_rows)) != cudaSuccess) return err;
     p.C = a.h;
     p.ldc = split_h ? 2 * a.F : a.F;
     p.n_out = a.F;
@@ -438,20 +558,25 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.b_k_shift = 0;
     p.R = R;
     p.n_tiles = swiglu ? (a.F + MMA_N / 2 - 1) / (MMA_N / 2) : (a.F + MMA_N - 1) / MMA_N;
-    const int g_up = grid_for(rows_max, a.E, p.n_tiles);
     if (swiglu)
-        err = split_h ? launch_mode<kSwiGLU, kOutHiLo>(mA, mB, p, g_up, stream)
-                      : launch_mode<kSwiGLU, kOutBF16>(mA, mB, p, g_up, stream);
+        err = split_h ? launch_mode<kSwiGLU, kOutHiLo>(mA, mB, p, rows_max, a.E, pair, stream)
+                      : launch_mode<kSwiGLU, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
     else
-        err = split_h ? launch_mode<kReLU, kOutHiLo>(mA, mB, p, g_up, stream)
-                      : launch_mode<kReLU, kOutBF16>(mA, mB, p, g_up, stream);
+        err = split_h ? launch_mode<kReLU, kOutHiLo>(mA, mB, p, rows_max, a.E, pair, stream)
+                      : launch_mode<kReLU, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
     if (err != cudaSuccess) return err;
-    if (mid_event && (err = cudaEventRecord(mid_event, stream)) != cudaSuccess) return err;
+    if (mid_event) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((err = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return err;
+        err = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(mid_event, stream, cudaEventRecordExternal)
+                                                  : cudaEventRecord(mid_event, stream);
+        if (err != cudaSuccess) return err;
+    }
 
     // Down projection: A = h [rows, F] (split: [rows, 2F] hi|lo blocks); B = W2 [E*d, F].
     const int kA = split_h ? 2 * a.F : a.F;
-    if ((err = make_map(&mA, a.h, kA, rows_max, BM)) != cudaSuccess) return err;
-    if ((err = make_map(&mB, a.W2, a.F, uint64_t(a.E) * a.d, MMA_N)) != cudaSuccess) return err;
+    if ((err = make_map(&mA, a.h, kA, rows_max, 128)) != cudaSuccess) return err;
+    if ((err = make_map(&mB, a.W2, a.F, uint64_t(a.E) * a.d, b_rows)) != cudaSuccess) return err;
     p.C = a.out;
     p.ldc = a.d;
     p.n_out = a.d;
@@ -459,9 +584,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.b_k_shift = split_h ? 1 : 0;
     p.R = a.d;
     p.n_tiles = (a.d + MMA_N - 1) / MMA_N;
-    const int g_dn = grid_for(rows_max, a.E, p.n_tiles);
-    return f32_out ? launch_mode<kPlain, kOutF32>(mA, mB, p, g_dn, stream)
-                   : launch_mode<kPlain, kOutBF16>(mA, mB, p, g_dn, stream);
+    return f32_out ? launch_mode<kPlain, kOutF32>(mA, mB, p, rows_max, a.E, pair, stream)
+                   : launch_mode<kPlain, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
 }
 
 }  // namespace moe

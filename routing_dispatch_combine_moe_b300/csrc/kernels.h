@@ -18,11 +18,22 @@ inline int dispatch_blocks(int64_t assignments) {
     return int((assignments + kDispatchBlock - 1) / kDispatchBlock);
 }
 
+// Router. The logits are summed from up to route_max_slices(E) split-K partials
+// held in `scratch`, whose size depends only on T and E.
+int route_max_slices(int E);
+int route_k_slices(int T, int d, int E);
+inline size_t route_scratch_bytes_max(int T, int E) {
+    return size_t(route_max_slices(E)) * size_t(T) * size_t(E) * sizeof(float);
+}
+// topk_idx / topk_gate have k + n_shared slots per token; the shared slots hold
+// experts E..E+n_shared-1 with gate 1.
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
-                         int k, int32_t* topk_idx, float* topk_gate, cudaStream_t stream);
+                         int k, int n_shared, int32_t* topk_idx, float* topk_gate, float* scratch,
+                         cudaStream_t stream);
 
 struct DispatchArgs {
-    int T, d, E, k, D;
+    int T, d, E, k, D;  // E: all experts (routed + shared), k: all slots per token
+    int E_capped;       // experts [0, E_capped) are routed: held to the capacity, split over D ranks
     int64_t capacity;  // < 0: dropless
     int act_bytes;
     const void* x;

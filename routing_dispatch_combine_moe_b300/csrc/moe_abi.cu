@@ -39,6 +39,10 @@ int fail_cuda(cudaError_t e, const char* where) {
 
 inline int act_bytes(const moe_config* c) { return c->act_dtype == MOE_F32 ? 4 : 2; }
 
+// All experts (routed + shared) and all slots per token (routed + shared).
+inline int n_experts(const moe_config* c) { return c->E + c->n_shared; }
+inline int n_slots(const moe_config* c) { return c->k + c->n_shared; }
+
 inline bool bf16_experts(const moe_config* c) {
     return c->act_dtype == MOE_BF16 && c->expert_kind != MOE_EXPERT_IDENTITY;
 }
@@ -64,12 +68,12 @@ int validate(const moe_config* c) {
     if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_F32_OUT &&
         c->precision != MOE_PRECISION_SPLIT_H)
         return MOE_ERR_ARG;
-    if (c->reserved != 0) return MOE_ERR_ARG;
+    if (c->n_shared < 0) return MOE_ERR_ARG;
     if (c->k > c->E) return MOE_ERR_ARG;
     if (c->E % c->D != 0) return MOE_ERR_ARG;
     if (c->expert_kind != MOE_EXPERT_IDENTITY && c->F < 1) return MOE_ERR_ARG;
-    if (c->E > MOE_MAX_E || c->k > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
-    if (int64_t(c->T) * c->k > int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+    if (n_experts(c) > MOE_MAX_E || n_slots(c) > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
+    if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
     if (c->expert_kind != MOE_EXPERT_IDENTITY && (int64_t(c->F) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
     if (split_h(c) && c->F % 64 != 0) return MOE_ERR_UNSUPPORTED;
@@ -77,14 +81,15 @@ int validate(const moe_config* c) {
 }
 
 struct Layout {
-    size_t status, hist, drop_offsets, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
+    size_t status, hist, drop_offsets, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
         n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
     size_t dispatch_end, forward_end, host_end;
 };
 
 Layout layout(const moe_config* c) {
     Layout L{};
-    const int64_t A = int64_t(c->T) * c->k;
+    const int64_t A = int64_t(c->T) * n_slots(c);
+    const int N = n_experts(c);
     const int nblk = dispatch_blocks(A);
     const size_t b = size_t(act_bytes(c));
     size_t o = 0;
@@ -94,14 +99,15 @@ Layout layout(const moe_config* c) {
         return at;
     };
     L.status = take(sizeof(int32_t));
-    L.hist = take(sizeof(int32_t) * size_t(c->E) * nblk);
-    L.drop_offsets = take(sizeof(int32_t) * size_t(c->E));
+    L.hist = take(sizeof(int32_t) * size_t(N) * nblk);
+    L.drop_offsets = take(sizeof(int32_t) * size_t(N));
     L.dispatch_end = o;
+    L.route_partial = take(route_scratch_bytes_max(c->T, c->E));
     L.topk_idx = take(sizeof(int32_t) * A);
     L.topk_gate = take(sizeof(float) * A);
-    L.counts_routed = take(sizeof(int32_t) * size_t(c->E));
-    L.counts_kept = take(sizeof(int32_t) * size_t(c->E));
-    L.offsets = take(sizeof(int32_t) * size_t(c->E + 1));
+    L.counts_routed = take(sizeof(int32_t) * size_t(N));
+    L.counts_kept = take(sizeof(int32_t) * size_t(N));
+    L.offsets = take(sizeof(int32_t) * size_t(N + 1));
     L.rank_offsets = take(sizeof(int32_t) * size_t(c->D + 1));
     L.n_dropped = take(sizeof(int32_t));
     L.pos = take(sizeof(int32_t) * A);
@@ -146,8 +152,9 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
-              cudaStream_t s) {
-    const cudaError_t e = launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, idx, gate, s);
+              float* scratch, cudaStream_t s) {
+    const cudaError_t e =
+        launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, c->n_shared, idx, gate, scratch, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
 }
 
@@ -155,7 +162,8 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const m
                  void* ws, cudaStream_t s) {
     const Layout L = layout(c);
     DispatchArgs a{};
-    a.T = c->T; a.d = c->d; a.E = c->E; a.k = c->k; a.D = c->D;
+    a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.D = c->D;
+    a.E_capped = c->E;
     a.capacity = c->capacity;
     a.act_bytes = act_bytes(c);
     a.x = x;
@@ -179,7 +187,7 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const m
 int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const void* W13, const void* W2, void* h,
             void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
     FfnArgs a{};
-    a.T = c->T; a.d = c->d; a.E = c->E; a.k = c->k; a.F = c->F;
+    a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.F = c->F;
     a.expert_kind = c->expert_kind;
     a.act_dtype = c->act_dtype;
     a.precision = c->precision;
@@ -194,9 +202,16 @@ int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, cons
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_expert_ffn");
 }
 
+// Records events[i] on s. Under stream capture the record becomes an event node of
+// the graph (external record), so the timestamps exist when the graph is replayed.
 int record(void* const* events, int n, int i, cudaStream_t s) {
     if (!events || i >= n || !events[i]) return MOE_OK;
-    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+    e = cs == cudaStreamCaptureStatusActive
+            ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s, cudaEventRecordExternal)
+            : cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "cudaEventRecord");
 }
 
@@ -216,7 +231,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     cudaError_t e = cudaMemsetAsync(v.status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     if ((rc = record(events, n_events, 0, s)) != MOE_OK) return rc;
-    if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, s)) != MOE_OK) return rc;
+    if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s)) != MOE_OK)
+        return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
     if ((rc = run_dispatch(c, x, v.topk_idx, &v.map, v.xperm, ws, s)) != MOE_OK) return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
@@ -227,7 +243,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
         return rc;
     }
     if ((rc = record(events, n_events, 4, s)) != MOE_OK) return rc;
-    e = launch_combine(c->act_dtype, out_dtype(c), v.out, v.topk_gate, v.map.pos, y, c->T, c->d, c->k, v.status, s);
+    e = launch_combine(c->act_dtype, out_dtype(c), v.out, v.topk_gate, v.map.pos, y, c->T, c->d, n_slots(c),
+                       v.status, s);
     if (e != cudaSuccess) return fail_cuda(e, "moe_combine");
     return record(events, n_events, 5, s);
 }
@@ -279,14 +296,22 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     return 1 + 4 + (cfg->expert_kind == MOE_EXPERT_IDENTITY ? 0 : 2) + 1;
 }
 
+size_t moe_route_workspace_bytes(const moe_config* cfg) {
+    return validate(cfg) == MOE_OK ? route_scratch_bytes_max(cfg->T, cfg->E) : 0;
+}
+
 int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias, int32_t* topk_idx,
-              float* topk_gate, moe_stream_t stream) {
+              float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
     if (!x || !Wg || !topk_idx || !topk_gate) return MOE_ERR_ARG;
-    if (!aligned16(x) || !aligned4(Wg) || (bias && !aligned4(bias)) || !aligned4(topk_idx) || !aligned4(topk_gate))
+    const size_t need = route_scratch_bytes_max(cfg->T, cfg->E);
+    if (need && !ws) return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned4(Wg) || (bias && !aligned4(bias)) || !aligned4(topk_idx) || !aligned4(topk_gate) ||
+        (ws && !aligned16(ws)))
         return MOE_ERR_ALIGN;
-    return run_route(cfg, x, Wg, bias, topk_idx, topk_gate, stream);
+    if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+    return run_route(cfg, x, Wg, bias, topk_idx, topk_gate, static_cast<float*>(ws), stream);
 }
 
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const moe_dispatch_map* map,
@@ -327,7 +352,7 @@ int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, 
     if (!out || !topk_gate || !pos || !y) return MOE_ERR_ARG;
     if (!aligned16(out) || !aligned16(y) || !aligned4(topk_gate) || !aligned4(pos)) return MOE_ERR_ALIGN;
     const cudaError_t e = launch_combine(cfg->act_dtype, out_dtype(cfg), out, topk_gate, pos, y, cfg->T, cfg->d,
-                                         cfg->k, status, stream);
+                                         n_slots(cfg), status, stream);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_combine");
 }
 

@@ -2,55 +2,40 @@
 // softmax over the kept logits ("Mixture-of-Experts (MoE) Architecture and Expert
 // Parallelism", section 2 "The Gating Network Formulation").
 //
-// One CTA of 256 threads owns 32 tokens and every expert. The logits are a small
-// fp32 GEMM [32 x d] x [d x E_pad] done on the FMA units: chunks of d are staged
-// through shared memory (x transposed so one 16-byte load gives a thread its four
-// tokens), each thread accumulates 4 tokens x 8 experts over one K-slice, and the
-// K-slices are summed in a fixed order. A running sum is folded every 256 products
-// so the fp32 rounding error of a 7168-long dot product stays near 1e-7.
-// The 32 logit rows then go to the 8 warps (4 tokens each): every lane holds
-// E_pad/32 logits, and k rounds of a shuffle arg-max (ties to the lower expert id)
-// pick the slots in descending order; the kept softmax uses expf in fp32.
+// The logits are an fp32 GEMM [T x d] x [d x E] on the FMA units (exactly rounded
+// products and sums). A CTA of 8 warps stages chunks of 16 elements of x (transposed)
+// and of W_g through double-buffered shared memory; lanes own 4 tokens each, so W_g
+// values are warp-wide broadcasts, and warps own 8 experts each (warps along experts
+// = 1, 2, 4 or 8 for E <= 8, 16, 32 or more; the rest of the 8 warps run along
+// tokens). Each thread keeps a 4 x 8 register tile. d is split into KS slices,
+// chosen on the host so the CTA count fills the SMs evenly; each slice writes its
+// partial logits, and the top-k kernel (one warp per token) adds the KS partials in
+// slice order, adds the bias, and selects. Running sums are folded every 256
+// products to keep the fp32 error of a long dot product near 1e-7.
+//
+// KeepTopK: k rounds of a warp arg-max over the logits held in registers, equal
+// values won by the lower expert id; slot j is the (j+1)-th largest.
 #include "common.cuh"
 #include "kernels.h"
 
-#include <float.h>
+#include <mutex>
 
 namespace moe {
 namespace {
 
-constexpr int kTM = 32;       // tokens per CTA
-constexpr int kThreads = 256;
-constexpr int kRT = 4;        // tokens per thread
-constexpr int kRE = 8;        // experts per thread
-constexpr int kXStride = kTM + 4;  // padded row of the transposed x tile (floats)
-
-template <int EG>
-struct RouteShape {
-    static constexpr int KS = 32 / EG;                  // K-slices per CTA
-    static constexpr int EPASS = kRE * EG;              // padded expert count
-    static constexpr int KC = (8 * KS > 32) ? 8 * KS : 32;  // d-chunk staged per step
-    static constexpr int EPS = KC / KS;                 // elements per slice per chunk
-    static constexpr int FOLD = (256 / EPS) > 0 ? 256 / EPS : 1;  // chunks per partial sum
-    static constexpr int VPL = (EPASS + 31) / 32;       // logits per lane in the top-k
-    static constexpr size_t smem_x = size_t(KC) * kXStride * 4;
-    static constexpr size_t smem_w = size_t(KC) * EPASS * 4;
-    static constexpr size_t smem_red = size_t(KS) * kTM * EPASS * 4;
-    static constexpr size_t smem = smem_x + smem_w + smem_red;
-};
-
+// ------------------------------------------------------------------ shared pieces
 template <typename TAct>
-struct ActVec;
+struct Act16;
 template <>
-struct ActVec<float> {
-    static constexpr int N = 4;  // elements per 16-byte vector
+struct Act16<float> {
+    static constexpr int N = 4;
     __device__ static void to_f32(const uint4& v, float* o) {
         o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
         o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
     }
 };
 template <>
-struct ActVec<__nv_bfloat16> {
+struct Act16<__nv_bfloat16> {
     static constexpr int N = 8;
     __device__ static void to_f32(const uint4& v, float* o) {
         o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x); o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
@@ -58,199 +43,297 @@ struct ActVec<__nv_bfloat16> {
     }
 };
 
-template <typename TAct, int EG>
-__global__ void __launch_bounds__(kThreads) route_kernel(const TAct* __restrict__ x, const float* __restrict__ Wg,
-                                                         const float* __restrict__ bias, int T, int d, int E, int k,
-                                                         int32_t* __restrict__ topk_idx,
-                                                         float* __restrict__ topk_gate) {
-    using S = RouteShape<EG>;
-    constexpr int KS = S::KS, EPASS = S::EPASS, KC = S::KC, EPS = S::EPS;
-    constexpr int VN = ActVec<TAct>::N;
-    constexpr int XV = (kTM * KC / VN + kThreads - 1) / kThreads;     // x vectors per thread per chunk
-    constexpr int WN = (KC * EPASS + kThreads - 1) / kThreads;        // Wg floats per thread per chunk
+// Top-k of the logits held by a warp (lane l holds experts l + 32 m, m < VPL, with
+// -inf for padding), then the kept softmax; lane j < k writes slot j.
+template <int VPL>
+__device__ __forceinline__ void topk_softmax_store(float (&v)[VPL], int lane, int E, int k, int n_shared,
+                                                   int32_t* idx_out, float* gate_out) {
+    float my_val = -INFINITY;
+    int my_idx = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int m = 0; m < VPL; ++m) {
+            const int e = lane + 32 * m;
+            if (v[m] > bv || (v[m] == bv && e < bi)) { bv = v[m]; bi = e; }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (bi >= E) bi = 0;  // only reachable with NaN logits; keeps the index in range
+        if (lane == j) { my_val = bv; my_idx = bi; }
+#pragma unroll
+        for (int m = 0; m < VPL; ++m)
+            if (lane + 32 * m == bi) v[m] = -INFINITY;
+    }
+    const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+    const float ex = (lane < k) ? expf(my_val - vmax) : 0.f;
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+    if (lane < k) {
+        idx_out[lane] = my_idx;
+        gate_out[lane] = ex / sum;
+    } else if (lane < k + n_shared) {  // shared experts follow the routed slots, gate 1
+        idx_out[lane] = E + (lane - k);
+        gate_out[lane] = 1.0f;
+    }
+}
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    float* xs = reinterpret_cast<float*>(smem_raw);                          // [KC][kXStride]
-    float* wsm = reinterpret_cast<float*>(smem_raw + S::smem_x);             // [KC][EPASS]
-    float* red = reinterpret_cast<float*>(smem_raw + S::smem_x + S::smem_w); // [KS][kTM][EPASS]
+// ------------------------------------------------------------------ logits GEMM
+// CTA of 8 warps: WE warps along experts (8 experts each), 8/WE warps along tokens
+// (128 tokens each, 4 per lane).
+constexpr int kGK = 16;    // d elements per staged chunk
 
-    const int tid = threadIdx.x;
-    const int eg = tid % EG;
-    const int s = (tid / EG) % KS;
-    const int tg = tid / (EG * KS);
-    const int t0 = blockIdx.x * kTM;
-    const int nchunks = (d + KC - 1) / KC;
+template <int WE>
+struct GemmShape {
+    static constexpr int WT = 8 / WE;
+    static constexpr int TT = 128 * WT;   // tokens per CTA
+    static constexpr int TE = 8 * WE;     // experts per CTA
+    static constexpr int XS = TT + 4;     // padded transposed-x row (floats)
+    static constexpr size_t smem = size_t(2) * kGK * XS * 4 + size_t(2) * kGK * TE * 4;
+};
+
+template <typename TAct, int WE>
+__global__ void __launch_bounds__(256, WE == 1 ? 1 : 2) route_gemm_kernel(const TAct* __restrict__ x,
+                                                                         const float* __restrict__ Wg, int T, int d,
+                                                                         int E, int k_slice,
+                                                                         float* __restrict__ partial) {
+    using G = GemmShape<WE>;
+    constexpr int VN = Act16<TAct>::N;
+    constexpr int XV = G::TT * kGK / VN / 256;              // x vectors per thread per chunk
+    constexpr int WN = kGK * G::TE / 4;                      // W_g float4s per chunk
+    constexpr int WV = (WN + 255) / 256;
+    extern __shared__ __align__(16) float sm[];
+    float* xs = sm;                                          // [2][kGK][XS]
+    float* ws = sm + 2 * kGK * G::XS;                        // [2][kGK][TE]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wexp = warp % WE, wtok = warp / WE;
+    const int t0 = blockIdx.x * G::TT, e0 = blockIdx.y * G::TE;
+    const int kb = blockIdx.z * k_slice;
+    const int ke = min(d, kb + k_slice);
+    const int nchunks = ke > kb ? (ke - kb + kGK - 1) / kGK : 0;
+    const bool w_vec = (E % 4) == 0;
 
     uint4 xr[XV];
-    float wr[WN];
-
-    auto load_chunk = [&](int c) {
-        const int k0 = c * KC;
+    float4 wr[WV];
+    auto load = [&](int c) {
+        const int k0 = kb + c * kGK;
 #pragma unroll
-        for (int v = 0; v < XV; ++v) {
-            const int vi = tid + v * kThreads;          // vector index inside the chunk
-            const int tok = vi / (KC / VN), col = (vi % (KC / VN)) * VN;
+        for (int i = 0; i < XV; ++i) {
+            const int vi = tid + i * 256;
+            const int tok = vi / (kGK / VN), col = (vi % (kGK / VN)) * VN;
             uint4 val = make_uint4(0, 0, 0, 0);
-            if (vi < kTM * KC / VN && t0 + tok < T && k0 + col < d)
+            if (t0 + tok < T && k0 + col < ke)
                 val = __ldg(reinterpret_cast<const uint4*>(x + size_t(t0 + tok) * d + k0 + col));
-            xr[v] = val;
+            xr[i] = val;
         }
 #pragma unroll
-        for (int v = 0; v < WN; ++v) {
-            const int wi = tid + v * kThreads;
-            const int row = wi / EPASS, e = wi % EPASS;
-            float val = 0.f;
-            if (wi < KC * EPASS && k0 + row < d && e < E) val = __ldg(Wg + size_t(k0 + row) * E + e);
-            wr[v] = val;
-        }
-    };
-    auto store_chunk = [&]() {
-#pragma unroll
-        for (int v = 0; v < XV; ++v) {
-            const int vi = tid + v * kThreads;
-            if (vi < kTM * KC / VN) {
-                const int tok = vi / (KC / VN), col = (vi % (KC / VN)) * VN;
-                float f[VN];
-                ActVec<TAct>::to_f32(xr[v], f);
-#pragma unroll
-                for (int q = 0; q < VN; ++q) xs[(col + q) * kXStride + tok] = f[q];
+        for (int i = 0; i < WV; ++i) {
+            const int wi = tid + i * 256;
+            const int row = wi / (G::TE / 4), col = (wi % (G::TE / 4)) * 4;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (wi < WN && k0 + row < ke) {
+                const float* src = Wg + size_t(k0 + row) * E + e0 + col;
+                if (w_vec && e0 + col + 4 <= E) {
+                    val = __ldg(reinterpret_cast<const float4*>(src));
+                } else {
+                    if (e0 + col + 0 < E) val.x = __ldg(src + 0);
+                    if (e0 + col + 1 < E) val.y = __ldg(src + 1);
+                    if (e0 + col + 2 < E) val.z = __ldg(src + 2);
+                    if (e0 + col + 3 < E) val.w = __ldg(src + 3);
+                }
             }
+            wr[i] = val;
         }
+    };
+    auto store = [&](int buf) {
+        float* xb = xs + buf * kGK * G::XS;
 #pragma unroll
-        for (int v = 0; v < WN; ++v) {
-            const int wi = tid + v * kThreads;
-            if (wi < KC * EPASS) wsm[wi] = wr[v];
+        for (int i = 0; i < XV; ++i) {
+            const int vi = tid + i * 256;
+            const int tok = vi / (kGK / VN), col = (vi % (kGK / VN)) * VN;
+            float f[VN];
+            Act16<TAct>::to_f32(xr[i], f);
+#pragma unroll
+            for (int q = 0; q < VN; ++q) xb[(col + q) * G::XS + tok] = f[q];
+        }
+        float* wb = ws + buf * kGK * G::TE;
+#pragma unroll
+        for (int i = 0; i < WV; ++i) {
+            const int wi = tid + i * 256;
+            if (wi < WN) *reinterpret_cast<float4*>(wb + wi * 4) = wr[i];
         }
     };
 
-    float acc[kRT][kRE], tot[kRT][kRE];
+    float acc[4][8], tot[4][8];
 #pragma unroll
-    for (int r = 0; r < kRT; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int c = 0; c < kRE; ++c) acc[r][c] = tot[r][c] = 0.f;
+        for (int q = 0; q < 8; ++q) acc[r][q] = tot[r][q] = 0.f;
 
-    load_chunk(0);
-    store_chunk();
+    if (nchunks > 0) {
+        load(0);
+        store(0);
+    }
     __syncthreads();
+    const int xoff = wtok * 128 + lane * 4;
     for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks) load_chunk(c + 1);
+        const int buf = c & 1;
+        if (c + 1 < nchunks) load(c + 1);
+        const float* xb = xs + buf * kGK * G::XS;
+        const float* wb = ws + buf * kGK * G::TE;
 #pragma unroll
-        for (int m = 0; m < EPS; ++m) {
-            const int i = s + KS * m;
-            const float4 xv = *reinterpret_cast<const float4*>(xs + i * kXStride + tg * kRT);
-            const float4 w0 = *reinterpret_cast<const float4*>(wsm + i * EPASS + eg * kRE);
-            const float4 w1 = *reinterpret_cast<const float4*>(wsm + i * EPASS + eg * kRE + 4);
+        for (int i = 0; i < kGK; ++i) {
+            const float4 xv = *reinterpret_cast<const float4*>(xb + i * G::XS + xoff);
+            const float4 w0 = *reinterpret_cast<const float4*>(wb + i * G::TE + wexp * 8);
+            const float4 w1 = *reinterpret_cast<const float4*>(wb + i * G::TE + wexp * 8 + 4);
             const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
             const float wa[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int r = 0; r < kRT; ++r)
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int q = 0; q < kRE; ++q) acc[r][q] = fmaf(xa[r], wa[q], acc[r][q]);
+                for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(xa[r], wa[q], acc[r][q]);
         }
-        if ((c + 1) % S::FOLD == 0) {
+        if ((c + 1) % (256 / kGK) == 0) {
 #pragma unroll
-            for (int r = 0; r < kRT; ++r)
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int q = 0; q < kRE; ++q) { tot[r][q] += acc[r][q]; acc[r][q] = 0.f; }
+                for (int q = 0; q < 8; ++q) { tot[r][q] += acc[r][q]; acc[r][q] = 0.f; }
         }
+        if (c + 1 < nchunks) store(buf ^ 1);
         __syncthreads();
-        if (c + 1 < nchunks) {
-            store_chunk();
-            __syncthreads();
-        }
     }
+    // partial[z][t][e]
+    float* out = partial + size_t(blockIdx.z) * T * E;
 #pragma unroll
-    for (int r = 0; r < kRT; ++r)
+    for (int r = 0; r < 4; ++r) {
+        const int t = t0 + xoff + r;
+        if (t >= T) continue;
 #pragma unroll
-        for (int q = 0; q < kRE; ++q) tot[r][q] += acc[r][q];
-
-    // K-slice partials -> shared memory, then summed in slice order per logit.
-#pragma unroll
-    for (int r = 0; r < kRT; ++r)
-#pragma unroll
-        for (int q = 0; q < kRE; ++q) red[(s * kTM + tg * kRT + r) * EPASS + eg * kRE + q] = tot[r][q];
-    __syncthreads();
-
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int tl = warp * (kTM / 8); tl < (warp + 1) * (kTM / 8); ++tl) {
-        const int t = t0 + tl;
-        if (t >= T) break;
-        float v[S::VPL];
-        int ids[S::VPL];
-#pragma unroll
-        for (int m = 0; m < S::VPL; ++m) {
-            const int e = lane + 32 * m;
-            ids[m] = e;
-            float h = -INFINITY;
-            if (e < E) {
-                h = 0.f;
-#pragma unroll
-                for (int q = 0; q < KS; ++q) h += red[(q * kTM + tl) * EPASS + e];
-                if (bias) h += __ldg(bias + e);
-            }
-            v[m] = h;
-        }
-        float my_val = -INFINITY;
-        int my_idx = 0;
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int bi = 0x7FFFFFFF;
-#pragma unroll
-            for (int m = 0; m < S::VPL; ++m)
-                if (v[m] > bv || (v[m] == bv && ids[m] < bi)) { bv = v[m]; bi = ids[m]; }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-            }
-            if (bi >= E) bi = 0;  // only reachable with NaN logits; keeps the index in range
-            if (lane == j) { my_val = bv; my_idx = bi; }
-#pragma unroll
-            for (int m = 0; m < S::VPL; ++m)
-                if (ids[m] == bi) v[m] = -INFINITY;
-        }
-        const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
-        const float ex = (lane < k) ? expf(my_val - vmax) : 0.f;
-        float sum = 0.f;
-        for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
-        if (lane < k) {
-            topk_idx[size_t(t) * k + lane] = my_idx;
-            topk_gate[size_t(t) * k + lane] = ex / sum;
+        for (int q = 0; q < 8; ++q) {
+            const int e = e0 + wexp * 8 + q;
+            if (e < E) out[size_t(t) * E + e] = tot[r][q] + acc[r][q];
         }
     }
 }
 
-template <typename TAct, int EG>
-cudaError_t launch_route_eg(const void* x, const float* Wg, const float* bias, int T, int d, int E, int k,
-                            int32_t* idx, float* gate, cudaStream_t stream) {
-    using S = RouteShape<EG>;
-    auto kern = route_kernel<TAct, EG>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(S::smem));
-    if (err != cudaSuccess) return err;
-    const int grid = (T + kTM - 1) / kTM;
-    kern<<<grid, kThreads, S::smem, stream>>>(static_cast<const TAct*>(x), Wg, bias, T, d, E, k, idx, gate);
+template <int VPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ partial, int KS,
+                                                         const float* __restrict__ bias, int T, int E, int k,
+                                                         int n_shared, int32_t* __restrict__ topk_idx,
+                                                         float* __restrict__ topk_gate) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    float v[VPL];
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) {
+        const int e = lane + 32 * m;
+        float h = -INFINITY;
+        if (e < E) {
+            // Issue 8 independent loads at a time, then add them in slice order.
+            h = 0.f;
+            for (int z0 = 0; z0 < KS; z0 += 8) {
+                float pz[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    pz[u] = (z0 + u < KS) ? __ldg(partial + (size_t(z0 + u) * T + t) * E + e) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (z0 + u < KS) h += pz[u];
+            }
+            if (bias) h += __ldg(bias + e);
+        }
+        v[m] = h;
+    }
+    const int K = k + n_shared;
+    topk_softmax_store<VPL>(v, lane, E, k, n_shared, topk_idx + size_t(t) * K, topk_gate + size_t(t) * K);
+}
+
+int warps_along_experts(int E) { return E <= 8 ? 1 : E <= 16 ? 2 : E <= 32 ? 4 : 8; }
+
+template <typename TAct, int WE>
+cudaError_t launch_gemm(const void* x, const float* Wg, int T, int d, int E, int slice, int ks, float* scratch,
+                        cudaStream_t stream) {
+    using G = GemmShape<WE>;
+    auto kern = route_gemm_kernel<TAct, WE>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const dim3 grid((T + G::TT - 1) / G::TT, (E + G::TE - 1) / G::TE, ks);
+    kern<<<grid, 256, G::smem, stream>>>(static_cast<const TAct*>(x), Wg, T, d, E, slice, scratch);
     return cudaGetLastError();
 }
 
 template <typename TAct>
-cudaError_t launch_route_t(const void* x, const float* Wg, const float* bias, int T, int d, int E, int k,
-                           int32_t* idx, float* gate, cudaStream_t stream) {
-    const int groups = (E + kRE - 1) / kRE;
-    if (groups <= 1) return launch_route_eg<TAct, 1>(x, Wg, bias, T, d, E, k, idx, gate, stream);
-    if (groups <= 2) return launch_route_eg<TAct, 2>(x, Wg, bias, T, d, E, k, idx, gate, stream);
-    if (groups <= 4) return launch_route_eg<TAct, 4>(x, Wg, bias, T, d, E, k, idx, gate, stream);
-    if (groups <= 8) return launch_route_eg<TAct, 8>(x, Wg, bias, T, d, E, k, idx, gate, stream);
-    if (groups <= 16) return launch_route_eg<TAct, 16>(x, Wg, bias, T, d, E, k, idx, gate, stream);
-    return launch_route_eg<TAct, 32>(x, Wg, bias, T, d, E, k, idx, gate, stream);
+cudaError_t launch_gemm_t(const void* x, const float* Wg, int T, int d, int E, int slice, int ks, float* scratch,
+                          cudaStream_t stream) {
+    switch (warps_along_experts(E)) {
+        case 1: return launch_gemm<TAct, 1>(x, Wg, T, d, E, slice, ks, scratch, stream);
+        case 2: return launch_gemm<TAct, 2>(x, Wg, T, d, E, slice, ks, scratch, stream);
+        case 4: return launch_gemm<TAct, 4>(x, Wg, T, d, E, slice, ks, scratch, stream);
+        default: return launch_gemm<TAct, 8>(x, Wg, T, d, E, slice, ks, scratch, stream);
+    }
 }
+
+int slice_len(int d, int ks) { return ((d + ks - 1) / ks + kGK - 1) / kGK * kGK; }
 
 }  // namespace
 
+int route_max_slices(int E) {
+    const int m = 2048 / (E > 0 ? E : 1);
+    return m < 8 ? 8 : (m > 64 ? 64 : m);
+}
+
+int route_k_slices(int T, int d, int E) {
+    const int we = warps_along_experts(E);
+    const int tt = 128 * (8 / we), te = 8 * we;
+    const int64_t tiles = int64_t((T + tt - 1) / tt) * ((E + te - 1) / te);
+    const int sms = device_sm_count();
+    // Pick the slice count whose waves of CTAs finish soonest, charging the partial
+    // logits' HBM round trip against larger counts.
+    int best = 1;
+    double best_cost = 1e300;
+    for (int ks = 1; ks <= route_max_slices(E); ++ks) {
+        const int slice = slice_len(d, ks);
+        if (ks > 1 && (slice < 64 || int64_t(slice) * (ks - 1) >= d)) break;
+        const int64_t ctas = tiles * ks;
+        const double waves = double((ctas + sms - 1) / sms);
+        const double compute = waves * double(tt) * te * slice / 128.0 + waves * 2000.0;  // SM clocks
+        const double traffic = double(ks) * T * E * 8.0 / 3200.0;                        // ~3.2 KB per GPU clock
+        const double cost = compute + traffic;
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = ks;
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
-                         int k, int32_t* topk_idx, float* topk_gate, cudaStream_t stream) {
-    if (act_dtype == MOE_F32) return launch_route_t<float>(x, Wg, bias, T, d, E, k, topk_idx, topk_gate, stream);
-    return launch_route_t<__nv_bfloat16>(x, Wg, bias, T, d, E, k, topk_idx, topk_gate, stream);
+                         int k, int n_shared, int32_t* topk_idx, float* topk_gate, float* scratch,
+                         cudaStream_t stream) {
+    const int ks = route_k_slices(T, d, E);
+    const int slice = slice_len(d, ks);
+    cudaError_t e = act_dtype == MOE_F32 ? launch_gemm_t<float>(x, Wg, T, d, E, slice, ks, scratch, stream)
+                                         : launch_gemm_t<__nv_bfloat16>(x, Wg, T, d, E, slice, ks, scratch, stream);
+    if (e != cudaSuccess) return e;
+    const int g2 = (T + 7) / 8;
+    const int S = n_shared;
+    if (E <= 32) route_topk_kernel<1><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
+    else if (E <= 64) route_topk_kernel<2><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
+    else if (E <= 128) route_topk_kernel<4><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
+    else if (E <= 256) route_topk_kernel<8><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
+    else route_topk_kernel<16><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

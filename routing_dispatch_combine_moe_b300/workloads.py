@@ -53,6 +53,7 @@ class Workload:
     # bf16 experts: "bf16" (h and expert outputs in bf16), "f32_out" (expert outputs in
     # fp32) or "split_h" (h as a bf16 hi/lo pair too); see the library header.
     precision: str = "f32_out"
+    n_shared: int = 0  # shared experts (ids E .. E+n_shared-1) every token also uses, gate 1
     note: str = field(default="", compare=False)
 
     @property
@@ -62,6 +63,16 @@ class Workload:
     @property
     def act_bytes(self) -> int:
         return 4 if self.act == "f32" else 2
+
+    @property
+    def n_experts(self) -> int:
+        """Routed plus shared experts (the expert weights hold this many)."""
+        return self.E + self.n_shared
+
+    @property
+    def slots(self) -> int:
+        """Experts each token visits: k routed plus the shared ones."""
+        return self.k + self.n_shared
 
     @property
     def w13_rows(self) -> int:
@@ -85,11 +96,15 @@ WORKLOADS: dict[str, Workload] = {
                       "shrink rms(y), so h is carried as a bf16 hi/lo pair"),
         Workload("dsv3_full", T=4096, d=7168, E=256, k=8, F=2048, act="bf16",
                  expert="swiglu", note="DeepSeek-V3-shaped full layer, 22.5 GB of experts"),
+        Workload("dsv3_decode", T=128, d=7168, E=256, k=8, F=2048, act="bf16", expert="swiglu",
+                 n_shared=1, D=8,
+                 note="decode-shaped DeepSeek-V3 layer: 128 tokens, 8 routed experts plus the shared "
+                      "expert per token (9 vectors each), 8 virtual ranks"),
     ]
 }
 
 # Workload order as they are listed: small parity case first, headline second.
-WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full"]
+WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"]
 
 
 def scaled(w: Workload, **changes) -> Workload:
@@ -118,15 +133,15 @@ def make_router_inputs(w: Workload, seed: int):
 
 
 def make_expert_weights(w: Workload, seed: int, device="cpu"):
-    """W13 [E, R, d] and W2 [E, d, F] in the activation dtype, drawn expert by expert."""
+    """W13 [E+S, R, d] and W2 [E+S, d, F] (S shared experts last), drawn expert by expert."""
     if w.expert == "identity":
         return None, None
     dev = torch.device(device)
     g = torch.Generator(device=dev).manual_seed(seed * 1000003 + 1)
-    W13 = torch.empty(w.E, w.w13_rows, w.d, dtype=w.torch_act, device=dev)
-    W2 = torch.empty(w.E, w.d, w.F, dtype=w.torch_act, device=dev)
+    W13 = torch.empty(w.n_experts, w.w13_rows, w.d, dtype=w.torch_act, device=dev)
+    W2 = torch.empty(w.n_experts, w.d, w.F, dtype=w.torch_act, device=dev)
     s13, s2 = 1.0 / math.sqrt(w.d), 1.0 / math.sqrt(w.F)
-    for e in range(w.E):
+    for e in range(w.n_experts):
         W13[e] = torch.randn(w.w13_rows, w.d, generator=g, device=dev) * s13
         W2[e] = torch.randn(w.d, w.F, generator=g, device=dev) * s2
     return W13, W2

@@ -61,14 +61,15 @@ class StageBuffers:
     """Output buffers of the four stage entry points, filled with sentinels."""
 
     def __init__(self, w, cfg, device="cuda"):
-        A = w.T * w.k
+        A = w.T * w.slots
+        N = w.n_experts
         i32 = dict(dtype=torch.int32, device=device)
         self.cfg = cfg
-        self.topk_idx = torch.full((w.T, w.k), -7, **i32)
-        self.topk_gate = torch.full((w.T, w.k), float("nan"), dtype=torch.float32, device=device)
-        self.counts_routed = torch.full((w.E,), -7, **i32)
-        self.counts_kept = torch.full((w.E,), -7, **i32)
-        self.offsets = torch.full((w.E + 1,), -7, **i32)
+        self.topk_idx = torch.full((w.T, w.slots), -7, **i32)
+        self.topk_gate = torch.full((w.T, w.slots), float("nan"), dtype=torch.float32, device=device)
+        self.counts_routed = torch.full((N,), -7, **i32)
+        self.counts_kept = torch.full((N,), -7, **i32)
+        self.offsets = torch.full((N + 1,), -7, **i32)
         self.rank_offsets = torch.full((w.D + 1,), -7, **i32)
         self.pos = torch.full((A,), -7, **i32)
         self.row_src = torch.full((A,), -7, **i32)
@@ -79,6 +80,8 @@ class StageBuffers:
         self.out = torch.full((A, w.d), float("nan"), dtype=abi.out_dtype(cfg), device=device)
         self.out_act = "f32" if abi.out_dtype(cfg) == torch.float32 else "bf16"
         self.y = torch.full((w.T, w.d), float("nan"), dtype=w.torch_act, device=device)
+        nr = abi.moe_route_workspace_bytes(cfg)
+        self.ws_route = torch.zeros(nr, dtype=torch.uint8, device=device) if nr else None
         self.ws_dispatch = torch.zeros(abi.moe_dispatch_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.ws_ffn = torch.zeros(abi.moe_ffn_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -88,7 +91,7 @@ class StageBuffers:
                                 self.row_src, self.drop_list, self.n_dropped)
 
     def route(self, inp):
-        abi.moe_route(self.cfg, inp["x"], inp["Wg"], inp.get("bias"), self.topk_idx, self.topk_gate)
+        abi.moe_route(self.cfg, inp["x"], inp["Wg"], inp.get("bias"), self.topk_idx, self.topk_gate, self.ws_route)
 
     def dispatch(self, inp, topk_idx=None):
         abi.moe_dispatch(self.cfg, inp["x"], self.topk_idx if topk_idx is None else topk_idx, self.dmap(),
@@ -119,8 +122,12 @@ def check_route(w, inp, bufs, H=None) -> dict:
     G_o = orc.kept_softmax(H, idx_o)
     set_tie, order_tie = orc.near_tie_flags(H, w.k)
     tie = set_tie | order_tie
-    idx_g = cpu(bufs.topk_idx).numpy()
-    G_g = cpu(bufs.topk_gate).numpy().astype(np.float64)
+    idx_all = cpu(bufs.topk_idx).numpy()
+    G_all = cpu(bufs.topk_gate).numpy().astype(np.float64)
+    S = getattr(w, "n_shared", 0)
+    if S:  # shared slots follow the routed ones: experts E.., gate 1
+        assert np.all(idx_all[:, w.k:] == w.E + np.arange(S)) and np.all(G_all[:, w.k:] == 1.0)
+    idx_g, G_g = idx_all[:, :w.k], G_all[:, :w.k]
     mismatch = (idx_g != idx_o).any(axis=1)
     assert not (mismatch & ~tie).any(), \
         f"top-k differs on {int((mismatch & ~tie).sum())} tokens without a near tie, e.g. {np.nonzero(mismatch & ~tie)[0][:5]}"
@@ -134,7 +141,7 @@ def check_route(w, inp, bufs, H=None) -> dict:
 def check_dispatch(w, inp, bufs, capacity) -> dict:
     """Stage check on the GPU's own top-k: every routing-map array bit-exact, rows copied exactly."""
     idx_g = cpu(bufs.topk_idx).numpy().astype(np.int64)
-    d = orc.dispatch(idx_g, w.E, capacity, w.D)
+    d = orc.dispatch(idx_g, w.n_experts, capacity, w.D, capped_experts=w.E)
     np.testing.assert_array_equal(cpu(bufs.counts_routed).numpy(), d["counts_routed"])
     np.testing.assert_array_equal(cpu(bufs.counts_kept).numpy(), d["counts_kept"])
     np.testing.assert_array_equal(cpu(bufs.offsets).numpy(), d["offsets"])
@@ -146,7 +153,7 @@ def check_dispatch(w, inp, bufs, capacity) -> dict:
     assert int(cpu(bufs.n_dropped)[0]) == nd
     np.testing.assert_array_equal(cpu(bufs.drop_list).numpy()[:nd], d["drop_list"])
     # dispatched rows are exact copies of x[row_src // k]
-    src_tok = torch.from_numpy(d["row_src"] // w.k).to(bufs.xperm.device)
+    src_tok = torch.from_numpy(d["row_src"] // w.slots).to(bufs.xperm.device)
     assert torch.equal(bufs.xperm[:rows], inp["x"][src_tok]), "dispatched rows are not exact copies of x"
     return d
 
@@ -155,7 +162,7 @@ def check_ffn(w, inp, bufs, rows: int, expert_subset=None) -> float:
     """Expert outputs of the GPU's dispatched rows against the oracle's experts."""
     offs = cpu(bufs.offsets).numpy()
     fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
-    experts = range(w.E) if expert_subset is None else expert_subset
+    experts = range(w.n_experts) if expert_subset is None else expert_subset
     worst = 0.0
     for e in experts:
         lo, hi = int(offs[e]), int(offs[e + 1])
@@ -170,7 +177,7 @@ def check_ffn(w, inp, bufs, rows: int, expert_subset=None) -> float:
 
 def check_combine(w, bufs) -> float:
     """Combine stage on the GPU's own expert outputs, gates and positions."""
-    exact = orc.combine(f64(bufs.topk_gate), cpu(bufs.pos).numpy().astype(np.int64), f64(bufs.out), w.T, w.k)
+    exact = orc.combine(f64(bufs.topk_gate), cpu(bufs.pos).numpy().astype(np.int64), f64(bufs.out), w.T, w.slots)
     return check_close(bufs.y, exact, w.act, "combine", tol=1e-5)
 
 

@@ -49,7 +49,8 @@ def cfg(**kw):
     (dict(E=8, D=3), abi.MOE_ERR_ARG),
     (dict(F=0), abi.MOE_ERR_ARG),
     (dict(F=0, expert="identity"), abi.MOE_OK),
-    (dict(E=300, k=2), abi.MOE_ERR_UNSUPPORTED),
+    (dict(E=300, k=2), abi.MOE_OK),
+    (dict(E=600, k=2), abi.MOE_ERR_UNSUPPORTED),
     (dict(E=64, k=17), abi.MOE_ERR_UNSUPPORTED),
     (dict(d=100), abi.MOE_ERR_ALIGN),       # 200 bytes per bf16 row
     (dict(d=100, act="f32"), abi.MOE_OK),   # 400 bytes per fp32 row
@@ -65,13 +66,25 @@ def test_validate_config(kw, code):
     assert abi.moe_validate_config(cfg(**kw)) == code
 
 
-def test_validate_rejects_unknown_precision_and_reserved():
+def test_validate_rejects_unknown_precision_and_bad_shared_counts():
     c = cfg()
     c.precision = 7
     assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
-    c = cfg()
-    c.reserved = 1
-    assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
+    assert abi.moe_validate_config(cfg(n_shared=-1)) == abi.MOE_ERR_ARG
+    assert abi.moe_validate_config(cfg(n_shared=2)) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(E=256, k=8, n_shared=1)) == abi.MOE_OK       # 257 experts, 9 slots
+    assert abi.moe_validate_config(cfg(E=510, k=2, n_shared=3)) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(E=64, k=15, n_shared=2)) == abi.MOE_ERR_UNSUPPORTED
+
+
+def test_shared_experts_size_the_routing_arrays():
+    base, shared = cfg(E=8, k=2), cfg(E=8, k=2, n_shared=1)
+    vb, vs = abi.moe_workspace_view(), abi.moe_workspace_view()
+    lib, b0 = abi.lib(), 1 << 40
+    assert lib.moe_workspace_get_view(ctypes.byref(base), b0, abi.moe_workspace_bytes(base), ctypes.byref(vb)) == 0
+    assert lib.moe_workspace_get_view(ctypes.byref(shared), b0, abi.moe_workspace_bytes(shared), ctypes.byref(vs)) == 0
+    # xperm holds T*K rows: 64 * 3 with one shared slot against 64 * 2
+    assert (vs.out - vs.xperm) - (vb.out - vb.xperm) >= 64 * 128 * 2 - 256
 
 
 def test_split_h_workspace_holds_hi_lo_pairs_and_fp32_outputs():
@@ -125,9 +138,15 @@ def test_entry_points_reject_bad_arguments_on_the_host():
     bad = cfg(k=9)
     ref = ctypes.byref
     # route
-    assert lib.moe_route(ref(bad), A16, A16, None, A16, A16, None) == abi.MOE_ERR_ARG
-    assert lib.moe_route(ref(c), None, A16, None, A16, A16, None) == abi.MOE_ERR_ARG
-    assert lib.moe_route(ref(c), MIS, A16, None, A16, A16, None) == abi.MOE_ERR_ALIGN
+    nc = abi.moe_route_workspace_bytes(c)
+    assert lib.moe_route(ref(bad), A16, A16, None, A16, A16, A16, nc, None) == abi.MOE_ERR_ARG
+    assert lib.moe_route(ref(c), None, A16, None, A16, A16, A16, nc, None) == abi.MOE_ERR_ARG
+    assert lib.moe_route(ref(c), MIS, A16, None, A16, A16, A16, nc, None) == abi.MOE_ERR_ALIGN
+    big = cfg(E=64, k=2)  # the split-K partial logits live in the route workspace
+    nr = abi.moe_route_workspace_bytes(big)
+    assert nr >= 64 * 64 * 4 and abi.moe_route_workspace_bytes(c) >= 64 * 8 * 4
+    assert lib.moe_route(ref(big), A16, A16, None, A16, A16, None, 0, None) == abi.MOE_ERR_ARG
+    assert lib.moe_route(ref(big), A16, A16, None, A16, A16, A16, nr - 1, None) == abi.MOE_ERR_WORKSPACE
     # dispatch
     m = abi.moe_dispatch_map(*([A16] * 8))
     nbytes = abi.moe_dispatch_workspace_bytes(c)

@@ -1,0 +1,39 @@
+"""Both grouped-GEMM variants against the oracle: one SM per 128x256 tile
+(cta_group::1) and SM pairs sharing a 256x256 tile (cta_group::2). The library picks
+one per shape; MOE_GEMM_PAIR=0/1 forces it, read once per process, so each variant
+runs in a child process."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+from routing_dispatch_combine_moe_b300 import workloads as wl
+from tests.test_gpu_parity import stagewise, EDGE
+cases = [
+    wl.scaled(wl.WORKLOADS["mixtral_bf16"], T=700, d=1024, F=1536),
+    wl.scaled(wl.WORKLOADS["zipf_cf125"], T=2048, d=512, F=384),
+    wl.scaled(wl.WORKLOADS["dsv3_full"], T=512, d=1024, F=256),
+    wl.scaled(wl.WORKLOADS["mixtral_bf16"], T=900, d=512, F=640, precision="bf16"),
+] + [w for w in EDGE if w.act == "bf16" and w.expert != "identity"]
+for w in cases:
+    r = stagewise(w, seed=13)
+    print(w.name, "ffn_err/rms", r["ffn_err"], flush=True)
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_gemm_variant_parity(pair):
+    env = dict(os.environ, MOE_GEMM_PAIR=pair)
+    r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT)], env=env, capture_output=True, text=True,
+                       timeout=900)
+    print(r.stdout[-3000:])
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-3000:]

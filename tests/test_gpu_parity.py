@@ -26,6 +26,7 @@ REDUCED = {
     "dsv3_route_only": W["dsv3_route_only"],
     "zipf_cf125": wl.scaled(W["zipf_cf125"], T=2048, d=512, F=384),
     "dsv3_full": wl.scaled(W["dsv3_full"], T=512, d=1024, F=256),
+    "dsv3_decode": wl.scaled(W["dsv3_decode"], d=1024, F=256),
 }
 
 
@@ -58,7 +59,7 @@ def stagewise(w, seed=0, inp=None):
 
 
 def check_combine_on(w, b, out):
-    exact = orc.combine(f64(b.topk_gate), cpu(b.pos).numpy().astype(np.int64), f64(out), w.T, w.k)
+    exact = orc.combine(f64(b.topk_gate), cpu(b.pos).numpy().astype(np.int64), f64(out), w.T, w.slots)
     return check_close(b.y, exact, w.act, "combine", tol=1e-5)
 
 
@@ -113,7 +114,7 @@ def test_deterministic_bitwise():
 def _ws_equal_used(cfg, ws1, ws2):
     v1, v2 = abi.moe_workspace_get_view(cfg, ws1), abi.moe_workspace_get_view(cfg, ws2)
     base1, base2 = ws1.data_ptr(), ws2.data_ptr()
-    A = cfg.T * cfg.k
+    A = cfg.T * (cfg.k + cfg.n_shared)
     for name, nbytes in [("topk_idx", 4 * A), ("topk_gate", 4 * A), ("pos", 4 * A), ("offsets", 4 * (cfg.E + 1))]:
         o1 = getattr(v1, name) - base1
         o2 = getattr(v2, name) - base2
@@ -172,7 +173,7 @@ def test_bf16_mode_within_its_rounding_budget(name):
     s, o = orc.near_tie_flags(ref["H"], w.k)
     keep = ~(s | o)
     out_half_ulp = half_ulp(ref["out"], "bf16")
-    extra = orc.combine(ref["G"], ref["pos"], out_half_ulp, w.T, w.k)
+    extra = orc.combine(ref["G"], ref["pos"], out_half_ulp, w.T, w.slots)
     got, exact = f64(y)[keep], ref["y"][keep]
     err = np.abs(got - exact)
     bound = 2e-2 * rms(exact) + half_ulp(exact, "bf16") + extra[keep]
@@ -234,11 +235,11 @@ def test_traced_forward_matches_and_times():
 def _sampled_y(w, inp, ref_route, disp, tokens):
     """Oracle y for a few tokens from the full-batch routing and dispatch (drops included)."""
     x = f64(inp["x"][torch.as_tensor(tokens, device="cuda")])
-    idx, G, pos = ref_route["idx"], ref_route["G"], disp["pos"].reshape(w.T, w.k)
+    idx, G, pos = ref_route["idx"], ref_route["G"], disp["pos"].reshape(w.T, w.slots)
     fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
     need = {}
     for r, t in enumerate(tokens):
-        for j in range(w.k):
+        for j in range(w.slots):
             if pos[t, j] >= 0:
                 need.setdefault(int(idx[t, j]), []).append((r, j))
     y = np.zeros((len(tokens), w.d))
@@ -250,15 +251,14 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
     return y
 
 
-@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full"])
+@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"])
 def test_full_size_sampled(name):
     w = W[name]
     inp = wl.make_inputs(w, 0, device="cuda")
     cfg = abi.config_for(w)
     y, ws, view, flags = run_layer(cfg, inp, w)
     assert flags == 0
-    A = w.T * w.k
-
+    A = w.T * w.slots
     base = ws.data_ptr()
     ws_i32 = lambda ptr, n: ws[ptr - base:ptr - base + 4 * n].view(torch.int32).cpu().numpy()
     ws_f32 = lambda ptr, n: ws[ptr - base:ptr - base + 4 * n].view(torch.float32).cpu().numpy()
@@ -268,23 +268,25 @@ def test_full_size_sampled(name):
     G_o = orc.kept_softmax(H, idx_o)
     s, o = orc.near_tie_flags(H, w.k)
     tie = s | o
-    idx_g = ws_i32(view.topk_idx, A).reshape(w.T, w.k)
-    G_g = ws_f32(view.topk_gate, A).reshape(w.T, w.k)
+    idx_all = ws_i32(view.topk_idx, A).reshape(w.T, w.slots)
+    G_all = ws_f32(view.topk_gate, A).reshape(w.T, w.slots)
+    assert np.all(idx_all[:, w.k:] == w.E + np.arange(w.n_shared)) and np.all(G_all[:, w.k:] == 1.0)
+    idx_g, G_g = idx_all[:, :w.k], G_all[:, :w.k]
     mism = (idx_g != idx_o).any(axis=1)
     assert not (mism & ~tie).any()
     assert np.abs(G_g[~mism] - G_o[~mism]).max() <= 2e-6
     # dispatch on the GPU's own ids: bit-exact
     cap = capacity_of(cfg)
-    d = orc.dispatch(idx_g.astype(np.int64), w.E, cap, w.D)
-    np.testing.assert_array_equal(ws_i32(view.counts_routed, w.E), d["counts_routed"])
-    np.testing.assert_array_equal(ws_i32(view.offsets, w.E + 1), d["offsets"])
+    d = orc.dispatch(idx_all.astype(np.int64), w.n_experts, cap, w.D, capped_experts=w.E)
+    np.testing.assert_array_equal(ws_i32(view.counts_routed, w.n_experts), d["counts_routed"])
+    np.testing.assert_array_equal(ws_i32(view.offsets, w.n_experts + 1), d["offsets"])
     np.testing.assert_array_equal(ws_i32(view.rank_offsets, w.D + 1), d["rank_offsets"])
     np.testing.assert_array_equal(ws_i32(view.pos, A), d["pos"])
     rows = int(d["offsets"][-1])
     np.testing.assert_array_equal(ws_i32(view.row_src, A)[:rows], d["row_src"])
     assert int(ws_i32(view.n_dropped, 1)[0]) == d["n_dropped"]
     xperm = ws[view.xperm - base:view.xperm - base + rows * w.d * 2].view(torch.bfloat16).view(rows, w.d)
-    src = torch.from_numpy(d["row_src"] // w.k).cuda()
+    src = torch.from_numpy(d["row_src"] // w.slots).cuda()
     assert torch.equal(xperm, inp["x"][src])
     if w.expert == "identity":
         assert torch.equal(y, inp["x"])
@@ -309,7 +311,36 @@ def test_full_size_sampled(name):
     tokens = sorted(rng.choice(cand, size=min(8, cand.size), replace=False).tolist())
     # sampled tokens have no near tie, so their ids and gates equal the GPU's; the drop
     # decisions come from the (bit-exact) dispatch of the GPU's ids
-    y_s = _sampled_y(w, inp, dict(idx=idx_o, G=G_o), d, tokens)
+    idx_full = np.concatenate([idx_o, np.broadcast_to(w.E + np.arange(w.n_shared), (w.T, w.n_shared))], axis=1)
+    G_full = np.concatenate([G_o, np.ones((w.T, w.n_shared))], axis=1)
+    y_s = _sampled_y(w, inp, dict(idx=idx_full, G=G_full), d, tokens)
     err = check_close(y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y")
     print(f"\n{name}: near-ties={int(tie.sum())} ffn_err/rms={worst_ffn:.4f} sampled y err/rms={err:.4f} "
           f"dropped={d['n_dropped']}")
+
+
+@pytest.mark.parametrize("name", ["mixtral_bf16", "zipf_cf125", "tiny_f32"])
+def test_layer_forward_replays_in_a_cuda_graph(name):
+    """The whole forward enqueues without host syncs, so it captures into a CUDA
+    graph; replays on new inputs equal eager calls bit for bit."""
+    w = REDUCED[name]
+    cfg = abi.config_for(w)
+    inp = wl.make_inputs(w, 14, device="cuda")
+    ws = abi.workspace(cfg)
+    y = torch.empty(w.T, w.d, dtype=w.torch_act, device="cuda")
+    fwd = lambda: abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"),
+                                        y, ws)
+    fwd()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd()
+    for seed in (15, 16):
+        new = wl.make_inputs(w, seed, device="cuda")
+        inp["x"].copy_(new["x"])
+        g.replay()
+        torch.cuda.synchronize()
+        y_graph = y.clone()
+        fwd()
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph, y)

@@ -305,3 +305,38 @@ def test_zipf_workload_hot_expert_draws_forty_percent():
     idx = orc.keep_topk(orc.router_logits(f64(x), f64(Wg), f64(bias)), w.k)
     share = np.bincount(idx.ravel(), minlength=w.E).max() / idx.size
     assert abs(share - 0.40) <= 0.01
+
+
+# ----------------------------------------------------------------------- shared experts
+def test_shared_expert_alone_is_the_ffn():
+    """Routed experts' down projections zero: the layer reduces to the shared FFN (torch witness)."""
+    w = wl.Workload("t", T=23, d=32, E=4, k=2, F=48, act="f32", expert="swiglu", n_shared=1)
+    inp = wl.make_inputs(w, seed=21)
+    inp["W2"][: w.E] = 0
+    res = run_oracle(w, inp)
+    x = inp["x"].double()
+    W13, W2 = inp["W13"][w.E].double(), inp["W2"][w.E].double()
+    ref = Fn.linear(Fn.silu(Fn.linear(x, W13[: w.F])) * Fn.linear(x, W13[w.F:]), W2)
+    np.testing.assert_allclose(res["y"], ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert res["idx"].shape == (w.T, 3) and np.all(res["idx"][:, 2] == w.E) and np.all(res["G"][:, 2] == 1.0)
+
+
+def test_shared_expert_adds_to_the_routed_layer():
+    """y(shared) = y(routed only) + FFN_shared(x): with the shared expert's W2 zero they agree."""
+    w1 = wl.Workload("t", T=40, d=32, E=6, k=2, F=32, act="f32", expert="relu", n_shared=1)
+    w0 = wl.Workload("t", T=40, d=32, E=6, k=2, F=32, act="f32", expert="relu")
+    inp = wl.make_inputs(w1, seed=22)
+    inp["W2"][w1.E] = 0
+    a = run_oracle(w1, inp)["y"]
+    b = run_oracle(w0, dict(inp, W13=inp["W13"][: w0.E], W2=inp["W2"][: w0.E]))["y"]
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
+
+
+def test_shared_expert_is_never_dropped():
+    """Capacity limits routed experts only; the shared expert keeps all T tokens."""
+    idx = np.array([[0, 3], [0, 3], [1, 3], [0, 3]])  # expert 3 plays the shared expert
+    d = orc.dispatch(idx, 4, capacity=1, D=1, capped_experts=3)
+    assert d["counts_routed"].tolist() == [3, 1, 0, 4]
+    assert d["counts_kept"].tolist() == [1, 1, 0, 4]
+    assert d["drop_list"].tolist() == [2, 6]
+    assert d["rank_offsets"].tolist() == [0, 2]
