@@ -174,12 +174,12 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int) -> dict:
     ident = w.expert == "identity"
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
-        route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.k * 8,
+        route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.slots * 8,
         dispatch_bytes=sizing.dispatch_hbm_bytes(w.T, w.d, rows, b),
         combine_bytes=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
         up_flops=up, down_flops=down,
-        up_bytes=0 if ident else w.E * w.w13_rows * w.d * b + rows * w.d * b + rows * h_cols * b,
-        down_bytes=0 if ident else w.E * w.d * w.F * b + rows * h_cols * b + rows * w.d * out_bytes,
+        up_bytes=0 if ident else w.n_experts * w.w13_rows * w.d * b + rows * w.d * b + rows * h_cols * b,
+        down_bytes=0 if ident else w.n_experts * w.d * w.F * b + rows * h_cols * b + rows * w.d * out_bytes,
     )
 
 
@@ -201,11 +201,11 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
     fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, cache=cache)
     if w.expert != "identity":  # model load: the experts this sample uses, converted once
         idx = orc.keep_topk(orc.router_logits(x, Wg, bias), w.k)
-        for e in np.unique(idx):
+        for e in list(np.unique(idx)) + list(range(w.E, w.n_experts)):
             fn(int(e), np.zeros((1, w.d)))
     cap = orc.expert_capacity(len(sel), w.k, w.E, w.capacity_factor, w.min_capacity)
     t0 = time.perf_counter()
-    orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D)
+    orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D, n_shared=w.n_shared)
     dt = time.perf_counter() - t0
     threads = cpu_threads()
     return dict(value=len(sel) / dt, seconds=dt, tokens=len(sel), cores=threads)
@@ -332,12 +332,22 @@ def run_ours(args, w, world, rank, local):
     dc_ms = stage_ms["dispatch"] + stage_ms["combine"]
     gemm_ms = stage_ms["expert_up"] + stage_ms["expert_down"]
     gemm_flops = work["up_flops"] + work["down_flops"]
-    # dominant kernel of the step
+    # dominant kernel of the step; a GEMM is tensor-bound when its arithmetic
+    # intensity (algorithmic flops / algorithmic bytes) is above the measured ridge
+    # point (bf16 peak / HBM bandwidth), else HBM-bound on its weight stream
+    ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+    up_name = "grouped_gemm_kernel<%s> (up)" % ("SwiGLU" if w.expert == "swiglu" else "ReLU")
+
+    def gemm_entry(name, flops, nbytes):
+        if nbytes and flops / nbytes < ridge:
+            return (name, "hbm", nbytes)
+        return (name, "tensor", flops)
+
     kernel_work = {
-        "route": ("route_kernel", "alu", work["route_flops"]),
+        "route": ("route_gemm_kernel + route_topk_kernel", "alu", work["route_flops"]),
         "dispatch": ("dispatch (count+scan+scatter+gather)", "hbm", work["dispatch_bytes"]),
-        "expert_up": ("grouped_gemm_kernel<SwiGLU> (up)", "tensor", work["up_flops"]),
-        "expert_down": ("grouped_gemm_kernel<Plain> (down)", "tensor", work["down_flops"]),
+        "expert_up": gemm_entry(up_name, work["up_flops"], work["up_bytes"]),
+        "expert_down": gemm_entry("grouped_gemm_kernel<Plain> (down)", work["down_flops"], work["down_bytes"]),
         "combine": ("combine_kernel", "hbm", work["combine_bytes"]),
     }
     dom = max(STAGES, key=lambda s: stage_ms[s])
@@ -357,6 +367,8 @@ def run_ours(args, w, world, rank, local):
                 "peak_source": "148 SMs x 128 FP32 lanes x 2 flop x max SM clock"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = kname
+    roof["algorithmic"] = amount
+    roof["ridge_flop_per_byte"] = ridge
     roof["traffic"] = load_traffic(w.name, dom)
     roof["ms_per_launch"] = stage_ms[dom]
 
@@ -365,11 +377,12 @@ def run_ours(args, w, world, rank, local):
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.act, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "F": w.F, "expert": w.expert,
+                   "n_shared": w.n_shared,
                    "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
                    "precision": w.precision,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
-                         "dispatched rows" % (w.E * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
+                         "dispatched rows" % (w.n_experts * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
                                               if w.expert != "identity" else 0.0,
                                               rows * w.d * w.act_bytes / 1e6)},
         "roofline": roof,
@@ -382,7 +395,7 @@ def run_ours(args, w, world, rank, local):
         "routing": {"rows": rows, "dropped": n_dropped, "hist": sizing.histogram_summary(counts),
                     "rank_imbalance": sizing.imbalance_ratio(np.diff(rank_offs)),
                     "remote_dispatch_bytes": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),
-                    "pages_dispatch_bytes": sizing.dispatch_bytes_per_direction(w.T, w.k, w.d, w.act_bytes,
+                    "pages_dispatch_bytes": sizing.dispatch_bytes_per_direction(w.T, w.slots, w.d, w.act_bytes,
                                                                                 w.D if w.D > 1 else None)},
         "device_status": flags,
         "clocks": clocks.summary(),

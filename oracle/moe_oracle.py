@@ -51,6 +51,12 @@ Readings where the pages are silent (each is listed in the design notes too):
 * shared experts are experts E .. E+n_shared-1: every token is also dispatched to
   each of them with gate 1, after its k routed slots; capacity limits only the
   routed experts.
+* drop by gate [SIZ "Capacity semantics decide what crosses the wire": overflow
+  dropped by selected probability]: an overflowing expert keeps the C assignments
+  with the largest gates, equal gates going to the lower token index; its kept rows
+  stay in token order;
+* padded layout [CAP: every expert's buffer holds C token slots, under-full experts
+  padded]: expert e's kept rows start at row e*C, the rest of its C rows are zero.
 
 Every arithmetic step runs in float64 on exact float64 copies of the inputs (bf16
 and fp32 values are exact in float64). ``round_to_bf16`` is only for the optional
@@ -170,7 +176,8 @@ def expert_capacity(T: int, k: int, E: int, capacity_factor, min_capacity: int =
     return max(C, int(min_capacity))
 
 
-def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None) -> dict:
+def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None, gates=None,
+             drop_policy: str = "token", layout: str = "packed") -> dict:
     """Group the T*k assignments by expert, dropping overflow.  [A2A], [CAP], [DROP]
 
     Assignment a = t*k + j is token t's j-th slot. For each expert in ascending id
@@ -182,12 +189,22 @@ def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None) -> dic
     rank_offsets[r]. Only experts with id < ``capped_experts`` (default: all E) are
     held to the capacity; the ranks then split those experts, and later experts
     (shared ones) follow after rank_offsets[D].
+
+    ``drop_policy`` "gate" keeps, per overflowing expert, the ``capacity``
+    assignments with the largest ``gates`` (equal gates: lower token first) instead
+    of the first ones by token; kept rows stay in token order. ``layout`` "padded"
+    gives every expert a fixed segment of ``capacity`` rows starting at e*C (offsets
+    are e*C); rows past an expert's kept count are padding.
     """
     idx = np.asarray(idx)
     T, k = idx.shape
     capped = E if capped_experts is None else capped_experts
     if capped % D != 0:
         raise ValueError("the routed experts must divide into D ranks")
+    if layout == "padded" and (capacity is None or capped != E):
+        raise ValueError("the padded layout needs a capacity and no uncapped experts")
+    if drop_policy == "gate":
+        gates = np.asarray(gates, np.float64).reshape(T, k)
     counts_routed = np.zeros(E, np.int64)
     counts_kept = np.zeros(E, np.int64)
     kept_ids, dropped_ids = [], []
@@ -195,15 +212,31 @@ def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None) -> dic
         tok, slot = np.nonzero(idx == e)  # row-major scan: ascending token index
         a = tok * k + slot
         counts_routed[e] = a.size
-        keep = a if (capacity is None or e >= capped) else a[:capacity]
+        if capacity is None or e >= capped or a.size <= capacity:
+            keep, drop = a, a[:0]
+        elif drop_policy == "token":
+            keep, drop = a[:capacity], a[capacity:]
+        else:
+            by_gate = np.lexsort((tok, -gates[tok, slot]))  # primary: gate desc; then token asc
+            chosen = np.zeros(a.size, bool)
+            chosen[by_gate[:capacity]] = True
+            keep, drop = a[chosen], a[~chosen]  # both still in token order
         counts_kept[e] = keep.size
         kept_ids.append(keep)
-        dropped_ids.append(a[keep.size:])
-    row_src = np.concatenate(kept_ids).astype(np.int64)
+        dropped_ids.append(drop)
     drop_list = np.concatenate(dropped_ids).astype(np.int64)
-    offsets = np.concatenate([[0], np.cumsum(counts_kept)]).astype(np.int64)
     pos = np.full(T * k, -1, np.int64)
-    pos[row_src] = np.arange(row_src.size)
+    if layout == "padded":
+        offsets = np.arange(E + 1, dtype=np.int64) * capacity
+        row_src = np.full(E * capacity, -1, np.int64)
+        for e in range(E):
+            row_src[offsets[e]:offsets[e] + kept_ids[e].size] = kept_ids[e]
+        valid = row_src >= 0
+        pos[row_src[valid]] = np.nonzero(valid)[0]
+    else:
+        row_src = np.concatenate(kept_ids).astype(np.int64)
+        offsets = np.concatenate([[0], np.cumsum(counts_kept)]).astype(np.int64)
+        pos[row_src] = np.arange(row_src.size)
     rank_offsets = offsets[np.arange(D + 1) * (capped // D)]
     return dict(
         counts_routed=counts_routed,
@@ -215,6 +248,7 @@ def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None) -> dic
         n_dropped=int(drop_list.size),
         rank_offsets=rank_offsets,
         capacity=capacity,
+        layout=layout,
     )
 
 
@@ -261,7 +295,8 @@ def combine(G, pos, out, T: int, k: int) -> np.ndarray:
     return y
 
 
-def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, n_shared: int = 0) -> dict:
+def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, n_shared: int = 0,
+                drop_policy: str = "token", layout: str = "packed") -> dict:
     """The whole layer: logits, KeepTopK, kept softmax, dispatch, experts, combine.
 
     ``expert_fn(e, X)`` returns Expert_e applied to the rows X (an [M, d] float64
@@ -280,8 +315,11 @@ def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, 
         idx = np.concatenate([idx, np.broadcast_to(E + np.arange(n_shared), (T, n_shared))], axis=1)
         G = np.concatenate([G, np.ones((T, n_shared))], axis=1)
         k = k + n_shared
-    disp = dispatch(idx, E + n_shared, capacity, D, capped_experts=E)
-    xperm = x[disp["row_src"] // k]
+    disp = dispatch(idx, E + n_shared, capacity, D, capped_experts=E, gates=G, drop_policy=drop_policy,
+                    layout=layout)
+    rs = disp["row_src"]
+    xperm = np.zeros((rs.size, d))
+    xperm[rs >= 0] = x[rs[rs >= 0] // k]  # padding rows (row_src -1) stay zero
     out = np.zeros_like(xperm)
     off = disp["offsets"]
     for e in range(E + n_shared):

@@ -58,4 +58,5 @@ def run_oracle(w, inp: dict, capacity="auto", faithful: bool = False, cache=None
         capacity = orc.expert_capacity(w.T, w.k, w.E, w.capacity_factor, w.min_capacity)
     fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, faithful=faithful, cache=cache)
     return orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), w.k, fn, capacity=capacity,
-                           bias=f64(inp.get("bias")), D=w.D, n_shared=getattr(w, "n_shared", 0))
+                           bias=f64(inp.get("bias")), D=w.D, n_shared=getattr(w, "n_shared", 0),
+                           drop_policy=getattr(w, "drop_policy", "token"), layout=getattr(w, "layout", "packed"))

@@ -54,6 +54,8 @@ class Workload:
     # fp32) or "split_h" (h as a bf16 hi/lo pair too); see the library header.
     precision: str = "f32_out"
     n_shared: int = 0  # shared experts (ids E .. E+n_shared-1) every token also uses, gate 1
+    drop_policy: str = "token"  # overflow dropped in token order, or "gate": lowest gates first
+    layout: str = "packed"      # "packed" rows, or "padded": a fixed segment of C rows per expert
     note: str = field(default="", compare=False)
 
     @property

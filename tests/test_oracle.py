@@ -340,3 +340,70 @@ def test_shared_expert_is_never_dropped():
     assert d["counts_kept"].tolist() == [1, 1, 0, 4]
     assert d["drop_list"].tolist() == [2, 6]
     assert d["rank_offsets"].tolist() == [0, 2]
+
+
+# ----------------------------------------------------------------------- drop order / padded layout
+def test_gate_ordered_drop_keeps_the_largest_gates():
+    """Expert 0 receives tokens 0..3 with gates .3 .9 .5 .7 and C = 2: tokens 1 and 3 stay, in token order."""
+    idx = np.array([[0, 1], [0, 2], [0, 1], [0, 2]])
+    gates = np.array([[0.3, 0.7], [0.9, 0.1], [0.5, 0.5], [0.7, 0.3]])
+    d = orc.dispatch(idx, 3, capacity=2, gates=gates, drop_policy="gate")
+    assert d["row_src"].tolist()[:2] == [2, 6]          # assignments t*k+j of tokens 1 and 3
+    assert d["drop_list"].tolist() == [0, 4]             # tokens 0 and 2, expert order then token order
+    assert d["counts_kept"].tolist() == [2, 2, 2]
+    t = orc.dispatch(idx, 3, capacity=2)                 # token order keeps tokens 0 and 1
+    assert t["row_src"].tolist()[:2] == [0, 2]
+
+
+def test_gate_ordered_drop_ties_go_to_the_lower_token():
+    idx = np.zeros((5, 1), np.int64)
+    gates = np.array([[0.5], [0.8], [0.5], [0.8], [0.5]])
+    d = orc.dispatch(idx, 1, capacity=3, gates=gates, drop_policy="gate")
+    assert d["row_src"].tolist() == [0, 1, 3]            # both 0.8s, then the first 0.5
+    assert d["drop_list"].tolist() == [2, 4]
+
+
+def _brute_gate_dispatch(idx, gates, E, C):
+    T, k = idx.shape
+    kept, drops = [], []
+    for e in range(E):
+        mine = [(-gates[t, j], t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        chosen = set((t, j) for _, t, j in sorted(mine)[:C])
+        kept += [t * k + j for _, t, j in sorted(mine, key=lambda m: m[1]) if (t, j) in chosen]
+        drops += [t * k + j for _, t, j in sorted(mine, key=lambda m: m[1]) if (t, j) not in chosen]
+    return kept, drops
+
+
+@pytest.mark.parametrize("C", [0, 1, 2, 5, 50])
+def test_gate_ordered_drop_matches_brute_force(C):
+    r = rng(31)
+    T, E, k = 41, 5, 2
+    idx = np.stack([r.permutation(E)[:k] for _ in range(T)])
+    gates = np.round(r.random((T, k)), 2)  # rounded so that some gates tie
+    d = orc.dispatch(idx, E, C, gates=gates, drop_policy="gate")
+    kept, drops = _brute_gate_dispatch(idx, gates, E, C)
+    assert d["row_src"].tolist() == kept and d["drop_list"].tolist() == drops
+
+
+def test_padded_layout_rows_and_layout_invariance():
+    w = wl.Workload("t", T=60, d=16, E=4, k=2, F=24, act="f32", expert="swiglu", capacity_factor="1")
+    inp = wl.make_inputs(w, seed=32)
+    packed = run_oracle(w, inp)
+    padded = run_oracle(wl.scaled(w, layout="padded"), inp)
+    C = orc.expert_capacity(w.T, w.k, w.E, "1")
+    assert padded["offsets"].tolist() == [e * C for e in range(w.E + 1)]
+    for e in range(w.E):
+        n = packed["counts_kept"][e]
+        lo = packed["offsets"][e]
+        np.testing.assert_array_equal(padded["row_src"][e * C:e * C + n], packed["row_src"][lo:lo + n])
+        assert np.all(padded["row_src"][e * C + n:(e + 1) * C] == -1)
+        assert np.all(padded["xperm"][e * C + n:(e + 1) * C] == 0)
+    np.testing.assert_array_equal(padded["y"], packed["y"])
+
+
+def test_gate_policy_equals_token_policy_without_overflow():
+    w = wl.Workload("t", T=30, d=16, E=4, k=2, F=24, act="f32", expert="relu", capacity_factor="4")
+    inp = wl.make_inputs(w, seed=33)
+    a = run_oracle(w, inp)
+    b = run_oracle(wl.scaled(w, drop_policy="gate"), inp)
+    assert a["n_dropped"] == 0 and np.array_equal(a["row_src"], b["row_src"])
