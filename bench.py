@@ -255,11 +255,14 @@ def run_ours(args, w, world, rank, local):
     if flags:
         raise RuntimeError(f"device status flags {flags:#x} after warm-up")
     base = ws.data_ptr()
-    offs = ws[view.offsets - base:view.offsets - base + 4 * (w.E + 1)].view(torch.int32).cpu().numpy()
+    N = w.n_experts
+    offs = ws[view.offsets - base:view.offsets - base + 4 * (N + 1)].view(torch.int32).cpu().numpy()
     rank_offs = ws[view.rank_offsets - base:view.rank_offsets - base + 4 * (w.D + 1)].view(torch.int32).cpu().numpy()
     counts = ws[view.counts_routed - base:view.counts_routed - base + 4 * w.E].view(torch.int32).cpu().numpy()
+    kept = ws[view.counts_kept - base:view.counts_kept - base + 4 * N].view(torch.int32).cpu().numpy()
     n_dropped = int(ws[view.n_dropped - base:view.n_dropped - base + 4].view(torch.int32).cpu()[0])
-    rows = int(offs[-1])
+    rows = int(kept.sum())          # rows holding an assignment: the algorithmic work
+    rows_computed = int(offs[-1])   # rows the expert GEMMs run over (padding included)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     for ev in events:  # materialise the event handles before timing
@@ -379,7 +382,7 @@ def run_ours(args, w, world, rank, local):
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "F": w.F, "expert": w.expert,
                    "n_shared": w.n_shared,
                    "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
-                   "precision": w.precision,
+                   "precision": w.precision, "drop_policy": w.drop_policy, "layout": w.layout,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
                          "dispatched rows" % (w.n_experts * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
@@ -392,7 +395,7 @@ def run_ours(args, w, world, rank, local):
         "grouped_gemm_frac_bf16_peak": (gemm_flops / (gemm_ms / 1e3) / 1e12) / float(peaks["bf16_tflops"])
         if gemm_ms > 0 and gemm_flops else None,
         "stage_ms": stage_ms,
-        "routing": {"rows": rows, "dropped": n_dropped, "hist": sizing.histogram_summary(counts),
+        "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "hist": sizing.histogram_summary(counts),
                     "rank_imbalance": sizing.imbalance_ratio(np.diff(rank_offs)),
                     "remote_dispatch_bytes": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),
                     "pages_dispatch_bytes": sizing.dispatch_bytes_per_direction(w.T, w.slots, w.d, w.act_bytes,
@@ -448,11 +451,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--drop-policy", choices=["token", "gate"], default=None,
+                    help="override the workload's drop policy (capacity workloads)")
+    ap.add_argument("--layout", choices=["packed", "padded"], default=None,
+                    help="override the workload's row layout (padded needs a capacity)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
     w = wl.WORKLOADS[args.workload]
+    changes = {k: v for k, v in (("drop_policy", args.drop_policy), ("layout", args.layout)) if v is not None}
+    if changes:
+        w = wl.scaled(w, **changes)
     if args.impl == "reference":
         line = run_reference(args, w, world, rank)
     else:

@@ -85,6 +85,19 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
                                    through the down projection against the same weights; expert outputs in
                                    fp32: y then carries essentially only its own final rounding */
 
+/* What an expert past its capacity drops (capacity >= 0 only). */
+#define MOE_DROP_TOKEN_ORDER 0 /* keep the first `capacity` assignments by token index */
+#define MOE_DROP_LOW_GATE 1    /* keep the `capacity` assignments with the largest gates, equal gates
+                                  to the lower token ("MoE Expert Parallelism Sizing", "Capacity
+                                  semantics decide what crosses the wire": drops by selected probability) */
+
+/* Row layout of the dispatched rows. */
+#define MOE_LAYOUT_PACKED 0 /* kept rows back to back: expert e's rows are [offsets[e], offsets[e+1]) */
+#define MOE_LAYOUT_PADDED 1 /* a fixed segment of `capacity` rows per expert, [e*C, (e+1)*C), the kept rows
+                               first and zero rows after ("EP Math", "Capacity factor": a dense
+                               [E, C, d] buffer with under-full experts padded); needs capacity >= 0
+                               and n_shared == 0. offsets[e] = e*C, so the experts run on all C rows. */
+
 /* Limits of this build. */
 #define MOE_MAX_K 16        /* experts per token, routed plus shared */
 #define MOE_MAX_E 512       /* experts, routed plus shared */
@@ -101,6 +114,8 @@ typedef struct moe_config {
     int32_t precision;   /* MOE_PRECISION_*; SPLIT_H needs F % 64 == 0 */
     int32_t n_shared;    /* shared experts S >= 0: experts E..E+S-1, used by every token with gate 1 */
     int64_t capacity;    /* tokens each expert keeps; < 0 = dropless (see moe_capacity) */
+    int32_t drop_policy; /* MOE_DROP_* */
+    int32_t layout;      /* MOE_LAYOUT_* */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
@@ -110,7 +125,8 @@ typedef struct moe_dispatch_map {
     int32_t* offsets;       /* [N+1] exclusive scan of counts_kept; rows of expert e are [offsets[e], offsets[e+1]) */
     int32_t* rank_offsets;  /* [D+1] offsets[r*E/D]: virtual rank r's send chunk is [rank_offsets[r], rank_offsets[r+1]) */
     int32_t* pos;           /* [T*K] row of assignment t*K+j, or -1 if it was dropped */
-    int32_t* row_src;       /* [T*K] assignment t*K+j held by each row; entries [0, offsets[N]) are written */
+    int32_t* row_src;       /* [rows] assignment t*K+j held by each row (-1 on padding rows); entries
+                               [0, offsets[N]) are written; rows = moe_rows_capacity(cfg) */
     int32_t* drop_list;     /* [T*K] dropped assignments, ordered by (expert, token); [0, n_dropped) written */
     int32_t* n_dropped;     /* [1]   number of dropped assignments */
 } moe_dispatch_map;
@@ -121,7 +137,7 @@ typedef struct moe_workspace_view {
     int32_t* topk_idx;   /* [T*K] */
     float* topk_gate;    /* [T*K] */
     moe_dispatch_map map;
-    void* xperm;         /* [T*K, d] act: dispatched rows (the dispatch "send buffer") */
+    void* xperm;         /* [rows, d] act: dispatched rows (the dispatch "send buffer") */
     void* h;             /* expert hidden activations, see moe_expert_ffn (NULL for identity) */
     void* out;           /* expert outputs, see moe_expert_ffn (aliases xperm for identity) */
 } moe_workspace_view;
@@ -137,6 +153,10 @@ int64_t moe_capacity(int32_t T, int32_t k, int32_t E, int64_t cf_num, int64_t cf
 
 /* MOE_OK if the config is valid and supported, else the code the entry points would return. */
 int moe_validate_config(const moe_config* cfg);
+
+/* Rows of the dispatched-row buffers (xperm, h, out): T*K packed, N*capacity padded
+ * (-1 for an invalid config). */
+int64_t moe_rows_capacity(const moe_config* cfg);
 
 /* Workspace bytes each entry point needs (0 when cfg is invalid). */
 size_t moe_route_workspace_bytes(const moe_config* cfg);
@@ -169,31 +189,36 @@ int moe_kernels_per_forward(const moe_config* cfg);
 int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
               int32_t* topk_idx, float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Dispatch: groups the T*k assignments by expert, keeps the first `capacity` of
- * each expert in token order, and gathers the kept rows of x into `xperm`
+/* Dispatch: groups the T*k assignments by expert, keeps `capacity` of each
+ * expert's assignments (MOE_DROP_TOKEN_ORDER: the first ones by token;
+ * MOE_DROP_LOW_GATE: the largest gates, equal gates by token) and gathers the kept
+ * rows of x into `xperm`, in token order inside each expert's segment
  * ("EP Math": "The dispatch all-to-all", "Capacity factor", "Token drop").
  *   x        [T, d] act;  topk_idx [T, K] int32 (ids outside [0, N) are skipped
  *            and flagged MOE_DEV_ERR_INDEX)
+ *   topk_gate [T, K] fp32, read only by MOE_DROP_LOW_GATE with a capacity (else may be NULL)
  *   map      output arrays (see moe_dispatch_map)
- *   xperm    [T*K, d] act out: row r = x[row_src[r] / K]; rows [0, offsets[N]) written
+ *   xperm    [rows, d] act out (rows = moe_rows_capacity(cfg)): row r = x[row_src[r] / K], zero on
+ *            padding rows; rows [0, offsets[N]) written. May be NULL when rows is 0.
  *   ws       >= moe_dispatch_workspace_bytes(cfg) bytes; its first 4 bytes are the
  *            device status word, which this call clears first.
  * Bit-exact and deterministic: the result does not depend on scheduling. */
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
-                 const moe_dispatch_map* map, void* xperm, void* ws, size_t ws_bytes,
-                 moe_stream_t stream);
+                 const float* topk_gate, const moe_dispatch_map* map, void* xperm, void* ws,
+                 size_t ws_bytes, moe_stream_t stream);
 
 /* Grouped expert FFN over the dispatched rows: for each expert e, rows
  * [offsets[e], offsets[e+1]) of xperm go through Expert_e ("EP Math", "What expert
  * parallelism actually shards": every expert is a complete FFN with private weights).
- *   xperm   [T*K, d] act;  offsets [N+1] int32 (from moe_dispatch)
+ *   xperm   [rows, d] act;  offsets [N+1] int32 (from moe_dispatch), offsets[N] <= rows.
+ *           xperm, h and out may be NULL when rows (moe_rows_capacity) is 0.
  *   W13     SwiGLU: [N, 2F, d] act, rows [0,F) = W_gate^T, rows [F,2F) = W_up^T;
  *           ReLU:   [N, F, d]  act (W1^T).   (The usual linear-layer layout.)
  *   W2      [N, d, F] act (W_down^T / W2^T)
- *   h       out: hidden activation of each row, [T*K, F] act; under MOE_PRECISION_SPLIT_H
- *           [T*K, 2F] bf16: for every 64-column block b of h the 64 "hi" values at
+ *   h       out: hidden activation of each row, [rows, F] act; under MOE_PRECISION_SPLIT_H
+ *           [rows, 2F] bf16: for every 64-column block b of h the 64 "hi" values at
  *           columns [128b, 128b+64) and the 64 "lo" values at [128b+64, 128b+128).
- *   out     out: expert output of each row, [T*K, d]; fp32 under MOE_PRECISION_F32_OUT
+ *   out     out: expert output of each row, [rows, d]; fp32 under MOE_PRECISION_F32_OUT
  *           and MOE_PRECISION_SPLIT_H with bf16 activations, else the act dtype.
  * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation); fp32
  * runs on the fp32 FMA units. Requires F * sizeof(act) % 16 == 0 besides the row
@@ -209,9 +234,9 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
  * summed in fp32 in slot order and rounded once ("Mixture-of-Experts (MoE)
  * Architecture and Expert Parallelism", section 2; "EP Math", "The combine
  * all-to-all"; "Token drop": a dropped slot adds nothing and the gates are not
- * renormalised). A row index >= T*K is skipped and flagged in `status` if
+ * renormalised). A row index >= rows is skipped and flagged in `status` if
  * status is not NULL. Deterministic, no atomics.
- *   out [T*K, d]; topk_gate [T, K] fp32; pos [T, K] int32; y [T, d] act out. */
+ *   out [rows, d]; topk_gate [T, K] fp32; pos [T, K] int32; y [T, d] act out. */
 int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate,
                 const int32_t* pos, void* y, int32_t* status, moe_stream_t stream);
 
@@ -249,8 +274,9 @@ int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const floa
  * callers.
  *
  * Same arguments, outputs and results as moe_dispatch, minus ws/ws_bytes. Its
- * scratch (histogram and drop offsets, 4 * (N * ceil(T*K/256) + N) bytes plus a
- * small header) lives in one device array of MOE_STATIC_SCRATCH_BYTES inside the
+ * scratch (histogram and offsets, 4 * (N * ceil(T*K/256) + 2N + 1) bytes, plus 4*T*K
+ * under MOE_DROP_LOW_GATE, plus a small header) lives in one device array of
+ * MOE_STATIC_SCRATCH_BYTES inside the
  * library, which every GPU that loads the library keeps until the process exits.
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
  * routine) and returns MOE_ERR_WORKSPACE when a config needs more scratch than that.
@@ -262,7 +288,8 @@ int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const floa
  * report them through. */
 #define MOE_STATIC_SCRATCH_BYTES (1u << 20)
 int moe_dispatch_static(const moe_config* cfg, const void* x, const int32_t* topk_idx,
-                        const moe_dispatch_map* map, void* xperm, moe_stream_t stream);
+                        const float* topk_gate, const moe_dispatch_map* map, void* xperm,
+                        moe_stream_t stream);
 
 /* ----------------------------------------------------------- diagnostics */
 

@@ -25,6 +25,10 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_EXPERT_IDENTITY, MOE_EXPERT_RELU, MOE_EXPERT_SWIGLU = 0, 1, 2
 MOE_PRECISION_BF16, MOE_PRECISION_F32_OUT, MOE_PRECISION_SPLIT_H = 0, 1, 2
 PRECISIONS = {"bf16": MOE_PRECISION_BF16, "f32_out": MOE_PRECISION_F32_OUT, "split_h": MOE_PRECISION_SPLIT_H}
+MOE_DROP_TOKEN_ORDER, MOE_DROP_LOW_GATE = 0, 1
+DROP_POLICIES = {"token": MOE_DROP_TOKEN_ORDER, "gate": MOE_DROP_LOW_GATE}
+MOE_LAYOUT_PACKED, MOE_LAYOUT_PADDED = 0, 1
+LAYOUTS = {"packed": MOE_LAYOUT_PACKED, "padded": MOE_LAYOUT_PADDED}
 MOE_MAX_K, MOE_MAX_E = 16, 512
 EXPERT_KINDS = {"identity": MOE_EXPERT_IDENTITY, "relu": MOE_EXPERT_RELU, "swiglu": MOE_EXPERT_SWIGLU}
 ACT_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
@@ -45,7 +49,7 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("F", _i32), ("D", _i32),
                 ("act_dtype", _i32), ("expert_kind", _i32), ("precision", _i32), ("n_shared", _i32),
-                ("capacity", _i64)]
+                ("capacity", _i64), ("drop_policy", _i32), ("layout", _i32)]
 
 
 class moe_dispatch_map(ctypes.Structure):
@@ -61,6 +65,7 @@ class moe_workspace_view(ctypes.Structure):
 _SIGNATURES = {
     "moe_capacity": (_i64, [_i32, _i32, _i32, _i64, _i64, _i64]),
     "moe_validate_config": (ctypes.c_int, [ctypes.POINTER(moe_config)]),
+    "moe_rows_capacity": (_i64, [ctypes.POINTER(moe_config)]),
     "moe_dispatch_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
     "moe_ffn_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
     "moe_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
@@ -69,15 +74,16 @@ _SIGNATURES = {
     "moe_kernels_per_forward": (ctypes.c_int, [ctypes.POINTER(moe_config)]),
     "moe_route_workspace_bytes": (_sz, [ctypes.POINTER(moe_config)]),
     "moe_route": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _sz, _p]),
-    "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p, _p, _sz, _p]),
+    "moe_dispatch": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_dispatch_map), _p, _p,
+                                    _sz, _p]),
     "moe_expert_ffn": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_combine": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p]),
     "moe_layer_forward": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_layer_forward_traced": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p,
                                                 ctypes.POINTER(_p), _i32]),
     "moe_layer_forward_host": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
-    "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
-                                           _p]),
+    "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_dispatch_map),
+                                           _p, _p]),
     "moe_read_status": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
@@ -129,11 +135,12 @@ def _stream(stream=None):
 
 # ------------------------------------------------------------------ config
 def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None, precision="f32_out",
-                n_shared=0) -> moe_config:
+                n_shared=0, drop_policy="token", layout="packed") -> moe_config:
     """A moe_config; ``capacity`` None (dropless) or a non-negative integer."""
     return moe_config(T=T, d=d, E=E, k=k, F=F, D=D, act_dtype=ACT_DTYPES[act],
                       expert_kind=EXPERT_KINDS[expert], precision=PRECISIONS[precision], n_shared=n_shared,
-                      capacity=-1 if capacity is None else int(capacity))
+                      capacity=-1 if capacity is None else int(capacity),
+                      drop_policy=DROP_POLICIES[drop_policy], layout=LAYOUTS[layout])
 
 
 def out_dtype(cfg) -> torch.dtype:
@@ -165,11 +172,20 @@ def config_for(w, capacity="auto") -> moe_config:
     if capacity == "auto":
         capacity = None if w.capacity_factor is None else moe_capacity(w.T, w.k, w.E, w.capacity_factor,
                                                                        w.min_capacity)
-    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision, w.n_shared)
+    return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision, w.n_shared,
+                       w.drop_policy, w.layout)
 
 
 def moe_validate_config(cfg) -> int:
     return lib().moe_validate_config(ctypes.byref(cfg))
+
+
+def moe_rows_capacity(cfg) -> int:
+    """Rows of the dispatched-row buffers (xperm, h, out, row_src) for this config."""
+    r = lib().moe_rows_capacity(ctypes.byref(cfg))
+    if r < 0:
+        raise MoeError(moe_validate_config(cfg), "moe_rows_capacity")
+    return int(r)
 
 
 def moe_workspace_bytes(cfg) -> int:
@@ -244,15 +260,16 @@ def dispatch_map(counts_routed, counts_kept, offsets, rank_offsets, pos, row_src
                                                 drop_list, n_dropped)])
 
 
-def moe_dispatch(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, ws, stream=None):
-    _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xperm),
-                              _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+def moe_dispatch(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, ws, stream=None, topk_gate=None):
+    """``topk_gate`` is read only by the gate drop policy with a capacity."""
+    _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_gate), ctypes.byref(dmap),
+                              _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
 
 
-def moe_dispatch_static(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, stream=None):
+def moe_dispatch_static(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, stream=None, topk_gate=None):
     """moe_dispatch with the library's built-in scratch array (no workspace argument)."""
-    _check(lib().moe_dispatch_static(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xperm),
-                                     _stream(stream)), "moe_dispatch_static")
+    _check(lib().moe_dispatch_static(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_gate),
+                                     ctypes.byref(dmap), _ptr(xperm), _stream(stream)), "moe_dispatch_static")
 
 
 def moe_expert_ffn(cfg, xperm, offsets, W13, W2, h, out, ws, stream=None):

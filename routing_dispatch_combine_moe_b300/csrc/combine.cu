@@ -169,8 +169,8 @@ void launch_k(int grid, const void* out, const float* gate, const int32_t* pos, 
 }  // namespace
 
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
-                           void* y, int T, int d, int k, int32_t* status, cudaStream_t stream) {
-    const int64_t max_rows = int64_t(T) * k;
+                           void* y, int T, int d, int k, int64_t rows, int32_t* status, cudaStream_t stream) {
+    const int64_t max_rows = rows;
     const int grid = (T + 7) / 8;
     if (act_dtype == MOE_F32) {
         if (d % 8 == 0)

@@ -85,15 +85,17 @@ __device__ int block_excl_scan(int v, int* warp_sums, int* total) {
 }
 
 __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, int nblk, int64_t capacity,
-                                                    int32_t* __restrict__ hist, int32_t* __restrict__ counts_routed,
+                                                    int padded, int32_t* __restrict__ hist,
+                                                    int32_t* __restrict__ counts_routed,
                                                     int32_t* __restrict__ counts_kept, int32_t* __restrict__ offsets,
                                                     int32_t* __restrict__ drop_offsets,
+                                                    int32_t* __restrict__ routed_offsets,
                                                     int32_t* __restrict__ rank_offsets,
                                                     int32_t* __restrict__ n_dropped) {
     __shared__ int routed[MOE_MAX_E];
     __shared__ int offs[MOE_MAX_E + 1];
     __shared__ int warp_sums[32];
-    __shared__ int totals[2];
+    __shared__ int totals[3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     for (int e = warp; e < E; e += 32) {
@@ -112,29 +114,39 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
 
     const int cr = tid < E ? routed[tid] : 0;
     const int ck = (capacity < 0 || tid >= E_capped || cr <= capacity) ? cr : int(capacity);
-    const int off = block_excl_scan(ck, warp_sums, &totals[0]);
+    const int scanned = block_excl_scan(ck, warp_sums, &totals[0]);
     const int doff = block_excl_scan(cr - ck, warp_sums, &totals[1]);
+    const int roff = block_excl_scan(cr, warp_sums, &totals[2]);
+    // padded layout: every expert owns `capacity` rows
+    const int off = padded ? tid * int(capacity) : scanned;
     if (tid < E) {
         counts_routed[tid] = cr;
         counts_kept[tid] = ck;
         offsets[tid] = off;
         drop_offsets[tid] = doff;
+        routed_offsets[tid] = roff;
         offs[tid] = off;
     }
     if (tid == 0) {
-        offsets[E] = totals[0];
-        offs[E] = totals[0];
+        const int end = padded ? E * int(capacity) : totals[0];
+        offsets[E] = end;
+        offs[E] = end;
+        routed_offsets[E] = totals[2];
         *n_dropped = totals[1];
     }
     __syncthreads();
     if (tid <= D) rank_offsets[tid] = offs[tid * (E_capped / D)];
 }
 
+// With `elist` set (gate drop policy) it only lists each expert's assignments in
+// token order at routed_offsets[e] + rank; select_kernel then places them.
 __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* __restrict__ topk_idx, int64_t A,
                                                                  int E, int E_capped, int nblk, int64_t capacity,
                                                                  const int32_t* __restrict__ hist,
                                                                  const int32_t* __restrict__ offsets,
                                                                  const int32_t* __restrict__ drop_offsets,
+                                                                 const int32_t* __restrict__ routed_offsets,
+                                                                 int32_t* __restrict__ elist,
                                                                  int32_t* __restrict__ pos,
                                                                  int32_t* __restrict__ row_src,
                                                                  int32_t* __restrict__ drop_list) {
@@ -163,6 +175,10 @@ __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* 
     }
     int rank = hist[size_t(e) * nblk + blockIdx.x] + rank_in_warp;
     for (int w = 0; w < warp; ++w) rank += cnt[w][e];
+    if (elist) {
+        elist[routed_offsets[e] + rank] = int32_t(a);
+        return;
+    }
     if (capacity < 0 || e >= E_capped || rank < capacity) {
         const int row = offsets[e] + rank;
         pos[a] = row;
@@ -170,6 +186,137 @@ __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* 
     } else {
         pos[a] = -1;
         drop_list[drop_offsets[e] + (rank - int(capacity))] = int32_t(a);
+    }
+}
+
+constexpr int kSelThreads = 512;
+
+// Block-wide exclusive scan of one int per thread (kSelThreads threads); *total gets the sum.
+__device__ int sel_excl_scan(int v, int* warp_sums, int* total) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int incl = warp_incl_scan(v, lane);
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int ws = lane < kSelThreads / 32 ? warp_sums[lane] : 0;
+        const int wi = warp_incl_scan(ws, lane);
+        if (lane < kSelThreads / 32) warp_sums[lane] = wi - ws;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int r = warp_sums[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// fp32 bits mapped so that unsigned order is value order (negatives flipped, the
+// sign bit set on non-negatives); -0 sorts just below +0.
+__device__ __forceinline__ uint32_t order_key(float g) {
+    const uint32_t b = __float_as_uint(g);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Gate drop policy, one CTA per expert: the expert's routed assignments are listed
+// in token order; the ones kept are those whose gate is above the keep_n-th largest
+// gate, plus, among the gates equal to it, the first ones by token. That gate is
+// found by a most-significant-digit-first radix select over order_key(gate). Kept
+// assignments take the expert's rows in token order; the others go to the drop
+// list in token order.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* __restrict__ elist,
+                                                             const int32_t* __restrict__ routed_offsets,
+                                                             const int32_t* __restrict__ counts_routed,
+                                                             const int32_t* __restrict__ counts_kept,
+                                                             const int32_t* __restrict__ offsets,
+                                                             const int32_t* __restrict__ drop_offsets,
+                                                             const float* __restrict__ gate,
+                                                             int32_t* __restrict__ pos,
+                                                             int32_t* __restrict__ row_src,
+                                                             int32_t* __restrict__ drop_list) {
+    __shared__ int hist[256];
+    __shared__ int warp_sums[32];
+    __shared__ int totals[3];
+    __shared__ int sel_bin, sel_rank;
+    const int e = blockIdx.x, tid = threadIdx.x;
+    const int n = counts_routed[e], keep_n = counts_kept[e];
+    const int32_t* list = elist + routed_offsets[e];
+    const int base = offsets[e], dbase = drop_offsets[e];
+
+    uint32_t thr = 0;
+    int need_eq = 0;
+    if (keep_n > 0 && keep_n < n) {
+        uint32_t prefix = 0, mask = 0;
+        int rank = keep_n;  // 1-based rank, from the largest, of the last kept key
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += kSelThreads) {
+                const uint32_t key = order_key(gate[list[i]]);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                int cum = 0, b = 255;
+                for (; b > 0; --b) {
+                    if (cum + hist[b] >= rank) break;
+                    cum += hist[b];
+                }
+                sel_bin = b;
+                sel_rank = rank - cum;
+            }
+            __syncthreads();
+            prefix |= uint32_t(sel_bin) << shift;
+            mask |= 0xFFu << shift;
+            rank = sel_rank;
+        }
+        thr = prefix;
+        need_eq = rank;
+    }
+
+    int carry_eq = 0, carry_keep = 0, carry_drop = 0;
+    for (int i0 = 0; i0 < n; i0 += kSelThreads) {
+        const int i = i0 + tid;
+        const bool valid = i < n;
+        const int a = valid ? list[i] : 0;
+        const uint32_t key = valid ? order_key(gate[a]) : 0u;
+        bool keep;
+        int eq_rank = 0;
+        if (keep_n >= n) {
+            keep = valid;
+        } else if (keep_n == 0) {
+            keep = false;
+        } else {
+            const bool is_eq = valid && key == thr;
+            eq_rank = carry_eq + sel_excl_scan(is_eq ? 1 : 0, warp_sums, &totals[0]);
+            keep = valid && (key > thr || (is_eq && eq_rank < need_eq));
+            carry_eq += totals[0];
+        }
+        const int kr = carry_keep + sel_excl_scan(keep ? 1 : 0, warp_sums, &totals[1]);
+        const int dr = carry_drop + sel_excl_scan((valid && !keep) ? 1 : 0, warp_sums, &totals[2]);
+        if (keep) {
+            pos[a] = base + kr;
+            row_src[base + kr] = a;
+        } else if (valid) {
+            pos[a] = -1;
+            drop_list[dbase + dr] = a;
+        }
+        carry_keep += totals[1];
+        carry_drop += totals[2];
+    }
+}
+
+// Padded layout: rows [offsets[e] + kept, offsets[e] + capacity) of expert e are
+// zeroed and marked as holding no assignment.
+__global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict__ counts_kept,
+                                                       const int32_t* __restrict__ offsets, int capacity,
+                                                       uint4* __restrict__ xperm, int vec_per_row,
+                                                       int32_t* __restrict__ row_src) {
+    const int e = blockIdx.x;
+    const int r0 = offsets[e] + counts_kept[e], r1 = offsets[e] + capacity;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int r = r0; r < r1; ++r) {
+        uint4* row = xperm + size_t(r) * vec_per_row;
+        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) row[v] = z;
+        if (threadIdx.x == 0) row_src[r] = -1;
     }
 }
 
@@ -216,14 +363,26 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const int64_t A = int64_t(a.T) * a.k;
     const int nblk = dispatch_blocks(A);
-    count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.hist, a.status);
-    scan_kernel<<<1, 1024, 0, stream>>>(a.E, a.E_capped, a.D, nblk, a.capacity, a.hist, a.counts_routed,
-                                        a.counts_kept, a.offsets, a.drop_offsets, a.rank_offsets, a.n_dropped);
-    scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, a.E_capped, nblk, a.capacity, a.hist,
-                                                        a.offsets, a.drop_offsets, a.pos, a.row_src, a.drop_list);
+    const bool by_gate = a.drop_policy == MOE_DROP_LOW_GATE && a.capacity >= 0;
+    const bool padded = a.layout == MOE_LAYOUT_PADDED;
     const int vec_per_row = int(int64_t(a.d) * a.act_bytes / 16);
+    const int64_t rows = padded ? int64_t(a.E) * a.capacity : A;
+    count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.hist, a.status);
+    scan_kernel<<<1, 1024, 0, stream>>>(a.E, a.E_capped, a.D, nblk, a.capacity, padded ? 1 : 0, a.hist,
+                                        a.counts_routed, a.counts_kept, a.offsets, a.drop_offsets, a.routed_offsets,
+                                        a.rank_offsets, a.n_dropped);
+    scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, a.E_capped, nblk, a.capacity, a.hist,
+                                                        a.offsets, a.drop_offsets, a.routed_offsets,
+                                                        by_gate ? a.elist : nullptr, a.pos, a.row_src, a.drop_list);
+    if (by_gate)
+        select_kernel<<<a.E, kSelThreads, 0, stream>>>(a.elist, a.routed_offsets, a.counts_routed, a.counts_kept,
+                                                       a.offsets, a.drop_offsets, a.topk_gate, a.pos, a.row_src,
+                                                       a.drop_list);
+    if (padded)
+        pad_rows_kernel<<<a.E, 256, 0, stream>>>(a.counts_kept, a.offsets, int(a.capacity),
+                                                 static_cast<uint4*>(a.xperm), vec_per_row, a.row_src);
     gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
-                                                      static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, A);
+                                                      static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, rows);
     return cudaGetLastError();
 }
 

@@ -25,7 +25,8 @@ namespace {
 
 constexpr size_t kStaticScratchInts = MOE_STATIC_SCRATCH_BYTES / sizeof(int32_t);
 
-// [0]: status word, [64, 64 + E*blocks): histogram, then E drop offsets.
+// [0]: status word, [64, 64 + N*blocks): histogram, then N drop offsets, N+1 routed
+// offsets and (gate drop policy) the T*K per-expert assignment list.
 __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
 
 constexpr int kMaxDevices = 64;
@@ -58,10 +59,13 @@ extern thread_local std::string g_last_cuda_error;
 using namespace moe;
 
 extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const int32_t* topk_idx,
-                                   const moe_dispatch_map* map, void* xperm, moe_stream_t stream) {
+                                   const float* topk_gate, const moe_dispatch_map* map, void* xperm,
+                                   moe_stream_t stream) {
     const int rc = moe_validate_config(cfg);
     if (rc != MOE_OK) return rc;
-    if (!x || !topk_idx || !map || !xperm) return MOE_ERR_ARG;
+    if (!x || !topk_idx || !map || (!xperm && moe_rows_capacity(cfg) > 0)) return MOE_ERR_ARG;
+    const bool by_gate = cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0;
+    if (by_gate && !topk_gate) return MOE_ERR_ARG;
     if (!map->counts_routed || !map->counts_kept || !map->offsets || !map->rank_offsets || !map->pos ||
         !map->row_src || !map->drop_list || !map->n_dropped)
         return MOE_ERR_ARG;
@@ -69,7 +73,8 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
     const int N = cfg->E + cfg->n_shared, K = cfg->k + cfg->n_shared;
     const int64_t A = int64_t(cfg->T) * K;
     const size_t hist_ints = size_t(N) * size_t(dispatch_blocks(A));
-    if (64 + hist_ints + size_t(N) > kStaticScratchInts) return MOE_ERR_WORKSPACE;
+    const size_t list_ints = by_gate ? size_t(A) : 0;
+    if (64 + hist_ints + 2 * size_t(N) + 1 + list_ints > kStaticScratchInts) return MOE_ERR_WORKSPACE;
 
     int32_t* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
@@ -82,6 +87,9 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
     DispatchArgs a{};
     a.T = cfg->T; a.d = cfg->d; a.E = N; a.k = K; a.D = cfg->D;
     a.E_capped = cfg->E;
+    a.drop_policy = cfg->drop_policy;
+    a.layout = cfg->layout;
+    a.topk_gate = topk_gate;
     a.capacity = cfg->capacity;
     a.act_bytes = cfg->act_dtype == MOE_F32 ? 4 : 2;
     a.x = x;
@@ -98,6 +106,8 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
     a.status = scratch;
     a.hist = scratch + 64;
     a.drop_offsets = scratch + 64 + hist_ints;
+    a.routed_offsets = a.drop_offsets + N;
+    a.elist = by_gate ? a.routed_offsets + N + 1 : nullptr;
     e = launch_dispatch(a, stream);
     if (e != cudaSuccess) {
         g_last_cuda_error = std::string("moe_dispatch_static: ") + cudaGetErrorName(e) + " (" +

@@ -142,7 +142,7 @@ cudaError_t launch_mode(const SimtParams& p, int64_t rows_max, cudaStream_t stre
 }  // namespace
 
 cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event) {
-    const int64_t rows_max = int64_t(a.T) * a.k;
+    const int64_t rows_max = a.rows;
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;
     SimtParams p{};
     p.offsets = a.offsets;

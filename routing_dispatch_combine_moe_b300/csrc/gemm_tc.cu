@@ -533,7 +533,7 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Para
 }  // namespace
 
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event) {
-    const int64_t rows_max = int64_t(a.T) * a.k;
+    const int64_t rows_max = a.rows;
     const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
     const bool f32_out = a.precision != MOE_PRECISION_BF16;
     const bool pair = use_pairs(rows_max, a.E);

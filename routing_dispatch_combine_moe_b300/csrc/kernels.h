@@ -35,7 +35,10 @@ struct DispatchArgs {
     int T, d, E, k, D;  // E: all experts (routed + shared), k: all slots per token
     int E_capped;       // experts [0, E_capped) are routed: held to the capacity, split over D ranks
     int64_t capacity;  // < 0: dropless
+    int drop_policy;   // MOE_DROP_*
+    int layout;        // MOE_LAYOUT_*
     int act_bytes;
+    const float* topk_gate;  // [T*k], read by the gate drop policy
     const void* x;
     const int32_t* topk_idx;
     int32_t* counts_routed;
@@ -51,16 +54,19 @@ struct DispatchArgs {
     int32_t* status;
     int32_t* hist;         // [E * nblk]
     int32_t* drop_offsets; // [E]
+    int32_t* routed_offsets; // [E+1] exclusive scan of the routed counts (gate policy)
+    int32_t* elist;          // [T*k] each expert's assignments in token order (gate policy)
 };
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 
 // `out_dtype` is the dtype of the expert outputs (MOE_F32 or MOE_BF16), `act_dtype` that of y.
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
-                           void* y, int T, int d, int k, int32_t* status, cudaStream_t stream);
+                           void* y, int T, int d, int k, int64_t rows, int32_t* status, cudaStream_t stream);
 
 struct FfnArgs {
     int T, d, E, k, F;
+    int64_t rows;  // rows of xperm / h / out
     int expert_kind;
     int act_dtype;
     int precision;  // MOE_PRECISION_*

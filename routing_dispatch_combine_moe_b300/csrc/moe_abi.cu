@@ -43,6 +43,12 @@ inline int act_bytes(const moe_config* c) { return c->act_dtype == MOE_F32 ? 4 :
 inline int n_experts(const moe_config* c) { return c->E + c->n_shared; }
 inline int n_slots(const moe_config* c) { return c->k + c->n_shared; }
 
+// Rows of the dispatched-row buffers: every kept assignment (packed), or a fixed
+// `capacity` rows per expert (padded).
+inline int64_t rows_cap(const moe_config* c) {
+    return c->layout == MOE_LAYOUT_PADDED ? int64_t(n_experts(c)) * c->capacity : int64_t(c->T) * n_slots(c);
+}
+
 inline bool bf16_experts(const moe_config* c) {
     return c->act_dtype == MOE_BF16 && c->expert_kind != MOE_EXPERT_IDENTITY;
 }
@@ -72,8 +78,12 @@ int validate(const moe_config* c) {
     if (c->k > c->E) return MOE_ERR_ARG;
     if (c->E % c->D != 0) return MOE_ERR_ARG;
     if (c->expert_kind != MOE_EXPERT_IDENTITY && c->F < 1) return MOE_ERR_ARG;
+    if (c->drop_policy != MOE_DROP_TOKEN_ORDER && c->drop_policy != MOE_DROP_LOW_GATE) return MOE_ERR_ARG;
+    if (c->layout != MOE_LAYOUT_PACKED && c->layout != MOE_LAYOUT_PADDED) return MOE_ERR_ARG;
     if (n_experts(c) > MOE_MAX_E || n_slots(c) > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
-    if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+    if (c->layout == MOE_LAYOUT_PADDED && (c->capacity < 0 || c->n_shared != 0)) return MOE_ERR_UNSUPPORTED;
+    if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX) || rows_cap(c) > int64_t(INT32_MAX))
+        return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
     if (c->expert_kind != MOE_EXPERT_IDENTITY && (int64_t(c->F) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
     if (split_h(c) && c->F % 64 != 0) return MOE_ERR_UNSUPPORTED;
@@ -81,7 +91,7 @@ int validate(const moe_config* c) {
 }
 
 struct Layout {
-    size_t status, hist, drop_offsets, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
+    size_t status, hist, drop_offsets, routed_offsets, elist, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
         n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
     size_t dispatch_end, forward_end, host_end;
 };
@@ -101,6 +111,8 @@ Layout layout(const moe_config* c) {
     L.status = take(sizeof(int32_t));
     L.hist = take(sizeof(int32_t) * size_t(N) * nblk);
     L.drop_offsets = take(sizeof(int32_t) * size_t(N));
+    L.routed_offsets = take(sizeof(int32_t) * size_t(N + 1));
+    L.elist = take(c->drop_policy == MOE_DROP_LOW_GATE ? sizeof(int32_t) * A : 0);
     L.dispatch_end = o;
     L.route_partial = take(route_scratch_bytes_max(c->T, c->E));
     L.topk_idx = take(sizeof(int32_t) * A);
@@ -110,13 +122,14 @@ Layout layout(const moe_config* c) {
     L.offsets = take(sizeof(int32_t) * size_t(N + 1));
     L.rank_offsets = take(sizeof(int32_t) * size_t(c->D + 1));
     L.n_dropped = take(sizeof(int32_t));
+    const size_t R = size_t(rows_cap(c));
     L.pos = take(sizeof(int32_t) * A);
-    L.row_src = take(sizeof(int32_t) * A);
+    L.row_src = take(sizeof(int32_t) * (R > size_t(A) ? R : size_t(A)));
     L.drop_list = take(sizeof(int32_t) * A);
-    L.xperm = take(b * A * size_t(c->d));
+    L.xperm = take(b * R * size_t(c->d));
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
-        L.h = take(split_h(c) ? 2 * 2 * A * size_t(c->F) : b * A * size_t(c->F));
-        L.out = take((out_dtype(c) == MOE_F32 ? 4 : b) * A * size_t(c->d));
+        L.h = take(split_h(c) ? 2 * 2 * R * size_t(c->F) : b * R * size_t(c->F));
+        L.out = take((out_dtype(c) == MOE_F32 ? 4 : b) * R * size_t(c->d));
     } else {
         L.h = 0;
         L.out = L.xperm;
@@ -158,13 +171,16 @@ int run_route(const moe_config* c, const void* x, const float* Wg, const float* 
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
 }
 
-int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const moe_dispatch_map* m, void* xperm,
-                 void* ws, cudaStream_t s) {
+int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const float* gate, const moe_dispatch_map* m,
+                 void* xperm, void* ws, cudaStream_t s) {
     const Layout L = layout(c);
     DispatchArgs a{};
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.D = c->D;
     a.E_capped = c->E;
     a.capacity = c->capacity;
+    a.drop_policy = c->drop_policy;
+    a.layout = c->layout;
+    a.topk_gate = gate;
     a.act_bytes = act_bytes(c);
     a.x = x;
     a.topk_idx = idx;
@@ -180,6 +196,8 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const m
     a.status = at<int32_t>(ws, L.status);
     a.hist = at<int32_t>(ws, L.hist);
     a.drop_offsets = at<int32_t>(ws, L.drop_offsets);
+    a.routed_offsets = at<int32_t>(ws, L.routed_offsets);
+    a.elist = c->drop_policy == MOE_DROP_LOW_GATE ? at<int32_t>(ws, L.elist) : nullptr;
     const cudaError_t e = launch_dispatch(a, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch");
 }
@@ -188,6 +206,7 @@ int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, cons
             void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
     FfnArgs a{};
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.F = c->F;
+    a.rows = rows_cap(c);
     a.expert_kind = c->expert_kind;
     a.act_dtype = c->act_dtype;
     a.precision = c->precision;
@@ -198,6 +217,15 @@ int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, cons
     a.h = h;
     a.out = out;
     a.status = status;
+    if (a.rows == 0) {  // padded layout with capacity 0: no rows, nothing to compute
+        if (!mid) return MOE_OK;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(s, &cs);
+        if (e == cudaSuccess)
+            e = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal)
+                                                    : cudaEventRecord(mid, s);
+        return e == cudaSuccess ? MOE_OK : fail_cuda(e, "cudaEventRecord");
+    }
     const cudaError_t e = c->act_dtype == MOE_BF16 ? launch_ffn_tc(a, s, mid) : launch_ffn_simt(a, s, mid);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_expert_ffn");
 }
@@ -234,7 +262,7 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
-    if ((rc = run_dispatch(c, x, v.topk_idx, &v.map, v.xperm, ws, s)) != MOE_OK) return rc;
+    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s)) != MOE_OK) return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
         cudaEvent_t mid = (events && n_events > 3) ? static_cast<cudaEvent_t>(events[3]) : nullptr;
@@ -244,7 +272,7 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     }
     if ((rc = record(events, n_events, 4, s)) != MOE_OK) return rc;
     e = launch_combine(c->act_dtype, out_dtype(c), v.out, v.topk_gate, v.map.pos, y, c->T, c->d, n_slots(c),
-                       v.status, s);
+                       rows_cap(c), v.status, s);
     if (e != cudaSuccess) return fail_cuda(e, "moe_combine");
     return record(events, n_events, 5, s);
 }
@@ -269,6 +297,8 @@ int64_t moe_capacity(int32_t T, int32_t k, int32_t E, int64_t cf_num, int64_t cf
 
 int moe_validate_config(const moe_config* cfg) { return validate(cfg); }
 
+int64_t moe_rows_capacity(const moe_config* cfg) { return validate(cfg) == MOE_OK ? rows_cap(cfg) : -1; }
+
 size_t moe_dispatch_workspace_bytes(const moe_config* cfg) {
     return validate(cfg) == MOE_OK ? layout(cfg).dispatch_end : 0;
 }
@@ -292,8 +322,11 @@ int moe_workspace_get_view(const moe_config* cfg, void* ws, size_t ws_bytes, moe
 
 int moe_kernels_per_forward(const moe_config* cfg) {
     if (validate(cfg) != MOE_OK) return 0;
-    // route + (count, scan, scatter, gather) + (up, down) + combine
-    return 1 + 4 + (cfg->expert_kind == MOE_EXPERT_IDENTITY ? 0 : 2) + 1;
+    // (logits, top-k) + (count, scan, scatter, [select], [pad], gather) + (up, down) + combine
+    const int select = cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0 ? 1 : 0;
+    const int pad = cfg->layout == MOE_LAYOUT_PADDED ? 1 : 0;
+    const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
+    return 2 + 4 + select + pad + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {
@@ -314,11 +347,13 @@ int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float
     return run_route(cfg, x, Wg, bias, topk_idx, topk_gate, static_cast<float*>(ws), stream);
 }
 
-int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const moe_dispatch_map* map,
-                 void* xperm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, const float* topk_gate,
+                 const moe_dispatch_map* map, void* xperm, void* ws, size_t ws_bytes, moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
-    if (!x || !topk_idx || !map || !xperm || !ws) return MOE_ERR_ARG;
+    // xperm may be NULL only when there are no rows (padded layout, capacity 0)
+    if (!x || !topk_idx || !map || (!xperm && rows_cap(cfg) > 0) || !ws) return MOE_ERR_ARG;
+    if (cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0 && !topk_gate) return MOE_ERR_ARG;
     if (!map->counts_routed || !map->counts_kept || !map->offsets || !map->rank_offsets || !map->pos ||
         !map->row_src || !map->drop_list || !map->n_dropped)
         return MOE_ERR_ARG;
@@ -326,7 +361,7 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, 
     if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
     const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
-    return run_dispatch(cfg, x, topk_idx, map, xperm, ws, stream);
+    return run_dispatch(cfg, x, topk_idx, topk_gate, map, xperm, ws, stream);
 }
 
 int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets, const void* W13, const void* W2,
@@ -334,7 +369,8 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
     if (cfg->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_ARG;
-    if (!xperm || !offsets || !W13 || !W2 || !h || !out || !ws) return MOE_ERR_ARG;
+    if (!offsets || !W13 || !W2 || !ws) return MOE_ERR_ARG;
+    if ((!xperm || !h || !out) && rows_cap(cfg) > 0) return MOE_ERR_ARG;
     if (!aligned16(xperm) || !aligned16(W13) || !aligned16(W2) || !aligned16(h) || !aligned16(out) ||
         !aligned16(ws))
         return MOE_ERR_ALIGN;
@@ -349,10 +385,10 @@ int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, 
                 int32_t* status, moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
-    if (!out || !topk_gate || !pos || !y) return MOE_ERR_ARG;
+    if ((!out && rows_cap(cfg) > 0) || !topk_gate || !pos || !y) return MOE_ERR_ARG;
     if (!aligned16(out) || !aligned16(y) || !aligned4(topk_gate) || !aligned4(pos)) return MOE_ERR_ALIGN;
     const cudaError_t e = launch_combine(cfg->act_dtype, out_dtype(cfg), out, topk_gate, pos, y, cfg->T, cfg->d,
-                                         n_slots(cfg), status, stream);
+                                         n_slots(cfg), rows_cap(cfg), status, stream);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_combine");
 }
 

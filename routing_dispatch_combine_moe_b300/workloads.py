@@ -161,3 +161,56 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu") -> dict:
         W13=W13,
         W2=W2,
     )
+
+
+def make_stage_inputs(w: Workload, seed: int = 0, device="cpu", rows: int | None = None,
+                      keep_frac: float = 0.8) -> dict:
+    """Seeded inputs of the stages after the router, drawn directly (no routing):
+
+      topk_idx [T, K] int32: k distinct routed ids per token, drawn with Zipf(s)
+                weights over the experts when the workload is skewed, else uniformly;
+                the shared slots hold E, E+1, ...
+      topk_gate [T, K] fp32: independent draws from U(0.01, 1) (shared slots: 1).
+      counts [N] int64: rows per expert for an expert-FFN call, summing to at most
+                ``rows`` (default T*K), with some experts left empty.
+      xperm [sum(counts), d] act: N(0, 1) rows.
+      pos [T*K] int32: a random injective map of a ``keep_frac`` share of the
+                assignments onto rows [0, rows); the rest are -1.
+      out_rows [rows, d]: N(0, 1) rows in fp32 (cast by the caller to the out dtype).
+    """
+    g = torch.Generator().manual_seed(1_000_003 + seed)
+    T, k, S, E, N = w.T, w.k, w.n_shared, w.E, w.n_experts
+    K = k + S
+    R = T * K if rows is None else rows
+    if w.zipf_s is not None:
+        p = torch.arange(1, E + 1, dtype=torch.float64) ** -float(w.zipf_s)
+        perm = torch.randperm(E, generator=g)
+        weights = torch.empty(E, dtype=torch.float64)
+        weights[perm] = p
+    else:
+        weights = torch.ones(E, dtype=torch.float64)
+    idx = torch.multinomial(weights.expand(T, E), k, replacement=False, generator=g).to(torch.int32)
+    gate = 0.01 + 0.99 * torch.rand(T, k, generator=g)
+    if S:
+        idx = torch.cat([idx, (E + torch.arange(S, dtype=torch.int32)).expand(T, S)], dim=1)
+        gate = torch.cat([gate, torch.ones(T, S)], dim=1)
+    total = int(torch.randint(R // 2, R + 1, (1,), generator=g)) if R > 0 else 0
+    empty = torch.rand(N, generator=g) < 0.15
+    share = torch.rand(N, generator=g).masked_fill(empty, 0.0)
+    if float(share.sum()) == 0.0:
+        share[0] = 1.0
+    counts = torch.floor(share / share.sum() * total).to(torch.int64)
+    A = T * K
+    n_keep = min(int(round(keep_frac * A)), R)
+    pos = torch.full((A,), -1, dtype=torch.int32)
+    chosen = torch.randperm(A, generator=g)[:n_keep]
+    pos[chosen] = torch.randperm(R, generator=g)[:n_keep].to(torch.int32)
+    dev = torch.device(device)
+    return dict(
+        topk_idx=idx.contiguous().to(dev),
+        topk_gate=gate.to(torch.float32).contiguous().to(dev),
+        counts=counts,
+        xperm=torch.randn(int(counts.sum()), w.d, generator=g).to(w.torch_act).to(dev),
+        pos=pos.to(dev),
+        out_rows=torch.randn(R, w.d, generator=g).to(dev),
+    )

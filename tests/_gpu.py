@@ -58,13 +58,16 @@ def check_close(got, exact, act: str, what: str, tol: float | None = None) -> fl
 
 
 class StageBuffers:
-    """Output buffers of the four stage entry points, filled with sentinels."""
+    """Output buffers of the four stage entry points, filled with sentinels. The
+    dispatched-row buffers have moe_rows_capacity(cfg) rows (N*C in the padded
+    layout, T*K otherwise)."""
 
     def __init__(self, w, cfg, device="cuda"):
         A = w.T * w.slots
         N = w.n_experts
+        R = abi.moe_rows_capacity(cfg)
         i32 = dict(dtype=torch.int32, device=device)
-        self.cfg = cfg
+        self.cfg, self.rows = cfg, R
         self.topk_idx = torch.full((w.T, w.slots), -7, **i32)
         self.topk_gate = torch.full((w.T, w.slots), float("nan"), dtype=torch.float32, device=device)
         self.counts_routed = torch.full((N,), -7, **i32)
@@ -72,12 +75,12 @@ class StageBuffers:
         self.offsets = torch.full((N + 1,), -7, **i32)
         self.rank_offsets = torch.full((w.D + 1,), -7, **i32)
         self.pos = torch.full((A,), -7, **i32)
-        self.row_src = torch.full((A,), -7, **i32)
+        self.row_src = torch.full((max(A, R),), -7, **i32)
         self.drop_list = torch.full((A,), -7, **i32)
         self.n_dropped = torch.full((1,), -7, **i32)
-        self.xperm = torch.full((A, w.d), float("nan"), dtype=w.torch_act, device=device)
-        self.h = torch.full((A, max(abi.hidden_cols(cfg), 1)), float("nan"), dtype=w.torch_act, device=device)
-        self.out = torch.full((A, w.d), float("nan"), dtype=abi.out_dtype(cfg), device=device)
+        self.xperm = torch.full((R, w.d), float("nan"), dtype=w.torch_act, device=device)
+        self.h = torch.full((R, max(abi.hidden_cols(cfg), 1)), float("nan"), dtype=w.torch_act, device=device)
+        self.out = torch.full((R, w.d), float("nan"), dtype=abi.out_dtype(cfg), device=device)
         self.out_act = "f32" if abi.out_dtype(cfg) == torch.float32 else "bf16"
         self.y = torch.full((w.T, w.d), float("nan"), dtype=w.torch_act, device=device)
         nr = abi.moe_route_workspace_bytes(cfg)
@@ -93,15 +96,18 @@ class StageBuffers:
     def route(self, inp):
         abi.moe_route(self.cfg, inp["x"], inp["Wg"], inp.get("bias"), self.topk_idx, self.topk_gate, self.ws_route)
 
-    def dispatch(self, inp, topk_idx=None):
+    def dispatch(self, inp, topk_idx=None, topk_gate=None):
         abi.moe_dispatch(self.cfg, inp["x"], self.topk_idx if topk_idx is None else topk_idx, self.dmap(),
-                         self.xperm, self.ws_dispatch)
+                         self.xperm, self.ws_dispatch, topk_gate=self.topk_gate if topk_gate is None else topk_gate)
 
-    def ffn(self, inp):
-        abi.moe_expert_ffn(self.cfg, self.xperm, self.offsets, inp["W13"], inp["W2"], self.h, self.out, self.ws_ffn)
+    def ffn(self, inp, xperm=None, offsets=None):
+        abi.moe_expert_ffn(self.cfg, self.xperm if xperm is None else xperm,
+                           self.offsets if offsets is None else offsets, inp["W13"], inp["W2"], self.h, self.out,
+                           self.ws_ffn)
 
-    def combine(self, out=None):
-        abi.moe_combine(self.cfg, self.out if out is None else out, self.topk_gate, self.pos, self.y, self.status)
+    def combine(self, out=None, topk_gate=None, pos=None):
+        abi.moe_combine(self.cfg, self.out if out is None else out, self.topk_gate if topk_gate is None else topk_gate,
+                        self.pos if pos is None else pos, self.y, self.status)
 
     def dispatch_status(self) -> int:
         return abi.moe_read_status(self.ws_dispatch.data_ptr())
@@ -114,17 +120,29 @@ def cpu(t):
     return t.detach().cpu()
 
 
-def check_route(w, inp, bufs, H=None) -> dict:
-    """Top-k ids exact away from near ties; gates within GATE_TOL. Returns stats."""
-    if H is None:
-        H = orc.router_logits(f64(inp["x"]), f64(inp["Wg"]), f64(inp.get("bias")))
-    idx_o = orc.keep_topk(H, w.k)
-    G_o = orc.kept_softmax(H, idx_o)
+def capacity_of(cfg):
+    return None if cfg.capacity < 0 else int(cfg.capacity)
+
+
+def oracle_route(w, inp) -> dict:
+    """The oracle's router on the original inputs, with the shared slots appended."""
+    H = orc.router_logits(f64(inp["x"]), f64(inp["Wg"]), f64(inp.get("bias")))
+    idx = orc.keep_topk(H, w.k)
+    G = orc.kept_softmax(H, idx)
     set_tie, order_tie = orc.near_tie_flags(H, w.k)
-    tie = set_tie | order_tie
+    S = w.n_shared
+    idx_full = np.concatenate([idx, np.broadcast_to(w.E + np.arange(S), (w.T, S))], axis=1)
+    G_full = np.concatenate([G, np.ones((w.T, S))], axis=1)
+    return dict(H=H, idx=idx, G=G, tie=set_tie | order_tie, idx_full=idx_full, G_full=G_full)
+
+
+def check_route(w, inp, bufs, ref=None) -> dict:
+    """Top-k ids exact away from near ties; gates within GATE_TOL. Returns stats."""
+    ref = oracle_route(w, inp) if ref is None else ref
+    idx_o, G_o, tie = ref["idx"], ref["G"], ref["tie"]
     idx_all = cpu(bufs.topk_idx).numpy()
     G_all = cpu(bufs.topk_gate).numpy().astype(np.float64)
-    S = getattr(w, "n_shared", 0)
+    S = w.n_shared
     if S:  # shared slots follow the routed ones: experts E.., gate 1
         assert np.all(idx_all[:, w.k:] == w.E + np.arange(S)) and np.all(G_all[:, w.k:] == 1.0)
     idx_g, G_g = idx_all[:, :w.k], G_all[:, :w.k]
@@ -135,32 +153,75 @@ def check_route(w, inp, bufs, H=None) -> dict:
     gerr = np.abs(G_g[ok] - G_o[ok]).max() if ok.any() else 0.0
     assert gerr <= GATE_TOL, f"gate error {gerr:.3e} > {GATE_TOL}"
     assert np.all((idx_g >= 0) & (idx_g < w.E))
-    return dict(near_ties=int(tie.sum()), flipped=int(mismatch.sum()), gate_err=float(gerr), H=H, idx=idx_o, G=G_o)
+    return dict(ref, near_ties=int(tie.sum()), flipped=int(mismatch.sum()), gate_err=float(gerr))
 
 
-def check_dispatch(w, inp, bufs, capacity) -> dict:
-    """Stage check on the GPU's own top-k: every routing-map array bit-exact, rows copied exactly."""
-    idx_g = cpu(bufs.topk_idx).numpy().astype(np.int64)
-    d = orc.dispatch(idx_g, w.n_experts, capacity, w.D, capped_experts=w.E)
+def gate_boundary_ties(w, idx, G, capacity, tol=2 * GATE_TOL) -> np.ndarray:
+    """Tokens whose gate on a capped, overflowing expert lies within ``tol`` of that
+    expert's keep cutoff (the capacity-th largest gate): under the gate drop policy
+    an fp32 and an fp64 router may keep different ones of them."""
+    flag = np.zeros(w.T, bool)
+    if capacity is None:
+        return flag
+    for e in range(w.E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size <= capacity:
+            continue
+        g = G[tok, slot]
+        order = np.sort(g)[::-1]
+        cut = order[capacity - 1] if capacity > 0 else np.inf
+        flag[tok[np.abs(g - cut) <= tol]] = True
+        if capacity > 0:
+            nxt = order[capacity]
+            flag[tok[np.abs(g - nxt) <= tol]] = True
+    return flag
+
+
+def compare_dispatch(w, bufs, d, x=None, xperm=None):
+    """Every routing-map array bit-exact against the oracle's dispatch ``d``; the
+    dispatched rows exact copies of x (padding rows zero)."""
     np.testing.assert_array_equal(cpu(bufs.counts_routed).numpy(), d["counts_routed"])
     np.testing.assert_array_equal(cpu(bufs.counts_kept).numpy(), d["counts_kept"])
     np.testing.assert_array_equal(cpu(bufs.offsets).numpy(), d["offsets"])
     np.testing.assert_array_equal(cpu(bufs.rank_offsets).numpy(), d["rank_offsets"])
     np.testing.assert_array_equal(cpu(bufs.pos).numpy(), d["pos"])
-    rows = int(d["offsets"][-1])
+    rows = d["row_src"].size
     np.testing.assert_array_equal(cpu(bufs.row_src).numpy()[:rows], d["row_src"])
     nd = d["n_dropped"]
     assert int(cpu(bufs.n_dropped)[0]) == nd
     np.testing.assert_array_equal(cpu(bufs.drop_list).numpy()[:nd], d["drop_list"])
-    # dispatched rows are exact copies of x[row_src // k]
-    src_tok = torch.from_numpy(d["row_src"] // w.slots).to(bufs.xperm.device)
-    assert torch.equal(bufs.xperm[:rows], inp["x"][src_tok]), "dispatched rows are not exact copies of x"
+    if x is not None:
+        xperm = bufs.xperm if xperm is None else xperm
+        src = torch.from_numpy(d["row_src"]).to(xperm.device)
+        valid = src >= 0
+        assert torch.equal(xperm[:rows][valid], x[src[valid] // w.slots]), "dispatched rows are not exact copies of x"
+        assert torch.count_nonzero(xperm[:rows][~valid]) == 0, "padding rows are not zero"
+
+
+def oracle_dispatch(w, idx, gates, capacity):
+    return orc.dispatch(np.asarray(idx, np.int64), w.n_experts, capacity, w.D, capped_experts=w.E,
+                        gates=None if gates is None else np.asarray(gates, np.float64),
+                        drop_policy=w.drop_policy, layout=w.layout)
+
+
+def check_dispatch(w, inp, bufs, capacity, st) -> dict:
+    """Dispatch stage on seeded synthetic ids and gates (``st`` from
+    workloads.make_stage_inputs): every map array bit-exact, rows copied exactly."""
+    bufs.dispatch(inp, topk_idx=st["topk_idx"], topk_gate=st["topk_gate"])
+    d = oracle_dispatch(w, cpu(st["topk_idx"]).numpy(), cpu(st["topk_gate"]).numpy(), capacity)
+    torch.cuda.synchronize()
+    compare_dispatch(w, bufs, d, inp["x"])
     return d
 
 
-def check_ffn(w, inp, bufs, rows: int, expert_subset=None) -> float:
-    """Expert outputs of the GPU's dispatched rows against the oracle's experts."""
-    offs = cpu(bufs.offsets).numpy()
+def check_ffn(w, inp, bufs, st, expert_subset=None) -> float:
+    """Expert FFN stage on seeded synthetic rows and per-expert counts: each
+    expert's output rows against the oracle's expert on the same rows."""
+    counts = st["counts"].numpy()
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    xperm = torch.zeros(bufs.rows, w.d, dtype=w.torch_act, device="cuda")
+    xperm[:offs[-1]] = st["xperm"]
+    bufs.ffn(inp, xperm=xperm, offsets=torch.from_numpy(offs).cuda())
     fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
     experts = range(w.n_experts) if expert_subset is None else expert_subset
     worst = 0.0
@@ -168,17 +229,109 @@ def check_ffn(w, inp, bufs, rows: int, expert_subset=None) -> float:
         lo, hi = int(offs[e]), int(offs[e + 1])
         if hi == lo:
             continue
-        X = f64(bufs.xperm[lo:hi])
-        exact = fn(e, X)
+        exact = fn(e, f64(st["xperm"][lo:hi]))
         worst = max(worst, check_close(bufs.out[lo:hi], exact, bufs.out_act, f"expert {e} output",
                                        tol=TOL[w.act]))
     return worst
 
 
-def check_combine(w, bufs) -> float:
-    """Combine stage on the GPU's own expert outputs, gates and positions."""
-    exact = orc.combine(f64(bufs.topk_gate), cpu(bufs.pos).numpy().astype(np.int64), f64(bufs.out), w.T, w.slots)
+def check_combine(w, bufs, st) -> float:
+    """Combine stage on seeded synthetic expert rows, gates and positions."""
+    out = st["out_rows"].to(bufs.out.dtype)
+    if out.shape[0] < bufs.rows:
+        out = torch.cat([out, torch.zeros(bufs.rows - out.shape[0], w.d, dtype=out.dtype, device=out.device)])
+    bufs.combine(out=out, topk_gate=st["topk_gate"], pos=st["pos"])
+    exact = orc.combine(f64(st["topk_gate"]), cpu(st["pos"]).numpy().astype(np.int64), f64(out), w.T, w.slots)
     return check_close(bufs.y, exact, w.act, "combine", tol=1e-5)
+
+
+def check_map_properties(w, m, capacity):
+    """What any correct dispatch of the GPU's own ids satisfies, at any size: counts
+    are the ids' histogram, offsets their prefix sum (or e*C), each kept assignment's
+    row lies in its expert's segment, row_src inverts pos, rows inside a segment are
+    in token order, nothing is kept beyond the capacity."""
+    idx = cpu(m.topk_idx).numpy().astype(np.int64)
+    N, A = w.n_experts, w.T * w.slots
+    flat = idx.reshape(-1)
+    routed = np.bincount(flat, minlength=N)
+    np.testing.assert_array_equal(cpu(m.counts_routed).numpy(), routed)
+    kept = cpu(m.counts_kept).numpy().astype(np.int64)
+    capped = np.arange(N) < w.E
+    limit = np.where(capped & (capacity is not None), capacity if capacity is not None else 0, routed)
+    np.testing.assert_array_equal(kept, np.minimum(routed, limit))
+    offs = cpu(m.offsets).numpy().astype(np.int64)
+    if w.layout == "padded":
+        np.testing.assert_array_equal(offs, np.arange(N + 1) * capacity)
+    else:
+        np.testing.assert_array_equal(offs, np.concatenate([[0], np.cumsum(kept)]))
+    pos = cpu(m.pos).numpy().astype(np.int64)
+    row_src = cpu(m.row_src).numpy().astype(np.int64)
+    k_mask = pos >= 0
+    assert k_mask.sum() == kept.sum() and int(cpu(m.n_dropped)[0]) == A - kept.sum()
+    a = np.nonzero(k_mask)[0]
+    e = flat[a]
+    assert np.all((pos[a] >= offs[e]) & (pos[a] < offs[e] + kept[e]))
+    np.testing.assert_array_equal(row_src[pos[a]], a)
+    for ee in range(N):
+        seg = row_src[offs[ee]:offs[ee] + kept[ee]]
+        assert np.all(np.diff(seg) > 0), f"expert {ee}: rows not in token order"
+
+
+def check_chained_dispatch(w, inp, m, r, capacity, xperm=None) -> str:
+    """The GPU's dispatch of its own routing. Where its ids equal the oracle's (no
+    near-tie flip) and, under the gate drop policy, no two gates meet at a keep
+    cutoff, it must equal the oracle's dispatch of the oracle's routing bit for bit;
+    otherwise it is held to the properties every correct dispatch has."""
+    exact = r["flipped"] == 0
+    if exact and w.drop_policy == "gate":
+        exact = not gate_boundary_ties(w, r["idx"], r["G"], capacity).any()
+    if exact:
+        compare_dispatch(w, m, oracle_dispatch(w, r["idx_full"], r["G_full"], capacity), inp["x"], xperm)
+        return "exact"
+    check_map_properties(w, m, capacity)
+    return "properties"
+
+
+class WorkspaceMap:
+    """The dispatch map inside a forward's workspace, as tensors named like StageBuffers'."""
+
+    def __init__(self, w, cfg, ws, view):
+        A, N = w.T * w.slots, w.n_experts
+        R = abi.moe_rows_capacity(cfg)
+        base = ws.data_ptr()
+        i32 = lambda ptr, n: ws[ptr - base:ptr - base + 4 * n].view(torch.int32)
+        mp = view
+        self.topk_idx = i32(view.topk_idx, A).view(w.T, w.slots)
+        self.topk_gate = ws[view.topk_gate - base:view.topk_gate - base + 4 * A].view(torch.float32).view(w.T, w.slots)
+        self.counts_routed = i32(mp.counts_routed, N)
+        self.counts_kept = i32(mp.counts_kept, N)
+        self.offsets = i32(mp.offsets, N + 1)
+        self.rank_offsets = i32(mp.rank_offsets, w.D + 1)
+        self.pos = i32(mp.pos, A)
+        self.row_src = i32(mp.row_src, max(A, R))
+        self.drop_list = i32(mp.drop_list, A)
+        self.n_dropped = i32(mp.n_dropped, 1)
+        esz = torch.tensor([], dtype=w.torch_act).element_size()
+        self.xperm = ws[view.xperm - base:view.xperm - base + R * w.d * esz].view(w.torch_act).view(R, w.d)
+        odt = abi.out_dtype(cfg)
+        osz = torch.tensor([], dtype=odt).element_size()
+        self.out = None if not view.out else \
+            ws[view.out - base:view.out - base + R * w.d * osz].view(odt).view(R, w.d)
+        self.out_act = "f32" if odt == torch.float32 else "bf16"
+
+
+def chain(w, inp, cfg) -> StageBuffers:
+    """The four stage entry points chained on the GPU, each on the previous one's output."""
+    b = StageBuffers(w, cfg)
+    b.route(inp)
+    b.dispatch(inp)
+    if w.expert != "identity":
+        b.ffn(inp)
+        b.combine()
+    else:
+        b.combine(out=b.xperm)
+    torch.cuda.synchronize()
+    return b
 
 
 def run_layer(cfg, inp, w, device="cuda"):

@@ -77,6 +77,45 @@ def test_validate_rejects_unknown_precision_and_bad_shared_counts():
     assert abi.moe_validate_config(cfg(E=64, k=15, n_shared=2)) == abi.MOE_ERR_UNSUPPORTED
 
 
+def test_drop_policy_and_layout_validation():
+    assert abi.moe_validate_config(cfg(capacity=16, drop_policy="gate")) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(drop_policy="gate")) == abi.MOE_OK          # dropless: nothing to select
+    assert abi.moe_validate_config(cfg(capacity=16, layout="padded")) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(capacity=0, layout="padded")) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(layout="padded")) == abi.MOE_ERR_UNSUPPORTED  # padded needs a capacity
+    assert abi.moe_validate_config(cfg(capacity=16, layout="padded", n_shared=1)) == abi.MOE_ERR_UNSUPPORTED
+    for field, bad in (("drop_policy", 2), ("layout", -1)):
+        c = cfg()
+        setattr(c, field, bad)
+        assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
+
+
+def test_rows_capacity_and_kernel_counts():
+    assert abi.moe_rows_capacity(cfg()) == 64 * 2
+    assert abi.moe_rows_capacity(cfg(n_shared=1)) == 64 * 3
+    assert abi.moe_rows_capacity(cfg(capacity=5)) == 64 * 2                 # packed: T*K whatever C is
+    assert abi.moe_rows_capacity(cfg(capacity=5, layout="padded")) == 8 * 5
+    assert abi.moe_rows_capacity(cfg(capacity=100, layout="padded")) == 8 * 100  # may exceed T*K
+    assert abi.moe_rows_capacity(cfg(capacity=0, layout="padded")) == 0
+    with pytest.raises(abi.MoeError):
+        abi.moe_rows_capacity(cfg(k=9))
+    assert abi.moe_kernels_per_forward(cfg()) == 9
+    assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate")) == 10
+    assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate", layout="padded")) == 11
+    assert abi.moe_kernels_per_forward(cfg(capacity=0, layout="padded")) == 8   # no rows: no expert GEMMs
+    assert abi.moe_kernels_per_forward(cfg(expert="identity", F=0)) == 7
+
+
+def test_padded_workspace_holds_n_times_c_rows():
+    big = cfg(capacity=100, layout="padded")     # 800 rows against T*K = 128
+    v = abi.moe_workspace_view()
+    base = 1 << 40
+    n = abi.moe_workspace_bytes(big)
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(big), base, n, ctypes.byref(v)) == 0
+    assert v.h - v.xperm >= 800 * 128 * 2 and base + n - v.out >= 800 * 128 * 4
+    assert v.map.drop_list - v.map.row_src >= 800 * 4
+
+
 def test_shared_experts_size_the_routing_arrays():
     base, shared = cfg(E=8, k=2), cfg(E=8, k=2, n_shared=1)
     vb, vs = abi.moe_workspace_view(), abi.moe_workspace_view()
@@ -129,7 +168,7 @@ def test_workspace_sizes_and_layout():
             assert view.xperm < view.h < view.out < base + fwd
             assert view.out + A * w.d * w.act_bytes <= base + fwd
         assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
-        assert abi.moe_kernels_per_forward(c) == (6 if w.expert == "identity" else 8)
+        assert abi.moe_kernels_per_forward(c) == (7 if w.expert == "identity" else 9)
 
 
 def test_entry_points_reject_bad_arguments_on_the_host():
@@ -150,10 +189,16 @@ def test_entry_points_reject_bad_arguments_on_the_host():
     # dispatch
     m = abi.moe_dispatch_map(*([A16] * 8))
     nbytes = abi.moe_dispatch_workspace_bytes(c)
-    assert lib.moe_dispatch(ref(c), A16, A16, ref(m), A16, A16, nbytes - 1, None) == abi.MOE_ERR_WORKSPACE
-    assert lib.moe_dispatch(ref(c), A16, A16, ref(m), MIS, A16, nbytes, None) == abi.MOE_ERR_ALIGN
+    assert lib.moe_dispatch(ref(c), A16, A16, None, ref(m), A16, A16, nbytes - 1, None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_dispatch(ref(c), A16, A16, None, ref(m), MIS, A16, nbytes, None) == abi.MOE_ERR_ALIGN
     m0 = abi.moe_dispatch_map(*([A16] * 7 + [None]))
-    assert lib.moe_dispatch(ref(c), A16, A16, ref(m0), A16, A16, nbytes, None) == abi.MOE_ERR_ARG
+    assert lib.moe_dispatch(ref(c), A16, A16, None, ref(m0), A16, A16, nbytes, None) == abi.MOE_ERR_ARG
+    # the gate drop policy with a capacity needs the gates
+    g = cfg(capacity=16, drop_policy="gate")
+    ng = abi.moe_dispatch_workspace_bytes(g)
+    assert ng >= nbytes + 64 * 2 * 4  # plus the per-expert assignment lists
+    assert lib.moe_dispatch(ref(g), A16, A16, None, ref(m), A16, A16, ng, None) == abi.MOE_ERR_ARG
+    assert lib.moe_dispatch_static(ref(g), A16, A16, None, ref(m), A16, None) == abi.MOE_ERR_ARG
     # expert ffn
     assert lib.moe_expert_ffn(ref(cfg(expert="identity", F=0)), A16, A16, A16, A16, A16, A16, A16, 256,
                               None) == abi.MOE_ERR_ARG

@@ -1,10 +1,13 @@
 """GPU parity: the CUDA path through the C ABI against the float64 CPU oracle.
 
-Stage-wise checks feed each oracle stage the GPU's own output of the previous stage
-(so a near-tie flip in the router cannot cascade), end-to-end checks run the whole
-layer from the original inputs and exclude only near-tie tokens. Reduced sizes span
-several tiles and ragged tails; the full workload sizes are checked on sampled
-experts and tokens in the launch configuration the benchmark times.
+Every oracle input comes from the seeded generators, never from the CUDA path:
+the router is checked on the original inputs; dispatch, expert FFN and combine
+each run on seeded synthetic inputs of their own (workloads.make_stage_inputs);
+the GPU's chained dispatch is compared with the oracle's dispatch of the oracle's
+routing where the two routings agree; end-to-end checks run the whole layer from
+the original inputs and exclude only near-tie tokens. Reduced sizes span several
+tiles and ragged tails; the full workload sizes are checked on sampled experts and
+tokens in the launch configuration the benchmark times.
 """
 import numpy as np
 import pytest
@@ -13,8 +16,9 @@ import torch
 from oracle import moe_oracle as orc
 from routing_dispatch_combine_moe_b300 import abi
 from routing_dispatch_combine_moe_b300 import workloads as wl
-from tests._gpu import (StageBuffers, check_close, check_combine, check_dispatch, check_ffn, check_route, cpu,
-                        half_ulp, rms, run_layer)
+from tests._gpu import (StageBuffers, WorkspaceMap, capacity_of, chain, check_chained_dispatch, check_close,
+                        check_combine, check_dispatch, check_ffn, check_route, cpu, gate_boundary_ties, half_ulp,
+                        oracle_dispatch, oracle_route, rms, run_layer)
 from tests._harness import expert_fn, f64, run_oracle
 
 pytestmark = pytest.mark.gpu
@@ -27,40 +31,41 @@ REDUCED = {
     "zipf_cf125": wl.scaled(W["zipf_cf125"], T=2048, d=512, F=384),
     "dsv3_full": wl.scaled(W["dsv3_full"], T=512, d=1024, F=256),
     "dsv3_decode": wl.scaled(W["dsv3_decode"], d=1024, F=256),
+    "zipf_gate_padded": wl.scaled(W["zipf_cf125"], T=2048, d=512, F=384, drop_policy="gate", layout="padded"),
 }
-
-
-def capacity_of(cfg):
-    return None if cfg.capacity < 0 else int(cfg.capacity)
 
 
 def stagewise(w, seed=0, inp=None):
     inp = wl.make_inputs(w, seed, device="cuda") if inp is None else inp
     cfg = abi.config_for(w)
+    cap = capacity_of(cfg)
+    st = wl.make_stage_inputs(w, seed, device="cuda", rows=abi.moe_rows_capacity(cfg))
     b = StageBuffers(w, cfg)
     b.route(inp)
     torch.cuda.synchronize()
     r = check_route(w, inp, b)
-    b.dispatch(inp)
-    d = check_dispatch(w, inp, b, capacity_of(cfg))
+    d = check_dispatch(w, inp, b, cap, st)
     assert b.dispatch_status() == 0
-    rows = int(d["offsets"][-1])
     ffn_err = None
-    out = b.xperm
     if w.expert != "identity":
-        b.ffn(inp)
-        ffn_err = check_ffn(w, inp, b, rows)
+        ffn_err = check_ffn(w, inp, b, st)
         assert b.ffn_status() == 0
-        out = b.out
-    b.combine(out)
-    comb_err = check_combine_on(w, b, out)
+    comb_err = check_combine(w, b, st)
     assert abi.moe_read_status(b.status.data_ptr()) == 0
-    return dict(inp=inp, cfg=cfg, bufs=b, route=r, dispatch=d, ffn_err=ffn_err, combine_err=comb_err)
+    c = chain(w, inp, cfg)
+    chained = check_chained_dispatch(w, inp, c, r, cap)
+    return dict(inp=inp, cfg=cfg, bufs=b, chain=c, route=r, dispatch=d, ffn_err=ffn_err, combine_err=comb_err,
+                chained=chained)
 
 
-def check_combine_on(w, b, out):
-    exact = orc.combine(f64(b.topk_gate), cpu(b.pos).numpy().astype(np.int64), f64(out), w.T, w.slots)
-    return check_close(b.y, exact, w.act, "combine", tol=1e-5)
+def layer_keep(w, ref, capacity):
+    """Tokens compared end to end: no near tie in the router, and under the gate
+    drop policy no gate at a keep cutoff."""
+    s, o = orc.near_tie_flags(ref["H"], w.k)
+    keep = ~(s | o)
+    if w.drop_policy == "gate":
+        keep &= ~gate_boundary_ties(w, orc.keep_topk(ref["H"], w.k), ref["G"][:, :w.k], capacity)
+    return keep
 
 
 @pytest.mark.parametrize("name", list(REDUCED))
@@ -69,7 +74,8 @@ def test_stagewise_parity(name):
     res = stagewise(w)
     print(f"\n{name}: near-ties={res['route']['near_ties']} flipped={res['route']['flipped']} "
           f"gate_err={res['route']['gate_err']:.2e} ffn_err/rms={res['ffn_err']} "
-          f"combine_err/rms={res['combine_err']:.2e} dropped={res['dispatch']['n_dropped']}")
+          f"combine_err/rms={res['combine_err']:.2e} dropped={res['dispatch']['n_dropped']} "
+          f"chained dispatch: {res['chained']}")
 
 
 @pytest.mark.parametrize("name", list(REDUCED))
@@ -80,8 +86,7 @@ def test_layer_forward_matches_oracle(name):
     y, ws, view, flags = run_layer(cfg, inp, w)
     assert flags == 0
     ref = run_oracle(w, inp)
-    s, o = orc.near_tie_flags(ref["H"], w.k)
-    keep = ~(s | o)
+    keep = layer_keep(w, ref, capacity_of(cfg))
     err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{name} layer y")
     print(f"\n{name}: layer max|err|/rms(y) = {err:.4f} (near-tie tokens excluded: {int((~keep).sum())})")
     if w.expert == "identity":
@@ -139,6 +144,18 @@ EDGE = [
     wl.Workload("split_h_relu", T=300, d=192, E=5, k=2, F=320, act="bf16", expert="relu", precision="split_h"),
     wl.Workload("split_h_ragged", T=333, d=136, E=12, k=3, F=192, act="bf16", expert="swiglu", D=4,
                 precision="split_h", capacity_factor="0.9"),
+    wl.Workload("gate_drops_ragged", T=333, d=136, E=12, k=3, F=200, act="bf16", expert="swiglu", D=4,
+                capacity_factor="0.75", drop_policy="gate", zipf_s=1.2),
+    wl.Workload("padded_token_order", T=300, d=128, E=8, k=2, F=128, act="bf16", expert="swiglu",
+                capacity_factor="1", layout="padded", zipf_s=1.2),
+    wl.Workload("padded_gate_f32", T=257, d=96, E=7, k=3, F=72, act="f32", expert="relu",
+                capacity_factor="1.25", drop_policy="gate", layout="padded", zipf_s=1.2),
+    wl.Workload("padded_zero_capacity", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu",
+                capacity_factor="0", layout="padded"),
+    wl.Workload("padded_cap_huge", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu",
+                capacity_factor="100", layout="padded", drop_policy="gate"),
+    wl.Workload("padded_identity_gate", T=500, d=256, E=16, k=4, F=0, act="bf16", expert="identity",
+                capacity_factor="0.5", D=4, layout="padded", drop_policy="gate"),
 ]
 
 
@@ -186,10 +203,9 @@ def test_edge_cases(w):
     inp, cfg = res["inp"], res["cfg"]
     y, ws, view, flags = run_layer(cfg, inp, w)
     assert flags == 0
-    assert torch.equal(y, res["bufs"].y), "layer and stage-wise calls must agree bit for bit"
+    assert torch.equal(y, res["chain"].y), "layer and chained stage calls must agree bit for bit"
     ref = run_oracle(w, inp)
-    s, o = orc.near_tie_flags(ref["H"], w.k)
-    keep = ~(s | o)
+    keep = layer_keep(w, ref, capacity_of(cfg))
     check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{w.name} layer y")
     if w.capacity_factor == "0":
         assert torch.count_nonzero(y) == 0
@@ -200,8 +216,9 @@ def test_all_tokens_to_one_expert_with_capacity():
     inp = wl.make_inputs(w, 5, device="cuda")
     inp["bias"] = torch.tensor([0, 0, 0, 1000.0, 0, 0, 0, 0], device="cuda")
     res = stagewise(w, inp=inp)
-    d = res["dispatch"]
-    assert d["counts_routed"][3] == 512 and d["counts_kept"][3] == 64 and d["n_dropped"] == 448
+    c = res["chain"]
+    assert res["chained"] == "exact"
+    assert int(c.counts_routed[3]) == 512 and int(c.counts_kept[3]) == 64 and int(c.n_dropped[0]) == 448
 
 
 def test_host_buffer_path_matches_device_path():
@@ -251,72 +268,62 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
     return y
 
 
-@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"])
+FULL = {n: W[n] for n in ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"]}
+FULL["zipf_gate_padded"] = wl.scaled(W["zipf_cf125"], drop_policy="gate", layout="padded")
+
+
+@pytest.mark.parametrize("name", list(FULL))
 def test_full_size_sampled(name):
-    w = W[name]
+    w = FULL[name]
     inp = wl.make_inputs(w, 0, device="cuda")
     cfg = abi.config_for(w)
+    cap = capacity_of(cfg)
     y, ws, view, flags = run_layer(cfg, inp, w)
     assert flags == 0
-    A = w.T * w.slots
-    base = ws.data_ptr()
-    ws_i32 = lambda ptr, n: ws[ptr - base:ptr - base + 4 * n].view(torch.int32).cpu().numpy()
-    ws_f32 = lambda ptr, n: ws[ptr - base:ptr - base + 4 * n].view(torch.float32).cpu().numpy()
+    m = WorkspaceMap(w, cfg, ws, view)
     # router: full oracle logits in float64
-    H = orc.router_logits(f64(inp["x"]), f64(inp["Wg"]), f64(inp.get("bias")))
-    idx_o = orc.keep_topk(H, w.k)
-    G_o = orc.kept_softmax(H, idx_o)
-    s, o = orc.near_tie_flags(H, w.k)
-    tie = s | o
-    idx_all = ws_i32(view.topk_idx, A).reshape(w.T, w.slots)
-    G_all = ws_f32(view.topk_gate, A).reshape(w.T, w.slots)
-    assert np.all(idx_all[:, w.k:] == w.E + np.arange(w.n_shared)) and np.all(G_all[:, w.k:] == 1.0)
-    idx_g, G_g = idx_all[:, :w.k], G_all[:, :w.k]
-    mism = (idx_g != idx_o).any(axis=1)
-    assert not (mism & ~tie).any()
-    assert np.abs(G_g[~mism] - G_o[~mism]).max() <= 2e-6
-    # dispatch on the GPU's own ids: bit-exact
-    cap = capacity_of(cfg)
-    d = orc.dispatch(idx_all.astype(np.int64), w.n_experts, cap, w.D, capped_experts=w.E)
-    np.testing.assert_array_equal(ws_i32(view.counts_routed, w.n_experts), d["counts_routed"])
-    np.testing.assert_array_equal(ws_i32(view.offsets, w.n_experts + 1), d["offsets"])
-    np.testing.assert_array_equal(ws_i32(view.rank_offsets, w.D + 1), d["rank_offsets"])
-    np.testing.assert_array_equal(ws_i32(view.pos, A), d["pos"])
-    rows = int(d["offsets"][-1])
-    np.testing.assert_array_equal(ws_i32(view.row_src, A)[:rows], d["row_src"])
-    assert int(ws_i32(view.n_dropped, 1)[0]) == d["n_dropped"]
-    xperm = ws[view.xperm - base:view.xperm - base + rows * w.d * 2].view(torch.bfloat16).view(rows, w.d)
-    src = torch.from_numpy(d["row_src"] // w.slots).cuda()
-    assert torch.equal(xperm, inp["x"][src])
+    r = check_route(w, inp, m)
+    # dispatch of the GPU's routing: bit-exact against the oracle's where the routings agree
+    how = check_chained_dispatch(w, inp, m, r, cap)
+    d = oracle_dispatch(w, r["idx_full"], r["G_full"], cap)
     if w.expert == "identity":
         assert torch.equal(y, inp["x"])
         return
-    # expert outputs of a few whole experts (largest, smallest non-empty, two more)
-    odt = abi.out_dtype(cfg)
-    osz = torch.tensor([], dtype=odt).element_size()
-    out = ws[view.out - base:view.out - base + rows * w.d * osz].view(odt).view(rows, w.d)
-    out_act = "f32" if odt == torch.float32 else "bf16"
-    counts = d["counts_kept"]
-    nz = np.nonzero(counts)[0]
-    pick = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(nz[len(nz) // 2]), int(nz[0])})
-    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
-    worst_ffn = 0.0
-    for e in pick:
-        lo, hi = int(d["offsets"][e]), int(d["offsets"][e + 1])
-        worst_ffn = max(worst_ffn, check_close(out[lo:hi], fn(e, f64(xperm[lo:hi])), out_act, f"expert {e}",
-                                               tol=2e-2))
-    # end to end on sampled tokens (no near ties), from the oracle's own routing and dispatch
+    # expert outputs of a few whole experts (largest, smallest non-empty, two more); with
+    # an exact dispatch their input rows are x at the oracle's row sources
+    worst_ffn = None
+    if how == "exact":
+        counts = d["counts_kept"]
+        nz = np.nonzero(counts)[0]
+        pick = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(nz[len(nz) // 2]),
+                       int(nz[0])})
+        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
+        worst_ffn = 0.0
+        for e in pick:
+            lo = int(d["offsets"][e])
+            hi = lo + int(counts[e])
+            src = torch.from_numpy(d["row_src"][lo:hi] // w.slots).cuda()
+            worst_ffn = max(worst_ffn, check_close(m.out[lo:hi], fn(e, f64(inp["x"][src])), m.out_act,
+                                                   f"expert {e}", tol=2e-2))
+    # end to end on sampled tokens from the oracle's own routing and dispatch: no near
+    # tie, no gate at a keep cutoff, and (with a capacity) no expert shared with a
+    # token whose routing flipped
+    ok = ~r["tie"]
+    if w.drop_policy == "gate":
+        ok &= ~gate_boundary_ties(w, r["idx"], r["G"], cap)
+    idx_g = cpu(m.topk_idx).numpy()[:, :w.k]
+    flipped = (idx_g != r["idx"]).any(axis=1)
+    if flipped.any() and cap is not None:
+        touched = set(r["idx"][flipped].ravel().tolist()) | set(idx_g[flipped].ravel().tolist())
+        ok &= ~np.isin(r["idx"], sorted(touched)).any(axis=1)
+    ok &= ~flipped
     rng = np.random.default_rng(0)
-    cand = np.nonzero(~tie)[0]
+    cand = np.nonzero(ok)[0]
     tokens = sorted(rng.choice(cand, size=min(8, cand.size), replace=False).tolist())
-    # sampled tokens have no near tie, so their ids and gates equal the GPU's; the drop
-    # decisions come from the (bit-exact) dispatch of the GPU's ids
-    idx_full = np.concatenate([idx_o, np.broadcast_to(w.E + np.arange(w.n_shared), (w.T, w.n_shared))], axis=1)
-    G_full = np.concatenate([G_o, np.ones((w.T, w.n_shared))], axis=1)
-    y_s = _sampled_y(w, inp, dict(idx=idx_full, G=G_full), d, tokens)
+    y_s = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
     err = check_close(y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y")
-    print(f"\n{name}: near-ties={int(tie.sum())} ffn_err/rms={worst_ffn:.4f} sampled y err/rms={err:.4f} "
-          f"dropped={d['n_dropped']}")
+    print(f"\n{name}: near-ties={r['near_ties']} flipped={r['flipped']} dispatch={how} ffn_err/rms={worst_ffn} "
+          f"sampled y err/rms={err:.4f} dropped={d['n_dropped']}")
 
 
 @pytest.mark.parametrize("name", ["mixtral_bf16", "zipf_cf125", "tiny_f32"])

@@ -26,11 +26,11 @@ def _run_both(w, seed):
     ref.route(inp)
     ref.dispatch(inp)
     got = StageBuffers(w, cfg)
-    abi.moe_dispatch_static(cfg, inp["x"], ref.topk_idx, got.dmap(), got.xperm)
+    abi.moe_dispatch_static(cfg, inp["x"], ref.topk_idx, got.dmap(), got.xperm, topk_gate=ref.topk_gate)
     torch.cuda.synchronize()
     for f in FIELDS:
         assert torch.equal(getattr(got, f), getattr(ref, f)), f
-    rows = int(cpu(ref.offsets)[-1])
+    rows = ref.rows if w.layout == "padded" else int(cpu(ref.offsets)[-1])
     nd = int(cpu(ref.n_dropped)[0])
     assert torch.equal(got.row_src[:rows], ref.row_src[:rows])
     assert torch.equal(got.drop_list[:nd], ref.drop_list[:nd])
@@ -45,6 +45,14 @@ def test_static_scratch_dispatch_matches_workspace_dispatch_twice():
     b = _run_both(wl.Workload("cap", T=3000, d=256, E=64, k=2, F=0, act="bf16", expert="identity",
                               capacity_factor="1", zipf_s=1.2, D=4), seed=12)
     assert a[0] == 2048 * 8 and b[1] > 0
+
+
+def test_static_scratch_gate_drops_into_padded_rows():
+    # the gate drop policy uses the extra per-expert list in the static array
+    _, nd = _run_both(wl.Workload("gate_pad", T=3000, d=256, E=64, k=2, F=0, act="bf16", expert="identity",
+                                  capacity_factor="1", zipf_s=1.2, D=4, drop_policy="gate", layout="padded"),
+                      seed=13)
+    assert nd > 0
 
 
 def test_static_scratch_rejects_configs_beyond_its_size():
