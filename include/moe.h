@@ -122,7 +122,9 @@ typedef struct moe_config {
 typedef struct moe_dispatch_map {
     int32_t* counts_routed; /* [N]   assignments routed to each expert */
     int32_t* counts_kept;   /* [N]   min(counts_routed, capacity) (shared experts: all T) */
-    int32_t* offsets;       /* [N+1] exclusive scan of counts_kept; rows of expert e are [offsets[e], offsets[e+1]) */
+    int32_t* offsets;       /* [N+1] rows of expert e are [offsets[e], offsets[e+1]): the exclusive scan of
+                             * counts_kept (packed), or e * capacity (padded; the segment's first
+                             * counts_kept[e] rows hold assignments, the rest are padding) */
     int32_t* rank_offsets;  /* [D+1] offsets[r*E/D]: virtual rank r's send chunk is [rank_offsets[r], rank_offsets[r+1]) */
     int32_t* pos;           /* [T*K] row of assignment t*K+j, or -1 if it was dropped */
     int32_t* row_src;       /* [rows] assignment t*K+j held by each row (-1 on padding rows); entries
@@ -139,7 +141,9 @@ typedef struct moe_workspace_view {
     moe_dispatch_map map;
     void* xperm;         /* [rows, d] act: dispatched rows (the dispatch "send buffer") */
     void* h;             /* expert hidden activations, see moe_expert_ffn (NULL for identity) */
-    void* out;           /* expert outputs, see moe_expert_ffn (aliases xperm for identity) */
+    void* out;           /* expert outputs, see moe_expert_ffn (aliases xperm for identity); in the
+                          * padded layout the forward computes kept rows only and leaves the
+                          * padding rows of out unwritten */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */

@@ -305,19 +305,20 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* __re
 }
 
 // Padded layout: rows [offsets[e] + kept, offsets[e] + capacity) of expert e are
-// zeroed and marked as holding no assignment.
+// zeroed and marked as holding no assignment. Grid (ceil(capacity / 8), E): one
+// warp per row, 16-byte stores.
 __global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict__ counts_kept,
                                                        const int32_t* __restrict__ offsets, int capacity,
                                                        uint4* __restrict__ xperm, int vec_per_row,
                                                        int32_t* __restrict__ row_src) {
-    const int e = blockIdx.x;
-    const int r0 = offsets[e] + counts_kept[e], r1 = offsets[e] + capacity;
+    const int e = blockIdx.y, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);  // row within the segment
+    if (i >= capacity || i < counts_kept[e]) return;
+    const int64_t r = int64_t(offsets[e]) + i;
+    uint4* row = xperm + r * vec_per_row;
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int r = r0; r < r1; ++r) {
-        uint4* row = xperm + size_t(r) * vec_per_row;
-        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) row[v] = z;
-        if (threadIdx.x == 0) row_src[r] = -1;
-    }
+    for (int v = lane; v < vec_per_row; v += 32) row[v] = z;
+    if (lane == 0) row_src[r] = -1;
 }
 
 // One warp per token: x[t] is read once and written to each of its kept rows.
@@ -378,8 +379,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
         select_kernel<<<a.E, kSelThreads, 0, stream>>>(a.elist, a.routed_offsets, a.counts_routed, a.counts_kept,
                                                        a.offsets, a.drop_offsets, a.topk_gate, a.pos, a.row_src,
                                                        a.drop_list);
-    if (padded)
-        pad_rows_kernel<<<a.E, 256, 0, stream>>>(a.counts_kept, a.offsets, int(a.capacity),
+    if (padded && a.capacity > 0)
+        pad_rows_kernel<<<dim3(unsigned((a.capacity + 7) / 8), unsigned(a.E)), 256, 0, stream>>>(
+            a.counts_kept, a.offsets, int(a.capacity),
                                                  static_cast<uint4*>(a.xperm), vec_per_row, a.row_src);
     gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
                                                       static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, rows);

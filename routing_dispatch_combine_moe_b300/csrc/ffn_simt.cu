@@ -23,6 +23,7 @@ struct SimtParams {
     const float* B;          // [E*R, K]
     float* C;                // [rows, ldc]
     const int32_t* offsets;  // [E+1]
+    const int32_t* counts;   // [E] rows used at the start of each segment, or null (all of it)
     int E, K, R, F, ldc, n_out, n_tiles;
 };
 
@@ -30,6 +31,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads) grouped_sgemm_kernel(const SimtParams p) {
     constexpr int NB = (MODE == kSwiGLU) ? 2 : 1;
     __shared__ int off[MOE_MAX_E + 1];
+    __shared__ int end[MOE_MAX_E];
     __shared__ int tile[MOE_MAX_E + 1];
     __shared__ __align__(16) float As[TK][TM + 4];
     __shared__ __align__(16) float Bs[NB][TK][TN + 4];
@@ -40,10 +42,18 @@ __global__ void __launch_bounds__(kThreads) grouped_sgemm_kernel(const SimtParam
         for (int e0 = 0; e0 <= E; e0 += 32)
             if (e0 + lane <= E) off[e0 + lane] = __ldg(p.offsets + e0 + lane);
         __syncwarp();
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            if (e < E) {
+                const int seg = off[e + 1] - off[e];
+                end[e] = off[e] + (p.counts ? min(max(__ldg(p.counts + e), 0), seg) : seg);
+            }
+        }
+        __syncwarp();
         int run = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
             const int e = e0 + lane;
-            const int v = e < E ? (off[e + 1] - off[e] + TM - 1) / TM : 0;
+            const int v = e < E ? (end[e] - off[e] + TM - 1) / TM : 0;
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -67,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) grouped_sgemm_kernel(const SimtParam
     const int local = t - tile[e] * p.n_tiles;
     const int mte = tile[e + 1] - tile[e];
     const int nt = local / mte, mt = local - nt * mte;
-    const int m0 = off[e] + mt * TM, m_end = off[e + 1];
+    const int m0 = off[e] + mt * TM, m_end = end[e];
     const int n0 = nt * TN;
 
     const int tx = tid % 16, ty = tid / 16;  // 4 output columns x 4 rows each
@@ -146,6 +156,7 @@ cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t stream, cudaEvent_t m
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;
     SimtParams p{};
     p.offsets = a.offsets;
+    p.counts = a.counts;
     p.E = a.E;
     p.F = a.F;
     // Up projection.

@@ -71,6 +71,7 @@ struct Cfg {
 
 struct Params {
     const int32_t* offsets;  // [E+1]
+    const int32_t* counts;   // [E] rows used at the start of each segment, or null (all of it)
     void* C;                 // output, row stride ldc (bf16, or fp32 for a kOutF32 down projection)
     int ldc;                 // elements
     int n_out;               // valid output columns
@@ -93,6 +94,7 @@ struct Smem {
     uint32_t tmem_base;
     int abort_flag;
     int off[MOE_MAX_E + 1];
+    int end[MOE_MAX_E];  // off[e] + rows of expert e that are computed
     int tile[MOE_MAX_E + 1];
 };
 
@@ -273,10 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             if (e <= E) S.off[e] = __ldg(p.offsets + e);
         }
         __syncwarp();
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            if (e < E) {
+                const int seg = S.off[e + 1] - S.off[e];
+                S.end[e] = S.off[e] + (p.counts ? min(max(__ldg(p.counts + e), 0), seg) : seg);
+            }
+        }
+        __syncwarp();
         int run = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
             const int e = e0 + lane;
-            const int v = e < E ? (S.off[e + 1] - S.off[e] + C::TILE_M - 1) / C::TILE_M : 0;
+            const int v = e < E ? (S.end[e] - S.off[e] + C::TILE_M - 1) / C::TILE_M : 0;
             int incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -403,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             if (!ok) break;
             tc_fence_after();
             const int row = S.off[e] + mt * C::TILE_M + int(rank) * 128 + r_in_tile;
-            const bool row_ok = row < S.off[e + 1];
+            const bool row_ok = row < S.end[e];
             const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + acc * MMA_N;
             epilogue_tile<MODE, OUT>(p, tbase, row, row_ok, nt);
             tc_fence_before();
@@ -422,6 +432,314 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         tc_fence_after();
         if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ swapped operands
+// SM pairs (cta_group::2, M = 256) with the weights as the MMA's A operand and the
+// dispatched rows as B. The 256 rows of a pair tile are output features: each SM
+// loads 128 weight rows (SwiGLU: 64 gate rows and the 64 matching up rows). The N
+// columns are up to 256 consecutive rows of one expert, N rounded up to a multiple
+// of 32 on the expert's last tile, split N/2 + N/2 between the two SMs. An expert's
+// row count then costs at most 31 idle columns, where the row-major pair tile costs up
+// to 255 idle rows, and each SM still lands 32 KB per stage (six stages). The
+// accumulator holds features on TMEM lanes and rows on columns, so each epilogue
+// thread owns one feature and stores it for 32 rows at a time: a warp writes 32
+// consecutive features of one row per store. For SwiGLU, warps holding up values
+// (lanes 64-127) pass them through shared memory to the warps holding the matching
+// gate values (lanes 0-63).
+constexpr int SW_STAGES = 6;
+constexpr int SW_A_STAGE = 128 * BK * 2;          // 16 KB: 128 weight rows per SM
+constexpr int SW_B_BIG = 128 * BK * 2;            // 16 KB: box of 128 dispatched rows
+constexpr int SW_B_SMALL = 16 * BK * 2;           // 2 KB: box of 16 rows, for N <= 32
+constexpr int SW_STAGE_SMEM = SW_A_STAGE + SW_B_BIG;
+constexpr int SW_TILE_N = 256;
+
+struct SwapXchg {
+    float v[2][32][33];  // up values for 32 rows x 32 features, per gate warp
+};
+
+constexpr size_t swap_smem_bytes() {
+    return 1024 + size_t(SW_STAGES) * SW_STAGE_SMEM + sizeof(Smem<SW_STAGES>) + sizeof(SwapXchg);
+}
+
+// Named barrier 1 over the four epilogue warps (128 threads); the second form also
+// returns whether `v` holds in every one of them.
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_bar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        " .reg .pred p, q;\n"
+        " setp.ne.u32 p, %1, 0;\n"
+        " bar.red.and.pred q, 1, 128, p;\n"
+        " selp.u32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(uint32_t(v))
+        : "memory");
+    return r != 0;
+}
+
+// Token-row tile mt of expert e: first row, rows used, and N. A pair MMA takes N as a
+// multiple of 32 in [32, 256] (each SM supplies N/2 rows, a multiple of 16).
+__device__ __forceinline__ void swap_tile_rows(const int* off, const int* end, int e, int mt, int& start, int& len,
+                                               int& n) {
+    start = off[e] + mt * SW_TILE_N;
+    len = min(SW_TILE_N, end[e] - start);
+    n = (len + 31) & ~31;
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_one(const Params& p, int row, int f, float v) {
+    if constexpr (OUT == kOutF32) {
+        static_cast<float*>(p.C)[size_t(row) * p.ldc + f] = v;
+    } else {
+        uint16_t* c = static_cast<uint16_t*>(p.C) + size_t(row) * p.ldc;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        if constexpr (OUT == kOutHiLo) {
+            const int col = 128 * (f >> 6) + (f & 63);
+            c[col] = __bfloat16_as_ushort(hi);
+            c[col + 64] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+        } else {
+            c[f] = __bfloat16_as_ushort(hi);
+        }
+    }
+}
+
+template <int MODE, int OUT>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap mapW,
+                                                                        const __grid_constant__ CUtensorMap mapX,
+                                                                        const __grid_constant__ CUtensorMap mapX16,
+                                                                        const Params p) {
+    constexpr int STAGES = SW_STAGES;
+    constexpr int EPI_WARPS_TOTAL = 8;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = base;
+    unsigned char* sB = base + STAGES * SW_A_STAGE;
+    Smem<STAGES>& S = *reinterpret_cast<Smem<STAGES>*>(base + STAGES * SW_STAGE_SMEM);
+    SwapXchg& X = *reinterpret_cast<SwapXchg*>(base + STAGES * SW_STAGE_SMEM + sizeof(Smem<STAGES>));
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = p.E;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int unit = int(blockIdx.x >> 1);
+    const int n_units = int(gridDim.x >> 1);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&S.tmem_full[a], 1);
+            mbar_init(&S.tmem_empty[a], EPI_WARPS_TOTAL);
+        }
+        mbar_init(&S.mma_done, 1);
+        S.abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&mapW);
+        tma_prefetch_desc(&mapX);
+        tma_prefetch_desc(&mapX16);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    if (warp == 2) {
+        for (int e0 = 0; e0 <= E; e0 += 32) {
+            const int e = e0 + lane;
+            if (e <= E) S.off[e] = __ldg(p.offsets + e);
+        }
+        __syncwarp();
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            if (e < E) {
+                const int seg = S.off[e + 1] - S.off[e];
+                S.end[e] = S.off[e] + (p.counts ? min(max(__ldg(p.counts + e), 0), seg) : seg);
+            }
+        }
+        __syncwarp();
+        int run = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int v = e < E ? (S.end[e] - S.off[e] + SW_TILE_N - 1) / SW_TILE_N : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            if (e < E) S.tile[e] = run + incl - v;
+            run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) S.tile[E] = run;
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+
+    const uint32_t tmem_base = S.tmem_base;
+    const int total = S.tile[E] * p.n_tiles;
+    const int nkb = (p.K + BK - 1) / BK;
+    volatile int* abort_flag = &S.abort_flag;
+    const uint32_t full_base = mapa_shared(smem_addr(&S.full[0]), 0);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t armed_mask = 0, armed_par = 0;
+            // An expert's rows are re-read by every feature tile: keep them in L2.
+            const uint64_t pol_x = l2_policy_evict_last();
+            for (int t = unit; t < total; t += n_units) {
+                int e, mt, nt, start, len, n;
+                decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
+                swap_tile_rows(S.off, S.end, e, mt, start, len, n);
+                const bool small = n <= 32;
+                const int xrow = start + int(rank) * (n >> 1);
+                const uint32_t stage_tx = uint32_t(SW_A_STAGE + (small ? SW_B_SMALL : SW_B_BIG));
+                int w0, w1 = 0;
+                if (MODE == kSwiGLU) {
+                    w0 = e * p.R + nt * 128 + int(rank) * 64;
+                    w1 = w0 + p.F;
+                } else {
+                    w0 = e * p.R + nt * 256 + int(rank) * 128;
+                }
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    const int kW = (kb >> p.b_k_shift) * BK;
+                    const int kX = kb * BK;
+                    unsigned char* a_dst = sA + s * SW_A_STAGE;
+                    unsigned char* b_dst = sB + s * SW_B_BIG;
+                    const uint32_t bar = full_base + uint32_t(s) * 8u;
+                    if (leader) mbar_arrive_expect_tx(&S.full[s], 2 * stage_tx);
+                    if (MODE == kSwiGLU) {
+                        tma_load_2d_pair(a_dst, &mapW, bar, kW, w0);
+                        tma_load_2d_pair(a_dst + SW_A_STAGE / 2, &mapW, bar, kW, w1);
+                    } else {
+                        tma_load_2d_pair(a_dst, &mapW, bar, kW, w0);
+                    }
+                    tma_load_2d_pair_hint(b_dst, small ? &mapX16 : &mapX, bar, kX, xrow, pol_x);
+                    armed_mask |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            if (leader)
+                for (int q = 0; q < STAGES; ++q)
+                    if (armed_mask & (1u << q)) drain_wait(&S.full[q], (armed_par >> q) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            int i = 0;
+            for (int t = unit; t < total; t += n_units, ++i) {
+                int e, mt, nt, start, len, n;
+                decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
+                swap_tile_rows(S.off, S.end, e, mt, start, len, n);
+                const uint32_t idesc = idesc_bf16_f32(256, uint32_t(n));
+                const int acc = i & 1;
+                const uint32_t aph = (i >> 1) & 1;
+                if (!mbar_wait(&S.tmem_empty[acc], aph ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * SW_TILE_N;
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(&S.full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * SW_A_STAGE));
+                    const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * SW_B_BIG));
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks)
+                        umma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+                    umma_commit_pair_multicast(&S.empty[s], 0x3);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair_multicast(&S.tmem_full[acc], 0x3);
+            }
+            umma_commit_pair_multicast(&S.mma_done, 0x1);
+            drain_wait(&S.mma_done, 0);
+        }
+    } else {
+        // Epilogue: warps 2..5 own TMEM lane quarters q = warp % 4 (features of this SM).
+        const int q = warp & 3;
+        const uint32_t empty_base = mapa_shared(smem_addr(&S.tmem_empty[0]), 0);
+        int i = 0;
+        for (int t = unit; t < total; t += n_units, ++i) {
+            int e, mt, nt, start, len, n;
+            decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
+            swap_tile_rows(S.off, S.end, e, mt, start, len, n);
+            const int acc = i & 1;
+            const uint32_t aph = (i >> 1) & 1;
+            bool ok = mbar_wait(&S.tmem_full[acc], aph, abort_flag, p.status);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            // All four epilogue warps must agree before the shared-memory hand-off below.
+            if (MODE == kSwiGLU) ok = epi_bar_and(ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + acc * SW_TILE_N;
+            if (MODE == kSwiGLU) {
+                const int f = nt * 128 + int(rank) * 64 + (q & 1) * 32 + lane;  // feature in [0, F)
+#pragma unroll 1
+                for (int c0 = 0; c0 < n; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c0, v);
+                    tmem_ld_wait();
+                    if (q >= 2) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) X.v[q - 2][j][lane] = __uint_as_float(v[j]);
+                    }
+                    epi_bar_sync();
+                    if (q < 2) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int row = start + c0 + j;
+                            if (c0 + j < len && f < p.n_out)
+                                store_one<OUT>(p, row, f, silu_f(__uint_as_float(v[j])) * X.v[q][j][lane]);
+                        }
+                    }
+                    epi_bar_sync();
+                }
+            } else {
+                const int f = nt * 256 + int(rank) * 128 + q * 32 + lane;
+#pragma unroll 1
+                for (int c0 = 0; c0 < n; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c0, v);
+                    tmem_ld_wait();
+                    if (f < p.n_out) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (c0 + j < len) {
+                                float x = __uint_as_float(v[j]);
+                                if (MODE == kReLU) x = fmaxf(x, 0.f);
+                                store_one<OUT>(p, start + c0 + j, f, x);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(empty_base + uint32_t(acc) * 8u);
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -498,18 +816,21 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const Pa
     }
 }
 
-// Whether a projection runs on SM pairs: MOE_GEMM_PAIR=0/1 forces it. Otherwise pairs
-// are used when experts average at least 1024 rows: a pair keeps the tensor pipe
-// about 88% busy against about 70% for one SM (each SM reads half the B tile from
-// shared memory), but an expert whose rows end inside a 256-row pair tile leaves up
-// to 128 rows of one SM idle, which costs up to ~12% at 512 rows per expert.
-bool use_pairs(int64_t rows_max, int E) {
+enum Variant : int { kOneSM = 0, kPairRows = 1, kPairSwap = 2 };
+
+// Which kernel runs a projection; MOE_GEMM_PAIR=0/1/2 forces one (read once per
+// process). One SM per 128x256 tile keeps the tensor pipe about 70% busy: each SM
+// lands 48 KB per k-block and four stages cover little load latency. SM pairs land
+// 32 KB per SM and keep it about 88% busy, but a 256-row tile that starts near an
+// expert's end leaves up to 255 rows idle, while the swapped pair tile (features x
+// rows) leaves at most 31 idle columns per expert.
+int gemm_variant(int64_t rows_max, int E) {
     static int forced = [] {
         const char* v = getenv("MOE_GEMM_PAIR");
         return v ? atoi(v) : -1;
     }();
-    if (forced >= 0) return forced != 0;
-    return rows_max >= int64_t(E) * 1024;
+    if (forced >= 0 && forced <= 2) return forced;
+    return rows_max >= int64_t(E) * 1024 ? kPairRows : kOneSM;
 }
 
 int grid_for(int64_t rows_max, int E, int n_tiles, bool pair) {
@@ -520,6 +841,42 @@ int grid_for(int64_t rows_max, int E, int n_tiles, bool pair) {
     int64_t g = upper < sms ? upper : sms;
     if (pair) g = (g + 1) & ~int64_t(1);
     return int(g > 0 ? g : (pair ? 2 : 1));
+}
+
+template <int MODE, int OUT>
+cudaError_t launch_swap(const CUtensorMap& mW, const CUtensorMap& mX, const CUtensorMap& mX16, const Params& p,
+                        int64_t rows_max, int E, cudaStream_t stream) {
+    auto kern = grouped_gemm_swap_kernel<MODE, OUT>;
+    constexpr size_t smem = swap_smem_bytes();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int64_t tiles = ((rows_max + SW_TILE_N - 1) / SW_TILE_N + E) * int64_t(p.n_tiles);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Persistent grid: never more pairs than can be resident at once.
+    static int max_clusters = -1;
+    if (max_clusters < 0) {
+        cfg.gridDim = dim3(2);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = device_sm_count() / 2;
+        max_clusters = n;
+    }
+    const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
+    cfg.gridDim = dim3(unsigned(2 * (pairs > 0 ? pairs : 1)));
+    return cudaLaunchKernelEx(&cfg, kern, mW, mX, mX16, p);
 }
 
 template <int MODE, int OUT>
@@ -536,12 +893,15 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     const int64_t rows_max = a.rows;
     const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
     const bool f32_out = a.precision != MOE_PRECISION_BF16;
-    const bool pair = use_pairs(rows_max, a.E);
+    const int variant = gemm_variant(rows_max, a.E);
+    const bool pair = variant == kPairRows;
+    const bool swap = variant == kPairSwap;
     const uint32_t b_rows = pair ? MMA_N / 2 : MMA_N;  // rows of one B box
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mX16;
     cudaError_t err;
     Params p{};
     p.offsets = a.offsets;
+    p.counts = a.counts;
     p.E = a.E;
     p.status = a.status;
     p.F = a.F;
@@ -549,21 +909,36 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     // Up projection: A = xperm [rows, d]; B = W13 [E*R, d]; C = h.
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;
     const int R = swiglu ? 2 * a.F : a.F;
-    if ((err = make_map(&mA, a.xperm, a.d, rows_max, 128)) != cudaSuccess) return err;
-    if ((err = make_map(&mB, a.W13, a.d, uint64_t(a.E) * R, swiglu ? MMA_N / 2 : b_rows)) != cudaSuccess) return err;
     p.C = a.h;
     p.ldc = split_h ? 2 * a.F : a.F;
     p.n_out = a.F;
     p.K = a.d;
     p.b_k_shift = 0;
     p.R = R;
-    p.n_tiles = swiglu ? (a.F + MMA_N / 2 - 1) / (MMA_N / 2) : (a.F + MMA_N - 1) / MMA_N;
-    if (swiglu)
-        err = split_h ? launch_mode<kSwiGLU, kOutHiLo>(mA, mB, p, rows_max, a.E, pair, stream)
-                      : launch_mode<kSwiGLU, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
-    else
-        err = split_h ? launch_mode<kReLU, kOutHiLo>(mA, mB, p, rows_max, a.E, pair, stream)
-                      : launch_mode<kReLU, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
+    if (swap) {
+        // weights as the MMA's A operand: 64-row boxes (gate | up halves) or 128-row boxes
+        if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128)) != cudaSuccess) return err;
+        if ((err = make_map(&mB, a.xperm, a.d, rows_max, 128)) != cudaSuccess) return err;
+        if ((err = make_map(&mX16, a.xperm, a.d, rows_max, 16)) != cudaSuccess) return err;
+        p.n_tiles = swiglu ? (a.F + 127) / 128 : (a.F + 255) / 256;
+        if (swiglu)
+            err = split_h ? launch_swap<kSwiGLU, kOutHiLo>(mA, mB, mX16, p, rows_max, a.E, stream)
+                          : launch_swap<kSwiGLU, kOutBF16>(mA, mB, mX16, p, rows_max, a.E, stream);
+        else
+            err = split_h ? launch_swap<kReLU, kOutHiLo>(mA, mB, mX16, p, rows_max, a.E, stream)
+                          : launch_swap<kReLU, kOutBF16>(mA, mB, mX16, p, rows_max, a.E, stream);
+    } else {
+        if ((err = make_map(&mA, a.xperm, a.d, rows_max, 128)) != cudaSuccess) return err;
+        if ((err = make_map(&mB, a.W13, a.d, uint64_t(a.E) * R, swiglu ? MMA_N / 2 : b_rows)) != cudaSuccess)
+            return err;
+        p.n_tiles = swiglu ? (a.F + MMA_N / 2 - 1) / (MMA_N / 2) : (a.F + MMA_N - 1) / MMA_N;
+        if (swiglu)
+            err = split_h ? launch_mode<kSwiGLU, kOutHiLo>(mA, mB, p, rows_max, a.E, pair, stream)
+                          : launch_mode<kSwiGLU, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
+        else
+            err = split_h ? launch_mode<kReLU, kOutHiLo>(mA, mB, p, rows_max, a.E, pair, stream)
+                          : launch_mode<kReLU, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
+    }
     if (err != cudaSuccess) return err;
     if (mid_event) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -575,8 +950,6 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
 
     // Down projection: A = h [rows, F] (split: [rows, 2F] hi|lo blocks); B = W2 [E*d, F].
     const int kA = split_h ? 2 * a.F : a.F;
-    if ((err = make_map(&mA, a.h, kA, rows_max, 128)) != cudaSuccess) return err;
-    if ((err = make_map(&mB, a.W2, a.F, uint64_t(a.E) * a.d, b_rows)) != cudaSuccess) return err;
     p.C = a.out;
     p.ldc = a.d;
     p.n_out = a.d;
@@ -584,6 +957,15 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.b_k_shift = split_h ? 1 : 0;
     p.R = a.d;
     p.n_tiles = (a.d + MMA_N - 1) / MMA_N;
+    if (swap) {
+        if ((err = make_map(&mA, a.W2, a.F, uint64_t(a.E) * a.d, 128)) != cudaSuccess) return err;
+        if ((err = make_map(&mB, a.h, kA, rows_max, 128)) != cudaSuccess) return err;
+        if ((err = make_map(&mX16, a.h, kA, rows_max, 16)) != cudaSuccess) return err;
+        return f32_out ? launch_swap<kPlain, kOutF32>(mA, mB, mX16, p, rows_max, a.E, stream)
+                       : launch_swap<kPlain, kOutBF16>(mA, mB, mX16, p, rows_max, a.E, stream);
+    }
+    if ((err = make_map(&mA, a.h, kA, rows_max, 128)) != cudaSuccess) return err;
+    if ((err = make_map(&mB, a.W2, a.F, uint64_t(a.E) * a.d, b_rows)) != cudaSuccess) return err;
     return f32_out ? launch_mode<kPlain, kOutF32>(mA, mB, p, rows_max, a.E, pair, stream)
                    : launch_mode<kPlain, kOutBF16>(mA, mB, p, rows_max, a.E, pair, stream);
 }

@@ -18,12 +18,12 @@ inline int dispatch_blocks(int64_t assignments) {
     return int((assignments + kDispatchBlock - 1) / kDispatchBlock);
 }
 
-// Router. The logits are summed from up to route_max_slices(E) split-K partials
+// Router. The logits are summed from up to route_max_slices(T, E) split-K partials
 // held in `scratch`, whose size depends only on T and E.
-int route_max_slices(int E);
+int route_max_slices(int T, int E);
 int route_k_slices(int T, int d, int E);
 inline size_t route_scratch_bytes_max(int T, int E) {
-    return size_t(route_max_slices(E)) * size_t(T) * size_t(E) * sizeof(float);
+    return size_t(route_max_slices(T, E)) * size_t(T) * size_t(E) * sizeof(float);
 }
 // topk_idx / topk_gate have k + n_shared slots per token; the shared slots hold
 // experts E..E+n_shared-1 with gate 1.
@@ -72,6 +72,7 @@ struct FfnArgs {
     int precision;  // MOE_PRECISION_*
     const void* xperm;
     const int32_t* offsets;
+    const int32_t* counts;  // [E] rows computed at the start of each segment, or null (whole segments)
     const void* W13;
     const void* W2;
     void* h;

@@ -202,8 +202,8 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const f
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch");
 }
 
-int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const void* W13, const void* W2, void* h,
-            void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
+int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const int32_t* counts, const void* W13,
+            const void* W2, void* h, void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
     FfnArgs a{};
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.F = c->F;
     a.rows = rows_cap(c);
@@ -212,6 +212,7 @@ int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, cons
     a.precision = c->precision;
     a.xperm = xperm;
     a.offsets = offsets;
+    a.counts = counts;
     a.W13 = W13;
     a.W2 = W2;
     a.h = h;
@@ -266,7 +267,11 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
         cudaEvent_t mid = (events && n_events > 3) ? static_cast<cudaEvent_t>(events[3]) : nullptr;
-        if ((rc = run_ffn(c, v.xperm, v.map.offsets, W13, W2, v.h, v.out, v.status, s, mid)) != MOE_OK) return rc;
+        // Padded layout: the GEMMs skip each segment's padding rows (only kept rows are
+        // ever combined), so those rows of `out` are left unwritten by the forward.
+        const int32_t* used = c->layout == MOE_LAYOUT_PADDED ? v.map.counts_kept : nullptr;
+        if ((rc = run_ffn(c, v.xperm, v.map.offsets, used, W13, W2, v.h, v.out, v.status, s, mid)) != MOE_OK)
+            return rc;
     } else if ((rc = record(events, n_events, 3, s)) != MOE_OK) {
         return rc;
     }
@@ -324,7 +329,7 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     if (validate(cfg) != MOE_OK) return 0;
     // (logits, top-k) + (count, scan, scatter, [select], [pad], gather) + (up, down) + combine
     const int select = cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0 ? 1 : 0;
-    const int pad = cfg->layout == MOE_LAYOUT_PADDED ? 1 : 0;
+    const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     return 2 + 4 + select + pad + ffn + 1;
 }
@@ -378,7 +383,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
     int32_t* status = static_cast<int32_t*>(ws);
     const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
-    return run_ffn(cfg, xperm, offsets, W13, W2, h, out, status, stream, nullptr);
+    return run_ffn(cfg, xperm, offsets, nullptr, W13, W2, h, out, status, stream, nullptr);
 }
 
 int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, const int32_t* pos, void* y,

@@ -288,9 +288,11 @@ int slice_len(int d, int ks) { return ((d + ks - 1) / ks + kGK - 1) / kGK * kGK;
 
 }  // namespace
 
-int route_max_slices(int E) {
-    const int m = 2048 / (E > 0 ? E : 1);
-    return m < 8 ? 8 : (m > 64 ? 64 : m);
+// Up to 64 slices while the partial logits stay within 16 MB (4M floats); at least 8.
+int route_max_slices(int T, int E) {
+    const int64_t te = int64_t(T > 0 ? T : 1) * (E > 0 ? E : 1);
+    const int64_t m = (int64_t(1) << 22) / te;
+    return m < 8 ? 8 : (m > 64 ? 64 : int(m));
 }
 
 int route_k_slices(int T, int d, int E) {
@@ -302,9 +304,10 @@ int route_k_slices(int T, int d, int E) {
     // logits' HBM round trip against larger counts.
     int best = 1;
     double best_cost = 1e300;
-    for (int ks = 1; ks <= route_max_slices(E); ++ks) {
+    for (int ks = 1; ks <= route_max_slices(T, E); ++ks) {
         const int slice = slice_len(d, ks);
-        if (ks > 1 && (slice < 64 || int64_t(slice) * (ks - 1) >= d)) break;
+        if (ks > 1 && slice < 64) break;
+        if (ks > 1 && int64_t(slice) * (ks - 1) >= d) continue;  // the last slice would be empty
         const int64_t ctas = tiles * ks;
         const double waves = double((ctas + sms - 1) / sms);
         const double compute = waves * double(tt) * te * slice / 128.0 + waves * 2000.0;  // SM clocks

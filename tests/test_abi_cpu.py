@@ -102,7 +102,7 @@ def test_rows_capacity_and_kernel_counts():
     assert abi.moe_kernels_per_forward(cfg()) == 9
     assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate")) == 10
     assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate", layout="padded")) == 11
-    assert abi.moe_kernels_per_forward(cfg(capacity=0, layout="padded")) == 8   # no rows: no expert GEMMs
+    assert abi.moe_kernels_per_forward(cfg(capacity=0, layout="padded")) == 7   # no rows: no padding, no GEMMs
     assert abi.moe_kernels_per_forward(cfg(expert="identity", F=0)) == 7
 
 

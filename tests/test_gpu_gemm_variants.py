@@ -1,6 +1,7 @@
-"""Both grouped-GEMM variants against the oracle: one SM per 128x256 tile
-(cta_group::1) and SM pairs sharing a 256x256 tile (cta_group::2). The library picks
-one per shape; MOE_GEMM_PAIR=0/1 forces it, read once per process, so each variant
+"""The three grouped-GEMM variants against the oracle: one SM per 128x256 tile
+(cta_group::1), SM pairs sharing a 256-row x 256-feature tile (cta_group::2), and SM
+pairs with swapped operands (256 features x up to 256 rows). The library picks one
+per shape; MOE_GEMM_PAIR=0/1/2 forces it, read once per process, so each variant
 runs in a child process."""
 import os
 import subprocess
@@ -22,6 +23,9 @@ cases = [
     wl.scaled(wl.WORKLOADS["zipf_cf125"], T=2048, d=512, F=384),
     wl.scaled(wl.WORKLOADS["dsv3_full"], T=512, d=1024, F=256),
     wl.scaled(wl.WORKLOADS["mixtral_bf16"], T=900, d=512, F=640, precision="bf16"),
+    wl.scaled(wl.WORKLOADS["dsv3_decode"], d=1024, F=256),
+    wl.scaled(wl.WORKLOADS["zipf_cf125"], T=2048, d=512, F=384, precision="split_h"),
+    wl.scaled(wl.WORKLOADS["zipf_cf125"], T=2048, d=512, F=384, drop_policy="gate", layout="padded"),
 ] + [w for w in EDGE if w.act == "bf16" and w.expert != "identity"]
 for w in cases:
     r = stagewise(w, seed=13)
@@ -30,7 +34,7 @@ print("ok")
 """
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("pair", ["0", "1", "2"])
 def test_gemm_variant_parity(pair):
     env = dict(os.environ, MOE_GEMM_PAIR=pair)
     r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT)], env=env, capture_output=True, text=True,
