@@ -339,7 +339,8 @@ def run_ours(args, w, world, rank, local):
     # intensity (algorithmic flops / algorithmic bytes) is above the measured ridge
     # point (bf16 peak / HBM bandwidth), else HBM-bound on its weight stream
     ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
-    up_name = "grouped_gemm_kernel<%s> (up)" % ("SwiGLU" if w.expert == "swiglu" else "ReLU")
+    ffn_kernel = abi.moe_ffn_kernel_name(cfg)
+    up_name = "%s<%s> (up)" % (ffn_kernel, "SwiGLU" if w.expert == "swiglu" else "ReLU")
 
     def gemm_entry(name, flops, nbytes):
         if nbytes and flops / nbytes < ridge:
@@ -350,7 +351,7 @@ def run_ours(args, w, world, rank, local):
         "route": ("route_gemm_kernel + route_topk_kernel", "alu", work["route_flops"]),
         "dispatch": ("dispatch (count+scan+scatter+gather)", "hbm", work["dispatch_bytes"]),
         "expert_up": gemm_entry(up_name, work["up_flops"], work["up_bytes"]),
-        "expert_down": gemm_entry("grouped_gemm_kernel<Plain> (down)", work["down_flops"], work["down_bytes"]),
+        "expert_down": gemm_entry("%s<Plain> (down)" % ffn_kernel, work["down_flops"], work["down_bytes"]),
         "combine": ("combine_kernel", "hbm", work["combine_bytes"]),
     }
     dom = max(STAGES, key=lambda s: stage_ms[s])

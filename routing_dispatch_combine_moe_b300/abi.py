@@ -88,6 +88,7 @@ _SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_version": (ctypes.c_int, []),
+    "moe_ffn_kernel_name": (ctypes.c_char_p, [ctypes.POINTER(moe_config)]),
 }
 
 _lib = None
@@ -322,3 +323,8 @@ def exported_symbols() -> list[str]:
     import re
     text = open(HEADER_PATH).read()
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def moe_ffn_kernel_name(cfg) -> str:
+    """Kernel the expert GEMMs of this config run on ("" for identity experts)."""
+    return lib().moe_ffn_kernel_name(ctypes.byref(cfg)).decode()

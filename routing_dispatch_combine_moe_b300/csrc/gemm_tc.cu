@@ -8,13 +8,18 @@
 //   down : out[r, :] = h[r, :] . W2[e]^T
 // for every dispatched row r of expert e (rows [offsets[e], offsets[e+1])).
 //
-// Persistent, warp-specialised kernel, one CTA per SM (192 threads); two variants:
-//   PAIR=false: one SM per 128x256 output tile (tcgen05 cta_group::1, M=128).
-//   PAIR=true : clusters of two SMs share a 256x256 tile (cta_group::2, M=256): each SM
-//               loads its own 128 rows of A and half of the 256 B rows (the gate half or
-//               the up half for SwiGLU), so a stage is 32 KB per SM instead of 48 KB and
-//               six stages fit; one thread of the even CTA issues the pair MMA, which
-//               writes each SM's 128 accumulator rows into its own TMEM.
+// Persistent, warp-specialised kernels, one CTA per SM (192 threads); three variants:
+//   grouped_gemm_kernel<PAIR=false>: one SM per 128x256 output tile (tcgen05
+//               cta_group::1, M=128).
+//   grouped_gemm_kernel<PAIR=true>: clusters of two SMs share a 256x256 tile
+//               (cta_group::2, M=256): each SM loads its own 128 rows of A and half of
+//               the 256 B rows (the gate half or the up half for SwiGLU), so a stage is
+//               32 KB per SM instead of 48 KB and six stages fit; one thread of the
+//               even CTA issues the pair MMA, which writes each SM's 128 accumulator
+//               rows into its own TMEM.
+//   grouped_gemm_swap_kernel: SM pairs with the operands swapped (weights as A,
+//               dispatched rows as B, N <= 256 rows per tile); see its own comment.
+// gemm_variant() picks one per projection.
 // Roles per CTA:
 //   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
 //               swizzle, 4-stage ring of 48 KB stages guarded by full/empty mbarriers.
@@ -125,7 +130,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and division intrinsics: their
+// few-ulp fp32 error is far below the bf16 rounding (or the hi/lo split) that h gets.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Stores 32 consecutive bf16 values (packed in pk[16]) at dst, the first n_valid of them.
 __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const uint32_t (&pk)[16], int n_valid) {
@@ -481,12 +488,19 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
     return r != 0;
 }
 
-// Token-row tile mt of expert e: first row, rows used, and N. A pair MMA takes N as a
-// multiple of 32 in [32, 256] (each SM supplies N/2 rows, a multiple of 16).
+// Token-row tile mt of expert e: first row, rows used, and N. The expert's rows are
+// split into ceil(rows / 256) tiles of equal width (rounded up to 32; the last one
+// takes what is left), so no tile is a thin remainder: a tile's time is bounded
+// below by the load latency of its weight stream whatever its N, and a thin tile
+// would pay that for little work. A pair MMA takes N as a multiple of 32 in
+// [32, 256] (each SM supplies N/2 rows, a multiple of 16).
 __device__ __forceinline__ void swap_tile_rows(const int* off, const int* end, int e, int mt, int& start, int& len,
                                                int& n) {
-    start = off[e] + mt * SW_TILE_N;
-    len = min(SW_TILE_N, end[e] - start);
+    const int rows = end[e] - off[e];
+    const int tiles = (rows + SW_TILE_N - 1) / SW_TILE_N;
+    const int width = ((rows + tiles - 1) / tiles + 31) & ~31;
+    start = off[e] + mt * width;
+    len = min(width, end[e] - start);
     n = (len + 31) & ~31;
 }
 
@@ -688,24 +702,34 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
             tc_fence_after();
             const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + acc * SW_TILE_N;
             if (MODE == kSwiGLU) {
-                const int f = nt * 128 + int(rank) * 64 + (q & 1) * 32 + lane;  // feature in [0, F)
+                // Warps q and q + 2 hold the gate and up values of the same 32 features;
+                // each hands the other half a chunk through shared memory, so both
+                // compute 16 of the chunk's 32 rows.
+                const int w = q & 1;
+                const bool gate_warp = q < 2;
+                const int f = nt * 128 + int(rank) * 64 + w * 32 + lane;  // feature in [0, F)
 #pragma unroll 1
                 for (int c0 = 0; c0 < n; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + c0, v);
                     tmem_ld_wait();
-                    if (q >= 2) {
+                    if (gate_warp) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) X.v[q - 2][j][lane] = __uint_as_float(v[j]);
+                        for (int j = 16; j < 32; ++j) X.v[w][j][lane] = __uint_as_float(v[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) X.v[w][j][lane] = __uint_as_float(v[j]);
                     }
                     epi_bar_sync();
-                    if (q < 2) {
+                    const int j0 = gate_warp ? 0 : 16;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int row = start + c0 + j;
-                            if (c0 + j < len && f < p.n_out)
-                                store_one<OUT>(p, row, f, silu_f(__uint_as_float(v[j])) * X.v[q][j][lane]);
-                        }
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = j0 + jj;
+                        const float mine = __uint_as_float(gate_warp ? v[jj] : v[16 + jj]);
+                        const float other = X.v[w][j][lane];
+                        const float g = gate_warp ? mine : other;
+                        const float u = gate_warp ? other : mine;
+                        if (c0 + j < len && f < p.n_out) store_one<OUT>(p, start + c0 + j, f, silu_f(g) * u);
                     }
                     epi_bar_sync();
                 }
@@ -821,16 +845,21 @@ enum Variant : int { kOneSM = 0, kPairRows = 1, kPairSwap = 2 };
 // Which kernel runs a projection; MOE_GEMM_PAIR=0/1/2 forces one (read once per
 // process). One SM per 128x256 tile keeps the tensor pipe about 70% busy: each SM
 // lands 48 KB per k-block and four stages cover little load latency. SM pairs land
-// 32 KB per SM and keep it about 88% busy, but a 256-row tile that starts near an
-// expert's end leaves up to 255 rows idle, while the swapped pair tile (features x
-// rows) leaves at most 31 idle columns per expert.
-int gemm_variant(int64_t rows_max, int E) {
+// 32 KB per SM, but a 256-row tile that starts near an expert's end leaves up to
+// 255 rows idle; the swapped pair tile (features x rows) leaves at most 31 idle
+// columns per expert. Measured on B300 (layer step, bf16): the swapped pairs win
+// when experts average 128 rows or more without a capacity (T=2048, d=4096, E=8,
+// k=2: 1.167 ms against 1.186 ms; T=4096, d=7168, E=256, k=8: 4.50 ms against
+// 4.70 ms); one SM per tile wins for decode-sized batches (128 tokens, 257 experts:
+// 3.43 against 3.54 ms) and under a capacity with skewed loads (Zipf 1.2, E=64,
+// capacity factor 1.25: 0.315 against 0.327 ms), where most experts hold few rows.
+int gemm_variant(int64_t rows_max, int E, int64_t capacity) {
     static int forced = [] {
         const char* v = getenv("MOE_GEMM_PAIR");
         return v ? atoi(v) : -1;
     }();
     if (forced >= 0 && forced <= 2) return forced;
-    return rows_max >= int64_t(E) * 1024 ? kPairRows : kOneSM;
+    return (capacity < 0 && rows_max >= int64_t(E) * 128) ? kPairSwap : kOneSM;
 }
 
 int grid_for(int64_t rows_max, int E, int n_tiles, bool pair) {
@@ -889,11 +918,13 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Para
 
 }  // namespace
 
+int ffn_tc_variant(int64_t rows, int E, int64_t capacity) { return gemm_variant(rows, E, capacity); }
+
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event) {
     const int64_t rows_max = a.rows;
     const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
     const bool f32_out = a.precision != MOE_PRECISION_BF16;
-    const int variant = gemm_variant(rows_max, a.E);
+    const int variant = gemm_variant(rows_max, a.E, a.capacity);
     const bool pair = variant == kPairRows;
     const bool swap = variant == kPairSwap;
     const uint32_t b_rows = pair ? MMA_N / 2 : MMA_N;  // rows of one B box

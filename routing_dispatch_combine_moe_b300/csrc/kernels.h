@@ -66,7 +66,8 @@ cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const 
 
 struct FfnArgs {
     int T, d, E, k, F;
-    int64_t rows;  // rows of xperm / h / out
+    int64_t rows;      // rows of xperm / h / out
+    int64_t capacity;  // per-expert row cap, or -1 (dropless); a hint for the kernel choice
     int expert_kind;
     int act_dtype;
     int precision;  // MOE_PRECISION_*
@@ -80,6 +81,9 @@ struct FfnArgs {
     int32_t* status;
 };
 
+// tcgen05 kernel a bf16 projection runs: 0 one SM per tile, 1 SM pairs on row
+// tiles, 2 SM pairs with swapped operands.
+int ffn_tc_variant(int64_t rows, int E, int64_t capacity);
 // bf16 experts on the tensor cores (tcgen05 + TMA).
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event);
 // fp32 experts on the FMA units.

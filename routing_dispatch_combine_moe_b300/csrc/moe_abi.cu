@@ -207,6 +207,7 @@ int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, cons
     FfnArgs a{};
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.F = c->F;
     a.rows = rows_cap(c);
+    a.capacity = c->capacity;
     a.expert_kind = c->expert_kind;
     a.act_dtype = c->act_dtype;
     a.precision = c->precision;
@@ -454,6 +455,16 @@ const char* moe_status_string(int code) {
 }
 
 const char* moe_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+const char* moe_ffn_kernel_name(const moe_config* cfg) {
+    if (validate(cfg) != MOE_OK || cfg->expert_kind == MOE_EXPERT_IDENTITY) return "";
+    if (cfg->act_dtype == MOE_F32) return "grouped_sgemm_kernel";
+    switch (ffn_tc_variant(rows_cap(cfg), n_experts(cfg), cfg->capacity)) {
+        case 1: return "grouped_gemm_kernel<pair>";
+        case 2: return "grouped_gemm_swap_kernel";
+        default: return "grouped_gemm_kernel";
+    }
+}
 
 int moe_version(void) { return 100; }
 

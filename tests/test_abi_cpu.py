@@ -225,3 +225,14 @@ def test_status_strings():
     for code in range(7):
         assert abi.status_string(code)
     assert abi.status_string(99) == "unknown status"
+
+
+def test_ffn_kernel_name_follows_the_variant_choice():
+    from routing_dispatch_combine_moe_b300 import workloads as wl
+    name = lambda n: abi.moe_ffn_kernel_name(abi.config_for(wl.WORKLOADS[n]))
+    assert name("tiny_f32") == "grouped_sgemm_kernel"
+    assert name("dsv3_route_only") == ""                      # identity experts
+    assert name("mixtral_bf16") == "grouped_gemm_swap_kernel"  # dropless, 512 rows per expert
+    assert name("zipf_cf125") == "grouped_gemm_kernel"         # under a capacity
+    assert name("dsv3_decode") == "grouped_gemm_kernel"        # ~4.5 rows per expert
+    assert abi.moe_ffn_kernel_name(cfg(k=9)) == ""
