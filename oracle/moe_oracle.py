@@ -34,6 +34,13 @@ Sources (page title, then section):
           prefill and decode are different workloads": a shared expert that every
           token uses; in DeepSeek's decode deployment it is handled like a routed
           one, so each token sends 9 vectors (8 routed + the shared expert).
+* [NODE]  same page, "First-order dispatch and combine bytes" (the node-limited
+          rows): each token is dispatched to at most M nodes (DeepSeek-V3: 4);
+          Megatron calls the same constraint group-limited routing.
+* [DEDUP] same page, same section (the deduplicated rows): a token goes once to
+          each destination node that holds any of its experts, so 8 uniformly
+          random experts over 8 nodes touch 8 (1 - (7/8)^8) ~ 5.25 nodes, of which
+          7 (1 - (7/8)^8) ~ 4.6 are remote.
 
 Readings where the pages are silent (each is listed in the design notes too):
 
@@ -57,6 +64,19 @@ Readings where the pages are silent (each is listed in the design notes too):
   stay in token order;
 * padded layout [CAP: every expert's buffer holds C token slots, under-full experts
   padded]: expert e's kept rows start at row e*C, the rest of its C rows are zero.
+* group-limited routing [NODE] (the pages name the constraint, not the rule): the
+  E experts form G equal contiguous groups; a group's score is its largest logit;
+  a token keeps the M groups with the largest scores (equal scores: lower group
+  first) and KeepTopK runs over the experts of those groups only. This is the same
+  as walking the experts in KeepTopK order and skipping an expert whose group would
+  be the (M+1)-th distinct group. The gates are the kept softmax over the k kept
+  logits, as without the limit.
+* deduplicated dispatch [DEDUP]: with D virtual ranks (rank r owns routed experts
+  [r E/D, (r+1) E/D)), token t sends one row to rank r when at least one of its
+  kept routed assignments lives there; send rows are rank-major, in token order
+  inside a rank's chunk; the receiving rank copies that row to each of the token's
+  expert rows it holds. Shared experts are replicated, so they take their rows from
+  x directly and send nothing.
 
 Every arithmetic step runs in float64 on exact float64 copies of the inputs (bf16
 and fp32 values are exact in float64). ``round_to_bf16`` is only for the optional
@@ -81,6 +101,9 @@ __all__ = [
     "combine",
     "moe_forward",
     "near_tie_flags",
+    "keep_topk_grouped",
+    "group_tie_flags",
+    "dedup_send",
     "round_to_bf16",
 ]
 
@@ -156,6 +179,41 @@ def near_tie_flags(H, k: int, rel: float = 1e-6):
     for j in range(k - 1):
         order_tie |= close(s[:, j], s[:, j + 1])
     return set_tie, order_tie
+
+
+def keep_topk_grouped(H, k: int, n_groups: int, topk_groups: int) -> np.ndarray:
+    """Group-limited KeepTopK, [T, k] int64.  [NODE]
+
+    The experts form ``n_groups`` contiguous groups of E / n_groups. Each group is
+    scored by its largest logit; the ``topk_groups`` best groups are kept (equal
+    scores: lower group first), every logit outside them is set to -inf, and
+    KeepTopK runs on what is left.
+    """
+    H = _f64(H)
+    T, E = H.shape
+    if n_groups < 1 or E % n_groups:
+        raise ValueError("the groups must split the experts evenly")
+    gs = E // n_groups
+    if not 1 <= topk_groups <= n_groups or k > topk_groups * gs:
+        raise ValueError("need 1 <= topk_groups <= n_groups and k <= topk_groups * E / n_groups")
+    score = H.reshape(T, n_groups, gs).max(axis=2)
+    order = np.argsort(-score, axis=1, kind="stable")  # stable: equal scores keep the lower group first
+    kept_group = np.zeros((T, n_groups), bool)
+    np.put_along_axis(kept_group, order[:, :topk_groups], True, axis=1)
+    allowed = np.repeat(kept_group, gs, axis=1)
+    return keep_topk(np.where(allowed, H, -np.inf), k)
+
+
+def group_tie_flags(H, n_groups: int, topk_groups: int, rel: float = 1e-6) -> np.ndarray:
+    """Tokens whose group choice rests on a near tie: the topk_groups-th and the next
+    group score differ by less than ``rel`` relative to the larger magnitude. [T] bool."""
+    H = _f64(H)
+    T, E = H.shape
+    if topk_groups >= n_groups:
+        return np.zeros(T, bool)
+    score = -np.sort(-H.reshape(T, n_groups, E // n_groups).max(axis=2), axis=1)
+    a, b = score[:, topk_groups - 1], score[:, topk_groups]
+    return (a - b) < rel * np.maximum(np.abs(a), np.abs(b))
 
 
 # ------------------------------------------------------------------------- dispatch
@@ -252,6 +310,51 @@ def dispatch(idx, E: int, capacity=None, D: int = 1, capped_experts=None, gates=
     )
 
 
+def dedup_send(idx, pos, n_routed: int, D: int) -> dict:
+    """Deduplicated dispatch: one row per (token, destination rank).  [DEDUP]
+
+    ``idx`` [T, K] and ``pos`` [T*K] come from KeepTopK and ``dispatch``; experts
+    below ``n_routed`` are routed and split over D ranks, E/D each (rank r holds
+    [r n_routed/D, (r+1) n_routed/D)); higher ids are shared experts, which send
+    nothing. Token t sends its row to rank r when one of its kept routed assignments
+    lives there. Returns:
+      sent          [T, D] bool
+      send_counts   [D] rows sent to each rank
+      send_offsets  [D+1] exclusive scan of send_counts
+      send_pos      [T*D] send row of (t, r), -1 when t sends nothing to r
+      send_src      [n_send] t*D + r of each send row (rank-major, then token)
+      fan_src       [T*K] send row feeding each kept routed assignment, else -1
+      n_send
+    """
+    idx = np.asarray(idx, np.int64)
+    T, K = idx.shape
+    pos = np.asarray(pos, np.int64).reshape(T, K)
+    if n_routed % D:
+        raise ValueError("the routed experts must divide into D ranks")
+    per_rank = n_routed // D
+    sent = np.zeros((T, D), bool)
+    for t in range(T):
+        for j in range(K):
+            if pos[t, j] >= 0 and idx[t, j] < n_routed:
+                sent[t, idx[t, j] // per_rank] = True
+    send_counts = sent.sum(axis=0).astype(np.int64)
+    send_offsets = np.concatenate([[0], np.cumsum(send_counts)]).astype(np.int64)
+    send_pos = np.full(T * D, -1, np.int64)
+    send_src = []
+    for r in range(D):
+        for t in range(T):
+            if sent[t, r]:
+                send_pos[t * D + r] = len(send_src)
+                send_src.append(t * D + r)
+    fan_src = np.full(T * K, -1, np.int64)
+    for t in range(T):
+        for j in range(K):
+            if pos[t, j] >= 0 and idx[t, j] < n_routed:
+                fan_src[t * K + j] = send_pos[t * D + idx[t, j] // per_rank]
+    return dict(sent=sent, send_counts=send_counts, send_offsets=send_offsets, send_pos=send_pos,
+                send_src=np.asarray(send_src, np.int64), fan_src=fan_src, n_send=len(send_src))
+
+
 # -------------------------------------------------------------------------- experts
 def silu(z):
     """silu(z) = z / (1 + e^-z)."""
@@ -296,20 +399,27 @@ def combine(G, pos, out, T: int, k: int) -> np.ndarray:
 
 
 def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, n_shared: int = 0,
-                drop_policy: str = "token", layout: str = "packed") -> dict:
+                drop_policy: str = "token", layout: str = "packed", n_groups: int = 0,
+                topk_groups: int = 0) -> dict:
     """The whole layer: logits, KeepTopK, kept softmax, dispatch, experts, combine.
 
     ``expert_fn(e, X)`` returns Expert_e applied to the rows X (an [M, d] float64
     array); for identity experts pass ``lambda e, X: X``. With ``n_shared`` shared
     experts [SHR], every token also uses experts E .. E+n_shared-1 with gate 1 in
-    slots k .. k+n_shared-1. Returns every intermediate the GPU path exposes, in
-    float64 (y is not rounded); ``idx`` and ``G`` then have k + n_shared slots.
+    slots k .. k+n_shared-1. With ``topk_groups`` (0 < topk_groups < n_groups) the
+    selection is group-limited [NODE]. Returns every intermediate the GPU path
+    exposes, in float64 (y is not rounded); ``idx`` and ``G`` then have k + n_shared
+    slots. The deduplicated send buffer changes where rows travel, not their values,
+    so y does not depend on it (``dedup_send`` describes it).
     """
     x = _f64(x)
     T, d = x.shape
     H = router_logits(x, Wg, bias)
     E = H.shape[1]
-    idx = keep_topk(H, k)
+    if n_groups and 0 < topk_groups < n_groups:
+        idx = keep_topk_grouped(H, k, n_groups, topk_groups)
+    else:
+        idx = keep_topk(H, k)
     G = kept_softmax(H, idx)
     if n_shared:
         idx = np.concatenate([idx, np.broadcast_to(E + np.arange(n_shared), (T, n_shared))], axis=1)

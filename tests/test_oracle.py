@@ -8,6 +8,7 @@ transposed operand or a wrong ordering rule fails at least one of them.
 """
 import itertools
 import math
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -407,3 +408,126 @@ def test_gate_policy_equals_token_policy_without_overflow():
     a = run_oracle(w, inp)
     b = run_oracle(wl.scaled(w, drop_policy="gate"), inp)
     assert a["n_dropped"] == 0 and np.array_equal(a["row_src"], b["row_src"])
+
+
+# ------------------------------------------------------------ group-limited routing
+def _greedy_group_limited(h, k, gs, M):
+    """The walk description: experts in KeepTopK order (logit desc, id asc), skipping an
+    expert whose group would be the (M+1)-th distinct group."""
+    order = sorted(range(len(h)), key=lambda e: (-h[e], e))
+    groups, out = [], []
+    for e in order:
+        g = e // gs
+        if g not in groups:
+            if len(groups) == M:
+                continue
+            groups.append(g)
+        out.append(e)
+        if len(out) == k:
+            break
+    return out
+
+
+@pytest.mark.parametrize("E,G,M,k", [(12, 4, 2, 3), (16, 8, 3, 4), (8, 2, 1, 2), (24, 6, 4, 8)])
+def test_group_limited_topk_matches_the_greedy_walk(E, G, M, k):
+    r = rng(40 + E)
+    H = r.normal(size=(200, E))
+    H[:20] = np.round(H[:20], 1)  # some equal logits and equal group scores
+    got = orc.keep_topk_grouped(H, k, G, M)
+    for t in range(H.shape[0]):
+        assert got[t].tolist() == _greedy_group_limited(H[t], k, E // G, M), t
+
+
+def test_group_limited_topk_hand_case():
+    # groups {0,1} {2,3} {4,5} {6,7}; scores 0.9, 0.8, 0.85, 0.3 -> keep groups 0 and 2
+    H = np.array([[0.9, 0.1, 0.8, 0.7, 0.85, 0.0, 0.2, 0.3]])
+    assert orc.keep_topk_grouped(H, 3, 4, 2).tolist() == [[0, 4, 1]]
+    assert orc.keep_topk(H, 3).tolist() == [[0, 4, 2]]
+    # equal scores keep the lower groups
+    assert orc.keep_topk_grouped(np.zeros((1, 8)), 3, 4, 2).tolist() == [[0, 1, 2]]
+
+
+def test_group_limited_topk_invariants():
+    r = rng(41)
+    E, G, M, k = 32, 8, 3, 6
+    H = r.normal(size=(300, E))
+    idx = orc.keep_topk_grouped(H, k, G, M)
+    full = orc.keep_topk(H, k)
+    for t in range(H.shape[0]):
+        groups = set((idx[t] // (E // G)).tolist())
+        assert len(groups) <= M
+        if len(set((full[t] // (E // G)).tolist())) <= M:  # the limit does not bind
+            assert idx[t].tolist() == full[t].tolist()
+    assert np.array_equal(orc.keep_topk_grouped(H, k, G, G), full)  # M = G: no limit
+
+
+def test_group_tie_flags():
+    H = np.array([[1.0, 0.0, 0.5, 0.0, 0.5 * (1 + 1e-8), 0.0],
+                  [1.0, 0.0, 0.5, 0.0, 0.4, 0.0]])
+    assert orc.group_tie_flags(H, 3, 2).tolist() == [True, False]
+    assert not orc.group_tie_flags(H, 3, 3).any()
+
+
+def test_forward_with_group_limit_keeps_at_most_m_groups():
+    w = wl.Workload("t", T=64, d=32, E=16, k=4, F=16, act="f32", expert="relu", D=4)
+    inp = wl.make_inputs(w, seed=42)
+    res = orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), w.k, expert_fn(w.expert, inp["W13"], inp["W2"], w.F),
+                          n_groups=4, topk_groups=2)
+    assert all(len(set((row // 4).tolist())) <= 2 for row in res["idx"])
+    np.testing.assert_allclose(res["G"].sum(axis=1), 1.0, rtol=1e-12)
+
+
+# ------------------------------------------------------------ deduplicated dispatch
+def test_dedup_brute_force_expectation_is_the_exact_closed_form():
+    # every k-subset of E experts as one token: the mean number of ranks touched is
+    # D (1 - C(E - E/D, k) / C(E, k)) exactly
+    E, D = 8, 4
+    for k in (1, 2, 3, 5):
+        idx = np.array(list(itertools.combinations(range(E), k)))
+        d = orc.dispatch(idx, E)
+        s = orc.dedup_send(idx, d["pos"], E, D)
+        exact = Fraction(D) * (1 - Fraction(math.comb(E - E // D, k), math.comb(E, k)))
+        assert Fraction(s["n_send"], len(idx)) == exact
+
+
+def test_dedup_closed_form_tends_to_the_pages_with_replacement_figure():
+    # with many experts per rank, drawing k distinct experts is close to k independent
+    # uniform rank picks: D (1 - (1 - 1/D)^k) ~ 5.25 for D = k = 8. Distinct experts
+    # touch slightly more ranks (5.29): a second pick avoids the first expert.
+    E, D, k = 256, 8, 8
+    exact = D * (1 - math.comb(E - E // D, k) / math.comb(E, k))
+    with_replacement = D * (1 - (1 - 1 / D) ** k)
+    assert with_replacement < exact < with_replacement * 1.01
+    assert round(D * (1 - (1 - 1 / D) ** k), 2) == 5.25 and round((D - 1) * (1 - (1 - 1 / D) ** k), 1) == 4.6
+
+
+def test_dedup_layout_and_fan_out():
+    r = rng(43)
+    T, E, k, D = 90, 16, 4, 4
+    idx = np.stack([r.permutation(E)[:k] for _ in range(T)])
+    d = orc.dispatch(idx, E, 20, D)  # capacity 20: some drops
+    assert d["n_dropped"] > 0
+    s = orc.dedup_send(idx, d["pos"], E, D)
+    # rows are rank-major, token order inside a rank, one per (token, rank) pair with a kept assignment
+    pairs = sorted({(int(e) // (E // D), t) for t in range(T) for j, e in enumerate(idx[t])
+                    if d["pos"][t * k + j] >= 0})
+    assert s["send_src"].tolist() == [t * D + rr for rr, t in pairs]
+    assert s["send_counts"].tolist() == [sum(1 for rr, _ in pairs if rr == q) for q in range(D)]
+    for a in range(T * k):
+        t, e = a // k, idx[a // k, a % k]
+        if d["pos"][a] >= 0:
+            assert s["send_src"][s["fan_src"][a]] == t * D + e // (E // D)
+        else:
+            assert s["fan_src"][a] == -1
+    # k = 1: one row per token; D = 1: one row per token with any kept assignment
+    one = orc.dedup_send(idx[:, :1], orc.dispatch(idx[:, :1], E)["pos"], E, D)
+    assert one["n_send"] == T
+    assert orc.dedup_send(idx, d["pos"], E, 1)["n_send"] == int((d["pos"].reshape(T, k) >= 0).any(axis=1).sum())
+
+
+def test_dedup_skips_shared_experts():
+    T, E, S = 10, 8, 1
+    idx = np.concatenate([np.tile([0, 5], (T, 1)), np.full((T, S), E)], axis=1)
+    d = orc.dispatch(idx, E + S, None, 2, capped_experts=E)
+    s = orc.dedup_send(idx, d["pos"], E, 2)
+    assert s["n_send"] == 2 * T and np.all(s["fan_src"].reshape(T, 3)[:, 2] == -1)
