@@ -167,15 +167,20 @@ def load_traffic(workload: str, kernel: str):
 
 
 # ------------------------------------------------------------------ algorithmic work
-def algorithmic(w, rows: int, out_bytes: int, h_cols: int) -> dict:
-    """Algorithmic work per launch: flops of the formulas, bytes each kernel must move at least."""
+def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0) -> dict:
+    """Algorithmic work per launch: flops of the formulas, bytes each kernel must move at least.
+
+    With the deduplicated dispatch the rows travel x -> send buffer -> expert rows: x is
+    read once, each send row written once and read once, each expert row written once.
+    """
     b = w.act_bytes
     up, down = sizing.expert_gemm_flops(rows, w.d, w.F, w.expert)
     ident = w.expert == "identity"
+    dispatch = sizing.dispatch_hbm_bytes(w.T, w.d, rows, b) + (2 * rows_sent * w.d * b if w.dedup else 0)
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
         route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.slots * 8,
-        dispatch_bytes=sizing.dispatch_hbm_bytes(w.T, w.d, rows, b),
+        dispatch_bytes=dispatch,
         combine_bytes=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
         up_flops=up, down_flops=down,
         up_bytes=0 if ident else w.n_experts * w.w13_rows * w.d * b + rows * w.d * b + rows * h_cols * b,
@@ -328,7 +333,15 @@ def run_ours(args, w, world, rank, local):
     if rank != 0:
         return None
     out_bytes = torch.tensor([], dtype=abi.out_dtype(cfg)).element_size()
-    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg))
+    dedup = None
+    if w.dedup:
+        send_counts = ws[view.send_counts - base:view.send_counts - base + 4 * w.D].view(torch.int32).cpu().numpy()
+        rows_sent = int(send_counts.sum())
+        dedup = {"rows_sent": rows_sent, "ranks_per_token": rows_sent / w.T,
+                 "remote_send_bytes": int((rows_sent - send_counts[0]) * w.d * w.act_bytes),
+                 "remote_bytes_without_dedup": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),
+                 "uniform_routing_ranks_per_token": sizing.expected_nodes_touched(w.k, w.D)}
+    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0)
     peaks, peak_src = load_peaks()
     value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
     dc_bytes = work["dispatch_bytes"] + work["combine_bytes"]
@@ -384,6 +397,7 @@ def run_ours(args, w, world, rank, local):
                    "n_shared": w.n_shared,
                    "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
                    "precision": w.precision, "drop_policy": w.drop_policy, "layout": w.layout,
+                   "n_groups": w.n_groups, "topk_groups": w.topk_groups, "dedup": w.dedup,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
                          "dispatched rows" % (w.n_experts * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
@@ -396,7 +410,8 @@ def run_ours(args, w, world, rank, local):
         "grouped_gemm_frac_bf16_peak": (gemm_flops / (gemm_ms / 1e3) / 1e12) / float(peaks["bf16_tflops"])
         if gemm_ms > 0 and gemm_flops else None,
         "stage_ms": stage_ms,
-        "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "hist": sizing.histogram_summary(counts),
+        "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "dedup": dedup,
+                    "group_limit": [w.topk_groups, w.n_groups] if 0 < w.topk_groups < w.n_groups else None, "hist": sizing.histogram_summary(counts),
                     "rank_imbalance": sizing.imbalance_ratio(np.diff(rank_offs)),
                     "remote_dispatch_bytes": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),
                     "pages_dispatch_bytes": sizing.dispatch_bytes_per_direction(w.T, w.slots, w.d, w.act_bytes,

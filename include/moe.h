@@ -116,6 +116,14 @@ typedef struct moe_config {
     int64_t capacity;    /* tokens each expert keeps; < 0 = dropless (see moe_capacity) */
     int32_t drop_policy; /* MOE_DROP_* */
     int32_t layout;      /* MOE_LAYOUT_* */
+    int32_t n_groups;    /* G: routed experts form G contiguous groups of E/G (used with topk_groups) */
+    int32_t topk_groups; /* M: 0 < M < G limits each token to the M groups with the largest best logit
+                          * ("MoE Expert Parallelism Sizing", "First-order dispatch and combine
+                          * bytes": node-limited / group-limited routing); 0 = no limit. Needs
+                          * E % G == 0, G <= 32, k <= M * E / G. */
+    int32_t dedup;       /* 1: moe_layer_forward sends each token once per virtual rank (the
+                          * deduplicated dispatch, see moe_dispatch_dedup) and fans the send rows
+                          * out into the expert rows; D <= 16. 0: rows go straight from x. */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
@@ -134,6 +142,14 @@ typedef struct moe_dispatch_map {
 } moe_dispatch_map;
 
 /* Pointers into a moe_layer_forward workspace (all device memory inside it). */
+/* The deduplicated send buffer's map (all device int32 arrays). */
+typedef struct moe_send_map {
+    int32_t* send_counts;  /* [D]   rows sent to virtual rank r: tokens with a kept routed assignment there */
+    int32_t* send_offsets; /* [D+1] exclusive scan; send_offsets[D] = rows sent in all */
+    int32_t* send_pos;     /* [T*D] send row of (token t, rank r) at t*D + r, or -1 */
+    int32_t* send_src;     /* [T*D] t*D + r held by each send row; entries [0, send_offsets[D]) written */
+} moe_send_map;
+
 typedef struct moe_workspace_view {
     int32_t* status;     /* device status word (MOE_DEV_* flags) */
     int32_t* topk_idx;   /* [T*K] */
@@ -144,6 +160,8 @@ typedef struct moe_workspace_view {
     void* out;           /* expert outputs, see moe_expert_ffn (aliases xperm for identity); in the
                           * padded layout the forward computes kept rows only and leaves the
                           * padding rows of out unwritten */
+    moe_send_map send;   /* cfg->dedup only (NULL pointers otherwise) */
+    void* xsend;         /* [T*D, d] act: the deduplicated send buffer (cfg->dedup only) */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -210,6 +228,26 @@ int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float
 int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                  const float* topk_gate, const moe_dispatch_map* map, void* xperm, void* ws,
                  size_t ws_bytes, moe_stream_t stream);
+
+/* Deduplicated dispatch ("MoE Expert Parallelism Sizing", "First-order dispatch and
+ * combine bytes", the deduplicated rows: a token crosses to each destination node
+ * once). With D virtual ranks (rank r holds routed experts [r E/D, (r+1) E/D)),
+ * token t sends its row once to every rank that holds one of its kept routed
+ * assignments; send rows are rank-major and in token order inside a rank (rank r's
+ * chunk is [send_offsets[r], send_offsets[r+1])). The receiving side then copies
+ * each send row to the token's expert rows on that rank; shared experts are
+ * replicated, so their rows come from x. The result in xperm equals what
+ * moe_dispatch's gather writes.
+ *   x        [T, d] act;  topk_idx [T, K] int32;  pos [T*K] int32 from moe_dispatch
+ *   map      output arrays (see moe_send_map)
+ *   xsend    [T*D, d] act out (rows [0, send_offsets[D]) written)
+ *   xperm    [rows, d] act out (rows = moe_rows_capacity(cfg)): the kept assignments' rows
+ *   ws       >= moe_dispatch_workspace_bytes(cfg) bytes (cfg->dedup set); its first 4
+ *            bytes are the device status word, cleared by this call.
+ * Needs 1 <= D <= 16. Bit-exact and deterministic. */
+int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
+                       const moe_send_map* map, void* xsend, void* xperm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /* Grouped expert FFN over the dispatched rows: for each expert e, rows
  * [offsets[e], offsets[e+1]) of xperm go through Expert_e ("EP Math", "What expert

@@ -102,6 +102,7 @@ __all__ = [
     "moe_forward",
     "near_tie_flags",
     "keep_topk_grouped",
+    "group_allowed",
     "group_tie_flags",
     "dedup_send",
     "round_to_bf16",
@@ -196,12 +197,19 @@ def keep_topk_grouped(H, k: int, n_groups: int, topk_groups: int) -> np.ndarray:
     gs = E // n_groups
     if not 1 <= topk_groups <= n_groups or k > topk_groups * gs:
         raise ValueError("need 1 <= topk_groups <= n_groups and k <= topk_groups * E / n_groups")
+    return keep_topk(np.where(group_allowed(H, n_groups, topk_groups), H, -np.inf), k)
+
+
+def group_allowed(H, n_groups: int, topk_groups: int) -> np.ndarray:
+    """[T, E] bool: the experts of each token's ``topk_groups`` best groups.  [NODE]"""
+    H = _f64(H)
+    T, E = H.shape
+    gs = E // n_groups
     score = H.reshape(T, n_groups, gs).max(axis=2)
     order = np.argsort(-score, axis=1, kind="stable")  # stable: equal scores keep the lower group first
     kept_group = np.zeros((T, n_groups), bool)
     np.put_along_axis(kept_group, order[:, :topk_groups], True, axis=1)
-    allowed = np.repeat(kept_group, gs, axis=1)
-    return keep_topk(np.where(allowed, H, -np.inf), k)
+    return np.repeat(kept_group, gs, axis=1)
 
 
 def group_tie_flags(H, n_groups: int, topk_groups: int, rel: float = 1e-6) -> np.ndarray:

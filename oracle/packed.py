@@ -59,4 +59,5 @@ def run_oracle(w, inp: dict, capacity="auto", faithful: bool = False, cache=None
     fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, faithful=faithful, cache=cache)
     return orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), w.k, fn, capacity=capacity,
                            bias=f64(inp.get("bias")), D=w.D, n_shared=getattr(w, "n_shared", 0),
-                           drop_policy=getattr(w, "drop_policy", "token"), layout=getattr(w, "layout", "packed"))
+                           drop_policy=getattr(w, "drop_policy", "token"), layout=getattr(w, "layout", "packed"),
+                           n_groups=getattr(w, "n_groups", 0), topk_groups=getattr(w, "topk_groups", 0))

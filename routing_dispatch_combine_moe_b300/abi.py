@@ -49,7 +49,8 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("F", _i32), ("D", _i32),
                 ("act_dtype", _i32), ("expert_kind", _i32), ("precision", _i32), ("n_shared", _i32),
-                ("capacity", _i64), ("drop_policy", _i32), ("layout", _i32)]
+                ("capacity", _i64), ("drop_policy", _i32), ("layout", _i32), ("n_groups", _i32),
+                ("topk_groups", _i32), ("dedup", _i32)]
 
 
 class moe_dispatch_map(ctypes.Structure):
@@ -57,9 +58,13 @@ class moe_dispatch_map(ctypes.Structure):
                                   "row_src", "drop_list", "n_dropped")]
 
 
+class moe_send_map(ctypes.Structure):
+    _fields_ = [(n, _p) for n in ("send_counts", "send_offsets", "send_pos", "send_src")]
+
+
 class moe_workspace_view(ctypes.Structure):
     _fields_ = [("status", _p), ("topk_idx", _p), ("topk_gate", _p), ("map", moe_dispatch_map),
-                ("xperm", _p), ("h", _p), ("out", _p)]
+                ("xperm", _p), ("h", _p), ("out", _p), ("send", moe_send_map), ("xsend", _p)]
 
 
 _SIGNATURES = {
@@ -82,6 +87,8 @@ _SIGNATURES = {
     "moe_layer_forward_traced": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p,
                                                 ctypes.POINTER(_p), _i32]),
     "moe_layer_forward_host": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_dispatch_dedup": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_send_map), _p,
+                                          _p, _p, _sz, _p]),
     "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_dispatch_map),
                                            _p, _p]),
     "moe_read_status": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
@@ -136,12 +143,14 @@ def _stream(stream=None):
 
 # ------------------------------------------------------------------ config
 def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None, precision="f32_out",
-                n_shared=0, drop_policy="token", layout="packed") -> moe_config:
+                n_shared=0, drop_policy="token", layout="packed", n_groups=0, topk_groups=0,
+                dedup=False) -> moe_config:
     """A moe_config; ``capacity`` None (dropless) or a non-negative integer."""
     return moe_config(T=T, d=d, E=E, k=k, F=F, D=D, act_dtype=ACT_DTYPES[act],
                       expert_kind=EXPERT_KINDS[expert], precision=PRECISIONS[precision], n_shared=n_shared,
                       capacity=-1 if capacity is None else int(capacity),
-                      drop_policy=DROP_POLICIES[drop_policy], layout=LAYOUTS[layout])
+                      drop_policy=DROP_POLICIES[drop_policy], layout=LAYOUTS[layout], n_groups=n_groups,
+                      topk_groups=topk_groups, dedup=int(bool(dedup)))
 
 
 def out_dtype(cfg) -> torch.dtype:
@@ -174,7 +183,7 @@ def config_for(w, capacity="auto") -> moe_config:
         capacity = None if w.capacity_factor is None else moe_capacity(w.T, w.k, w.E, w.capacity_factor,
                                                                        w.min_capacity)
     return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision, w.n_shared,
-                       w.drop_policy, w.layout)
+                       w.drop_policy, w.layout, w.n_groups, w.topk_groups, w.dedup)
 
 
 def moe_validate_config(cfg) -> int:
@@ -233,6 +242,11 @@ class WorkspaceView:
     xperm: int
     h: int | None
     out: int
+    send_counts: int | None = None
+    send_offsets: int | None = None
+    send_pos: int | None = None
+    send_src: int | None = None
+    xsend: int | None = None
 
 
 def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
@@ -240,8 +254,10 @@ def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
     _check(lib().moe_workspace_get_view(ctypes.byref(cfg), _ptr(ws), ws.numel(), ctypes.byref(v)),
            "moe_workspace_get_view")
     m = v.map
+    sm = v.send
     return WorkspaceView(v.status, v.topk_idx, v.topk_gate, m.counts_routed, m.counts_kept, m.offsets,
-                         m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out)
+                         m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out,
+                         sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend)
 
 
 # ------------------------------------------------------------------ hot path
@@ -265,6 +281,17 @@ def moe_dispatch(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, ws, stream=Non
     """``topk_gate`` is read only by the gate drop policy with a capacity."""
     _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_gate), ctypes.byref(dmap),
                               _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def send_map(send_counts, send_offsets, send_pos, send_src):
+    return moe_send_map(*[_ptr(t) for t in (send_counts, send_offsets, send_pos, send_src)])
+
+
+def moe_dispatch_dedup(cfg, x, topk_idx, pos, smap: moe_send_map, xsend, xperm, ws, stream=None):
+    """Deduplicated send buffer (one row per token and destination rank) and its fan-out into xperm."""
+    _check(lib().moe_dispatch_dedup(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(pos), ctypes.byref(smap),
+                                    _ptr(xsend), _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_dispatch_dedup")
 
 
 def moe_dispatch_static(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, stream=None, topk_gate=None):

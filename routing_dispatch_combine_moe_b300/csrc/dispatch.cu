@@ -31,9 +31,10 @@ namespace {
 
 constexpr int kWarps = kDispatchBlock / 32;
 
+// quiet_empty: an id of -1 marks "no assignment" and is skipped without a flag.
 __global__ void __launch_bounds__(kDispatchBlock) count_kernel(const int32_t* __restrict__ topk_idx, int64_t A,
                                                                int E, int nblk, int32_t* __restrict__ hist,
-                                                               int32_t* status) {
+                                                               int32_t* status, int quiet_empty = 0) {
     __shared__ int sh[MOE_MAX_E];
     const int tid = threadIdx.x, lane = tid & 31;
     for (int e = tid; e < E; e += kDispatchBlock) sh[e] = 0;
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(kDispatchBlock) count_kernel(const int32_t* __
     if (a < A) {
         e = topk_idx[a];
         if (e < 0 || e >= E) {
-            set_status(status, MOE_DEV_ERR_INDEX);
+            if (!(quiet_empty && e == -1)) set_status(status, MOE_DEV_ERR_INDEX);
             e = -1;
         }
     }
@@ -383,8 +384,99 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
         pad_rows_kernel<<<dim3(unsigned((a.capacity + 7) / 8), unsigned(a.E)), 256, 0, stream>>>(
             a.counts_kept, a.offsets, int(a.capacity),
                                                  static_cast<uint4*>(a.xperm), vec_per_row, a.row_src);
-    gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
-                                                      static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, rows);
+    if (!a.skip_gather)
+        gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
+                                                          static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, rows);
+    return cudaGetLastError();
+}
+
+namespace {
+
+// Deduplicated dispatch ("MoE Expert Parallelism Sizing", "First-order dispatch and
+// combine bytes", the deduplicated rows): token t sends its row once to each virtual
+// rank holding one of its kept routed assignments, and the receiving rank copies it
+// to each of its expert rows. Launches:
+//   1. mask    - per token, the set of ranks its kept routed assignments live on,
+//                written as D slots (slot r = r, or -1 when nothing goes to r);
+//   2-4.       - count / scan / scatter over those T*D slots with D "experts" and no
+//                capacity: send counts, send offsets, and each (token, rank) pair's
+//                send row, rank-major and in token order inside a rank;
+//   5. gather  - x rows into the send buffer (one warp per token, one read of x[t]);
+//   6. fan-out - the receiving side: every kept assignment's row is copied from the
+//                send row of (token, rank of its expert); shared experts (ids past the
+//                routed ones) are replicated, so their rows come from x itself.
+__global__ void __launch_bounds__(256) dedup_mask_kernel(const int32_t* __restrict__ topk_idx,
+                                                         const int32_t* __restrict__ pos, int T, int K,
+                                                         int E_routed, int D, int32_t* __restrict__ slots) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const int per_rank = E_routed / D;
+    uint32_t mask = 0;
+    for (int j = 0; j < K; ++j) {
+        const int e = topk_idx[size_t(t) * K + j];
+        if (pos[size_t(t) * K + j] >= 0 && e >= 0 && e < E_routed) mask |= 1u << (e / per_rank);
+    }
+    for (int r = 0; r < D; ++r) slots[size_t(t) * D + r] = ((mask >> r) & 1u) ? r : -1;
+}
+
+__global__ void __launch_bounds__(256) fanout_kernel(const uint4* __restrict__ x, const uint4* __restrict__ xsend,
+                                                     const int32_t* __restrict__ topk_idx,
+                                                     const int32_t* __restrict__ pos,
+                                                     const int32_t* __restrict__ send_pos, uint4* __restrict__ xperm,
+                                                     int T, int K, int E_routed, int D, int vec_per_row,
+                                                     int64_t max_rows, int64_t max_send, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int dst = -1, src = -1;  // src >= 0: send row; src == -2: x[t]
+    if (lane < K) {
+        const size_t a = size_t(t) * K + lane;
+        const int p = pos[a], e = topk_idx[a];
+        if (p >= 0 && p < max_rows) {
+            if (e >= 0 && e < E_routed) {
+                const int s = send_pos[size_t(t) * D + e / (E_routed / D)];
+                if (s >= 0 && s < max_send) {
+                    dst = p;
+                    src = s;
+                } else {
+                    set_status(status, MOE_DEV_ERR_INDEX);
+                }
+            } else {
+                dst = p;
+                src = -2;
+            }
+        }
+    }
+    for (int j = 0; j < K; ++j) {
+        const int dj = __shfl_sync(0xFFFFFFFFu, dst, j);
+        const int sj = __shfl_sync(0xFFFFFFFFu, src, j);
+        if (dj < 0) continue;
+        const uint4* from = sj == -2 ? x + size_t(t) * vec_per_row : xsend + size_t(sj) * vec_per_row;
+        uint4* to = xperm + size_t(dj) * vec_per_row;
+        for (int v = lane; v < vec_per_row; v += 32) to[v] = __ldg(from + v);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream) {
+    const int64_t A2 = int64_t(a.T) * a.D;
+    const int nblk = dispatch_blocks(A2);
+    const int vec_per_row = int(int64_t(a.d) * a.act_bytes / 16);
+    dedup_mask_kernel<<<(a.T + 255) / 256, 256, 0, stream>>>(a.topk_idx, a.pos, a.T, a.K, a.E_routed, a.D, a.slots);
+    count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, nblk, a.hist, a.status, 1);
+    scan_kernel<<<1, 1024, 0, stream>>>(a.D, a.D, 1, nblk, -1, 0, a.hist, a.send_counts, a.kept_scratch,
+                                        a.send_offsets, a.drop_offsets, a.routed_offsets, a.rank_offsets,
+                                        a.n_dropped);
+    scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, a.D, nblk, -1, a.hist, a.send_offsets,
+                                                        a.drop_offsets, a.routed_offsets, nullptr, a.send_pos,
+                                                        a.send_src, nullptr);
+    gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.send_pos,
+                                                      static_cast<uint4*>(a.xsend), a.T, a.D, vec_per_row, A2);
+    fanout_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x),
+                                                      static_cast<const uint4*>(a.xsend), a.topk_idx, a.pos,
+                                                      a.send_pos, static_cast<uint4*>(a.xperm), a.T, a.K,
+                                                      a.E_routed, a.D, vec_per_row, a.rows, A2, a.status);
     return cudaGetLastError();
 }
 

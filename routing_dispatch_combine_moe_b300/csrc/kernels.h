@@ -26,10 +26,11 @@ inline size_t route_scratch_bytes_max(int T, int E) {
     return size_t(route_max_slices(T, E)) * size_t(T) * size_t(E) * sizeof(float);
 }
 // topk_idx / topk_gate have k + n_shared slots per token; the shared slots hold
-// experts E..E+n_shared-1 with gate 1.
+// experts E..E+n_shared-1 with gate 1. With 0 < topk_groups < n_groups the selection
+// is limited to the topk_groups best of n_groups contiguous expert groups.
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
-                         int k, int n_shared, int32_t* topk_idx, float* topk_gate, float* scratch,
-                         cudaStream_t stream);
+                         int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
+                         float* scratch, cudaStream_t stream);
 
 struct DispatchArgs {
     int T, d, E, k, D;  // E: all experts (routed + shared), k: all slots per token
@@ -56,9 +57,37 @@ struct DispatchArgs {
     int32_t* drop_offsets; // [E]
     int32_t* routed_offsets; // [E+1] exclusive scan of the routed counts (gate policy)
     int32_t* elist;          // [T*k] each expert's assignments in token order (gate policy)
+    bool skip_gather;        // leave xperm to launch_dedup
 };
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
+
+// Deduplicated send buffer and the receiving side's fan-out into xperm.
+struct DedupArgs {
+    int T, d, K, E_routed, D;  // K: slots per token; experts [0, E_routed) split over D ranks
+    int act_bytes;
+    int64_t rows;              // rows of xperm
+    const void* x;
+    const int32_t* topk_idx;   // [T*K]
+    const int32_t* pos;        // [T*K] from launch_dispatch
+    int32_t* send_counts;      // [D]
+    int32_t* send_offsets;     // [D+1]
+    int32_t* send_pos;         // [T*D]
+    int32_t* send_src;         // [T*D]
+    void* xsend;               // [T*D, d]
+    void* xperm;
+    int32_t* status;
+    // scratch
+    int32_t* slots;            // [T*D]
+    int32_t* hist;             // [D * ceil(T*D / 256)]
+    int32_t* kept_scratch;     // [D]
+    int32_t* drop_offsets;     // [D]
+    int32_t* routed_offsets;   // [D+1]
+    int32_t* rank_offsets;     // [2]
+    int32_t* n_dropped;        // [1]
+};
+
+cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream);
 
 // `out_dtype` is the dtype of the expert outputs (MOE_F32 or MOE_BF16), `act_dtype` that of y.
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,

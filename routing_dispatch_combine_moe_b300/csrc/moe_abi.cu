@@ -82,6 +82,14 @@ int validate(const moe_config* c) {
     if (c->layout != MOE_LAYOUT_PACKED && c->layout != MOE_LAYOUT_PADDED) return MOE_ERR_ARG;
     if (n_experts(c) > MOE_MAX_E || n_slots(c) > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
     if (c->layout == MOE_LAYOUT_PADDED && (c->capacity < 0 || c->n_shared != 0)) return MOE_ERR_UNSUPPORTED;
+    if (c->n_groups < 0 || c->topk_groups < 0 || (c->dedup != 0 && c->dedup != 1)) return MOE_ERR_ARG;
+    if (c->topk_groups > 0) {
+        if (c->n_groups < 1 || c->E % c->n_groups != 0 || c->topk_groups > c->n_groups ||
+            int64_t(c->k) > int64_t(c->topk_groups) * (c->E / c->n_groups))
+            return MOE_ERR_ARG;
+        if (c->n_groups > 32) return MOE_ERR_UNSUPPORTED;
+    }
+    if (c->dedup && c->D > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
     if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX) || rows_cap(c) > int64_t(INT32_MAX))
         return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
@@ -93,6 +101,9 @@ int validate(const moe_config* c) {
 struct Layout {
     size_t status, hist, drop_offsets, routed_offsets, elist, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
         n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
+    // deduplicated dispatch (cfg->dedup): scratch in the dispatch part, outputs in the forward part
+    size_t dd_slots, dd_hist, dd_kept, dd_drop, dd_routed, dd_rank, dd_ndrop;
+    size_t send_counts, send_offsets, send_pos, send_src, xsend;
     size_t dispatch_end, forward_end, host_end;
 };
 
@@ -113,6 +124,15 @@ Layout layout(const moe_config* c) {
     L.drop_offsets = take(sizeof(int32_t) * size_t(N));
     L.routed_offsets = take(sizeof(int32_t) * size_t(N + 1));
     L.elist = take(c->drop_policy == MOE_DROP_LOW_GATE ? sizeof(int32_t) * A : 0);
+    const bool dd = c->dedup != 0;
+    const size_t TD = size_t(c->T) * size_t(c->D);
+    L.dd_slots = take(dd ? sizeof(int32_t) * TD : 0);
+    L.dd_hist = take(dd ? sizeof(int32_t) * size_t(c->D) * size_t(dispatch_blocks(int64_t(TD))) : 0);
+    L.dd_kept = take(dd ? sizeof(int32_t) * size_t(c->D) : 0);
+    L.dd_drop = take(dd ? sizeof(int32_t) * size_t(c->D) : 0);
+    L.dd_routed = take(dd ? sizeof(int32_t) * size_t(c->D + 1) : 0);
+    L.dd_rank = take(dd ? sizeof(int32_t) * 2 : 0);
+    L.dd_ndrop = take(dd ? sizeof(int32_t) : 0);
     L.dispatch_end = o;
     L.route_partial = take(route_scratch_bytes_max(c->T, c->E));
     L.topk_idx = take(sizeof(int32_t) * A);
@@ -134,6 +154,11 @@ Layout layout(const moe_config* c) {
         L.h = 0;
         L.out = L.xperm;
     }
+    L.send_counts = take(dd ? sizeof(int32_t) * size_t(c->D) : 0);
+    L.send_offsets = take(dd ? sizeof(int32_t) * size_t(c->D + 1) : 0);
+    L.send_pos = take(dd ? sizeof(int32_t) * TD : 0);
+    L.send_src = take(dd ? sizeof(int32_t) * TD : 0);
+    L.xsend = take(dd ? b * TD * size_t(c->d) : 0);
     L.forward_end = o;
     L.x_stage = take(b * size_t(c->T) * c->d);
     L.y_stage = take(b * size_t(c->T) * c->d);
@@ -162,17 +187,23 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->xperm = at<void>(ws, L.xperm);
     v->h = c->expert_kind == MOE_EXPERT_IDENTITY ? nullptr : at<void>(ws, L.h);
     v->out = at<void>(ws, L.out);
+    const bool dd = c->dedup != 0;
+    v->send.send_counts = dd ? at<int32_t>(ws, L.send_counts) : nullptr;
+    v->send.send_offsets = dd ? at<int32_t>(ws, L.send_offsets) : nullptr;
+    v->send.send_pos = dd ? at<int32_t>(ws, L.send_pos) : nullptr;
+    v->send.send_src = dd ? at<int32_t>(ws, L.send_src) : nullptr;
+    v->xsend = dd ? at<void>(ws, L.xsend) : nullptr;
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
               float* scratch, cudaStream_t s) {
-    const cudaError_t e =
-        launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, c->n_shared, idx, gate, scratch, s);
+    const cudaError_t e = launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, c->n_shared, c->n_groups,
+                                       c->topk_groups, idx, gate, scratch, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
 }
 
 int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const float* gate, const moe_dispatch_map* m,
-                 void* xperm, void* ws, cudaStream_t s) {
+                 void* xperm, void* ws, cudaStream_t s, bool skip_gather = false) {
     const Layout L = layout(c);
     DispatchArgs a{};
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.D = c->D;
@@ -198,8 +229,38 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const f
     a.drop_offsets = at<int32_t>(ws, L.drop_offsets);
     a.routed_offsets = at<int32_t>(ws, L.routed_offsets);
     a.elist = c->drop_policy == MOE_DROP_LOW_GATE ? at<int32_t>(ws, L.elist) : nullptr;
+    a.skip_gather = skip_gather;
     const cudaError_t e = launch_dispatch(a, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch");
+}
+
+// Deduplicated send buffer + fan-out into xperm; the scratch lives in the dispatch part of ws.
+int run_dedup(const moe_config* c, const void* x, const int32_t* idx, const int32_t* pos, const moe_send_map* m,
+              void* xsend, void* xperm, void* ws, cudaStream_t s) {
+    const Layout L = layout(c);
+    DedupArgs a{};
+    a.T = c->T; a.d = c->d; a.K = n_slots(c); a.E_routed = c->E; a.D = c->D;
+    a.act_bytes = act_bytes(c);
+    a.rows = rows_cap(c);
+    a.x = x;
+    a.topk_idx = idx;
+    a.pos = pos;
+    a.send_counts = m->send_counts;
+    a.send_offsets = m->send_offsets;
+    a.send_pos = m->send_pos;
+    a.send_src = m->send_src;
+    a.xsend = xsend;
+    a.xperm = xperm;
+    a.status = at<int32_t>(ws, L.status);
+    a.slots = at<int32_t>(ws, L.dd_slots);
+    a.hist = at<int32_t>(ws, L.dd_hist);
+    a.kept_scratch = at<int32_t>(ws, L.dd_kept);
+    a.drop_offsets = at<int32_t>(ws, L.dd_drop);
+    a.routed_offsets = at<int32_t>(ws, L.dd_routed);
+    a.rank_offsets = at<int32_t>(ws, L.dd_rank);
+    a.n_dropped = at<int32_t>(ws, L.dd_ndrop);
+    const cudaError_t e = launch_dedup(a, s);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch_dedup");
 }
 
 int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const int32_t* counts, const void* W13,
@@ -264,7 +325,10 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
-    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s)) != MOE_OK) return rc;
+    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0)) != MOE_OK)
+        return rc;
+    if (c->dedup && (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s)) != MOE_OK)
+        return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
         cudaEvent_t mid = (events && n_events > 3) ? static_cast<cudaEvent_t>(events[3]) : nullptr;
@@ -332,7 +396,8 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     const int select = cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0 ? 1 : 0;
     const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
-    return 2 + 4 + select + pad + ffn + 1;
+    const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
+    return 2 + 4 + select + pad + dedup + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {
@@ -368,6 +433,24 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, 
     const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     return run_dispatch(cfg, x, topk_idx, topk_gate, map, xperm, ws, stream);
+}
+
+int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
+                       const moe_send_map* map, void* xsend, void* xperm, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!cfg->dedup) return MOE_ERR_ARG;
+    if (!x || !topk_idx || !pos || !map || !ws || !map->send_counts || !map->send_offsets || !map->send_pos ||
+        !map->send_src || !xsend || (!xperm && rows_cap(cfg) > 0))
+        return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(xsend) || (xperm && !aligned16(xperm)) || !aligned4(topk_idx) || !aligned4(pos) ||
+        !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_dedup(cfg, x, topk_idx, pos, map, xsend, xperm, ws, stream);
 }
 
 int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets, const void* W13, const void* W2,

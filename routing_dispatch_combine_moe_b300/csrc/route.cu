@@ -222,35 +222,81 @@ __global__ void __launch_bounds__(256, WE == 1 ? 1 : 2) route_gemm_kernel(const 
     }
 }
 
+// Group-limited selection: the E experts form G contiguous groups of E/G; each group is
+// scored by its largest logit, the M best groups are kept (equal scores: lower group
+// first) and every other logit is set to -inf before KeepTopK. G <= 32: lane g holds
+// group g's score.
 template <int VPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ partial, int KS,
+__device__ __forceinline__ void limit_groups(float (&v)[VPL], int lane, int E, int G, int M) {
+    const int gs = E / G;
+    float score = -INFINITY;
+    for (int g = 0; g < G; ++g) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q) {
+            const int e = lane + 32 * q;
+            if (e < E && e / gs == g) m = fmaxf(m, v[q]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        if (lane == g) score = m;
+    }
+    uint32_t kept = 0;
+    for (int r = 0; r < M; ++r) {
+        float bv = (lane < G && !((kept >> lane) & 1u)) ? score : -INFINITY;
+        int bi = (lane < G && !((kept >> lane) & 1u)) ? lane : 0x7FFFFFFF;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (bi < G) kept |= 1u << bi;
+    }
+#pragma unroll
+    for (int q = 0; q < VPL; ++q) {
+        const int e = lane + 32 * q;
+        if (e < E && !((kept >> (e / gs)) & 1u)) v[q] = -INFINITY;
+    }
+}
+
+// One warp per token (4 per CTA): the KS partial logits of each of the lane's VPL
+// experts are loaded UB slices at a time (VPL * UB loads in flight) and added in slice
+// order, then the bias; then the optional group limit and KeepTopK + kept softmax.
+template <int VPL>
+__global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict__ partial, int KS,
                                                          const float* __restrict__ bias, int T, int E, int k,
-                                                         int n_shared, int32_t* __restrict__ topk_idx,
+                                                         int n_shared, int n_groups, int topk_groups,
+                                                         int32_t* __restrict__ topk_idx,
                                                          float* __restrict__ topk_gate) {
+    constexpr int UB = VPL >= 16 ? 4 : (VPL >= 4 ? 8 : 32 / VPL);
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (t >= T) return;
     float v[VPL];
 #pragma unroll
-    for (int m = 0; m < VPL; ++m) {
-        const int e = lane + 32 * m;
-        float h = -INFINITY;
-        if (e < E) {
-            // Issue 8 independent loads at a time, then add them in slice order.
-            h = 0.f;
-            for (int z0 = 0; z0 < KS; z0 += 8) {
-                float pz[8];
+    for (int q = 0; q < VPL; ++q) v[q] = (lane + 32 * q < E) ? 0.f : -INFINITY;
+    for (int z0 = 0; z0 < KS; z0 += UB) {
+        float pz[VPL][UB];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    pz[u] = (z0 + u < KS) ? __ldg(partial + (size_t(z0 + u) * T + t) * E + e) : 0.f;
+        for (int q = 0; q < VPL; ++q) {
+            const int e = lane + 32 * q;
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (z0 + u < KS) h += pz[u];
-            }
-            if (bias) h += __ldg(bias + e);
+            for (int u = 0; u < UB; ++u)
+                pz[q][u] = (e < E && z0 + u < KS) ? __ldg(partial + (size_t(z0 + u) * T + t) * E + e) : 0.f;
         }
-        v[m] = h;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q)
+#pragma unroll
+            for (int u = 0; u < UB; ++u)
+                if (lane + 32 * q < E && z0 + u < KS) v[q] += pz[q][u];
     }
+    if (bias) {
+#pragma unroll
+        for (int q = 0; q < VPL; ++q)
+            if (lane + 32 * q < E) v[q] += __ldg(bias + lane + 32 * q);
+    }
+    if (topk_groups > 0 && topk_groups < n_groups) limit_groups<VPL>(v, lane, E, n_groups, topk_groups);
     const int K = k + n_shared;
     topk_softmax_store<VPL>(v, lane, E, k, n_shared, topk_idx + size_t(t) * K, topk_gate + size_t(t) * K);
 }
@@ -322,20 +368,20 @@ int route_k_slices(int T, int d, int E) {
 }
 
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
-                         int k, int n_shared, int32_t* topk_idx, float* topk_gate, float* scratch,
-                         cudaStream_t stream) {
+                         int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
+                         float* scratch, cudaStream_t stream) {
     const int ks = route_k_slices(T, d, E);
     const int slice = slice_len(d, ks);
     cudaError_t e = act_dtype == MOE_F32 ? launch_gemm_t<float>(x, Wg, T, d, E, slice, ks, scratch, stream)
                                          : launch_gemm_t<__nv_bfloat16>(x, Wg, T, d, E, slice, ks, scratch, stream);
     if (e != cudaSuccess) return e;
-    const int g2 = (T + 7) / 8;
-    const int S = n_shared;
-    if (E <= 32) route_topk_kernel<1><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
-    else if (E <= 64) route_topk_kernel<2><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
-    else if (E <= 128) route_topk_kernel<4><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
-    else if (E <= 256) route_topk_kernel<8><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
-    else route_topk_kernel<16><<<g2, 256, 0, stream>>>(scratch, ks, bias, T, E, k, S, topk_idx, topk_gate);
+    const int g2 = (T + 3) / 4;
+    const int S = n_shared, G = n_groups, M = topk_groups;
+    if (E <= 32) route_topk_kernel<1><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
+    else if (E <= 64) route_topk_kernel<2><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
+    else if (E <= 128) route_topk_kernel<4><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
+    else if (E <= 256) route_topk_kernel<8><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
+    else route_topk_kernel<16><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
     return cudaGetLastError();
 }
 

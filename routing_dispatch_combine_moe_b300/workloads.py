@@ -56,6 +56,9 @@ class Workload:
     n_shared: int = 0  # shared experts (ids E .. E+n_shared-1) every token also uses, gate 1
     drop_policy: str = "token"  # overflow dropped in token order, or "gate": lowest gates first
     layout: str = "packed"      # "packed" rows, or "padded": a fixed segment of C rows per expert
+    n_groups: int = 0           # expert groups for group-limited routing (with topk_groups)
+    topk_groups: int = 0        # 0 < M < n_groups: each token keeps experts of at most M groups
+    dedup: bool = False         # send each token once per virtual rank, then fan out
     note: str = field(default="", compare=False)
 
     @property
@@ -102,11 +105,16 @@ WORKLOADS: dict[str, Workload] = {
                  n_shared=1, D=8,
                  note="decode-shaped DeepSeek-V3 layer: 128 tokens, 8 routed experts plus the shared "
                       "expert per token (9 vectors each), 8 virtual ranks"),
+        Workload("dsv3_grouped_dedup", T=4096, d=7168, E=256, k=8, F=0, act="bf16", expert="identity", D=8,
+                 n_groups=8, topk_groups=4, dedup=True,
+                 note="DeepSeek-V3 routing shape with each token limited to 4 of 8 expert groups (one "
+                      "group per virtual rank) and the send buffer deduplicated per rank"),
     ]
 }
 
 # Workload order as they are listed: small parity case first, headline second.
-WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"]
+WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
+                  "dsv3_grouped_dedup"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

@@ -88,6 +88,19 @@ class StageBuffers:
         self.ws_dispatch = torch.zeros(abi.moe_dispatch_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.ws_ffn = torch.zeros(abi.moe_ffn_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        if w.dedup:
+            TD = w.T * w.D
+            self.send_counts = torch.full((w.D,), -7, **i32)
+            self.send_offsets = torch.full((w.D + 1,), -7, **i32)
+            self.send_pos = torch.full((TD,), -7, **i32)
+            self.send_src = torch.full((TD,), -7, **i32)
+            self.xsend = torch.full((TD, w.d), float("nan"), dtype=w.torch_act, device=device)
+
+    def smap(self):
+        return abi.send_map(self.send_counts, self.send_offsets, self.send_pos, self.send_src)
+
+    def dedup(self, inp, topk_idx, pos, xperm):
+        abi.moe_dispatch_dedup(self.cfg, inp["x"], topk_idx, pos, self.smap(), self.xsend, xperm, self.ws_dispatch)
 
     def dmap(self):
         return abi.dispatch_map(self.counts_routed, self.counts_kept, self.offsets, self.rank_offsets, self.pos,
@@ -125,15 +138,34 @@ def capacity_of(cfg):
 
 
 def oracle_route(w, inp) -> dict:
-    """The oracle's router on the original inputs, with the shared slots appended."""
+    """The oracle's router on the original inputs, with the shared slots appended.
+    Under a group limit the near ties are those of the group choice and those of
+    KeepTopK inside the kept groups."""
     H = orc.router_logits(f64(inp["x"]), f64(inp["Wg"]), f64(inp.get("bias")))
-    idx = orc.keep_topk(H, w.k)
+    Hs = selectable_logits(w, H)
+    idx = orc.keep_topk(Hs, w.k)
     G = orc.kept_softmax(H, idx)
-    set_tie, order_tie = orc.near_tie_flags(H, w.k)
+    tie = route_tie_flags(w, H)
     S = w.n_shared
     idx_full = np.concatenate([idx, np.broadcast_to(w.E + np.arange(S), (w.T, S))], axis=1)
     G_full = np.concatenate([G, np.ones((w.T, S))], axis=1)
-    return dict(H=H, idx=idx, G=G, tie=set_tie | order_tie, idx_full=idx_full, G_full=G_full)
+    return dict(H=H, idx=idx, G=G, tie=tie, idx_full=idx_full, G_full=G_full)
+
+
+def selectable_logits(w, H):
+    """H with the logits outside each token's kept groups at -inf (group-limited routing)."""
+    if 0 < w.topk_groups < w.n_groups:
+        return np.where(orc.group_allowed(H, w.n_groups, w.topk_groups), H, -np.inf)
+    return H
+
+
+def route_tie_flags(w, H):
+    """Near ties of the selection: KeepTopK's (inside the kept groups) and the group choice's."""
+    s, o = orc.near_tie_flags(selectable_logits(w, H), w.k)
+    tie = s | o
+    if 0 < w.topk_groups < w.n_groups:
+        tie |= orc.group_tie_flags(H, w.n_groups, w.topk_groups)
+    return tie
 
 
 def check_route(w, inp, bufs, ref=None) -> dict:
@@ -212,6 +244,28 @@ def check_dispatch(w, inp, bufs, capacity, st) -> dict:
     torch.cuda.synchronize()
     compare_dispatch(w, bufs, d, inp["x"])
     return d
+
+
+def check_dedup(w, inp, bufs, st, d) -> dict:
+    """Deduplicated dispatch on the synthetic ids' dispatch map ``d`` (already on the
+    GPU in ``bufs``): the send map bit-exact against the oracle, the send rows exact
+    copies of x, and the fanned-out expert rows equal to the direct gather's."""
+    direct = bufs.xperm.clone()
+    fanned = torch.full_like(bufs.xperm, float("nan"))
+    bufs.dedup(inp, st["topk_idx"], bufs.pos, fanned)
+    s = orc.dedup_send(cpu(st["topk_idx"]).numpy(), d["pos"], w.E, w.D)
+    torch.cuda.synchronize()
+    assert bufs.dispatch_status() == 0
+    np.testing.assert_array_equal(cpu(bufs.send_counts).numpy(), s["send_counts"])
+    np.testing.assert_array_equal(cpu(bufs.send_offsets).numpy(), s["send_offsets"])
+    np.testing.assert_array_equal(cpu(bufs.send_pos).numpy(), s["send_pos"])
+    n = s["n_send"]
+    np.testing.assert_array_equal(cpu(bufs.send_src).numpy()[:n], s["send_src"])
+    src_tok = torch.from_numpy(s["send_src"] // w.D).to(bufs.xsend.device)
+    assert torch.equal(bufs.xsend[:n], inp["x"][src_tok]), "send rows are not exact copies of x"
+    rows = d["row_src"].size
+    assert torch.equal(fanned[:rows], direct[:rows]), "fanned-out rows differ from the direct gather"
+    return s
 
 
 def check_ffn(w, inp, bufs, st, expert_subset=None) -> float:
@@ -318,6 +372,13 @@ class WorkspaceMap:
         self.out = None if not view.out else \
             ws[view.out - base:view.out - base + R * w.d * osz].view(odt).view(R, w.d)
         self.out_act = "f32" if odt == torch.float32 else "bf16"
+        if w.dedup:
+            TD = w.T * w.D
+            self.send_counts = i32(view.send_counts, w.D)
+            self.send_offsets = i32(view.send_offsets, w.D + 1)
+            self.send_pos = i32(view.send_pos, TD)
+            self.send_src = i32(view.send_src, TD)
+            self.xsend = ws[view.xsend - base:view.xsend - base + TD * w.d * esz].view(w.torch_act).view(TD, w.d)
 
 
 def chain(w, inp, cfg) -> StageBuffers:

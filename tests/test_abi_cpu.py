@@ -168,7 +168,7 @@ def test_workspace_sizes_and_layout():
             assert view.xperm < view.h < view.out < base + fwd
             assert view.out + A * w.d * w.act_bytes <= base + fwd
         assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
-        assert abi.moe_kernels_per_forward(c) == (7 if w.expert == "identity" else 9)
+        assert abi.moe_kernels_per_forward(c) == (7 if w.expert == "identity" else 9) + (5 if w.dedup else 0)
 
 
 def test_entry_points_reject_bad_arguments_on_the_host():
@@ -236,3 +236,41 @@ def test_ffn_kernel_name_follows_the_variant_choice():
     assert name("zipf_cf125") == "grouped_gemm_kernel"         # under a capacity
     assert name("dsv3_decode") == "grouped_gemm_kernel"        # ~4.5 rows per expert
     assert abi.moe_ffn_kernel_name(cfg(k=9)) == ""
+
+
+def test_group_limit_and_dedup_validation():
+    ok = abi.MOE_OK
+    assert abi.moe_validate_config(cfg(E=16, k=4, n_groups=4, topk_groups=2)) == ok
+    assert abi.moe_validate_config(cfg(E=16, k=4, n_groups=4, topk_groups=4)) == ok   # no limit in effect
+    assert abi.moe_validate_config(cfg(E=16, k=4, n_groups=4)) == ok                  # groups alone: ignored
+    assert abi.moe_validate_config(cfg(E=16, k=4, n_groups=5, topk_groups=2)) == abi.MOE_ERR_ARG  # 16 % 5
+    assert abi.moe_validate_config(cfg(E=16, k=4, n_groups=4, topk_groups=5)) == abi.MOE_ERR_ARG  # M > G
+    assert abi.moe_validate_config(cfg(E=16, k=5, n_groups=4, topk_groups=1)) == abi.MOE_ERR_ARG  # k > M*E/G
+    assert abi.moe_validate_config(cfg(E=64, k=2, n_groups=64, topk_groups=2)) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(E=16, k=2, D=4, dedup=True)) == ok
+    assert abi.moe_validate_config(cfg(E=64, k=2, D=32, dedup=True)) == abi.MOE_ERR_UNSUPPORTED   # D > 16
+    c = cfg()
+    c.dedup = 2
+    assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
+
+
+def test_dedup_workspace_and_kernel_count():
+    plain, dd = cfg(E=16, k=2, D=4), cfg(E=16, k=2, D=4, dedup=True)
+    assert abi.moe_kernels_per_forward(dd) == abi.moe_kernels_per_forward(plain) + 5
+    assert abi.moe_dispatch_workspace_bytes(dd) > abi.moe_dispatch_workspace_bytes(plain)
+    v = abi.moe_workspace_view()
+    base = 1 << 40
+    n = abi.moe_workspace_bytes(dd)
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(dd), base, n, ctypes.byref(v)) == 0
+    assert v.xsend and v.send.send_pos and base + n - v.xsend >= 64 * 4 * 128 * 2
+    vp = abi.moe_workspace_view()
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(plain), base, abi.moe_workspace_bytes(plain),
+                                            ctypes.byref(vp)) == 0
+    assert not vp.xsend and not vp.send.send_pos
+    m = abi.send_map(*([None] * 4))
+    A16 = 1 << 20
+    assert abi.lib().moe_dispatch_dedup(ctypes.byref(plain), A16, A16, A16, ctypes.byref(m), A16, A16, A16,
+                                        1 << 20, None) == abi.MOE_ERR_ARG  # cfg.dedup not set
+    assert abi.lib().moe_dispatch_dedup(ctypes.byref(dd), A16, A16, A16, ctypes.byref(m), A16, A16, A16,
+                                        1 << 20, None) == abi.MOE_ERR_ARG  # null map arrays
+

@@ -17,8 +17,9 @@ from oracle import moe_oracle as orc
 from routing_dispatch_combine_moe_b300 import abi
 from routing_dispatch_combine_moe_b300 import workloads as wl
 from tests._gpu import (StageBuffers, WorkspaceMap, capacity_of, chain, check_chained_dispatch, check_close,
-                        check_combine, check_dispatch, check_ffn, check_route, cpu, gate_boundary_ties, half_ulp,
-                        oracle_dispatch, oracle_route, rms, run_layer)
+                        check_combine, check_dedup, check_dispatch, check_ffn, check_route, cpu,
+                        gate_boundary_ties, half_ulp, oracle_dispatch, oracle_route, rms, route_tie_flags,
+                        run_layer)
 from tests._harness import expert_fn, f64, run_oracle
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +33,10 @@ REDUCED = {
     "dsv3_full": wl.scaled(W["dsv3_full"], T=512, d=1024, F=256),
     "dsv3_decode": wl.scaled(W["dsv3_decode"], d=1024, F=256),
     "zipf_gate_padded": wl.scaled(W["zipf_cf125"], T=2048, d=512, F=384, drop_policy="gate", layout="padded"),
+    "grouped_dedup": wl.scaled(W["dsv3_grouped_dedup"], T=512, d=1024),
+    "grouped_dedup_swiglu": wl.Workload("grouped_dedup_swiglu", T=700, d=512, E=64, k=6, F=256, act="bf16",
+                                        expert="swiglu", D=8, n_groups=8, topk_groups=3, dedup=True,
+                                        capacity_factor="1"),
 }
 
 
@@ -46,6 +51,7 @@ def stagewise(w, seed=0, inp=None):
     r = check_route(w, inp, b)
     d = check_dispatch(w, inp, b, cap, st)
     assert b.dispatch_status() == 0
+    dd = check_dedup(w, inp, b, st, d) if w.dedup else None
     ffn_err = None
     if w.expert != "identity":
         ffn_err = check_ffn(w, inp, b, st)
@@ -54,17 +60,16 @@ def stagewise(w, seed=0, inp=None):
     assert abi.moe_read_status(b.status.data_ptr()) == 0
     c = chain(w, inp, cfg)
     chained = check_chained_dispatch(w, inp, c, r, cap)
-    return dict(inp=inp, cfg=cfg, bufs=b, chain=c, route=r, dispatch=d, ffn_err=ffn_err, combine_err=comb_err,
-                chained=chained)
+    return dict(inp=inp, cfg=cfg, bufs=b, chain=c, route=r, dispatch=d, dedup=dd, ffn_err=ffn_err,
+                combine_err=comb_err, chained=chained)
 
 
 def layer_keep(w, ref, capacity):
     """Tokens compared end to end: no near tie in the router, and under the gate
     drop policy no gate at a keep cutoff."""
-    s, o = orc.near_tie_flags(ref["H"], w.k)
-    keep = ~(s | o)
+    keep = ~route_tie_flags(w, ref["H"])
     if w.drop_policy == "gate":
-        keep &= ~gate_boundary_ties(w, orc.keep_topk(ref["H"], w.k), ref["G"][:, :w.k], capacity)
+        keep &= ~gate_boundary_ties(w, ref["idx"][:, :w.k], ref["G"][:, :w.k], capacity)
     return keep
 
 
@@ -91,6 +96,27 @@ def test_layer_forward_matches_oracle(name):
     print(f"\n{name}: layer max|err|/rms(y) = {err:.4f} (near-tie tokens excluded: {int((~keep).sum())})")
     if w.expert == "identity":
         assert torch.equal(y, inp["x"]), "identity experts must return x exactly"
+
+
+@pytest.mark.parametrize("name", ["grouped_dedup", "grouped_dedup_swiglu"])
+def test_dedup_forward_equals_the_direct_forward_bitwise(name):
+    """The deduplicated dispatch changes where rows travel, not their values: the layer
+    output is the same bits, and the send map in the workspace is the oracle's."""
+    w = REDUCED[name]
+    inp = wl.make_inputs(w, 17, device="cuda")
+    y_dd, ws, view, flags = run_layer(abi.config_for(w), inp, w)
+    y_direct, _, _, _ = run_layer(abi.config_for(wl.scaled(w, dedup=False)), inp, w)
+    assert flags == 0 and torch.equal(y_dd, y_direct)
+    idx = cpu(WorkspaceMap(w, abi.config_for(w), ws, view).topk_idx).numpy()
+    pos = ws[view.pos - ws.data_ptr():view.pos - ws.data_ptr() + 4 * w.T * w.slots].view(torch.int32).cpu().numpy()
+    s = orc.dedup_send(idx, pos, w.E, w.D)
+    base = ws.data_ptr()
+    send_offsets = ws[view.send_offsets - base:view.send_offsets - base + 4 * (w.D + 1)].view(torch.int32).cpu()
+    np.testing.assert_array_equal(send_offsets.numpy(), s["send_offsets"])
+    # each token touches at most topk_groups ranks when the groups are the ranks
+    assert int(s["sent"].sum(axis=1).max()) <= w.topk_groups
+    print(f"\n{name}: rows sent {s['n_send']} for {int((pos >= 0).sum())} kept assignments "
+          f"({s['n_send'] / w.T:.2f} ranks per token)")
 
 
 def test_identity_experts_return_x_exactly_with_drops_zeroed():
@@ -270,6 +296,7 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
 
 FULL = {n: W[n] for n in ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"]}
 FULL["zipf_gate_padded"] = wl.scaled(W["zipf_cf125"], drop_policy="gate", layout="padded")
+FULL["dsv3_grouped_dedup"] = W["dsv3_grouped_dedup"]
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -286,6 +313,14 @@ def test_full_size_sampled(name):
     # dispatch of the GPU's routing: bit-exact against the oracle's where the routings agree
     how = check_chained_dispatch(w, inp, m, r, cap)
     d = oracle_dispatch(w, r["idx_full"], r["G_full"], cap)
+    if w.dedup and how == "exact":
+        s = orc.dedup_send(r["idx_full"], d["pos"], w.E, w.D)
+        np.testing.assert_array_equal(cpu(m.send_offsets).numpy(), s["send_offsets"])
+        np.testing.assert_array_equal(cpu(m.send_pos).numpy(), s["send_pos"])
+        np.testing.assert_array_equal(cpu(m.send_src).numpy()[:s["n_send"]], s["send_src"])
+        src = torch.from_numpy(s["send_src"] // w.D).cuda()
+        assert torch.equal(m.xsend[:s["n_send"]], inp["x"][src])
+        print(f"\n{name}: {s['n_send']} send rows, {s['n_send'] / w.T:.3f} ranks per token")
     if w.expert == "identity":
         assert torch.equal(y, inp["x"])
         return
