@@ -316,7 +316,7 @@ int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const floa
  * callers.
  *
  * Same arguments, outputs and results as moe_dispatch, minus ws/ws_bytes. Its
- * scratch (histogram and offsets, 4 * (N * ceil(T*K/256) + 2N + 1) bytes, plus 4*T*K
+ * scratch (histogram and offsets, 4 * (N * ceil(T*K/256) + 2N + 1) bytes, plus 8*T*K
  * under MOE_DROP_LOW_GATE, plus a small header) lives in one device array of
  * MOE_STATIC_SCRATCH_BYTES inside the
  * library, which every GPU that loads the library keeps until the process exits.

@@ -99,17 +99,44 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
     __shared__ int totals[3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    for (int e = warp; e < E; e += 32) {
-        int run = 0;
-        int32_t* row = hist + size_t(e) * nblk;
-        for (int b0 = 0; b0 < nblk; b0 += 32) {
-            const int b = b0 + lane;
-            const int v = b < nblk ? row[b] : 0;
-            const int incl = warp_incl_scan(v, lane);
-            if (b < nblk) row[b] = run + incl - v;
-            run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    // Per expert, an exclusive scan of its row of block counts. A warp takes four experts
+    // (e, e + 32, e + 64, e + 96) at a time and loads 4 chunks of 32 blocks of each before
+    // scanning, so 16 independent loads per lane are in flight instead of one.
+    constexpr int SB = 4, EX = 4;
+    for (int e0 = warp; e0 < E; e0 += 32 * EX) {
+        int32_t* row[EX];
+        int run[EX];
+        bool has[EX];
+#pragma unroll
+        for (int x = 0; x < EX; ++x) {
+            has[x] = e0 + 32 * x < E;
+            row[x] = hist + size_t(has[x] ? e0 + 32 * x : e0) * nblk;
+            run[x] = 0;
         }
-        if (lane == 0) routed[e] = run;
+        for (int b0 = 0; b0 < nblk; b0 += 32 * SB) {
+            int v[EX][SB];
+#pragma unroll
+            for (int x = 0; x < EX; ++x)
+#pragma unroll
+                for (int j = 0; j < SB; ++j) {
+                    const int b = b0 + 32 * j + lane;
+                    v[x][j] = (b < nblk && has[x]) ? row[x][b] : 0;
+                }
+#pragma unroll
+            for (int x = 0; x < EX; ++x)
+#pragma unroll
+                for (int j = 0; j < SB; ++j) {
+                    const int b = b0 + 32 * j + lane;
+                    const int incl = warp_incl_scan(v[x][j], lane);
+                    if (b < nblk && has[x]) row[x][b] = run[x] + incl - v[x][j];
+                    run[x] += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int x = 0; x < EX; ++x)
+                if (has[x]) routed[e0 + 32 * x] = run[x];
+        }
     }
     __syncthreads();
 
@@ -139,8 +166,16 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
     if (tid <= D) rank_offsets[tid] = offs[tid * (E_capped / D)];
 }
 
+// fp32 bits mapped so that unsigned order is value order (negatives flipped, the
+// sign bit set on non-negatives); -0 sorts just below +0.
+__device__ __forceinline__ uint32_t order_key(float g) {
+    const uint32_t b = __float_as_uint(g);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // With `elist` set (gate drop policy) it only lists each expert's assignments in
-// token order at routed_offsets[e] + rank; select_kernel then places them.
+// token order at elist[routed_offsets[e] + rank], with their gates' order keys at the
+// same place of elist + A; select_kernel then places them.
 __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* __restrict__ topk_idx, int64_t A,
                                                                  int E, int E_capped, int nblk, int64_t capacity,
                                                                  const int32_t* __restrict__ hist,
@@ -148,6 +183,7 @@ __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* 
                                                                  const int32_t* __restrict__ drop_offsets,
                                                                  const int32_t* __restrict__ routed_offsets,
                                                                  int32_t* __restrict__ elist,
+                                                                 const float* __restrict__ topk_gate,
                                                                  int32_t* __restrict__ pos,
                                                                  int32_t* __restrict__ row_src,
                                                                  int32_t* __restrict__ drop_list) {
@@ -178,6 +214,7 @@ __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* 
     for (int w = 0; w < warp; ++w) rank += cnt[w][e];
     if (elist) {
         elist[routed_offsets[e] + rank] = int32_t(a);
+        elist[A + routed_offsets[e] + rank] = int32_t(order_key(topk_gate[a]));
         return;
     }
     if (capacity < 0 || e >= E_capped || rank < capacity) {
@@ -191,6 +228,7 @@ __global__ void __launch_bounds__(kDispatchBlock) scatter_kernel(const int32_t* 
 }
 
 constexpr int kSelThreads = 512;
+constexpr int kSelKeys = 9216;  // keys of one expert cached in shared memory (36 KB)
 
 // Block-wide exclusive scan of one int per thread (kSelThreads threads); *total gets the sum.
 __device__ int sel_excl_scan(int v, int* warp_sums, int* total) {
@@ -210,98 +248,113 @@ __device__ int sel_excl_scan(int v, int* warp_sums, int* total) {
     return r;
 }
 
-// fp32 bits mapped so that unsigned order is value order (negatives flipped, the
-// sign bit set on non-negatives); -0 sorts just below +0.
-__device__ __forceinline__ uint32_t order_key(float g) {
-    const uint32_t b = __float_as_uint(g);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Gate drop policy, one CTA per expert: the expert's routed assignments are listed
-// in token order; the ones kept are those whose gate is above the keep_n-th largest
-// gate, plus, among the gates equal to it, the first ones by token. That gate is
-// found by a most-significant-digit-first radix select over order_key(gate). Kept
-// assignments take the expert's rows in token order; the others go to the drop
-// list in token order.
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* __restrict__ elist,
+// Gate drop policy, one CTA per expert. The expert's n routed assignments are listed
+// in token order with their gates' order keys (scatter_kernel). Kept are the keys
+// above thr, the keep_n-th largest key, plus the first need_eq keys equal to it in
+// token order; thr is found by a most-significant-digit-first radix select (digits
+// of 11, 11 and 10 bits over 2048 shared bins, the bin crossing the wanted rank found
+// by a block suffix scan). The keys sit in shared memory when they fit. A final pass
+// scans, per 512-key chunk, the packed pair (greater, equal) to place every
+// assignment: kept_before = greater_before + min(equal_before, need_eq); kept rows go
+// to the expert's rows in token order, the rest to the drop list in token order.
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const int32_t* __restrict__ elist, int64_t A,
                                                              const int32_t* __restrict__ routed_offsets,
                                                              const int32_t* __restrict__ counts_routed,
                                                              const int32_t* __restrict__ counts_kept,
                                                              const int32_t* __restrict__ offsets,
                                                              const int32_t* __restrict__ drop_offsets,
-                                                             const float* __restrict__ gate,
                                                              int32_t* __restrict__ pos,
                                                              int32_t* __restrict__ row_src,
                                                              int32_t* __restrict__ drop_list) {
-    __shared__ int hist[256];
+    __shared__ uint32_t skey[kSelKeys];
+    __shared__ int hist[2048];
     __shared__ int warp_sums[32];
-    __shared__ int totals[3];
+    __shared__ int totals[2];
     __shared__ int sel_bin, sel_rank;
     const int e = blockIdx.x, tid = threadIdx.x;
     const int n = counts_routed[e], keep_n = counts_kept[e];
     const int32_t* list = elist + routed_offsets[e];
+    const uint32_t* gkey = reinterpret_cast<const uint32_t*>(elist + A) + routed_offsets[e];
     const int base = offsets[e], dbase = drop_offsets[e];
+    const bool cached = n <= kSelKeys;
+    const bool partial = keep_n > 0 && keep_n < n;
+    if (cached && partial)
+        for (int i = tid; i < n; i += kSelThreads) skey[i] = gkey[i];
+    __syncthreads();
+    auto key_at = [&](int i) -> uint32_t { return cached ? skey[i] : __ldg(gkey + i); };
 
     uint32_t thr = 0;
     int need_eq = 0;
-    if (keep_n > 0 && keep_n < n) {
+    if (partial) {
         uint32_t prefix = 0, mask = 0;
         int rank = keep_n;  // 1-based rank, from the largest, of the last kept key
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int b = tid; b < 256; b += kSelThreads) hist[b] = 0;
+#pragma unroll
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+            for (int b = tid; b < 2048; b += kSelThreads) hist[b] = 0;
             __syncthreads();
             for (int i = tid; i < n; i += kSelThreads) {
-                const uint32_t key = order_key(gate[list[i]]);
-                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+                const uint32_t key = key_at(i);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1);
             }
             __syncthreads();
-            if (tid == 0) {
-                int cum = 0, b = 255;
-                for (; b > 0; --b) {
-                    if (cum + hist[b] >= rank) break;
-                    cum += hist[b];
+            // thread t owns bins 4t..4t+3; count the keys in all higher bins
+            int own = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) own += hist[4 * tid + q];
+            const int below = sel_excl_scan(own, warp_sums, &totals[0]);  // keys in the bins of lower threads
+            int cum = totals[0] - below - own;                             // keys in the bins of higher threads
+            for (int q = 3; q >= 0; --q) {
+                const int b = 4 * tid + q;
+                const int h = hist[b];
+                if (cum < rank && cum + h >= rank) {
+                    sel_bin = b;
+                    sel_rank = rank - cum;
                 }
-                sel_bin = b;
-                sel_rank = rank - cum;
+                cum += h;
             }
             __syncthreads();
             prefix |= uint32_t(sel_bin) << shift;
-            mask |= 0xFFu << shift;
+            mask |= dmask << shift;
             rank = sel_rank;
+            __syncthreads();
         }
         thr = prefix;
         need_eq = rank;
     }
 
-    int carry_eq = 0, carry_keep = 0, carry_drop = 0;
+    int carry_gt = 0, carry_eq = 0;
     for (int i0 = 0; i0 < n; i0 += kSelThreads) {
         const int i = i0 + tid;
         const bool valid = i < n;
         const int a = valid ? list[i] : 0;
-        const uint32_t key = valid ? order_key(gate[a]) : 0u;
+        int kept_before;
         bool keep;
-        int eq_rank = 0;
         if (keep_n >= n) {
             keep = valid;
+            kept_before = i;
         } else if (keep_n == 0) {
             keep = false;
+            kept_before = 0;
         } else {
-            const bool is_eq = valid && key == thr;
-            eq_rank = carry_eq + sel_excl_scan(is_eq ? 1 : 0, warp_sums, &totals[0]);
-            keep = valid && (key > thr || (is_eq && eq_rank < need_eq));
-            carry_eq += totals[0];
+            const uint32_t key = valid ? key_at(i) : 0u;
+            const bool gt = valid && key > thr, eq = valid && key == thr;
+            const int packed = (gt ? 1 << 16 : 0) | (eq ? 1 : 0);
+            const int excl = sel_excl_scan(packed, warp_sums, &totals[0]);
+            const int gt_before = carry_gt + (excl >> 16), eq_before = carry_eq + (excl & 0xFFFF);
+            keep = gt || (eq && eq_before < need_eq);
+            kept_before = gt_before + min(eq_before, need_eq);
+            carry_gt += totals[0] >> 16;
+            carry_eq += totals[0] & 0xFFFF;
         }
-        const int kr = carry_keep + sel_excl_scan(keep ? 1 : 0, warp_sums, &totals[1]);
-        const int dr = carry_drop + sel_excl_scan((valid && !keep) ? 1 : 0, warp_sums, &totals[2]);
         if (keep) {
-            pos[a] = base + kr;
-            row_src[base + kr] = a;
+            pos[a] = base + kept_before;
+            row_src[base + kept_before] = a;
         } else if (valid) {
             pos[a] = -1;
-            drop_list[dbase + dr] = a;
+            drop_list[dbase + (i - kept_before)] = a;
         }
-        carry_keep += totals[1];
-        carry_drop += totals[2];
     }
 }
 
@@ -375,10 +428,11 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
                                         a.rank_offsets, a.n_dropped);
     scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, a.E_capped, nblk, a.capacity, a.hist,
                                                         a.offsets, a.drop_offsets, a.routed_offsets,
-                                                        by_gate ? a.elist : nullptr, a.pos, a.row_src, a.drop_list);
+                                                        by_gate ? a.elist : nullptr, a.topk_gate, a.pos, a.row_src,
+                                                        a.drop_list);
     if (by_gate)
-        select_kernel<<<a.E, kSelThreads, 0, stream>>>(a.elist, a.routed_offsets, a.counts_routed, a.counts_kept,
-                                                       a.offsets, a.drop_offsets, a.topk_gate, a.pos, a.row_src,
+        select_kernel<<<a.E, kSelThreads, 0, stream>>>(a.elist, A, a.routed_offsets, a.counts_routed,
+                                                       a.counts_kept, a.offsets, a.drop_offsets, a.pos, a.row_src,
                                                        a.drop_list);
     if (padded && a.capacity > 0)
         pad_rows_kernel<<<dim3(unsigned((a.capacity + 7) / 8), unsigned(a.E)), 256, 0, stream>>>(
@@ -469,8 +523,8 @@ cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream) {
                                         a.send_offsets, a.drop_offsets, a.routed_offsets, a.rank_offsets,
                                         a.n_dropped);
     scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, a.D, nblk, -1, a.hist, a.send_offsets,
-                                                        a.drop_offsets, a.routed_offsets, nullptr, a.send_pos,
-                                                        a.send_src, nullptr);
+                                                        a.drop_offsets, a.routed_offsets, nullptr, nullptr,
+                                                        a.send_pos, a.send_src, nullptr);
     gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.send_pos,
                                                       static_cast<uint4*>(a.xsend), a.T, a.D, vec_per_row, A2);
     fanout_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x),

@@ -73,7 +73,7 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
     const int N = cfg->E + cfg->n_shared, K = cfg->k + cfg->n_shared;
     const int64_t A = int64_t(cfg->T) * K;
     const size_t hist_ints = size_t(N) * size_t(dispatch_blocks(A));
-    const size_t list_ints = by_gate ? size_t(A) : 0;
+    const size_t list_ints = by_gate ? 2 * size_t(A) : 0;  // assignment ids, then their gates' order keys
     if (64 + hist_ints + 2 * size_t(N) + 1 + list_ints > kStaticScratchInts) return MOE_ERR_WORKSPACE;
 
     int32_t* scratch = nullptr;

@@ -56,7 +56,7 @@ struct DispatchArgs {
     int32_t* hist;         // [E * nblk]
     int32_t* drop_offsets; // [E]
     int32_t* routed_offsets; // [E+1] exclusive scan of the routed counts (gate policy)
-    int32_t* elist;          // [T*k] each expert's assignments in token order (gate policy)
+    int32_t* elist;          // [2*T*k] each expert's assignments in token order, then their gate keys (gate policy)
     bool skip_gather;        // leave xperm to launch_dedup
 };
 

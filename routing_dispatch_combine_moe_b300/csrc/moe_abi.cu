@@ -123,7 +123,7 @@ Layout layout(const moe_config* c) {
     L.hist = take(sizeof(int32_t) * size_t(N) * nblk);
     L.drop_offsets = take(sizeof(int32_t) * size_t(N));
     L.routed_offsets = take(sizeof(int32_t) * size_t(N + 1));
-    L.elist = take(c->drop_policy == MOE_DROP_LOW_GATE ? sizeof(int32_t) * A : 0);
+    L.elist = take(c->drop_policy == MOE_DROP_LOW_GATE ? 2 * sizeof(int32_t) * A : 0);  // ids, then gate keys
     const bool dd = c->dedup != 0;
     const size_t TD = size_t(c->T) * size_t(c->D);
     L.dd_slots = take(dd ? sizeof(int32_t) * TD : 0);

@@ -273,23 +273,25 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (t >= T) return;
+    // Padding lanes (e >= E) start at -inf, which the finite partials do not change.
+    // Every load is unconditional (indices clamped into range) so that all VPL * UB of
+    // them are in flight before the first add; slices past KS add zero.
     float v[VPL];
 #pragma unroll
     for (int q = 0; q < VPL; ++q) v[q] = (lane + 32 * q < E) ? 0.f : -INFINITY;
+    const float* base = partial + size_t(t) * E;
     for (int z0 = 0; z0 < KS; z0 += UB) {
         float pz[VPL][UB];
 #pragma unroll
         for (int q = 0; q < VPL; ++q) {
-            const int e = lane + 32 * q;
+            const int e = min(lane + 32 * q, E - 1);
 #pragma unroll
-            for (int u = 0; u < UB; ++u)
-                pz[q][u] = (e < E && z0 + u < KS) ? __ldg(partial + (size_t(z0 + u) * T + t) * E + e) : 0.f;
+            for (int u = 0; u < UB; ++u) pz[q][u] = __ldg(base + size_t(min(z0 + u, KS - 1)) * T * E + e);
         }
 #pragma unroll
         for (int q = 0; q < VPL; ++q)
 #pragma unroll
-            for (int u = 0; u < UB; ++u)
-                if (lane + 32 * q < E && z0 + u < KS) v[q] += pz[q][u];
+            for (int u = 0; u < UB; ++u) v[q] += (z0 + u < KS) ? pz[q][u] : 0.f;
     }
     if (bias) {
 #pragma unroll
