@@ -41,6 +41,9 @@ Sources (page title, then section):
           each destination node that holds any of its experts, so 8 uniformly
           random experts over 8 nodes touch 8 (1 - (7/8)^8) ~ 5.25 nodes, of which
           7 (1 - (7/8)^8) ~ 4.6 are remote.
+* [FP8]   same page, same section and "Decode": FP8 dispatch sends the token rows in
+          FP8 (e4m3) with scale tensors, halving the dispatch bytes, while the
+          combine may stay in BF16; the decode example counts 128-element blocks.
 
 Readings where the pages are silent (each is listed in the design notes too):
 
@@ -71,6 +74,12 @@ Readings where the pages are silent (each is listed in the design notes too):
   as walking the experts in KeepTopK order and skipping an expert whose group would
   be the (M+1)-th distinct group. The gates are the kept softmax over the k kept
   logits, as without the limit.
+* FP8 dispatch [FP8] (the pages give the format, not the scale rule): every
+  128-element block of a token row (the last block of a row may be shorter) gets
+  a power-of-two scale 2^s, s the smallest integer with amax / 2^s <= 448 (448 is
+  e4m3's largest finite value; an all-zero block takes s = 0); each element is
+  x / 2^s rounded to the nearest e4m3 value (ties to the even code); the receiver
+  multiplies back by 2^s, which is exact, so the experts see q * 2^s.
 * deduplicated dispatch [DEDUP]: with D virtual ranks (rank r owns routed experts
   [r E/D, (r+1) E/D)), token t sends one row to rank r when at least one of its
   kept routed assignments lives there; send rows are rank-major, in token order
@@ -105,6 +114,8 @@ __all__ = [
     "group_allowed",
     "group_tie_flags",
     "dedup_send",
+    "e4m3_values",
+    "quantize_fp8_blocks",
     "round_to_bf16",
 ]
 
@@ -363,6 +374,71 @@ def dedup_send(idx, pos, n_routed: int, D: int) -> dict:
                 send_src=np.asarray(send_src, np.int64), fan_src=fan_src, n_send=len(send_src))
 
 
+# ------------------------------------------------------------------- FP8 dispatch
+def e4m3_values() -> np.ndarray:
+    """The value of each of the 256 e4m3 codes (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent 0 is subnormal, m * 2^-9; codes 0x7F and 0xFF are NaN,
+    there is no infinity), float64.  [FP8]"""
+    v = np.empty(256)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        ex, man = (c >> 3) & 0xF, c & 0x7
+        if ex == 0xF and man == 0x7:
+            v[c] = np.nan
+        elif ex == 0:
+            v[c] = sign * man * 2.0 ** -9
+        else:
+            v[c] = sign * (1 + man / 8) * 2.0 ** (ex - 7)
+    return v
+
+
+def _e4m3_round(a) -> np.ndarray:
+    """Code of the nearest finite e4m3 value to each element: the magnitude is rounded
+    to the nearest of the codes 0x00..0x7E (ties: the even code), then the sign bit is
+    set for negative inputs (-0.0 included), as an IEEE-style rounding does."""
+    a = np.asarray(a, np.float64)
+    mags = e4m3_values()[:0x7F]           # codes 0x00..0x7E, increasing magnitudes
+    m = np.abs(a).ravel()
+    hi = np.clip(np.searchsorted(mags, m), 1, 0x7E)
+    lo = hi - 1
+    dlo, dhi = m - mags[lo], mags[hi] - m
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    pick = np.where(m >= mags[-1], 0x7E, pick)
+    neg = np.signbit(a.ravel())
+    return (pick | np.where(neg, 0x80, 0)).astype(np.uint8).reshape(a.shape)
+
+
+def quantize_fp8_blocks(x, block: int = 128) -> dict:
+    """Per-block e4m3 quantization of the rows of ``x`` [rows, d].  [FP8]
+
+    Returns codes [rows, d] uint8, scale exponents s [rows, ceil(d/block)] int64, the
+    scales 2^s (float64) and the dequantized rows q * 2^s (float64).
+    """
+    x = _f64(x)
+    rows, d = x.shape
+    nb = -(-d // block)
+    exps = np.zeros((rows, nb), np.int64)
+    codes = np.zeros((rows, d), np.uint8)
+    deq = np.zeros_like(x)
+    vals = e4m3_values()
+    for r in range(rows):
+        for b in range(nb):
+            seg = x[r, b * block:(b + 1) * block]
+            amax = np.abs(seg).max()
+            s = 0
+            if amax > 0:
+                s = math.ceil(math.log2(amax / 448.0))
+                while amax / 2.0 ** s > 448.0:  # guard the log against rounding
+                    s += 1
+                while amax / 2.0 ** (s - 1) <= 448.0:
+                    s -= 1
+            exps[r, b] = s
+            c = _e4m3_round(seg / 2.0 ** s)
+            codes[r, b * block:(b + 1) * block] = c
+            deq[r, b * block:(b + 1) * block] = vals[c] * 2.0 ** s
+    return dict(codes=codes, exps=exps, scales=2.0 ** exps, deq=deq)
+
+
 # -------------------------------------------------------------------------- experts
 def silu(z):
     """silu(z) = z / (1 + e^-z)."""
@@ -408,7 +484,7 @@ def combine(G, pos, out, T: int, k: int) -> np.ndarray:
 
 def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, n_shared: int = 0,
                 drop_policy: str = "token", layout: str = "packed", n_groups: int = 0,
-                topk_groups: int = 0) -> dict:
+                topk_groups: int = 0, dispatch_dtype: str = "act") -> dict:
     """The whole layer: logits, KeepTopK, kept softmax, dispatch, experts, combine.
 
     ``expert_fn(e, X)`` returns Expert_e applied to the rows X (an [M, d] float64
@@ -418,7 +494,9 @@ def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, 
     selection is group-limited [NODE]. Returns every intermediate the GPU path
     exposes, in float64 (y is not rounded); ``idx`` and ``G`` then have k + n_shared
     slots. The deduplicated send buffer changes where rows travel, not their values,
-    so y does not depend on it (``dedup_send`` describes it).
+    so y does not depend on it (``dedup_send`` describes it). With ``dispatch_dtype``
+    "fp8" the rows travel as per-block e4m3 codes [FP8] and the experts receive the
+    dequantized rows; shared experts are replicated and read x itself.
     """
     x = _f64(x)
     T, d = x.shape
@@ -438,6 +516,10 @@ def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, 
     rs = disp["row_src"]
     xperm = np.zeros((rs.size, d))
     xperm[rs >= 0] = x[rs[rs >= 0] // k]  # padding rows (row_src -1) stay zero
+    if dispatch_dtype == "fp8":
+        xq = quantize_fp8_blocks(x)["deq"]
+        routed = (rs >= 0) & (idx.reshape(-1)[np.maximum(rs, 0)] < E)
+        xperm[routed] = xq[rs[routed] // k]
     out = np.zeros_like(xperm)
     off = disp["offsets"]
     for e in range(E + n_shared):

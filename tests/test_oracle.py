@@ -531,3 +531,55 @@ def test_dedup_skips_shared_experts():
     d = orc.dispatch(idx, E + S, None, 2, capped_experts=E)
     s = orc.dedup_send(idx, d["pos"], E, 2)
     assert s["n_send"] == 2 * T and np.all(s["fan_src"].reshape(T, 3)[:, 2] == -1)
+
+
+# ------------------------------------------------------------ FP8 dispatch
+def test_e4m3_table():
+    v = orc.e4m3_values()
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.sum(~np.isnan(v)) == 254
+    assert v[0x7E] == 448.0 and v[0x38] == 1.0 and v[0x01] == 2.0 ** -9 and v[0x08] == 2.0 ** -6
+    assert np.array_equal(v[0x80:0xFF], -v[0x00:0x7F]) and np.all(np.diff(v[:0x7F]) > 0)
+
+
+def test_e4m3_rounding_matches_torch_float8():
+    r = rng(50)
+    x = r.normal(size=50000) * r.choice([1e-3, 0.05, 1.0, 30.0, 300.0], 50000)
+    x = x[np.abs(x) <= 448].astype(np.float32).astype(np.float64)
+    ref = torch.tensor(x, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc._e4m3_round(x), ref)
+
+
+def test_e4m3_rounding_hand_cases():
+    cases = [(1.0625, 0x38),          # halfway between 1.0 (even) and 1.125
+             (1.1875, 0x3A),          # halfway between 1.125 and 1.25 (even)
+             (2.0 ** -10, 0x00),      # halfway between 0 and the smallest subnormal: +0
+             (-(2.0 ** -11), 0x80),   # rounds to zero, keeps its sign
+             (0.0, 0x00), (-0.0, 0x80), (448.0, 0x7E), (-448.0, 0xFE), (3.3, 0x45)]
+    for x, code in cases:
+        assert int(orc._e4m3_round(np.array([x]))[0]) == code, x
+
+
+def test_fp8_block_scales_and_error_bound():
+    x = np.zeros((4, 200))
+    x[0, 0], x[1, 5], x[2, 7] = 448.0, 449.0, 1.0    # first blocks: s = 0, 1, -8
+    x[3, 150] = -3.0                                 # ragged second block (72 elements)
+    q = orc.quantize_fp8_blocks(x)
+    assert q["exps"].tolist() == [[0, 0], [1, 0], [-8, 0], [0, -7]]
+    assert q["deq"][1, 5] == 448.0 and q["deq"][3, 150] == -3.0 and not q["deq"][0, 1:].any()
+    r = rng(51)
+    x = r.normal(size=(16, 384)) * np.exp(r.normal(size=(16, 1)) * 3)
+    q = orc.quantize_fp8_blocks(x)
+    s = np.repeat(q["exps"], 128, axis=1)
+    amax = np.abs(x).reshape(16, 3, 128).max(axis=2)
+    assert np.all(amax / 2.0 ** q["exps"] <= 448) and np.all(amax / 2.0 ** (q["exps"] - 1) > 448)  # smallest s
+    err = np.abs(q["deq"] - x)
+    assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** (s - 10)))
+    again = orc.quantize_fp8_blocks(q["deq"])       # dequantized rows are fixed points
+    assert np.array_equal(again["deq"], q["deq"]) and np.array_equal(again["codes"], q["codes"])
+
+
+def test_fp8_forward_sends_the_dequantized_rows():
+    w = wl.Workload("t", T=40, d=256, E=4, k=1, F=0, act="bf16", expert="identity")
+    inp = wl.make_inputs(w, seed=52)
+    res = orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), 1, lambda e, X: X, dispatch_dtype="fp8")
+    np.testing.assert_array_equal(res["y"], orc.quantize_fp8_blocks(f64(inp["x"]))["deq"])
