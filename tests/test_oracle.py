@@ -574,8 +574,9 @@ def test_fp8_block_scales_and_error_bound():
     assert np.all(amax / 2.0 ** q["exps"] <= 448) and np.all(amax / 2.0 ** (q["exps"] - 1) > 448)  # smallest s
     err = np.abs(q["deq"] - x)
     assert np.all(err <= np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** (s - 10)))
-    again = orc.quantize_fp8_blocks(q["deq"])       # dequantized rows are fixed points
-    assert np.array_equal(again["deq"], q["deq"]) and np.array_equal(again["codes"], q["codes"])
+    # dequantized rows are fixed points (their codes may differ: a block's amax can round
+    # down to a value that takes a smaller scale)
+    assert np.array_equal(orc.quantize_fp8_blocks(q["deq"])["deq"], q["deq"])
 
 
 def test_fp8_forward_sends_the_dequantized_rows():
