@@ -167,16 +167,25 @@ def load_traffic(workload: str, kernel: str):
 
 
 # ------------------------------------------------------------------ algorithmic work
-def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0) -> dict:
+def fp8_row_bytes(d: int) -> int:
+    """Wire bytes of one FP8-dispatched row: d e4m3 codes and a 4-byte scale per 128-element block."""
+    return d + 4 * ((d + 127) // 128)
+
+
+def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, routed_rows: int = 0) -> dict:
     """Algorithmic work per launch: flops of the formulas, bytes each kernel must move at least.
 
     With the deduplicated dispatch the rows travel x -> send buffer -> expert rows: x is
     read once, each send row written once and read once, each expert row written once.
+    With the FP8 dispatch each routed row is written as codes + scales, read back and
+    written as a bf16 row.
     """
     b = w.act_bytes
     up, down = sizing.expert_gemm_flops(rows, w.d, w.F, w.expert)
     ident = w.expert == "identity"
     dispatch = sizing.dispatch_hbm_bytes(w.T, w.d, rows, b) + (2 * rows_sent * w.d * b if w.dedup else 0)
+    if w.dispatch_dtype == "fp8":
+        dispatch += 2 * routed_rows * fp8_row_bytes(w.d)
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
         route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.slots * 8,
@@ -341,7 +350,12 @@ def run_ours(args, w, world, rank, local):
                  "remote_send_bytes": int((rows_sent - send_counts[0]) * w.d * w.act_bytes),
                  "remote_bytes_without_dedup": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),
                  "uniform_routing_ranks_per_token": sizing.expected_nodes_touched(w.k, w.D)}
-    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0)
+    routed_rows = int(kept[:w.E].sum())
+    fp8 = None
+    if w.dispatch_dtype == "fp8":
+        fp8 = {"wire_bytes": routed_rows * fp8_row_bytes(w.d), "bf16_wire_bytes": routed_rows * w.d * 2,
+               "ratio": fp8_row_bytes(w.d) / (w.d * 2)}
+    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0, routed_rows)
     peaks, peak_src = load_peaks()
     value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
     dc_bytes = work["dispatch_bytes"] + work["combine_bytes"]
@@ -398,6 +412,7 @@ def run_ours(args, w, world, rank, local):
                    "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
                    "precision": w.precision, "drop_policy": w.drop_policy, "layout": w.layout,
                    "n_groups": w.n_groups, "topk_groups": w.topk_groups, "dedup": w.dedup,
+                   "dispatch_dtype": w.dispatch_dtype,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
                          "dispatched rows" % (w.n_experts * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
@@ -411,6 +426,7 @@ def run_ours(args, w, world, rank, local):
         if gemm_ms > 0 and gemm_flops else None,
         "stage_ms": stage_ms,
         "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "dedup": dedup,
+                    "fp8_dispatch": fp8,
                     "group_limit": [w.topk_groups, w.n_groups] if 0 < w.topk_groups < w.n_groups else None, "hist": sizing.histogram_summary(counts),
                     "rank_imbalance": sizing.imbalance_ratio(np.diff(rank_offs)),
                     "remote_dispatch_bytes": sizing.remote_dispatch_bytes(rank_offs, w.d, w.act_bytes),

@@ -98,6 +98,13 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
                                [E, C, d] buffer with under-full experts padded); needs capacity >= 0
                                and n_shared == 0. offsets[e] = e*C, so the experts run on all C rows. */
 
+/* Wire format of the dispatched rows. */
+#define MOE_DISPATCH_ACT 0 /* rows in the activation dtype */
+#define MOE_DISPATCH_FP8 1 /* routed rows as e4m3 codes with one power-of-two fp32 scale per 128-element
+                              block ("MoE Expert Parallelism Sizing", "First-order dispatch and combine
+                              bytes": FP8 dispatch halves the row, the combine stays wide); the receiving
+                              side turns them back into bf16 rows (exact); bf16 activations only */
+
 /* Limits of this build. */
 #define MOE_MAX_K 16        /* experts per token, routed plus shared */
 #define MOE_MAX_E 512       /* experts, routed plus shared */
@@ -124,6 +131,7 @@ typedef struct moe_config {
     int32_t dedup;       /* 1: moe_layer_forward sends each token once per virtual rank (the
                           * deduplicated dispatch, see moe_dispatch_dedup) and fans the send rows
                           * out into the expert rows; D <= 16. 0: rows go straight from x. */
+    int32_t dispatch_dtype; /* MOE_DISPATCH_*; FP8 needs bf16 activations and no dedup */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
@@ -162,6 +170,8 @@ typedef struct moe_workspace_view {
                           * padding rows of out unwritten */
     moe_send_map send;   /* cfg->dedup only (NULL pointers otherwise) */
     void* xsend;         /* [T*D, d] act: the deduplicated send buffer (cfg->dedup only) */
+    uint8_t* xq;         /* [rows, d] e4m3 codes of the routed rows (MOE_DISPATCH_FP8 only) */
+    float* xscale;       /* [rows, ceil(d/128)] their block scales (MOE_DISPATCH_FP8 only) */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -248,6 +258,24 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
 int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
                        const moe_send_map* map, void* xsend, void* xperm, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
+
+/* FP8 dispatch of the rows a moe_dispatch with the same cfg mapped (its pos, row_src
+ * and offsets): each token row is quantized once, per 128-element block, to e4m3 codes
+ * with the scale 2^s, s the smallest integer with amax/2^s <= 448 (round to nearest,
+ * ties to even, sign kept), and written to each of its kept routed rows
+ * ("MoE Expert Parallelism Sizing", "First-order dispatch and combine bytes": the
+ * FP8 dispatch row with its scale tensors). Shared experts are replicated: their rows
+ * are copied from x into xperm. With xperm non-NULL the receiving side also turns the
+ * routed rows back into bf16 (exactly q * 2^s).
+ *   x       [T, d] bf16;  topk_idx [T, K];  map: pos, row_src and offsets from moe_dispatch
+ *   xq      [rows, d] uint8 out;  xscale [rows, ceil(d/128)] fp32 out (rows = moe_rows_capacity)
+ *   xperm   [rows, d] bf16 out, or NULL (shared rows then need a moe_dispatch gather)
+ *   ws      >= moe_dispatch_workspace_bytes(cfg); its first 4 bytes are the status word,
+ *           cleared by this call.
+ * Needs cfg->dispatch_dtype == MOE_DISPATCH_FP8. Bit-exact and deterministic. */
+int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                     const moe_dispatch_map* map, uint8_t* xq, float* xscale, void* xperm, void* ws,
+                     size_t ws_bytes, moe_stream_t stream);
 
 /* Grouped expert FFN over the dispatched rows: for each expert e, rows
  * [offsets[e], offsets[e+1]) of xperm go through Expert_e ("EP Math", "What expert

@@ -60,4 +60,5 @@ def run_oracle(w, inp: dict, capacity="auto", faithful: bool = False, cache=None
     return orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), w.k, fn, capacity=capacity,
                            bias=f64(inp.get("bias")), D=w.D, n_shared=getattr(w, "n_shared", 0),
                            drop_policy=getattr(w, "drop_policy", "token"), layout=getattr(w, "layout", "packed"),
-                           n_groups=getattr(w, "n_groups", 0), topk_groups=getattr(w, "topk_groups", 0))
+                           n_groups=getattr(w, "n_groups", 0), topk_groups=getattr(w, "topk_groups", 0),
+                           dispatch_dtype=getattr(w, "dispatch_dtype", "act"))

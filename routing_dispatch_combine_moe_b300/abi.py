@@ -29,6 +29,8 @@ MOE_DROP_TOKEN_ORDER, MOE_DROP_LOW_GATE = 0, 1
 DROP_POLICIES = {"token": MOE_DROP_TOKEN_ORDER, "gate": MOE_DROP_LOW_GATE}
 MOE_LAYOUT_PACKED, MOE_LAYOUT_PADDED = 0, 1
 LAYOUTS = {"packed": MOE_LAYOUT_PACKED, "padded": MOE_LAYOUT_PADDED}
+MOE_DISPATCH_ACT, MOE_DISPATCH_FP8 = 0, 1
+DISPATCH_DTYPES = {"act": MOE_DISPATCH_ACT, "fp8": MOE_DISPATCH_FP8}
 MOE_MAX_K, MOE_MAX_E = 16, 512
 EXPERT_KINDS = {"identity": MOE_EXPERT_IDENTITY, "relu": MOE_EXPERT_RELU, "swiglu": MOE_EXPERT_SWIGLU}
 ACT_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
@@ -50,7 +52,7 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", _i32), ("d", _i32), ("E", _i32), ("k", _i32), ("F", _i32), ("D", _i32),
                 ("act_dtype", _i32), ("expert_kind", _i32), ("precision", _i32), ("n_shared", _i32),
                 ("capacity", _i64), ("drop_policy", _i32), ("layout", _i32), ("n_groups", _i32),
-                ("topk_groups", _i32), ("dedup", _i32)]
+                ("topk_groups", _i32), ("dedup", _i32), ("dispatch_dtype", _i32)]
 
 
 class moe_dispatch_map(ctypes.Structure):
@@ -64,7 +66,8 @@ class moe_send_map(ctypes.Structure):
 
 class moe_workspace_view(ctypes.Structure):
     _fields_ = [("status", _p), ("topk_idx", _p), ("topk_gate", _p), ("map", moe_dispatch_map),
-                ("xperm", _p), ("h", _p), ("out", _p), ("send", moe_send_map), ("xsend", _p)]
+                ("xperm", _p), ("h", _p), ("out", _p), ("send", moe_send_map), ("xsend", _p), ("xq", _p),
+                ("xscale", _p)]
 
 
 _SIGNATURES = {
@@ -89,6 +92,8 @@ _SIGNATURES = {
     "moe_layer_forward_host": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_dispatch_dedup": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_send_map), _p,
                                           _p, _p, _sz, _p]),
+    "moe_dispatch_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
+                                        _p, _p, _p, _sz, _p]),
     "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_dispatch_map),
                                            _p, _p]),
     "moe_read_status": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
@@ -144,13 +149,14 @@ def _stream(stream=None):
 # ------------------------------------------------------------------ config
 def make_config(T, d, E, k, F=0, D=1, act="bf16", expert="swiglu", capacity=None, precision="f32_out",
                 n_shared=0, drop_policy="token", layout="packed", n_groups=0, topk_groups=0,
-                dedup=False) -> moe_config:
+                dedup=False, dispatch_dtype="act") -> moe_config:
     """A moe_config; ``capacity`` None (dropless) or a non-negative integer."""
     return moe_config(T=T, d=d, E=E, k=k, F=F, D=D, act_dtype=ACT_DTYPES[act],
                       expert_kind=EXPERT_KINDS[expert], precision=PRECISIONS[precision], n_shared=n_shared,
                       capacity=-1 if capacity is None else int(capacity),
                       drop_policy=DROP_POLICIES[drop_policy], layout=LAYOUTS[layout], n_groups=n_groups,
-                      topk_groups=topk_groups, dedup=int(bool(dedup)))
+                      topk_groups=topk_groups, dedup=int(bool(dedup)),
+                      dispatch_dtype=DISPATCH_DTYPES[dispatch_dtype])
 
 
 def out_dtype(cfg) -> torch.dtype:
@@ -183,7 +189,7 @@ def config_for(w, capacity="auto") -> moe_config:
         capacity = None if w.capacity_factor is None else moe_capacity(w.T, w.k, w.E, w.capacity_factor,
                                                                        w.min_capacity)
     return make_config(w.T, w.d, w.E, w.k, w.F, w.D, w.act, w.expert, capacity, w.precision, w.n_shared,
-                       w.drop_policy, w.layout, w.n_groups, w.topk_groups, w.dedup)
+                       w.drop_policy, w.layout, w.n_groups, w.topk_groups, w.dedup, w.dispatch_dtype)
 
 
 def moe_validate_config(cfg) -> int:
@@ -247,6 +253,8 @@ class WorkspaceView:
     send_pos: int | None = None
     send_src: int | None = None
     xsend: int | None = None
+    xq: int | None = None
+    xscale: int | None = None
 
 
 def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
@@ -257,7 +265,7 @@ def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
     sm = v.send
     return WorkspaceView(v.status, v.topk_idx, v.topk_gate, m.counts_routed, m.counts_kept, m.offsets,
                          m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out,
-                         sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend)
+                         sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend, v.xq, v.xscale)
 
 
 # ------------------------------------------------------------------ hot path
@@ -292,6 +300,13 @@ def moe_dispatch_dedup(cfg, x, topk_idx, pos, smap: moe_send_map, xsend, xperm, 
     _check(lib().moe_dispatch_dedup(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(pos), ctypes.byref(smap),
                                     _ptr(xsend), _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_dispatch_dedup")
+
+
+def moe_dispatch_fp8(cfg, x, topk_idx, dmap: moe_dispatch_map, xq, xscale, xperm, ws, stream=None):
+    """FP8 (e4m3, per-128 power-of-two scales) rows of a moe_dispatch map; xperm may be None."""
+    _check(lib().moe_dispatch_fp8(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xq),
+                                  _ptr(xscale), _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_dispatch_fp8")
 
 
 def moe_dispatch_static(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, stream=None, topk_gate=None):

@@ -1,0 +1,146 @@
+// FP8 dispatch ("MoE Expert Parallelism Sizing: Traffic, Capacity, Fabric", "First-order
+// dispatch and combine bytes" and "Decode": the dispatched rows travel as FP8 with
+// scale tensors, half the bytes of BF16, while the combine stays wide).
+//
+// Wire format of one routed row: d e4m3 codes plus one fp32 scale 2^s per 128-element
+// block (the last block of a row may be shorter). s is the smallest integer with
+// amax / 2^s <= 448, so every x / 2^s is in e4m3's finite range and rounds (to nearest,
+// ties to even, sign kept) without saturating; the receiver's q * 2^s is exact in
+// bf16. Shared experts are replicated, not dispatched: their rows are copied from x.
+//
+//   gather_fp8_kernel   one warp per token: each half-warp takes one 128-element block
+//                       (16 lanes x 8 bf16), reduces its amax with shuffles, picks s,
+//                       converts its 8 values, and writes the 8 codes (and the scale)
+//                       to each of the token's kept routed rows;
+//   dequant_fp8_kernel  one warp per dispatched row: codes x scale back to bf16 rows
+//                       for the expert GEMMs (the receiving side).
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// Smallest s with amax / 2^s <= 448 (448 = 0.875 * 2^9); amax = m * 2^e, m in [0.5, 1).
+__device__ __forceinline__ int block_exponent(float amax) {
+    if (!(amax > 0.f)) return 0;
+    int e;
+    const float m = frexpf(amax, &e);
+    return e - 9 + (m > 0.875f ? 1 : 0);
+}
+
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ x,
+                                                         const int32_t* __restrict__ topk_idx,
+                                                         const int32_t* __restrict__ pos, int T, int K, int d,
+                                                         int E_routed, int64_t max_rows, uint8_t* __restrict__ xq,
+                                                         float* __restrict__ xscale, uint4* __restrict__ xperm,
+                                                         int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int nb = (d + 127) / 128, vpr = d / 8;  // 16-byte pieces per bf16 row
+    int p = -1, shared_dst = -1;
+    if (lane < K) {
+        const size_t a = size_t(t) * K + lane;
+        const int r = pos[a], e = topk_idx[a];
+        if (r >= max_rows) {
+            set_status(status, MOE_DEV_ERR_INDEX);
+        } else if (r >= 0) {
+            if (e >= 0 && e < E_routed) p = r;
+            else shared_dst = r;
+        }
+    }
+    int dst[MOE_MAX_K], sdst[MOE_MAX_K];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) {
+        dst[j] = __shfl_sync(0xFFFFFFFFu, p, j);
+        sdst[j] = __shfl_sync(0xFFFFFFFFu, shared_dst, j);
+    }
+    const uint4* src = x + size_t(t) * vpr;
+    // each iteration covers two 128-element blocks: lanes 0-15 and 16-31
+    for (int v0 = 0; v0 < vpr; v0 += 32) {
+        const int v = v0 + lane;
+        const bool ok = v < vpr;
+        const uint4 raw = ok ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        // shared experts take the bf16 row as it is
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j)
+            if (j < K && sdst[j] >= 0 && ok) xperm[size_t(sdst[j]) * vpr + v] = raw;
+        float f[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                      bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+        const int s = block_exponent(am);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t c = __nv_cvt_float_to_fp8(ldexpf(f[i], -s), __NV_SATFINITE, __NV_E4M3);
+            if (i < 4) lo |= c << (8 * i);
+            else hi |= c << (8 * (i - 4));
+        }
+        const int blk = v0 / 16 + (lane >> 4);  // 128-element block of this half-warp
+        const bool writes_scale = (lane & 15) == 0 && blk < nb;
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) {
+            if (j < K && dst[j] >= 0) {
+                if (ok) *reinterpret_cast<uint2*>(xq + size_t(dst[j]) * d + size_t(v) * 8) = make_uint2(lo, hi);
+                if (writes_scale) xscale[size_t(dst[j]) * nb + blk] = ldexpf(1.f, s);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restrict__ xq,
+                                                          const float* __restrict__ xscale,
+                                                          const int32_t* __restrict__ row_src,
+                                                          const int32_t* __restrict__ topk_idx,
+                                                          const int32_t* __restrict__ offsets, int n_offsets,
+                                                          int d, int E_routed, int64_t rows,
+                                                          uint4* __restrict__ xperm) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (r >= rows || r >= offsets[n_offsets]) return;
+    const int a = row_src[r];
+    if (a < 0) return;                         // padding row (zeroed by the dispatch)
+    const int e = topk_idx[a];
+    if (e < 0 || e >= E_routed) return;        // shared expert: the row came from x
+    const int nb = (d + 127) / 128, vpr = d / 8;
+    const uint8_t* q = xq + size_t(r) * d;
+    // each lane converts 8 codes (8 bytes) per step into one 16-byte bf16 piece
+    for (int v = lane; v < vpr; v += 32) {
+        const uint2 c = *reinterpret_cast<const uint2*>(q + size_t(v) * 8);
+        const float sc = xscale[size_t(r) * nb + (v * 8) / 128];
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = i < 4 ? c.x : c.y;
+            const __nv_fp8_storage_t code = __nv_fp8_storage_t((w >> (8 * (i & 3))) & 0xFFu);
+            const __half_raw h = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);
+            f[i] = __half2float(__half(h)) * sc;
+        }
+        xperm[size_t(r) * vpr + v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream) {
+    gather_fp8_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.topk_idx, a.pos, a.T,
+                                                          a.K, a.d, a.E_routed, a.rows, a.xq, a.xscale,
+                                                          static_cast<uint4*>(a.xperm), a.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !a.dequant) return e;
+    if (a.rows > 0)
+        dequant_fp8_kernel<<<unsigned((a.rows + 7) / 8), 256, 0, stream>>>(a.xq, a.xscale, a.row_src, a.topk_idx,
+                                                                            a.offsets, a.n_experts, a.d,
+                                                                            a.E_routed, a.rows,
+                                                                            static_cast<uint4*>(a.xperm));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

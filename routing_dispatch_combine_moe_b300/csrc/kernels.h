@@ -89,6 +89,26 @@ struct DedupArgs {
 
 cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream);
 
+// FP8 dispatch: e4m3 rows with power-of-two per-128 block scales for the kept routed
+// assignments (shared experts' rows copied from x into xperm), then, with `dequant`,
+// the receiving side's bf16 rows in xperm.
+struct Fp8Args {
+    int T, d, K, E_routed, n_experts;  // K: slots per token; n_experts: routed + shared
+    int64_t rows;                      // rows of xq / xscale / xperm
+    const void* x;
+    const int32_t* topk_idx;
+    const int32_t* pos;
+    const int32_t* row_src;
+    const int32_t* offsets;            // [n_experts + 1]; rows [0, offsets[n_experts]) are dispatched
+    uint8_t* xq;                       // [rows, d]
+    float* xscale;                     // [rows, ceil(d / 128)]
+    void* xperm;
+    bool dequant;
+    int32_t* status;
+};
+
+cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream);
+
 // `out_dtype` is the dtype of the expert outputs (MOE_F32 or MOE_BF16), `act_dtype` that of y.
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
                            void* y, int T, int d, int k, int64_t rows, int32_t* status, cudaStream_t stream);

@@ -90,6 +90,9 @@ int validate(const moe_config* c) {
         if (c->n_groups > 32) return MOE_ERR_UNSUPPORTED;
     }
     if (c->dedup && c->D > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
+    if (c->dispatch_dtype != MOE_DISPATCH_ACT && c->dispatch_dtype != MOE_DISPATCH_FP8) return MOE_ERR_ARG;
+    if (c->dispatch_dtype == MOE_DISPATCH_FP8 && (c->act_dtype != MOE_BF16 || c->dedup))
+        return MOE_ERR_UNSUPPORTED;
     if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX) || rows_cap(c) > int64_t(INT32_MAX))
         return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
@@ -104,6 +107,7 @@ struct Layout {
     // deduplicated dispatch (cfg->dedup): scratch in the dispatch part, outputs in the forward part
     size_t dd_slots, dd_hist, dd_kept, dd_drop, dd_routed, dd_rank, dd_ndrop;
     size_t send_counts, send_offsets, send_pos, send_src, xsend;
+    size_t xq, xscale;  // FP8 dispatch
     size_t dispatch_end, forward_end, host_end;
 };
 
@@ -159,6 +163,9 @@ Layout layout(const moe_config* c) {
     L.send_pos = take(dd ? sizeof(int32_t) * TD : 0);
     L.send_src = take(dd ? sizeof(int32_t) * TD : 0);
     L.xsend = take(dd ? b * TD * size_t(c->d) : 0);
+    const bool f8 = c->dispatch_dtype == MOE_DISPATCH_FP8;
+    L.xq = take(f8 ? R * size_t(c->d) : 0);
+    L.xscale = take(f8 ? sizeof(float) * R * size_t((c->d + 127) / 128) : 0);
     L.forward_end = o;
     L.x_stage = take(b * size_t(c->T) * c->d);
     L.y_stage = take(b * size_t(c->T) * c->d);
@@ -193,6 +200,9 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->send.send_pos = dd ? at<int32_t>(ws, L.send_pos) : nullptr;
     v->send.send_src = dd ? at<int32_t>(ws, L.send_src) : nullptr;
     v->xsend = dd ? at<void>(ws, L.xsend) : nullptr;
+    const bool f8 = c->dispatch_dtype == MOE_DISPATCH_FP8;
+    v->xq = f8 ? at<uint8_t>(ws, L.xq) : nullptr;
+    v->xscale = f8 ? at<float>(ws, L.xscale) : nullptr;
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
@@ -263,6 +273,26 @@ int run_dedup(const moe_config* c, const void* x, const int32_t* idx, const int3
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch_dedup");
 }
 
+int run_fp8(const moe_config* c, const void* x, const int32_t* idx, const moe_dispatch_map* m, uint8_t* xq,
+            float* xscale, void* xperm, void* ws, cudaStream_t s) {
+    const Layout L = layout(c);
+    Fp8Args a{};
+    a.T = c->T; a.d = c->d; a.K = n_slots(c); a.E_routed = c->E; a.n_experts = n_experts(c);
+    a.rows = rows_cap(c);
+    a.x = x;
+    a.topk_idx = idx;
+    a.pos = m->pos;
+    a.row_src = m->row_src;
+    a.offsets = m->offsets;
+    a.xq = xq;
+    a.xscale = xscale;
+    a.xperm = xperm;
+    a.dequant = xperm != nullptr;
+    a.status = at<int32_t>(ws, L.status);
+    const cudaError_t e = launch_fp8_dispatch(a, s);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch_fp8");
+}
+
 int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const int32_t* counts, const void* W13,
             const void* W2, void* h, void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
     FfnArgs a{};
@@ -325,8 +355,10 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
-    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0)) != MOE_OK)
+    const bool f8 = c->dispatch_dtype == MOE_DISPATCH_FP8;
+    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0 || f8)) != MOE_OK)
         return rc;
+    if (f8 && (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, v.xperm, ws, s)) != MOE_OK) return rc;
     if (c->dedup && (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
@@ -397,7 +429,8 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
-    return 2 + 4 + select + pad + dedup + ffn + 1;
+    const int fp8 = cfg->dispatch_dtype == MOE_DISPATCH_FP8 ? 1 : 0;  // dequant (the gather quantizes)
+    return 2 + 4 + select + pad + dedup + fp8 + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {
@@ -451,6 +484,23 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
     const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     return run_dedup(cfg, x, topk_idx, pos, map, xsend, xperm, ws, stream);
+}
+
+int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx, const moe_dispatch_map* map,
+                     uint8_t* xq, float* xscale, void* xperm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (cfg->dispatch_dtype != MOE_DISPATCH_FP8) return MOE_ERR_ARG;
+    const bool rows = rows_cap(cfg) > 0;
+    if (!x || !topk_idx || !map || !map->pos || !map->row_src || !map->offsets || !ws || (rows && (!xq || !xscale)))
+        return MOE_ERR_ARG;
+    if (!aligned16(x) || (xperm && !aligned16(xperm)) || (xq && !aligned16(xq)) || (xscale && !aligned4(xscale)) ||
+        !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_fp8(cfg, x, topk_idx, map, xq, xscale, xperm, ws, stream);
 }
 
 int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets, const void* W13, const void* W2,

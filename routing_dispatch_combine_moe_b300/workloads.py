@@ -59,6 +59,7 @@ class Workload:
     n_groups: int = 0           # expert groups for group-limited routing (with topk_groups)
     topk_groups: int = 0        # 0 < M < n_groups: each token keeps experts of at most M groups
     dedup: bool = False         # send each token once per virtual rank, then fan out
+    dispatch_dtype: str = "act"  # "fp8": routed rows travel as e4m3 with per-128 block scales
     note: str = field(default="", compare=False)
 
     @property
@@ -109,12 +110,16 @@ WORKLOADS: dict[str, Workload] = {
                  n_groups=8, topk_groups=4, dedup=True,
                  note="DeepSeek-V3 routing shape with each token limited to 4 of 8 expert groups (one "
                       "group per virtual rank) and the send buffer deduplicated per rank"),
+        Workload("mixtral_fp8_dispatch", T=2048, d=4096, E=8, k=2, F=14336, act="bf16", expert="swiglu",
+                 dispatch_dtype="fp8",
+                 note="the Mixtral-shaped layer with its dispatched rows sent as e4m3 codes and "
+                      "per-128 power-of-two scales"),
     ]
 }
 
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
-                  "dsv3_grouped_dedup"]
+                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

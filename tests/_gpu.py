@@ -88,6 +88,9 @@ class StageBuffers:
         self.ws_dispatch = torch.zeros(abi.moe_dispatch_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.ws_ffn = torch.zeros(abi.moe_ffn_workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        if w.dispatch_dtype == "fp8":
+            self.xq = torch.full((R, w.d), 0xAB, dtype=torch.uint8, device=device)
+            self.xscale = torch.full((R, (w.d + 127) // 128), float("nan"), dtype=torch.float32, device=device)
         if w.dedup:
             TD = w.T * w.D
             self.send_counts = torch.full((w.D,), -7, **i32)
@@ -266,6 +269,32 @@ def check_dedup(w, inp, bufs, st, d) -> dict:
     rows = d["row_src"].size
     assert torch.equal(fanned[:rows], direct[:rows]), "fanned-out rows differ from the direct gather"
     return s
+
+
+def check_fp8(w, inp, bufs, st, d) -> dict:
+    """FP8 dispatch of the synthetic ids' dispatch map ``d``: every routed row's e4m3
+    codes and block scales bit-exact against the oracle's quantization of its token,
+    the receiving side's bf16 rows equal to the oracle's dequantized values, shared
+    experts' rows equal to x."""
+    rows_out = torch.full_like(bufs.xperm, float("nan"))
+    abi.moe_dispatch_fp8(bufs.cfg, inp["x"], st["topk_idx"], bufs.dmap(), bufs.xq, bufs.xscale, rows_out,
+                         bufs.ws_dispatch)
+    q = orc.quantize_fp8_blocks(f64(inp["x"]))
+    torch.cuda.synchronize()
+    assert bufs.dispatch_status() == 0
+    idx = cpu(st["topk_idx"]).numpy().reshape(-1)
+    rs = d["row_src"]
+    rows = np.nonzero(rs >= 0)[0]
+    routed = rows[idx[rs[rows]] < w.E]
+    shared = rows[idx[rs[rows]] >= w.E]
+    tok = rs[routed] // w.slots
+    np.testing.assert_array_equal(cpu(bufs.xq).numpy()[routed], q["codes"][tok])
+    np.testing.assert_array_equal(cpu(bufs.xscale).numpy().astype(np.float64)[routed], q["scales"][tok])
+    got = f64(rows_out)
+    np.testing.assert_array_equal(got[routed], q["deq"][tok])
+    if shared.size:
+        np.testing.assert_array_equal(got[shared], f64(inp["x"])[rs[shared] // w.slots])
+    return dict(rows=int(routed.size), mean_abs_scale_exp=float(np.abs(q["exps"]).mean()))
 
 
 def check_ffn(w, inp, bufs, st, expert_subset=None) -> float:

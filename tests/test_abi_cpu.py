@@ -168,7 +168,8 @@ def test_workspace_sizes_and_layout():
             assert view.xperm < view.h < view.out < base + fwd
             assert view.out + A * w.d * w.act_bytes <= base + fwd
         assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
-        assert abi.moe_kernels_per_forward(c) == (7 if w.expert == "identity" else 9) + (5 if w.dedup else 0)
+        assert abi.moe_kernels_per_forward(c) == ((7 if w.expert == "identity" else 9) + (5 if w.dedup else 0)
+                                                  + (1 if w.dispatch_dtype == "fp8" else 0))
 
 
 def test_entry_points_reject_bad_arguments_on_the_host():
@@ -273,4 +274,24 @@ def test_dedup_workspace_and_kernel_count():
                                         1 << 20, None) == abi.MOE_ERR_ARG  # cfg.dedup not set
     assert abi.lib().moe_dispatch_dedup(ctypes.byref(dd), A16, A16, A16, ctypes.byref(m), A16, A16, A16,
                                         1 << 20, None) == abi.MOE_ERR_ARG  # null map arrays
+
+
+def test_fp8_dispatch_validation_and_workspace():
+    f8 = cfg(dispatch_dtype="fp8")
+    assert abi.moe_validate_config(f8) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(act="f32", dispatch_dtype="fp8")) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(D=4, dedup=True, dispatch_dtype="fp8")) == abi.MOE_ERR_UNSUPPORTED
+    c = cfg()
+    c.dispatch_dtype = 5
+    assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
+    assert abi.moe_kernels_per_forward(f8) == abi.moe_kernels_per_forward(cfg()) + 1
+    v = abi.moe_workspace_view()
+    base = 1 << 40
+    n = abi.moe_workspace_bytes(f8)
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(f8), base, n, ctypes.byref(v)) == 0
+    assert v.xq and v.xscale and v.xscale - v.xq >= 64 * 2 * 128      # rows x d codes
+    assert base + n - v.xscale >= 64 * 2 * 1 * 4                      # rows x ceil(d/128) scales
+    m = abi.dispatch_map(*([None] * 8))
+    assert abi.lib().moe_dispatch_fp8(ctypes.byref(cfg()), 1 << 20, 1 << 20, ctypes.byref(m), 1 << 20, 1 << 20,
+                                      None, 1 << 20, 1 << 20, None) == abi.MOE_ERR_ARG   # not an fp8 config
 

@@ -17,7 +17,7 @@ from oracle import moe_oracle as orc
 from routing_dispatch_combine_moe_b300 import abi
 from routing_dispatch_combine_moe_b300 import workloads as wl
 from tests._gpu import (StageBuffers, WorkspaceMap, capacity_of, chain, check_chained_dispatch, check_close,
-                        check_combine, check_dedup, check_dispatch, check_ffn, check_route, cpu,
+                        check_combine, check_dedup, check_dispatch, check_ffn, check_fp8, check_route, cpu,
                         gate_boundary_ties, half_ulp, oracle_dispatch, oracle_route, rms, route_tie_flags,
                         run_layer)
 from tests._harness import expert_fn, f64, run_oracle
@@ -37,6 +37,8 @@ REDUCED = {
     "grouped_dedup_swiglu": wl.Workload("grouped_dedup_swiglu", T=700, d=512, E=64, k=6, F=256, act="bf16",
                                         expert="swiglu", D=8, n_groups=8, topk_groups=3, dedup=True,
                                         capacity_factor="1"),
+    "mixtral_fp8": wl.scaled(W["mixtral_fp8_dispatch"], T=512, d=1024, F=1536),
+    "decode_fp8": wl.scaled(W["dsv3_decode"], d=1088, F=256, dispatch_dtype="fp8"),  # ragged last block
 }
 
 
@@ -52,6 +54,7 @@ def stagewise(w, seed=0, inp=None):
     d = check_dispatch(w, inp, b, cap, st)
     assert b.dispatch_status() == 0
     dd = check_dedup(w, inp, b, st, d) if w.dedup else None
+    f8 = check_fp8(w, inp, b, st, d) if w.dispatch_dtype == "fp8" else None
     ffn_err = None
     if w.expert != "identity":
         ffn_err = check_ffn(w, inp, b, st)
