@@ -213,13 +213,19 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
     Wg, bias = f64(inp["Wg"]), f64(inp.get("bias"))
     cache = {} if cache is None else cache
     fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, cache=cache)
+    grouped = 0 < w.topk_groups < w.n_groups
     if w.expert != "identity":  # model load: the experts this sample uses, converted once
-        idx = orc.keep_topk(orc.router_logits(x, Wg, bias), w.k)
+        H = orc.router_logits(x, Wg, bias)
+        idx = orc.keep_topk_grouped(H, w.k, w.n_groups, w.topk_groups) if grouped else orc.keep_topk(H, w.k)
         for e in list(np.unique(idx)) + list(range(w.E, w.n_experts)):
             fn(int(e), np.zeros((1, w.d)))
     cap = orc.expert_capacity(len(sel), w.k, w.E, w.capacity_factor, w.min_capacity)
     t0 = time.perf_counter()
-    orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D, n_shared=w.n_shared)
+    res = orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D, n_shared=w.n_shared,
+                          drop_policy=w.drop_policy, layout=w.layout, n_groups=w.n_groups,
+                          topk_groups=w.topk_groups, dispatch_dtype=w.dispatch_dtype)
+    if w.dedup:
+        orc.dedup_send(res["idx"], res["pos"], w.E, w.D)
     dt = time.perf_counter() - t0
     threads = cpu_threads()
     return dict(value=len(sel) / dt, seconds=dt, tokens=len(sel), cores=threads)

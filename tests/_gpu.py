@@ -401,6 +401,10 @@ class WorkspaceMap:
         self.out = None if not view.out else \
             ws[view.out - base:view.out - base + R * w.d * osz].view(odt).view(R, w.d)
         self.out_act = "f32" if odt == torch.float32 else "bf16"
+        if w.dispatch_dtype == "fp8":
+            nb = (w.d + 127) // 128
+            self.xq = ws[view.xq - base:view.xq - base + R * w.d].view(R, w.d)
+            self.xscale = ws[view.xscale - base:view.xscale - base + 4 * R * nb].view(torch.float32).view(R, nb)
         if w.dedup:
             TD = w.T * w.D
             self.send_counts = i32(view.send_counts, w.D)

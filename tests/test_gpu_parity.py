@@ -279,8 +279,10 @@ def test_traced_forward_matches_and_times():
 
 # ------------------------------------------------------------------ full sizes, sampled
 def _sampled_y(w, inp, ref_route, disp, tokens):
-    """Oracle y for a few tokens from the full-batch routing and dispatch (drops included)."""
+    """Oracle y for a few tokens from the full-batch routing and dispatch (drops included);
+    with the FP8 dispatch routed experts see the dequantized rows."""
     x = f64(inp["x"][torch.as_tensor(tokens, device="cuda")])
+    xq = orc.quantize_fp8_blocks(x)["deq"] if w.dispatch_dtype == "fp8" else x
     idx, G, pos = ref_route["idx"], ref_route["G"], disp["pos"].reshape(w.T, w.slots)
     fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
     need = {}
@@ -291,7 +293,7 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
     y = np.zeros((len(tokens), w.d))
     for e, uses in need.items():
         rows = np.array([r for r, _ in uses])
-        outs = fn(e, x[rows])
+        outs = fn(e, (xq if e < w.E else x)[rows])
         for (r, j), o in zip(uses, outs):
             y[r] += G[tokens[r], j] * o
     return y
@@ -300,6 +302,7 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
 FULL = {n: W[n] for n in ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"]}
 FULL["zipf_gate_padded"] = wl.scaled(W["zipf_cf125"], drop_policy="gate", layout="padded")
 FULL["dsv3_grouped_dedup"] = W["dsv3_grouped_dedup"]
+FULL["mixtral_fp8_dispatch"] = W["mixtral_fp8_dispatch"]
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -324,11 +327,21 @@ def test_full_size_sampled(name):
         src = torch.from_numpy(s["send_src"] // w.D).cuda()
         assert torch.equal(m.xsend[:s["n_send"]], inp["x"][src])
         print(f"\n{name}: {s['n_send']} send rows, {s['n_send'] / w.T:.3f} ranks per token")
+    fp8 = w.dispatch_dtype == "fp8"
+    if fp8 and how == "exact":
+        # codes and scales of 64 sampled routed rows against the oracle's quantization
+        rows = np.nonzero(d["row_src"] >= 0)[0]
+        rows = np.random.default_rng(1).choice(rows, size=min(64, rows.size), replace=False)
+        tok = d["row_src"][rows] // w.slots
+        q = orc.quantize_fp8_blocks(f64(inp["x"][torch.from_numpy(tok).cuda()]))
+        np.testing.assert_array_equal(cpu(m.xq).numpy()[rows], q["codes"])
+        np.testing.assert_array_equal(cpu(m.xscale).numpy().astype(np.float64)[rows], q["scales"])
     if w.expert == "identity":
         assert torch.equal(y, inp["x"])
         return
     # expert outputs of a few whole experts (largest, smallest non-empty, two more); with
-    # an exact dispatch their input rows are x at the oracle's row sources
+    # an exact dispatch their input rows are x at the oracle's row sources (FP8 dispatch:
+    # the dequantized rows)
     worst_ffn = None
     if how == "exact":
         counts = d["counts_kept"]
@@ -341,8 +354,10 @@ def test_full_size_sampled(name):
             lo = int(d["offsets"][e])
             hi = lo + int(counts[e])
             src = torch.from_numpy(d["row_src"][lo:hi] // w.slots).cuda()
-            worst_ffn = max(worst_ffn, check_close(m.out[lo:hi], fn(e, f64(inp["x"][src])), m.out_act,
-                                                   f"expert {e}", tol=2e-2))
+            xin = f64(inp["x"][src])
+            if fp8 and e < w.E:
+                xin = orc.quantize_fp8_blocks(xin)["deq"]
+            worst_ffn = max(worst_ffn, check_close(m.out[lo:hi], fn(e, xin), m.out_act, f"expert {e}", tol=2e-2))
     # end to end on sampled tokens from the oracle's own routing and dispatch: no near
     # tie, no gate at a keep cutoff, and (with a capacity) no expert shared with a
     # token whose routing flipped
