@@ -212,7 +212,7 @@ def gate_boundary_ties(w, idx, G, capacity, tol=2 * GATE_TOL) -> np.ndarray:
     return flag
 
 
-def compare_dispatch(w, bufs, d, x=None, xperm=None):
+def compare_dispatch(w, bufs, d, x=None, xperm=None, fp8_rows=None):
     """Every routing-map array bit-exact against the oracle's dispatch ``d``; the
     dispatched rows exact copies of x (padding rows zero)."""
     np.testing.assert_array_equal(cpu(bufs.counts_routed).numpy(), d["counts_routed"])
@@ -229,7 +229,12 @@ def compare_dispatch(w, bufs, d, x=None, xperm=None):
         xperm = bufs.xperm if xperm is None else xperm
         src = torch.from_numpy(d["row_src"]).to(xperm.device)
         valid = src >= 0
-        assert torch.equal(xperm[:rows][valid], x[src[valid] // w.slots]), "dispatched rows are not exact copies of x"
+        expect = x[src[valid] // w.slots]
+        if fp8_rows is not None:  # the FP8 dispatch's routed rows are the dequantized rows of x
+            q = torch.from_numpy(orc.quantize_fp8_blocks(f64(expect))["deq"]).to(expect.dtype).to(expect.device)
+            routed = (torch.from_numpy(np.asarray(fp8_rows)).to(xperm.device))[valid]
+            expect = torch.where(routed[:, None], q, expect)
+        assert torch.equal(xperm[:rows][valid], expect), "dispatched rows are not exact copies of x"
         assert torch.count_nonzero(xperm[:rows][~valid]) == 0, "padding rows are not zero"
 
 
@@ -266,8 +271,8 @@ def check_dedup(w, inp, bufs, st, d) -> dict:
     np.testing.assert_array_equal(cpu(bufs.send_src).numpy()[:n], s["send_src"])
     src_tok = torch.from_numpy(s["send_src"] // w.D).to(bufs.xsend.device)
     assert torch.equal(bufs.xsend[:n], inp["x"][src_tok]), "send rows are not exact copies of x"
-    rows = d["row_src"].size
-    assert torch.equal(fanned[:rows], direct[:rows]), "fanned-out rows differ from the direct gather"
+    held = torch.from_numpy(np.nonzero(d["row_src"] >= 0)[0]).to(fanned.device)  # padding rows are not sent
+    assert torch.equal(fanned[held], direct[held]), "fanned-out rows differ from the direct gather"
     return s
 
 
@@ -369,7 +374,12 @@ def check_chained_dispatch(w, inp, m, r, capacity, xperm=None) -> str:
     if exact and w.drop_policy == "gate":
         exact = not gate_boundary_ties(w, r["idx"], r["G"], capacity).any()
     if exact:
-        compare_dispatch(w, m, oracle_dispatch(w, r["idx_full"], r["G_full"], capacity), inp["x"], xperm)
+        d = oracle_dispatch(w, r["idx_full"], r["G_full"], capacity)
+        fp8_rows = None
+        if w.dispatch_dtype == "fp8":  # rows holding a routed assignment travel as FP8
+            rs = d["row_src"]
+            fp8_rows = (rs >= 0) & (r["idx_full"].reshape(-1)[np.maximum(rs, 0)] < w.E)
+        compare_dispatch(w, m, d, inp["x"], xperm, fp8_rows)
         return "exact"
     check_map_properties(w, m, capacity)
     return "properties"
@@ -419,6 +429,8 @@ def chain(w, inp, cfg) -> StageBuffers:
     b = StageBuffers(w, cfg)
     b.route(inp)
     b.dispatch(inp)
+    if w.dispatch_dtype == "fp8":  # the routed rows travel as FP8 and come back as bf16
+        abi.moe_dispatch_fp8(cfg, inp["x"], b.topk_idx, b.dmap(), b.xq, b.xscale, b.xperm, b.ws_dispatch)
     if w.expert != "identity":
         b.ffn(inp)
         b.combine()

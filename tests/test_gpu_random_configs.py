@@ -1,0 +1,74 @@
+"""Randomised small configurations through every stage and the layer forward.
+
+Each case draws a shape (T, d, E, k, F, D), an expert kind and activation dtype, an
+optional capacity with either drop policy and layout, an optional group limit, shared
+experts, the deduplicated or the FP8 dispatch, from a fixed seed. The stage checks
+(route, dispatch, dedup / FP8, expert FFN, combine) and the end-to-end comparison with
+the oracle are the same as for the named workloads."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as orc
+from routing_dispatch_combine_moe_b300 import abi
+from routing_dispatch_combine_moe_b300 import workloads as wl
+from tests._gpu import capacity_of, cpu, run_layer
+from tests._harness import run_oracle
+from tests.test_gpu_parity import layer_keep, stagewise, check_close
+
+pytestmark = pytest.mark.gpu
+
+
+def draw(seed: int) -> wl.Workload:
+    r = np.random.default_rng(1000 + seed)
+    act = "f32" if r.random() < 0.2 else "bf16"
+    D = int(r.choice([1, 2, 4, 8]))
+    E = D * int(r.integers(1, 9)) * int(r.choice([1, 2, 4]))
+    E = max(E, 2)
+    if E % D:
+        E = D * max(1, E // D)
+    k = int(r.integers(1, min(E, 8) + 1))
+    d = int(r.choice([64, 128, 136, 256, 520])) if act == "bf16" else int(r.choice([32, 96, 100, 128]))
+    expert = str(r.choice(["swiglu", "relu", "identity"]))
+    F = 0 if expert == "identity" else int(r.choice([64, 96, 128, 200, 256]))
+    if act == "bf16" and F % 8:
+        F = 96
+    T = int(r.integers(1, 600))
+    cf = None if r.random() < 0.5 else str(r.choice(["0.5", "1", "1.25", "2"]))
+    policy = "gate" if cf is not None and r.random() < 0.5 else "token"
+    n_shared = int(r.integers(0, 2)) if r.random() < 0.3 and k < 16 else 0
+    layout = "padded" if cf is not None and n_shared == 0 and r.random() < 0.4 else "packed"
+    n_groups = topk_groups = 0
+    if r.random() < 0.35 and E >= 4:
+        n_groups = int(r.choice([g for g in (2, 4, 8) if E % g == 0] or [1]))
+        topk_groups = int(r.integers(1, n_groups + 1))
+        if k > topk_groups * (E // n_groups):
+            n_groups = topk_groups = 0
+    dedup = D > 1 and r.random() < 0.3
+    fp8 = act == "bf16" and not dedup and r.random() < 0.3
+    precision = "f32_out" if r.random() < 0.6 else "split_h"
+    if precision == "split_h" and (F % 64 or act == "f32"):
+        precision = "f32_out"
+    return wl.Workload(f"rand{seed}", T=T, d=d, E=E, k=k, F=F, act=act, expert=expert, D=D,
+                       capacity_factor=cf, drop_policy=policy, layout=layout, n_shared=n_shared,
+                       n_groups=n_groups, topk_groups=topk_groups, dedup=dedup,
+                       dispatch_dtype="fp8" if fp8 else "act", precision=precision,
+                       zipf_s=1.2 if r.random() < 0.3 else None)
+
+
+CASES = [draw(i) for i in range(40)]
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_random_config(w):
+    cfg = abi.config_for(w)
+    assert abi.moe_validate_config(cfg) == abi.MOE_OK, w
+    res = stagewise(w, seed=7)
+    inp = res["inp"]
+    y, ws, view, flags = run_layer(cfg, inp, w)
+    assert flags == 0
+    assert torch.equal(y, res["chain"].y), "layer and chained stage calls must agree bit for bit"
+    ref = run_oracle(w, inp)
+    keep = layer_keep(w, ref, capacity_of(cfg))
+    err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{w.name} layer y")
+    print(f"\n{w}: err/rms={err:.4f} chained={res['chained']} dropped={res['dispatch']['n_dropped']}")
