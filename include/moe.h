@@ -35,7 +35,8 @@
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) without host synchronisation, so a sequence of calls can be
  *     captured in a CUDA graph. Exceptions: moe_read_status and
- *     moe_layer_forward_host (see their comments).
+ *     moe_layer_forward_host (see their comments); moe_layer_forward_host_async
+ *     enqueues host copies, which a graph capture can hold only with pinned buffers.
  *   - Argument errors are returned synchronously as a MOE_ERR_* code before any
  *     work is enqueued. Errors found on the device (an expert id or row index
  *     out of range, a bounded wait that gave up) set bits in a device status
@@ -335,6 +336,16 @@ int moe_layer_forward_traced(const moe_config* cfg, const void* x, const float* 
 int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const float* Wg,
                            const float* bias, const void* W13, const void* W2, void* y_host,
                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_layer_forward_host without the final synchronisation: the copy in, the layer and
+ * the copy out are enqueued on `stream` and the call returns; y_host is ready once the
+ * stream reaches that point (cudaStreamSynchronize, or an event). With page-locked
+ * host buffers the copies run on the copy engines, so a caller that keeps two batches
+ * in flight on two streams (each with its own workspace and y_host) overlaps one
+ * batch's copies with the other's kernels. Same arguments as moe_layer_forward_host. */
+int moe_layer_forward_host_async(const moe_config* cfg, const void* x_host, const float* Wg,
+                                 const float* bias, const void* W13, const void* W2, void* y_host,
+                                 void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* moe_dispatch without a workspace, for callers that cannot give the library device
  * memory for scratch: for example a serving loop that must not allocate device

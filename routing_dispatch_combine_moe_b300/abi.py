@@ -90,6 +90,8 @@ _SIGNATURES = {
     "moe_layer_forward_traced": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p,
                                                 ctypes.POINTER(_p), _i32]),
     "moe_layer_forward_host": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_layer_forward_host_async": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _sz,
+                                                    _p]),
     "moe_dispatch_dedup": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_send_map), _p,
                                           _p, _p, _sz, _p]),
     "moe_dispatch_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
@@ -345,6 +347,13 @@ def moe_layer_forward_host(cfg, x_host, Wg, bias, W13, W2, y_host, ws, stream=No
     _check(lib().moe_layer_forward_host(ctypes.byref(cfg), _ptr(x_host), _ptr(Wg), _ptr(bias), _ptr(W13), _ptr(W2),
                                         _ptr(y_host), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_layer_forward_host")
+
+
+def moe_layer_forward_host_async(cfg, x_host, Wg, bias, W13, W2, y_host, ws, stream=None):
+    """moe_layer_forward_host without the final sync: y_host is ready once `stream` gets there."""
+    _check(lib().moe_layer_forward_host_async(ctypes.byref(cfg), _ptr(x_host), _ptr(Wg), _ptr(bias), _ptr(W13),
+                                              _ptr(W2), _ptr(y_host), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_layer_forward_host_async")
 
 
 def moe_read_status(status_ptr: int, stream=None) -> int:

@@ -543,9 +543,9 @@ int moe_layer_forward_traced(const moe_config* cfg, const void* x, const float* 
     return forward(cfg, x, Wg, bias, W13, W2, y, ws, ws_bytes, stream, events, n_events);
 }
 
-int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const float* Wg, const float* bias,
-                           const void* W13, const void* W2, void* y_host, void* ws, size_t ws_bytes,
-                           moe_stream_t stream) {
+int moe_layer_forward_host_async(const moe_config* cfg, const void* x_host, const float* Wg, const float* bias,
+                                 const void* W13, const void* W2, void* y_host, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
     int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
     if (!x_host || !y_host || !ws) return MOE_ERR_ARG;
@@ -558,8 +558,15 @@ int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const floa
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(x)");
     if ((rc = forward(cfg, xs, Wg, bias, W13, W2, ys, ws, ws_bytes, stream, nullptr, 0)) != MOE_OK) return rc;
     e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync(y)");
-    e = cudaStreamSynchronize(stream);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "cudaMemcpyAsync(y)");
+}
+
+int moe_layer_forward_host(const moe_config* cfg, const void* x_host, const float* Wg, const float* bias,
+                           const void* W13, const void* W2, void* y_host, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+    const int rc = moe_layer_forward_host_async(cfg, x_host, Wg, bias, W13, W2, y_host, ws, ws_bytes, stream);
+    if (rc != MOE_OK) return rc;
+    const cudaError_t e = cudaStreamSynchronize(stream);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "cudaStreamSynchronize");
 }
 

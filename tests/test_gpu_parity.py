@@ -404,3 +404,20 @@ def test_layer_forward_replays_in_a_cuda_graph(name):
         fwd()
         torch.cuda.synchronize()
         assert torch.equal(y_graph, y)
+
+
+def test_async_host_forward_on_two_streams_matches_the_device_forward():
+    w = REDUCED["mixtral_bf16"]
+    inp = wl.make_inputs(w, 18, device="cuda")
+    cfg = abi.config_for(w)
+    y_dev, _, _, _ = run_layer(cfg, inp, w)
+    x_host = inp["x"].cpu().pin_memory()
+    ws = [abi.workspace(cfg, host=True) for _ in range(2)]
+    ys = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for i in range(4):
+        abi.moe_layer_forward_host_async(cfg, x_host, inp["Wg"], None, inp["W13"], inp["W2"], ys[i % 2], ws[i % 2],
+                                         streams[i % 2])
+    for st in streams:
+        st.synchronize()
+    assert torch.equal(ys[0], y_dev.cpu()) and torch.equal(ys[1], y_dev.cpu())
