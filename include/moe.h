@@ -392,6 +392,13 @@ const char* moe_last_cuda_error(void);
  * MOE_GEMM_PAIR=0/1/2 forces a tcgen05 variant. Static storage; never freed. */
 const char* moe_ffn_kernel_name(const moe_config* cfg);
 
+/* Environment switches (read once per process):
+ *   MOE_GEMM_PAIR=0/1/2    force the tcgen05 expert-GEMM variant (see moe_ffn_kernel_name);
+ *   MOE_DEBUG_SKIP_ARRIVE=1 failure-path test only: the grouped GEMMs leave their first
+ *                          finished accumulator unsignalled, so their bounded wait runs
+ *                          out (2 s) and MOE_DEV_ERR_TIMEOUT is set in the status word;
+ *                          the kernels drain, free tensor memory and return. */
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int moe_version(void);
 

@@ -87,6 +87,7 @@ struct Params {
     int F;                   // SwiGLU: up rows start at e*R + F
     int n_tiles;             // output column tiles
     int32_t* status;
+    int skip_arrive;         // failure-path test: never signal the first finished accumulator
 };
 
 template <int STAGES>
@@ -397,8 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                if constexpr (PAIR) umma_commit_pair_multicast(&S.tmem_full[acc], 0x3);
-                else umma_commit(&S.tmem_full[acc]);
+                if (!(p.skip_arrive && i == 0)) {
+                    if constexpr (PAIR) umma_commit_pair_multicast(&S.tmem_full[acc], 0x3);
+                    else umma_commit(&S.tmem_full[acc]);
+                }
             }
             if constexpr (PAIR) umma_commit_pair_multicast(&S.mma_done, 0x1);
             else umma_commit(&S.mma_done);
@@ -678,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit_pair_multicast(&S.tmem_full[acc], 0x3);
+                if (!(p.skip_arrive && i == 0)) umma_commit_pair_multicast(&S.tmem_full[acc], 0x3);
             }
             umma_commit_pair_multicast(&S.mma_done, 0x1);
             drain_wait(&S.mma_done, 0);
@@ -920,6 +923,18 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Para
 
 int ffn_tc_variant(int64_t rows, int E, int64_t capacity) { return gemm_variant(rows, E, capacity); }
 
+// MOE_DEBUG_SKIP_ARRIVE=1 (read once per process) makes every grouped-GEMM launch leave
+// its first finished accumulator unsignalled: the epilogue's bounded wait then runs out,
+// the kernel flags MOE_DEV_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and
+// returns. It exists to test that failure path; nothing else sets it.
+int debug_skip_arrive() {
+    static const int v = [] {
+        const char* e = getenv("MOE_DEBUG_SKIP_ARRIVE");
+        return e && atoi(e) != 0 ? 1 : 0;
+    }();
+    return v;
+}
+
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event) {
     const int64_t rows_max = a.rows;
     const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
@@ -936,6 +951,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.E = a.E;
     p.status = a.status;
     p.F = a.F;
+    p.skip_arrive = debug_skip_arrive();
 
     // Up projection: A = xperm [rows, d]; B = W13 [E*R, d]; C = h.
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;
