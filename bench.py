@@ -147,6 +147,21 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def versions(device) -> dict:
+    """Software and hardware the numbers come from."""
+    v = {"torch": torch.__version__, "cuda_runtime": torch.version.cuda, "library": abi.lib().moe_version(),
+         "gpu": torch.cuda.get_device_name(device), "sms": torch.cuda.get_device_properties(device).multi_processor_count,
+         "host_cores": os.cpu_count()}
+    try:
+        import pynvml
+        pynvml.nvmlInit()
+        drv = pynvml.nvmlSystemGetDriverVersion()
+        v["driver"] = drv.decode() if isinstance(drv, bytes) else drv
+    except Exception:  # noqa: BLE001 - the versions are informative only
+        v["driver"] = None
+    return v
+
+
 def file_sha(path: str) -> str:
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
@@ -461,6 +476,7 @@ def run_ours(args, w, world, rank, local):
         "gpu_launches": abi.moe_kernels_per_forward(cfg) * args.steps,
         "launch": launch_mode,
         "cpu_baseline": cpu,
+        "versions": versions(device),
     }
     return line
 
