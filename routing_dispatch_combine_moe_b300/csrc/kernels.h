@@ -21,6 +21,7 @@ inline int dispatch_blocks(int64_t assignments) {
 // Router. The logits are summed from up to route_max_slices(T, E) split-K partials
 // held in `scratch`, whose size depends only on T and E.
 int route_max_slices(int T, int E);
+bool route_uses_small_kernel(int d, int E);  // one fused launch instead of logits + top-k
 int route_k_slices(int T, int d, int E);
 inline size_t route_scratch_bytes_max(int T, int E) {
     return size_t(route_max_slices(T, E)) * size_t(T) * size_t(E) * sizeof(float);

@@ -303,6 +303,174 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
     topk_softmax_store<VPL>(v, lane, E, k, n_shared, topk_idx + size_t(t) * K, topk_gate + size_t(t) * K);
 }
 
+// ------------------------------------------------------------------ small E, fused
+// For E <= 32 with W_g small (d * E * 4 <= 128 KB, e.g. 4096 x 8) one kernel does the
+// logits, KeepTopK and the softmax. A CTA takes 16 tokens; thread (tok, ks) of a 16 x 16
+// grid sums the products of token tok over the ks-th sixteenth of d into EB partial
+// logits (x in 16-byte pieces; each W_g row is read by 16 threads at once, so it comes
+// from L1 as one sector per load). The 16 partials of a logit are then added in ks
+// order through shared memory by thread (tok, 0), which also selects the top k (equal
+// logits: lower id), applies the optional group limit and the kept softmax, exactly
+// as the warp-wide path does. Deterministic: every sum has a fixed order.
+template <int EB>
+__device__ __forceinline__ void topk_softmax_thread(float (&v)[EB], int E, int k, int n_shared, int n_groups,
+                                                    int topk_groups, int32_t* idx_out, float* gate_out) {
+    if (topk_groups > 0 && topk_groups < n_groups) {
+        const int gs = E / n_groups;
+        uint32_t kept = 0;
+        for (int r = 0; r < topk_groups; ++r) {
+            float best = -INFINITY;
+            int bg = -1;
+            for (int g = 0; g < n_groups; ++g) {
+                if ((kept >> g) & 1u) continue;
+                float m = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < EB; ++e)
+                    if (e < E && e / gs == g) m = fmaxf(m, v[e]);
+                if (bg < 0 || m > best) { best = m; bg = g; }
+            }
+            kept |= 1u << bg;
+        }
+#pragma unroll
+        for (int e = 0; e < EB; ++e)
+            if (e < E && !((kept >> (e / gs)) & 1u)) v[e] = -INFINITY;
+    }
+    uint32_t taken = 0;
+    float val[MOE_MAX_K];
+    int id[MOE_MAX_K];
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int e = 0; e < EB; ++e)
+            if (e < E && !((taken >> e) & 1u) && (bi < 0 || v[e] > bv)) { bv = v[e]; bi = e; }
+        if (bi < 0) bi = 0;  // only reachable with NaN logits; keeps the index in range
+        taken |= 1u << bi;
+        val[j] = bv;
+        id[j] = bi;
+    }
+    float ex[MOE_MAX_K];
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) {
+        ex[j] = expf(val[j] - val[0]);
+        sum += ex[j];
+    }
+    for (int j = 0; j < k; ++j) {
+        idx_out[j] = id[j];
+        gate_out[j] = ex[j] / sum;
+    }
+    for (int j = 0; j < n_shared; ++j) {
+        idx_out[k + j] = E + j;
+        gate_out[k + j] = 1.0f;
+    }
+}
+
+template <typename TAct, int EB>
+__global__ void __launch_bounds__(256) route_small_kernel(const TAct* __restrict__ x, const float* __restrict__ Wg,
+                                                          const float* __restrict__ bias, int T, int d, int E, int k,
+                                                          int n_shared, int n_groups, int topk_groups, bool wvec,
+                                                          int32_t* __restrict__ topk_idx,
+                                                          float* __restrict__ topk_gate) {
+    constexpr int VN = Act16<TAct>::N, UV = 4;
+    extern __shared__ __align__(16) float smw[];        // W_g [d][E], then the partial logits
+    float (*red)[16][EB + 1] = reinterpret_cast<float (*)[16][EB + 1]>(smw + size_t(d) * E);
+    const int tid = threadIdx.x, tok = tid & 15, ks = tid >> 4;
+    // W_g once per CTA into shared memory (coalesced, independent loads)
+    const int nw = d * E;
+    if (wvec) {  // asynchronous 16-byte copies, all in flight at once
+        const float4* src = reinterpret_cast<const float4*>(Wg);
+        for (int i = tid; i < nw / 4; i += 256)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smw + 4 * i)), "l"(src + i)
+                         : "memory");
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        for (int i = tid; i < nw; i += 256) smw[i] = __ldg(Wg + i);
+    }
+    __syncthreads();
+    const int t = blockIdx.x * 16 + tok;
+    const int vpr = d / VN;                 // 16-byte pieces per row
+    const int per = (vpr + 15) / 16;        // pieces per sixteenth
+    const int v0 = ks * per, v1 = min(vpr, v0 + per);
+    float acc[EB];
+#pragma unroll
+    for (int e = 0; e < EB; ++e) acc[e] = 0.f;
+    if (t < T) {
+        const uint4* row = reinterpret_cast<const uint4*>(x + size_t(t) * d);
+        for (int vb = v0; vb < v1; vb += UV) {
+            uint4 raw[UV];
+#pragma unroll
+            for (int u = 0; u < UV; ++u) raw[u] = vb + u < v1 ? __ldg(row + vb + u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < UV; ++u) {
+                if (vb + u >= v1) break;
+                float xv[VN];
+                Act16<TAct>::to_f32(raw[u], xv);
+#pragma unroll
+                for (int q = 0; q < VN; ++q) {
+                    const float* wrow = smw + size_t((vb + u) * VN + q) * E;
+                    if (wvec) {  // E == EB: EB/4 vector reads per row
+#pragma unroll
+                        for (int e4 = 0; e4 < EB / 4; ++e4) {
+                            const float4 w4 = reinterpret_cast<const float4*>(wrow)[e4];
+                            acc[4 * e4 + 0] = fmaf(xv[q], w4.x, acc[4 * e4 + 0]);
+                            acc[4 * e4 + 1] = fmaf(xv[q], w4.y, acc[4 * e4 + 1]);
+                            acc[4 * e4 + 2] = fmaf(xv[q], w4.z, acc[4 * e4 + 2]);
+                            acc[4 * e4 + 3] = fmaf(xv[q], w4.w, acc[4 * e4 + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EB; ++e)
+                            if (e < E) acc[e] = fmaf(xv[q], wrow[e], acc[e]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EB; ++e) red[ks][tok][e] = acc[e];
+    __syncthreads();
+    if (ks != 0 || t >= T) return;
+    float h[EB];
+#pragma unroll
+    for (int e = 0; e < EB; ++e) {
+        float sum = 0.f;
+        for (int q = 0; q < 16; ++q) sum += red[q][tok][e];
+        h[e] = e < E ? sum + (bias ? __ldg(bias + e) : 0.f) : -INFINITY;
+    }
+    const int K = k + n_shared;
+    topk_softmax_thread<EB>(h, E, k, n_shared, n_groups, topk_groups, topk_idx + size_t(t) * K,
+                            topk_gate + size_t(t) * K);
+}
+
+constexpr int kSmallRouteWBytes = 128 << 10;  // W_g bytes the fused small-E router holds
+
+template <typename TAct, int EB>
+cudaError_t launch_small(const void* x, const float* Wg, const float* bias, int T, int d, int E, int k, int S,
+                         int G, int M, int32_t* idx, float* gate, cudaStream_t stream) {
+    auto kern = route_small_kernel<TAct, EB>;
+    constexpr size_t max_smem = size_t(kSmallRouteWBytes) + sizeof(float) * 16 * 16 * (EB + 1);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(max_smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const size_t smem = sizeof(float) * (size_t(d) * E + 16 * 16 * (EB + 1));
+    const bool wvec = E == EB && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;
+    kern<<<(T + 15) / 16, 256, smem, stream>>>(static_cast<const TAct*>(x), Wg, bias, T, d, E, k, S, G, M, wvec, idx,
+                                               gate);
+    return cudaGetLastError();
+}
+
+template <typename TAct>
+cudaError_t launch_small_t(const void* x, const float* Wg, const float* bias, int T, int d, int E, int k, int S,
+                           int G, int M, int32_t* idx, float* gate, cudaStream_t stream) {
+    if (E <= 4) return launch_small<TAct, 4>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
+    if (E <= 8) return launch_small<TAct, 8>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
+    if (E <= 16) return launch_small<TAct, 16>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
+    return launch_small<TAct, 32>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
+}
+
 int warps_along_experts(int E) { return E <= 8 ? 1 : E <= 16 ? 2 : E <= 32 ? 4 : 8; }
 
 template <typename TAct, int WE>
@@ -369,9 +537,18 @@ int route_k_slices(int T, int d, int E) {
     return best;
 }
 
+// The fused small-E kernel while W_g stays in L1 (E <= 32, d * E * 4 <= 128 KB).
+bool route_uses_small_kernel(int d, int E) { return E <= 32 && int64_t(d) * E * 4 <= kSmallRouteWBytes; }
+
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
                          float* scratch, cudaStream_t stream) {
+    if (route_uses_small_kernel(d, E))
+        return act_dtype == MOE_F32
+                   ? launch_small_t<float>(x, Wg, bias, T, d, E, k, n_shared, n_groups, topk_groups, topk_idx,
+                                           topk_gate, stream)
+                   : launch_small_t<__nv_bfloat16>(x, Wg, bias, T, d, E, k, n_shared, n_groups, topk_groups,
+                                                   topk_idx, topk_gate, stream);
     const int ks = route_k_slices(T, d, E);
     const int slice = slice_len(d, ks);
     cudaError_t e = act_dtype == MOE_F32 ? launch_gemm_t<float>(x, Wg, T, d, E, slice, ks, scratch, stream)
