@@ -424,13 +424,14 @@ int moe_workspace_get_view(const moe_config* cfg, void* ws, size_t ws_bytes, moe
 
 int moe_kernels_per_forward(const moe_config* cfg) {
     if (validate(cfg) != MOE_OK) return 0;
-    // (logits, top-k) + (count, scan, scatter, [select], [pad], gather) + (up, down) + combine
+    // router + (count, scan, scatter, [select], [pad], gather) + (up, down) + combine
     const int select = cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0 ? 1 : 0;
     const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
     const int fp8 = cfg->dispatch_dtype == MOE_DISPATCH_FP8 ? 1 : 0;  // dequant (the gather quantizes)
-    return 2 + 4 + select + pad + dedup + fp8 + ffn + 1;
+    const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : 2;  // fused, or logits + top-k
+    return route + 4 + select + pad + dedup + fp8 + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {
