@@ -82,38 +82,51 @@ __global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ o
         gj[j] = __shfl_sync(0xFFFFFFFFu, g, j);
         if (j >= k) src[j] = -1;
     }
-    for (int c0 = lane * EPL; c0 < d; c0 += 32 * EPL) {
-        const bool full = c0 + EPL <= d;
-        uint4 raw[KMAX][2];
+    // UNR column steps are loaded before any arithmetic, so a lane keeps UNR x KMAX x 32
+    // bytes in flight even when k is small (k = 2: 256 bytes).
+    constexpr int UNR = KMAX >= 8 ? 1 : 8 / KMAX;
+    for (int c00 = lane * EPL; c00 < d; c00 += 32 * EPL * UNR) {
+        uint4 raw[UNR][KMAX][2];
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (src[j] >= 0) {
-                const uint4* rp = reinterpret_cast<const uint4*>(out + size_t(src[j]) * d + c0);
-                raw[j][0] = __ldg(rp);
-                raw[j][1] = full ? __ldg(rp + 1) : make_uint4(0, 0, 0, 0);
-            }
-        }
-        float acc[EPL];
+        for (int u = 0; u < UNR; ++u) {
+            const int c0 = c00 + u * 32 * EPL;
+            const bool full = c0 + EPL <= d;
 #pragma unroll
-        for (int q = 0; q < EPL; ++q) acc[q] = 0.f;
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (src[j] >= 0) {
-                float f[EPL];
-                if constexpr (sizeof(TOut) == 2) {
-                    Vec16<__nv_bfloat16>::unpack(raw[j][0], f);
-                    Vec16<__nv_bfloat16>::unpack(raw[j][1], f + 8);
-                } else {
-                    Vec16<float>::unpack(raw[j][0], f);
-                    Vec16<float>::unpack(raw[j][1], f + 4);
+            for (int j = 0; j < KMAX; ++j) {
+                if (src[j] >= 0 && c0 < d) {
+                    const uint4* rp = reinterpret_cast<const uint4*>(out + size_t(src[j]) * d + c0);
+                    raw[u][j][0] = __ldg(rp);
+                    raw[u][j][1] = full ? __ldg(rp + 1) : make_uint4(0, 0, 0, 0);
                 }
-#pragma unroll
-                for (int q = 0; q < EPL; ++q) acc[q] = fmaf(gj[j], f[q], acc[q]);
             }
         }
 #pragma unroll
-        for (int h = 0; h < EPL / 8; ++h)
-            if (full || h == 0) store8<TY>(y + size_t(t) * d + c0 + 8 * h, acc + 8 * h);
+        for (int u = 0; u < UNR; ++u) {
+            const int c0 = c00 + u * 32 * EPL;
+            if (c0 >= d) break;
+            const bool full = c0 + EPL <= d;
+            float acc[EPL];
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) acc[q] = 0.f;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (src[j] >= 0) {
+                    float f[EPL];
+                    if constexpr (sizeof(TOut) == 2) {
+                        Vec16<__nv_bfloat16>::unpack(raw[u][j][0], f);
+                        Vec16<__nv_bfloat16>::unpack(raw[u][j][1], f + 8);
+                    } else {
+                        Vec16<float>::unpack(raw[u][j][0], f);
+                        Vec16<float>::unpack(raw[u][j][1], f + 4);
+                    }
+#pragma unroll
+                    for (int q = 0; q < EPL; ++q) acc[q] = fmaf(gj[j], f[q], acc[q]);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < EPL / 8; ++h)
+                if (full || h == 0) store8<TY>(y + size_t(t) * d + c0 + 8 * h, acc + 8 * h);
+        }
     }
 }
 
