@@ -85,7 +85,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ o
     // UNR column steps are loaded before any arithmetic, so a lane keeps UNR x KMAX x 32
     // bytes in flight even when k is small (k = 2: 256 bytes).
     constexpr int UNR = KMAX >= 8 ? 1 : 8 / KMAX;
-    for (int c00 = lane * EPL; c00 < d; c00 += 32 * EPL * UNR) {
+    // column slice blockIdx.y of gridDim.y, in whole warp steps of 32 * EPL columns
+    const int steps = (d + 32 * EPL - 1) / (32 * EPL);
+    const int per = (steps + gridDim.y - 1) / gridDim.y;
+    const int cbeg = blockIdx.y * per * 32 * EPL, cend = min(d, cbeg + per * 32 * EPL);
+    for (int c00 = cbeg + lane * EPL; c00 < cend; c00 += 32 * EPL * UNR) {
         uint4 raw[UNR][KMAX][2];
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ o
             const bool full = c0 + EPL <= d;
 #pragma unroll
             for (int j = 0; j < KMAX; ++j) {
-                if (src[j] >= 0 && c0 < d) {
+                if (src[j] >= 0 && c0 < cend) {
                     const uint4* rp = reinterpret_cast<const uint4*>(out + size_t(src[j]) * d + c0);
                     raw[u][j][0] = __ldg(rp);
                     raw[u][j][1] = full ? __ldg(rp + 1) : make_uint4(0, 0, 0, 0);
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const TOut* __restrict__ o
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
             const int c0 = c00 + u * 32 * EPL;
-            if (c0 >= d) break;
+            if (c0 >= cend) break;
             const bool full = c0 + EPL <= d;
             float acc[EPL];
 #pragma unroll
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(256) combine_kernel_f32x4(const float* __restr
 }
 
 template <typename TOut, typename TY>
-void launch_k(int grid, const void* out, const float* gate, const int32_t* pos, void* y, int T, int k, int d,
+void launch_k(dim3 grid, const void* out, const float* gate, const int32_t* pos, void* y, int T, int k, int d,
               int64_t max_rows, int32_t* status, cudaStream_t stream) {
     const TOut* o = static_cast<const TOut*>(out);
     TY* yy = static_cast<TY*>(y);
@@ -184,12 +188,17 @@ void launch_k(int grid, const void* out, const float* gate, const int32_t* pos, 
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
                            void* y, int T, int d, int k, int64_t rows, int32_t* status, cudaStream_t stream) {
     const int64_t max_rows = rows;
-    const int grid = (T + 7) / 8;
+    // token blocks of 8 warps; small batches also split each row into column slices of
+    // at least 512 elements, until about two CTAs per SM are in flight
+    const int nb = (T + 7) / 8;
+    const int want = (2 * device_sm_count() + nb - 1) / nb;
+    const int cap = d / 512 > 1 ? d / 512 : 1;
+    const dim3 grid(unsigned(nb), unsigned(want < cap ? (want > 1 ? want : 1) : cap));
     if (act_dtype == MOE_F32) {
         if (d % 8 == 0)
             launch_k<float, float>(grid, out, gate, pos, y, T, k, d, max_rows, status, stream);
         else
-            combine_kernel_f32x4<<<grid, 256, 0, stream>>>(static_cast<const float*>(out), gate, pos,
+            combine_kernel_f32x4<<<nb, 256, 0, stream>>>(static_cast<const float*>(out), gate, pos,
                                                            static_cast<float*>(y), T, k, d, max_rows, status);
     } else if (out_dtype == MOE_F32) {
         launch_k<float, __nv_bfloat16>(grid, out, gate, pos, y, T, k, d, max_rows, status, stream);

@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
             for (int x = 0; x < EX; ++x)
 #pragma unroll
                 for (int j = 0; j < SB; ++j) {
+                    if (b0 + 32 * j >= nblk) break;  // no blocks left (uniform over the warp)
                     const int b = b0 + 32 * j + lane;
                     const int incl = warp_incl_scan(v[x][j], lane);
                     if (b < nblk && has[x]) row[x][b] = run[x] + incl - v[x][j];
@@ -375,13 +376,17 @@ __global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict
     if (lane == 0) row_src[r] = -1;
 }
 
-// One warp per token: x[t] is read once and written to each of its kept rows.
+// One warp per token and column slice (blockIdx.y of gridDim.y): the slice of x[t] is
+// read once and written to each of the token's kept rows. Small batches split the row
+// over several warps so that enough of them are in flight.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ pos,
                                                      uint4* __restrict__ xperm, int T, int k, int vec_per_row,
                                                      int64_t max_rows) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
+    const int per = (vec_per_row + gridDim.y - 1) / gridDim.y;
+    const int vbeg = blockIdx.y * per, vend = min(vec_per_row, vbeg + per);
     int p = -1;
     if (lane < k) {
         p = pos[size_t(t) * k + lane];
@@ -392,12 +397,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
     for (int j = 0; j < MOE_MAX_K; ++j) dst[j] = __shfl_sync(0xFFFFFFFFu, p, j);
     const uint4* src = x + size_t(t) * vec_per_row;
     constexpr int U = 8;  // 16-byte pieces per lane in flight
-    for (int v0 = lane; v0 < vec_per_row; v0 += 32 * U) {
+    for (int v0 = vbeg + lane; v0 < vend; v0 += 32 * U) {
         uint4 buf[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int v = v0 + 32 * u;
-            if (v < vec_per_row) buf[u] = __ldg(src + v);
+            if (v < vend) buf[u] = __ldg(src + v);
         }
 #pragma unroll
         for (int j = 0; j < MOE_MAX_K; ++j) {
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + 32 * u;
-                    if (v < vec_per_row) d[v] = buf[u];
+                    if (v < vend) d[v] = buf[u];
                 }
             }
         }
@@ -414,6 +419,15 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
 }
 
 }  // namespace
+
+// Token blocks of 8 warps, times column slices of at least 64 pieces, until about two
+// CTAs per SM are in flight.
+dim3 gather_grid(int T, int vec_per_row) {
+    const int nb = (T + 7) / 8;
+    const int want = (2 * device_sm_count() + nb - 1) / nb;
+    const int cap = vec_per_row / 64 > 1 ? vec_per_row / 64 : 1;
+    return dim3(unsigned(nb), unsigned(want < cap ? (want > 1 ? want : 1) : cap));
+}
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const int64_t A = int64_t(a.T) * a.k;
@@ -439,8 +453,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
             a.counts_kept, a.offsets, int(a.capacity),
                                                  static_cast<uint4*>(a.xperm), vec_per_row, a.row_src);
     if (!a.skip_gather)
-        gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
-                                                          static_cast<uint4*>(a.xperm), a.T, a.k, vec_per_row, rows);
+        gather_kernel<<<gather_grid(a.T, vec_per_row), 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
+                                                                         static_cast<uint4*>(a.xperm), a.T, a.k,
+                                                                         vec_per_row, rows);
     return cudaGetLastError();
 }
 
@@ -525,8 +540,9 @@ cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream) {
     scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, a.D, nblk, -1, a.hist, a.send_offsets,
                                                         a.drop_offsets, a.routed_offsets, nullptr, nullptr,
                                                         a.send_pos, a.send_src, nullptr);
-    gather_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.send_pos,
-                                                      static_cast<uint4*>(a.xsend), a.T, a.D, vec_per_row, A2);
+    gather_kernel<<<gather_grid(a.T, vec_per_row), 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.send_pos,
+                                                                     static_cast<uint4*>(a.xsend), a.T, a.D,
+                                                                     vec_per_row, A2);
     fanout_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x),
                                                       static_cast<const uint4*>(a.xsend), a.topk_idx, a.pos,
                                                       a.send_pos, static_cast<uint4*>(a.xperm), a.T, a.K,
