@@ -83,6 +83,18 @@ __device__ __forceinline__ void topk_softmax_store(float (&v)[VPL], int lane, in
     }
 }
 
+// Two fp32 fused multiply-adds in one instruction (Blackwell's packed f32x2 FMA):
+// c0 = fma(a, b0, c0), c1 = fma(a, b1, c1), each rounded to nearest exactly like fmaf,
+// with half the instructions to issue.
+__device__ __forceinline__ void fma2_rn(float a, float b0, float b1, float& c0, float& c1) {
+    uint64_t aa, bb, cc;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(aa) : "f"(a));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(bb) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(cc) : "f"(c0), "f"(c1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(cc) : "l"(aa), "l"(bb));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(cc));
+}
+
 // ------------------------------------------------------------------ logits GEMM
 // CTA of 8 warps: WE warps along experts (8 experts each), 8/WE warps along tokens
 // (128 tokens each, 4 per lane).
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(256, WE == 1 ? 1 : 2) route_gemm_kernel(const 
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(xa[r], wa[q], acc[r][q]);
+                for (int q = 0; q < 8; q += 2) fma2_rn(xa[r], wa[q], wa[q + 1], acc[r][q], acc[r][q + 1]);
         }
         if ((c + 1) % (256 / kGK) == 0) {
 #pragma unroll
