@@ -452,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 // columns are up to 256 consecutive rows of one expert, N rounded up to a multiple
 // of 32 on the expert's last tile, split N/2 + N/2 between the two SMs. An expert's
 // row count then costs at most 31 idle columns, where the row-major pair tile costs up
-// to 255 idle rows, and each SM still lands 32 KB per stage (six stages). The
+// to 255 idle rows; per stage each SM lands 16 KB of weights and its N/2 rows (at
+// most 16 KB; six stages), one copy for each. The
 // accumulator holds features on TMEM lanes and rows on columns, so each epilogue
 // thread owns one feature and stores it for 32 rows at a time: a warp writes 32
 // consecutive features of one row per store. For SwiGLU, warps holding up values
@@ -460,10 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 // gate values (lanes 0-63).
 constexpr int SW_STAGES = 6;
 constexpr int SW_A_STAGE = 128 * BK * 2;          // 16 KB: 128 weight rows per SM
-constexpr int SW_B_BIG = 128 * BK * 2;            // 16 KB: box of 128 dispatched rows
-constexpr int SW_B_SMALL = 16 * BK * 2;           // 2 KB: box of 16 rows, for N <= 32
+constexpr int SW_B_BIG = 128 * BK * 2;            // 16 KB: up to 128 dispatched rows per SM
 constexpr int SW_STAGE_SMEM = SW_A_STAGE + SW_B_BIG;
 constexpr int SW_TILE_N = 256;
+constexpr int SW_ROW_MAPS = SW_TILE_N / 32;        // row boxes of 16, 32, ..., 128 rows
+
+// Tensor maps over the dispatched rows, one per box height 16 (i + 1): a tile of N
+// rows loads exactly its N / 2 rows per SM with one copy per stage.
+struct RowMaps {
+    CUtensorMap m[SW_ROW_MAPS];
+};
 
 struct SwapXchg {
     float v[2][32][33];  // up values for 32 rows x 32 features, per gate warp
@@ -526,8 +533,7 @@ __device__ __forceinline__ void store_one(const Params& p, int row, int f, float
 
 template <int MODE, int OUT>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap mapW,
-                                                                        const __grid_constant__ CUtensorMap mapX,
-                                                                        const __grid_constant__ CUtensorMap mapX16,
+                                                                        const __grid_constant__ RowMaps mapX,
                                                                         const Params p) {
     constexpr int STAGES = SW_STAGES;
     constexpr int EPI_WARPS_TOTAL = 8;
@@ -559,8 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
         fence_barrier_init();
         fence_proxy_async_smem();
         tma_prefetch_desc(&mapW);
-        tma_prefetch_desc(&mapX);
-        tma_prefetch_desc(&mapX16);
+        for (int i = 0; i < SW_ROW_MAPS; ++i) tma_prefetch_desc(&mapX.m[i]);
     }
     if (warp == 1) {
         tmem_alloc_pair(&S.tmem_base, TMEM_COLS);
@@ -617,9 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 int e, mt, nt, start, len, n;
                 decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
                 swap_tile_rows(S.off, S.end, e, mt, start, len, n);
-                const bool small = n <= 32;
+                const CUtensorMap* mx = &mapX.m[(n >> 5) - 1];  // box of n / 2 rows
                 const int xrow = start + int(rank) * (n >> 1);
-                const uint32_t stage_tx = uint32_t(SW_A_STAGE + (small ? SW_B_SMALL : SW_B_BIG));
+                const uint32_t stage_tx = uint32_t(SW_A_STAGE + (n >> 1) * BK * 2);
                 int w0, w1 = 0;
                 if (MODE == kSwiGLU) {
                     w0 = e * p.R + nt * 128 + int(rank) * 64;
@@ -642,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                     } else {
                         tma_load_2d_pair(a_dst, &mapW, bar, kW, w0);
                     }
-                    tma_load_2d_pair_hint(b_dst, small ? &mapX16 : &mapX, bar, kX, xrow, pol_x);
+                    tma_load_2d_pair_hint(b_dst, mx, bar, kX, xrow, pol_x);
                     armed_mask |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -804,6 +809,14 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_row_maps(RowMaps* maps, const void* base, uint64_t inner, uint64_t rows) {
+    for (int i = 0; i < SW_ROW_MAPS; ++i) {
+        const cudaError_t err = make_map(&maps->m[i], base, inner, rows, uint32_t(16 * (i + 1)));
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
 template <int MODE, int OUT, bool PAIR>
 cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const Params& p, int grid,
                           cudaStream_t stream) {
@@ -876,7 +889,7 @@ int grid_for(int64_t rows_max, int E, int n_tiles, bool pair) {
 }
 
 template <int MODE, int OUT>
-cudaError_t launch_swap(const CUtensorMap& mW, const CUtensorMap& mX, const CUtensorMap& mX16, const Params& p,
+cudaError_t launch_swap(const CUtensorMap& mW, const RowMaps& mX, const Params& p,
                         int64_t rows_max, int E, cudaStream_t stream) {
     auto kern = grouped_gemm_swap_kernel<MODE, OUT>;
     constexpr size_t smem = swap_smem_bytes();
@@ -908,7 +921,7 @@ cudaError_t launch_swap(const CUtensorMap& mW, const CUtensorMap& mX, const CUte
     }
     const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
     cfg.gridDim = dim3(unsigned(2 * (pairs > 0 ? pairs : 1)));
-    return cudaLaunchKernelEx(&cfg, kern, mW, mX, mX16, p);
+    return cudaLaunchKernelEx(&cfg, kern, mW, mX, p);
 }
 
 template <int MODE, int OUT>
@@ -943,7 +956,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     const bool pair = variant == kPairRows;
     const bool swap = variant == kPairSwap;
     const uint32_t b_rows = pair ? MMA_N / 2 : MMA_N;  // rows of one B box
-    CUtensorMap mA, mB, mX16;
+    CUtensorMap mA, mB;
+    RowMaps mX;
     cudaError_t err;
     Params p{};
     p.offsets = a.offsets;
@@ -965,15 +979,14 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     if (swap) {
         // weights as the MMA's A operand: 64-row boxes (gate | up halves) or 128-row boxes
         if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128)) != cudaSuccess) return err;
-        if ((err = make_map(&mB, a.xperm, a.d, rows_max, 128)) != cudaSuccess) return err;
-        if ((err = make_map(&mX16, a.xperm, a.d, rows_max, 16)) != cudaSuccess) return err;
+        if ((err = make_row_maps(&mX, a.xperm, a.d, rows_max)) != cudaSuccess) return err;
         p.n_tiles = swiglu ? (a.F + 127) / 128 : (a.F + 255) / 256;
         if (swiglu)
-            err = split_h ? launch_swap<kSwiGLU, kOutHiLo>(mA, mB, mX16, p, rows_max, a.E, stream)
-                          : launch_swap<kSwiGLU, kOutBF16>(mA, mB, mX16, p, rows_max, a.E, stream);
+            err = split_h ? launch_swap<kSwiGLU, kOutHiLo>(mA, mX, p, rows_max, a.E, stream)
+                          : launch_swap<kSwiGLU, kOutBF16>(mA, mX, p, rows_max, a.E, stream);
         else
-            err = split_h ? launch_swap<kReLU, kOutHiLo>(mA, mB, mX16, p, rows_max, a.E, stream)
-                          : launch_swap<kReLU, kOutBF16>(mA, mB, mX16, p, rows_max, a.E, stream);
+            err = split_h ? launch_swap<kReLU, kOutHiLo>(mA, mX, p, rows_max, a.E, stream)
+                          : launch_swap<kReLU, kOutBF16>(mA, mX, p, rows_max, a.E, stream);
     } else {
         if ((err = make_map(&mA, a.xperm, a.d, rows_max, 128)) != cudaSuccess) return err;
         if ((err = make_map(&mB, a.W13, a.d, uint64_t(a.E) * R, swiglu ? MMA_N / 2 : b_rows)) != cudaSuccess)
@@ -1006,10 +1019,9 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.n_tiles = (a.d + MMA_N - 1) / MMA_N;
     if (swap) {
         if ((err = make_map(&mA, a.W2, a.F, uint64_t(a.E) * a.d, 128)) != cudaSuccess) return err;
-        if ((err = make_map(&mB, a.h, kA, rows_max, 128)) != cudaSuccess) return err;
-        if ((err = make_map(&mX16, a.h, kA, rows_max, 16)) != cudaSuccess) return err;
-        return f32_out ? launch_swap<kPlain, kOutF32>(mA, mB, mX16, p, rows_max, a.E, stream)
-                       : launch_swap<kPlain, kOutBF16>(mA, mB, mX16, p, rows_max, a.E, stream);
+        if ((err = make_row_maps(&mX, a.h, kA, rows_max)) != cudaSuccess) return err;
+        return f32_out ? launch_swap<kPlain, kOutF32>(mA, mX, p, rows_max, a.E, stream)
+                       : launch_swap<kPlain, kOutBF16>(mA, mX, p, rows_max, a.E, stream);
     }
     if ((err = make_map(&mA, a.h, kA, rows_max, 128)) != cudaSuccess) return err;
     if ((err = make_map(&mB, a.W2, a.F, uint64_t(a.E) * a.d, b_rows)) != cudaSuccess) return err;
