@@ -80,6 +80,13 @@ Readings where the pages are silent (each is listed in the design notes too):
   e4m3's largest finite value; an all-zero block takes s = 0); each element is
   x / 2^s rounded to the nearest e4m3 value (ties to the even code); the receiver
   multiplies back by 2^s, which is exact, so the experts see q * 2^s.
+* FP8 expert GEMM ([FP8], and "Memory residency for the same shape" of the same page,
+  which sizes the experts' weights in FP8 with scale tensors; the scale granularity
+  of the GEMM's operands is ours): the same rule with one block per row. Every dispatched
+  row (routed and shared) is q * 2^s with one s per token row, and the up projection's
+  weights are quantized per output channel (one s per row of W13) the same way; the
+  up projection then multiplies those exact values, h and the down projection are
+  as in the bf16 path.
 * deduplicated dispatch [DEDUP]: with D virtual ranks (rank r owns routed experts
   [r E/D, (r+1) E/D)), token t sends one row to rank r when at least one of its
   kept routed assignments lives there; send rows are rank-major, in token order
@@ -116,6 +123,7 @@ __all__ = [
     "dedup_send",
     "e4m3_values",
     "quantize_fp8_blocks",
+    "quantize_fp8_rows",
     "round_to_bf16",
 ]
 
@@ -439,6 +447,37 @@ def quantize_fp8_blocks(x, block: int = 128) -> dict:
     return dict(codes=codes, exps=exps, scales=2.0 ** exps, deq=deq)
 
 
+def quantize_fp8_rows(x, chunk: int = 2048) -> dict:
+    """Row-wise e4m3 quantization: the [FP8] rule of quantize_fp8_blocks with one block
+    per row (one scale 2^s per row). Rows are independent; they are taken ``chunk`` at a
+    time only to bound the memory of the float64 temporaries.
+
+    Returns codes [rows, d] uint8, exponents s [rows] int64, scales 2^s and the
+    dequantized rows q * 2^s (float64).
+    """
+    x = _f64(x)
+    rows, d = x.shape
+    exps = np.zeros(rows, np.int64)
+    codes = np.zeros((rows, d), np.uint8)
+    vals = e4m3_values()
+    for r0 in range(0, rows, chunk):
+        seg = x[r0:r0 + chunk]
+        amax = np.abs(seg).max(axis=1) if d else np.zeros(seg.shape[0])
+        nz = amax > 0
+        s = np.zeros(seg.shape[0], np.int64)
+        s[nz] = np.ceil(np.log2(amax[nz] / 448.0)).astype(np.int64)
+        while True:  # guard the log against rounding: the smallest s with amax / 2^s <= 448
+            up = nz & (np.ldexp(amax, -s) > 448.0)
+            down = nz & (np.ldexp(amax, -(s - 1)) <= 448.0)
+            if not (up.any() or down.any()):
+                break
+            s = s + up - down
+        exps[r0:r0 + chunk] = s
+        codes[r0:r0 + chunk] = _e4m3_round(np.ldexp(seg, -s[:, None]))
+    deq = np.ldexp(vals[codes], exps[:, None])
+    return dict(codes=codes, exps=exps, scales=np.ldexp(1.0, exps), deq=deq)
+
+
 # -------------------------------------------------------------------------- experts
 def silu(z):
     """silu(z) = z / (1 + e^-z)."""
@@ -496,7 +535,10 @@ def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, 
     slots. The deduplicated send buffer changes where rows travel, not their values,
     so y does not depend on it (``dedup_send`` describes it). With ``dispatch_dtype``
     "fp8" the rows travel as per-block e4m3 codes [FP8] and the experts receive the
-    dequantized rows; shared experts are replicated and read x itself.
+    dequantized rows; shared experts are replicated and read x itself. With
+    "fp8_gemm" every kept row (shared ones too) is the row-quantized token row
+    (``quantize_fp8_rows``); ``expert_fn`` then stands for the FP8 experts (their up
+    weights quantized per output channel, see packed.expert_fn).
     """
     x = _f64(x)
     T, d = x.shape
@@ -520,6 +562,9 @@ def moe_forward(x, Wg, k: int, expert_fn, capacity=None, bias=None, D: int = 1, 
         xq = quantize_fp8_blocks(x)["deq"]
         routed = (rs >= 0) & (idx.reshape(-1)[np.maximum(rs, 0)] < E)
         xperm[routed] = xq[rs[routed] // k]
+    elif dispatch_dtype == "fp8_gemm":
+        xq = quantize_fp8_rows(x)["deq"]
+        xperm[rs >= 0] = xq[rs[rs >= 0] // k]
     out = np.zeros_like(xperm)
     off = disp["offsets"]
     for e in range(E + n_shared):

@@ -23,10 +23,12 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def expert_fn(kind: str, W13, W2, F: int, faithful: bool = False, cache=None):
+def expert_fn(kind: str, W13, W2, F: int, faithful: bool = False, cache=None, fp8_up: bool = False):
     """Expert_e(X) for the oracle, reading expert e's packed weights on demand.
 
-    ``cache`` (a dict) keeps each expert's float64 weights after first use.
+    ``cache`` (a dict) keeps each expert's float64 weights after first use. With
+    ``fp8_up`` the up-projection weights are the oracle's row-wise e4m3 quantization of
+    W13[e] (one scale per output channel), as the FP8 expert GEMM uses them.
     """
     if kind == "identity":
         return lambda e, X: X
@@ -34,7 +36,10 @@ def expert_fn(kind: str, W13, W2, F: int, faithful: bool = False, cache=None):
     def weights(e):
         if cache is not None and e in cache:
             return cache[e]
-        w = (f64(W13[e]), f64(W2[e]))
+        w13 = f64(W13[e])
+        if fp8_up:
+            w13 = orc.quantize_fp8_rows(w13)["deq"]
+        w = (w13, f64(W2[e]))
         if cache is not None:
             cache[e] = w
         return w
@@ -56,7 +61,8 @@ def run_oracle(w, inp: dict, capacity="auto", faithful: bool = False, cache=None
     """Oracle forward of workload ``w`` (sizes, expert kind, capacity) on tensors ``inp``."""
     if capacity == "auto":
         capacity = orc.expert_capacity(w.T, w.k, w.E, w.capacity_factor, w.min_capacity)
-    fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, faithful=faithful, cache=cache)
+    fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, faithful=faithful, cache=cache,
+                   fp8_up=getattr(w, "dispatch_dtype", "act") == "fp8_gemm")
     return orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), w.k, fn, capacity=capacity,
                            bias=f64(inp.get("bias")), D=w.D, n_shared=getattr(w, "n_shared", 0),
                            drop_policy=getattr(w, "drop_policy", "token"), layout=getattr(w, "layout", "packed"),

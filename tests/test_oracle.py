@@ -584,3 +584,54 @@ def test_fp8_forward_sends_the_dequantized_rows():
     inp = wl.make_inputs(w, seed=52)
     res = orc.moe_forward(f64(inp["x"]), f64(inp["Wg"]), 1, lambda e, X: X, dispatch_dtype="fp8")
     np.testing.assert_array_equal(res["y"], orc.quantize_fp8_blocks(f64(inp["x"]))["deq"])
+
+
+def test_fp8_rows_are_the_block_rule_with_one_block_per_row():
+    r = rng(53)
+    x = r.normal(size=(40, 300)) * np.exp(r.normal(size=(40, 1)) * 4)
+    x[3] = 0.0
+    x[5] = -0.0
+    x[7, 11] = 449.0
+    x[8, :] = 2.0 ** -140  # far below e4m3's range: a large negative scale exponent
+    q = orc.quantize_fp8_rows(x, chunk=7)
+    b = orc.quantize_fp8_blocks(x, block=300)
+    assert np.array_equal(q["codes"], b["codes"]) and np.array_equal(q["exps"], b["exps"][:, 0])
+    assert np.array_equal(q["deq"], b["deq"])
+    assert q["exps"][3] == 0 and not q["deq"][3].any() and np.all(q["codes"][5] == 0x80)
+    assert q["exps"][8] == -148 and np.all(q["deq"][8] == 2.0 ** -140)  # 2^-140 / 2^-148 = 256 <= 448 < 512
+    # cross-check of the codes against torch's float8 conversion of x / 2^s
+    ref = torch.tensor(np.ldexp(x, -q["exps"][:, None]), dtype=torch.float64).to(torch.float32)
+    assert np.array_equal(q["codes"], ref.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+
+
+def test_fp8_gemm_forward_quantizes_every_kept_row_once_per_token():
+    w = wl.Workload("t", T=40, d=256, E=4, k=1, F=0, act="bf16", expert="identity", n_shared=1)
+    inp = wl.make_inputs(w, seed=54)
+    x = f64(inp["x"])
+    res = orc.moe_forward(x, f64(inp["Wg"]), 1, lambda e, X: X, n_shared=1, dispatch_dtype="fp8_gemm")
+    # one routed expert (gate 1) plus the shared one (gate 1), both fed the row-quantized token
+    np.testing.assert_array_equal(res["y"], 2 * orc.quantize_fp8_rows(x)["deq"])
+
+
+def test_fp8_expert_equals_the_plain_expert_on_e4m3_exact_weights():
+    """Weights whose rows are e4m3 values times one power of two per row (with a
+    full-range value in each row, so the row scale is that power) quantize to
+    themselves: the FP8 up projection must then be the plain expert exactly."""
+    from oracle.packed import expert_fn
+    r = rng(55)
+    E, d, F = 2, 64, 32
+    vals = orc.e4m3_values()[:0x7F]
+    codes = r.integers(0, 0x7F, size=(E, 2 * F, d))
+    W13 = vals[codes] * np.where(r.random((E, 2 * F, d)) < 0.5, -1, 1)
+    W13[:, :, 0] = 448.0
+    W13 = W13 * np.ldexp(1.0, r.integers(-12, -4, size=(E, 2 * F, 1)))
+    W2 = r.normal(size=(E, d, F))
+    X = r.normal(size=(5, d))
+    plain = expert_fn("swiglu", W13, W2, F)
+    fp8 = expert_fn("swiglu", W13, W2, F, fp8_up=True)
+    for e in range(E):
+        np.testing.assert_array_equal(fp8(e, X), plain(e, X))
+    # a weight that is not e4m3-exact changes the result
+    W13[0, 0, 1] = 448.0 * 1.01 * 2.0 ** -12
+    assert not np.array_equal(expert_fn("swiglu", W13, W2, F, fp8_up=True)(0, X), plain(0, X))
+
