@@ -182,9 +182,10 @@ def load_traffic(workload: str, kernel: str):
 
 
 # ------------------------------------------------------------------ algorithmic work
-def fp8_row_bytes(d: int) -> int:
-    """Wire bytes of one FP8-dispatched row: d e4m3 codes and a 4-byte scale per 128-element block."""
-    return d + 4 * ((d + 127) // 128)
+def fp8_row_bytes(d: int, per_row: bool = False) -> int:
+    """Wire bytes of one FP8-dispatched row: d e4m3 codes and a 4-byte scale per 128-element
+    block (or one per row, the FP8-GEMM format)."""
+    return d + 4 * (1 if per_row else (d + 127) // 128)
 
 
 def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, routed_rows: int = 0) -> dict:
@@ -193,21 +194,27 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
     With the deduplicated dispatch the rows travel x -> send buffer -> expert rows: x is
     read once, each send row written once and read once, each expert row written once.
     With the FP8 dispatch each routed row is written as codes + scales, read back and
-    written as a bf16 row.
+    written as a bf16 row. With the FP8 GEMM every row is written once as codes + its
+    scale (instead of a bf16 row) and the up projection reads those and the e4m3 weights.
     """
     b = w.act_bytes
     up, down = sizing.expert_gemm_flops(rows, w.d, w.F, w.expert)
     ident = w.expert == "identity"
+    f8g = w.dispatch_dtype == "fp8_gemm"
     dispatch = sizing.dispatch_hbm_bytes(w.T, w.d, rows, b) + (2 * rows_sent * w.d * b if w.dedup else 0)
     if w.dispatch_dtype == "fp8":
         dispatch += 2 * routed_rows * fp8_row_bytes(w.d)
+    if f8g:  # x read once, each row written as codes + one scale
+        dispatch = dispatch - rows * w.d * b + rows * fp8_row_bytes(w.d, per_row=True)
+    up_in = rows * fp8_row_bytes(w.d, per_row=True) if f8g else rows * w.d * b
+    w13_bytes = w.n_experts * w.w13_rows * (w.d + 4) if f8g else w.n_experts * w.w13_rows * w.d * b
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
         route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.slots * 8,
         dispatch_bytes=dispatch,
         combine_bytes=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
         up_flops=up, down_flops=down,
-        up_bytes=0 if ident else w.n_experts * w.w13_rows * w.d * b + rows * w.d * b + rows * h_cols * b,
+        up_bytes=0 if ident else w13_bytes + up_in + rows * h_cols * b,
         down_bytes=0 if ident else w.n_experts * w.d * w.F * b + rows * h_cols * b + rows * w.d * out_bytes,
     )
 
@@ -227,7 +234,8 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
     x = f64(inp["x"][torch.as_tensor(sel, device=inp["x"].device)])
     Wg, bias = f64(inp["Wg"]), f64(inp.get("bias"))
     cache = {} if cache is None else cache
-    fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, cache=cache)
+    fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, cache=cache,
+                   fp8_up=w.dispatch_dtype == "fp8_gemm")
     grouped = 0 < w.topk_groups < w.n_groups
     if w.expert != "identity":  # model load: the experts this sample uses, converted once
         H = orc.router_logits(x, Wg, bias)
@@ -271,16 +279,19 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.set_device(device)
     inp = wl.make_inputs(w, seed=rank, device=device)
     cfg = abi.config_for(w)
+    # the FP8-GEMM layer takes its up weights as the library's e4m3 buffer (quantized
+    # once, like a model load, before any timing)
+    w13 = abi.fp8_weights(cfg, inp["W13"]) if w.dispatch_dtype == "fp8_gemm" else inp.get("W13")
     ws = abi.workspace(cfg, device)
     y = torch.empty(w.T, w.d, dtype=w.torch_act, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step(events=None):
         if events is None:
-            abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"), y, ws)
+            abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), w13, inp.get("W2"), y, ws)
         else:
-            abi.moe_layer_forward_traced(cfg, inp["x"], inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"),
-                                         y, ws, events)
+            abi.moe_layer_forward_traced(cfg, inp["x"], inp["Wg"], inp.get("bias"), w13, inp.get("W2"), y, ws,
+                                         events)
 
     for _ in range(args.warmup):
         step()
@@ -343,7 +354,7 @@ def run_ours(args, w, world, rank, local):
     # (moe_layer_forward_host_async, one workspace and one y buffer per stream), so that
     # one batch's copies run on the copy engines under the other's kernels.
     x_host = inp["x"].cpu().pin_memory()
-    fwd_args = (inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"))
+    fwd_args = (inp["Wg"], inp.get("bias"), w13, inp.get("W2"))
     ws_h = [abi.workspace(cfg, device, host=True) for _ in range(2)]
     y_h = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
     streams = [torch.cuda.Stream(device) for _ in range(2)]
@@ -390,6 +401,10 @@ def run_ours(args, w, world, rank, local):
     if w.dispatch_dtype == "fp8":
         fp8 = {"wire_bytes": routed_rows * fp8_row_bytes(w.d), "bf16_wire_bytes": routed_rows * w.d * 2,
                "ratio": fp8_row_bytes(w.d) / (w.d * 2)}
+    if w.dispatch_dtype == "fp8_gemm":
+        fp8 = {"format": "e4m3 codes + one power-of-two scale per row, read as they are by the e4m3 up GEMM",
+               "wire_bytes": rows * fp8_row_bytes(w.d, True), "bf16_wire_bytes": rows * w.d * 2,
+               "ratio": fp8_row_bytes(w.d, True) / (w.d * 2)}
     work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0, routed_rows)
     peaks, peak_src = load_peaks()
     value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
@@ -402,24 +417,38 @@ def run_ours(args, w, world, rank, local):
     # point (bf16 peak / HBM bandwidth), else HBM-bound on its weight stream
     ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
     ffn_kernel = abi.moe_ffn_kernel_name(cfg)
+    f8g = w.dispatch_dtype == "fp8_gemm"
+    # e4m3 up projection: the swapped-pair kernel on FP8; the down projection is the bf16 variant
+    down_kernel = abi.moe_ffn_kernel_name(abi.config_for(wl.scaled(w, dispatch_dtype="act"))) if f8g else ffn_kernel
     up_name = "%s<%s> (up)" % (ffn_kernel, "SwiGLU" if w.expert == "swiglu" else "ReLU")
+    # peak of each contraction in its own dtype: e4m3 takes the measured bf16 peak times
+    # the nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
+    up_peak_scale = 2.0 if f8g else 1.0
 
     def gemm_entry(name, flops, nbytes):
         if nbytes and flops / nbytes < ridge:
             return (name, "hbm", nbytes)
         return (name, "tensor", flops)
 
+    up_entry = gemm_entry(up_name, work["up_flops"] / up_peak_scale, work["up_bytes"])
+    if up_entry[1] == "tensor":
+        up_entry = (up_name, "tensor", work["up_flops"])
+
     kernel_work = {
         "route": ("route_gemm_kernel + route_topk_kernel", "alu", work["route_flops"]),
         "dispatch": ("dispatch (count+scan+scatter+gather)", "hbm", work["dispatch_bytes"]),
-        "expert_up": gemm_entry(up_name, work["up_flops"], work["up_bytes"]),
-        "expert_down": gemm_entry("%s<Plain> (down)" % ffn_kernel, work["down_flops"], work["down_bytes"]),
+        "expert_up": up_entry,
+        "expert_down": gemm_entry("%s<Plain> (down)" % down_kernel, work["down_flops"], work["down_bytes"]),
         "combine": ("combine_kernel", "hbm", work["combine_bytes"]),
     }
     dom = max(STAGES, key=lambda s: stage_ms[s])
     kname, bound, amount = kernel_work[dom]
     dom_s = stage_ms[dom] / 1e3
-    if bound == "tensor":
+    if bound == "tensor" and dom == "expert_up" and f8g:
+        peak = float(peaks["bf16_tflops"]) * up_peak_scale
+        roof = {"bound": "tensor", "achieved": amount / dom_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16 burst x 2 (nominal e4m3 / bf16 dense ratio)"}
+    elif bound == "tensor":
         peak = float(peaks["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": amount / dom_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16 burst"}
@@ -441,7 +470,8 @@ def run_ours(args, w, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.act, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 up, bf16 down" if f8g else w.act,
+        "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "F": w.F, "expert": w.expert,
                    "n_shared": w.n_shared,
                    "capacity": None if cfg.capacity < 0 else int(cfg.capacity), "D_virtual": w.D,
@@ -450,7 +480,8 @@ def run_ours(args, w, world, rank, local):
                    "dispatch_dtype": w.dispatch_dtype,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
-                         "dispatched rows" % (w.n_experts * (w.w13_rows + w.F) * w.d * w.act_bytes / 1e9
+                         "dispatched rows" % (w.n_experts * (w.w13_rows * (1 if f8g else w.act_bytes)
+                                                              + w.F * w.act_bytes) * w.d / 1e9
                                               if w.expert != "identity" else 0.0,
                                               rows * w.d * w.act_bytes / 1e6)},
         "roofline": roof,

@@ -105,6 +105,14 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
                               block ("MoE Expert Parallelism Sizing", "First-order dispatch and combine
                               bytes": FP8 dispatch halves the row, the combine stays wide); the receiving
                               side turns them back into bf16 rows (exact); bf16 activations only */
+#define MOE_DISPATCH_FP8_GEMM 2 /* every dispatched row (routed and shared) as e4m3 codes with one
+                              power-of-two fp32 scale per row, consumed as they are by an FP8 up
+                              projection (tcgen05 kind::f8f6f4: e4m3 x e4m3 products, fp32
+                              accumulation) against e4m3 W13 with one power-of-two scale per output
+                              channel (moe_quantize_weights_fp8); h, W2 and the down projection stay
+                              bf16. One scale per row, not per 128-element block, so that the GEMM can
+                              apply it after the K loop. bf16 activations, ReLU or SwiGLU experts,
+                              d % 16 == 0, no dedup, not MOE_PRECISION_SPLIT_H */
 
 /* Limits of this build. */
 #define MOE_MAX_K 16        /* experts per token, routed plus shared */
@@ -132,7 +140,7 @@ typedef struct moe_config {
     int32_t dedup;       /* 1: moe_layer_forward sends each token once per virtual rank (the
                           * deduplicated dispatch, see moe_dispatch_dedup) and fans the send rows
                           * out into the expert rows; D <= 16. 0: rows go straight from x. */
-    int32_t dispatch_dtype; /* MOE_DISPATCH_*; FP8 needs bf16 activations and no dedup */
+    int32_t dispatch_dtype; /* MOE_DISPATCH_*; the FP8 formats need bf16 activations and no dedup */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
@@ -171,8 +179,10 @@ typedef struct moe_workspace_view {
                           * padding rows of out unwritten */
     moe_send_map send;   /* cfg->dedup only (NULL pointers otherwise) */
     void* xsend;         /* [T*D, d] act: the deduplicated send buffer (cfg->dedup only) */
-    uint8_t* xq;         /* [rows, d] e4m3 codes of the routed rows (MOE_DISPATCH_FP8 only) */
-    float* xscale;       /* [rows, ceil(d/128)] their block scales (MOE_DISPATCH_FP8 only) */
+    uint8_t* xq;         /* [rows, d] e4m3 codes of the dispatched rows (MOE_DISPATCH_FP8: routed rows;
+                          * MOE_DISPATCH_FP8_GEMM: all rows); NULL for MOE_DISPATCH_ACT */
+    float* xscale;       /* their scales: [rows, ceil(d/128)] block scales (MOE_DISPATCH_FP8) or [rows]
+                          * row scales (MOE_DISPATCH_FP8_GEMM); NULL for MOE_DISPATCH_ACT */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -261,7 +271,8 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
                        moe_stream_t stream);
 
 /* FP8 dispatch of the rows a moe_dispatch with the same cfg mapped (its pos, row_src
- * and offsets): each token row is quantized once, per 128-element block, to e4m3 codes
+ * and offsets).
+ * MOE_DISPATCH_FP8: each token row is quantized once, per 128-element block, to e4m3 codes
  * with the scale 2^s, s the smallest integer with amax/2^s <= 448 (round to nearest,
  * ties to even, sign kept), and written to each of its kept routed rows
  * ("MoE Expert Parallelism Sizing", "First-order dispatch and combine bytes": the
@@ -273,7 +284,10 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
  *   xperm   [rows, d] bf16 out, or NULL (shared rows then need a moe_dispatch gather)
  *   ws      >= moe_dispatch_workspace_bytes(cfg); its first 4 bytes are the status word,
  *           cleared by this call.
- * Needs cfg->dispatch_dtype == MOE_DISPATCH_FP8. Bit-exact and deterministic. */
+ * MOE_DISPATCH_FP8_GEMM: the same rule over the whole row (one scale 2^s per token row),
+ * and every kept row, routed or shared, receives the codes: xq [rows, d] uint8 and
+ * xscale [rows] fp32 out; xperm must be NULL (the FP8 up projection reads xq as it is).
+ * Needs one of the two FP8 dispatch dtypes. Bit-exact and deterministic. */
 int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                      const moe_dispatch_map* map, uint8_t* xq, float* xscale, void* xperm, void* ws,
                      size_t ws_bytes, moe_stream_t stream);
@@ -294,10 +308,34 @@ int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_i
  * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation); fp32
  * runs on the fp32 FMA units. Requires F * sizeof(act) % 16 == 0 besides the row
  * rule. ws >= moe_ffn_workspace_bytes(cfg); its first 4 bytes are the status word
- * (cleared). */
+ * (cleared). A MOE_DISPATCH_FP8_GEMM config takes moe_expert_ffn_fp8 instead (MOE_ERR_ARG
+ * here). */
 int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets,
                    const void* W13, const void* W2, void* h, void* out,
                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Bytes of the FP8 up-projection weights of a MOE_DISPATCH_FP8_GEMM config: the e4m3
+ * codes of W13 ([N, R, d] uint8, R = 2F for SwiGLU, F for ReLU), then, at the next
+ * 256-byte boundary, one fp32 scale per weight row ([N, R]). 0 for other configs. */
+size_t moe_fp8_weight_bytes(const moe_config* cfg);
+
+/* Quantizes the bf16 W13 [N, R, d] (layout as in moe_expert_ffn) into that buffer:
+ * each weight row (one output channel) gets the scale 2^s, s the smallest integer with
+ * amax/2^s <= 448, and the codes round(w / 2^s) to the nearest e4m3 value (ties to
+ * even, sign kept). W13_fp8 holds moe_fp8_weight_bytes(cfg) bytes, 16-byte aligned.
+ * Needs cfg->dispatch_dtype == MOE_DISPATCH_FP8_GEMM. Bit-exact and deterministic. */
+int moe_quantize_weights_fp8(const moe_config* cfg, const void* W13, void* W13_fp8, moe_stream_t stream);
+
+/* moe_expert_ffn for a MOE_DISPATCH_FP8_GEMM config: the up projection runs on the
+ * e4m3 rows and weights (tcgen05 kind::f8f6f4 on SM pairs), its fp32 accumulator
+ * multiplied by the row scale and the weight row's scale before the activation; h is
+ * rounded once to bf16 and the down projection is the bf16 one.
+ *   xq      [rows, d] uint8 e4m3 codes;  xscale [rows] fp32 row scales (moe_dispatch_fp8)
+ *   W13_fp8 moe_quantize_weights_fp8's buffer;  W2 [N, d, F] bf16
+ *   offsets, h, out, ws as in moe_expert_ffn. */
+int moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* xscale, const int32_t* offsets,
+                       const void* W13_fp8, const void* W2, void* h, void* out, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /* Combine: y[t] = sum over slots j < K with pos[t*K+j] >= 0 of topk_gate[t*K+j] * out[pos[t*K+j]],
  * with `out` in the dtype moe_expert_ffn writes (see there; the activation dtype for
@@ -313,7 +351,8 @@ int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate,
 
 /* The whole layer: route, dispatch, expert FFN, combine. Intermediates live in ws
  * (layout: moe_workspace_get_view). ws >= moe_workspace_bytes(cfg); the status word
- * is cleared at the start. W13/W2 may be NULL for identity experts. y [T, d] act. */
+ * is cleared at the start. W13/W2 may be NULL for identity experts. Under
+ * MOE_DISPATCH_FP8_GEMM, W13 is moe_quantize_weights_fp8's buffer. y [T, d] act. */
 int moe_layer_forward(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
                       const void* W13, const void* W2, void* y, void* ws, size_t ws_bytes,
                       moe_stream_t stream);

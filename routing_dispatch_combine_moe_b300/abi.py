@@ -29,8 +29,8 @@ MOE_DROP_TOKEN_ORDER, MOE_DROP_LOW_GATE = 0, 1
 DROP_POLICIES = {"token": MOE_DROP_TOKEN_ORDER, "gate": MOE_DROP_LOW_GATE}
 MOE_LAYOUT_PACKED, MOE_LAYOUT_PADDED = 0, 1
 LAYOUTS = {"packed": MOE_LAYOUT_PACKED, "padded": MOE_LAYOUT_PADDED}
-MOE_DISPATCH_ACT, MOE_DISPATCH_FP8 = 0, 1
-DISPATCH_DTYPES = {"act": MOE_DISPATCH_ACT, "fp8": MOE_DISPATCH_FP8}
+MOE_DISPATCH_ACT, MOE_DISPATCH_FP8, MOE_DISPATCH_FP8_GEMM = 0, 1, 2
+DISPATCH_DTYPES = {"act": MOE_DISPATCH_ACT, "fp8": MOE_DISPATCH_FP8, "fp8_gemm": MOE_DISPATCH_FP8_GEMM}
 MOE_MAX_K, MOE_MAX_E = 16, 512
 EXPERT_KINDS = {"identity": MOE_EXPERT_IDENTITY, "relu": MOE_EXPERT_RELU, "swiglu": MOE_EXPERT_SWIGLU}
 ACT_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16}
@@ -96,6 +96,9 @@ _SIGNATURES = {
                                           _p, _p, _sz, _p]),
     "moe_dispatch_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
                                         _p, _p, _p, _sz, _p]),
+    "moe_fp8_weight_bytes": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_quantize_weights_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p]),
+    "moe_expert_ffn_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_dispatch_map),
                                            _p, _p]),
     "moe_read_status": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
@@ -305,7 +308,8 @@ def moe_dispatch_dedup(cfg, x, topk_idx, pos, smap: moe_send_map, xsend, xperm, 
 
 
 def moe_dispatch_fp8(cfg, x, topk_idx, dmap: moe_dispatch_map, xq, xscale, xperm, ws, stream=None):
-    """FP8 (e4m3, per-128 power-of-two scales) rows of a moe_dispatch map; xperm may be None."""
+    """FP8 (e4m3, power-of-two scales per 128-element block, or per row for "fp8_gemm")
+    rows of a moe_dispatch map; xperm may be None (and must be for "fp8_gemm")."""
     _check(lib().moe_dispatch_fp8(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), ctypes.byref(dmap), _ptr(xq),
                                   _ptr(xscale), _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_dispatch_fp8")
@@ -320,6 +324,36 @@ def moe_dispatch_static(cfg, x, topk_idx, dmap: moe_dispatch_map, xperm, stream=
 def moe_expert_ffn(cfg, xperm, offsets, W13, W2, h, out, ws, stream=None):
     _check(lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(xperm), _ptr(offsets), _ptr(W13), _ptr(W2), _ptr(h),
                                 _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_fp8_weight_bytes(cfg) -> int:
+    """Bytes of the FP8 W13 buffer of an "fp8_gemm" config (codes, then row scales)."""
+    return lib().moe_fp8_weight_bytes(ctypes.byref(cfg))
+
+
+def moe_quantize_weights_fp8(cfg, W13, W13_fp8, stream=None):
+    _check(lib().moe_quantize_weights_fp8(ctypes.byref(cfg), _ptr(W13), _ptr(W13_fp8), _stream(stream)),
+           "moe_quantize_weights_fp8")
+
+
+def fp8_weights(cfg, W13, stream=None) -> torch.Tensor:
+    """The FP8 W13 buffer (uint8, on W13's device) of an "fp8_gemm" config."""
+    q = torch.empty(moe_fp8_weight_bytes(cfg), dtype=torch.uint8, device=W13.device)
+    moe_quantize_weights_fp8(cfg, W13, q, stream)
+    return q
+
+
+def fp8_weight_parts(cfg, W13_fp8, N: int, R: int, d: int):
+    """Views of an FP8 W13 buffer: codes [N, R, d] uint8 and row scales [N, R] fp32."""
+    n = N * R * d
+    off = (n + 255) // 256 * 256
+    return W13_fp8[:n].view(N, R, d), W13_fp8[off:off + 4 * N * R].view(torch.float32).view(N, R)
+
+
+def moe_expert_ffn_fp8(cfg, xq, xscale, offsets, W13_fp8, W2, h, out, ws, stream=None):
+    _check(lib().moe_expert_ffn_fp8(ctypes.byref(cfg), _ptr(xq), _ptr(xscale), _ptr(offsets), _ptr(W13_fp8),
+                                    _ptr(W2), _ptr(h), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_expert_ffn_fp8")
 
 
 def moe_combine(cfg, out, topk_gate, pos, y, status=None, stream=None):

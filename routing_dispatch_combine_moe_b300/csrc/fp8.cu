@@ -14,6 +14,14 @@
 //                       to each of the token's kept routed rows;
 //   dequant_fp8_kernel  one warp per dispatched row: codes x scale back to bf16 rows
 //                       for the expert GEMMs (the receiving side).
+//
+// Row-scaled format (the FP8 up projection's input): the same rule with one block per
+// row, so a row has one scale 2^s; every kept row of a token, routed or shared, gets the
+// codes, and the expert GEMM reads them as they are (the scale is applied to its fp32
+// accumulator). The expert weights take the same format, one scale per weight row.
+//   gather_fp8_row_kernel  one warp per token: amax over the row, then the codes to
+//                          each kept row and the scale;
+//   quantize_rows_kernel   one warp per row of a bf16 matrix (the W13 weights).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -28,6 +36,78 @@ __device__ __forceinline__ int block_exponent(float amax) {
     int e;
     const float m = frexpf(amax, &e);
     return e - 9 + (m > 0.875f ? 1 : 0);
+}
+
+// e4m3 codes of the 8 bf16 values of `raw` divided by 2^s, packed little-end first.
+__device__ __forceinline__ uint2 e4m3_pack8(const uint4 raw, int s) {
+    const float f[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                        bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t c = __nv_cvt_float_to_fp8(ldexpf(f[i], -s), __NV_SATFINITE, __NV_E4M3);
+        if (i < 4) lo |= c << (8 * i);
+        else hi |= c << (8 * (i - 4));
+    }
+    return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ float absmax8(const uint4 raw) {
+    const float m0 = fmaxf(fmaxf(fabsf(bf16_lo(raw.x)), fabsf(bf16_hi(raw.x))),
+                           fmaxf(fabsf(bf16_lo(raw.y)), fabsf(bf16_hi(raw.y))));
+    const float m1 = fmaxf(fmaxf(fabsf(bf16_lo(raw.z)), fabsf(bf16_hi(raw.z))),
+                           fmaxf(fabsf(bf16_lo(raw.w)), fabsf(bf16_hi(raw.w))));
+    return fmaxf(m0, m1);
+}
+
+// Scale exponent of one bf16 row of vpr 16-byte pieces, read by the 32 lanes of a warp.
+__device__ __forceinline__ int row_exponent(const uint4* __restrict__ src, int vpr, int lane) {
+    float am = 0.f;
+    for (int v = lane; v < vpr; v += 32) am = fmaxf(am, absmax8(__ldg(src + v)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+    return block_exponent(am);
+}
+
+__global__ void __launch_bounds__(256) gather_fp8_row_kernel(const uint4* __restrict__ x,
+                                                             const int32_t* __restrict__ pos, int T, int K, int d,
+                                                             int64_t max_rows, uint8_t* __restrict__ xq,
+                                                             float* __restrict__ xscale, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int vpr = d / 8;
+    int p = -1;
+    if (lane < K) {
+        const int r = pos[size_t(t) * K + lane];
+        if (r >= max_rows) set_status(status, MOE_DEV_ERR_INDEX);
+        else p = r;
+    }
+    int dst[MOE_MAX_K];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_K; ++j) dst[j] = __shfl_sync(0xFFFFFFFFu, p, j);
+    const uint4* src = x + size_t(t) * vpr;
+    const int s = row_exponent(src, vpr, lane);
+    for (int v = lane; v < vpr; v += 32) {
+        const uint2 c = e4m3_pack8(__ldg(src + v), s);
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j)
+            if (j < K && dst[j] >= 0) *reinterpret_cast<uint2*>(xq + size_t(dst[j]) * d + size_t(v) * 8) = c;
+    }
+    if (lane < K && p >= 0) xscale[p] = ldexpf(1.f, s);
+}
+
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ w, int64_t n_rows, int d,
+                                                            uint8_t* __restrict__ q, float* __restrict__ scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (r >= n_rows) return;
+    const int vpr = d / 8;
+    const uint4* src = w + size_t(r) * vpr;
+    const int s = row_exponent(src, vpr, lane);
+    for (int v = lane; v < vpr; v += 32)
+        *reinterpret_cast<uint2*>(q + size_t(r) * d + size_t(v) * 8) = e4m3_pack8(__ldg(src + v), s);
+    if (lane == 0) scale[r] = ldexpf(1.f, s);
 }
 
 __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ x,
@@ -67,27 +147,17 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict
 #pragma unroll
         for (int j = 0; j < MOE_MAX_K; ++j)
             if (j < K && sdst[j] >= 0 && ok) xperm[size_t(sdst[j]) * vpr + v] = raw;
-        float f[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
-                      bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
-        float am = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+        float am = absmax8(raw);
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
         const int s = block_exponent(am);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t c = __nv_cvt_float_to_fp8(ldexpf(f[i], -s), __NV_SATFINITE, __NV_E4M3);
-            if (i < 4) lo |= c << (8 * i);
-            else hi |= c << (8 * (i - 4));
-        }
+        const uint2 c = e4m3_pack8(raw, s);
         const int blk = v0 / 16 + (lane >> 4);  // 128-element block of this half-warp
         const bool writes_scale = (lane & 15) == 0 && blk < nb;
 #pragma unroll
         for (int j = 0; j < MOE_MAX_K; ++j) {
             if (j < K && dst[j] >= 0) {
-                if (ok) *reinterpret_cast<uint2*>(xq + size_t(dst[j]) * d + size_t(v) * 8) = make_uint2(lo, hi);
+                if (ok) *reinterpret_cast<uint2*>(xq + size_t(dst[j]) * d + size_t(v) * 8) = c;
                 if (writes_scale) xscale[size_t(dst[j]) * nb + blk] = ldexpf(1.f, s);
             }
         }
@@ -130,6 +200,11 @@ __global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restr
 }  // namespace
 
 cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream) {
+    if (a.per_row) {
+        gather_fp8_row_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos, a.T, a.K,
+                                                                  a.d, a.rows, a.xq, a.xscale, a.status);
+        return cudaGetLastError();
+    }
     gather_fp8_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.topk_idx, a.pos, a.T,
                                                           a.K, a.d, a.E_routed, a.rows, a.xq, a.xscale,
                                                           static_cast<uint4*>(a.xperm), a.status);
@@ -140,6 +215,14 @@ cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream) {
                                                                             a.offsets, a.n_experts, a.d,
                                                                             a.E_routed, a.rows,
                                                                             static_cast<uint4*>(a.xperm));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows_fp8(const void* w, int64_t n_rows, int d, uint8_t* q, float* scale,
+                                     cudaStream_t stream) {
+    if (n_rows <= 0) return cudaSuccess;
+    quantize_rows_kernel<<<unsigned((n_rows + 7) / 8), 256, 0, stream>>>(static_cast<const uint4*>(w), n_rows, d, q,
+                                                                         scale);
     return cudaGetLastError();
 }
 

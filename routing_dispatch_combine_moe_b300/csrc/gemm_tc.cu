@@ -88,6 +88,8 @@ struct Params {
     int n_tiles;             // output column tiles
     int32_t* status;
     int skip_arrive;         // failure-path test: never signal the first finished accumulator
+    const float* xscale;     // e4m3 inputs: scale of each row of B (swapped pairs) ...
+    const float* wscale;     // ... and of each weight row
 };
 
 template <int STAGES>
@@ -514,6 +516,16 @@ __device__ __forceinline__ void swap_tile_rows(const int* off, const int* end, i
     n = (len + 31) & ~31;
 }
 
+// e4m3 inputs: accumulator column j (row row0 + j) times the thread's weight-row scale
+// and that row's scale; lane j fetches row j's scale (0 past the n_valid rows).
+__device__ __forceinline__ void scale_columns(uint32_t (&v)[32], float wsc, const float* __restrict__ xscale,
+                                              int row0, int n_valid, int lane) {
+    const float sx = lane < n_valid ? __ldg(xscale + row0 + lane) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        v[j] = __float_as_uint(__uint_as_float(v[j]) * (wsc * __shfl_sync(0xFFFFFFFFu, sx, j)));
+}
+
 template <int OUT>
 __device__ __forceinline__ void store_one(const Params& p, int row, int f, float v) {
     if constexpr (OUT == kOutF32) {
@@ -531,11 +543,15 @@ __device__ __forceinline__ void store_one(const Params& p, int row, int f, float
     }
 }
 
-template <int MODE, int OUT>
+// F8: weights and rows are e4m3 codes (kind::f8f6f4, 128 K elements per 128-byte stage
+// row); the epilogue multiplies each accumulator by its weight row's scale and its
+// row's scale, both powers of two, before the activation.
+template <int MODE, int OUT, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap mapW,
                                                                         const __grid_constant__ RowMaps mapX,
                                                                         const Params p) {
     constexpr int STAGES = SW_STAGES;
+    constexpr int BKE = F8 ? 128 : BK;  // K elements per stage: 128 bytes of every row
     constexpr int EPI_WARPS_TOTAL = 8;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -607,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
 
     const uint32_t tmem_base = S.tmem_base;
     const int total = S.tile[E] * p.n_tiles;
-    const int nkb = (p.K + BK - 1) / BK;
+    const int nkb = (p.K + BKE - 1) / BKE;
     volatile int* abort_flag = &S.abort_flag;
     const uint32_t full_base = mapa_shared(smem_addr(&S.full[0]), 0);
 
@@ -635,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    const int kW = (kb >> p.b_k_shift) * BK;
-                    const int kX = kb * BK;
+                    const int kW = (kb >> p.b_k_shift) * BKE;
+                    const int kX = kb * BKE;
                     unsigned char* a_dst = sA + s * SW_A_STAGE;
                     unsigned char* b_dst = sB + s * SW_B_BIG;
                     const uint32_t bar = full_base + uint32_t(s) * 8u;
@@ -667,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 int e, mt, nt, start, len, n;
                 decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
                 swap_tile_rows(S.off, S.end, e, mt, start, len, n);
-                const uint32_t idesc = idesc_bf16_f32(256, uint32_t(n));
+                const uint32_t idesc = F8 ? idesc_e4m3_f32(256, uint32_t(n)) : idesc_bf16_f32(256, uint32_t(n));
                 const int acc = i & 1;
                 const uint32_t aph = (i >> 1) & 1;
                 if (!mbar_wait(&S.tmem_empty[acc], aph ^ 1u, abort_flag, p.status)) break;
@@ -679,9 +695,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * SW_A_STAGE));
                     const uint64_t bdesc = sw128_kmajor_desc(smem_addr(sB + s * SW_B_BIG));
+                    // four K slices of 32 bytes per 128-byte row (descriptor addresses in 16-byte units)
 #pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks)
-                        umma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        if constexpr (F8)
+                            umma_f8_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
                     umma_commit_pair_multicast(&S.empty[s], 0x3);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -716,11 +737,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 const int w = q & 1;
                 const bool gate_warp = q < 2;
                 const int f = nt * 128 + int(rank) * 64 + w * 32 + lane;  // feature in [0, F)
+                float wsc = 1.f;
+                if constexpr (F8)
+                    wsc = f < p.F ? __ldg(p.wscale + size_t(e) * p.R + (gate_warp ? 0 : p.F) + f) : 0.f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < n; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + c0, v);
                     tmem_ld_wait();
+                    if constexpr (F8) scale_columns(v, wsc, p.xscale, start + c0, len - c0, lane);
                     if (gate_warp) {
 #pragma unroll
                         for (int j = 16; j < 32; ++j) X.v[w][j][lane] = __uint_as_float(v[j]);
@@ -743,11 +768,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 }
             } else {
                 const int f = nt * 256 + int(rank) * 128 + q * 32 + lane;
+                float wsc = 1.f;
+                if constexpr (F8) wsc = f < p.n_out ? __ldg(p.wscale + size_t(e) * p.R + f) : 0.f;
 #pragma unroll 1
                 for (int c0 = 0; c0 < n; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + c0, v);
                     tmem_ld_wait();
+                    if constexpr (F8) scale_columns(v, wsc, p.xscale, start + c0, len - c0, lane);
                     if (f < p.n_out) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -794,24 +822,27 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, inner] matrix, box = 64 x box_rows,
-// 128-byte swizzle, zero fill out of bounds.
-cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+// 2-D tensor map over a row-major [rows, inner] matrix of bf16 (or bytes, u8), box =
+// 128 bytes x box_rows, 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                     bool u8 = false) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    const uint32_t esz = u8 ? 1 : 2;
     const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {uint32_t(BK), box_rows};
+    const cuuint64_t strides[1] = {inner * esz};
+    const cuuint32_t box[2] = {128u / esz, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    const CUresult r = enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           const_cast<void*>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_row_maps(RowMaps* maps, const void* base, uint64_t inner, uint64_t rows) {
+cudaError_t make_row_maps(RowMaps* maps, const void* base, uint64_t inner, uint64_t rows, bool u8 = false) {
     for (int i = 0; i < SW_ROW_MAPS; ++i) {
-        const cudaError_t err = make_map(&maps->m[i], base, inner, rows, uint32_t(16 * (i + 1)));
+        const cudaError_t err = make_map(&maps->m[i], base, inner, rows, uint32_t(16 * (i + 1)), u8);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -888,10 +919,10 @@ int grid_for(int64_t rows_max, int E, int n_tiles, bool pair) {
     return int(g > 0 ? g : (pair ? 2 : 1));
 }
 
-template <int MODE, int OUT>
+template <int MODE, int OUT, bool F8 = false>
 cudaError_t launch_swap(const CUtensorMap& mW, const RowMaps& mX, const Params& p,
                         int64_t rows_max, int E, cudaStream_t stream) {
-    auto kern = grouped_gemm_swap_kernel<MODE, OUT>;
+    auto kern = grouped_gemm_swap_kernel<MODE, OUT, F8>;
     constexpr size_t smem = swap_smem_bytes();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -976,7 +1007,17 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.K = a.d;
     p.b_k_shift = 0;
     p.R = R;
-    if (swap) {
+    if (a.in_fp8) {
+        // e4m3 rows and weights (split_h is excluded for them): always the swapped pairs
+        p.xscale = a.xscale;
+        p.wscale = a.w13_scale;
+        if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128, true)) != cudaSuccess) return err;
+        if ((err = make_row_maps(&mX, a.xperm, a.d, rows_max, true)) != cudaSuccess) return err;
+        p.n_tiles = swiglu ? (a.F + 127) / 128 : (a.F + 255) / 256;
+        err = swiglu ? launch_swap<kSwiGLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream)
+                     : launch_swap<kReLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream);
+        p.xscale = p.wscale = nullptr;
+    } else if (swap) {
         // weights as the MMA's A operand: 64-row boxes (gate | up halves) or 128-row boxes
         if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128)) != cudaSuccess) return err;
         if ((err = make_row_maps(&mX, a.xperm, a.d, rows_max)) != cudaSuccess) return err;

@@ -102,13 +102,17 @@ struct Fp8Args {
     const int32_t* row_src;
     const int32_t* offsets;            // [n_experts + 1]; rows [0, offsets[n_experts]) are dispatched
     uint8_t* xq;                       // [rows, d]
-    float* xscale;                     // [rows, ceil(d / 128)]
+    float* xscale;                     // [rows, ceil(d / 128)], or [rows] with per_row
     void* xperm;
     bool dequant;
+    bool per_row;                      // one scale per row, codes to every kept row (the FP8 GEMM input)
     int32_t* status;
 };
 
 cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream);
+// Row-scaled e4m3 codes [n_rows, d] and scales [n_rows] of a bf16 matrix [n_rows, d].
+cudaError_t launch_quantize_rows_fp8(const void* w, int64_t n_rows, int d, uint8_t* q, float* scale,
+                                     cudaStream_t stream);
 
 // `out_dtype` is the dtype of the expert outputs (MOE_F32 or MOE_BF16), `act_dtype` that of y.
 cudaError_t launch_combine(int act_dtype, int out_dtype, const void* out, const float* gate, const int32_t* pos,
@@ -121,9 +125,12 @@ struct FfnArgs {
     int expert_kind;
     int act_dtype;
     int precision;  // MOE_PRECISION_*
-    const void* xperm;
+    const void* xperm;      // bf16 rows, or e4m3 codes with in_fp8
     const int32_t* offsets;
     const int32_t* counts;  // [E] rows computed at the start of each segment, or null (whole segments)
+    bool in_fp8;            // up projection on e4m3 rows and weights (row-scaled)
+    const float* xscale;    // [rows] with in_fp8
+    const float* w13_scale; // [E * R] with in_fp8 (W13 then holds e4m3 codes)
     const void* W13;
     const void* W2;
     void* h;

@@ -61,6 +61,13 @@ inline int out_dtype(const moe_config* c) {
     return (bf16_experts(c) && c->precision != MOE_PRECISION_BF16) ? MOE_F32 : c->act_dtype;
 }
 
+// The FP8 wire formats: block-scaled rows turned back into bf16, or row-scaled rows for the FP8 GEMM.
+inline bool fp8_blocks(const moe_config* c) { return c->dispatch_dtype == MOE_DISPATCH_FP8; }
+inline bool fp8_gemm(const moe_config* c) { return c->dispatch_dtype == MOE_DISPATCH_FP8_GEMM; }
+
+// Rows of W13 per expert: gate and up rows for SwiGLU, W1's rows for ReLU.
+inline int64_t w13_rows(const moe_config* c) { return c->expert_kind == MOE_EXPERT_SWIGLU ? 2 * int64_t(c->F) : c->F; }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -90,9 +97,13 @@ int validate(const moe_config* c) {
         if (c->n_groups > 32) return MOE_ERR_UNSUPPORTED;
     }
     if (c->dedup && c->D > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
-    if (c->dispatch_dtype != MOE_DISPATCH_ACT && c->dispatch_dtype != MOE_DISPATCH_FP8) return MOE_ERR_ARG;
-    if (c->dispatch_dtype == MOE_DISPATCH_FP8 && (c->act_dtype != MOE_BF16 || c->dedup))
+    if (c->dispatch_dtype != MOE_DISPATCH_ACT && c->dispatch_dtype != MOE_DISPATCH_FP8 &&
+        c->dispatch_dtype != MOE_DISPATCH_FP8_GEMM)
+        return MOE_ERR_ARG;
+    if ((fp8_blocks(c) || fp8_gemm(c)) && (c->act_dtype != MOE_BF16 || c->dedup)) return MOE_ERR_UNSUPPORTED;
+    if (fp8_gemm(c) && (c->expert_kind == MOE_EXPERT_IDENTITY || c->precision == MOE_PRECISION_SPLIT_H))
         return MOE_ERR_UNSUPPORTED;
+    if (fp8_gemm(c) && c->d % 16 != 0) return MOE_ERR_ALIGN;  // e4m3 rows of d bytes, 16-byte aligned
     if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX) || rows_cap(c) > int64_t(INT32_MAX))
         return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
@@ -163,9 +174,10 @@ Layout layout(const moe_config* c) {
     L.send_pos = take(dd ? sizeof(int32_t) * TD : 0);
     L.send_src = take(dd ? sizeof(int32_t) * TD : 0);
     L.xsend = take(dd ? b * TD * size_t(c->d) : 0);
-    const bool f8 = c->dispatch_dtype == MOE_DISPATCH_FP8;
-    L.xq = take(f8 ? R * size_t(c->d) : 0);
-    L.xscale = take(f8 ? sizeof(float) * R * size_t((c->d + 127) / 128) : 0);
+    L.xq = take(fp8_blocks(c) || fp8_gemm(c) ? R * size_t(c->d) : 0);
+    L.xscale = take(fp8_blocks(c)  ? sizeof(float) * R * size_t((c->d + 127) / 128)
+                    : fp8_gemm(c) ? sizeof(float) * R
+                                  : 0);
     L.forward_end = o;
     L.x_stage = take(b * size_t(c->T) * c->d);
     L.y_stage = take(b * size_t(c->T) * c->d);
@@ -200,7 +212,7 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->send.send_pos = dd ? at<int32_t>(ws, L.send_pos) : nullptr;
     v->send.send_src = dd ? at<int32_t>(ws, L.send_src) : nullptr;
     v->xsend = dd ? at<void>(ws, L.xsend) : nullptr;
-    const bool f8 = c->dispatch_dtype == MOE_DISPATCH_FP8;
+    const bool f8 = fp8_blocks(c) || fp8_gemm(c);
     v->xq = f8 ? at<uint8_t>(ws, L.xq) : nullptr;
     v->xscale = f8 ? at<float>(ws, L.xscale) : nullptr;
 }
@@ -287,15 +299,30 @@ int run_fp8(const moe_config* c, const void* x, const int32_t* idx, const moe_di
     a.xq = xq;
     a.xscale = xscale;
     a.xperm = xperm;
-    a.dequant = xperm != nullptr;
+    a.per_row = fp8_gemm(c);
+    a.dequant = xperm != nullptr && !a.per_row;
     a.status = at<int32_t>(ws, L.status);
     const cudaError_t e = launch_fp8_dispatch(a, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch_fp8");
 }
 
+// Byte offset of the weight scales inside an FP8 W13 buffer (after the codes).
+inline size_t fp8_weight_scale_offset(const moe_config* c) {
+    return align_up(size_t(n_experts(c)) * size_t(w13_rows(c)) * size_t(c->d));
+}
+
+// xscale: the rows' scales when cfg is MOE_DISPATCH_FP8_GEMM (xperm then holds their
+// e4m3 codes and W13 the FP8 weight buffer).
 int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const int32_t* counts, const void* W13,
-            const void* W2, void* h, void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid) {
+            const void* W2, void* h, void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid,
+            const float* xscale = nullptr) {
     FfnArgs a{};
+    if (fp8_gemm(c)) {
+        a.in_fp8 = true;
+        a.xscale = xscale;
+        a.w13_scale = reinterpret_cast<const float*>(static_cast<const unsigned char*>(W13) +
+                                                     fp8_weight_scale_offset(c));
+    }
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.F = c->F;
     a.rows = rows_cap(c);
     a.capacity = c->capacity;
@@ -355,10 +382,12 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
-    const bool f8 = c->dispatch_dtype == MOE_DISPATCH_FP8;
+    const bool f8 = fp8_blocks(c) || fp8_gemm(c);
     if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0 || f8)) != MOE_OK)
         return rc;
-    if (f8 && (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, v.xperm, ws, s)) != MOE_OK) return rc;
+    if (f8 && (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, fp8_gemm(c) ? nullptr : v.xperm, ws, s)) !=
+                  MOE_OK)
+        return rc;
     if (c->dedup && (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
@@ -367,7 +396,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
         // Padded layout: the GEMMs skip each segment's padding rows (only kept rows are
         // ever combined), so those rows of `out` are left unwritten by the forward.
         const int32_t* used = c->layout == MOE_LAYOUT_PADDED ? v.map.counts_kept : nullptr;
-        if ((rc = run_ffn(c, v.xperm, v.map.offsets, used, W13, W2, v.h, v.out, v.status, s, mid)) != MOE_OK)
+        const void* rows = fp8_gemm(c) ? static_cast<const void*>(v.xq) : v.xperm;
+        if ((rc = run_ffn(c, rows, v.map.offsets, used, W13, W2, v.h, v.out, v.status, s, mid, v.xscale)) != MOE_OK)
             return rc;
     } else if ((rc = record(events, n_events, 3, s)) != MOE_OK) {
         return rc;
@@ -429,7 +459,7 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
-    const int fp8 = cfg->dispatch_dtype == MOE_DISPATCH_FP8 ? 1 : 0;  // dequant (the gather quantizes)
+    const int fp8 = fp8_blocks(cfg) ? 1 : 0;  // dequant (the gather quantizes; FP8_GEMM rows are used as they are)
     const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : 2;  // fused, or logits + top-k
     return route + 4 + select + pad + dedup + fp8 + ffn + 1;
 }
@@ -491,7 +521,8 @@ int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_i
                      uint8_t* xq, float* xscale, void* xperm, void* ws, size_t ws_bytes, moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
-    if (cfg->dispatch_dtype != MOE_DISPATCH_FP8) return MOE_ERR_ARG;
+    if (!fp8_blocks(cfg) && !fp8_gemm(cfg)) return MOE_ERR_ARG;
+    if (fp8_gemm(cfg) && xperm) return MOE_ERR_ARG;
     const bool rows = rows_cap(cfg) > 0;
     if (!x || !topk_idx || !map || !map->pos || !map->row_src || !map->offsets || !ws || (rows && (!xq || !xscale)))
         return MOE_ERR_ARG;
@@ -508,7 +539,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
                    void* h, void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
-    if (cfg->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_ARG;
+    if (cfg->expert_kind == MOE_EXPERT_IDENTITY || fp8_gemm(cfg)) return MOE_ERR_ARG;
     if (!offsets || !W13 || !W2 || !ws) return MOE_ERR_ARG;
     if ((!xperm || !h || !out) && rows_cap(cfg) > 0) return MOE_ERR_ARG;
     if (!aligned16(xperm) || !aligned16(W13) || !aligned16(W2) || !aligned16(h) || !aligned16(out) ||
@@ -519,6 +550,41 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
     const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     return run_ffn(cfg, xperm, offsets, nullptr, W13, W2, h, out, status, stream, nullptr);
+}
+
+size_t moe_fp8_weight_bytes(const moe_config* cfg) {
+    if (validate(cfg) != MOE_OK || !fp8_gemm(cfg)) return 0;
+    return fp8_weight_scale_offset(cfg) + sizeof(float) * size_t(n_experts(cfg)) * size_t(w13_rows(cfg));
+}
+
+int moe_quantize_weights_fp8(const moe_config* cfg, const void* W13, void* W13_fp8, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!fp8_gemm(cfg) || !W13 || !W13_fp8) return MOE_ERR_ARG;
+    if (!aligned16(W13) || !aligned16(W13_fp8)) return MOE_ERR_ALIGN;
+    unsigned char* q = static_cast<unsigned char*>(W13_fp8);
+    const cudaError_t e = launch_quantize_rows_fp8(W13, int64_t(n_experts(cfg)) * w13_rows(cfg), cfg->d, q,
+                                                   reinterpret_cast<float*>(q + fp8_weight_scale_offset(cfg)),
+                                                   stream);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_quantize_weights_fp8");
+}
+
+int moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* xscale, const int32_t* offsets,
+                       const void* W13_fp8, const void* W2, void* h, void* out, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!fp8_gemm(cfg)) return MOE_ERR_ARG;
+    if (!offsets || !W13_fp8 || !W2 || !ws) return MOE_ERR_ARG;
+    if ((!xq || !xscale || !h || !out) && rows_cap(cfg) > 0) return MOE_ERR_ARG;
+    if (!aligned16(xq) || !aligned4(xscale) || !aligned16(W13_fp8) || !aligned16(W2) || !aligned16(h) ||
+        !aligned16(out) || !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+    int32_t* status = static_cast<int32_t*>(ws);
+    const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_ffn(cfg, xq, offsets, nullptr, W13_fp8, W2, h, out, status, stream, nullptr, xscale);
 }
 
 int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, const int32_t* pos, void* y,
@@ -600,6 +666,7 @@ const char* moe_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 const char* moe_ffn_kernel_name(const moe_config* cfg) {
     if (validate(cfg) != MOE_OK || cfg->expert_kind == MOE_EXPERT_IDENTITY) return "";
     if (cfg->act_dtype == MOE_F32) return "grouped_sgemm_kernel";
+    if (fp8_gemm(cfg)) return "grouped_gemm_swap_kernel<e4m3>";
     switch (ffn_tc_variant(rows_cap(cfg), n_experts(cfg), cfg->capacity)) {
         case 1: return "grouped_gemm_kernel<pair>";
         case 2: return "grouped_gemm_swap_kernel";

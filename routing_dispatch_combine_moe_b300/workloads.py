@@ -59,7 +59,8 @@ class Workload:
     n_groups: int = 0           # expert groups for group-limited routing (with topk_groups)
     topk_groups: int = 0        # 0 < M < n_groups: each token keeps experts of at most M groups
     dedup: bool = False         # send each token once per virtual rank, then fan out
-    dispatch_dtype: str = "act"  # "fp8": routed rows travel as e4m3 with per-128 block scales
+    dispatch_dtype: str = "act"  # "fp8": routed rows travel as e4m3 with per-128 block scales;
+    # "fp8_gemm": every row as row-scaled e4m3, fed to an FP8 up projection (e4m3 W13)
     note: str = field(default="", compare=False)
 
     @property
@@ -114,12 +115,17 @@ WORKLOADS: dict[str, Workload] = {
                  dispatch_dtype="fp8",
                  note="the Mixtral-shaped layer with its dispatched rows sent as e4m3 codes and "
                       "per-128 power-of-two scales"),
+            Workload("mixtral_fp8_gemm", T=2048, d=4096, E=8, k=2, F=14336, act="bf16", expert="swiglu",
+                 dispatch_dtype="fp8_gemm",
+                 note="the Mixtral-shaped layer with its dispatched rows as row-scaled e4m3 codes fed as "
+                      "they are to an FP8 up projection (e4m3 W13, one scale per output channel); h and the "
+                      "down projection stay bf16"),
     ]
 }
 
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
-                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch"]
+                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

@@ -91,6 +91,9 @@ class StageBuffers:
         if w.dispatch_dtype == "fp8":
             self.xq = torch.full((R, w.d), 0xAB, dtype=torch.uint8, device=device)
             self.xscale = torch.full((R, (w.d + 127) // 128), float("nan"), dtype=torch.float32, device=device)
+        if w.dispatch_dtype == "fp8_gemm":
+            self.xq = torch.full((R, w.d), 0xAB, dtype=torch.uint8, device=device)
+            self.xscale = torch.full((R,), float("nan"), dtype=torch.float32, device=device)
         if w.dedup:
             TD = w.T * w.D
             self.send_counts = torch.full((w.D,), -7, **i32)
@@ -116,10 +119,14 @@ class StageBuffers:
         abi.moe_dispatch(self.cfg, inp["x"], self.topk_idx if topk_idx is None else topk_idx, self.dmap(),
                          self.xperm, self.ws_dispatch, topk_gate=self.topk_gate if topk_gate is None else topk_gate)
 
-    def ffn(self, inp, xperm=None, offsets=None):
-        abi.moe_expert_ffn(self.cfg, self.xperm if xperm is None else xperm,
-                           self.offsets if offsets is None else offsets, inp["W13"], inp["W2"], self.h, self.out,
-                           self.ws_ffn)
+    def ffn(self, inp, xperm=None, offsets=None, xq=None, xscale=None):
+        offsets = self.offsets if offsets is None else offsets
+        if self.cfg.dispatch_dtype == abi.MOE_DISPATCH_FP8_GEMM:
+            abi.moe_expert_ffn_fp8(self.cfg, self.xq if xq is None else xq, self.xscale if xscale is None else xscale,
+                                   offsets, api_w13(self.cfg, inp), inp["W2"], self.h, self.out, self.ws_ffn)
+            return
+        abi.moe_expert_ffn(self.cfg, self.xperm if xperm is None else xperm, offsets, inp["W13"], inp["W2"],
+                           self.h, self.out, self.ws_ffn)
 
     def combine(self, out=None, topk_gate=None, pos=None):
         abi.moe_combine(self.cfg, self.out if out is None else out, self.topk_gate if topk_gate is None else topk_gate,
@@ -130,6 +137,38 @@ class StageBuffers:
 
     def ffn_status(self) -> int:
         return abi.moe_read_status(self.ws_ffn.data_ptr())
+
+
+def api_w13(cfg, inp):
+    """The W13 the library takes for this config: the bf16 weights, or (FP8 GEMM) their
+    FP8 buffer, quantized once on the device by the library and kept in ``inp``."""
+    if cfg.dispatch_dtype != abi.MOE_DISPATCH_FP8_GEMM or inp.get("W13") is None:
+        return inp.get("W13")
+    if "W13_fp8" not in inp:
+        inp["W13_fp8"] = abi.fp8_weights(cfg, inp["W13"])
+    return inp["W13_fp8"]
+
+
+def check_fp8_weights(w, cfg, inp, experts) -> None:
+    """The library's FP8 weight buffer: codes and per-row scales of the given experts
+    bit-exact against the oracle's row-wise quantization of W13."""
+    codes, scales = abi.fp8_weight_parts(cfg, api_w13(cfg, inp), w.n_experts, w.w13_rows, w.d)
+    for e in experts:
+        q = orc.quantize_fp8_rows(f64(inp["W13"][e]))
+        np.testing.assert_array_equal(cpu(codes[e]).numpy(), q["codes"])
+        np.testing.assert_array_equal(cpu(scales[e]).numpy().astype(np.float64), q["scales"])
+
+
+def compare_fp8_rows(w, xq, xscale, row_src, x, rows=None) -> int:
+    """FP8-GEMM dispatch: the codes and row scale of every kept row (or of ``rows``)
+    bit-exact against the oracle's row-wise quantization of its token's row."""
+    rs = np.asarray(row_src)
+    held = np.nonzero(rs >= 0)[0] if rows is None else np.asarray(rows)
+    tok = rs[held] // w.slots
+    q = orc.quantize_fp8_rows(f64(x[torch.from_numpy(tok).to(x.device)]))
+    np.testing.assert_array_equal(cpu(xq).numpy()[held], q["codes"])
+    np.testing.assert_array_equal(cpu(xscale).numpy().astype(np.float64)[held], q["scales"])
+    return int(held.size)
 
 
 def cpu(t):
@@ -280,7 +319,13 @@ def check_fp8(w, inp, bufs, st, d) -> dict:
     """FP8 dispatch of the synthetic ids' dispatch map ``d``: every routed row's e4m3
     codes and block scales bit-exact against the oracle's quantization of its token,
     the receiving side's bf16 rows equal to the oracle's dequantized values, shared
-    experts' rows equal to x."""
+    experts' rows equal to x. FP8 GEMM format: every kept row's codes and row scale."""
+    if w.dispatch_dtype == "fp8_gemm":
+        abi.moe_dispatch_fp8(bufs.cfg, inp["x"], st["topk_idx"], bufs.dmap(), bufs.xq, bufs.xscale, None,
+                             bufs.ws_dispatch)
+        torch.cuda.synchronize()
+        assert bufs.dispatch_status() == 0
+        return dict(rows=compare_fp8_rows(w, bufs.xq, bufs.xscale, d["row_src"], inp["x"]))
     rows_out = torch.full_like(bufs.xperm, float("nan"))
     abi.moe_dispatch_fp8(bufs.cfg, inp["x"], st["topk_idx"], bufs.dmap(), bufs.xq, bufs.xscale, rows_out,
                          bufs.ws_dispatch)
@@ -307,17 +352,30 @@ def check_ffn(w, inp, bufs, st, expert_subset=None) -> float:
     expert's output rows against the oracle's expert on the same rows."""
     counts = st["counts"].numpy()
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-    xperm = torch.zeros(bufs.rows, w.d, dtype=w.torch_act, device="cuda")
-    xperm[:offs[-1]] = st["xperm"]
-    bufs.ffn(inp, xperm=xperm, offsets=torch.from_numpy(offs).cuda())
-    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
+    fp8 = w.dispatch_dtype == "fp8_gemm"
+    rows_in = f64(st["xperm"])
+    if fp8:  # the FP8 GEMM's input rows: the oracle's row-wise quantization of the synthetic rows
+        q = orc.quantize_fp8_rows(rows_in)
+        rows_in = q["deq"]
+        xq = torch.zeros(bufs.rows, w.d, dtype=torch.uint8, device="cuda")
+        xq[:offs[-1]] = torch.from_numpy(q["codes"]).cuda()
+        xs = torch.zeros(bufs.rows, dtype=torch.float32, device="cuda")
+        xs[:offs[-1]] = torch.from_numpy(q["scales"]).float().cuda()
+        bufs.ffn(inp, offsets=torch.from_numpy(offs).cuda(), xq=xq, xscale=xs)
+    else:
+        xperm = torch.zeros(bufs.rows, w.d, dtype=w.torch_act, device="cuda")
+        xperm[:offs[-1]] = st["xperm"]
+        bufs.ffn(inp, xperm=xperm, offsets=torch.from_numpy(offs).cuda())
+    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8)
     experts = range(w.n_experts) if expert_subset is None else expert_subset
+    if fp8:
+        check_fp8_weights(w, bufs.cfg, inp, [e for e in experts if counts[e] > 0][:3])
     worst = 0.0
     for e in experts:
         lo, hi = int(offs[e]), int(offs[e + 1])
         if hi == lo:
             continue
-        exact = fn(e, f64(st["xperm"][lo:hi]))
+        exact = fn(e, rows_in[lo:hi])
         worst = max(worst, check_close(bufs.out[lo:hi], exact, bufs.out_act, f"expert {e} output",
                                        tol=TOL[w.act]))
     return worst
@@ -375,6 +433,13 @@ def check_chained_dispatch(w, inp, m, r, capacity, xperm=None) -> str:
         exact = not gate_boundary_ties(w, r["idx"], r["G"], capacity).any()
     if exact:
         d = oracle_dispatch(w, r["idx_full"], r["G_full"], capacity)
+        if w.dispatch_dtype == "fp8_gemm":  # rows travel only as codes + row scales
+            compare_dispatch(w, m, d)
+            if xperm is None:
+                sample = np.nonzero(d["row_src"] >= 0)[0]
+                sample = np.random.default_rng(2).choice(sample, size=min(256, sample.size), replace=False)
+                compare_fp8_rows(w, m.xq, m.xscale, d["row_src"], inp["x"], rows=sample)
+            return "exact"
         fp8_rows = None
         if w.dispatch_dtype == "fp8":  # rows holding a routed assignment travel as FP8
             rs = d["row_src"]
@@ -411,10 +476,12 @@ class WorkspaceMap:
         self.out = None if not view.out else \
             ws[view.out - base:view.out - base + R * w.d * osz].view(odt).view(R, w.d)
         self.out_act = "f32" if odt == torch.float32 else "bf16"
-        if w.dispatch_dtype == "fp8":
-            nb = (w.d + 127) // 128
+        if w.dispatch_dtype in ("fp8", "fp8_gemm"):
+            nb = (w.d + 127) // 128 if w.dispatch_dtype == "fp8" else 1
             self.xq = ws[view.xq - base:view.xq - base + R * w.d].view(R, w.d)
             self.xscale = ws[view.xscale - base:view.xscale - base + 4 * R * nb].view(torch.float32).view(R, nb)
+            if w.dispatch_dtype == "fp8_gemm":
+                self.xscale = self.xscale.view(R)
         if w.dedup:
             TD = w.T * w.D
             self.send_counts = i32(view.send_counts, w.D)
@@ -431,6 +498,8 @@ def chain(w, inp, cfg) -> StageBuffers:
     b.dispatch(inp)
     if w.dispatch_dtype == "fp8":  # the routed rows travel as FP8 and come back as bf16
         abi.moe_dispatch_fp8(cfg, inp["x"], b.topk_idx, b.dmap(), b.xq, b.xscale, b.xperm, b.ws_dispatch)
+    if w.dispatch_dtype == "fp8_gemm":  # every row travels as row-scaled FP8, read by the FP8 GEMM as it is
+        abi.moe_dispatch_fp8(cfg, inp["x"], b.topk_idx, b.dmap(), b.xq, b.xscale, None, b.ws_dispatch)
     if w.expert != "identity":
         b.ffn(inp)
         b.combine()
@@ -443,7 +512,7 @@ def chain(w, inp, cfg) -> StageBuffers:
 def run_layer(cfg, inp, w, device="cuda"):
     ws = abi.workspace(cfg, device)
     y = torch.full((w.T, w.d), float("nan"), dtype=w.torch_act, device=device)
-    abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), inp.get("W13"), inp.get("W2"), y, ws)
+    abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), api_w13(cfg, inp), inp.get("W2"), y, ws)
     view = abi.moe_workspace_get_view(cfg, ws)
     flags = abi.moe_read_status(view.status)
     return y, ws, view, flags

@@ -298,3 +298,49 @@ def test_fp8_dispatch_validation_and_workspace():
     assert abi.lib().moe_dispatch_fp8(ctypes.byref(cfg()), 1 << 20, 1 << 20, ctypes.byref(m), 1 << 20, 1 << 20,
                                       None, 1 << 20, 1 << 20, None) == abi.MOE_ERR_ARG   # not an fp8 config
 
+
+
+def test_fp8_gemm_validation_workspace_and_weight_bytes():
+    g = cfg(dispatch_dtype="fp8_gemm")
+    assert abi.moe_validate_config(g) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(dispatch_dtype="fp8_gemm", expert="relu")) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(act="f32", dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(D=4, dedup=True, dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(F=0, expert="identity", dispatch_dtype="fp8_gemm")) == \
+        abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(precision="split_h", dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(d=136, dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_ALIGN  # 136-byte code rows
+    assert abi.moe_validate_config(cfg(d=136)) == abi.MOE_OK
+    # the quantizing gather replaces the plain one: same kernel count as the bf16 layer
+    assert abi.moe_kernels_per_forward(g) == abi.moe_kernels_per_forward(cfg())
+    v = abi.moe_workspace_view()
+    base = 1 << 40
+    n = abi.moe_workspace_bytes(g)
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(g), base, n, ctypes.byref(v)) == 0
+    rows = 64 * 2
+    assert v.xq and v.xscale and v.xscale - v.xq >= rows * 128 and base + n - v.xscale >= rows * 4
+    # weight buffer: N*R*d codes, the next 256-byte boundary, N*R fp32 scales
+    codes = 8 * 128 * 128
+    assert abi.moe_fp8_weight_bytes(g) == (codes + 255) // 256 * 256 + 4 * 8 * 128
+    relu = cfg(dispatch_dtype="fp8_gemm", expert="relu", F=80)
+    assert abi.moe_fp8_weight_bytes(relu) == (8 * 80 * 128 + 255) // 256 * 256 + 4 * 8 * 80
+    assert abi.moe_fp8_weight_bytes(cfg()) == 0 and abi.moe_fp8_weight_bytes(cfg(dispatch_dtype="fp8")) == 0
+    assert abi.moe_ffn_kernel_name(g) == "grouped_gemm_swap_kernel<e4m3>"
+    lib = abi.lib()
+    # the bf16 FFN entry refuses an fp8_gemm config, the FP8 entry any other config
+    assert lib.moe_expert_ffn(ctypes.byref(g), A16, A16, A16, A16, A16, A16, A16, 1 << 20, None) == abi.MOE_ERR_ARG
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(cfg()), A16, A16, A16, A16, A16, A16, A16, A16, 1 << 20,
+                                  None) == abi.MOE_ERR_ARG
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(g), None, A16, A16, A16, A16, A16, A16, A16, 1 << 20,
+                                  None) == abi.MOE_ERR_ARG
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(g), MIS, A16, A16, A16, A16, A16, A16, A16, 1 << 20,
+                                  None) == abi.MOE_ERR_ALIGN
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(g), A16, A16, A16, A16, A16, A16, A16, A16, 16,
+                                  None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_quantize_weights_fp8(ctypes.byref(cfg()), A16, A16, None) == abi.MOE_ERR_ARG
+    assert lib.moe_quantize_weights_fp8(ctypes.byref(g), A16, MIS, None) == abi.MOE_ERR_ALIGN
+    m = abi.dispatch_map(*([None] * 8))
+    m.pos = m.row_src = m.offsets = A16
+    # the row-scaled format feeds the FP8 GEMM directly: no bf16 rows to write
+    assert lib.moe_dispatch_fp8(ctypes.byref(g), A16, A16, ctypes.byref(m), A16, A16, A16, A16, 1 << 20,
+                                None) == abi.MOE_ERR_ARG

@@ -39,6 +39,11 @@ REDUCED = {
                                         capacity_factor="1"),
     "mixtral_fp8": wl.scaled(W["mixtral_fp8_dispatch"], T=512, d=1024, F=1536),
     "decode_fp8": wl.scaled(W["dsv3_decode"], d=1088, F=256, dispatch_dtype="fp8"),  # ragged last block
+    "mixtral_fp8_gemm": wl.scaled(W["mixtral_fp8_gemm"], T=512, d=1024, F=1536),
+    # shared expert, 8 virtual ranks, d not a multiple of 128 (a partial last K block)
+    "decode_fp8_gemm": wl.scaled(W["dsv3_decode"], d=1072, F=256, dispatch_dtype="fp8_gemm"),
+    "relu_fp8_gemm": wl.Workload("relu_fp8_gemm", T=300, d=512, E=6, k=2, F=448, act="bf16", expert="relu",
+                                 dispatch_dtype="fp8_gemm"),
 }
 
 
@@ -54,7 +59,7 @@ def stagewise(w, seed=0, inp=None):
     d = check_dispatch(w, inp, b, cap, st)
     assert b.dispatch_status() == 0
     dd = check_dedup(w, inp, b, st, d) if w.dedup else None
-    f8 = check_fp8(w, inp, b, st, d) if w.dispatch_dtype == "fp8" else None
+    f8 = check_fp8(w, inp, b, st, d) if w.dispatch_dtype in ("fp8", "fp8_gemm") else None
     ffn_err = None
     if w.expert != "identity":
         ffn_err = check_ffn(w, inp, b, st)
@@ -204,7 +209,7 @@ def test_split_h_mode_is_limited_by_the_output_rounding(name):
     print(f"\n{name} split_h: raw max|err|/rms(y) = {err:.4f}")
 
 
-@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_full"])
+@pytest.mark.parametrize("name", ["mixtral_bf16", "dsv3_full", "mixtral_fp8_gemm"])
 def test_bf16_mode_within_its_rounding_budget(name):
     """All-bf16 mode: the expert outputs are rounded to bf16 too, so the bound adds
     their half-ulp, weighted by the gates, to the f32-output bound. (Dropless layers
@@ -283,8 +288,11 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
     with the FP8 dispatch routed experts see the dequantized rows."""
     x = f64(inp["x"][torch.as_tensor(tokens, device="cuda")])
     xq = orc.quantize_fp8_blocks(x)["deq"] if w.dispatch_dtype == "fp8" else x
+    fp8_gemm = w.dispatch_dtype == "fp8_gemm"
+    if fp8_gemm:  # every row, shared ones too, is the row-quantized token
+        x = xq = orc.quantize_fp8_rows(x)["deq"]
     idx, G, pos = ref_route["idx"], ref_route["G"], disp["pos"].reshape(w.T, w.slots)
-    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
+    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm)
     need = {}
     for r, t in enumerate(tokens):
         for j in range(w.slots):
@@ -303,6 +311,7 @@ FULL = {n: W[n] for n in ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3
 FULL["zipf_gate_padded"] = wl.scaled(W["zipf_cf125"], drop_policy="gate", layout="padded")
 FULL["dsv3_grouped_dedup"] = W["dsv3_grouped_dedup"]
 FULL["mixtral_fp8_dispatch"] = W["mixtral_fp8_dispatch"]
+FULL["mixtral_fp8_gemm"] = W["mixtral_fp8_gemm"]
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -348,7 +357,8 @@ def test_full_size_sampled(name):
         nz = np.nonzero(counts)[0]
         pick = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(nz[len(nz) // 2]),
                        int(nz[0])})
-        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F)
+        fp8_gemm = w.dispatch_dtype == "fp8_gemm"
+        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm)
         worst_ffn = 0.0
         for e in pick:
             lo = int(d["offsets"][e])
@@ -357,6 +367,8 @@ def test_full_size_sampled(name):
             xin = f64(inp["x"][src])
             if fp8 and e < w.E:
                 xin = orc.quantize_fp8_blocks(xin)["deq"]
+            if fp8_gemm:
+                xin = orc.quantize_fp8_rows(xin)["deq"]
             worst_ffn = max(worst_ffn, check_close(m.out[lo:hi], fn(e, xin), m.out_act, f"expert {e}", tol=2e-2))
     # end to end on sampled tokens from the oracle's own routing and dispatch: no near
     # tie, no gate at a keep cutoff, and (with a capacity) no expert shared with a

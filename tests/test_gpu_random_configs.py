@@ -2,7 +2,8 @@
 
 Each case draws a shape (T, d, E, k, F, D), an expert kind and activation dtype, an
 optional capacity with either drop policy and layout, an optional group limit, shared
-experts, the deduplicated or the FP8 dispatch, from a fixed seed. The stage checks
+experts, the deduplicated or the FP8 dispatch, from a fixed seed; a second set draws
+FP8-GEMM layers (row-scaled e4m3 rows and up weights). The stage checks
 (route, dispatch, dedup / FP8, expert FFN, combine) and the end-to-end comparison with
 the oracle are the same as for the named workloads."""
 import numpy as np
@@ -57,6 +58,21 @@ def draw(seed: int) -> wl.Workload:
 
 
 CASES = [draw(i) for i in range(40)]
+
+
+def draw_fp8_gemm(seed: int) -> wl.Workload:
+    """A layer with the FP8 up projection: bf16, ReLU or SwiGLU, d a multiple of 16."""
+    w = draw(500 + seed)
+    r = np.random.default_rng(5000 + seed)
+    d = int(r.choice([64, 128, 144, 256, 528]))
+    expert = str(r.choice(["swiglu", "relu"]))
+    F = int(r.choice([64, 96, 128, 200, 256]))
+    # f32 expert outputs, as in draw(): the all-bf16 mode has its own budget (test_gpu_parity)
+    return wl.scaled(w, name=f"rand_fp8_gemm{seed}", act="bf16", d=d, expert=expert, F=F, dedup=False,
+                     dispatch_dtype="fp8_gemm", precision="f32_out")
+
+
+CASES += [draw_fp8_gemm(i) for i in range(12)]
 
 
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
