@@ -112,7 +112,7 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
                               channel (moe_quantize_weights_fp8); h, W2 and the down projection stay
                               bf16. One scale per row, not per 128-element block, so that the GEMM can
                               apply it after the K loop. bf16 activations, ReLU or SwiGLU experts,
-                              d % 16 == 0, no dedup, not MOE_PRECISION_SPLIT_H */
+                              d % 16 == 0, no dedup */
 
 /* Limits of this build. */
 #define MOE_MAX_K 16        /* experts per token, routed plus shared */
@@ -329,7 +329,8 @@ int moe_quantize_weights_fp8(const moe_config* cfg, const void* W13, void* W13_f
 /* moe_expert_ffn for a MOE_DISPATCH_FP8_GEMM config: the up projection runs on the
  * e4m3 rows and weights (tcgen05 kind::f8f6f4 on SM pairs), its fp32 accumulator
  * multiplied by the row scale and the weight row's scale before the activation; h is
- * rounded once to bf16 and the down projection is the bf16 one.
+ * stored as for moe_expert_ffn (bf16, or a hi/lo pair under MOE_PRECISION_SPLIT_H) and
+ * the down projection is the bf16 one.
  *   xq      [rows, d] uint8 e4m3 codes;  xscale [rows] fp32 row scales (moe_dispatch_fp8)
  *   W13_fp8 moe_quantize_weights_fp8's buffer;  W2 [N, d, F] bf16
  *   offsets, h, out, ws as in moe_expert_ffn. */

@@ -1008,14 +1008,18 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.b_k_shift = 0;
     p.R = R;
     if (a.in_fp8) {
-        // e4m3 rows and weights (split_h is excluded for them): always the swapped pairs
+        // e4m3 rows and weights: always the swapped pairs
         p.xscale = a.xscale;
         p.wscale = a.w13_scale;
         if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128, true)) != cudaSuccess) return err;
         if ((err = make_row_maps(&mX, a.xperm, a.d, rows_max, true)) != cudaSuccess) return err;
         p.n_tiles = swiglu ? (a.F + 127) / 128 : (a.F + 255) / 256;
-        err = swiglu ? launch_swap<kSwiGLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream)
-                     : launch_swap<kReLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream);
+        if (swiglu)
+            err = split_h ? launch_swap<kSwiGLU, kOutHiLo, true>(mA, mX, p, rows_max, a.E, stream)
+                          : launch_swap<kSwiGLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream);
+        else
+            err = split_h ? launch_swap<kReLU, kOutHiLo, true>(mA, mX, p, rows_max, a.E, stream)
+                          : launch_swap<kReLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream);
         p.xscale = p.wscale = nullptr;
     } else if (swap) {
         // weights as the MMA's A operand: 64-row boxes (gate | up halves) or 128-row boxes

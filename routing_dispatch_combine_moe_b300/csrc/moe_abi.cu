@@ -101,8 +101,7 @@ int validate(const moe_config* c) {
         c->dispatch_dtype != MOE_DISPATCH_FP8_GEMM)
         return MOE_ERR_ARG;
     if ((fp8_blocks(c) || fp8_gemm(c)) && (c->act_dtype != MOE_BF16 || c->dedup)) return MOE_ERR_UNSUPPORTED;
-    if (fp8_gemm(c) && (c->expert_kind == MOE_EXPERT_IDENTITY || c->precision == MOE_PRECISION_SPLIT_H))
-        return MOE_ERR_UNSUPPORTED;
+    if (fp8_gemm(c) && c->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_UNSUPPORTED;
     if (fp8_gemm(c) && c->d % 16 != 0) return MOE_ERR_ALIGN;  // e4m3 rows of d bytes, 16-byte aligned
     if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX) || rows_cap(c) > int64_t(INT32_MAX))
         return MOE_ERR_UNSUPPORTED;

@@ -308,7 +308,7 @@ def test_fp8_gemm_validation_workspace_and_weight_bytes():
     assert abi.moe_validate_config(cfg(D=4, dedup=True, dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
     assert abi.moe_validate_config(cfg(F=0, expert="identity", dispatch_dtype="fp8_gemm")) == \
         abi.MOE_ERR_UNSUPPORTED
-    assert abi.moe_validate_config(cfg(precision="split_h", dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
+    assert abi.moe_validate_config(cfg(precision="split_h", dispatch_dtype="fp8_gemm")) == abi.MOE_OK
     assert abi.moe_validate_config(cfg(d=136, dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_ALIGN  # 136-byte code rows
     assert abi.moe_validate_config(cfg(d=136)) == abi.MOE_OK
     # the quantizing gather replaces the plain one: same kernel count as the bf16 layer
