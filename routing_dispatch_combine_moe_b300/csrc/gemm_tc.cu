@@ -475,7 +475,8 @@ struct RowMaps {
 };
 
 struct SwapXchg {
-    float v[2][32][33];  // up values for 32 rows x 32 features, per gate warp
+    float v[2][32][33];     // up values for 32 rows x 32 features, per gate warp
+    float sx[SW_TILE_N];    // e4m3 inputs: the scales of the tile's rows (0 past its end)
 };
 
 constexpr size_t swap_smem_bytes() {
@@ -514,16 +515,6 @@ __device__ __forceinline__ void swap_tile_rows(const int* off, const int* end, i
     start = off[e] + mt * width;
     len = min(width, end[e] - start);
     n = (len + 31) & ~31;
-}
-
-// e4m3 inputs: accumulator column j (row row0 + j) times the thread's weight-row scale
-// and that row's scale; lane j fetches row j's scale (0 past the n_valid rows).
-__device__ __forceinline__ void scale_columns(uint32_t (&v)[32], float wsc, const float* __restrict__ xscale,
-                                              int row0, int n_valid, int lane) {
-    const float sx = lane < n_valid ? __ldg(xscale + row0 + lane) : 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-        v[j] = __float_as_uint(__uint_as_float(v[j]) * (wsc * __shfl_sync(0xFFFFFFFFu, sx, j)));
 }
 
 template <int OUT>
@@ -714,7 +705,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
         }
     } else {
         // Epilogue: warps 2..5 own TMEM lane quarters q = warp % 4 (features of this SM).
+        // Each tile's columns go in chunks of 32: the TMEM load of the next chunk is in
+        // flight while the current one is processed, and the accumulator is handed back
+        // to the MMA warp as soon as its last chunk is in registers.
         const int q = warp & 3;
+        const int te = (warp - 2) * 32 + lane;  // 0..127 over the four epilogue warps
         const uint32_t empty_base = mapa_shared(smem_addr(&S.tmem_empty[0]), 0);
         int i = 0;
         for (int t = unit; t < total; t += n_units, ++i) {
@@ -723,29 +718,43 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
             swap_tile_rows(S.off, S.end, e, mt, start, len, n);
             const int acc = i & 1;
             const uint32_t aph = (i >> 1) & 1;
+            const int w = q & 1;
+            const bool gate_warp = q < 2;
+            // feature of this thread's TMEM lane, in [0, n_out) when it is stored
+            const int f = MODE == kSwiGLU ? nt * 128 + int(rank) * 64 + w * 32 + lane
+                                          : nt * 256 + int(rank) * 128 + q * 32 + lane;
+            float wsc = 1.f;
+            if constexpr (F8) {
+                // e4m3 inputs: the weight row's scale and the tile's row scales, read
+                // before the accumulator wait so that their latency hides behind it (the
+                // previous tile's last barrier has passed every read of X.sx)
+                if (f < p.n_out)
+                    wsc = __ldg(p.wscale + size_t(e) * p.R + (MODE == kSwiGLU && !gate_warp ? p.F : 0) + f);
+                X.sx[te] = te < len ? __ldg(p.xscale + start + te) : 0.f;
+                X.sx[te + 128] = te + 128 < len ? __ldg(p.xscale + start + te + 128) : 0.f;
+            }
             bool ok = mbar_wait(&S.tmem_full[acc], aph, abort_flag, p.status);
             ok = __all_sync(0xFFFFFFFFu, ok);
-            // All four epilogue warps must agree before the shared-memory hand-off below.
-            if (MODE == kSwiGLU) ok = epi_bar_and(ok);
+            // All four epilogue warps agree before the shared-memory hand-off (and the
+            // row scales) below.
+            if (MODE == kSwiGLU || F8) ok = epi_bar_and(ok);
             if (!ok) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + acc * SW_TILE_N;
-            if (MODE == kSwiGLU) {
-                // Warps q and q + 2 hold the gate and up values of the same 32 features;
-                // each hands the other half a chunk through shared memory, so both
-                // compute 16 of the chunk's 32 rows.
-                const int w = q & 1;
-                const bool gate_warp = q < 2;
-                const int f = nt * 128 + int(rank) * 64 + w * 32 + lane;  // feature in [0, F)
-                float wsc = 1.f;
-                if constexpr (F8)
-                    wsc = f < p.F ? __ldg(p.wscale + size_t(e) * p.R + (gate_warp ? 0 : p.F) + f) : 0.f;
-#pragma unroll 1
-                for (int c0 = 0; c0 < n; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c0, v);
-                    tmem_ld_wait();
-                    if constexpr (F8) scale_columns(v, wsc, p.xscale, start + c0, len - c0, lane);
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_base + uint32_t(acc) * 8u);
+            };
+            auto chunk = [&](int c0, uint32_t(&v)[32]) {
+                if constexpr (F8) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * (wsc * X.sx[c0 + j]));
+                }
+                if constexpr (MODE == kSwiGLU) {
+                    // Warps q and q + 2 hold the gate and up values of the same 32 features;
+                    // each hands the other half a chunk through shared memory, so both
+                    // compute 16 of the chunk's 32 rows.
                     if (gate_warp) {
 #pragma unroll
                         for (int j = 16; j < 32; ++j) X.v[w][j][lane] = __uint_as_float(v[j]);
@@ -765,32 +774,36 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                         if (c0 + j < len && f < p.n_out) store_one<OUT>(p, start + c0 + j, f, silu_f(g) * u);
                     }
                     epi_bar_sync();
-                }
-            } else {
-                const int f = nt * 256 + int(rank) * 128 + q * 32 + lane;
-                float wsc = 1.f;
-                if constexpr (F8) wsc = f < p.n_out ? __ldg(p.wscale + size_t(e) * p.R + f) : 0.f;
-#pragma unroll 1
-                for (int c0 = 0; c0 < n; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c0, v);
-                    tmem_ld_wait();
-                    if constexpr (F8) scale_columns(v, wsc, p.xscale, start + c0, len - c0, lane);
-                    if (f < p.n_out) {
+                } else if (f < p.n_out) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (c0 + j < len) {
-                                float x = __uint_as_float(v[j]);
-                                if (MODE == kReLU) x = fmaxf(x, 0.f);
-                                store_one<OUT>(p, start + c0 + j, f, x);
-                            }
+                    for (int j = 0; j < 32; ++j) {
+                        if (c0 + j < len) {
+                            float x = __uint_as_float(v[j]);
+                            if (MODE == kReLU) x = fmaxf(x, 0.f);
+                            store_one<OUT>(p, start + c0 + j, f, x);
                         }
                     }
                 }
+            };
+            uint32_t va[32], vb[32];
+            tmem_ld_32x32b_x32(tbase, va);
+            tmem_ld_wait();
+#pragma unroll 1
+            for (int c0 = 0; c0 < n; c0 += 64) {
+                const bool more1 = c0 + 32 < n;
+                if (more1) tmem_ld_32x32b_x32(tbase + c0 + 32, vb);
+                else release();
+                chunk(c0, va);
+                if (!more1) break;
+                tmem_ld_wait();
+                const bool more2 = c0 + 64 < n;
+                if (more2) tmem_ld_32x32b_x32(tbase + c0 + 64, va);
+                else release();
+                chunk(c0 + 32, vb);
+                if (more2) tmem_ld_wait();
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(empty_base + uint32_t(acc) * 8u);
+            // plain mode has no barrier inside the chunks: keep X.sx until every warp is done
+            if constexpr (F8 && MODE != kSwiGLU) epi_bar_sync();
         }
     }
 
