@@ -632,13 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 const CUtensorMap* mx = &mapX.m[(n >> 5) - 1];  // box of n / 2 rows
                 const int xrow = start + int(rank) * (n >> 1);
                 const uint32_t stage_tx = uint32_t(SW_A_STAGE + (n >> 1) * BK * 2);
-                int w0, w1 = 0;
-                if (MODE == kSwiGLU) {
-                    w0 = e * p.R + nt * 128 + int(rank) * 64;
-                    w1 = w0 + p.F;
-                } else {
-                    w0 = e * p.R + nt * 256 + int(rank) * 128;
-                }
+                // SwiGLU: feature row wf of the gate and up halves (a 3-D map over [2E, F, d]);
+                // otherwise row w0 of [E * R, d]
+                const int wf = nt * 128 + int(rank) * 64;
+                const int w0 = e * p.R + nt * 256 + int(rank) * 128;
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -649,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                     const uint32_t bar = full_base + uint32_t(s) * 8u;
                     if (leader) mbar_arrive_expect_tx(&S.full[s], 2 * stage_tx);
                     if (MODE == kSwiGLU) {
-                        tma_load_2d_pair(a_dst, &mapW, bar, kW, w0);
-                        tma_load_2d_pair(a_dst + SW_A_STAGE / 2, &mapW, bar, kW, w1);
+                        // one 3-D box: 64 gate rows of expert e, then the 64 matching up rows
+                        tma_load_3d_pair(a_dst, &mapW, bar, kW, wf, 2 * e);
                     } else {
                         tma_load_2d_pair(a_dst, &mapW, bar, kW, w0);
                     }
@@ -853,6 +850,23 @@ cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D map over SwiGLU weights [E, 2, F, inner] seen as [2E, F, inner]: box = 128 bytes x
+// 64 feature rows x both halves (gate, up) of one expert, 128-byte swizzle.
+cudaError_t make_gate_up_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t F, uint64_t E, bool u8) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const uint32_t esz = u8 ? 1 : 2;
+    const cuuint64_t dims[3] = {inner, F, 2 * E};
+    const cuuint64_t strides[2] = {inner * esz, F * inner * esz};
+    const cuuint32_t box[3] = {128u / esz, 64u, 2u};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_row_maps(RowMaps* maps, const void* base, uint64_t inner, uint64_t rows, bool u8 = false) {
     for (int i = 0; i < SW_ROW_MAPS; ++i) {
         const cudaError_t err = make_map(&maps->m[i], base, inner, rows, uint32_t(16 * (i + 1)), u8);
@@ -1024,7 +1038,9 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
         // e4m3 rows and weights: always the swapped pairs
         p.xscale = a.xscale;
         p.wscale = a.w13_scale;
-        if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128, true)) != cudaSuccess) return err;
+        err = swiglu ? make_gate_up_map(&mA, a.W13, a.d, a.F, a.E, true)
+                     : make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, 128, true);
+        if (err != cudaSuccess) return err;
         if ((err = make_row_maps(&mX, a.xperm, a.d, rows_max, true)) != cudaSuccess) return err;
         p.n_tiles = swiglu ? (a.F + 127) / 128 : (a.F + 255) / 256;
         if (swiglu)
@@ -1035,8 +1051,10 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
                           : launch_swap<kReLU, kOutBF16, true>(mA, mX, p, rows_max, a.E, stream);
         p.xscale = p.wscale = nullptr;
     } else if (swap) {
-        // weights as the MMA's A operand: 64-row boxes (gate | up halves) or 128-row boxes
-        if ((err = make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, swiglu ? 64 : 128)) != cudaSuccess) return err;
+        // weights as the MMA's A operand: a 3-D box of 64 gate + 64 up rows, or 128-row boxes
+        err = swiglu ? make_gate_up_map(&mA, a.W13, a.d, a.F, a.E, false)
+                     : make_map(&mA, a.W13, a.d, uint64_t(a.E) * R, 128);
+        if (err != cudaSuccess) return err;
         if ((err = make_row_maps(&mX, a.xperm, a.d, rows_max)) != cudaSuccess) return err;
         p.n_tiles = swiglu ? (a.F + 127) / 128 : (a.F + 255) / 256;
         if (swiglu)
