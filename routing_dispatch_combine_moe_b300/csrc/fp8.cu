@@ -19,7 +19,7 @@
 // row, so a row has one scale 2^s; every kept row of a token, routed or shared, gets the
 // codes, and the expert GEMM reads them as they are (the scale is applied to its fp32
 // accumulator). The expert weights take the same format, one scale per weight row.
-//   gather_fp8_row_kernel  one warp per token: amax over the row, then the codes to
+//   gather_fp8_row_kernel  one CTA per token: amax over the row, then the codes to
 //                          each kept row and the scale;
 //   quantize_rows_kernel   one warp per row of a bf16 matrix (the W13 weights).
 #include <cuda_fp8.h>
@@ -69,32 +69,42 @@ __device__ __forceinline__ int row_exponent(const uint4* __restrict__ src, int v
     return block_exponent(am);
 }
 
-__global__ void __launch_bounds__(256) gather_fp8_row_kernel(const uint4* __restrict__ x,
+// One CTA of 128 threads per token, so that a decode-sized batch still spreads over the
+// SMs: the row's amax is reduced over the CTA, then every thread converts its 16-byte
+// pieces and writes them to each kept row of the token.
+__global__ void __launch_bounds__(128) gather_fp8_row_kernel(const uint4* __restrict__ x,
                                                              const int32_t* __restrict__ pos, int T, int K, int d,
                                                              int64_t max_rows, uint8_t* __restrict__ xq,
                                                              float* __restrict__ xscale, int32_t* status) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= T) return;
+    __shared__ int dst[MOE_MAX_K];
+    __shared__ float am_w[4];
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vpr = d / 8;
-    int p = -1;
-    if (lane < K) {
-        const int r = pos[size_t(t) * K + lane];
-        if (r >= max_rows) set_status(status, MOE_DEV_ERR_INDEX);
-        else p = r;
+    if (tid < K) {
+        int r = pos[size_t(t) * K + tid];
+        if (r >= max_rows) {
+            set_status(status, MOE_DEV_ERR_INDEX);
+            r = -1;
+        }
+        dst[tid] = r < 0 ? -1 : r;
     }
-    int dst[MOE_MAX_K];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_K; ++j) dst[j] = __shfl_sync(0xFFFFFFFFu, p, j);
     const uint4* src = x + size_t(t) * vpr;
-    const int s = row_exponent(src, vpr, lane);
-    for (int v = lane; v < vpr; v += 32) {
-        const uint2 c = e4m3_pack8(__ldg(src + v), s);
+    float am = 0.f;
+    for (int v = tid; v < vpr; v += 128) am = fmaxf(am, absmax8(__ldg(src + v)));
 #pragma unroll
-        for (int j = 0; j < MOE_MAX_K; ++j)
-            if (j < K && dst[j] >= 0) *reinterpret_cast<uint2*>(xq + size_t(dst[j]) * d + size_t(v) * 8) = c;
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+    if (lane == 0) am_w[warp] = am;
+    __syncthreads();
+    const int s = block_exponent(fmaxf(fmaxf(am_w[0], am_w[1]), fmaxf(am_w[2], am_w[3])));
+    for (int v = tid; v < vpr; v += 128) {
+        const uint2 c = e4m3_pack8(__ldg(src + v), s);
+        for (int j = 0; j < K; ++j) {
+            const int r = dst[j];
+            if (r >= 0) *reinterpret_cast<uint2*>(xq + size_t(r) * d + size_t(v) * 8) = c;
+        }
     }
-    if (lane < K && p >= 0) xscale[p] = ldexpf(1.f, s);
+    if (tid < K && dst[tid] >= 0) xscale[dst[tid]] = ldexpf(1.f, s);
 }
 
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ w, int64_t n_rows, int d,
@@ -201,8 +211,8 @@ __global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restr
 
 cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream) {
     if (a.per_row) {
-        gather_fp8_row_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos, a.T, a.K,
-                                                                  a.d, a.rows, a.xq, a.xscale, a.status);
+        gather_fp8_row_kernel<<<a.T, 128, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos, a.T, a.K, a.d, a.rows,
+                                                        a.xq, a.xscale, a.status);
         return cudaGetLastError();
     }
     gather_fp8_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.topk_idx, a.pos, a.T,

@@ -120,12 +120,16 @@ WORKLOADS: dict[str, Workload] = {
                  note="the Mixtral-shaped layer with its dispatched rows as row-scaled e4m3 codes fed as "
                       "they are to an FP8 up projection (e4m3 W13, one scale per output channel); h and the "
                       "down projection stay bf16"),
+        Workload("dsv3_decode_fp8_gemm", T=128, d=7168, E=256, k=8, F=2048, act="bf16", expert="swiglu",
+                 n_shared=1, D=8, dispatch_dtype="fp8_gemm",
+                 note="the decode-shaped DeepSeek-V3 layer with FP8 rows and e4m3 up-projection weights: "
+                      "the weight stream of the up projection halves"),
     ]
 }
 
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
-                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm"]
+                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm", "dsv3_decode_fp8_gemm"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

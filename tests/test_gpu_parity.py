@@ -312,6 +312,7 @@ FULL["zipf_gate_padded"] = wl.scaled(W["zipf_cf125"], drop_policy="gate", layout
 FULL["dsv3_grouped_dedup"] = W["dsv3_grouped_dedup"]
 FULL["mixtral_fp8_dispatch"] = W["mixtral_fp8_dispatch"]
 FULL["mixtral_fp8_gemm"] = W["mixtral_fp8_gemm"]
+FULL["dsv3_decode_fp8_gemm"] = W["dsv3_decode_fp8_gemm"]
 
 
 @pytest.mark.parametrize("name", list(FULL))
