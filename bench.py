@@ -345,6 +345,8 @@ def run_ours(args, w, world, rank, local):
         barrier(world)
     total_ms = start.elapsed_time(end)
     stage_ms = {s: float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in events])) for j, s in enumerate(STAGES)}
+    # per-step times from the first to the last stage event of each step
+    step_times = np.array([ev[0].elapsed_time(ev[len(STAGES)]) for ev in events])
     flags = abi.moe_read_status(view.status)
     max_ms = reduce_max(total_ms, world, device)
 
@@ -491,6 +493,8 @@ def run_ours(args, w, world, rank, local):
         "grouped_gemm_frac_bf16_peak": (gemm_flops / (gemm_ms / 1e3) / 1e12) / float(peaks["bf16_tflops"])
         if gemm_ms > 0 and gemm_flops else None,
         "stage_ms": stage_ms,
+        "step_ms": {"median": float(np.median(step_times)), "p95": float(np.percentile(step_times, 95)),
+                    "min": float(step_times.min()), "max": float(step_times.max())},
         "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "dedup": dedup,
                     "fp8_dispatch": fp8,
                     "group_limit": [w.topk_groups, w.n_groups] if 0 < w.topk_groups < w.n_groups else None, "hist": sizing.histogram_summary(counts),

@@ -124,12 +124,17 @@ WORKLOADS: dict[str, Workload] = {
                  n_shared=1, D=8, dispatch_dtype="fp8_gemm",
                  note="the decode-shaped DeepSeek-V3 layer with FP8 rows and e4m3 up-projection weights: "
                       "the weight stream of the up projection halves"),
+        Workload("dsv3_full_fp8_gemm", T=4096, d=7168, E=256, k=8, F=2048, act="bf16", expert="swiglu",
+                 dispatch_dtype="fp8_gemm",
+                 note="the DeepSeek-V3-shaped full layer with FP8 rows and e4m3 up-projection weights "
+                      "(15.0 GB of bf16 W13 become 7.5 GB)"),
     ]
 }
 
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
-                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm", "dsv3_decode_fp8_gemm"]
+                  "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm", "dsv3_decode_fp8_gemm",
+                  "dsv3_full_fp8_gemm"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

@@ -190,6 +190,20 @@ EDGE = [
                 capacity_factor="100", layout="padded", drop_policy="gate"),
     wl.Workload("padded_identity_gate", T=500, d=256, E=16, k=4, F=0, act="bf16", expert="identity",
                 capacity_factor="0.5", D=4, layout="padded", drop_policy="gate"),
+    # the FP8 up projection: one token, every expert per token, zero and huge capacity in
+    # the padded layout, heavy drops with h as a hi/lo pair, rows longer than a stage ring
+    wl.Workload("fp8_gemm_T1_k1", T=1, d=64, E=4, k=1, F=64, act="bf16", expert="swiglu",
+                dispatch_dtype="fp8_gemm"),
+    wl.Workload("fp8_gemm_k_eq_E", T=77, d=128, E=6, k=6, F=96, act="bf16", expert="swiglu", D=3,
+                dispatch_dtype="fp8_gemm"),
+    wl.Workload("fp8_gemm_padded_zero_capacity", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu",
+                capacity_factor="0", layout="padded", dispatch_dtype="fp8_gemm"),
+    wl.Workload("fp8_gemm_padded_cap_huge", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="relu",
+                capacity_factor="100", layout="padded", drop_policy="gate", dispatch_dtype="fp8_gemm"),
+    wl.Workload("fp8_gemm_split_h_drops", T=333, d=144, E=12, k=3, F=192, act="bf16", expert="swiglu", D=4,
+                precision="split_h", capacity_factor="0.6", zipf_s=1.2, dispatch_dtype="fp8_gemm"),
+    wl.Workload("fp8_gemm_long_rows", T=130, d=8192, E=4, k=2, F=256, act="bf16", expert="swiglu",
+                dispatch_dtype="fp8_gemm"),
 ]
 
 
