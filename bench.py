@@ -438,7 +438,7 @@ def run_ours(args, w, world, rank, local):
 
     kernel_work = {
         "route": ("route_gemm_kernel + route_topk_kernel", "alu", work["route_flops"]),
-        "dispatch": ("dispatch (count+scan+scatter+gather)", "hbm", work["dispatch_bytes"]),
+        "dispatch": ("dispatch (scan+scatter+gather; the router counts)", "hbm", work["dispatch_bytes"]),
         "expert_up": up_entry,
         "expert_down": gemm_entry("%s<Plain> (down)" % down_kernel, work["down_flops"], work["down_bytes"]),
         "combine": ("combine_kernel", "hbm", work["combine_bytes"]),

@@ -436,7 +436,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const bool padded = a.layout == MOE_LAYOUT_PADDED;
     const int vec_per_row = int(int64_t(a.d) * a.act_bytes / 16);
     const int64_t rows = padded ? int64_t(a.E) * a.capacity : A;
-    count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.hist, a.status);
+    if (!a.counted) count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.hist, a.status);
     scan_kernel<<<1, 1024, 0, stream>>>(a.E, a.E_capped, a.D, nblk, a.capacity, padded ? 1 : 0, a.hist,
                                         a.counts_routed, a.counts_kept, a.offsets, a.drop_offsets, a.routed_offsets,
                                         a.rank_offsets, a.n_dropped);

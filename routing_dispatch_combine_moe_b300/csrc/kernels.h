@@ -28,10 +28,12 @@ inline size_t route_scratch_bytes_max(int T, int E) {
 }
 // topk_idx / topk_gate have k + n_shared slots per token; the shared slots hold
 // experts E..E+n_shared-1 with gate 1. With 0 < topk_groups < n_groups the selection
-// is limited to the topk_groups best of n_groups contiguous expert groups.
+// is limited to the topk_groups best of n_groups contiguous expert groups. A non-null
+// hist (zeroed, [(E + n_shared) * dispatch_blocks(T * (k + n_shared))]) receives the
+// dispatch's per-block expert counts, so the dispatch can skip its count kernel.
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
-                         float* scratch, cudaStream_t stream);
+                         float* scratch, int32_t* hist, cudaStream_t stream);
 
 struct DispatchArgs {
     int T, d, E, k, D;  // E: all experts (routed + shared), k: all slots per token
@@ -59,6 +61,7 @@ struct DispatchArgs {
     int32_t* routed_offsets; // [E+1] exclusive scan of the routed counts (gate policy)
     int32_t* elist;          // [2*T*k] each expert's assignments in token order, then their gate keys (gate policy)
     bool skip_gather;        // leave xperm to launch_dedup
+    bool counted;            // hist already holds the counts (the router filled it)
 };
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream);

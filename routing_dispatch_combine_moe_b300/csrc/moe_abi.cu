@@ -217,14 +217,14 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
-              float* scratch, cudaStream_t s) {
+              float* scratch, cudaStream_t s, int32_t* hist = nullptr) {
     const cudaError_t e = launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, c->n_shared, c->n_groups,
-                                       c->topk_groups, idx, gate, scratch, s);
+                                       c->topk_groups, idx, gate, scratch, hist, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
 }
 
 int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const float* gate, const moe_dispatch_map* m,
-                 void* xperm, void* ws, cudaStream_t s, bool skip_gather = false) {
+                 void* xperm, void* ws, cudaStream_t s, bool skip_gather = false, bool counted = false) {
     const Layout L = layout(c);
     DispatchArgs a{};
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.D = c->D;
@@ -251,6 +251,7 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const f
     a.routed_offsets = at<int32_t>(ws, L.routed_offsets);
     a.elist = c->drop_policy == MOE_DROP_LOW_GATE ? at<int32_t>(ws, L.elist) : nullptr;
     a.skip_gather = skip_gather;
+    a.counted = counted;
     const cudaError_t e = launch_dispatch(a, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_dispatch");
 }
@@ -375,14 +376,21 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if (ws_bytes < L.forward_end) return MOE_ERR_WORKSPACE;
     moe_workspace_view v{};
     fill_view(c, ws, &v);
-    cudaError_t e = cudaMemsetAsync(v.status, 0, sizeof(int32_t), s);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    // The router also counts each expert's assignments per dispatch block (the fused
+    // route + count): one memset clears the status word and that histogram, which
+    // follow each other at the start of the workspace.
+    const size_t hist_end = L.hist + sizeof(int32_t) * size_t(n_experts(c)) *
+                                         size_t(dispatch_blocks(int64_t(c->T) * n_slots(c)));
+    cudaError_t e = cudaMemsetAsync(ws, 0, hist_end, s);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status, histogram)");
     if ((rc = record(events, n_events, 0, s)) != MOE_OK) return rc;
-    if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s)) != MOE_OK)
+    if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s,
+                        at<int32_t>(ws, L.hist))) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
     const bool f8 = fp8_blocks(c) || fp8_gemm(c);
-    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0 || f8)) != MOE_OK)
+    if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0 || f8, true)) !=
+        MOE_OK)
         return rc;
     if (f8 && (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, fp8_gemm(c) ? nullptr : v.xperm, ws, s)) !=
                   MOE_OK)
@@ -453,14 +461,14 @@ int moe_workspace_get_view(const moe_config* cfg, void* ws, size_t ws_bytes, moe
 
 int moe_kernels_per_forward(const moe_config* cfg) {
     if (validate(cfg) != MOE_OK) return 0;
-    // router + (count, scan, scatter, [select], [pad], gather) + (up, down) + combine
+    // router (which also counts) + (scan, scatter, [select], [pad], gather) + (up, down) + combine
     const int select = cfg->drop_policy == MOE_DROP_LOW_GATE && cfg->capacity >= 0 ? 1 : 0;
     const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
     const int fp8 = fp8_blocks(cfg) ? 1 : 0;  // dequant (the gather quantizes; FP8_GEMM rows are used as they are)
     const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : 2;  // fused, or logits + top-k
-    return route + 4 + select + pad + dedup + fp8 + ffn + 1;
+    return route + 3 + select + pad + dedup + fp8 + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {

@@ -43,11 +43,25 @@ struct Act16<__nv_bfloat16> {
     }
 };
 
+// The dispatch histogram the layer forward has the router fill: hist[e * nblk + b]
+// counts the assignments of expert e among assignments [256 b, 256 (b + 1)) (the count
+// kernel's blocks), zeroed beforehand; integer atomics, so the counts do not depend on
+// their order. A null hist leaves the counting to the dispatch.
+struct RouteCounts {
+    int32_t* hist;
+    int nblk;
+};
+
+__device__ __forceinline__ void count_assignment(const RouteCounts c, int e, int64_t a) {
+    if (c.hist) atomicAdd(c.hist + size_t(e) * c.nblk + size_t(a / kDispatchBlock), 1);
+}
+
 // Top-k of the logits held by a warp (lane l holds experts l + 32 m, m < VPL, with
 // -inf for padding), then the kept softmax; lane j < k writes slot j.
 template <int VPL>
 __device__ __forceinline__ void topk_softmax_store(float (&v)[VPL], int lane, int E, int k, int n_shared,
-                                                   int32_t* idx_out, float* gate_out) {
+                                                   int32_t* idx_out, float* gate_out, const RouteCounts cnt,
+                                                   int64_t a0) {
     float my_val = -INFINITY;
     int my_idx = 0;
     for (int j = 0; j < k; ++j) {
@@ -77,9 +91,11 @@ __device__ __forceinline__ void topk_softmax_store(float (&v)[VPL], int lane, in
     if (lane < k) {
         idx_out[lane] = my_idx;
         gate_out[lane] = ex / sum;
+        count_assignment(cnt, my_idx, a0 + lane);
     } else if (lane < k + n_shared) {  // shared experts follow the routed slots, gate 1
         idx_out[lane] = E + (lane - k);
         gate_out[lane] = 1.0f;
+        count_assignment(cnt, E + (lane - k), a0 + lane);
     }
 }
 
@@ -280,7 +296,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
                                                          const float* __restrict__ bias, int T, int E, int k,
                                                          int n_shared, int n_groups, int topk_groups,
                                                          int32_t* __restrict__ topk_idx,
-                                                         float* __restrict__ topk_gate) {
+                                                         float* __restrict__ topk_gate, const RouteCounts cnt) {
     constexpr int UB = VPL >= 16 ? 4 : (VPL >= 4 ? 8 : 32 / VPL);
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -312,7 +328,8 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
     }
     if (topk_groups > 0 && topk_groups < n_groups) limit_groups<VPL>(v, lane, E, n_groups, topk_groups);
     const int K = k + n_shared;
-    topk_softmax_store<VPL>(v, lane, E, k, n_shared, topk_idx + size_t(t) * K, topk_gate + size_t(t) * K);
+    topk_softmax_store<VPL>(v, lane, E, k, n_shared, topk_idx + size_t(t) * K, topk_gate + size_t(t) * K, cnt,
+                            int64_t(t) * K);
 }
 
 // ------------------------------------------------------------------ small E, fused
@@ -326,7 +343,8 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
 // as the warp-wide path does. Deterministic: every sum has a fixed order.
 template <int EB>
 __device__ __forceinline__ void topk_softmax_thread(float (&v)[EB], int E, int k, int n_shared, int n_groups,
-                                                    int topk_groups, int32_t* idx_out, float* gate_out) {
+                                                    int topk_groups, int32_t* idx_out, float* gate_out,
+                                                    const RouteCounts cnt, int64_t a0) {
     if (topk_groups > 0 && topk_groups < n_groups) {
         const int gs = E / n_groups;
         uint32_t kept = 0;
@@ -370,10 +388,12 @@ __device__ __forceinline__ void topk_softmax_thread(float (&v)[EB], int E, int k
     for (int j = 0; j < k; ++j) {
         idx_out[j] = id[j];
         gate_out[j] = ex[j] / sum;
+        count_assignment(cnt, id[j], a0 + j);
     }
     for (int j = 0; j < n_shared; ++j) {
         idx_out[k + j] = E + j;
         gate_out[k + j] = 1.0f;
+        count_assignment(cnt, E + j, a0 + k + j);
     }
 }
 
@@ -382,7 +402,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const TAct* __restrict
                                                           const float* __restrict__ bias, int T, int d, int E, int k,
                                                           int n_shared, int n_groups, int topk_groups, bool wvec,
                                                           int32_t* __restrict__ topk_idx,
-                                                          float* __restrict__ topk_gate) {
+                                                          float* __restrict__ topk_gate, const RouteCounts cnt) {
     constexpr int VN = Act16<TAct>::N, UV = 4;
     extern __shared__ __align__(16) float smw[];        // W_g [d][E], then the partial logits
     float (*red)[16][EB + 1] = reinterpret_cast<float (*)[16][EB + 1]>(smw + size_t(d) * E);
@@ -451,14 +471,14 @@ __global__ void __launch_bounds__(256) route_small_kernel(const TAct* __restrict
     }
     const int K = k + n_shared;
     topk_softmax_thread<EB>(h, E, k, n_shared, n_groups, topk_groups, topk_idx + size_t(t) * K,
-                            topk_gate + size_t(t) * K);
+                            topk_gate + size_t(t) * K, cnt, int64_t(t) * K);
 }
 
 constexpr int kSmallRouteWBytes = 128 << 10;  // W_g bytes the fused small-E router holds
 
 template <typename TAct, int EB>
 cudaError_t launch_small(const void* x, const float* Wg, const float* bias, int T, int d, int E, int k, int S,
-                         int G, int M, int32_t* idx, float* gate, cudaStream_t stream) {
+                         int G, int M, int32_t* idx, float* gate, const RouteCounts cnt, cudaStream_t stream) {
     auto kern = route_small_kernel<TAct, EB>;
     constexpr size_t max_smem = size_t(kSmallRouteWBytes) + sizeof(float) * 16 * 16 * (EB + 1);
     static std::once_flag once;
@@ -470,17 +490,17 @@ cudaError_t launch_small(const void* x, const float* Wg, const float* bias, int 
     const size_t smem = sizeof(float) * (size_t(d) * E + 16 * 16 * (EB + 1));
     const bool wvec = E == EB && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;
     kern<<<(T + 15) / 16, 256, smem, stream>>>(static_cast<const TAct*>(x), Wg, bias, T, d, E, k, S, G, M, wvec, idx,
-                                               gate);
+                                               gate, cnt);
     return cudaGetLastError();
 }
 
 template <typename TAct>
 cudaError_t launch_small_t(const void* x, const float* Wg, const float* bias, int T, int d, int E, int k, int S,
-                           int G, int M, int32_t* idx, float* gate, cudaStream_t stream) {
-    if (E <= 4) return launch_small<TAct, 4>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
-    if (E <= 8) return launch_small<TAct, 8>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
-    if (E <= 16) return launch_small<TAct, 16>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
-    return launch_small<TAct, 32>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, stream);
+                           int G, int M, int32_t* idx, float* gate, const RouteCounts cnt, cudaStream_t stream) {
+    if (E <= 4) return launch_small<TAct, 4>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, cnt, stream);
+    if (E <= 8) return launch_small<TAct, 8>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, cnt, stream);
+    if (E <= 16) return launch_small<TAct, 16>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, cnt, stream);
+    return launch_small<TAct, 32>(x, Wg, bias, T, d, E, k, S, G, M, idx, gate, cnt, stream);
 }
 
 int warps_along_experts(int E) { return E <= 8 ? 1 : E <= 16 ? 2 : E <= 32 ? 4 : 8; }
@@ -554,13 +574,14 @@ bool route_uses_small_kernel(int d, int E) { return E <= 32 && int64_t(d) * E * 
 
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
-                         float* scratch, cudaStream_t stream) {
+                         float* scratch, int32_t* hist, cudaStream_t stream) {
+    const RouteCounts cnt{hist, dispatch_blocks(int64_t(T) * (k + n_shared))};
     if (route_uses_small_kernel(d, E))
         return act_dtype == MOE_F32
                    ? launch_small_t<float>(x, Wg, bias, T, d, E, k, n_shared, n_groups, topk_groups, topk_idx,
-                                           topk_gate, stream)
+                                           topk_gate, cnt, stream)
                    : launch_small_t<__nv_bfloat16>(x, Wg, bias, T, d, E, k, n_shared, n_groups, topk_groups,
-                                                   topk_idx, topk_gate, stream);
+                                                   topk_idx, topk_gate, cnt, stream);
     const int ks = route_k_slices(T, d, E);
     const int slice = slice_len(d, ks);
     cudaError_t e = act_dtype == MOE_F32 ? launch_gemm_t<float>(x, Wg, T, d, E, slice, ks, scratch, stream)
@@ -568,11 +589,11 @@ cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const fl
     if (e != cudaSuccess) return e;
     const int g2 = (T + 3) / 4;
     const int S = n_shared, G = n_groups, M = topk_groups;
-    if (E <= 32) route_topk_kernel<1><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
-    else if (E <= 64) route_topk_kernel<2><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
-    else if (E <= 128) route_topk_kernel<4><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
-    else if (E <= 256) route_topk_kernel<8><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
-    else route_topk_kernel<16><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate);
+    if (E <= 32) route_topk_kernel<1><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate, cnt);
+    else if (E <= 64) route_topk_kernel<2><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate, cnt);
+    else if (E <= 128) route_topk_kernel<4><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate, cnt);
+    else if (E <= 256) route_topk_kernel<8><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate, cnt);
+    else route_topk_kernel<16><<<g2, 128, 0, stream>>>(scratch, ks, bias, T, E, k, S, G, M, topk_idx, topk_gate, cnt);
     return cudaGetLastError();
 }
 

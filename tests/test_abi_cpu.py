@@ -99,13 +99,14 @@ def test_rows_capacity_and_kernel_counts():
     assert abi.moe_rows_capacity(cfg(capacity=0, layout="padded")) == 0
     with pytest.raises(abi.MoeError):
         abi.moe_rows_capacity(cfg(k=9))
-    # cfg(): E=8, d=128, so the router is one fused launch
-    assert abi.moe_kernels_per_forward(cfg()) == 8
-    assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate")) == 9
-    assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate", layout="padded")) == 10
-    assert abi.moe_kernels_per_forward(cfg(capacity=0, layout="padded")) == 6   # no rows: no padding, no GEMMs
-    assert abi.moe_kernels_per_forward(cfg(expert="identity", F=0)) == 6
-    assert abi.moe_kernels_per_forward(cfg(E=64, d=1024)) == 9                 # split-K logits + top-k
+    # cfg(): E=8, d=128, so the router is one fused launch; the router also counts the
+    # dispatch histogram, so the dispatch is scan, scatter and gather
+    assert abi.moe_kernels_per_forward(cfg()) == 7
+    assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate")) == 8
+    assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate", layout="padded")) == 9
+    assert abi.moe_kernels_per_forward(cfg(capacity=0, layout="padded")) == 5   # no rows: no padding, no GEMMs
+    assert abi.moe_kernels_per_forward(cfg(expert="identity", F=0)) == 5
+    assert abi.moe_kernels_per_forward(cfg(E=64, d=1024)) == 8                 # split-K logits + top-k
 
 
 def test_padded_workspace_holds_n_times_c_rows():
@@ -171,7 +172,7 @@ def test_workspace_sizes_and_layout():
             assert view.out + A * w.d * w.act_bytes <= base + fwd
         assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
         small_router = w.E <= 32 and w.d * w.E * 4 <= 128 * 1024  # one fused router launch instead of two
-        assert abi.moe_kernels_per_forward(c) == ((7 if w.expert == "identity" else 9) + (5 if w.dedup else 0)
+        assert abi.moe_kernels_per_forward(c) == ((6 if w.expert == "identity" else 8) + (5 if w.dedup else 0)
                                                   + (1 if w.dispatch_dtype == "fp8" else 0) - (1 if small_router else 0))
 
 
