@@ -87,6 +87,11 @@ Readings where the pages are silent (each is listed in the design notes too):
   weights are quantized per output channel (one s per row of W13) the same way; the
   up projection then multiplies those exact values, h and the down projection are
   as in the bf16 path.
+* FP8 down projection (the same pages; ours too): h, as the bf16 value the up
+  projection stores, is quantized per row by the same rule, and W2 per output channel
+  (one s per row of W2 [d, F]); the down projection multiplies those values. The bf16
+  rounding comes first because h is stored in bf16 before it is quantized: the
+  e4m3 decision is taken on the stored value (``fp8_hidden``).
 * deduplicated dispatch [DEDUP]: with D virtual ranks (rank r owns routed experts
   [r E/D, (r+1) E/D)), token t sends one row to rank r when at least one of its
   kept routed assignments lives there; send rows are rank-major, in token order
@@ -124,6 +129,7 @@ __all__ = [
     "e4m3_values",
     "quantize_fp8_blocks",
     "quantize_fp8_rows",
+    "fp8_hidden",
     "round_to_bf16",
 ]
 
@@ -478,6 +484,12 @@ def quantize_fp8_rows(x, chunk: int = 2048) -> dict:
     return dict(codes=codes, exps=exps, scales=np.ldexp(1.0, exps), deq=deq)
 
 
+def fp8_hidden(h) -> np.ndarray:
+    """The FP8 form of the hidden activation: each row of h rounded to bf16 (where the up
+    projection stores it), then quantized per row (``quantize_fp8_rows``); float64."""
+    return quantize_fp8_rows(round_to_bf16(h))["deq"]
+
+
 # -------------------------------------------------------------------------- experts
 def silu(z):
     """silu(z) = z / (1 + e^-z)."""
@@ -485,21 +497,28 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
-def expert_relu(X, W1, W2) -> np.ndarray:
-    """ReLU FFN expert: relu(X W1) W2, with W1 [d, F] and W2 [F, d]."""
-    return np.maximum(_f64(X) @ _f64(W1), 0.0) @ _f64(W2)
+def expert_relu(X, W1, W2, hidden=None) -> np.ndarray:
+    """ReLU FFN expert: relu(X W1) W2, with W1 [d, F] and W2 [F, d]. ``hidden``, if
+    given, maps h before the down projection (``fp8_hidden`` for the FP8 down projection)."""
+    h = np.maximum(_f64(X) @ _f64(W1), 0.0)
+    if hidden is not None:
+        h = hidden(h)
+    return h @ _f64(W2)
 
 
-def expert_swiglu(X, Wgate, Wup, Wdown, faithful: bool = False) -> np.ndarray:
+def expert_swiglu(X, Wgate, Wup, Wdown, faithful: bool = False, hidden=None) -> np.ndarray:
     """Gated expert [SWI]: (silu(X Wgate) * (X Wup)) Wdown; Wgate, Wup [d, F], Wdown [F, d].
 
     ``faithful`` rounds the hidden activation to bf16 before the down projection,
-    where the GPU path stores it (diagnostic only).
+    where the GPU path stores it (diagnostic only). ``hidden``, if given, maps h before
+    the down projection (``fp8_hidden`` for the FP8 down projection).
     """
     X = _f64(X)
     h = silu(X @ _f64(Wgate)) * (X @ _f64(Wup))
     if faithful:
         h = round_to_bf16(h)
+    if hidden is not None:
+        h = hidden(h)
     return h @ _f64(Wdown)
 
 

@@ -635,3 +635,47 @@ def test_fp8_expert_equals_the_plain_expert_on_e4m3_exact_weights():
     W13[0, 0, 1] = 448.0 * 1.01 * 2.0 ** -12
     assert not np.array_equal(expert_fn("swiglu", W13, W2, F, fp8_up=True)(0, X), plain(0, X))
 
+
+
+def test_fp8_hidden_rounds_to_bf16_first():
+    """h is stored in bf16 before it is quantized: a value just above an e4m3 midpoint
+    that bf16 rounds onto the midpoint then ties to the even e4m3 code."""
+    h = np.array([[448.0, 1.0625 + 2.0 ** -12, 1.1875 + 2.0 ** -12, -3.0]])  # row scale 2^0
+    got = orc.fp8_hidden(h)
+    # direct e4m3 rounding would give 1.125 and 1.25 for the two middle values
+    assert got.tolist() == [[448.0, 1.0, 1.25, -3.0]]
+    assert orc.quantize_fp8_rows(h)["deq"].tolist() == [[448.0, 1.125, 1.25, -3.0]]
+    # a row whose largest value is 0.5 takes the scale 2^-9 and keeps e4m3-exact values
+    h = np.array([[0.5, 0.25 * 1.125, -0.0009765625]])
+    assert np.array_equal(orc.fp8_hidden(h), h)
+
+
+def test_fp8_down_projection_equals_the_plain_expert_on_exact_values():
+    """ReLU experts with one-hot token rows, so h is a set of rows of W1^T: with W1, W2
+    e4m3 values times one power of two per row (and a full-range value per row) every
+    quantization is exact and the FP8 expert must equal the plain one."""
+    from oracle.packed import expert_fn
+    r = rng(56)
+    E, d, F = 2, 32, 48
+    vals = orc.e4m3_values()[:0x7F]
+
+    def exact_rows(n, m, lo, hi):
+        w = vals[r.integers(0, 0x7F, size=(E, n, m))] * np.where(r.random((E, n, m)) < 0.5, -1, 1)
+        w[:, :, 0] = 448.0
+        return w * np.ldexp(1.0, r.integers(lo, hi, size=(E, n, 1)))
+
+    W1 = np.abs(exact_rows(F, d, -10, -6))  # [E, F, d], rows = output channels, >= 0 so relu keeps h
+    W2 = exact_rows(d, F, -12, -8)          # [E, d, F]
+    # token rows one-hot on column 0: h[f] = W1[e, f, 0] = 448 * 2^s_f, s_f within 4 of
+    # each other, so h is bf16-exact and e4m3-exact under its row scale
+    X = np.zeros((4, d))
+    X[:, 0] = 1.0
+    plain = expert_fn("relu", W1, W2, F)
+    fp8 = expert_fn("relu", W1, W2, F, fp8_up=True, fp8_h=True)
+    for e in range(E):
+        np.testing.assert_array_equal(fp8(e, X), plain(e, X))
+    # a token value that is not e4m3-exact changes the result
+    X2 = np.zeros((1, d))
+    X2[0, 0] = 1.0
+    X2[0, 1] = 1.0 + 2.0 ** -20
+    assert not np.array_equal(fp8(0, X2), plain(0, X2))
