@@ -208,6 +208,11 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
         dispatch = dispatch - rows * w.d * b + rows * fp8_row_bytes(w.d, per_row=True)
     up_in = rows * fp8_row_bytes(w.d, per_row=True) if f8g else rows * w.d * b
     w13_bytes = w.n_experts * w.w13_rows * (w.d + 4) if f8g else w.n_experts * w.w13_rows * w.d * b
+    # FP8 hidden activation: the down stage also quantizes h (reads it in bf16, writes codes
+    # + a scale per row) and then reads those and the e4m3 W2
+    f8h = w.precision == "fp8_h"
+    w2_bytes = w.n_experts * w.d * (w.F + 4) if f8h else w.n_experts * w.d * w.F * b
+    down_in = rows * h_cols * b + 2 * rows * (w.F + 4) if f8h else rows * h_cols * b
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
         route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.slots * 8,
@@ -215,7 +220,7 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
         combine_bytes=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
         up_flops=up, down_flops=down,
         up_bytes=0 if ident else w13_bytes + up_in + rows * h_cols * b,
-        down_bytes=0 if ident else w.n_experts * w.d * w.F * b + rows * h_cols * b + rows * w.d * out_bytes,
+        down_bytes=0 if ident else w2_bytes + down_in + rows * w.d * out_bytes,
     )
 
 
@@ -282,16 +287,16 @@ def run_ours(args, w, world, rank, local):
     # the FP8-GEMM layer takes its up weights as the library's e4m3 buffer (quantized
     # once, like a model load, before any timing)
     w13 = abi.fp8_weights(cfg, inp["W13"]) if w.dispatch_dtype == "fp8_gemm" else inp.get("W13")
+    w2 = abi.fp8_w2(cfg, inp["W2"]) if w.precision == "fp8_h" else inp.get("W2")
     ws = abi.workspace(cfg, device)
     y = torch.empty(w.T, w.d, dtype=w.torch_act, device=device)
     stream = torch.cuda.current_stream(device)
 
     def step(events=None):
         if events is None:
-            abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), w13, inp.get("W2"), y, ws)
+            abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), w13, w2, y, ws)
         else:
-            abi.moe_layer_forward_traced(cfg, inp["x"], inp["Wg"], inp.get("bias"), w13, inp.get("W2"), y, ws,
-                                         events)
+            abi.moe_layer_forward_traced(cfg, inp["x"], inp["Wg"], inp.get("bias"), w13, w2, y, ws, events)
 
     for _ in range(args.warmup):
         step()
@@ -356,7 +361,7 @@ def run_ours(args, w, world, rank, local):
     # (moe_layer_forward_host_async, one workspace and one y buffer per stream), so that
     # one batch's copies run on the copy engines under the other's kernels.
     x_host = inp["x"].cpu().pin_memory()
-    fwd_args = (inp["Wg"], inp.get("bias"), w13, inp.get("W2"))
+    fwd_args = (inp["Wg"], inp.get("bias"), w13, w2)
     ws_h = [abi.workspace(cfg, device, host=True) for _ in range(2)]
     y_h = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
     streams = [torch.cuda.Stream(device) for _ in range(2)]
@@ -422,32 +427,41 @@ def run_ours(args, w, world, rank, local):
     f8g = w.dispatch_dtype == "fp8_gemm"
     # e4m3 up projection: the swapped-pair kernel on FP8; the down projection is the bf16 variant
     down_kernel = abi.moe_ffn_kernel_name(abi.config_for(wl.scaled(w, dispatch_dtype="act"))) if f8g else ffn_kernel
+    f8h = w.precision == "fp8_h"
+    if f8h:
+        down_kernel = ffn_kernel
     up_name = "%s<%s> (up)" % (ffn_kernel, "SwiGLU" if w.expert == "swiglu" else "ReLU")
     # peak of each contraction in its own dtype: e4m3 takes the measured bf16 peak times
     # the nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
     up_peak_scale = 2.0 if f8g else 1.0
+    down_peak_scale = 2.0 if f8h else 1.0
 
     def gemm_entry(name, flops, nbytes):
         if nbytes and flops / nbytes < ridge:
             return (name, "hbm", nbytes)
         return (name, "tensor", flops)
 
+    # the ridge test in the contraction's own dtype (its peak is up_/down_peak_scale x bf16)
     up_entry = gemm_entry(up_name, work["up_flops"] / up_peak_scale, work["up_bytes"])
     if up_entry[1] == "tensor":
         up_entry = (up_name, "tensor", work["up_flops"])
+    down_name = "%s<Plain> (down%s)" % (down_kernel, ", with the h quantization" if f8h else "")
+    down_entry = gemm_entry(down_name, work["down_flops"] / down_peak_scale, work["down_bytes"])
+    if down_entry[1] == "tensor":
+        down_entry = (down_name, "tensor", work["down_flops"])
 
     kernel_work = {
         "route": ("route_gemm_kernel + route_topk_kernel", "alu", work["route_flops"]),
         "dispatch": ("dispatch (scan+scatter+gather; the router counts)", "hbm", work["dispatch_bytes"]),
         "expert_up": up_entry,
-        "expert_down": gemm_entry("%s<Plain> (down)" % down_kernel, work["down_flops"], work["down_bytes"]),
+        "expert_down": down_entry,
         "combine": ("combine_kernel", "hbm", work["combine_bytes"]),
     }
     dom = max(STAGES, key=lambda s: stage_ms[s])
     kname, bound, amount = kernel_work[dom]
     dom_s = stage_ms[dom] / 1e3
-    if bound == "tensor" and dom == "expert_up" and f8g:
-        peak = float(peaks["bf16_tflops"]) * up_peak_scale
+    if bound == "tensor" and ((dom == "expert_up" and f8g) or (dom == "expert_down" and f8h)):
+        peak = float(peaks["bf16_tflops"]) * 2.0
         roof = {"bound": "tensor", "achieved": amount / dom_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16 burst x 2 (nominal e4m3 / bf16 dense ratio)"}
     elif bound == "tensor":

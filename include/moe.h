@@ -85,6 +85,11 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
 #define MOE_PRECISION_SPLIT_H 2 /* h carried as a bf16 pair (hi = bf16(h), lo = bf16(h - hi)); both halves go
                                    through the down projection against the same weights; expert outputs in
                                    fp32: y then carries essentially only its own final rounding */
+#define MOE_PRECISION_FP8_H 3   /* MOE_DISPATCH_FP8_GEMM only: h, as the bf16 value the up projection stores,
+                                   quantized per row to e4m3 (one power-of-two scale per row, the rule of the
+                                   FP8 rows), and the down projection on tcgen05 kind::f8f6f4 against e4m3 W2
+                                   with one scale per output channel (moe_quantize_w2_fp8); expert outputs in
+                                   fp32. Needs F % 16 == 0 */
 
 /* What an expert past its capacity drops (capacity >= 0 only). */
 #define MOE_DROP_TOKEN_ORDER 0 /* keep the first `capacity` assignments by token index */
@@ -183,6 +188,8 @@ typedef struct moe_workspace_view {
                           * MOE_DISPATCH_FP8_GEMM: all rows); NULL for MOE_DISPATCH_ACT */
     float* xscale;       /* their scales: [rows, ceil(d/128)] block scales (MOE_DISPATCH_FP8) or [rows]
                           * row scales (MOE_DISPATCH_FP8_GEMM); NULL for MOE_DISPATCH_ACT */
+    uint8_t* hq;         /* [rows, F] e4m3 codes of h (MOE_PRECISION_FP8_H only, else NULL) */
+    float* hscale;       /* [rows] their row scales (MOE_PRECISION_FP8_H only, else NULL) */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -326,14 +333,26 @@ size_t moe_fp8_weight_bytes(const moe_config* cfg);
  * Needs cfg->dispatch_dtype == MOE_DISPATCH_FP8_GEMM. Bit-exact and deterministic. */
 int moe_quantize_weights_fp8(const moe_config* cfg, const void* W13, void* W13_fp8, moe_stream_t stream);
 
+/* Bytes of the FP8 down-projection weights of a MOE_PRECISION_FP8_H config: the e4m3
+ * codes of W2 ([N, d, F] uint8), then, at the next 256-byte boundary, one fp32 scale per
+ * row of W2 (output channel, [N, d]). 0 for other configs. */
+size_t moe_fp8_w2_bytes(const moe_config* cfg);
+
+/* Quantizes the bf16 W2 [N, d, F] into that buffer, each row (output channel) by the
+ * rule of moe_quantize_weights_fp8. Needs cfg->precision == MOE_PRECISION_FP8_H.
+ * Bit-exact and deterministic. */
+int moe_quantize_w2_fp8(const moe_config* cfg, const void* W2, void* W2_fp8, moe_stream_t stream);
+
 /* moe_expert_ffn for a MOE_DISPATCH_FP8_GEMM config: the up projection runs on the
  * e4m3 rows and weights (tcgen05 kind::f8f6f4 on SM pairs), its fp32 accumulator
  * multiplied by the row scale and the weight row's scale before the activation; h is
  * stored as for moe_expert_ffn (bf16, or a hi/lo pair under MOE_PRECISION_SPLIT_H) and
  * the down projection is the bf16 one.
  *   xq      [rows, d] uint8 e4m3 codes;  xscale [rows] fp32 row scales (moe_dispatch_fp8)
- *   W13_fp8 moe_quantize_weights_fp8's buffer;  W2 [N, d, F] bf16
- *   offsets, h, out, ws as in moe_expert_ffn. */
+ *   W13_fp8 moe_quantize_weights_fp8's buffer;  W2 [N, d, F] bf16, or under MOE_PRECISION_FP8_H
+ *           moe_quantize_w2_fp8's buffer (h is then quantized per row between the two GEMMs)
+ *   offsets, h, out as in moe_expert_ffn;  ws >= moe_ffn_workspace_bytes(cfg) (under
+ *   MOE_PRECISION_FP8_H it also holds h's codes and scales). */
 int moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* xscale, const int32_t* offsets,
                        const void* W13_fp8, const void* W2, void* h, void* out, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
@@ -353,7 +372,8 @@ int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate,
 /* The whole layer: route, dispatch, expert FFN, combine. Intermediates live in ws
  * (layout: moe_workspace_get_view). ws >= moe_workspace_bytes(cfg); the status word
  * is cleared at the start. W13/W2 may be NULL for identity experts. Under
- * MOE_DISPATCH_FP8_GEMM, W13 is moe_quantize_weights_fp8's buffer. y [T, d] act. */
+ * MOE_DISPATCH_FP8_GEMM, W13 is moe_quantize_weights_fp8's buffer, and under
+ * MOE_PRECISION_FP8_H W2 is moe_quantize_w2_fp8's. y [T, d] act. */
 int moe_layer_forward(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
                       const void* W13, const void* W2, void* y, void* ws, size_t ws_bytes,
                       moe_stream_t stream);

@@ -497,10 +497,21 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
+def hidden_relu(X, W1) -> np.ndarray:
+    """Hidden activation of the ReLU expert: h = relu(X W1), W1 [d, F]."""
+    return np.maximum(_f64(X) @ _f64(W1), 0.0)
+
+
+def hidden_swiglu(X, Wgate, Wup) -> np.ndarray:
+    """Hidden activation of the gated expert [SWI]: h = silu(X Wgate) * (X Wup)."""
+    X = _f64(X)
+    return silu(X @ _f64(Wgate)) * (X @ _f64(Wup))
+
+
 def expert_relu(X, W1, W2, hidden=None) -> np.ndarray:
     """ReLU FFN expert: relu(X W1) W2, with W1 [d, F] and W2 [F, d]. ``hidden``, if
     given, maps h before the down projection (``fp8_hidden`` for the FP8 down projection)."""
-    h = np.maximum(_f64(X) @ _f64(W1), 0.0)
+    h = hidden_relu(X, W1)
     if hidden is not None:
         h = hidden(h)
     return h @ _f64(W2)
@@ -513,8 +524,7 @@ def expert_swiglu(X, Wgate, Wup, Wdown, faithful: bool = False, hidden=None) -> 
     where the GPU path stores it (diagnostic only). ``hidden``, if given, maps h before
     the down projection (``fp8_hidden`` for the FP8 down projection).
     """
-    X = _f64(X)
-    h = silu(X @ _f64(Wgate)) * (X @ _f64(Wup))
+    h = hidden_swiglu(X, Wgate, Wup)
     if faithful:
         h = round_to_bf16(h)
     if hidden is not None:

@@ -23,8 +23,9 @@ MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = 4, 5, 6
 MOE_DEV_ERR_INDEX, MOE_DEV_ERR_TIMEOUT = 0x1, 0x2
 MOE_F32, MOE_BF16 = 0, 1
 MOE_EXPERT_IDENTITY, MOE_EXPERT_RELU, MOE_EXPERT_SWIGLU = 0, 1, 2
-MOE_PRECISION_BF16, MOE_PRECISION_F32_OUT, MOE_PRECISION_SPLIT_H = 0, 1, 2
-PRECISIONS = {"bf16": MOE_PRECISION_BF16, "f32_out": MOE_PRECISION_F32_OUT, "split_h": MOE_PRECISION_SPLIT_H}
+MOE_PRECISION_BF16, MOE_PRECISION_F32_OUT, MOE_PRECISION_SPLIT_H, MOE_PRECISION_FP8_H = 0, 1, 2, 3
+PRECISIONS = {"bf16": MOE_PRECISION_BF16, "f32_out": MOE_PRECISION_F32_OUT, "split_h": MOE_PRECISION_SPLIT_H,
+              "fp8_h": MOE_PRECISION_FP8_H}
 MOE_DROP_TOKEN_ORDER, MOE_DROP_LOW_GATE = 0, 1
 DROP_POLICIES = {"token": MOE_DROP_TOKEN_ORDER, "gate": MOE_DROP_LOW_GATE}
 MOE_LAYOUT_PACKED, MOE_LAYOUT_PADDED = 0, 1
@@ -67,7 +68,7 @@ class moe_send_map(ctypes.Structure):
 class moe_workspace_view(ctypes.Structure):
     _fields_ = [("status", _p), ("topk_idx", _p), ("topk_gate", _p), ("map", moe_dispatch_map),
                 ("xperm", _p), ("h", _p), ("out", _p), ("send", moe_send_map), ("xsend", _p), ("xq", _p),
-                ("xscale", _p)]
+                ("xscale", _p), ("hq", _p), ("hscale", _p)]
 
 
 _SIGNATURES = {
@@ -98,6 +99,8 @@ _SIGNATURES = {
                                         _p, _p, _p, _sz, _p]),
     "moe_fp8_weight_bytes": (_sz, [ctypes.POINTER(moe_config)]),
     "moe_quantize_weights_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p]),
+    "moe_fp8_w2_bytes": (_sz, [ctypes.POINTER(moe_config)]),
+    "moe_quantize_w2_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p]),
     "moe_expert_ffn_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_dispatch_static": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_dispatch_map),
                                            _p, _p]),
@@ -260,6 +263,8 @@ class WorkspaceView:
     xsend: int | None = None
     xq: int | None = None
     xscale: int | None = None
+    hq: int | None = None
+    hscale: int | None = None
 
 
 def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
@@ -270,7 +275,8 @@ def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
     sm = v.send
     return WorkspaceView(v.status, v.topk_idx, v.topk_gate, m.counts_routed, m.counts_kept, m.offsets,
                          m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out,
-                         sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend, v.xq, v.xscale)
+                         sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend, v.xq, v.xscale,
+                         v.hq, v.hscale)
 
 
 # ------------------------------------------------------------------ hot path
@@ -348,6 +354,23 @@ def fp8_weight_parts(cfg, W13_fp8, N: int, R: int, d: int):
     n = N * R * d
     off = (n + 255) // 256 * 256
     return W13_fp8[:n].view(N, R, d), W13_fp8[off:off + 4 * N * R].view(torch.float32).view(N, R)
+
+
+def moe_fp8_w2_bytes(cfg) -> int:
+    """Bytes of the FP8 W2 buffer of an "fp8_h" config (codes, then row scales)."""
+    return lib().moe_fp8_w2_bytes(ctypes.byref(cfg))
+
+
+def moe_quantize_w2_fp8(cfg, W2, W2_fp8, stream=None):
+    _check(lib().moe_quantize_w2_fp8(ctypes.byref(cfg), _ptr(W2), _ptr(W2_fp8), _stream(stream)),
+           "moe_quantize_w2_fp8")
+
+
+def fp8_w2(cfg, W2, stream=None) -> torch.Tensor:
+    """The FP8 W2 buffer (uint8, on W2's device) of an "fp8_h" config."""
+    q = torch.empty(moe_fp8_w2_bytes(cfg), dtype=torch.uint8, device=W2.device)
+    moe_quantize_w2_fp8(cfg, W2, q, stream)
+    return q
 
 
 def moe_expert_ffn_fp8(cfg, xq, xscale, offsets, W13_fp8, W2, h, out, ws, stream=None):

@@ -1093,6 +1093,16 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.b_k_shift = split_h ? 1 : 0;
     p.R = a.d;
     p.n_tiles = (a.d + MMA_N - 1) / MMA_N;
+    if (a.h_fp8) {
+        // h quantized per row (its bf16 value, as stored) into e4m3 codes + row scales,
+        // then the down projection on e4m3 against e4m3 W2: always the swapped pairs
+        if ((err = launch_quantize_rows_fp8(a.h, rows_max, a.F, a.hq, a.hscale, stream)) != cudaSuccess) return err;
+        p.xscale = a.hscale;
+        p.wscale = a.w2_scale;
+        if ((err = make_map(&mA, a.W2, a.F, uint64_t(a.E) * a.d, 128, true)) != cudaSuccess) return err;
+        if ((err = make_row_maps(&mX, a.hq, a.F, rows_max, true)) != cudaSuccess) return err;
+        return launch_swap<kPlain, kOutF32, true>(mA, mX, p, rows_max, a.E, stream);
+    }
     if (swap) {
         if ((err = make_map(&mA, a.W2, a.F, uint64_t(a.E) * a.d, 128)) != cudaSuccess) return err;
         if ((err = make_row_maps(&mX, a.h, kA, rows_max)) != cudaSuccess) return err;

@@ -134,6 +134,10 @@ struct FfnArgs {
     bool in_fp8;            // up projection on e4m3 rows and weights (row-scaled)
     const float* xscale;    // [rows] with in_fp8
     const float* w13_scale; // [E * R] with in_fp8 (W13 then holds e4m3 codes)
+    bool h_fp8;             // h quantized per row, down projection on e4m3 (W2 then holds e4m3 codes)
+    uint8_t* hq;            // [rows, F] with h_fp8
+    float* hscale;          // [rows] with h_fp8
+    const float* w2_scale;  // [E * d] with h_fp8
     const void* W13;
     const void* W2;
     void* h;

@@ -64,6 +64,8 @@ inline int out_dtype(const moe_config* c) {
 // The FP8 wire formats: block-scaled rows turned back into bf16, or row-scaled rows for the FP8 GEMM.
 inline bool fp8_blocks(const moe_config* c) { return c->dispatch_dtype == MOE_DISPATCH_FP8; }
 inline bool fp8_gemm(const moe_config* c) { return c->dispatch_dtype == MOE_DISPATCH_FP8_GEMM; }
+// h quantized per row and the down projection on e4m3 (with the FP8 up projection).
+inline bool fp8_h(const moe_config* c) { return fp8_gemm(c) && c->precision == MOE_PRECISION_FP8_H; }
 
 // Rows of W13 per expert: gate and up rows for SwiGLU, W1's rows for ReLU.
 inline int64_t w13_rows(const moe_config* c) { return c->expert_kind == MOE_EXPERT_SWIGLU ? 2 * int64_t(c->F) : c->F; }
@@ -79,7 +81,7 @@ int validate(const moe_config* c) {
         c->expert_kind != MOE_EXPERT_SWIGLU)
         return MOE_ERR_ARG;
     if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_F32_OUT &&
-        c->precision != MOE_PRECISION_SPLIT_H)
+        c->precision != MOE_PRECISION_SPLIT_H && c->precision != MOE_PRECISION_FP8_H)
         return MOE_ERR_ARG;
     if (c->n_shared < 0) return MOE_ERR_ARG;
     if (c->k > c->E) return MOE_ERR_ARG;
@@ -103,6 +105,11 @@ int validate(const moe_config* c) {
     if ((fp8_blocks(c) || fp8_gemm(c)) && (c->act_dtype != MOE_BF16 || c->dedup)) return MOE_ERR_UNSUPPORTED;
     if (fp8_gemm(c) && c->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_UNSUPPORTED;
     if (fp8_gemm(c) && c->d % 16 != 0) return MOE_ERR_ALIGN;  // e4m3 rows of d bytes, 16-byte aligned
+    // the FP8 hidden activation goes with the FP8 up projection (bf16 activations), h rows of F bytes
+    if (c->precision == MOE_PRECISION_FP8_H && c->act_dtype == MOE_BF16 && c->expert_kind != MOE_EXPERT_IDENTITY) {
+        if (!fp8_gemm(c)) return MOE_ERR_UNSUPPORTED;
+        if (c->F % 16 != 0) return MOE_ERR_ALIGN;
+    }
     if (int64_t(c->T) * n_slots(c) > int64_t(INT32_MAX) || rows_cap(c) > int64_t(INT32_MAX))
         return MOE_ERR_UNSUPPORTED;
     if ((int64_t(c->d) * act_bytes(c)) % 16 != 0) return MOE_ERR_ALIGN;
@@ -118,6 +125,7 @@ struct Layout {
     size_t dd_slots, dd_hist, dd_kept, dd_drop, dd_routed, dd_rank, dd_ndrop;
     size_t send_counts, send_offsets, send_pos, send_src, xsend;
     size_t xq, xscale;  // FP8 dispatch
+    size_t hq, hscale;  // FP8 hidden activation
     size_t dispatch_end, forward_end, host_end;
 };
 
@@ -177,6 +185,8 @@ Layout layout(const moe_config* c) {
     L.xscale = take(fp8_blocks(c)  ? sizeof(float) * R * size_t((c->d + 127) / 128)
                     : fp8_gemm(c) ? sizeof(float) * R
                                   : 0);
+    L.hq = take(fp8_h(c) ? R * size_t(c->F) : 0);
+    L.hscale = take(fp8_h(c) ? sizeof(float) * R : 0);
     L.forward_end = o;
     L.x_stage = take(b * size_t(c->T) * c->d);
     L.y_stage = take(b * size_t(c->T) * c->d);
@@ -214,6 +224,22 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     const bool f8 = fp8_blocks(c) || fp8_gemm(c);
     v->xq = f8 ? at<uint8_t>(ws, L.xq) : nullptr;
     v->xscale = f8 ? at<float>(ws, L.xscale) : nullptr;
+    v->hq = fp8_h(c) ? at<uint8_t>(ws, L.hq) : nullptr;
+    v->hscale = fp8_h(c) ? at<float>(ws, L.hscale) : nullptr;
+}
+
+// Standalone moe_expert_ffn(_fp8) workspace: the status word, then (FP8 hidden
+// activation) h's codes and row scales.
+struct FfnLayout {
+    size_t hq, hscale, end;
+};
+FfnLayout ffn_layout(const moe_config* c) {
+    FfnLayout F{};
+    F.hq = kAlign;
+    const size_t R = size_t(rows_cap(c));
+    F.hscale = align_up(F.hq + (fp8_h(c) ? R * size_t(c->F) : 0));
+    F.end = align_up(F.hscale + (fp8_h(c) ? sizeof(float) * R : 0));
+    return F;
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
@@ -311,17 +337,28 @@ inline size_t fp8_weight_scale_offset(const moe_config* c) {
     return align_up(size_t(n_experts(c)) * size_t(w13_rows(c)) * size_t(c->d));
 }
 
+// Same for an FP8 W2 buffer.
+inline size_t fp8_w2_scale_offset(const moe_config* c) {
+    return align_up(size_t(n_experts(c)) * size_t(c->d) * size_t(c->F));
+}
+
 // xscale: the rows' scales when cfg is MOE_DISPATCH_FP8_GEMM (xperm then holds their
 // e4m3 codes and W13 the FP8 weight buffer).
 int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const int32_t* counts, const void* W13,
             const void* W2, void* h, void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid,
-            const float* xscale = nullptr) {
+            const float* xscale = nullptr, uint8_t* hq = nullptr, float* hscale = nullptr) {
     FfnArgs a{};
     if (fp8_gemm(c)) {
         a.in_fp8 = true;
         a.xscale = xscale;
         a.w13_scale = reinterpret_cast<const float*>(static_cast<const unsigned char*>(W13) +
                                                      fp8_weight_scale_offset(c));
+    }
+    if (fp8_h(c)) {
+        a.h_fp8 = true;
+        a.hq = hq;
+        a.hscale = hscale;
+        a.w2_scale = reinterpret_cast<const float*>(static_cast<const unsigned char*>(W2) + fp8_w2_scale_offset(c));
     }
     a.T = c->T; a.d = c->d; a.E = n_experts(c); a.k = n_slots(c); a.F = c->F;
     a.rows = rows_cap(c);
@@ -404,7 +441,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
         // ever combined), so those rows of `out` are left unwritten by the forward.
         const int32_t* used = c->layout == MOE_LAYOUT_PADDED ? v.map.counts_kept : nullptr;
         const void* rows = fp8_gemm(c) ? static_cast<const void*>(v.xq) : v.xperm;
-        if ((rc = run_ffn(c, rows, v.map.offsets, used, W13, W2, v.h, v.out, v.status, s, mid, v.xscale)) != MOE_OK)
+        if ((rc = run_ffn(c, rows, v.map.offsets, used, W13, W2, v.h, v.out, v.status, s, mid, v.xscale, v.hq,
+                          v.hscale)) != MOE_OK)
             return rc;
     } else if ((rc = record(events, n_events, 3, s)) != MOE_OK) {
         return rc;
@@ -442,7 +480,7 @@ size_t moe_dispatch_workspace_bytes(const moe_config* cfg) {
     return validate(cfg) == MOE_OK ? layout(cfg).dispatch_end : 0;
 }
 
-size_t moe_ffn_workspace_bytes(const moe_config* cfg) { return validate(cfg) == MOE_OK ? kAlign : 0; }
+size_t moe_ffn_workspace_bytes(const moe_config* cfg) { return validate(cfg) == MOE_OK ? ffn_layout(cfg).end : 0; }
 
 size_t moe_workspace_bytes(const moe_config* cfg) { return validate(cfg) == MOE_OK ? layout(cfg).forward_end : 0; }
 
@@ -467,8 +505,9 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
     const int fp8 = fp8_blocks(cfg) ? 1 : 0;  // dequant (the gather quantizes; FP8_GEMM rows are used as they are)
+    const int fp8h = fp8_h(cfg) && ffn ? 1 : 0;  // h quantized between the two GEMMs
     const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : 2;  // fused, or logits + top-k
-    return route + 3 + select + pad + dedup + fp8 + ffn + 1;
+    return route + 3 + select + pad + dedup + fp8 + fp8h + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {
@@ -576,6 +615,22 @@ int moe_quantize_weights_fp8(const moe_config* cfg, const void* W13, void* W13_f
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_quantize_weights_fp8");
 }
 
+size_t moe_fp8_w2_bytes(const moe_config* cfg) {
+    if (validate(cfg) != MOE_OK || !fp8_h(cfg)) return 0;
+    return fp8_w2_scale_offset(cfg) + sizeof(float) * size_t(n_experts(cfg)) * size_t(cfg->d);
+}
+
+int moe_quantize_w2_fp8(const moe_config* cfg, const void* W2, void* W2_fp8, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!fp8_h(cfg) || !W2 || !W2_fp8) return MOE_ERR_ARG;
+    if (!aligned16(W2) || !aligned16(W2_fp8)) return MOE_ERR_ALIGN;
+    unsigned char* q = static_cast<unsigned char*>(W2_fp8);
+    const cudaError_t e = launch_quantize_rows_fp8(W2, int64_t(n_experts(cfg)) * cfg->d, cfg->F, q,
+                                                   reinterpret_cast<float*>(q + fp8_w2_scale_offset(cfg)), stream);
+    return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_quantize_w2_fp8");
+}
+
 int moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* xscale, const int32_t* offsets,
                        const void* W13_fp8, const void* W2, void* h, void* out, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
@@ -587,11 +642,13 @@ int moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* xs
     if (!aligned16(xq) || !aligned4(xscale) || !aligned16(W13_fp8) || !aligned16(W2) || !aligned16(h) ||
         !aligned16(out) || !aligned16(ws))
         return MOE_ERR_ALIGN;
-    if (ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+    const FfnLayout FL = ffn_layout(cfg);
+    if (ws_bytes < FL.end) return MOE_ERR_WORKSPACE;
     int32_t* status = static_cast<int32_t*>(ws);
     const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
-    return run_ffn(cfg, xq, offsets, nullptr, W13_fp8, W2, h, out, status, stream, nullptr, xscale);
+    return run_ffn(cfg, xq, offsets, nullptr, W13_fp8, W2, h, out, status, stream, nullptr, xscale,
+                   fp8_h(cfg) ? at<uint8_t>(ws, FL.hq) : nullptr, fp8_h(cfg) ? at<float>(ws, FL.hscale) : nullptr);
 }
 
 int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, const int32_t* pos, void* y,

@@ -51,7 +51,9 @@ class Workload:
     D: int = 1  # virtual expert-parallel ranks the dispatch is laid out for
     zipf_s: float | None = None
     # bf16 experts: "bf16" (h and expert outputs in bf16), "f32_out" (expert outputs in
-    # fp32) or "split_h" (h as a bf16 hi/lo pair too); see the library header.
+    # fp32), "split_h" (h as a bf16 hi/lo pair too) or "fp8_h" (with dispatch_dtype
+    # "fp8_gemm": h quantized to e4m3 per row, the down projection on e4m3); see the
+    # library header.
     precision: str = "f32_out"
     n_shared: int = 0  # shared experts (ids E .. E+n_shared-1) every token also uses, gate 1
     drop_policy: str = "token"  # overflow dropped in token order, or "gate": lowest gates first
@@ -124,6 +126,10 @@ WORKLOADS: dict[str, Workload] = {
                  n_shared=1, D=8, dispatch_dtype="fp8_gemm",
                  note="the decode-shaped DeepSeek-V3 layer with FP8 rows and e4m3 up-projection weights: "
                       "the weight stream of the up projection halves"),
+        Workload("mixtral_fp8_experts", T=2048, d=4096, E=8, k=2, F=14336, act="bf16", expert="swiglu",
+                 dispatch_dtype="fp8_gemm", precision="fp8_h",
+                 note="the Mixtral-shaped layer with both expert projections on e4m3: FP8 rows and W13 for "
+                      "the up projection, h quantized per row and e4m3 W2 for the down projection"),
         Workload("dsv3_full_fp8_gemm", T=4096, d=7168, E=256, k=8, F=2048, act="bf16", expert="swiglu",
                  dispatch_dtype="fp8_gemm",
                  note="the DeepSeek-V3-shaped full layer with FP8 rows and e4m3 up-projection weights "
@@ -134,7 +140,7 @@ WORKLOADS: dict[str, Workload] = {
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
                   "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm", "dsv3_decode_fp8_gemm",
-                  "dsv3_full_fp8_gemm"]
+                  "dsv3_full_fp8_gemm", "mixtral_fp8_experts"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

@@ -39,15 +39,16 @@ def rms(v) -> float:
     return float(np.sqrt(np.mean(v * v))) if v.size else 0.0
 
 
-def check_close(got, exact, act: str, what: str, tol: float | None = None) -> float:
-    """Asserts the float tolerance; returns the raw max|err| / rms(exact)."""
+def check_close(got, exact, act: str, what: str, tol: float | None = None, extra=None) -> float:
+    """Asserts the float tolerance (plus a per-element ``extra`` bound, if given); returns
+    the raw max|err| / rms(exact)."""
     tol = TOL[act] if tol is None else tol
     got = f64(got)
     exact = np.asarray(exact, np.float64)
     assert got.shape == exact.shape, (what, got.shape, exact.shape)
     r = rms(exact)
     err = np.abs(got - exact)
-    bound = tol * r + half_ulp(exact, act)
+    bound = tol * r + half_ulp(exact, act) + (0.0 if extra is None else np.asarray(extra, np.float64))
     bad = err > bound
     assert not np.isnan(got).any(), f"{what}: NaN in GPU output"
     if bad.any():
@@ -123,7 +124,8 @@ class StageBuffers:
         offsets = self.offsets if offsets is None else offsets
         if self.cfg.dispatch_dtype == abi.MOE_DISPATCH_FP8_GEMM:
             abi.moe_expert_ffn_fp8(self.cfg, self.xq if xq is None else xq, self.xscale if xscale is None else xscale,
-                                   offsets, api_w13(self.cfg, inp), inp["W2"], self.h, self.out, self.ws_ffn)
+                                   offsets, api_w13(self.cfg, inp), api_w2(self.cfg, inp), self.h, self.out,
+                                   self.ws_ffn)
             return
         abi.moe_expert_ffn(self.cfg, self.xperm if xperm is None else xperm, offsets, inp["W13"], inp["W2"],
                            self.h, self.out, self.ws_ffn)
@@ -149,6 +151,59 @@ def api_w13(cfg, inp):
     return inp["W13_fp8"]
 
 
+def api_w2(cfg, inp):
+    """The W2 the library takes: the bf16 weights, or (FP8 hidden activation) their FP8
+    buffer, quantized once on the device by the library and kept in ``inp``."""
+    if cfg.precision != abi.MOE_PRECISION_FP8_H or inp.get("W2") is None:
+        return inp.get("W2")
+    if "W2_fp8" not in inp:
+        inp["W2_fp8"] = abi.fp8_w2(cfg, inp["W2"])
+    return inp["W2_fp8"]
+
+
+# Relative error of the GPU's fp32 hidden activation against the exact one that the FP8
+# hidden-activation budget allows for: fp32 sums of K exact e4m3 products and the fast
+# exp/divide of silu stay near 1e-6; 2^-16 leaves a margin.
+FP8_H_EPS = 2.0 ** -16
+
+
+def fp8_h_jump(h, eps: float = FP8_H_EPS) -> np.ndarray:
+    """How far the FP8 form of each element of h (``fp8_hidden``, a step function of h)
+    can move when h is off by a relative eps: the e4m3 code the GPU picks from its own
+    bf16 h may differ from the oracle's next to a rounding boundary, as a top-k may
+    differ at a near tie."""
+    mid = orc.fp8_hidden(h)
+    return np.maximum(np.abs(orc.fp8_hidden(h * (1 - eps)) - mid), np.abs(orc.fp8_hidden(h * (1 + eps)) - mid))
+
+
+def fp8_h_budget(w, inp, e, X) -> np.ndarray:
+    """Bound [rows, d] on what those code changes can move expert e's outputs for the
+    rows X: sum over features of the jump times |W2| (row-quantized). The quantized
+    weights are kept in ``inp`` after first use."""
+    cache = inp.setdefault("_fp8_h_budget_cache", {})
+    if e not in cache:
+        w13q = orc.quantize_fp8_rows(f64(inp["W13"][e]))["deq"]
+        w2q = orc.quantize_fp8_rows(f64(inp["W2"][e]))["deq"]  # [d, F]
+        cache[e] = (w13q, np.abs(w2q).T.astype(np.float32))
+    w13q, w2abs = cache[e]
+    X = np.asarray(X, np.float64)
+    F = w.F
+    h = orc.hidden_relu(X, w13q.T) if w.expert == "relu" else orc.hidden_swiglu(X, w13q[:F].T, w13q[F:].T)
+    return (fp8_h_jump(h).astype(np.float32) @ w2abs).astype(np.float64)
+
+
+def fp8_h_layer_budget(w, inp, ref) -> np.ndarray:
+    """The same bound carried through the combine: [T, d] for an oracle forward ``ref``."""
+    out_b = np.zeros_like(ref["out"])
+    off = ref["offsets"]
+    for e in range(w.n_experts):
+        lo, hi = int(off[e]), int(off[e + 1])
+        held = np.arange(lo, hi)[ref["row_src"][lo:hi] >= 0]
+        if held.size:
+            out_b[held] = fp8_h_budget(w, inp, e, ref["xperm"][held])
+    return orc.combine(ref["G"], ref["pos"], out_b, w.T, w.slots)
+
+
 def check_fp8_weights(w, cfg, inp, experts) -> None:
     """The library's FP8 weight buffer: codes and per-row scales of the given experts
     bit-exact against the oracle's row-wise quantization of W13."""
@@ -157,6 +212,12 @@ def check_fp8_weights(w, cfg, inp, experts) -> None:
         q = orc.quantize_fp8_rows(f64(inp["W13"][e]))
         np.testing.assert_array_equal(cpu(codes[e]).numpy(), q["codes"])
         np.testing.assert_array_equal(cpu(scales[e]).numpy().astype(np.float64), q["scales"])
+    if cfg.precision == abi.MOE_PRECISION_FP8_H:  # the W2 buffer has the same layout: [N, d, F] + [N, d]
+        codes, scales = abi.fp8_weight_parts(cfg, api_w2(cfg, inp), w.n_experts, w.d, w.F)
+        for e in experts:
+            q = orc.quantize_fp8_rows(f64(inp["W2"][e]))
+            np.testing.assert_array_equal(cpu(codes[e]).numpy(), q["codes"])
+            np.testing.assert_array_equal(cpu(scales[e]).numpy().astype(np.float64), q["scales"])
 
 
 def compare_fp8_rows(w, xq, xscale, row_src, x, rows=None) -> int:
@@ -366,7 +427,7 @@ def check_ffn(w, inp, bufs, st, expert_subset=None) -> float:
         xperm = torch.zeros(bufs.rows, w.d, dtype=w.torch_act, device="cuda")
         xperm[:offs[-1]] = st["xperm"]
         bufs.ffn(inp, xperm=xperm, offsets=torch.from_numpy(offs).cuda())
-    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8)
+    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8, fp8_h=w.precision == "fp8_h")
     experts = range(w.n_experts) if expert_subset is None else expert_subset
     if fp8:
         check_fp8_weights(w, bufs.cfg, inp, [e for e in experts if counts[e] > 0][:3])
@@ -376,6 +437,10 @@ def check_ffn(w, inp, bufs, st, expert_subset=None) -> float:
         if hi == lo:
             continue
         exact = fn(e, rows_in[lo:hi])
+        if w.precision == "fp8_h":
+            worst = max(worst, check_close(bufs.out[lo:hi], exact, bufs.out_act, f"expert {e} output",
+                                           tol=TOL[w.act], extra=fp8_h_budget(w, inp, e, rows_in[lo:hi])))
+            continue
         worst = max(worst, check_close(bufs.out[lo:hi], exact, bufs.out_act, f"expert {e} output",
                                        tol=TOL[w.act]))
     return worst
@@ -512,7 +577,7 @@ def chain(w, inp, cfg) -> StageBuffers:
 def run_layer(cfg, inp, w, device="cuda"):
     ws = abi.workspace(cfg, device)
     y = torch.full((w.T, w.d), float("nan"), dtype=w.torch_act, device=device)
-    abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), api_w13(cfg, inp), inp.get("W2"), y, ws)
+    abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], inp.get("bias"), api_w13(cfg, inp), api_w2(cfg, inp), y, ws)
     view = abi.moe_workspace_get_view(cfg, ws)
     flags = abi.moe_read_status(view.status)
     return y, ws, view, flags

@@ -173,7 +173,9 @@ def test_workspace_sizes_and_layout():
         assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
         small_router = w.E <= 32 and w.d * w.E * 4 <= 128 * 1024  # one fused router launch instead of two
         assert abi.moe_kernels_per_forward(c) == ((6 if w.expert == "identity" else 8) + (5 if w.dedup else 0)
-                                                  + (1 if w.dispatch_dtype == "fp8" else 0) - (1 if small_router else 0))
+                                                  + (1 if w.dispatch_dtype == "fp8" else 0)
+                                                  + (1 if w.precision == "fp8_h" else 0)  # h quantized between GEMMs
+                                                  - (1 if small_router else 0))
 
 
 def test_entry_points_reject_bad_arguments_on_the_host():
@@ -345,3 +347,34 @@ def test_fp8_gemm_validation_workspace_and_weight_bytes():
     # the row-scaled format feeds the FP8 GEMM directly: no bf16 rows to write
     assert lib.moe_dispatch_fp8(ctypes.byref(g), A16, A16, ctypes.byref(m), A16, A16, A16, A16, 1 << 20,
                                 None) == abi.MOE_ERR_ARG
+
+
+def test_fp8_h_validation_workspace_and_w2_bytes():
+    h8 = cfg(dispatch_dtype="fp8_gemm", precision="fp8_h")
+    assert abi.moe_validate_config(h8) == abi.MOE_OK
+    assert abi.moe_validate_config(cfg(precision="fp8_h")) == abi.MOE_ERR_UNSUPPORTED        # needs the FP8 up GEMM
+    assert abi.moe_validate_config(cfg(dispatch_dtype="fp8_gemm", precision="fp8_h", F=72)) == abi.MOE_ERR_ALIGN
+    assert abi.moe_validate_config(cfg(precision="fp8_h", act="f32")) == abi.MOE_OK   # fp32 ignores the mode
+    assert abi.out_dtype(h8) == torch.float32 and abi.hidden_cols(h8) == 64
+    g = cfg(dispatch_dtype="fp8_gemm")
+    assert abi.moe_kernels_per_forward(h8) == abi.moe_kernels_per_forward(g) + 1
+    # W2 buffer: N*d*F codes, the next 256-byte boundary, N*d fp32 scales
+    assert abi.moe_fp8_w2_bytes(h8) == (8 * 128 * 64 + 255) // 256 * 256 + 4 * 8 * 128
+    assert abi.moe_fp8_w2_bytes(g) == 0
+    # the FFN workspace holds h's codes and scales after the status word
+    rows = 64 * 2
+    assert abi.moe_ffn_workspace_bytes(h8) >= 256 + rows * 64 + rows * 4
+    assert abi.moe_ffn_workspace_bytes(g) == 256
+    v = abi.moe_workspace_view()
+    base = 1 << 40
+    n = abi.moe_workspace_bytes(h8)
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(h8), base, n, ctypes.byref(v)) == 0
+    assert v.hq and v.hscale and v.hscale - v.hq >= rows * 64 and base + n - v.hscale >= rows * 4
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(g), base, abi.moe_workspace_bytes(g), ctypes.byref(v)) == 0
+    assert not v.hq and not v.hscale
+    lib = abi.lib()
+    assert lib.moe_quantize_w2_fp8(ctypes.byref(g), A16, A16, None) == abi.MOE_ERR_ARG
+    assert lib.moe_quantize_w2_fp8(ctypes.byref(h8), MIS, A16, None) == abi.MOE_ERR_ALIGN
+    assert lib.moe_expert_ffn_fp8(ctypes.byref(h8), A16, A16, A16, A16, A16, A16, A16, A16, 256,
+                                  None) == abi.MOE_ERR_WORKSPACE
+

@@ -18,8 +18,8 @@ from routing_dispatch_combine_moe_b300 import abi
 from routing_dispatch_combine_moe_b300 import workloads as wl
 from tests._gpu import (StageBuffers, WorkspaceMap, capacity_of, chain, check_chained_dispatch, check_close,
                         check_combine, check_dedup, check_dispatch, check_ffn, check_fp8, check_route, cpu,
-                        gate_boundary_ties, half_ulp, oracle_dispatch, oracle_route, rms, route_tie_flags,
-                        run_layer)
+                        fp8_h_budget, fp8_h_layer_budget, gate_boundary_ties, half_ulp, oracle_dispatch,
+                        oracle_route, rms, route_tie_flags, run_layer)
 from tests._harness import expert_fn, f64, run_oracle
 
 pytestmark = pytest.mark.gpu
@@ -44,6 +44,8 @@ REDUCED = {
     "decode_fp8_gemm": wl.scaled(W["dsv3_decode"], d=1072, F=256, dispatch_dtype="fp8_gemm"),
     "relu_fp8_gemm": wl.Workload("relu_fp8_gemm", T=300, d=512, E=6, k=2, F=448, act="bf16", expert="relu",
                                  dispatch_dtype="fp8_gemm"),
+    "mixtral_fp8_experts": wl.scaled(W["mixtral_fp8_experts"], T=512, d=1024, F=1536),
+    "decode_fp8_experts": wl.scaled(W["dsv3_decode"], d=1072, F=272, dispatch_dtype="fp8_gemm", precision="fp8_h"),
 }
 
 
@@ -100,7 +102,8 @@ def test_layer_forward_matches_oracle(name):
     assert flags == 0
     ref = run_oracle(w, inp)
     keep = layer_keep(w, ref, capacity_of(cfg))
-    err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{name} layer y")
+    extra = fp8_h_layer_budget(w, inp, ref)[keep] if w.precision == "fp8_h" else None
+    err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{name} layer y", extra=extra)
     print(f"\n{name}: layer max|err|/rms(y) = {err:.4f} (near-tie tokens excluded: {int((~keep).sum())})")
     if w.expert == "identity":
         assert torch.equal(y, inp["x"]), "identity experts must return x exactly"
@@ -299,26 +302,31 @@ def test_traced_forward_matches_and_times():
 # ------------------------------------------------------------------ full sizes, sampled
 def _sampled_y(w, inp, ref_route, disp, tokens):
     """Oracle y for a few tokens from the full-batch routing and dispatch (drops included);
-    with the FP8 dispatch routed experts see the dequantized rows."""
+    with the FP8 dispatch routed experts see the dequantized rows. Also returns the FP8
+    hidden-activation budget of those tokens (zeros unless the precision is fp8_h)."""
     x = f64(inp["x"][torch.as_tensor(tokens, device="cuda")])
     xq = orc.quantize_fp8_blocks(x)["deq"] if w.dispatch_dtype == "fp8" else x
     fp8_gemm = w.dispatch_dtype == "fp8_gemm"
     if fp8_gemm:  # every row, shared ones too, is the row-quantized token
         x = xq = orc.quantize_fp8_rows(x)["deq"]
     idx, G, pos = ref_route["idx"], ref_route["G"], disp["pos"].reshape(w.T, w.slots)
-    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm)
+    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm, fp8_h=w.precision == "fp8_h")
     need = {}
     for r, t in enumerate(tokens):
         for j in range(w.slots):
             if pos[t, j] >= 0:
                 need.setdefault(int(idx[t, j]), []).append((r, j))
     y = np.zeros((len(tokens), w.d))
+    budget = np.zeros_like(y)
     for e, uses in need.items():
         rows = np.array([r for r, _ in uses])
-        outs = fn(e, (xq if e < w.E else x)[rows])
-        for (r, j), o in zip(uses, outs):
+        xin = (xq if e < w.E else x)[rows]
+        outs = fn(e, xin)
+        b = fp8_h_budget(w, inp, e, xin) if w.precision == "fp8_h" else np.zeros_like(outs)
+        for (r, j), o, bo in zip(uses, outs, b):
             y[r] += G[tokens[r], j] * o
-    return y
+            budget[r] += G[tokens[r], j] * bo
+    return y, budget
 
 
 FULL = {n: W[n] for n in ["mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode"]}
@@ -327,6 +335,7 @@ FULL["dsv3_grouped_dedup"] = W["dsv3_grouped_dedup"]
 FULL["mixtral_fp8_dispatch"] = W["mixtral_fp8_dispatch"]
 FULL["mixtral_fp8_gemm"] = W["mixtral_fp8_gemm"]
 FULL["dsv3_decode_fp8_gemm"] = W["dsv3_decode_fp8_gemm"]
+FULL["mixtral_fp8_experts"] = W["mixtral_fp8_experts"]
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -372,8 +381,10 @@ def test_full_size_sampled(name):
         nz = np.nonzero(counts)[0]
         pick = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])]), int(nz[len(nz) // 2]),
                        int(nz[0])})
+        if w.precision == "fp8_h":  # the code-flip budget costs a second pass per expert: two experts
+            pick = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])})
         fp8_gemm = w.dispatch_dtype == "fp8_gemm"
-        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm)
+        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm, fp8_h=w.precision == "fp8_h")
         worst_ffn = 0.0
         for e in pick:
             lo = int(d["offsets"][e])
@@ -384,7 +395,9 @@ def test_full_size_sampled(name):
                 xin = orc.quantize_fp8_blocks(xin)["deq"]
             if fp8_gemm:
                 xin = orc.quantize_fp8_rows(xin)["deq"]
-            worst_ffn = max(worst_ffn, check_close(m.out[lo:hi], fn(e, xin), m.out_act, f"expert {e}", tol=2e-2))
+            extra = fp8_h_budget(w, inp, e, xin) if w.precision == "fp8_h" else None
+            worst_ffn = max(worst_ffn, check_close(m.out[lo:hi], fn(e, xin), m.out_act, f"expert {e}", tol=2e-2,
+                                                   extra=extra))
     # end to end on sampled tokens from the oracle's own routing and dispatch: no near
     # tie, no gate at a keep cutoff, and (with a capacity) no expert shared with a
     # token whose routing flipped
@@ -400,8 +413,8 @@ def test_full_size_sampled(name):
     rng = np.random.default_rng(0)
     cand = np.nonzero(ok)[0]
     tokens = sorted(rng.choice(cand, size=min(8, cand.size), replace=False).tolist())
-    y_s = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
-    err = check_close(y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y")
+    y_s, budget = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
+    err = check_close(y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y", extra=budget)
     print(f"\n{name}: near-ties={r['near_ties']} flipped={r['flipped']} dispatch={how} ffn_err/rms={worst_ffn} "
           f"sampled y err/rms={err:.4f} dropped={d['n_dropped']}")
 
