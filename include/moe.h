@@ -448,8 +448,9 @@ const char* moe_last_cuda_error(void);
 /* Name of the kernel moe_expert_ffn / moe_layer_forward run for this config's
  * expert GEMMs ("" for identity experts or an invalid config): the fp32 FMA
  * kernel, or one of the three tcgen05 variants (one SM per 128x256 tile, SM pairs
- * on 256-row tiles, SM pairs with swapped operands). The environment variable
- * MOE_GEMM_PAIR=0/1/2 forces a tcgen05 variant. Static storage; never freed. */
+ * on 256-row tiles, SM pairs with swapped operands); under MOE_DISPATCH_FP8_GEMM the
+ * e4m3 swapped-pair kernel of the up projection. The environment variable
+ * MOE_GEMM_PAIR=0/1/2 forces a bf16 tcgen05 variant. Static storage; never freed. */
 const char* moe_ffn_kernel_name(const moe_config* cfg);
 
 /* Environment switches (read once per process):

@@ -8,7 +8,9 @@
 // Four launches, all deterministic:
 //   1. count   - per 256-assignment block, a per-expert histogram built with
 //                warp-aggregated shared-memory atomics (__match_any_sync leaders);
-//                stored expert-major, hist[e][block].
+//                stored expert-major, hist[e][block]. Skipped when the router has
+//                already counted (the layer forward: integer atomics from the top-k
+//                writers into the zeroed histogram give the same counts).
 //   2. scan    - one CTA: per expert an exclusive scan over blocks (so hist becomes
 //                "assignments of e in earlier blocks"), then block-wide scans of the
 //                kept counts (row offsets), of the dropped counts (drop-list offsets)

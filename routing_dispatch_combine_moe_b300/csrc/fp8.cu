@@ -21,7 +21,9 @@
 // accumulator). The expert weights take the same format, one scale per weight row.
 //   gather_fp8_row_kernel  one CTA per token: amax over the row, then the codes to
 //                          each kept row and the scale;
-//   quantize_rows_kernel   one warp per row of a bf16 matrix (the W13 weights).
+//   quantize_rows_kernel   one warp per row of a bf16 matrix: the W13 and W2 weights
+//                          (once), and h between the two expert GEMMs when the down
+//                          projection runs on e4m3 too.
 #include <cuda_fp8.h>
 
 #include "common.cuh"

@@ -1,5 +1,6 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05) for bf16
-// experts: the only dense contraction of the layer ("EP Math - Expert Parallelism
+// experts (and, with e4m3 rows and weights, kind::f8f6f4 on the swapped pairs for the
+// up projection and optionally the down projection): the only dense contraction of the layer ("EP Math - Expert Parallelism
 // (MoE)", "What expert parallelism actually shards": every expert is a complete FFN
 // with private weights; the gated three-matrix form is the one in "MoE Expert
 // Parallelism Sizing", "Memory residency for the same shape").

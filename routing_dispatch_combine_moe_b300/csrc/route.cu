@@ -14,7 +14,9 @@
 // products to keep the fp32 error of a long dot product near 1e-7.
 //
 // KeepTopK: k rounds of a warp arg-max over the logits held in registers, equal
-// values won by the lower expert id; slot j is the (j+1)-th largest.
+// values won by the lower expert id; slot j is the (j+1)-th largest. Inside the layer
+// forward the top-k writers also add each assignment to the dispatch's per-block
+// expert histogram (RouteCounts), so the dispatch needs no count pass.
 #include "common.cuh"
 #include "kernels.h"
 
