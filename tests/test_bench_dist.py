@@ -44,3 +44,28 @@ def test_two_gloo_ranks_take_the_slowest_rank_time():
         assert world == 2
         assert slowest == pytest.approx(2.0)
         assert value == pytest.approx(2048 * 10 * 2 / 2.0)
+
+
+def test_algorithmic_work_of_the_bf16_and_fp8_layers():
+    """The per-launch work bench.py divides by its timings: the flops of the formulas and
+    the least bytes each stage moves, in bf16 and with e4m3 rows, W13, h and W2."""
+    import bench
+    from routing_dispatch_combine_moe_b300 import workloads as wl
+    W = wl.WORKLOADS
+    T, d, E, k, F = 2048, 4096, 8, 2, 14336
+    rows = T * k
+    bf = bench.algorithmic(W["mixtral_bf16"], rows, out_bytes=4, h_cols=F)
+    assert bf["up_flops"] == 2 * rows * d * 2 * F and bf["down_flops"] == 2 * rows * F * d
+    assert bf["up_bytes"] == E * 2 * F * d * 2 + rows * d * 2 + rows * F * 2
+    assert bf["down_bytes"] == E * d * F * 2 + rows * F * 2 + rows * d * 4
+    assert bf["combine_bytes"] == rows * d * 4 + T * d * 2
+    f8 = bench.algorithmic(W["mixtral_fp8_gemm"], rows, out_bytes=4, h_cols=F)
+    assert f8["up_flops"] == bf["up_flops"] and f8["down_bytes"] == bf["down_bytes"]
+    # e4m3 W13 with one scale per row, rows as d codes + one scale, h still bf16
+    assert f8["up_bytes"] == E * 2 * F * (d + 4) + rows * (d + 4) + rows * F * 2
+    # the dispatch writes codes + a scale per row instead of bf16 rows
+    assert f8["dispatch_bytes"] - bf["dispatch_bytes"] == rows * (d + 4) - rows * d * 2
+    both = bench.algorithmic(W["mixtral_fp8_experts"], rows, out_bytes=4, h_cols=F)
+    # the down stage reads bf16 h, writes and reads its codes + scales, reads e4m3 W2
+    assert both["down_bytes"] == E * d * (F + 4) + rows * F * 2 + 2 * rows * (F + 4) + rows * d * 4
+    assert bench.fp8_row_bytes(4096) == 4096 + 4 * 32 and bench.fp8_row_bytes(4096, per_row=True) == 4100
