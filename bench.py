@@ -240,7 +240,7 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
     Wg, bias = f64(inp["Wg"]), f64(inp.get("bias"))
     cache = {} if cache is None else cache
     fn = expert_fn(w.expert, inp.get("W13"), inp.get("W2"), w.F, cache=cache,
-                   fp8_up=w.dispatch_dtype == "fp8_gemm")
+                   fp8_up=w.dispatch_dtype == "fp8_gemm", fp8_h=w.precision == "fp8_h")
     grouped = 0 < w.topk_groups < w.n_groups
     if w.expert != "identity":  # model load: the experts this sample uses, converted once
         H = orc.router_logits(x, Wg, bias)
