@@ -190,6 +190,10 @@ typedef struct moe_workspace_view {
                           * row scales (MOE_DISPATCH_FP8_GEMM); NULL for MOE_DISPATCH_ACT */
     uint8_t* hq;         /* [rows, F] e4m3 codes of h (MOE_PRECISION_FP8_H only, else NULL) */
     float* hscale;       /* [rows] their row scales (MOE_PRECISION_FP8_H only, else NULL) */
+    int32_t* n_near_ties; /* one int the forward's router writes: tokens whose k-th and (k+1)-th
+                           * largest selectable fp32 logits differ by less than 1e-6 of the larger
+                           * magnitude (a near tie, where another valid rounding of the logits could
+                           * select other experts) */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -421,8 +425,9 @@ int moe_layer_forward_host_async(const moe_config* cfg, const void* x_host, cons
  * library, which every GPU that loads the library keeps until the process exits.
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
  * routine) and returns MOE_ERR_WORKSPACE when a config needs more scratch than that.
- * The first call on a device looks up the array's device address on that device
- * (cudaGetSymbolAddress, with the device current); make that first call before any
+ * The first call in each device context looks up the array's device address there
+ * (cudaGetSymbolAddress, with the device current): once per device, and once more if
+ * cudaDeviceReset re-creates the device's context; make that first call before any
  * stream capture. All calls share the one array: calls that may overlap on the GPU
  * (other streams, other threads) race and must be serialised by the caller. Expert
  * ids outside [0, E) are skipped, as in moe_dispatch, but there is no status word to

@@ -68,7 +68,7 @@ class moe_send_map(ctypes.Structure):
 class moe_workspace_view(ctypes.Structure):
     _fields_ = [("status", _p), ("topk_idx", _p), ("topk_gate", _p), ("map", moe_dispatch_map),
                 ("xperm", _p), ("h", _p), ("out", _p), ("send", moe_send_map), ("xsend", _p), ("xq", _p),
-                ("xscale", _p), ("hq", _p), ("hscale", _p)]
+                ("xscale", _p), ("hq", _p), ("hscale", _p), ("n_near_ties", _p)]
 
 
 _SIGNATURES = {
@@ -265,6 +265,7 @@ class WorkspaceView:
     xscale: int | None = None
     hq: int | None = None
     hscale: int | None = None
+    n_near_ties: int | None = None
 
 
 def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
@@ -276,7 +277,7 @@ def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
     return WorkspaceView(v.status, v.topk_idx, v.topk_gate, m.counts_routed, m.counts_kept, m.offsets,
                          m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out,
                          sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend, v.xq, v.xscale,
-                         v.hq, v.hscale)
+                         v.hq, v.hscale, v.n_near_ties)
 
 
 # ------------------------------------------------------------------ hot path

@@ -11,9 +11,10 @@
 // cudaMalloc, cudaFree or allocating library routine.
 //
 // Host code cannot use the array's name as a device address (in host code it
-// names a host-side stand-in), so the device address is looked up once per device
-// with cudaGetSymbolAddress, with that device current, on the first call made on
-// it; that first call should therefore come before any stream capture.
+// names a host-side stand-in), so the device address is looked up with
+// cudaGetSymbolAddress on the first call made in each device context (once per
+// device, with that device current, and again if cudaDeviceReset re-creates the
+// context); that first call should therefore come before any stream capture.
 #include <mutex>
 #include <string>
 
@@ -29,25 +30,20 @@ constexpr size_t kStaticScratchInts = MOE_STATIC_SCRATCH_BYTES / sizeof(int32_t)
 // offsets and (gate drop policy) the T*K per-expert assignment list.
 __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
+// Device address of g_dispatch_scratch in the current context, looked up once per
+// context: once per device, and again after a cudaDeviceReset re-creates the device's
+// context (the module, and with it the array, is then loaded anew).
+PerContext<int32_t*> g_scratch_addr;
 
-// Device address of g_dispatch_scratch on the current device, looked up once.
 cudaError_t scratch_address(int32_t** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<int32_t*>(p);
-    }
-    *out = g_scratch_addr[dev];
-    return cudaSuccess;
+    const cudaError_t e = g_scratch_addr.get(out, [](int32_t** p) {
+        void* q = nullptr;
+        const cudaError_t err = cudaGetSymbolAddress(&q, g_dispatch_scratch);
+        *p = static_cast<int32_t*>(q);
+        return err;
+    });
+    if (e == cudaSuccess && !*out) return cudaErrorInvalidSymbol;
+    return e;
 }
 
 }  // namespace

@@ -881,11 +881,8 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const Pa
                           cudaStream_t stream) {
     auto kern = grouped_gemm_kernel<MODE, OUT, PAIR>;
     constexpr size_t smem = smem_bytes<PAIR>();
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    });
+    static PerContext<int> smem_set;
+    const cudaError_t attr_err = set_smem_limit_once(smem_set, kern, smem);
     if (attr_err != cudaSuccess) return attr_err;
     if constexpr (PAIR) {
         cudaLaunchConfig_t cfg = {};
@@ -901,12 +898,12 @@ cudaError_t launch_kernel(const CUtensorMap& mA, const CUtensorMap& mB, const Pa
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         // The grid is persistent: never launch more pairs than can be resident at once.
-        static int max_clusters = -1;
-        if (max_clusters < 0) {
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = device_sm_count() / 2;
-            max_clusters = n;
-        }
+        static PerContext<int> resident;
+        int max_clusters = 0;
+        resident.get(&max_clusters, [&](int* n) {
+            if (cudaOccupancyMaxActiveClusters(n, kern, &cfg) != cudaSuccess || *n <= 0) *n = device_sm_count() / 2;
+            return cudaSuccess;
+        });
         if (int(cfg.gridDim.x) > 2 * max_clusters) cfg.gridDim.x = unsigned(2 * max_clusters);
         return cudaLaunchKernelEx(&cfg, kern, mA, mB, p);
     } else {
@@ -952,11 +949,8 @@ cudaError_t launch_swap(const CUtensorMap& mW, const RowMaps& mX, const Params& 
                         int64_t rows_max, int E, cudaStream_t stream) {
     auto kern = grouped_gemm_swap_kernel<MODE, OUT, F8>;
     constexpr size_t smem = swap_smem_bytes();
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    });
+    static PerContext<int> smem_set;
+    const cudaError_t attr_err = set_smem_limit_once(smem_set, kern, smem);
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t tiles = ((rows_max + SW_TILE_N - 1) / SW_TILE_N + E) * int64_t(p.n_tiles);
     cudaLaunchConfig_t cfg = {};
@@ -971,13 +965,13 @@ cudaError_t launch_swap(const CUtensorMap& mW, const RowMaps& mX, const Params& 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // Persistent grid: never more pairs than can be resident at once.
-    static int max_clusters = -1;
-    if (max_clusters < 0) {
-        cfg.gridDim = dim3(2);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = device_sm_count() / 2;
-        max_clusters = n;
-    }
+    static PerContext<int> resident;
+    int max_clusters = 0;
+    cfg.gridDim = dim3(2);
+    resident.get(&max_clusters, [&](int* n) {
+        if (cudaOccupancyMaxActiveClusters(n, kern, &cfg) != cudaSuccess || *n <= 0) *n = device_sm_count() / 2;
+        return cudaSuccess;
+    });
     const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
     cfg.gridDim = dim3(unsigned(2 * (pairs > 0 ? pairs : 1)));
     return cudaLaunchKernelEx(&cfg, kern, mW, mX, p);

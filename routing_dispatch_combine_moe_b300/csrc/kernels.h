@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace moe {
 
 // Assignments per dispatch block: the histogram, scan and scatter kernels all cut
@@ -30,10 +32,12 @@ inline size_t route_scratch_bytes_max(int T, int E) {
 // experts E..E+n_shared-1 with gate 1. With 0 < topk_groups < n_groups the selection
 // is limited to the topk_groups best of n_groups contiguous expert groups. A non-null
 // hist (zeroed, [(E + n_shared) * dispatch_blocks(T * (k + n_shared))]) receives the
-// dispatch's per-block expert counts, so the dispatch can skip its count kernel.
+// dispatch's per-block expert counts, so the dispatch can skip its count kernel. A
+// non-null near_ties (one zeroed int) receives the number of tokens whose k-th and
+// (k+1)-th largest selectable fp32 logits differ by less than 1e-6 relative.
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
-                         float* scratch, int32_t* hist, cudaStream_t stream);
+                         float* scratch, int32_t* hist, int32_t* near_ties, cudaStream_t stream);
 
 struct DispatchArgs {
     int T, d, E, k, D;  // E: all experts (routed + shared), k: all slots per token
@@ -155,5 +159,56 @@ cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t stream, cudaEvent_t m
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
+
+// Key of the CUDA context current on this thread: the driver's unique context id
+// (a context re-created after cudaDeviceReset gets a new one), or the device index
+// with the top bit set where the driver does not report ids.
+uint64_t current_context_key();
+
+// A value set up once per CUDA context and then reused: kernel attributes, occupancy
+// figures and module symbol addresses belong to the context they were made in, so a
+// second device, or a context re-created after a reset, sets up its own. `make`
+// returns the setup's cudaError_t, which is cached with the value. Thread-safe.
+template <typename T>
+class PerContext {
+public:
+    template <typename Make>
+    cudaError_t get(T* out, Make&& make) {
+        const uint64_t key = current_context_key();
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < n_; ++i)
+            if (keys_[i] == key) {
+                *out = vals_[i];
+                return errs_[i];
+            }
+        T v{};
+        const cudaError_t e = make(&v);
+        if (n_ < kSlots) {  // beyond kSlots contexts the setup simply runs on every call
+            keys_[n_] = key;
+            vals_[n_] = v;
+            errs_[n_] = e;
+            ++n_;
+        }
+        *out = v;
+        return e;
+    }
+
+private:
+    static constexpr int kSlots = 64;
+    std::mutex mu_;
+    int n_ = 0;
+    uint64_t keys_[kSlots] = {};
+    T vals_[kSlots] = {};
+    cudaError_t errs_[kSlots] = {};
+};
+
+// Raises a kernel's dynamic shared-memory limit once per context.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(PerContext<int>& cache, Kernel kern, size_t bytes) {
+    int unused = 0;
+    return cache.get(&unused, [&](int*) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    });
+}
 
 }  // namespace moe

@@ -26,6 +26,35 @@ int device_sm_count() {
     return cache[dev];
 }
 
+uint64_t current_context_key() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const uint64_t fallback = (uint64_t(1) << 63) | uint64_t(uint32_t(dev));
+    if (!get_current || !get_id) return fallback;
+    // No context current yet (nothing has touched the device on this thread): the
+    // device key stands in; the setup that follows makes the primary context current.
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return fallback;
+    return uint64_t(id) & ~(uint64_t(1) << 63);
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -119,7 +148,7 @@ int validate(const moe_config* c) {
 }
 
 struct Layout {
-    size_t status, hist, drop_offsets, routed_offsets, elist, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
+    size_t status, near_ties, hist, drop_offsets, routed_offsets, elist, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
         n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
     // deduplicated dispatch (cfg->dedup): scratch in the dispatch part, outputs in the forward part
     size_t dd_slots, dd_hist, dd_kept, dd_drop, dd_routed, dd_rank, dd_ndrop;
@@ -142,6 +171,7 @@ Layout layout(const moe_config* c) {
         return at;
     };
     L.status = take(sizeof(int32_t));
+    L.near_ties = take(sizeof(int32_t));
     L.hist = take(sizeof(int32_t) * size_t(N) * nblk);
     L.drop_offsets = take(sizeof(int32_t) * size_t(N));
     L.routed_offsets = take(sizeof(int32_t) * size_t(N + 1));
@@ -226,6 +256,7 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->xscale = f8 ? at<float>(ws, L.xscale) : nullptr;
     v->hq = fp8_h(c) ? at<uint8_t>(ws, L.hq) : nullptr;
     v->hscale = fp8_h(c) ? at<float>(ws, L.hscale) : nullptr;
+    v->n_near_ties = at<int32_t>(ws, L.near_ties);
 }
 
 // Standalone moe_expert_ffn(_fp8) workspace: the status word, then (FP8 hidden
@@ -243,9 +274,9 @@ FfnLayout ffn_layout(const moe_config* c) {
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
-              float* scratch, cudaStream_t s, int32_t* hist = nullptr) {
+              float* scratch, cudaStream_t s, int32_t* hist = nullptr, int32_t* near_ties = nullptr) {
     const cudaError_t e = launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, c->n_shared, c->n_groups,
-                                       c->topk_groups, idx, gate, scratch, hist, s);
+                                       c->topk_groups, idx, gate, scratch, hist, near_ties, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
 }
 
@@ -414,15 +445,16 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     moe_workspace_view v{};
     fill_view(c, ws, &v);
     // The router also counts each expert's assignments per dispatch block (the fused
-    // route + count): one memset clears the status word and that histogram, which
-    // follow each other at the start of the workspace.
+    // route + count) and the near-tie tokens: one memset clears the status word, the
+    // near-tie count and that histogram, which follow each other at the start of the
+    // workspace.
     const size_t hist_end = L.hist + sizeof(int32_t) * size_t(n_experts(c)) *
                                          size_t(dispatch_blocks(int64_t(c->T) * n_slots(c)));
     cudaError_t e = cudaMemsetAsync(ws, 0, hist_end, s);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status, histogram)");
     if ((rc = record(events, n_events, 0, s)) != MOE_OK) return rc;
     if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s,
-                        at<int32_t>(ws, L.hist))) != MOE_OK)
+                        at<int32_t>(ws, L.hist), v.n_near_ties)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
     const bool f8 = fp8_blocks(c) || fp8_gemm(c);

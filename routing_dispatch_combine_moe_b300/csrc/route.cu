@@ -48,14 +48,24 @@ struct Act16<__nv_bfloat16> {
 // The dispatch histogram the layer forward has the router fill: hist[e * nblk + b]
 // counts the assignments of expert e among assignments [256 b, 256 (b + 1)) (the count
 // kernel's blocks), zeroed beforehand; integer atomics, so the counts do not depend on
-// their order. A null hist leaves the counting to the dispatch.
+// their order. A null hist leaves the counting to the dispatch. A non-null near_ties
+// (zeroed beforehand) counts the tokens whose k-th and (k+1)-th largest selectable
+// logits are a near tie (see is_near_tie).
 struct RouteCounts {
     int32_t* hist;
     int nblk;
+    int32_t* near_ties;
 };
 
 __device__ __forceinline__ void count_assignment(const RouteCounts c, int e, int64_t a) {
     if (c.hist) atomicAdd(c.hist + size_t(e) * c.nblk + size_t(a / kDispatchBlock), 1);
+}
+
+// A near tie of the selection: the k-th largest logit vk and the (k+1)-th vn (-inf
+// when there is none) differ by less than 1e-6 of the larger magnitude, so another
+// rounding of the logits could select a different set of experts.
+__device__ __forceinline__ bool is_near_tie(float vk, float vn) {
+    return (vk - vn) < 1e-6f * fmaxf(fabsf(vk), fabsf(vn));
 }
 
 // Top-k of the logits held by a warp (lane l holds experts l + 32 m, m < VPL, with
@@ -85,6 +95,15 @@ __device__ __forceinline__ void topk_softmax_store(float (&v)[VPL], int lane, in
 #pragma unroll
         for (int m = 0; m < VPL; ++m)
             if (lane + 32 * m == bi) v[m] = -INFINITY;
+    }
+    if (cnt.near_ties) {  // the (k+1)-th largest: one more arg-max round, value only
+        float nv = -INFINITY;
+#pragma unroll
+        for (int m = 0; m < VPL; ++m) nv = fmaxf(nv, v[m]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) nv = fmaxf(nv, __shfl_xor_sync(0xFFFFFFFFu, nv, off));
+        const float vk = __shfl_sync(0xFFFFFFFFu, my_val, k - 1);
+        if (lane == 0 && is_near_tie(vk, nv)) atomicAdd(cnt.near_ties, 1);
     }
     const float vmax = __shfl_sync(0xFFFFFFFFu, my_val, 0);
     const float ex = (lane < k) ? expf(my_val - vmax) : 0.f;
@@ -381,6 +400,13 @@ __device__ __forceinline__ void topk_softmax_thread(float (&v)[EB], int E, int k
         val[j] = bv;
         id[j] = bi;
     }
+    if (cnt.near_ties) {  // the (k+1)-th largest of the logits not taken
+        float nv = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < EB; ++e)
+            if (e < E && !((taken >> e) & 1u)) nv = fmaxf(nv, v[e]);
+        if (is_near_tie(val[k - 1], nv)) atomicAdd(cnt.near_ties, 1);
+    }
     float ex[MOE_MAX_K];
     float sum = 0.f;
     for (int j = 0; j < k; ++j) {
@@ -483,11 +509,8 @@ cudaError_t launch_small(const void* x, const float* Wg, const float* bias, int 
                          int G, int M, int32_t* idx, float* gate, const RouteCounts cnt, cudaStream_t stream) {
     auto kern = route_small_kernel<TAct, EB>;
     constexpr size_t max_smem = size_t(kSmallRouteWBytes) + sizeof(float) * 16 * 16 * (EB + 1);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(max_smem));
-    });
+    static PerContext<int> smem_set;
+    const cudaError_t attr_err = set_smem_limit_once(smem_set, kern, max_smem);
     if (attr_err != cudaSuccess) return attr_err;
     const size_t smem = sizeof(float) * (size_t(d) * E + 16 * 16 * (EB + 1));
     const bool wvec = E == EB && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;
@@ -512,11 +535,8 @@ cudaError_t launch_gemm(const void* x, const float* Wg, int T, int d, int E, int
                         cudaStream_t stream) {
     using G = GemmShape<WE>;
     auto kern = route_gemm_kernel<TAct, WE>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::smem));
-    });
+    static PerContext<int> smem_set;
+    const cudaError_t attr_err = set_smem_limit_once(smem_set, kern, G::smem);
     if (attr_err != cudaSuccess) return attr_err;
     const dim3 grid((T + G::TT - 1) / G::TT, (E + G::TE - 1) / G::TE, ks);
     kern<<<grid, 256, G::smem, stream>>>(static_cast<const TAct*>(x), Wg, T, d, E, slice, scratch);
@@ -576,8 +596,8 @@ bool route_uses_small_kernel(int d, int E) { return E <= 32 && int64_t(d) * E * 
 
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
-                         float* scratch, int32_t* hist, cudaStream_t stream) {
-    const RouteCounts cnt{hist, dispatch_blocks(int64_t(T) * (k + n_shared))};
+                         float* scratch, int32_t* hist, int32_t* near_ties, cudaStream_t stream) {
+    const RouteCounts cnt{hist, dispatch_blocks(int64_t(T) * (k + n_shared)), near_ties};
     if (route_uses_small_kernel(d, E))
         return act_dtype == MOE_F32
                    ? launch_small_t<float>(x, Wg, bias, T, d, E, k, n_shared, n_groups, topk_groups, topk_idx,
