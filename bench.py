@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one moe_layer_forward over one batch of the workload (default: the
-Mixtral-shaped bf16 layer, T=2048, d=4096, E=8, k=2, SwiGLU F=14336), inputs and
-weights resident in HBM, timed with CUDA events on the launching stream. Under
+DeepSeek-V3-shaped bf16 layer, T=4096, d=7168, E=256 routed experts, k=8, SwiGLU
+F=2048, 22.5 GB of expert weights), inputs and weights resident in HBM, timed with
+CUDA events on the launching stream. Under
 torchrun each rank runs an independent replica on its own GPU (the layer needs no
 cross-GPU exchange on one device; see the design notes), so the job processes
 N * T tokens per step and the step time is the max over ranks.
@@ -36,9 +37,10 @@ from routing_dispatch_combine_moe_b300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE-layer tokens/s"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "mixtral_bf16"
+DEFAULT_WORKLOAD = "dsv3_full"
 STAGES = ["route", "dispatch", "expert_up", "expert_down", "combine"]
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_FLUSH_BYTES = 256 << 20  # twice the 126 MB L2
 
 
 # ------------------------------------------------------------------ distributed
@@ -217,7 +219,11 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
         route_flops=sizing.router_flops(w.T, w.d, w.E),
         route_bytes=w.T * w.d * b + w.d * w.E * 4 + w.T * w.slots * 8,
         dispatch_bytes=dispatch,
-        combine_bytes=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
+        # the combine's algorithmic bytes: every kept expert row read once in the
+        # activation dtype, y written once; with fp32 expert outputs it moves rows * d
+        # * 4 instead (combine_bytes_moved)
+        combine_bytes=rows * w.d * b + w.T * w.d * b,
+        combine_bytes_moved=rows * w.d * (b if ident else out_bytes) + w.T * w.d * b,
         up_flops=up, down_flops=down,
         up_bytes=0 if ident else w13_bytes + up_in + rows * h_cols * b,
         down_bytes=0 if ident else w2_bytes + down_in + rows * w.d * out_bytes,
@@ -225,11 +231,14 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
+def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None, threads: int | None = None,
+                        cache_budget: float = 16e9) -> dict:
     """Times the float64 oracle on `tokens` tokens of the workload.
 
     Expert weights are converted to float64 once ("model load", untimed) and kept in
-    `cache` across calls.
+    `cache` across calls; experts this sample does not use are dropped from the cache
+    first whenever it holds more than `cache_budget` bytes. `threads` limits the BLAS
+    thread pools (None: all host cores).
     """
     from oracle import moe_oracle as orc  # the timed CPU baseline is the oracle, as it stands
     from oracle.packed import expert_fn, f64
@@ -245,18 +254,35 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None) -> dict:
     if w.expert != "identity":  # model load: the experts this sample uses, converted once
         H = orc.router_logits(x, Wg, bias)
         idx = orc.keep_topk_grouped(H, w.k, w.n_groups, w.topk_groups) if grouped else orc.keep_topk(H, w.k)
-        for e in list(np.unique(idx)) + list(range(w.E, w.n_experts)):
-            fn(int(e), np.zeros((1, w.d)))
+        need = [int(e) for e in np.unique(idx)] + list(range(w.E, w.n_experts))
+        per_expert = (w.w13_rows + w.F) * w.d * 8
+        if len(cache) * per_expert > cache_budget:
+            for e in [e for e in cache if e not in set(need)]:
+                del cache[e]
+        for e in need:
+            fn(e, np.zeros((1, w.d)))
     cap = orc.expert_capacity(len(sel), w.k, w.E, w.capacity_factor, w.min_capacity)
-    t0 = time.perf_counter()
-    res = orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D, n_shared=w.n_shared,
-                          drop_policy=w.drop_policy, layout=w.layout, n_groups=w.n_groups,
-                          topk_groups=w.topk_groups, dispatch_dtype=w.dispatch_dtype)
-    if w.dedup:
-        orc.dedup_send(res["idx"], res["pos"], w.E, w.D)
-    dt = time.perf_counter() - t0
-    threads = cpu_threads()
-    return dict(value=len(sel) / dt, seconds=dt, tokens=len(sel), cores=threads)
+
+    def run():
+        res = orc.moe_forward(x, Wg, w.k, fn, capacity=cap, bias=bias, D=w.D, n_shared=w.n_shared,
+                              drop_policy=w.drop_policy, layout=w.layout, n_groups=w.n_groups,
+                              topk_groups=w.topk_groups, dispatch_dtype=w.dispatch_dtype)
+        if w.dedup:
+            orc.dedup_send(res["idx"], res["pos"], w.E, w.D)
+
+    if threads is None:
+        t0 = time.perf_counter()
+        run()
+        dt = time.perf_counter() - t0
+        used = cpu_threads()
+    else:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=threads):
+            t0 = time.perf_counter()
+            run()
+            dt = time.perf_counter() - t0
+            used = cpu_threads()
+    return dict(value=len(sel) / dt, seconds=dt, tokens=len(sel), cores=used)
 
 
 def cpu_threads() -> int:
@@ -268,7 +294,7 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_sample_tokens(w, max_tokens: int = 2048, mem_budget: float = 24e9) -> int:
+def oracle_sample_tokens(w, max_tokens: int = 2048, mem_budget: float = 16e9) -> int:
     """Tokens per oracle sample, bounded so the float64 copies of the experts it touches fit mem_budget."""
     if w.expert == "identity":
         return min(w.T, max_tokens)
@@ -312,6 +338,7 @@ def run_ours(args, w, world, rank, local):
     counts = ws[view.counts_routed - base:view.counts_routed - base + 4 * w.E].view(torch.int32).cpu().numpy()
     kept = ws[view.counts_kept - base:view.counts_kept - base + 4 * N].view(torch.int32).cpu().numpy()
     n_dropped = int(ws[view.n_dropped - base:view.n_dropped - base + 4].view(torch.int32).cpu()[0])
+    near_ties = int(ws[view.n_near_ties - base:view.n_near_ties - base + 4].view(torch.int32).cpu()[0])
     rows = int(kept.sum())          # rows holding an assignment: the algorithmic work
     rows_computed = int(offs[-1])   # rows the expert GEMMs run over (padding included)
 
@@ -319,7 +346,13 @@ def run_ours(args, w, world, rank, local):
     for ev in events:  # materialise the event handles before timing
         for e in ev:
             e.record(stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device) if args.cold_l2 else None
     torch.cuda.synchronize()
+
+    def timed_step(i):
+        if flush is not None:  # overwrite twice the L2 before the step, outside its events
+            flush.fill_(float(i))
+        step(events[i])
     # The K timed steps are captured once into a CUDA graph and replayed, so small
     # layers are not timed as CPU launch latency; eager launches if capture fails.
     graph, launch_mode = None, "eager"
@@ -328,7 +361,7 @@ def run_ours(args, w, world, rank, local):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
                 for i in range(args.steps):
-                    step(events[i])
+                    timed_step(i)
             graph.replay()  # one untimed replay of the captured steps
             torch.cuda.synchronize()
             launch_mode = "cuda_graph"
@@ -344,7 +377,7 @@ def run_ours(args, w, world, rank, local):
             graph.replay()
         else:
             for i in range(args.steps):
-                step(events[i])
+                timed_step(i)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -352,6 +385,8 @@ def run_ours(args, w, world, rank, local):
     stage_ms = {s: float(np.mean([ev[j].elapsed_time(ev[j + 1]) for ev in events])) for j, s in enumerate(STAGES)}
     # per-step times from the first to the last stage event of each step
     step_times = np.array([ev[0].elapsed_time(ev[len(STAGES)]) for ev in events])
+    if args.cold_l2:  # the flushes between steps are not the layer's time: sum the steps themselves
+        total_ms = float(step_times.sum())
     flags = abi.moe_read_status(view.status)
     max_ms = reduce_max(total_ms, world, device)
 
@@ -386,11 +421,19 @@ def run_ours(args, w, world, rank, local):
     del ws_h
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = oracle_tokens_per_s(w, inp, oracle_sample_tokens(w))
+        cache = {}
+        n_tok = oracle_sample_tokens(w)
+        r = oracle_tokens_per_s(w, inp, n_tok, cache=cache)
+        # the same oracle on one thread, on the first tokens of the same sample size
+        # scaled so that it takes about as long as the all-core run did
+        n1 = max(1, min(n_tok, int(round(n_tok / max(1, r["cores"])))))
+        r1 = oracle_tokens_per_s(w, inp, n1, cache=cache, threads=1)
         cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['tokens']} random tokens of the workload, float64 numpy oracle "
                          f"(route, dispatch, experts, combine), {r['seconds']:.2f} s; expert weights converted "
-                         f"to float64 once before timing"}
+                         f"to float64 once before timing",
+               "single_thread": {"value": r1["value"], "unit": UNIT, "cores": r1["cores"],
+                                 "sample": f"{r1['tokens']} random tokens, {r1['seconds']:.2f} s"}}
 
     if rank != 0:
         return None
@@ -416,9 +459,11 @@ def run_ours(args, w, world, rank, local):
     peaks, peak_src = load_peaks()
     value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
     dc_bytes = work["dispatch_bytes"] + work["combine_bytes"]
+    dc_moved = work["dispatch_bytes"] + work["combine_bytes_moved"]
     dc_ms = stage_ms["dispatch"] + stage_ms["combine"]
     gemm_ms = stage_ms["expert_up"] + stage_ms["expert_down"]
     gemm_flops = work["up_flops"] + work["down_flops"]
+    gemm_bytes = work["up_bytes"] + work["down_bytes"]
     # dominant kernel of the step; a GEMM is tensor-bound when its arithmetic
     # intensity (algorithmic flops / algorithmic bytes) is above the measured ridge
     # point (bf16 peak / HBM bandwidth), else HBM-bound on its weight stream
@@ -495,7 +540,9 @@ def run_ours(args, w, world, rank, local):
                    "n_groups": w.n_groups, "topk_groups": w.topk_groups, "dedup": w.dedup,
                    "dispatch_dtype": w.dispatch_dtype,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
+                   "l2": ("flushed: %d MB written between timed steps, outside the steps' events; "
+                          % (L2_FLUSH_BYTES >> 20) if args.cold_l2 else "") +
+                         "inputs larger than L2: the step streams %.2f GB of expert weights and %.0f MB of "
                          "dispatched rows" % (w.n_experts * (w.w13_rows * (1 if f8g else w.act_bytes)
                                                               + w.F * w.act_bytes) * w.d / 1e9
                                               if w.expert != "identity" else 0.0,
@@ -506,10 +553,24 @@ def run_ours(args, w, world, rank, local):
         "grouped_gemm_tflops": gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 and gemm_flops else None,
         "grouped_gemm_frac_bf16_peak": (gemm_flops / (gemm_ms / 1e3) / 1e12) / float(peaks["bf16_tflops"])
         if gemm_ms > 0 and gemm_flops else None,
+        # against what the GEMMs can reach at their arithmetic intensity: min(bf16 peak,
+        # AI x HBM bandwidth) with AI = algorithmic flops / algorithmic bytes (weights,
+        # rows in, rows out)
+        "grouped_gemm_frac_attainable": (gemm_flops / (gemm_ms / 1e3) / 1e12) /
+        min(float(peaks["bf16_tflops"]), gemm_flops / gemm_bytes * float(peaks["hbm_gbs"]) / 1e3)
+        if gemm_ms > 0 and gemm_flops and gemm_bytes else None,
+        "grouped_gemm_arith_intensity": gemm_flops / gemm_bytes if gemm_bytes else None,
+        "dispatch_combine_bytes": dc_bytes,
+        "dispatch_combine_moved": {
+            "bytes": dc_moved, "gbs": dc_moved / (dc_ms / 1e3) / 1e9 if dc_ms > 0 else None,
+            "frac_hbm": (dc_moved / (dc_ms / 1e3) / 1e9) / float(peaks["hbm_gbs"]) if dc_ms > 0 else None,
+            "why": "the bytes the kernels move: the combine reads the expert rows in their stored dtype "
+                   "(fp32 with the f32_out precision) instead of the activation dtype"},
         "stage_ms": stage_ms,
         "step_ms": {"median": float(np.median(step_times)), "p95": float(np.percentile(step_times, 95)),
                     "min": float(step_times.min()), "max": float(step_times.max())},
-        "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "dedup": dedup,
+        "routing": {"rows": rows, "rows_computed": rows_computed, "dropped": n_dropped, "near_ties": near_ties,
+                    "dedup": dedup,
                     "fp8_dispatch": fp8,
                     "group_limit": [w.topk_groups, w.n_groups] if 0 < w.topk_groups < w.n_groups else None, "hist": sizing.histogram_summary(counts),
                     "rank_imbalance": sizing.imbalance_ratio(np.diff(rank_offs)),
@@ -538,16 +599,22 @@ def run_reference(args, w, world, rank):
     per_step = []
     cache = {}
     tokens = min(args.ref_tokens, oracle_sample_tokens(w))
+    # a new token sample every step while every expert's float64 weights fit the cache;
+    # otherwise (the DeepSeek-V3 shapes) the same sample each step, so that the weights
+    # are converted once
+    fits = w.expert == "identity" or w.n_experts * (w.w13_rows + w.F) * w.d * 8 <= 16e9
     for i in range(args.warmup + args.steps):
-        r = oracle_tokens_per_s(w, inp, tokens, seed=i, cache=cache)
+        r = oracle_tokens_per_s(w, inp, tokens, seed=i if fits else 0, cache=cache)
         if i >= args.warmup:
             per_step.append(r)
     tokens = sum(r["tokens"] for r in per_step)
     secs = sum(r["seconds"] for r in per_step)
     value = tokens / secs
     cores = per_step[0]["cores"]
-    sample = (f"each step: {tokens} random tokens of the workload through the float64 numpy oracle "
-              f"(route, dispatch, experts, combine); expert weights converted to float64 once, untimed")
+    sample = (f"each step: {per_step[0]['tokens']} random tokens of the workload "
+              f"({'a new sample per step' if fits else 'the same sample every step'}) through the float64 "
+              f"numpy oracle (route, dispatch, experts, combine); expert weights converted to float64 once, "
+              f"untimed")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs / len(per_step) * 1e3, "higher_is_better": True,
@@ -569,6 +636,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--cold-l2", action="store_true",
+                    help="overwrite 256 MB (twice the L2) before every timed step, outside its events; the "
+                         "value then sums the steps' own times")
     ap.add_argument("--drop-policy", choices=["token", "gate"], default=None,
                     help="override the workload's drop policy (capacity workloads)")
     ap.add_argument("--layout", choices=["packed", "padded"], default=None,

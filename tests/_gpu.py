@@ -1,15 +1,18 @@
 """GPU-side test glue: runs the library through its C ABI and compares with the oracle.
 
 Tolerances (floating point):
-  * layer output y and expert outputs: max |gpu - exact| <= tol * rms(exact) + half an
-    ulp of the activation dtype at the exact value, tol = 2e-2 (bf16) or 1e-4 (fp32).
-    The half-ulp term is the representation error of the output format itself: no
-    result delivered in bf16 can be closer to the exact value than that, so the
-    relative tolerance is read as bounding the arithmetic (fp32 accumulation, the
-    bf16 rounding of h and of the expert outputs) on top of it.
+  * layer output y and expert outputs: max |gpu - exact| <= tol * rms(exact), tol =
+    2e-2 (bf16) or 1e-4 (fp32), as stated for the layer, with nothing added.
+  * ROUNDING_LIMITED workloads only (named below): a capacity that drops most of a
+    hot expert's assignments shrinks rms(y) while the largest surviving elements keep
+    their size, so even the correctly rounded bf16 value of the exact y is more than
+    half the budget away from it (the tests assert that this holds). There the bound
+    is tol * rms(exact) + half an ulp of bf16 at the exact value: the format's own
+    representation error on top of the arithmetic's budget.
+  * the combine stage alone (random rows and gates): tol = 1e-5 plus the half ulp of
+    y's one rounding, which checks that the sum is taken in fp32 and rounded once.
   * gates: |gpu - exact| <= 2e-6 (fp32 logits carry ~1e-7 absolute error from a
-    d-long dot product summed in 256-term pieces; exp and the division add a few
-    ulp).
+    d-long dot product summed in short pieces; exp and the division add a few ulp).
 Integer and index outputs (top-k ids away from near ties, counts, offsets, the
 permutation, drop lists, dispatched rows) are compared bit for bit.
 """
@@ -25,6 +28,12 @@ from tests._harness import expert_fn, f64
 TOL = {"bf16": 2e-2, "f32": 1e-4}
 GATE_TOL = 2e-6
 
+# Workloads whose correctly rounded bf16 output alone uses more than half of the
+# 2e-2 * rms(y) budget (capacity factor 1.25 with a Zipf(1.2)-skewed router: the hot
+# expert drops about 95% of its assignments): the Zipf workload and its gate-policy /
+# padded-layout variant, at full and reduced size.
+ROUNDING_LIMITED = {"zipf_cf125", "zipf_gate_padded"}
+
 
 def half_ulp(v: np.ndarray, act: str) -> np.ndarray:
     """Half an ulp of the activation dtype at |v| (bf16: 8 significant bits, fp32: 24)."""
@@ -39,23 +48,52 @@ def rms(v) -> float:
     return float(np.sqrt(np.mean(v * v))) if v.size else 0.0
 
 
-def check_close(got, exact, act: str, what: str, tol: float | None = None, extra=None) -> float:
-    """Asserts the float tolerance (plus a per-element ``extra`` bound, if given); returns
-    the raw max|err| / rms(exact)."""
+def rounding_limited(exact, act: str, tol: float) -> bool:
+    """Whether the correctly rounded ``act`` value of ``exact`` is already more than half
+    of tol * rms(exact) away from it somewhere."""
+    exact = np.asarray(exact, np.float64)
+    if act == "f32":
+        rounded = exact.astype(np.float32).astype(np.float64)
+    else:
+        rounded = torch.from_numpy(exact).to(torch.bfloat16).to(torch.float64).numpy()
+    return bool(np.abs(rounded - exact).max() > 0.5 * tol * rms(exact))
+
+
+def check_close(got, exact, act: str, what: str, tol: float | None = None, extra=None,
+                with_half_ulp: bool = False) -> float:
+    """Asserts max|got - exact| <= tol * rms(exact) elementwise (plus a per-element
+    ``extra`` bound, if given; plus half an ulp of ``act`` at the exact value with
+    ``with_half_ulp``, for the rounding-limited workloads and the combine-stage check);
+    returns the raw max|err| / rms(exact)."""
     tol = TOL[act] if tol is None else tol
     got = f64(got)
     exact = np.asarray(exact, np.float64)
     assert got.shape == exact.shape, (what, got.shape, exact.shape)
     r = rms(exact)
     err = np.abs(got - exact)
-    bound = tol * r + half_ulp(exact, act) + (0.0 if extra is None else np.asarray(extra, np.float64))
+    bound = tol * r + (half_ulp(exact, act) if with_half_ulp else 0.0) + \
+        (0.0 if extra is None else np.asarray(extra, np.float64))
     bad = err > bound
     assert not np.isnan(got).any(), f"{what}: NaN in GPU output"
     if bad.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)
-        raise AssertionError(f"{what}: {bad.sum()} elements beyond {tol}*rms + half-ulp; worst at {i}: "
-                             f"gpu={got[i]!r} exact={exact[i]!r} err={err[i]:.3e} bound={bound[i]:.3e} rms={r:.3e}")
+        raise AssertionError(f"{what}: {bad.sum()} elements beyond {tol}*rms{' + half-ulp' if with_half_ulp else ''}"
+                             f"; worst at {i}: gpu={got[i]!r} exact={exact[i]!r} err={err[i]:.3e} "
+                             f"bound={bound[i]:.3e} rms={r:.3e}")
     return float(err.max() / r) if r > 0 else 0.0
+
+
+def check_layer_close(name: str, got, exact, act: str, what: str, extra=None, auto: bool = False) -> float:
+    """The layer tolerance for workload ``name``: the literal bound, or (ROUNDING_LIMITED
+    workloads, whose rounding limit is asserted here) the bound plus the output half-ulp.
+    With ``auto`` (randomly drawn layers, which have no name to list) a layer takes the
+    half-ulp term exactly when its own exact output is rounding-limited."""
+    limited = name in ROUNDING_LIMITED
+    if limited:
+        assert rounding_limited(exact, act, TOL[act]), f"{name} is listed as rounding-limited but is not"
+    elif auto:
+        limited = rounding_limited(exact, act, TOL[act])
+    return check_close(got, exact, act, what, extra=extra, with_half_ulp=limited)
 
 
 class StageBuffers:
@@ -344,6 +382,41 @@ def oracle_dispatch(w, idx, gates, capacity):
                         drop_policy=w.drop_policy, layout=w.layout)
 
 
+def check_dispatch_of_oracle_routing(w, inp, cfg, r, capacity) -> dict:
+    """The GPU dispatch run on the oracle's own routing (its top-k ids, and its gates
+    rounded to fp32 for the gate drop policy) against the oracle's dispatch of the same
+    ids and gates: every map array and every row bit for bit, at any size and whatever
+    near ties the GPU's router met. The inputs go from the oracle to the GPU, never the
+    other way."""
+    b = StageBuffers(w, cfg)
+    idx = torch.from_numpy(np.ascontiguousarray(r["idx_full"]).astype(np.int32)).cuda()
+    gates32 = np.ascontiguousarray(r["G_full"]).astype(np.float32)
+    b.dispatch(inp, topk_idx=idx, topk_gate=torch.from_numpy(gates32).cuda())
+    d = oracle_dispatch(w, r["idx_full"], gates32.astype(np.float64), capacity)
+    torch.cuda.synchronize()
+    assert b.dispatch_status() == 0
+    if w.dispatch_dtype == "fp8_gemm":  # the dispatched rows themselves are checked as e4m3 codes elsewhere
+        compare_dispatch(w, b, d)
+    else:
+        compare_dispatch(w, b, d, inp["x"])
+    return d
+
+
+def check_near_tie_count(w, ws, view, H) -> int:
+    """The forward's own near-tie count (tokens whose k-th and (k+1)-th largest fp32
+    logits are within 1e-6 relative) against the oracle's float64 logits: it must lie
+    between the number of tokens with a float64 gap below 0.5e-6 and below 2e-6 (fp32
+    logits are off by about 1e-7 absolute, which moves a gap by far less than that
+    band near the selected logits' magnitudes). Returns the GPU count."""
+    base = ws.data_ptr()
+    n = int(ws[view.n_near_ties - base:view.n_near_ties - base + 4].view(torch.int32).cpu()[0])
+    Hs = selectable_logits(w, H)
+    lo = int(orc.near_tie_flags(Hs, w.k, rel=0.5e-6)[0].sum())
+    hi = int(orc.near_tie_flags(Hs, w.k, rel=2e-6)[0].sum())
+    assert lo <= n <= hi, f"near-tie count {n} outside [{lo}, {hi}]"
+    return n
+
+
 def check_dispatch(w, inp, bufs, capacity, st) -> dict:
     """Dispatch stage on seeded synthetic ids and gates (``st`` from
     workloads.make_stage_inputs): every map array bit-exact, rows copied exactly."""
@@ -453,7 +526,7 @@ def check_combine(w, bufs, st) -> float:
         out = torch.cat([out, torch.zeros(bufs.rows - out.shape[0], w.d, dtype=out.dtype, device=out.device)])
     bufs.combine(out=out, topk_gate=st["topk_gate"], pos=st["pos"])
     exact = orc.combine(f64(st["topk_gate"]), cpu(st["pos"]).numpy().astype(np.int64), f64(out), w.T, w.slots)
-    return check_close(bufs.y, exact, w.act, "combine", tol=1e-5)
+    return check_close(bufs.y, exact, w.act, "combine", tol=1e-5, with_half_ulp=True)
 
 
 def check_map_properties(w, m, capacity):

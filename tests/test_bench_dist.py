@@ -58,7 +58,13 @@ def test_algorithmic_work_of_the_bf16_and_fp8_layers():
     assert bf["up_flops"] == 2 * rows * d * 2 * F and bf["down_flops"] == 2 * rows * F * d
     assert bf["up_bytes"] == E * 2 * F * d * 2 + rows * d * 2 + rows * F * 2
     assert bf["down_bytes"] == E * d * F * 2 + rows * F * 2 + rows * d * 4
-    assert bf["combine_bytes"] == rows * d * 4 + T * d * 2
+    # the combine's algorithmic bytes take the activation dtype; the fp32 expert rows it
+    # actually reads are counted apart
+    assert bf["combine_bytes"] == rows * d * 2 + T * d * 2
+    assert bf["combine_bytes_moved"] == rows * d * 4 + T * d * 2
+    # the DeepSeek-V3-shaped layer: x read, rows written, rows read, y written = 1057 MB
+    ds = bench.algorithmic(W["dsv3_full"], 4096 * 8, out_bytes=4, h_cols=2048)
+    assert ds["dispatch_bytes"] + ds["combine_bytes"] == 2 * (4096 + 32768) * 7168 * 2 == 1_056_964_608
     f8 = bench.algorithmic(W["mixtral_fp8_gemm"], rows, out_bytes=4, h_cols=F)
     assert f8["up_flops"] == bf["up_flops"] and f8["down_bytes"] == bf["down_bytes"]
     # e4m3 W13 with one scale per row, rows as d codes + one scale, h still bf16

@@ -3,7 +3,8 @@ bounded (2 s), after which the kernel flags MOE_DEV_ERR_TIMEOUT in the status wo
 drains its copies and MMAs, frees its tensor memory and returns, leaving the context
 usable. MOE_DEBUG_SKIP_ARRIVE=1 (read once per process, so the check runs in a child
 process) makes the MMA thread leave the first finished accumulator unsignalled, so the
-epilogue's wait runs out. Both the one-SM and the SM-pair kernels are exercised."""
+epilogue's wait runs out. All three expert-GEMM kernels are exercised: one SM per
+tile, SM pairs on 256-row tiles and SM pairs with swapped operands."""
 import os
 import subprocess
 import sys
@@ -49,7 +50,7 @@ print("ok")
 """
 
 
-@pytest.mark.parametrize("variant", ["0", "2"])
+@pytest.mark.parametrize("variant", ["0", "1", "2"])
 def test_bounded_wait_reports_timeout_and_leaves_the_context_usable(variant):
     env = dict(os.environ, MOE_DEBUG_SKIP_ARRIVE="1", MOE_GEMM_PAIR=variant)
     r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT)], env=env, capture_output=True, text=True,

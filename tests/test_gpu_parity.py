@@ -17,6 +17,7 @@ from oracle import moe_oracle as orc
 from routing_dispatch_combine_moe_b300 import abi
 from routing_dispatch_combine_moe_b300 import workloads as wl
 from tests._gpu import (StageBuffers, WorkspaceMap, capacity_of, chain, check_chained_dispatch, check_close,
+                        check_dispatch_of_oracle_routing, check_layer_close, check_near_tie_count,
                         check_combine, check_dedup, check_dispatch, check_ffn, check_fp8, check_route, cpu,
                         fp8_h_budget, fp8_h_layer_budget, gate_boundary_ties, half_ulp, oracle_dispatch,
                         oracle_route, rms, route_tie_flags, run_layer)
@@ -103,7 +104,8 @@ def test_layer_forward_matches_oracle(name):
     ref = run_oracle(w, inp)
     keep = layer_keep(w, ref, capacity_of(cfg))
     extra = fp8_h_layer_budget(w, inp, ref)[keep] if w.precision == "fp8_h" else None
-    err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{name} layer y", extra=extra)
+    err = check_layer_close(name, cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{name} layer y",
+                            extra=extra)
     print(f"\n{name}: layer max|err|/rms(y) = {err:.4f} (near-tie tokens excluded: {int((~keep).sum())})")
     if w.expert == "identity":
         assert torch.equal(y, inp["x"]), "identity experts must return x exactly"
@@ -138,7 +140,7 @@ def test_identity_experts_return_x_exactly_with_drops_zeroed():
     y, ws, view, flags = run_layer(cfg, inp, w)
     ref = run_oracle(w, inp)
     # with drops the layer returns x scaled by the kept gates' sum, once rounded
-    check_close(y, ref["y"], "bf16", "identity with drops", tol=1e-5)
+    check_close(y, ref["y"], "bf16", "identity with drops", tol=1e-5, with_half_ulp=True)
     assert ref["n_dropped"] > 0
 
 
@@ -222,7 +224,8 @@ def test_split_h_mode_is_limited_by_the_output_rounding(name):
     ref = run_oracle(w, inp)
     s, o = orc.near_tie_flags(ref["H"], w.k)
     keep = ~(s | o)
-    err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], "bf16", f"{name} split-h y", tol=2e-3)
+    err = check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], "bf16", f"{name} split-h y", tol=2e-3,
+                      with_half_ulp=True)
     print(f"\n{name} split_h: raw max|err|/rms(y) = {err:.4f}")
 
 
@@ -257,9 +260,29 @@ def test_edge_cases(w):
     assert torch.equal(y, res["chain"].y), "layer and chained stage calls must agree bit for bit"
     ref = run_oracle(w, inp)
     keep = layer_keep(w, ref, capacity_of(cfg))
-    check_close(cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{w.name} layer y")
+    check_layer_close(w.name, cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{w.name} layer y")
     if w.capacity_factor == "0":
         assert torch.count_nonzero(y) == 0
+
+
+@pytest.mark.parametrize("E", [8, 64])
+def test_near_tie_count_with_duplicated_router_columns(E):
+    """Two identical columns of W_g give two exactly equal logits on every token, so
+    each token that ranks them k-th and (k+1)-th is a near tie the forward must count
+    (within the band of check_near_tie_count); the fused small-E router (E = 8) and
+    the split-K router (E = 64) each count their own."""
+    w = wl.Workload(f"dup_cols_E{E}", T=3000, d=256, E=E, k=2, F=0, act="bf16", expert="identity")
+    inp = wl.make_inputs(w, 21, device="cuda")
+    inp["Wg"][:, 5] = inp["Wg"][:, 3]
+    cfg = abi.config_for(w)
+    y, ws, view, flags = run_layer(cfg, inp, w)
+    assert flags == 0
+    H = orc.router_logits(f64(inp["x"]), f64(inp["Wg"]), None)
+    s = -np.sort(-H, axis=1)
+    planted = int(((s[:, w.k - 1] == s[:, w.k]) & (s[:, w.k] != 0)).sum())
+    n = check_near_tie_count(w, ws, view, H)
+    assert planted > 0 and n >= planted, (n, planted)
+    print(f"\nE={E}: {n} near-tie tokens counted, {planted} of them planted exact ties")
 
 
 def test_all_tokens_to_one_expert_with_capacity():
@@ -338,6 +361,11 @@ FULL["dsv3_decode_fp8_gemm"] = W["dsv3_decode_fp8_gemm"]
 FULL["mixtral_fp8_experts"] = W["mixtral_fp8_experts"]
 
 
+# Tokens whose y is compared element by element at full size (all of them for the
+# 128-token decode layers).
+SAMPLED_TOKENS = 256
+
+
 @pytest.mark.parametrize("name", list(FULL))
 def test_full_size_sampled(name):
     w = FULL[name]
@@ -347,8 +375,11 @@ def test_full_size_sampled(name):
     y, ws, view, flags = run_layer(cfg, inp, w)
     assert flags == 0
     m = WorkspaceMap(w, cfg, ws, view)
-    # router: full oracle logits in float64
+    # router: full oracle logits in float64, and the forward's own near-tie count
     r = check_route(w, inp, m)
+    n_ties = check_near_tie_count(w, ws, view, r["H"])
+    # the GPU dispatch of the oracle's routing: bit-exact at full size, always
+    check_dispatch_of_oracle_routing(w, inp, cfg, r, cap)
     # dispatch of the GPU's routing: bit-exact against the oracle's where the routings agree
     how = check_chained_dispatch(w, inp, m, r, cap)
     d = oracle_dispatch(w, r["idx_full"], r["G_full"], cap)
@@ -412,11 +443,13 @@ def test_full_size_sampled(name):
     ok &= ~flipped
     rng = np.random.default_rng(0)
     cand = np.nonzero(ok)[0]
-    tokens = sorted(rng.choice(cand, size=min(8, cand.size), replace=False).tolist())
+    tokens = sorted(rng.choice(cand, size=min(SAMPLED_TOKENS, cand.size), replace=False).tolist())
     y_s, budget = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
-    err = check_close(y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y", extra=budget)
-    print(f"\n{name}: near-ties={r['near_ties']} flipped={r['flipped']} dispatch={how} ffn_err/rms={worst_ffn} "
-          f"sampled y err/rms={err:.4f} dropped={d['n_dropped']}")
+    err = check_layer_close(name, y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y",
+                            extra=budget)
+    print(f"\n{name}: near-ties={r['near_ties']} (GPU count of k-th/(k+1)-th ties: {n_ties}) flipped={r['flipped']} "
+          f"dispatch={how} ffn_err/rms={worst_ffn} sampled y err/rms={err:.4f} over {len(tokens)} tokens "
+          f"dropped={d['n_dropped']}")
 
 
 @pytest.mark.parametrize("name", ["mixtral_bf16", "zipf_cf125", "tiny_f32"])
