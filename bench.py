@@ -276,8 +276,7 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None, threads:
         dt = time.perf_counter() - t0
         used = cpu_threads()
     else:
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=threads):
+        with blas_threads(threads):
             t0 = time.perf_counter()
             run()
             dt = time.perf_counter() - t0
@@ -285,13 +284,66 @@ def oracle_tokens_per_s(w, inp, tokens: int, seed: int = 0, cache=None, threads:
     return dict(value=len(sel) / dt, seconds=dt, tokens=len(sel), cores=used)
 
 
+def _openblas():
+    """numpy's own OpenBLAS thread getter and setter, found among the loaded libraries
+    (for hosts without threadpoolctl); (None, None) when there is none."""
+    import ctypes
+    try:
+        paths = {line.split()[-1] for line in open("/proc/self/maps") if "openblas" in line and ".so" in line}
+    except OSError:
+        return None, None
+    for path in sorted(paths):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for suffix in ("64_", "", "_64"):
+            for prefix in ("scipy_openblas_", "openblas_"):
+                get = getattr(lib, f"{prefix}get_num_threads{suffix}", None)
+                put = getattr(lib, f"{prefix}set_num_threads{suffix}", None)
+                if get is not None and put is not None:
+                    get.restype = ctypes.c_int
+                    put.argtypes = [ctypes.c_int]
+                    return get, put
+    return None, None
+
+
 def cpu_threads() -> int:
+    """Threads the oracle's BLAS calls use."""
     try:
         from threadpoolctl import threadpool_info
         n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
         return int(n)
     except Exception:
-        return os.cpu_count() or 1
+        get, _ = _openblas()
+        return int(get()) if get is not None else (os.cpu_count() or 1)
+
+
+class blas_threads:
+    """Limits the BLAS thread pools to n threads inside the block (threadpoolctl, else
+    numpy's OpenBLAS setter, else nothing)."""
+
+    def __init__(self, n: int):
+        self.n, self.ctx, self.old = n, None, None
+
+    def __enter__(self):
+        try:
+            from threadpoolctl import threadpool_limits
+            self.ctx = threadpool_limits(limits=self.n)
+            self.ctx.__enter__()
+        except ImportError:
+            get, put = _openblas()
+            if put is not None:
+                self.old = get()
+                put(self.n)
+                self.put = put
+        return self
+
+    def __exit__(self, *exc):
+        if self.ctx is not None:
+            self.ctx.__exit__(*exc)
+        elif self.old is not None:
+            self.put(self.old)
 
 
 def oracle_sample_tokens(w, max_tokens: int = 2048, mem_budget: float = 16e9) -> int:

@@ -106,7 +106,9 @@ def test_rows_capacity_and_kernel_counts():
     assert abi.moe_kernels_per_forward(cfg(capacity=5, drop_policy="gate", layout="padded")) == 9
     assert abi.moe_kernels_per_forward(cfg(capacity=0, layout="padded")) == 5   # no rows: no padding, no GEMMs
     assert abi.moe_kernels_per_forward(cfg(expert="identity", F=0)) == 5
-    assert abi.moe_kernels_per_forward(cfg(E=64, d=1024)) == 8                 # split-K logits + top-k
+    # bf16 and E >= 64: W_g's split, tensor-core split-K logits, top-k; fp32: FMA logits + top-k
+    assert abi.moe_kernels_per_forward(cfg(E=64, d=1024)) == 9
+    assert abi.moe_kernels_per_forward(cfg(E=64, d=1024, act="f32")) == 8
 
 
 def test_padded_workspace_holds_n_times_c_rows():
@@ -172,10 +174,11 @@ def test_workspace_sizes_and_layout():
             assert view.out + A * w.d * w.act_bytes <= base + fwd
         assert v.moe_workspace_get_view(ctypes.byref(c), base, fwd - 1, ctypes.byref(view)) == abi.MOE_ERR_WORKSPACE
         small_router = w.E <= 32 and w.d * w.E * 4 <= 128 * 1024  # one fused router launch instead of two
+        tc_router = w.act == "bf16" and w.E >= 64 and not small_router  # W_g's split kernel comes first
         assert abi.moe_kernels_per_forward(c) == ((6 if w.expert == "identity" else 8) + (5 if w.dedup else 0)
                                                   + (1 if w.dispatch_dtype == "fp8" else 0)
                                                   + (1 if w.precision == "fp8_h" else 0)  # h quantized between GEMMs
-                                                  - (1 if small_router else 0))
+                                                  - (1 if small_router else 0) + (1 if tc_router else 0))
 
 
 def test_entry_points_reject_bad_arguments_on_the_host():

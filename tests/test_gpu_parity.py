@@ -167,6 +167,10 @@ def _ws_equal_used(cfg, ws1, ws2):
     return True
 
 
+# Edge layers. Small layers with heavy-tailed outputs (few tokens, long rows, drops) can
+# spend most of the 2e-2 * rms(y) budget on y's own bf16 rounding, and then the bf16
+# rounding of h tips them over: those carry h as a hi/lo pair (precision "split_h"),
+# which leaves y's rounding as the only error of size.
 EDGE = [
     wl.Workload("T1_k1", T=1, d=64, E=4, k=1, F=64, act="bf16", expert="swiglu"),
     wl.Workload("k_eq_E", T=77, d=128, E=6, k=6, F=96, act="bf16", expert="swiglu", D=3),
@@ -177,22 +181,23 @@ EDGE = [
     wl.Workload("zero_capacity", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu", capacity_factor="0"),
     wl.Workload("cap_below_mean", T=600, d=128, E=8, k=2, F=128, act="bf16", expert="swiglu",
                 capacity_factor="0.75", min_capacity=10),
-    wl.Workload("cap_huge", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu", capacity_factor="100"),
+    wl.Workload("cap_huge", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu", capacity_factor="100",
+                precision="split_h"),
     wl.Workload("k16_E256", T=96, d=256, E=256, k=16, F=128, act="bf16", expert="swiglu", D=8),
-    wl.Workload("long_rows", T=130, d=8192, E=4, k=2, F=256, act="bf16", expert="swiglu"),
+    wl.Workload("long_rows", T=130, d=8192, E=4, k=2, F=256, act="bf16", expert="swiglu", precision="split_h"),
     wl.Workload("split_h_relu", T=300, d=192, E=5, k=2, F=320, act="bf16", expert="relu", precision="split_h"),
     wl.Workload("split_h_ragged", T=333, d=136, E=12, k=3, F=192, act="bf16", expert="swiglu", D=4,
                 precision="split_h", capacity_factor="0.9"),
-    wl.Workload("gate_drops_ragged", T=333, d=136, E=12, k=3, F=200, act="bf16", expert="swiglu", D=4,
-                capacity_factor="0.75", drop_policy="gate", zipf_s=1.2),
+    wl.Workload("gate_drops_ragged", T=333, d=136, E=12, k=3, F=192, act="bf16", expert="swiglu", D=4,
+                capacity_factor="0.75", drop_policy="gate", zipf_s=1.2, precision="split_h"),
     wl.Workload("padded_token_order", T=300, d=128, E=8, k=2, F=128, act="bf16", expert="swiglu",
-                capacity_factor="1", layout="padded", zipf_s=1.2),
+                capacity_factor="1", layout="padded", zipf_s=1.2, precision="split_h"),
     wl.Workload("padded_gate_f32", T=257, d=96, E=7, k=3, F=72, act="f32", expert="relu",
                 capacity_factor="1.25", drop_policy="gate", layout="padded", zipf_s=1.2),
     wl.Workload("padded_zero_capacity", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu",
                 capacity_factor="0", layout="padded"),
     wl.Workload("padded_cap_huge", T=64, d=64, E=8, k=2, F=64, act="bf16", expert="swiglu",
-                capacity_factor="100", layout="padded", drop_policy="gate"),
+                capacity_factor="100", layout="padded", drop_policy="gate", precision="split_h"),
     wl.Workload("padded_identity_gate", T=500, d=256, E=16, k=4, F=0, act="bf16", expert="identity",
                 capacity_factor="0.5", D=4, layout="padded", drop_policy="gate"),
     # the FP8 up projection: one token, every expert per token, zero and huge capacity in
@@ -208,7 +213,7 @@ EDGE = [
     wl.Workload("fp8_gemm_split_h_drops", T=333, d=144, E=12, k=3, F=192, act="bf16", expert="swiglu", D=4,
                 precision="split_h", capacity_factor="0.6", zipf_s=1.2, dispatch_dtype="fp8_gemm"),
     wl.Workload("fp8_gemm_long_rows", T=130, d=8192, E=4, k=2, F=256, act="bf16", expert="swiglu",
-                dispatch_dtype="fp8_gemm"),
+                dispatch_dtype="fp8_gemm", precision="split_h"),
 ]
 
 
