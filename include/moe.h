@@ -237,9 +237,16 @@ int moe_kernels_per_forward(const moe_config* cfg);
  *             rank the lower expert id first; slots k..K-1 hold the shared experts
  *   topk_gate [T, K] fp32 out: G = exp(H_j - H_max) / sum over kept slots (1 for shared)
  *   ws        scratch of moe_route_workspace_bytes(cfg) bytes: the logits are summed
- *             from split-K partials kept there.
- * Logits are fp32 sums of fp32 products (x is promoted exactly), summed in a fixed
- * order, so the result is deterministic. */
+ *             from split-K partials kept there (and, on the tensor-core path, W_g's
+ *             three bf16 terms).
+ * Logits are fp32-accurate sums of exact products (x is promoted exactly), summed in a
+ * fixed order, so the result is deterministic. For bf16 x and E >= 64 (unless the
+ * small-E kernel applies) they come from the tensor cores: W_g is split exactly into
+ * three bf16 terms (hi + mid + lo = W_g), each 128-element chunk of d accumulates in a
+ * fresh fp32 tensor-memory accumulator, and the chunk sums are added in fp32 in chunk
+ * order; otherwise from fp32 FMAs, folded every 256 products. A bounded wait of the
+ * tensor-core kernel that gives up ends it early (MOE_DEV_ERR_TIMEOUT in the forward's
+ * status word; this stage entry point has no status word). */
 int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias,
               int32_t* topk_idx, float* topk_gate, void* ws, size_t ws_bytes, moe_stream_t stream);
 
@@ -460,6 +467,9 @@ const char* moe_ffn_kernel_name(const moe_config* cfg);
 
 /* Environment switches (read once per process):
  *   MOE_GEMM_PAIR=0/1/2    force the tcgen05 expert-GEMM variant (see moe_ffn_kernel_name);
+ *   MOE_ROUTE_TC=0         keep the router's logits on the FMA units for every config;
+ *   MOE_ROUTE_TC_CHUNK=n   elements of d per fresh accumulator on the tensor-core router
+ *                          (a multiple of 64; default 128), for accuracy experiments;
  *   MOE_DEBUG_SKIP_ARRIVE=1 failure-path test only: the grouped GEMMs leave their first
  *                          finished accumulator unsignalled, so their bounded wait runs
  *                          out (2 s) and MOE_DEV_ERR_TIMEOUT is set in the status word;

@@ -11,10 +11,10 @@
 //                stored expert-major, hist[e][block]. Skipped when the router has
 //                already counted (the layer forward: integer atomics from the top-k
 //                writers into the zeroed histogram give the same counts).
-//   2. scan    - one CTA: per expert an exclusive scan over blocks (so hist becomes
-//                "assignments of e in earlier blocks"), then block-wide scans of the
-//                kept counts (row offsets), of the dropped counts (drop-list offsets)
-//                and the virtual-rank chunk offsets.
+//   2. scan    - a warp per expert scans its row of block counts (so hist becomes
+//                "assignments of e in earlier blocks"); the last CTA to finish then
+//                scans the kept counts (row offsets), the dropped counts (drop-list
+//                offsets) and the virtual-rank chunk offsets.
 //   3. scatter - per block again: an assignment's rank among its expert's
 //                assignments is the scanned block prefix + the counts of earlier warps
 //                in the block + its rank among equal ids in its warp (match_any +
@@ -87,6 +87,13 @@ __device__ int block_excl_scan(int v, int* warp_sums, int* total) {
     return r;
 }
 
+// Scan, over ceil(E / 32) CTAs of 32 warps: warp w of CTA c turns expert e = 32 c + w's
+// row of block counts into its exclusive scan (so hist[e][b] becomes "assignments of e
+// in earlier blocks") and writes the row total to counts_routed[e]. Each CTA then
+// takes a ticket; the last one to finish (no CTA waits for another) reads all totals
+// back and scans the kept counts (row offsets), the dropped counts (drop-list
+// offsets), the routed counts and the virtual-rank chunk offsets. With one CTA no
+// ticket is needed (ticket may be null); otherwise *ticket starts at 0 and is left at 0.
 __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, int nblk, int64_t capacity,
                                                     int padded, int32_t* __restrict__ hist,
                                                     int32_t* __restrict__ counts_routed,
@@ -94,56 +101,49 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
                                                     int32_t* __restrict__ drop_offsets,
                                                     int32_t* __restrict__ routed_offsets,
                                                     int32_t* __restrict__ rank_offsets,
-                                                    int32_t* __restrict__ n_dropped) {
-    __shared__ int routed[MOE_MAX_E];
+                                                    int32_t* __restrict__ n_dropped, int32_t* ticket) {
     __shared__ int offs[MOE_MAX_E + 1];
     __shared__ int warp_sums[32];
     __shared__ int totals[3];
+    __shared__ int is_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // Per expert, an exclusive scan of its row of block counts. A warp takes four experts
-    // (e, e + 32, e + 64, e + 96) at a time and loads 4 chunks of 32 blocks of each before
-    // scanning, so 16 independent loads per lane are in flight instead of one.
-    constexpr int SB = 4, EX = 4;
-    for (int e0 = warp; e0 < E; e0 += 32 * EX) {
-        int32_t* row[EX];
-        int run[EX];
-        bool has[EX];
-#pragma unroll
-        for (int x = 0; x < EX; ++x) {
-            has[x] = e0 + 32 * x < E;
-            row[x] = hist + size_t(has[x] ? e0 + 32 * x : e0) * nblk;
-            run[x] = 0;
-        }
+    // this warp's expert: SB chunks of 32 blocks loaded before they are scanned
+    constexpr int SB = 8;
+    const int e = int(blockIdx.x) * 32 + warp;
+    if (e < E) {
+        int32_t* row = hist + size_t(e) * nblk;
+        int run = 0;
         for (int b0 = 0; b0 < nblk; b0 += 32 * SB) {
-            int v[EX][SB];
+            int v[SB];
 #pragma unroll
-            for (int x = 0; x < EX; ++x)
+            for (int j = 0; j < SB; ++j) {
+                const int b = b0 + 32 * j + lane;
+                v[j] = b < nblk ? row[b] : 0;
+            }
 #pragma unroll
-                for (int j = 0; j < SB; ++j) {
-                    const int b = b0 + 32 * j + lane;
-                    v[x][j] = (b < nblk && has[x]) ? row[x][b] : 0;
-                }
-#pragma unroll
-            for (int x = 0; x < EX; ++x)
-#pragma unroll
-                for (int j = 0; j < SB; ++j) {
-                    if (b0 + 32 * j >= nblk) break;  // no blocks left (uniform over the warp)
-                    const int b = b0 + 32 * j + lane;
-                    const int incl = warp_incl_scan(v[x][j], lane);
-                    if (b < nblk && has[x]) row[x][b] = run[x] + incl - v[x][j];
-                    run[x] += __shfl_sync(0xFFFFFFFFu, incl, 31);
-                }
+            for (int j = 0; j < SB; ++j) {
+                if (b0 + 32 * j >= nblk) break;  // no blocks left (uniform over the warp)
+                const int b = b0 + 32 * j + lane;
+                const int incl = warp_incl_scan(v[j], lane);
+                if (b < nblk) row[b] = run + incl - v[j];
+                run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
         }
-        if (lane == 0) {
-#pragma unroll
-            for (int x = 0; x < EX; ++x)
-                if (has[x]) routed[e0 + 32 * x] = run[x];
-        }
+        if (lane == 0) counts_routed[e] = run;
     }
-    __syncthreads();
+    if (gridDim.x > 1) {
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) is_last = atomicAdd(ticket, 1) == int(gridDim.x) - 1;
+        __syncthreads();
+        if (!is_last) return;
+        __threadfence();
+    } else {
+        __syncthreads();
+    }
 
-    const int cr = tid < E ? routed[tid] : 0;
+    const int cr = tid < E ? __ldcg(counts_routed + tid) : 0;
     const int ck = (capacity < 0 || tid >= E_capped || cr <= capacity) ? cr : int(capacity);
     const int scanned = block_excl_scan(ck, warp_sums, &totals[0]);
     const int doff = block_excl_scan(cr - ck, warp_sums, &totals[1]);
@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
     // padded layout: every expert owns `capacity` rows
     const int off = padded ? tid * int(capacity) : scanned;
     if (tid < E) {
-        counts_routed[tid] = cr;
         counts_kept[tid] = ck;
         offsets[tid] = off;
         drop_offsets[tid] = doff;
@@ -164,6 +163,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int E, int E_capped, int D, 
         offs[E] = end;
         routed_offsets[E] = totals[2];
         *n_dropped = totals[1];
+        if (gridDim.x > 1) *ticket = 0;
     }
     __syncthreads();
     if (tid <= D) rank_offsets[tid] = offs[tid * (E_capped / D)];
@@ -420,7 +420,118 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
     }
 }
 
+// Gather by bulk copies: one thread per CTA moves each of its tokens' x row into
+// shared memory with one bulk copy (completion counted on an mbarrier) and writes it
+// to each of the token's kept rows with one bulk store per row, so the copy engine
+// moves whole rows and the SM only issues. Tokens t = blockIdx.x + i * gridDim.x go
+// through kGbBufs row buffers: while one buffer's stores drain, the next row loads.
+// Rows are row_bytes long (a multiple of 16, as are the addresses).
+constexpr int kGbBufs = 3;
+
+__device__ __forceinline__ void bulk_load_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_row(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until every committed bulk group has completed, its writes included.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(32) gather_bulk_kernel(const unsigned char* __restrict__ x,
+                                                         const int32_t* __restrict__ pos,
+                                                         unsigned char* __restrict__ xperm, int T, int k,
+                                                         uint32_t row_bytes, int64_t max_rows, int32_t* status) {
+    extern __shared__ __align__(128) unsigned char gb_rows[];
+    __shared__ uint64_t full[kGbBufs];
+    if (threadIdx.x != 0) return;
+    for (int b = 0; b < kGbBufs; ++b) mbar_init(&full[b], 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    const int first = int(blockIdx.x), step = int(gridDim.x);
+    const int n = first < T ? (T - 1 - first) / step + 1 : 0;  // tokens of this CTA
+    int issued = 0;                                             // loads issued: tokens [0, issued)
+    auto load = [&]() {
+        const int b = issued % kGbBufs;
+        mbar_arrive_expect_tx(&full[b], row_bytes);
+        bulk_load_row(gb_rows + size_t(b) * row_bytes, x + size_t(first + issued * step) * row_bytes, row_bytes,
+                      &full[b]);
+        ++issued;
+    };
+    // bounded wait for load i; false after the time limit
+    auto wait_load = [&](int i) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full[i % kGbBufs], uint32_t(i / kGbBufs) & 1u))
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+        return true;
+    };
+    while (issued < kGbBufs - 1 && issued < n) load();
+    int i = 0;
+    for (; i < n; ++i) {
+        if (!wait_load(i)) {
+            set_status(status, MOE_DEV_ERR_TIMEOUT);
+            break;
+        }
+        fence_proxy_async_smem();
+        const int b = i % kGbBufs;
+        const int t = first + i * step;
+        for (int j = 0; j < k; ++j) {
+            const int p = __ldg(pos + size_t(t) * k + j);
+            if (p >= 0 && p < max_rows)
+                bulk_store_row(xperm + size_t(p) * row_bytes, gb_rows + size_t(b) * row_bytes, row_bytes);
+        }
+        bulk_commit();
+        // the buffer of token i - 1 is free once every group but the newest has read it
+        bulk_wait_read<1>();
+        if (issued < n) load();
+    }
+    bulk_wait_all();
+    // loads still in flight after a timeout must land before the CTA's shared memory goes
+    for (int j = i; j < issued; ++j) wait_load(j);
+}
+
 }  // namespace
+
+dim3 gather_grid(int T, int vec_per_row);
+
+// Rows a bulk-copy gather CTA holds (kGbBufs of them) must fit its shared memory; small
+// batches keep the warp gather, whose column slices spread one token over several SMs.
+bool gather_uses_bulk(int T, int64_t row_bytes) { return T >= 512 && row_bytes * kGbBufs <= 96 * 1024; }
+
+cudaError_t launch_gather(const void* x, const int32_t* pos, void* xperm, int T, int k, int64_t row_bytes,
+                          int64_t max_rows, int32_t* status, cudaStream_t stream) {
+    if (gather_uses_bulk(T, row_bytes)) {
+        const size_t smem = size_t(kGbBufs) * size_t(row_bytes);
+        static PerContext<int> smem_set;
+        const cudaError_t e = set_smem_limit_once(smem_set, gather_bulk_kernel, 96 * 1024);
+        if (e != cudaSuccess) return e;
+        const int per_sm = int((200 * 1024) / (smem + 1024));
+        const int ctas = T < device_sm_count() * per_sm ? T : device_sm_count() * per_sm;
+        gather_bulk_kernel<<<ctas, 32, smem, stream>>>(static_cast<const unsigned char*>(x), pos,
+                                                       static_cast<unsigned char*>(xperm), T, k, uint32_t(row_bytes),
+                                                       max_rows, status);
+        return cudaGetLastError();
+    }
+    const int vec_per_row = int(row_bytes / 16);
+    gather_kernel<<<gather_grid(T, vec_per_row), 256, 0, stream>>>(static_cast<const uint4*>(x), pos,
+                                                                   static_cast<uint4*>(xperm), T, k, vec_per_row,
+                                                                   max_rows);
+    return cudaGetLastError();
+}
 
 // Token blocks of 8 warps, times column slices of at least 64 pieces, until about two
 // CTAs per SM are in flight.
@@ -439,9 +550,10 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const int vec_per_row = int(int64_t(a.d) * a.act_bytes / 16);
     const int64_t rows = padded ? int64_t(a.E) * a.capacity : A;
     if (!a.counted) count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, nblk, a.hist, a.status);
-    scan_kernel<<<1, 1024, 0, stream>>>(a.E, a.E_capped, a.D, nblk, a.capacity, padded ? 1 : 0, a.hist,
-                                        a.counts_routed, a.counts_kept, a.offsets, a.drop_offsets, a.routed_offsets,
-                                        a.rank_offsets, a.n_dropped);
+    scan_kernel<<<(a.E + 31) / 32, 1024, 0, stream>>>(a.E, a.E_capped, a.D, nblk, a.capacity, padded ? 1 : 0,
+                                                       a.hist, a.counts_routed, a.counts_kept, a.offsets,
+                                                       a.drop_offsets, a.routed_offsets, a.rank_offsets, a.n_dropped,
+                                                       a.scan_ticket);
     scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.topk_idx, A, a.E, a.E_capped, nblk, a.capacity, a.hist,
                                                         a.offsets, a.drop_offsets, a.routed_offsets,
                                                         by_gate ? a.elist : nullptr, a.topk_gate, a.pos, a.row_src,
@@ -454,10 +566,11 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
         pad_rows_kernel<<<dim3(unsigned((a.capacity + 7) / 8), unsigned(a.E)), 256, 0, stream>>>(
             a.counts_kept, a.offsets, int(a.capacity),
                                                  static_cast<uint4*>(a.xperm), vec_per_row, a.row_src);
-    if (!a.skip_gather)
-        gather_kernel<<<gather_grid(a.T, vec_per_row), 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.pos,
-                                                                         static_cast<uint4*>(a.xperm), a.T, a.k,
-                                                                         vec_per_row, rows);
+    if (!a.skip_gather) {
+        const cudaError_t e = launch_gather(a.x, a.pos, a.xperm, a.T, a.k, int64_t(vec_per_row) * 16, rows, a.status,
+                                            stream);
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 
@@ -538,13 +651,13 @@ cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream) {
     count_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, nblk, a.hist, a.status, 1);
     scan_kernel<<<1, 1024, 0, stream>>>(a.D, a.D, 1, nblk, -1, 0, a.hist, a.send_counts, a.kept_scratch,
                                         a.send_offsets, a.drop_offsets, a.routed_offsets, a.rank_offsets,
-                                        a.n_dropped);
+                                        a.n_dropped, nullptr);
     scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, a.D, nblk, -1, a.hist, a.send_offsets,
                                                         a.drop_offsets, a.routed_offsets, nullptr, nullptr,
                                                         a.send_pos, a.send_src, nullptr);
-    gather_kernel<<<gather_grid(a.T, vec_per_row), 256, 0, stream>>>(static_cast<const uint4*>(a.x), a.send_pos,
-                                                                     static_cast<uint4*>(a.xsend), a.T, a.D,
-                                                                     vec_per_row, A2);
+    const cudaError_t ge = launch_gather(a.x, a.send_pos, a.xsend, a.T, a.D, int64_t(vec_per_row) * 16, A2, a.status,
+                                         stream);
+    if (ge != cudaSuccess) return ge;
     fanout_kernel<<<(a.T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(a.x),
                                                       static_cast<const uint4*>(a.xsend), a.topk_idx, a.pos,
                                                       a.send_pos, static_cast<uint4*>(a.xperm), a.T, a.K,

@@ -26,8 +26,8 @@ namespace {
 
 constexpr size_t kStaticScratchInts = MOE_STATIC_SCRATCH_BYTES / sizeof(int32_t);
 
-// [0]: status word, [64, 64 + N*blocks): histogram, then N drop offsets, N+1 routed
-// offsets and (gate drop policy) the T*K per-expert assignment list.
+// [0]: status word, [1]: the scan's ticket, [64, 64 + N*blocks): histogram, then N drop
+// offsets, N+1 routed offsets and (gate drop policy) the T*K per-expert assignment list.
 __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchInts];
 
 // Device address of g_dispatch_scratch in the current context, looked up once per
@@ -74,7 +74,7 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
 
     int32_t* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
-    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(int32_t), stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, 2 * sizeof(int32_t), stream);
     if (e != cudaSuccess) {
         g_last_cuda_error = std::string("moe_dispatch_static: ") + cudaGetErrorName(e) + " (" +
                             cudaGetErrorString(e) + ")";
@@ -100,6 +100,7 @@ extern "C" int moe_dispatch_static(const moe_config* cfg, const void* x, const i
     a.n_dropped = map->n_dropped;
     a.xperm = xperm;
     a.status = scratch;
+    a.scan_ticket = scratch + 1;
     a.hist = scratch + 64;
     a.drop_offsets = scratch + 64 + hist_ints;
     a.routed_offsets = a.drop_offsets + N;

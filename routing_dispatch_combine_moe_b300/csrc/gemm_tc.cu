@@ -815,57 +815,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
 }
 
 // ------------------------------------------------------------------ host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
 // 2-D tensor map over a row-major [rows, inner] matrix of bf16 (or bytes, u8), box =
 // 128 bytes x box_rows, 128-byte swizzle, zero fill out of bounds.
 cudaError_t make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
                      bool u8 = false) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    const uint32_t esz = u8 ? 1 : 2;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * esz};
-    const cuuint32_t box[2] = {128u / esz, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                           const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return make_tensor_map_sw128(map, base, u8 ? 1 : 2, inner, rows, 1, box_rows, 1);
 }
 
 // 3-D map over SwiGLU weights [E, 2, F, inner] seen as [2E, F, inner]: box = 128 bytes x
 // 64 feature rows x both halves (gate, up) of one expert, 128-byte swizzle.
 cudaError_t make_gate_up_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t F, uint64_t E, bool u8) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    const uint32_t esz = u8 ? 1 : 2;
-    const cuuint64_t dims[3] = {inner, F, 2 * E};
-    const cuuint64_t strides[2] = {inner * esz, F * inner * esz};
-    const cuuint32_t box[3] = {128u / esz, 64u, 2u};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = enc(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return make_tensor_map_sw128(map, base, u8 ? 1 : 2, inner, F, 2 * E, 64, 2);
 }
 
 cudaError_t make_row_maps(RowMaps* maps, const void* base, uint64_t inner, uint64_t rows, bool u8 = false) {
@@ -986,6 +946,40 @@ cudaError_t launch_mode(const CUtensorMap& mA, const CUtensorMap& mB, const Para
 }
 
 }  // namespace
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+cudaError_t make_tensor_map_sw128(CUtensorMap* map, const void* base, uint32_t esz, uint64_t inner, uint64_t rows,
+                                  uint64_t depth, uint32_t box_rows, uint32_t box_depth) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {inner, rows, depth};
+    const cuuint64_t strides[2] = {inner * esz, rows * inner * esz};
+    const cuuint32_t box[3] = {128u / esz, box_rows, box_depth};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t rank = depth > 1 || box_depth > 1 ? 3 : 2;
+    const CUresult r = enc(map, esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 int ffn_tc_variant(int64_t rows, int E, int64_t capacity) { return gemm_variant(rows, E, capacity); }
 

@@ -21,13 +21,25 @@ inline int dispatch_blocks(int64_t assignments) {
 }
 
 // Router. The logits are summed from up to route_max_slices(T, E) split-K partials
-// held in `scratch`, whose size depends only on T and E.
+// held in `scratch`; the tensor-core router also keeps W_g's three bf16 terms there.
 int route_max_slices(int T, int E);
 bool route_uses_small_kernel(int d, int E);  // one fused launch instead of logits + top-k
 int route_k_slices(int T, int d, int E);
-inline size_t route_scratch_bytes_max(int T, int E) {
-    return size_t(route_max_slices(T, E)) * size_t(T) * size_t(E) * sizeof(float);
+// Logits on the tensor cores (bf16 x, E >= 64, not the small-E kernel; MOE_ROUTE_TC=0
+// keeps them on the FMA units).
+bool route_uses_tc(int act_dtype, int d, int E);
+size_t route_tc_weight_bytes(int d, int E);  // [3][E][d] bf16, 256-byte rounded
+int route_tc_slices(int T, int d, int E);
+inline size_t route_partial_bytes_max(int T, int E) {
+    return (size_t(route_max_slices(T, E)) * size_t(T) * size_t(E) * sizeof(float) + 255) & ~size_t(255);
 }
+inline size_t route_scratch_bytes(int act_dtype, int T, int d, int E) {
+    return route_partial_bytes_max(T, E) + (route_uses_tc(act_dtype, d, E) ? route_tc_weight_bytes(d, E) : 0);
+}
+// Splits W_g into its three bf16 terms in `wsplit`, then writes ks_out split-K partial
+// logits [ks][T][E] into `partial` from the tensor cores.
+cudaError_t launch_route_tc(const void* x, const float* Wg, int T, int d, int E, float* partial, void* wsplit,
+                            int32_t* status, int* ks_out, cudaStream_t stream);
 // topk_idx / topk_gate have k + n_shared slots per token; the shared slots hold
 // experts E..E+n_shared-1 with gate 1. With 0 < topk_groups < n_groups the selection
 // is limited to the topk_groups best of n_groups contiguous expert groups. A non-null
@@ -35,9 +47,10 @@ inline size_t route_scratch_bytes_max(int T, int E) {
 // dispatch's per-block expert counts, so the dispatch can skip its count kernel. A
 // non-null near_ties (one zeroed int) receives the number of tokens whose k-th and
 // (k+1)-th largest selectable fp32 logits differ by less than 1e-6 relative.
+// `status` (nullable) receives MOE_DEV_ERR_TIMEOUT from the tensor-core router's bounded waits.
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
-                         float* scratch, int32_t* hist, int32_t* near_ties, cudaStream_t stream);
+                         float* scratch, int32_t* hist, int32_t* near_ties, int32_t* status, cudaStream_t stream);
 
 struct DispatchArgs {
     int T, d, E, k, D;  // E: all experts (routed + shared), k: all slots per token
@@ -64,6 +77,7 @@ struct DispatchArgs {
     int32_t* drop_offsets; // [E]
     int32_t* routed_offsets; // [E+1] exclusive scan of the routed counts (gate policy)
     int32_t* elist;          // [2*T*k] each expert's assignments in token order, then their gate keys (gate policy)
+    int32_t* scan_ticket;    // one int, 0 on entry (left at 0): orders the scan's CTAs when E > 32
     bool skip_gather;        // leave xperm to launch_dedup
     bool counted;            // hist already holds the counts (the router filled it)
 };
@@ -156,6 +170,12 @@ int ffn_tc_variant(int64_t rows, int E, int64_t capacity);
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event);
 // fp32 experts on the FMA units.
 cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event);
+
+// Tensor map for TMA over a row-major [depth, rows, inner] array of bf16 (esz 2) or
+// bytes (esz 1): box = 128 bytes x box_rows x box_depth, 128-byte swizzle, zero fill
+// out of bounds (a 2-D map when depth and box_depth are 1).
+cudaError_t make_tensor_map_sw128(CUtensorMap* map, const void* base, uint32_t esz, uint64_t inner, uint64_t rows,
+                                  uint64_t depth, uint32_t box_rows, uint32_t box_depth);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();

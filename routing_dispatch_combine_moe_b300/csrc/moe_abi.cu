@@ -170,7 +170,7 @@ Layout layout(const moe_config* c) {
         o = align_up(o + bytes);
         return at;
     };
-    L.status = take(sizeof(int32_t));
+    L.status = take(2 * sizeof(int32_t));  // the status word, then the dispatch scan's ticket
     L.near_ties = take(sizeof(int32_t));
     L.hist = take(sizeof(int32_t) * size_t(N) * nblk);
     L.drop_offsets = take(sizeof(int32_t) * size_t(N));
@@ -186,7 +186,7 @@ Layout layout(const moe_config* c) {
     L.dd_rank = take(dd ? sizeof(int32_t) * 2 : 0);
     L.dd_ndrop = take(dd ? sizeof(int32_t) : 0);
     L.dispatch_end = o;
-    L.route_partial = take(route_scratch_bytes_max(c->T, c->E));
+    L.route_partial = take(route_scratch_bytes(c->act_dtype, c->T, c->d, c->E));
     L.topk_idx = take(sizeof(int32_t) * A);
     L.topk_gate = take(sizeof(float) * A);
     L.counts_routed = take(sizeof(int32_t) * size_t(N));
@@ -274,9 +274,10 @@ FfnLayout ffn_layout(const moe_config* c) {
 }
 
 int run_route(const moe_config* c, const void* x, const float* Wg, const float* bias, int32_t* idx, float* gate,
-              float* scratch, cudaStream_t s, int32_t* hist = nullptr, int32_t* near_ties = nullptr) {
+              float* scratch, cudaStream_t s, int32_t* hist = nullptr, int32_t* near_ties = nullptr,
+              int32_t* status = nullptr) {
     const cudaError_t e = launch_route(c->act_dtype, x, Wg, bias, c->T, c->d, c->E, c->k, c->n_shared, c->n_groups,
-                                       c->topk_groups, idx, gate, scratch, hist, near_ties, s);
+                                       c->topk_groups, idx, gate, scratch, hist, near_ties, status, s);
     return e == cudaSuccess ? MOE_OK : fail_cuda(e, "moe_route");
 }
 
@@ -303,6 +304,7 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const f
     a.n_dropped = m->n_dropped;
     a.xperm = xperm;
     a.status = at<int32_t>(ws, L.status);
+    a.scan_ticket = at<int32_t>(ws, L.status) + 1;  // the int after the status word, zeroed with it
     a.hist = at<int32_t>(ws, L.hist);
     a.drop_offsets = at<int32_t>(ws, L.drop_offsets);
     a.routed_offsets = at<int32_t>(ws, L.routed_offsets);
@@ -454,7 +456,7 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status, histogram)");
     if ((rc = record(events, n_events, 0, s)) != MOE_OK) return rc;
     if ((rc = run_route(c, x, Wg, bias, v.topk_idx, v.topk_gate, at<float>(ws, L.route_partial), s,
-                        at<int32_t>(ws, L.hist), v.n_near_ties)) != MOE_OK)
+                        at<int32_t>(ws, L.hist), v.n_near_ties, v.status)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 1, s)) != MOE_OK) return rc;
     const bool f8 = fp8_blocks(c) || fp8_gemm(c);
@@ -538,12 +540,13 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
     const int fp8 = fp8_blocks(cfg) ? 1 : 0;  // dequant (the gather quantizes; FP8_GEMM rows are used as they are)
     const int fp8h = fp8_h(cfg) && ffn ? 1 : 0;  // h quantized between the two GEMMs
-    const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : 2;  // fused, or logits + top-k
+    // fused; or logits + top-k; or (tensor cores) W_g's split + logits + top-k
+    const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : (route_uses_tc(cfg->act_dtype, cfg->d, cfg->E) ? 3 : 2);
     return route + 3 + select + pad + dedup + fp8 + fp8h + ffn + 1;
 }
 
 size_t moe_route_workspace_bytes(const moe_config* cfg) {
-    return validate(cfg) == MOE_OK ? route_scratch_bytes_max(cfg->T, cfg->E) : 0;
+    return validate(cfg) == MOE_OK ? route_scratch_bytes(cfg->act_dtype, cfg->T, cfg->d, cfg->E) : 0;
 }
 
 int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float* bias, int32_t* topk_idx,
@@ -551,7 +554,7 @@ int moe_route(const moe_config* cfg, const void* x, const float* Wg, const float
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
     if (!x || !Wg || !topk_idx || !topk_gate) return MOE_ERR_ARG;
-    const size_t need = route_scratch_bytes_max(cfg->T, cfg->E);
+    const size_t need = route_scratch_bytes(cfg->act_dtype, cfg->T, cfg->d, cfg->E);
     if (need && !ws) return MOE_ERR_ARG;
     if (!aligned16(x) || !aligned4(Wg) || (bias && !aligned4(bias)) || !aligned4(topk_idx) || !aligned4(topk_gate) ||
         (ws && !aligned16(ws)))
@@ -572,7 +575,8 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx, 
         return MOE_ERR_ARG;
     if (!aligned16(x) || !aligned16(xperm) || !aligned16(ws)) return MOE_ERR_ALIGN;
     if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
-    const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+    // the status word and the scan's ticket after it
+    const cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     return run_dispatch(cfg, x, topk_idx, topk_gate, map, xperm, ws, stream);
 }
@@ -770,6 +774,6 @@ const char* moe_ffn_kernel_name(const moe_config* cfg) {
     }
 }
 
-int moe_version(void) { return 100; }
+int moe_version(void) { return 200; }
 
 }  // extern "C"

@@ -2,8 +2,9 @@
 // softmax over the kept logits ("Mixture-of-Experts (MoE) Architecture and Expert
 // Parallelism", section 2 "The Gating Network Formulation").
 //
-// The logits are an fp32 GEMM [T x d] x [d x E] on the FMA units (exactly rounded
-// products and sums). A CTA of 8 warps stages chunks of 16 elements of x (transposed)
+// For bf16 activations and E >= 64 the logits come from the tensor cores
+// (route_tc.cu); otherwise they are an fp32 GEMM [T x d] x [d x E] on the FMA units
+// (exactly rounded products and sums), as follows. A CTA of 8 warps stages chunks of 16 elements of x (transposed)
 // and of W_g through double-buffered shared memory; lanes own 4 tokens each, so W_g
 // values are warp-wide broadcasts, and warps own 8 experts each (warps along experts
 // = 1, 2, 4 or 8 for E <= 8, 16, 32 or more; the rest of the 8 warps run along
@@ -596,7 +597,7 @@ bool route_uses_small_kernel(int d, int E) { return E <= 32 && int64_t(d) * E * 
 
 cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const float* bias, int T, int d, int E,
                          int k, int n_shared, int n_groups, int topk_groups, int32_t* topk_idx, float* topk_gate,
-                         float* scratch, int32_t* hist, int32_t* near_ties, cudaStream_t stream) {
+                         float* scratch, int32_t* hist, int32_t* near_ties, int32_t* status, cudaStream_t stream) {
     const RouteCounts cnt{hist, dispatch_blocks(int64_t(T) * (k + n_shared)), near_ties};
     if (route_uses_small_kernel(d, E))
         return act_dtype == MOE_F32
@@ -604,10 +605,17 @@ cudaError_t launch_route(int act_dtype, const void* x, const float* Wg, const fl
                                            topk_gate, cnt, stream)
                    : launch_small_t<__nv_bfloat16>(x, Wg, bias, T, d, E, k, n_shared, n_groups, topk_groups,
                                                    topk_idx, topk_gate, cnt, stream);
-    const int ks = route_k_slices(T, d, E);
-    const int slice = slice_len(d, ks);
-    cudaError_t e = act_dtype == MOE_F32 ? launch_gemm_t<float>(x, Wg, T, d, E, slice, ks, scratch, stream)
-                                         : launch_gemm_t<__nv_bfloat16>(x, Wg, T, d, E, slice, ks, scratch, stream);
+    int ks = 0;
+    cudaError_t e;
+    if (route_uses_tc(act_dtype, d, E)) {
+        void* wsplit = reinterpret_cast<unsigned char*>(scratch) + route_partial_bytes_max(T, E);
+        e = launch_route_tc(x, Wg, T, d, E, scratch, wsplit, status, &ks, stream);
+    } else {
+        ks = route_k_slices(T, d, E);
+        const int slice = slice_len(d, ks);
+        e = act_dtype == MOE_F32 ? launch_gemm_t<float>(x, Wg, T, d, E, slice, ks, scratch, stream)
+                                 : launch_gemm_t<__nv_bfloat16>(x, Wg, T, d, E, slice, ks, scratch, stream);
+    }
     if (e != cudaSuccess) return e;
     const int g2 = (T + 3) / 4;
     const int S = n_shared, G = n_groups, M = topk_groups;
