@@ -476,9 +476,9 @@ def run_ours(args, w, world, rank, local):
         cache = {}
         n_tok = oracle_sample_tokens(w)
         r = oracle_tokens_per_s(w, inp, n_tok, cache=cache)
-        # the same oracle on one thread, on the first tokens of the same sample size
-        # scaled so that it takes about as long as the all-core run did
-        n1 = max(1, min(n_tok, int(round(n_tok / max(1, r["cores"])))))
+        # the same oracle on one thread: on the same sample when the all-core run was
+        # short, else on a sample scaled down by the core count
+        n1 = n_tok if r["seconds"] < 5 else max(1, int(round(n_tok / max(1, r["cores"]))))
         r1 = oracle_tokens_per_s(w, inp, n1, cache=cache, threads=1)
         cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                "sample": f"{r['tokens']} random tokens of the workload, float64 numpy oracle "

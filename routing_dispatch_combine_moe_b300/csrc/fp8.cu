@@ -21,9 +21,11 @@
 // accumulator). The expert weights take the same format, one scale per weight row.
 //   gather_fp8_row_kernel  one CTA per token: amax over the row, then the codes to
 //                          each kept row and the scale;
-//   quantize_rows_kernel   one warp per row of a bf16 matrix: the W13 and W2 weights
-//                          (once), and h between the two expert GEMMs when the down
-//                          projection runs on e4m3 too.
+//   quantize_rows_cta_kernel / quantize_rows_kernel   a bf16 matrix row by row (one
+//                          CTA per row held in registers, read once; one warp per row
+//                          for short or very long rows): the W13 and W2 weights (once),
+//                          and h between the two expert GEMMs when the down projection
+//                          runs on e4m3 too.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -120,6 +122,41 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
     for (int v = lane; v < vpr; v += 32)
         *reinterpret_cast<uint2*>(q + size_t(r) * d + size_t(v) * 8) = e4m3_pack8(__ldg(src + v), s);
     if (lane == 0) scale[r] = ldexpf(1.f, s);
+}
+
+// One CTA of 256 threads per row, for rows of at most 256 * VPT 16-byte pieces: each
+// thread keeps its VPT pieces in registers, so the row is read from memory once; the
+// amax is reduced over the CTA, then the same registers are converted and stored.
+template <int VPT>
+__global__ void __launch_bounds__(256) quantize_rows_cta_kernel(const uint4* __restrict__ w, int d,
+                                                                uint8_t* __restrict__ q, float* __restrict__ scale) {
+    __shared__ float am_w[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t r = blockIdx.x;
+    const int vpr = d / 8;
+    const uint4* src = w + size_t(r) * vpr;
+    uint4 raw[VPT];
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int v = tid + 256 * i;
+        raw[i] = v < vpr ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        am = fmaxf(am, absmax8(raw[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, off));
+    if (lane == 0) am_w[warp] = am;
+    __syncthreads();
+    am = am_w[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) am = fmaxf(am, am_w[i]);
+    const int s = block_exponent(am);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int v = tid + 256 * i;
+        if (v < vpr) *reinterpret_cast<uint2*>(q + size_t(r) * d + size_t(v) * 8) = e4m3_pack8(raw[i], s);
+    }
+    if (tid == 0) scale[r] = ldexpf(1.f, s);
 }
 
 __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ x,
@@ -233,8 +270,17 @@ cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream) {
 cudaError_t launch_quantize_rows_fp8(const void* w, int64_t n_rows, int d, uint8_t* q, float* scale,
                                      cudaStream_t stream) {
     if (n_rows <= 0) return cudaSuccess;
-    quantize_rows_kernel<<<unsigned((n_rows + 7) / 8), 256, 0, stream>>>(static_cast<const uint4*>(w), n_rows, d, q,
-                                                                         scale);
+    const uint4* src = static_cast<const uint4*>(w);
+    const int vpr = d / 8;
+    // rows of up to 16384 elements: one CTA per row, read once; longer rows: one warp per row
+    if (n_rows <= int64_t(INT32_MAX) && vpr > 256 * 4 && vpr <= 256 * 8)
+        quantize_rows_cta_kernel<8><<<unsigned(n_rows), 256, 0, stream>>>(src, d, q, scale);
+    else if (n_rows <= int64_t(INT32_MAX) && vpr > 256 * 2 && vpr <= 256 * 4)
+        quantize_rows_cta_kernel<4><<<unsigned(n_rows), 256, 0, stream>>>(src, d, q, scale);
+    else if (n_rows <= int64_t(INT32_MAX) && vpr > 256 && vpr <= 256 * 2)
+        quantize_rows_cta_kernel<2><<<unsigned(n_rows), 256, 0, stream>>>(src, d, q, scale);
+    else
+        quantize_rows_kernel<<<unsigned((n_rows + 7) / 8), 256, 0, stream>>>(src, n_rows, d, q, scale);
     return cudaGetLastError();
 }
 
