@@ -204,7 +204,9 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
     ident = w.expert == "identity"
     f8g = w.dispatch_dtype == "fp8_gemm"
     dispatch = sizing.dispatch_hbm_bytes(w.T, w.d, rows, b) + (2 * rows_sent * w.d * b if w.dedup else 0)
-    if w.dispatch_dtype == "fp8":
+    if w.dispatch_dtype == "fp8" and w.dedup:  # the send rows travel as codes + block scales
+        dispatch += 2 * rows_sent * (fp8_row_bytes(w.d) - w.d * b)
+    elif w.dispatch_dtype == "fp8":
         dispatch += 2 * routed_rows * fp8_row_bytes(w.d)
     if f8g:  # x read once, each row written as codes + one scale
         dispatch = dispatch - rows * w.d * b + rows * fp8_row_bytes(w.d, per_row=True)
@@ -501,8 +503,11 @@ def run_ours(args, w, world, rank, local):
     routed_rows = int(kept[:w.E].sum())
     fp8 = None
     if w.dispatch_dtype == "fp8":
-        fp8 = {"wire_bytes": routed_rows * fp8_row_bytes(w.d), "bf16_wire_bytes": routed_rows * w.d * 2,
+        sent = dedup["rows_sent"] if dedup else routed_rows  # with dedup the FP8 rows are the send rows
+        fp8 = {"wire_bytes": sent * fp8_row_bytes(w.d), "bf16_wire_bytes": sent * w.d * 2,
                "ratio": fp8_row_bytes(w.d) / (w.d * 2)}
+        if dedup:
+            dedup["remote_send_bytes_fp8"] = int((dedup["rows_sent"] - int(send_counts[0])) * fp8_row_bytes(w.d))
     if w.dispatch_dtype == "fp8_gemm":
         fp8 = {"format": "e4m3 codes + one power-of-two scale per row, read as they are by the e4m3 up GEMM",
                "wire_bytes": rows * fp8_row_bytes(w.d, True), "bf16_wire_bytes": rows * w.d * 2,

@@ -145,7 +145,9 @@ typedef struct moe_config {
     int32_t dedup;       /* 1: moe_layer_forward sends each token once per virtual rank (the
                           * deduplicated dispatch, see moe_dispatch_dedup) and fans the send rows
                           * out into the expert rows; D <= 16. 0: rows go straight from x. */
-    int32_t dispatch_dtype; /* MOE_DISPATCH_*; the FP8 formats need bf16 activations and no dedup */
+    int32_t dispatch_dtype; /* MOE_DISPATCH_*; the FP8 formats need bf16 activations, and
+                             * MOE_DISPATCH_FP8_GEMM no dedup (with dedup, MOE_DISPATCH_FP8 sends
+                             * the deduplicated rows as FP8, see moe_dispatch_dedup_fp8) */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
@@ -183,11 +185,14 @@ typedef struct moe_workspace_view {
                           * padded layout the forward computes kept rows only and leaves the
                           * padding rows of out unwritten */
     moe_send_map send;   /* cfg->dedup only (NULL pointers otherwise) */
-    void* xsend;         /* [T*D, d] act: the deduplicated send buffer (cfg->dedup only) */
+    void* xsend;         /* [T*D, d] act: the deduplicated send buffer (cfg->dedup only); with
+                          * MOE_DISPATCH_FP8 it holds the send rows' e4m3 codes [T*D, d] uint8 */
     uint8_t* xq;         /* [rows, d] e4m3 codes of the dispatched rows (MOE_DISPATCH_FP8: routed rows;
-                          * MOE_DISPATCH_FP8_GEMM: all rows); NULL for MOE_DISPATCH_ACT */
-    float* xscale;       /* their scales: [rows, ceil(d/128)] block scales (MOE_DISPATCH_FP8) or [rows]
-                          * row scales (MOE_DISPATCH_FP8_GEMM); NULL for MOE_DISPATCH_ACT */
+                          * MOE_DISPATCH_FP8_GEMM: all rows); with cfg->dedup and MOE_DISPATCH_FP8 the
+                          * send rows' codes [T*D, d] (= xsend); NULL for MOE_DISPATCH_ACT */
+    float* xscale;       /* their scales: [rows, ceil(d/128)] block scales (MOE_DISPATCH_FP8; with
+                          * cfg->dedup [T*D, ceil(d/128)] of the send rows) or [rows] row scales
+                          * (MOE_DISPATCH_FP8_GEMM); NULL for MOE_DISPATCH_ACT */
     uint8_t* hq;         /* [rows, F] e4m3 codes of h (MOE_PRECISION_FP8_H only, else NULL) */
     float* hscale;       /* [rows] their row scales (MOE_PRECISION_FP8_H only, else NULL) */
     int32_t* n_near_ties; /* one int the forward's router writes: tokens whose k-th and (k+1)-th
@@ -287,6 +292,24 @@ int moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
 int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
                        const moe_send_map* map, void* xsend, void* xperm, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
+
+/* The deduplicated dispatch with FP8 send rows, for cfg->dedup with MOE_DISPATCH_FP8
+ * ("MoE Expert Parallelism Sizing", "First-order dispatch and combine bytes": the
+ * deduplicated rows, and the FP8 rows with their scale tensors): the same send map as
+ * moe_dispatch_dedup, but each send row is the token's row quantized once, per
+ * 128-element block, by the rule of moe_dispatch_fp8 (e4m3 codes and a power-of-two
+ * scale per block), so the bytes crossing to other ranks are d + 4 * ceil(d/128) per
+ * send row. The receiving side turns each kept routed assignment's send row back into
+ * bf16 (exactly q * 2^s) as it fans it out into xperm; shared experts' rows come from x.
+ * xperm then equals what moe_dispatch_fp8 writes for the same map.
+ *   x, topk_idx, pos, map, xperm, ws: as for moe_dispatch_dedup
+ *   xsend_q     [T*D, d] uint8 out: the send rows' codes (rows [0, send_offsets[D]) written)
+ *   xsend_scale [T*D, ceil(d/128)] fp32 out: their block scales
+ * MOE_ERR_ARG unless cfg->dedup and MOE_DISPATCH_FP8 (and then moe_dispatch_dedup
+ * rejects the config). Bit-exact and deterministic. */
+int moe_dispatch_dedup_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
+                           const moe_send_map* map, uint8_t* xsend_q, float* xsend_scale, void* xperm, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
 
 /* FP8 dispatch of the rows a moe_dispatch with the same cfg mapped (its pos, row_src
  * and offsets).

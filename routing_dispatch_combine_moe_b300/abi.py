@@ -95,6 +95,8 @@ _SIGNATURES = {
                                                     _p]),
     "moe_dispatch_dedup": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_send_map), _p,
                                           _p, _p, _sz, _p]),
+    "moe_dispatch_dedup_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_send_map),
+                                              _p, _p, _p, _p, _sz, _p]),
     "moe_dispatch_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
                                         _p, _p, _p, _sz, _p]),
     "moe_fp8_weight_bytes": (_sz, [ctypes.POINTER(moe_config)]),
@@ -312,6 +314,13 @@ def moe_dispatch_dedup(cfg, x, topk_idx, pos, smap: moe_send_map, xsend, xperm, 
     _check(lib().moe_dispatch_dedup(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(pos), ctypes.byref(smap),
                                     _ptr(xsend), _ptr(xperm), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_dispatch_dedup")
+
+
+def moe_dispatch_dedup_fp8(cfg, x, topk_idx, pos, smap: moe_send_map, xsend_q, xsend_scale, xperm, ws, stream=None):
+    """Deduplicated send buffer as e4m3 codes + per-128 block scales, dequantized into xperm by the fan-out."""
+    _check(lib().moe_dispatch_dedup_fp8(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(pos), ctypes.byref(smap),
+                                        _ptr(xsend_q), _ptr(xsend_scale), _ptr(xperm), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "moe_dispatch_dedup_fp8")
 
 
 def moe_dispatch_fp8(cfg, x, topk_idx, dmap: moe_dispatch_map, xq, xscale, xperm, ws, stream=None):

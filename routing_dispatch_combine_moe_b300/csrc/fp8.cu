@@ -246,7 +246,93 @@ __global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t* __restr
     }
 }
 
+// bf16 values of the 8 e4m3 codes of `c` times the scale sc (exact: q * 2^s is a bf16).
+__device__ __forceinline__ uint4 e4m3_unpack8(const uint2 c, float sc) {
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = i < 4 ? c.x : c.y;
+        const __nv_fp8_storage_t code = __nv_fp8_storage_t((w >> (8 * (i & 3))) & 0xFFu);
+        const __half_raw h = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);
+        f[i] = __half2float(__half(h)) * sc;
+    }
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// The deduplicated dispatch's receiving side with FP8 send rows: one warp per token; each
+// kept routed assignment's row is the dequantized send row of (token, rank of its expert),
+// each shared expert's row is x[t].
+__global__ void __launch_bounds__(256) fanout_fp8_kernel(const uint4* __restrict__ x,
+                                                         const uint8_t* __restrict__ xq,
+                                                         const float* __restrict__ xscale,
+                                                         const int32_t* __restrict__ topk_idx,
+                                                         const int32_t* __restrict__ pos,
+                                                         const int32_t* __restrict__ send_pos,
+                                                         uint4* __restrict__ xperm, int T, int K, int E_routed, int D,
+                                                         int d, int64_t max_rows, int64_t max_send, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int nb = (d + 127) / 128, vpr = d / 8;
+    int dst = -1, src = -1;  // src >= 0: send row; src == -2: x[t]
+    if (lane < K) {
+        const size_t a = size_t(t) * K + lane;
+        const int p = pos[a], e = topk_idx[a];
+        if (p >= 0 && p < max_rows) {
+            if (e >= 0 && e < E_routed) {
+                const int sr = send_pos[size_t(t) * D + e / (E_routed / D)];
+                if (sr >= 0 && sr < max_send) {
+                    dst = p;
+                    src = sr;
+                } else {
+                    set_status(status, MOE_DEV_ERR_INDEX);
+                }
+            } else {
+                dst = p;
+                src = -2;
+            }
+        } else if (p >= max_rows) {
+            set_status(status, MOE_DEV_ERR_INDEX);
+        }
+    }
+    for (int j = 0; j < K; ++j) {
+        const int dj = __shfl_sync(0xFFFFFFFFu, dst, j);
+        const int sj = __shfl_sync(0xFFFFFFFFu, src, j);
+        if (dj < 0) continue;
+        uint4* to = xperm + size_t(dj) * vpr;
+        if (sj == -2) {
+            const uint4* from = x + size_t(t) * vpr;
+            for (int v = lane; v < vpr; v += 32) to[v] = __ldg(from + v);
+        } else {
+            const uint8_t* q = xq + size_t(sj) * d;
+            const float* sc = xscale + size_t(sj) * nb;
+            for (int v = lane; v < vpr; v += 32)
+                to[v] = e4m3_unpack8(*reinterpret_cast<const uint2*>(q + size_t(v) * 8), __ldg(sc + (v * 8) / 128));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_fp8_send(const void* x, const int32_t* slots, const int32_t* send_pos, int T, int D, int d,
+                            int64_t max_send, uint8_t* xq, float* xscale, int32_t* status, cudaStream_t stream) {
+    // the slots array stands for the ids: slot r of a token holds r (a "routed" expert of
+    // the D ranks) or -1, so every send row is quantized and none is copied as it is
+    gather_fp8_kernel<<<(T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(x), slots, send_pos, T, D, d, D,
+                                                        max_send, xq, xscale, nullptr, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_fanout(const void* x, const uint8_t* xq, const float* xscale, const int32_t* topk_idx,
+                              const int32_t* pos, const int32_t* send_pos, void* xperm, int T, int K, int E_routed,
+                              int D, int d, int64_t max_rows, int64_t max_send, int32_t* status,
+                              cudaStream_t stream) {
+    fanout_fp8_kernel<<<(T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(x), xq, xscale, topk_idx, pos,
+                                                        send_pos, static_cast<uint4*>(xperm), T, K, E_routed, D, d,
+                                                        max_rows, max_send, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream) {
     if (a.per_row) {

@@ -96,7 +96,9 @@ struct DedupArgs {
     int32_t* send_offsets;     // [D+1]
     int32_t* send_pos;         // [T*D]
     int32_t* send_src;         // [T*D]
-    void* xsend;               // [T*D, d]
+    void* xsend;               // [T*D, d] act, or (fp8) its e4m3 codes [T*D, d] uint8
+    float* xsend_scale;        // fp8: [T*D, ceil(d/128)] block scales of the send rows
+    bool fp8;                  // send rows as e4m3 + per-128 block scales; the fan-out dequantizes
     void* xperm;
     int32_t* status;
     // scratch
@@ -131,6 +133,16 @@ struct Fp8Args {
 };
 
 cudaError_t launch_fp8_dispatch(const Fp8Args& a, cudaStream_t stream);
+// The deduplicated dispatch's FP8 legs: x rows quantized once per (token, rank) slot into
+// the send buffer (slots[t*D + r] = r or -1, send_pos from the send-map scatter), and the
+// receiving side's fan-out: each kept routed assignment's row dequantized from its send
+// row into xperm (exactly q * 2^s), shared experts' rows copied from x.
+cudaError_t launch_fp8_send(const void* x, const int32_t* slots, const int32_t* send_pos, int T, int D, int d,
+                            int64_t max_send, uint8_t* xq, float* xscale, int32_t* status, cudaStream_t stream);
+cudaError_t launch_fp8_fanout(const void* x, const uint8_t* xq, const float* xscale, const int32_t* topk_idx,
+                              const int32_t* pos, const int32_t* send_pos, void* xperm, int T, int K, int E_routed,
+                              int D, int d, int64_t max_rows, int64_t max_send, int32_t* status,
+                              cudaStream_t stream);
 // Row-scaled e4m3 codes [n_rows, d] and scales [n_rows] of a bf16 matrix [n_rows, d].
 cudaError_t launch_quantize_rows_fp8(const void* w, int64_t n_rows, int d, uint8_t* q, float* scale,
                                      cudaStream_t stream);

@@ -131,7 +131,8 @@ int validate(const moe_config* c) {
     if (c->dispatch_dtype != MOE_DISPATCH_ACT && c->dispatch_dtype != MOE_DISPATCH_FP8 &&
         c->dispatch_dtype != MOE_DISPATCH_FP8_GEMM)
         return MOE_ERR_ARG;
-    if ((fp8_blocks(c) || fp8_gemm(c)) && (c->act_dtype != MOE_BF16 || c->dedup)) return MOE_ERR_UNSUPPORTED;
+    if ((fp8_blocks(c) || fp8_gemm(c)) && c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (fp8_gemm(c) && c->dedup) return MOE_ERR_UNSUPPORTED;  // dedup sends block-scaled FP8 rows only
     if (fp8_gemm(c) && c->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_UNSUPPORTED;
     if (fp8_gemm(c) && c->d % 16 != 0) return MOE_ERR_ALIGN;  // e4m3 rows of d bytes, 16-byte aligned
     // the FP8 hidden activation goes with the FP8 up projection (bf16 activations), h rows of F bytes
@@ -152,7 +153,7 @@ struct Layout {
         n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
     // deduplicated dispatch (cfg->dedup): scratch in the dispatch part, outputs in the forward part
     size_t dd_slots, dd_hist, dd_kept, dd_drop, dd_routed, dd_rank, dd_ndrop;
-    size_t send_counts, send_offsets, send_pos, send_src, xsend;
+    size_t send_counts, send_offsets, send_pos, send_src, xsend, xsend_scale;
     size_t xq, xscale;  // FP8 dispatch
     size_t hq, hscale;  // FP8 hidden activation
     size_t dispatch_end, forward_end, host_end;
@@ -210,9 +211,10 @@ Layout layout(const moe_config* c) {
     L.send_offsets = take(dd ? sizeof(int32_t) * size_t(c->D + 1) : 0);
     L.send_pos = take(dd ? sizeof(int32_t) * TD : 0);
     L.send_src = take(dd ? sizeof(int32_t) * TD : 0);
-    L.xsend = take(dd ? b * TD * size_t(c->d) : 0);
-    L.xq = take(fp8_blocks(c) || fp8_gemm(c) ? R * size_t(c->d) : 0);
-    L.xscale = take(fp8_blocks(c)  ? sizeof(float) * R * size_t((c->d + 127) / 128)
+    L.xsend = take(dd ? b * TD * size_t(c->d) : 0);  // with FP8: the send rows' e4m3 codes
+    L.xsend_scale = take(dd && fp8_blocks(c) ? sizeof(float) * TD * size_t((c->d + 127) / 128) : 0);
+    L.xq = take((fp8_blocks(c) && !dd) || fp8_gemm(c) ? R * size_t(c->d) : 0);
+    L.xscale = take(fp8_blocks(c) && !dd ? sizeof(float) * R * size_t((c->d + 127) / 128)
                     : fp8_gemm(c) ? sizeof(float) * R
                                   : 0);
     L.hq = take(fp8_h(c) ? R * size_t(c->F) : 0);
@@ -252,8 +254,9 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->send.send_src = dd ? at<int32_t>(ws, L.send_src) : nullptr;
     v->xsend = dd ? at<void>(ws, L.xsend) : nullptr;
     const bool f8 = fp8_blocks(c) || fp8_gemm(c);
-    v->xq = f8 ? at<uint8_t>(ws, L.xq) : nullptr;
-    v->xscale = f8 ? at<float>(ws, L.xscale) : nullptr;
+    // FP8 with the deduplicated dispatch: the codes and scales are the send rows'
+    v->xq = f8 ? at<uint8_t>(ws, dd && fp8_blocks(c) ? L.xsend : L.xq) : nullptr;
+    v->xscale = f8 ? at<float>(ws, dd && fp8_blocks(c) ? L.xsend_scale : L.xscale) : nullptr;
     v->hq = fp8_h(c) ? at<uint8_t>(ws, L.hq) : nullptr;
     v->hscale = fp8_h(c) ? at<float>(ws, L.hscale) : nullptr;
     v->n_near_ties = at<int32_t>(ws, L.near_ties);
@@ -317,7 +320,7 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const f
 
 // Deduplicated send buffer + fan-out into xperm; the scratch lives in the dispatch part of ws.
 int run_dedup(const moe_config* c, const void* x, const int32_t* idx, const int32_t* pos, const moe_send_map* m,
-              void* xsend, void* xperm, void* ws, cudaStream_t s) {
+              void* xsend, void* xperm, void* ws, cudaStream_t s, float* xsend_scale = nullptr) {
     const Layout L = layout(c);
     DedupArgs a{};
     a.T = c->T; a.d = c->d; a.K = n_slots(c); a.E_routed = c->E; a.D = c->D;
@@ -331,6 +334,8 @@ int run_dedup(const moe_config* c, const void* x, const int32_t* idx, const int3
     a.send_pos = m->send_pos;
     a.send_src = m->send_src;
     a.xsend = xsend;
+    a.xsend_scale = xsend_scale;
+    a.fp8 = fp8_blocks(c);
     a.xperm = xperm;
     a.status = at<int32_t>(ws, L.status);
     a.slots = at<int32_t>(ws, L.dd_slots);
@@ -463,10 +468,13 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if ((rc = run_dispatch(c, x, v.topk_idx, v.topk_gate, &v.map, v.xperm, ws, s, c->dedup != 0 || f8, true)) !=
         MOE_OK)
         return rc;
-    if (f8 && (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, fp8_gemm(c) ? nullptr : v.xperm, ws, s)) !=
-                  MOE_OK)
+    // with the deduplicated dispatch the FP8 rows travel in the send buffer (run_dedup)
+    if (f8 && !c->dedup &&
+        (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, fp8_gemm(c) ? nullptr : v.xperm, ws, s)) != MOE_OK)
         return rc;
-    if (c->dedup && (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s)) != MOE_OK)
+    if (c->dedup &&
+        (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s,
+                        fp8_blocks(c) ? at<float>(ws, L.xsend_scale) : nullptr)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
@@ -538,7 +546,8 @@ int moe_kernels_per_forward(const moe_config* cfg) {
     const int pad = cfg->layout == MOE_LAYOUT_PADDED && cfg->capacity > 0 ? 1 : 0;
     const int ffn = cfg->expert_kind == MOE_EXPERT_IDENTITY || rows_cap(cfg) == 0 ? 0 : 2;
     const int dedup = cfg->dedup ? 5 : 0;  // mask, count, scan, scatter, fan-out (the gather goes to xsend)
-    const int fp8 = fp8_blocks(cfg) ? 1 : 0;  // dequant (the gather quantizes; FP8_GEMM rows are used as they are)
+    // dequant (the gather quantizes; FP8_GEMM rows are used as they are; with dedup the fan-out dequantizes)
+    const int fp8 = fp8_blocks(cfg) && !cfg->dedup ? 1 : 0;
     const int fp8h = fp8_h(cfg) && ffn ? 1 : 0;  // h quantized between the two GEMMs
     // fused; or logits + top-k; or (tensor cores) W_g's split + logits + top-k
     const int route = route_uses_small_kernel(cfg->d, cfg->E) ? 1 : (route_uses_tc(cfg->act_dtype, cfg->d, cfg->E) ? 3 : 2);
@@ -586,7 +595,7 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
                        moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
-    if (!cfg->dedup) return MOE_ERR_ARG;
+    if (!cfg->dedup || fp8_blocks(cfg)) return MOE_ERR_ARG;
     if (!x || !topk_idx || !pos || !map || !ws || !map->send_counts || !map->send_offsets || !map->send_pos ||
         !map->send_src || !xsend || (!xperm && rows_cap(cfg) > 0))
         return MOE_ERR_ARG;
@@ -597,6 +606,24 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
     const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     return run_dedup(cfg, x, topk_idx, pos, map, xsend, xperm, ws, stream);
+}
+
+int moe_dispatch_dedup_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
+                           const moe_send_map* map, uint8_t* xsend_q, float* xsend_scale, void* xperm, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!cfg->dedup || !fp8_blocks(cfg)) return MOE_ERR_ARG;
+    if (!x || !topk_idx || !pos || !map || !ws || !map->send_counts || !map->send_offsets || !map->send_pos ||
+        !map->send_src || !xsend_q || !xsend_scale || (!xperm && rows_cap(cfg) > 0))
+        return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(xsend_q) || !aligned4(xsend_scale) || (xperm && !aligned16(xperm)) ||
+        !aligned4(topk_idx) || !aligned4(pos) || !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_dedup(cfg, x, topk_idx, pos, map, xsend_q, xperm, ws, stream, xsend_scale);
 }
 
 int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx, const moe_dispatch_map* map,

@@ -134,6 +134,10 @@ WORKLOADS: dict[str, Workload] = {
                  dispatch_dtype="fp8_gemm",
                  note="the DeepSeek-V3-shaped full layer with FP8 rows and e4m3 up-projection weights "
                       "(15.0 GB of bf16 W13 become 7.5 GB)"),
+        Workload("dsv3_grouped_dedup_fp8", T=4096, d=7168, E=256, k=8, F=0, act="bf16", expert="identity", D=8,
+                 n_groups=8, topk_groups=4, dedup=True, dispatch_dtype="fp8",
+                 note="the group-limited, deduplicated DeepSeek-V3 routing shape with the send rows as e4m3 "
+                      "codes and per-128 power-of-two scales, dequantized by the receiving side's fan-out"),
         Workload("dsv3_e32_slice", T=512, d=7168, E=32, k=8, F=2048, act="bf16", expert="swiglu",
                  note="an eighth of the DeepSeek-V3-shaped layer: the same d, F and k and the same 128 rows per "
                       "expert on average, with 32 experts (2.8 GB of weights), small enough for counter captures"),
@@ -143,7 +147,7 @@ WORKLOADS: dict[str, Workload] = {
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
                   "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm", "dsv3_decode_fp8_gemm",
-                  "dsv3_full_fp8_gemm", "mixtral_fp8_experts", "dsv3_e32_slice"]
+                  "dsv3_full_fp8_gemm", "mixtral_fp8_experts", "dsv3_grouped_dedup_fp8", "dsv3_e32_slice"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

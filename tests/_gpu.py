@@ -146,12 +146,21 @@ class StageBuffers:
             self.send_offsets = torch.full((w.D + 1,), -7, **i32)
             self.send_pos = torch.full((TD,), -7, **i32)
             self.send_src = torch.full((TD,), -7, **i32)
-            self.xsend = torch.full((TD, w.d), float("nan"), dtype=w.torch_act, device=device)
+            if w.dispatch_dtype == "fp8":  # the send rows travel as e4m3 codes + block scales
+                self.xsend = torch.full((TD, w.d), 0xAB, dtype=torch.uint8, device=device)
+                self.xsend_scale = torch.full((TD, (w.d + 127) // 128), float("nan"), dtype=torch.float32,
+                                              device=device)
+            else:
+                self.xsend = torch.full((TD, w.d), float("nan"), dtype=w.torch_act, device=device)
 
     def smap(self):
         return abi.send_map(self.send_counts, self.send_offsets, self.send_pos, self.send_src)
 
     def dedup(self, inp, topk_idx, pos, xperm):
+        if self.cfg.dispatch_dtype == abi.MOE_DISPATCH_FP8:
+            abi.moe_dispatch_dedup_fp8(self.cfg, inp["x"], topk_idx, pos, self.smap(), self.xsend, self.xsend_scale,
+                                       xperm, self.ws_dispatch)
+            return
         abi.moe_dispatch_dedup(self.cfg, inp["x"], topk_idx, pos, self.smap(), self.xsend, xperm, self.ws_dispatch)
 
     def dmap(self):
@@ -437,8 +446,16 @@ def check_dispatch(w, inp, bufs, capacity, st) -> dict:
 def check_dedup(w, inp, bufs, st, d) -> dict:
     """Deduplicated dispatch on the synthetic ids' dispatch map ``d`` (already on the
     GPU in ``bufs``): the send map bit-exact against the oracle, the send rows exact
-    copies of x, and the fanned-out expert rows equal to the direct gather's."""
+    copies of x (FP8: their codes and block scales bit-exact against the oracle's
+    quantization of x), and the fanned-out expert rows equal to the direct gather's
+    (FP8: to the direct FP8 dispatch's dequantized rows)."""
+    fp8 = w.dispatch_dtype == "fp8"
     direct = bufs.xperm.clone()
+    if fp8:  # the direct FP8 dispatch of the same map: routed rows dequantized, shared rows from x
+        direct = torch.full_like(bufs.xperm, float("nan"))
+        xq = torch.empty(bufs.rows, w.d, dtype=torch.uint8, device=direct.device)
+        xs = torch.empty(bufs.rows, (w.d + 127) // 128, dtype=torch.float32, device=direct.device)
+        abi.moe_dispatch_fp8(bufs.cfg, inp["x"], st["topk_idx"], bufs.dmap(), xq, xs, direct, bufs.ws_dispatch)
     fanned = torch.full_like(bufs.xperm, float("nan"))
     bufs.dedup(inp, st["topk_idx"], bufs.pos, fanned)
     s = orc.dedup_send(cpu(st["topk_idx"]).numpy(), d["pos"], w.E, w.D)
@@ -450,9 +467,14 @@ def check_dedup(w, inp, bufs, st, d) -> dict:
     n = s["n_send"]
     np.testing.assert_array_equal(cpu(bufs.send_src).numpy()[:n], s["send_src"])
     src_tok = torch.from_numpy(s["send_src"] // w.D).to(bufs.xsend.device)
-    assert torch.equal(bufs.xsend[:n], inp["x"][src_tok]), "send rows are not exact copies of x"
+    if fp8:
+        q = orc.quantize_fp8_blocks(f64(inp["x"][src_tok]))
+        np.testing.assert_array_equal(cpu(bufs.xsend).numpy()[:n], q["codes"])
+        np.testing.assert_array_equal(cpu(bufs.xsend_scale).numpy().astype(np.float64)[:n], q["scales"])
+    else:
+        assert torch.equal(bufs.xsend[:n], inp["x"][src_tok]), "send rows are not exact copies of x"
     held = torch.from_numpy(np.nonzero(d["row_src"] >= 0)[0]).to(fanned.device)  # padding rows are not sent
-    assert torch.equal(fanned[held], direct[held]), "fanned-out rows differ from the direct gather"
+    assert torch.equal(fanned[held], direct[held]), "fanned-out rows differ from the direct dispatch's"
     return s
 
 
@@ -621,7 +643,7 @@ class WorkspaceMap:
         self.out = None if not view.out else \
             ws[view.out - base:view.out - base + R * w.d * osz].view(odt).view(R, w.d)
         self.out_act = "f32" if odt == torch.float32 else "bf16"
-        if w.dispatch_dtype in ("fp8", "fp8_gemm"):
+        if w.dispatch_dtype in ("fp8", "fp8_gemm") and not w.dedup:
             nb = (w.d + 127) // 128 if w.dispatch_dtype == "fp8" else 1
             self.xq = ws[view.xq - base:view.xq - base + R * w.d].view(R, w.d)
             self.xscale = ws[view.xscale - base:view.xscale - base + 4 * R * nb].view(torch.float32).view(R, nb)
@@ -633,7 +655,13 @@ class WorkspaceMap:
             self.send_offsets = i32(view.send_offsets, w.D + 1)
             self.send_pos = i32(view.send_pos, TD)
             self.send_src = i32(view.send_src, TD)
-            self.xsend = ws[view.xsend - base:view.xsend - base + TD * w.d * esz].view(w.torch_act).view(TD, w.d)
+            if w.dispatch_dtype == "fp8":  # codes [TD, d] and block scales [TD, nb] of the send rows
+                nb = (w.d + 127) // 128
+                self.xsend = ws[view.xsend - base:view.xsend - base + TD * w.d].view(TD, w.d)
+                self.xsend_scale = ws[view.xscale - base:view.xscale - base + 4 * TD * nb].view(torch.float32) \
+                    .view(TD, nb)
+            else:
+                self.xsend = ws[view.xsend - base:view.xsend - base + TD * w.d * esz].view(w.torch_act).view(TD, w.d)
 
 
 def chain(w, inp, cfg) -> StageBuffers:

@@ -176,7 +176,7 @@ def test_workspace_sizes_and_layout():
         small_router = w.E <= 32 and w.d * w.E * 4 <= 128 * 1024  # one fused router launch instead of two
         tc_router = w.act == "bf16" and w.E >= 64 and not small_router  # W_g's split kernel comes first
         assert abi.moe_kernels_per_forward(c) == ((6 if w.expert == "identity" else 8) + (5 if w.dedup else 0)
-                                                  + (1 if w.dispatch_dtype == "fp8" else 0)
+                                                  + (1 if w.dispatch_dtype == "fp8" and not w.dedup else 0)
                                                   + (1 if w.precision == "fp8_h" else 0)  # h quantized between GEMMs
                                                   - (1 if small_router else 0) + (1 if tc_router else 0))
 
@@ -289,7 +289,26 @@ def test_fp8_dispatch_validation_and_workspace():
     f8 = cfg(dispatch_dtype="fp8")
     assert abi.moe_validate_config(f8) == abi.MOE_OK
     assert abi.moe_validate_config(cfg(act="f32", dispatch_dtype="fp8")) == abi.MOE_ERR_UNSUPPORTED
-    assert abi.moe_validate_config(cfg(D=4, dedup=True, dispatch_dtype="fp8")) == abi.MOE_ERR_UNSUPPORTED
+    # the deduplicated dispatch sends its rows as FP8: same kernel count as the bf16 dedup
+    # (the send gather quantizes, the fan-out dequantizes), the send codes and scales in
+    # the view; moe_dispatch_dedup rejects it, moe_dispatch_dedup_fp8 takes it
+    ddf = cfg(D=4, dedup=True, dispatch_dtype="fp8")
+    dd = cfg(D=4, dedup=True)
+    assert abi.moe_validate_config(ddf) == abi.MOE_OK
+    assert abi.moe_kernels_per_forward(ddf) == abi.moe_kernels_per_forward(dd)
+    vd = abi.moe_workspace_view()
+    nd = abi.moe_workspace_bytes(ddf)
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(ddf), 1 << 40, nd, ctypes.byref(vd)) == 0
+    assert vd.xq == vd.xsend and vd.xscale and vd.xscale >= vd.xsend + 64 * 4 * 128
+    m = abi.moe_send_map(*([A16] * 4))
+    assert abi.lib().moe_dispatch_dedup(ctypes.byref(ddf), A16, A16, A16, ctypes.byref(m), A16, A16, A16, nd,
+                                        None) == abi.MOE_ERR_ARG
+    assert abi.lib().moe_dispatch_dedup_fp8(ctypes.byref(dd), A16, A16, A16, ctypes.byref(m), A16, A16, A16, A16,
+                                            nd, None) == abi.MOE_ERR_ARG          # not an FP8 config
+    assert abi.lib().moe_dispatch_dedup_fp8(ctypes.byref(ddf), A16, A16, A16, ctypes.byref(m), MIS, A16, A16, A16,
+                                            nd, None) == abi.MOE_ERR_ALIGN
+    assert abi.lib().moe_dispatch_dedup_fp8(ctypes.byref(ddf), A16, A16, A16, ctypes.byref(m), A16, A16, A16, A16,
+                                            abi.moe_dispatch_workspace_bytes(ddf) - 1, None) == abi.MOE_ERR_WORKSPACE
     c = cfg()
     c.dispatch_dtype = 5
     assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG

@@ -75,3 +75,8 @@ def test_algorithmic_work_of_the_bf16_and_fp8_layers():
     # the down stage reads bf16 h, writes and reads its codes + scales, reads e4m3 W2
     assert both["down_bytes"] == E * d * (F + 4) + rows * F * 2 + 2 * rows * (F + 4) + rows * d * 4
     assert bench.fp8_row_bytes(4096) == 4096 + 4 * 32 and bench.fp8_row_bytes(4096, per_row=True) == 4100
+    # deduplicated FP8 send rows: x read once, each send row written and read as codes +
+    # block scales, each expert row written in bf16
+    T2, d2, rows2, sent = 4096, 7168, 32768, 16000
+    ddf = bench.algorithmic(W["dsv3_grouped_dedup_fp8"], rows2, out_bytes=2, h_cols=0, rows_sent=sent)
+    assert ddf["dispatch_bytes"] == T2 * d2 * 2 + rows2 * d2 * 2 + 2 * sent * (d2 + 4 * 56)

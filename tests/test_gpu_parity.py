@@ -38,6 +38,12 @@ REDUCED = {
     "grouped_dedup_swiglu": wl.Workload("grouped_dedup_swiglu", T=700, d=512, E=64, k=6, F=256, act="bf16",
                                         expert="swiglu", D=8, n_groups=8, topk_groups=3, dedup=True,
                                         capacity_factor="1"),
+    # FP8 send rows with the deduplicated dispatch: identity experts with a ragged last block,
+    # and SwiGLU experts with a shared expert and drops
+    "grouped_dedup_fp8": wl.scaled(W["dsv3_grouped_dedup_fp8"], T=512, d=1088),
+    "grouped_dedup_fp8_swiglu": wl.Workload("grouped_dedup_fp8_swiglu", T=700, d=512, E=64, k=6, F=256,
+                                            act="bf16", expert="swiglu", D=8, n_groups=8, topk_groups=3, dedup=True,
+                                            capacity_factor="1", n_shared=1, dispatch_dtype="fp8"),
     "mixtral_fp8": wl.scaled(W["mixtral_fp8_dispatch"], T=512, d=1024, F=1536),
     "decode_fp8": wl.scaled(W["dsv3_decode"], d=1088, F=256, dispatch_dtype="fp8"),  # ragged last block
     "mixtral_fp8_gemm": wl.scaled(W["mixtral_fp8_gemm"], T=512, d=1024, F=1536),
@@ -107,11 +113,12 @@ def test_layer_forward_matches_oracle(name):
     err = check_layer_close(name, cpu(y)[torch.from_numpy(keep)], ref["y"][keep], w.act, f"{name} layer y",
                             extra=extra)
     print(f"\n{name}: layer max|err|/rms(y) = {err:.4f} (near-tie tokens excluded: {int((~keep).sum())})")
-    if w.expert == "identity":
+    if w.expert == "identity" and w.dispatch_dtype == "act":
         assert torch.equal(y, inp["x"]), "identity experts must return x exactly"
 
 
-@pytest.mark.parametrize("name", ["grouped_dedup", "grouped_dedup_swiglu"])
+@pytest.mark.parametrize("name", ["grouped_dedup", "grouped_dedup_swiglu", "grouped_dedup_fp8",
+                                  "grouped_dedup_fp8_swiglu"])
 def test_dedup_forward_equals_the_direct_forward_bitwise(name):
     """The deduplicated dispatch changes where rows travel, not their values: the layer
     output is the same bits, and the send map in the workspace is the oracle's."""
@@ -364,6 +371,7 @@ FULL["mixtral_fp8_dispatch"] = W["mixtral_fp8_dispatch"]
 FULL["mixtral_fp8_gemm"] = W["mixtral_fp8_gemm"]
 FULL["dsv3_decode_fp8_gemm"] = W["dsv3_decode_fp8_gemm"]
 FULL["mixtral_fp8_experts"] = W["mixtral_fp8_experts"]
+FULL["dsv3_grouped_dedup_fp8"] = W["dsv3_grouped_dedup_fp8"]
 
 
 # Tokens whose y is compared element by element at full size (all of them for the
@@ -394,10 +402,16 @@ def test_full_size_sampled(name):
         np.testing.assert_array_equal(cpu(m.send_pos).numpy(), s["send_pos"])
         np.testing.assert_array_equal(cpu(m.send_src).numpy()[:s["n_send"]], s["send_src"])
         src = torch.from_numpy(s["send_src"] // w.D).cuda()
-        assert torch.equal(m.xsend[:s["n_send"]], inp["x"][src])
+        if w.dispatch_dtype == "fp8":  # codes and block scales of 64 sampled send rows
+            rows = np.random.default_rng(3).choice(s["n_send"], size=min(64, s["n_send"]), replace=False)
+            q = orc.quantize_fp8_blocks(f64(inp["x"][src[torch.from_numpy(rows).cuda()]]))
+            np.testing.assert_array_equal(cpu(m.xsend).numpy()[rows], q["codes"])
+            np.testing.assert_array_equal(cpu(m.xsend_scale).numpy().astype(np.float64)[rows], q["scales"])
+        else:
+            assert torch.equal(m.xsend[:s["n_send"]], inp["x"][src])
         print(f"\n{name}: {s['n_send']} send rows, {s['n_send'] / w.T:.3f} ranks per token")
     fp8 = w.dispatch_dtype == "fp8"
-    if fp8 and how == "exact":
+    if fp8 and how == "exact" and not w.dedup:
         # codes and scales of 64 sampled routed rows against the oracle's quantization
         rows = np.nonzero(d["row_src"] >= 0)[0]
         rows = np.random.default_rng(1).choice(rows, size=min(64, rows.size), replace=False)
@@ -405,7 +419,7 @@ def test_full_size_sampled(name):
         q = orc.quantize_fp8_blocks(f64(inp["x"][torch.from_numpy(tok).cuda()]))
         np.testing.assert_array_equal(cpu(m.xq).numpy()[rows], q["codes"])
         np.testing.assert_array_equal(cpu(m.xscale).numpy().astype(np.float64)[rows], q["scales"])
-    if w.expert == "identity":
+    if w.expert == "identity" and w.dispatch_dtype == "act":
         assert torch.equal(y, inp["x"])
         return
     # expert outputs of a few whole experts (largest, smallest non-empty, two more); with
