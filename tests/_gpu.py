@@ -92,13 +92,13 @@ def check_close(got, exact, act: str, what: str, tol: float | None = None, extra
     return float(err.max() / r) if r > 0 else 0.0
 
 
-def check_layer_close(name: str, got, exact, act: str, what: str, extra=None) -> float:
+def check_layer_close(name: str, got, exact, act: str, what: str, extra=None, whole: bool = True) -> float:
     """The layer tolerance for workload ``name``: the literal bound, or, where no output
-    in the activation dtype can meet it (the ROUNDING_LIMITED workloads, for which this
-    is asserted, and any layer whose own exact output shows it), the bound plus the
-    output half-ulp."""
+    in the activation dtype can meet it (any layer whose exact output shows it; for the
+    ROUNDING_LIMITED workloads this is asserted when ``whole`` output is compared, not on
+    a token sample, whose own tail may be lighter), the bound plus the output half-ulp."""
     limited = rounding_limited(exact, act, TOL[act])
-    if name in ROUNDING_LIMITED:
+    if name in ROUNDING_LIMITED and whole:
         assert limited, f"{name} is listed as rounding-limited but is not"
     return check_close(got, exact, act, what, extra=extra, with_half_ulp=limited)
 

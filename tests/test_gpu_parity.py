@@ -374,9 +374,10 @@ FULL["mixtral_fp8_experts"] = W["mixtral_fp8_experts"]
 FULL["dsv3_grouped_dedup_fp8"] = W["dsv3_grouped_dedup_fp8"]
 
 
-# Tokens whose y is compared element by element at full size (all of them for the
-# 128-token decode layers).
+# Tokens whose y is compared element by element at full size: 256 on the DeepSeek-V3-shaped
+# layer, 64 on the others (all of them for the 128-token decode layers).
 SAMPLED_TOKENS = 256
+SAMPLED_TOKENS_OTHERS = 64
 
 
 @pytest.mark.parametrize("name", list(FULL))
@@ -462,10 +463,11 @@ def test_full_size_sampled(name):
     ok &= ~flipped
     rng = np.random.default_rng(0)
     cand = np.nonzero(ok)[0]
-    tokens = sorted(rng.choice(cand, size=min(SAMPLED_TOKENS, cand.size), replace=False).tolist())
+    n_tok = SAMPLED_TOKENS if name == "dsv3_full" else SAMPLED_TOKENS_OTHERS
+    tokens = sorted(rng.choice(cand, size=min(n_tok, cand.size), replace=False).tolist())
     y_s, budget = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
     err = check_layer_close(name, y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y",
-                            extra=budget)
+                            extra=budget, whole=False)
     print(f"\n{name}: near-ties={r['near_ties']} (GPU count of k-th/(k+1)-th ties: {n_ties}) flipped={r['flipped']} "
           f"dispatch={how} ffn_err/rms={worst_ffn} sampled y err/rms={err:.4f} over {len(tokens)} tokens "
           f"dropped={d['n_dropped']}")
