@@ -409,15 +409,19 @@ def e4m3_values() -> np.ndarray:
 def _e4m3_round(a) -> np.ndarray:
     """Code of the nearest finite e4m3 value to each element: the magnitude is rounded
     to the nearest of the codes 0x00..0x7E (ties: the even code), then the sign bit is
-    set for negative inputs (-0.0 included), as an IEEE-style rounding does."""
+    set for negative inputs (-0.0 included), as an IEEE-style rounding does.
+
+    Code c (0 <= c < 0x7E) is nearest for the magnitudes from the midpoint between
+    codes c - 1 and c to the midpoint between c and c + 1; a magnitude exactly on a
+    midpoint goes to the even code of the two; magnitudes at or past the midpoint
+    below 448 go to 448 (0x7E), the largest finite value."""
     a = np.asarray(a, np.float64)
     mags = e4m3_values()[:0x7F]           # codes 0x00..0x7E, increasing magnitudes
+    mid = (mags[:-1] + mags[1:]) / 2.0    # mid[c] lies between codes c and c + 1
     m = np.abs(a).ravel()
-    hi = np.clip(np.searchsorted(mags, m), 1, 0x7E)
-    lo = hi - 1
-    dlo, dhi = m - mags[lo], mags[hi] - m
-    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
-    pick = np.where(m >= mags[-1], 0x7E, pick)
+    pick = np.searchsorted(mid, m, side="left")        # the first code whose upper midpoint is >= m
+    on_mid = (pick < mid.size) & (m == mid[np.minimum(pick, mid.size - 1)])
+    pick = pick + (on_mid & (pick % 2 == 1))           # a tie between codes pick and pick + 1: the even one
     neg = np.signbit(a.ravel())
     return (pick | np.where(neg, 0x80, 0)).astype(np.uint8).reshape(a.shape)
 
@@ -431,26 +435,25 @@ def quantize_fp8_blocks(x, block: int = 128) -> dict:
     x = _f64(x)
     rows, d = x.shape
     nb = -(-d // block)
-    exps = np.zeros((rows, nb), np.int64)
-    codes = np.zeros((rows, d), np.uint8)
-    deq = np.zeros_like(x)
+    # every block of every row at once: the row padded with zeros to nb whole blocks (a
+    # zero changes no block's amax; the padding's codes are dropped)
+    xb = np.zeros((rows, nb * block))
+    xb[:, :d] = x
+    xb = xb.reshape(rows, nb, block)
+    amax = np.abs(xb).max(axis=2)
+    nz = amax > 0
+    s = np.zeros((rows, nb), np.int64)
+    s[nz] = np.ceil(np.log2(amax[nz] / 448.0)).astype(np.int64)
+    while True:  # guard the log against rounding: the smallest s with amax / 2^s <= 448
+        up = nz & (np.ldexp(amax, -s) > 448.0)
+        down = nz & (np.ldexp(amax, -(s - 1)) <= 448.0)
+        if not (up.any() or down.any()):
+            break
+        s = s + up - down
+    codes = _e4m3_round(np.ldexp(xb, -s[:, :, None])).reshape(rows, nb * block)[:, :d]
     vals = e4m3_values()
-    for r in range(rows):
-        for b in range(nb):
-            seg = x[r, b * block:(b + 1) * block]
-            amax = np.abs(seg).max()
-            s = 0
-            if amax > 0:
-                s = math.ceil(math.log2(amax / 448.0))
-                while amax / 2.0 ** s > 448.0:  # guard the log against rounding
-                    s += 1
-                while amax / 2.0 ** (s - 1) <= 448.0:
-                    s -= 1
-            exps[r, b] = s
-            c = _e4m3_round(seg / 2.0 ** s)
-            codes[r, b * block:(b + 1) * block] = c
-            deq[r, b * block:(b + 1) * block] = vals[c] * 2.0 ** s
-    return dict(codes=codes, exps=exps, scales=2.0 ** exps, deq=deq)
+    deq = np.ldexp(vals[codes].reshape(rows, -1), np.repeat(s, block, axis=1)[:, :d])
+    return dict(codes=np.ascontiguousarray(codes), exps=s, scales=np.ldexp(1.0, s), deq=deq)
 
 
 def quantize_fp8_rows(x, chunk: int = 2048) -> dict:
