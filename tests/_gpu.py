@@ -236,8 +236,12 @@ def fp8_h_budget(w, inp, e, X) -> np.ndarray:
     weights are kept in ``inp`` after first use."""
     cache = inp.setdefault("_fp8_h_budget_cache", {})
     if e not in cache:
-        w13q = orc.quantize_fp8_rows(f64(inp["W13"][e]))["deq"]
-        w2q = orc.quantize_fp8_rows(f64(inp["W2"][e]))["deq"]  # [d, F]
+        shared = inp.get("_expert_cache", {})  # the expert function's quantized weights, if it ran first
+        if e in shared:
+            w13q, w2q = shared[e]
+        else:
+            w13q = orc.quantize_fp8_rows(f64(inp["W13"][e]))["deq"]
+            w2q = orc.quantize_fp8_rows(f64(inp["W2"][e]))["deq"]  # [d, F]
         cache[e] = (w13q, np.abs(w2q).T.astype(np.float32))
     w13q, w2abs = cache[e]
     X = np.asarray(X, np.float64)

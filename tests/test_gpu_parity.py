@@ -345,7 +345,10 @@ def _sampled_y(w, inp, ref_route, disp, tokens):
     if fp8_gemm:  # every row, shared ones too, is the row-quantized token
         x = xq = orc.quantize_fp8_rows(x)["deq"]
     idx, G, pos = ref_route["idx"], ref_route["G"], disp["pos"].reshape(w.T, w.slots)
-    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm, fp8_h=w.precision == "fp8_h")
+    # the FP8 hidden activation's budget reuses the quantized weights (kept for that layer only:
+    # the float64 weights of every expert of the larger layers would not fit the host)
+    fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm, fp8_h=w.precision == "fp8_h",
+                   cache=inp.setdefault("_expert_cache", {}) if w.precision == "fp8_h" else None)
     need = {}
     for r, t in enumerate(tokens):
         for j in range(w.slots):
@@ -375,7 +378,7 @@ FULL["dsv3_grouped_dedup_fp8"] = W["dsv3_grouped_dedup_fp8"]
 
 
 # Tokens whose y is compared element by element at full size: 256 on the DeepSeek-V3-shaped
-# layer, 64 on the others (all of them for the 128-token decode layers).
+# layer, 64 on the others, fewer on the FP8-GEMM layers (below).
 SAMPLED_TOKENS = 256
 SAMPLED_TOKENS_OTHERS = 64
 
@@ -435,7 +438,8 @@ def test_full_size_sampled(name):
         if w.precision == "fp8_h":  # the code-flip budget costs a second pass per expert: two experts
             pick = sorted({int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])})
         fp8_gemm = w.dispatch_dtype == "fp8_gemm"
-        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm, fp8_h=w.precision == "fp8_h")
+        fn = expert_fn(w.expert, inp["W13"], inp["W2"], w.F, fp8_up=fp8_gemm, fp8_h=w.precision == "fp8_h",
+                       cache=inp.setdefault("_expert_cache", {}) if w.precision == "fp8_h" else None)
         worst_ffn = 0.0
         for e in pick:
             lo = int(d["offsets"][e])
@@ -464,6 +468,10 @@ def test_full_size_sampled(name):
     rng = np.random.default_rng(0)
     cand = np.nonzero(ok)[0]
     n_tok = SAMPLED_TOKENS if name == "dsv3_full" else SAMPLED_TOKENS_OTHERS
+    if w.dispatch_dtype == "fp8_gemm" and w.expert != "identity":
+        # the oracle quantizes every expert a sampled token uses (2F x d weights each, in
+        # float64): 8 tokens, 4 on the decode layer, whose tokens touch 9 of 257 experts each
+        n_tok = 4 if w.T <= 128 else 8
     tokens = sorted(rng.choice(cand, size=min(n_tok, cand.size), replace=False).tolist())
     y_s, budget = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
     err = check_layer_close(name, y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y",
@@ -498,6 +506,55 @@ def test_layer_forward_replays_in_a_cuda_graph(name):
         fwd()
         torch.cuda.synchronize()
         assert torch.equal(y_graph, y)
+
+
+def test_forward_from_two_host_threads_shares_the_context_setup():
+    """Kernel attributes, cluster occupancy and the static dispatch scratch address are set
+    up once per CUDA context and then looked up: two host threads calling the layer (and the
+    static dispatch) on the same device, each on its own stream, must find that setup and
+    give the same bits as one thread does."""
+    import threading
+    w = REDUCED["dsv3_full"]
+    inp = wl.make_inputs(w, 19, device="cuda")
+    cfg = abi.config_for(w)
+    y_ref, _, _, _ = run_layer(cfg, inp, w)
+    torch.cuda.synchronize()
+    results, errors = {}, []
+    static_lock = threading.Lock()  # static-dispatch calls share one scratch array: never overlap them
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                ws = abi.workspace(cfg)
+                y = torch.empty_like(y_ref)
+                for _ in range(3):
+                    abi.moe_layer_forward(cfg, inp["x"], inp["Wg"], None, inp["W13"], inp["W2"], y, ws,
+                                          stream=stream)
+                b = StageBuffers(w, cfg)
+                b.route(inp)
+                with static_lock:
+                    abi.moe_dispatch_static(cfg, inp["x"], b.topk_idx, b.dmap(), b.xperm, stream=stream,
+                                            topk_gate=b.topk_gate)
+                    stream.synchronize()
+            stream.synchronize()
+            results[i] = (y, b)
+        except Exception as exc:  # noqa: BLE001 - reported below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert abi.lib().moe_last_cuda_error() in (b"", None)
+    for i in range(2):
+        y, b = results[i]
+        assert torch.equal(y, y_ref)
+    assert torch.equal(results[0][1].offsets, results[1][1].offsets)
+    assert torch.equal(results[0][1].pos, results[1][1].pos)
 
 
 def test_async_host_forward_on_two_streams_matches_the_device_forward():
