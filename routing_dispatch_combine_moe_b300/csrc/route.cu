@@ -280,16 +280,32 @@ template <int VPL>
 __device__ __forceinline__ void limit_groups(float (&v)[VPL], int lane, int E, int G, int M) {
     const int gs = E / G;
     float score = -INFINITY;
-    for (int g = 0; g < G; ++g) {
-        float m = -INFINITY;
+    if (gs % 32 == 0) {
+        // every register slot q lies in one group, q / (gs / 32): reduce the slots over the
+        // warp (independent reductions) and take each group's largest
+        float wq[VPL];
 #pragma unroll
-        for (int q = 0; q < VPL; ++q) {
-            const int e = lane + 32 * q;
-            if (e < E && e / gs == g) m = fmaxf(m, v[q]);
+        for (int q = 0; q < VPL; ++q) wq[q] = lane + 32 * q < E ? v[q] : -INFINITY;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int q = 0; q < VPL; ++q) wq[q] = fmaxf(wq[q], __shfl_xor_sync(0xFFFFFFFFu, wq[q], off));
+        const int qpg = gs / 32;
+#pragma unroll
+        for (int q = 0; q < VPL; ++q)
+            if (q / qpg == lane) score = fmaxf(score, wq[q]);
+    } else {
+        for (int g = 0; g < G; ++g) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < VPL; ++q) {
+                const int e = lane + 32 * q;
+                if (e < E && e / gs == g) m = fmaxf(m, v[q]);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+            if (lane == g) score = m;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-        if (lane == g) score = m;
     }
     uint32_t kept = 0;
     for (int r = 0; r < M; ++r) {
