@@ -349,8 +349,13 @@ int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_i
  * bf16 runs on the tensor cores (bf16 x bf16 products, fp32 accumulation); fp32
  * runs on the fp32 FMA units. Requires F * sizeof(act) % 16 == 0 besides the row
  * rule. ws >= moe_ffn_workspace_bytes(cfg); its first 4 bytes are the status word
- * (cleared). A MOE_DISPATCH_FP8_GEMM config takes moe_expert_ffn_fp8 instead (MOE_ERR_ARG
- * here). */
+ * (cleared). With bf16 experts it also holds the tickets (cleared on every call) and
+ * fp32 partial slots of the split over k: when the tiles of a swapped-pair projection
+ * without SwiGLU leave their last wave of SM pairs at most half busy, each tile of that
+ * wave is cut into up to 4 ranges of k that run on idle pairs, and the range that
+ * finishes last sums the ranges' partials in range order (deterministic; the sums are
+ * associated differently from an uncut tile's). A MOE_DISPATCH_FP8_GEMM config takes
+ * moe_expert_ffn_fp8 instead (MOE_ERR_ARG here). */
 int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offsets,
                    const void* W13, const void* W2, void* h, void* out,
                    void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -490,6 +495,8 @@ const char* moe_ffn_kernel_name(const moe_config* cfg);
 
 /* Environment switches (read once per process):
  *   MOE_GEMM_PAIR=0/1/2    force the tcgen05 expert-GEMM variant (see moe_ffn_kernel_name);
+ *   MOE_GEMM_SPLITK=0      never split the expert GEMMs' last partial wave over k (see
+ *                          moe_expert_ffn), for comparisons;
  *   MOE_ROUTE_TC=0         keep the router's logits on the FMA units for every config;
  *   MOE_ROUTE_TC_CHUNK=n   elements of d per fresh accumulator on the tensor-core router
  *                          (a multiple of 64; default 128), for accuracy experiments;

@@ -91,6 +91,12 @@ struct Params {
     int skip_arrive;         // failure-path test: never signal the first finished accumulator
     const float* xscale;     // e4m3 inputs: scale of each row of B (swapped pairs) ...
     const float* wscale;     // ... and of each weight row
+    // Swapped pairs, modes without SwiGLU: the split of the last partial wave's tiles
+    // over k (null: never split). split_part holds split_slots slots of fp32 partials,
+    // split_tickets 2 * split_slots counters that are zero at launch and left zero.
+    float* split_part;
+    int32_t* split_tickets;
+    int split_slots;
 };
 
 template <int STAGES>
@@ -478,6 +484,7 @@ struct RowMaps {
 struct SwapXchg {
     float v[2][32][33];     // up values for 32 rows x 32 features, per gate warp
     float sx[SW_TILE_N];    // e4m3 inputs: the scales of the tile's rows (0 past its end)
+    int split_last;         // this CTA's k range was the last of its tile to finish
 };
 
 constexpr size_t swap_smem_bytes() {
@@ -516,6 +523,43 @@ __device__ __forceinline__ void swap_tile_rows(const int* off, const int* end, i
     start = off[e] + mt * width;
     len = min(width, end[e] - start);
     n = (len + 31) & ~31;
+}
+
+// Split of the last partial wave over k. When the tiles leave the last wave of pairs at
+// most half busy, each of its `rem` tiles is cut into `parts` consecutive ranges of
+// k-blocks that run on pairs which would otherwise idle; every range leaves its fp32
+// accumulator in a slot of split_part, and the range that finishes last (an atomic
+// ticket per tile and SM, no waiting) sums the slots in range order, so the result does
+// not depend on which range finishes last. The work items are the `full` whole tiles,
+// then rem * parts ranges, at most one per pair.
+constexpr int SW_SPLIT_MAX = 4;         // ranges per tile
+constexpr int SW_SPLIT_MIN_KB = 8;      // k-blocks per range at least
+constexpr int SW_SPLIT_SLOT = 2 * SW_TILE_N * 128;  // floats per slot: both SMs, 128 features x 256 rows
+
+struct SplitPlan {
+    int full, rem, parts;
+    __device__ int items() const { return full + rem * parts; }
+};
+
+__device__ __forceinline__ SplitPlan plan_split(const Params& p, int total, int n_units, int nkb, bool allowed) {
+    SplitPlan sp{total, 0, 1};
+    const int r = total % n_units;
+    if (!allowed || p.split_part == nullptr || r == 0 || 2 * r > n_units) return sp;
+    const int parts = min(min(n_units / r, SW_SPLIT_MAX), min(p.split_slots / r, nkb / SW_SPLIT_MIN_KB));
+    if (parts >= 2) sp = SplitPlan{total - r, r, parts};
+    return sp;
+}
+
+// Work item u: tile t and k-blocks [kb0, kb1); slot = the partial slot of a range (-1 for a
+// whole tile), tile r = slot / parts of the split ones, range slot % parts.
+struct SwapItem {
+    int t, kb0, kb1, slot;
+};
+
+__device__ __forceinline__ SwapItem swap_item(int u, const SplitPlan& sp, int nkb) {
+    if (u < sp.full) return SwapItem{u, 0, nkb, -1};
+    const int j = u - sp.full, part = j % sp.parts;
+    return SwapItem{sp.full + j / sp.parts, part * nkb / sp.parts, (part + 1) * nkb / sp.parts, j};
 }
 
 template <int OUT>
@@ -618,6 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
     const int nkb = (p.K + BKE - 1) / BKE;
     volatile int* abort_flag = &S.abort_flag;
     const uint32_t full_base = mapa_shared(smem_addr(&S.full[0]), 0);
+    const SplitPlan sp = plan_split(p, total, n_units, nkb, MODE != kSwiGLU);
+    const int n_items = sp.items();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -626,9 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
             uint32_t armed_mask = 0, armed_par = 0;
             // An expert's rows are re-read by every feature tile: keep them in L2.
             const uint64_t pol_x = l2_policy_evict_last();
-            for (int t = unit; t < total; t += n_units) {
+            for (int u = unit; u < n_items; u += n_units) {
+                const SwapItem it = swap_item(u, sp, nkb);
                 int e, mt, nt, start, len, n;
-                decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
+                decode_tile(it.t, S.tile, E, p.n_tiles, e, mt, nt);
                 swap_tile_rows(S.off, S.end, e, mt, start, len, n);
                 const CUtensorMap* mx = &mapX.m[(n >> 5) - 1];  // box of n / 2 rows
                 const int xrow = start + int(rank) * (n >> 1);
@@ -638,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 const int wf = nt * 128 + int(rank) * 64;
                 const int w0 = e * p.R + nt * 256 + int(rank) * 128;
                 bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     const int kW = (kb >> p.b_k_shift) * BKE;
                     const int kX = kb * BKE;
@@ -668,9 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
             int s = 0;
             uint32_t ph = 0;
             int i = 0;
-            for (int t = unit; t < total; t += n_units, ++i) {
+            for (int u = unit; u < n_items; u += n_units, ++i) {
+                const SwapItem it = swap_item(u, sp, nkb);
                 int e, mt, nt, start, len, n;
-                decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
+                decode_tile(it.t, S.tile, E, p.n_tiles, e, mt, nt);
                 swap_tile_rows(S.off, S.end, e, mt, start, len, n);
                 const uint32_t idesc = F8 ? idesc_e4m3_f32(256, uint32_t(n)) : idesc_bf16_f32(256, uint32_t(n));
                 const int acc = i & 1;
@@ -679,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * SW_TILE_N;
                 bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!mbar_wait(&S.full[s], ph, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(smem_addr(sA + s * SW_A_STAGE));
@@ -687,10 +735,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                     // four K slices of 32 bytes per 128-byte row (descriptor addresses in 16-byte units)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t accum = (kb != it.kb0 || ks != 0) ? 1u : 0u;
                         if constexpr (F8)
-                            umma_f8_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+                            umma_f8_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
                         else
-                            umma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, (kb | ks) != 0 ? 1u : 0u);
+                            umma_bf16_pair(d_tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, accum);
                     }
                     umma_commit_pair_multicast(&S.empty[s], 0x3);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -708,11 +757,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
         // to the MMA warp as soon as its last chunk is in registers.
         const int q = warp & 3;
         const int te = (warp - 2) * 32 + lane;  // 0..127 over the four epilogue warps
+        const int fl = q * 32 + lane;           // this thread's TMEM lane: feature of the SM's 128
         const uint32_t empty_base = mapa_shared(smem_addr(&S.tmem_empty[0]), 0);
         int i = 0;
-        for (int t = unit; t < total; t += n_units, ++i) {
+        for (int u = unit; u < n_items; u += n_units, ++i) {
+            const SwapItem it = swap_item(u, sp, nkb);
             int e, mt, nt, start, len, n;
-            decode_tile(t, S.tile, E, p.n_tiles, e, mt, nt);
+            decode_tile(it.t, S.tile, E, p.n_tiles, e, mt, nt);
             swap_tile_rows(S.off, S.end, e, mt, start, len, n);
             const int acc = i & 1;
             const uint32_t aph = (i >> 1) & 1;
@@ -745,6 +796,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 if (lane == 0) mbar_arrive_cluster(empty_base + uint32_t(acc) * 8u);
             };
             auto chunk = [&](int c0, uint32_t(&v)[32]) {
+                if constexpr (MODE != kSwiGLU) {
+                    if (it.slot >= 0) {
+                        // a k range: its raw fp32 accumulator goes to the range's slot, laid
+                        // out [SM][row / 4][feature][row % 4] so that each thread stores
+                        // (and the reducer loads) four rows of its feature at once and a warp
+                        // covers 512 contiguous bytes
+                        float4* dst = reinterpret_cast<float4*>(p.split_part + size_t(it.slot) * SW_SPLIT_SLOT +
+                                                                size_t(rank) * (SW_TILE_N * 128)) +
+                                      (c0 >> 2) * 128 + fl;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            if (c0 + 4 * g < len)
+                                __stcg(dst + g * 128, make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                                                  __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+                        return;
+                    }
+                }
                 if constexpr (F8) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * (wsc * X.sx[c0 + j]));
@@ -799,6 +867,68 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_swap_kernel(const __
                 else release();
                 chunk(c0 + 32, vb);
                 if (more2) tmem_ld_wait();
+            }
+            if constexpr (MODE != kSwiGLU) {
+                if (it.slot >= 0) {
+                    // Ticket of this tile and SM: the range that counts last sums all the
+                    // ranges' slots, in range order, and applies the epilogue.
+                    const int r = it.slot / sp.parts;
+                    __threadfence();
+                    epi_bar_sync();
+                    if (te == 0) {
+                        int32_t* ticket = p.split_tickets + 2 * r + int(rank);
+                        __threadfence();
+                        const bool last = atomicAdd(ticket, 1) == sp.parts - 1;
+                        if (last) *ticket = 0;  // every range has counted: zero for the next launch
+                        X.split_last = last;
+                    }
+                    epi_bar_sync();
+                    if (X.split_last) {
+                        __threadfence();
+                        const float4* src = reinterpret_cast<const float4*>(p.split_part +
+                                                                            size_t(r) * sp.parts * SW_SPLIT_SLOT +
+                                                                            size_t(rank) * (SW_TILE_N * 128)) +
+                                            fl;
+                        // 16 rows per step, every range's values for them loaded before any
+                        // is added, then summed in range order
+                        constexpr int G = 4;  // float4 groups of rows per step
+#pragma unroll 1
+                        for (int c0 = 0; c0 < len; c0 += 4 * G) {
+                            float4 a[SW_SPLIT_MAX][G];
+#pragma unroll
+                            for (int r2 = 0; r2 < SW_SPLIT_MAX; ++r2)
+#pragma unroll
+                                for (int g = 0; g < G; ++g)
+                                    a[r2][g] = (r2 < sp.parts && c0 + 4 * g < len)
+                                                   ? __ldcg(src + r2 * (SW_SPLIT_SLOT / 4) + ((c0 >> 2) + g) * 128)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                float4 sum = a[0][g];
+#pragma unroll
+                                for (int r2 = 1; r2 < SW_SPLIT_MAX; ++r2) {
+                                    if (r2 < sp.parts) {
+                                        sum.x += a[r2][g].x;
+                                        sum.y += a[r2][g].y;
+                                        sum.z += a[r2][g].z;
+                                        sum.w += a[r2][g].w;
+                                    }
+                                }
+                                const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const int c = c0 + 4 * g + j;
+                                    if (c < len && f < p.n_out) {
+                                        float x = s4[j];
+                                        if constexpr (F8) x *= wsc * X.sx[c];
+                                        if (MODE == kReLU) x = fmaxf(x, 0.f);
+                                        store_one<OUT>(p, start + c, f, x);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
             }
             // plain mode has no barrier inside the chunks: keep X.sx until every warp is done
             if constexpr (F8 && MODE != kSwiGLU) epi_bar_sync();
@@ -995,6 +1125,16 @@ int debug_skip_arrive() {
     return v;
 }
 
+// MOE_GEMM_SPLITK=0 (read once per process) turns the split of the last partial wave
+// over k off, for comparisons; it is on otherwise.
+bool gemm_splitk_enabled() {
+    static const bool v = [] {
+        const char* e = getenv("MOE_GEMM_SPLITK");
+        return !(e && atoi(e) == 0);
+    }();
+    return v;
+}
+
 cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid_event) {
     const int64_t rows_max = a.rows;
     const bool split_h = a.precision == MOE_PRECISION_SPLIT_H;
@@ -1013,6 +1153,11 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, cudaStream_t stream, cudaEvent_t mid
     p.status = a.status;
     p.F = a.F;
     p.skip_arrive = debug_skip_arrive();
+    if (a.split_part && a.split_tickets && a.split_slots > 0 && gemm_splitk_enabled()) {
+        p.split_part = a.split_part;
+        p.split_tickets = a.split_tickets;
+        p.split_slots = a.split_slots;
+    }
 
     // Up projection: A = xperm [rows, d]; B = W13 [E*R, d]; C = h.
     const bool swiglu = a.expert_kind == MOE_EXPERT_SWIGLU;

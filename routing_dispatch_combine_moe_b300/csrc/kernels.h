@@ -173,7 +173,18 @@ struct FfnArgs {
     void* h;
     void* out;
     int32_t* status;
+    // Swapped-pair GEMMs without SwiGLU: fp32 partial slots for the split of the last
+    // partial wave over k, and their tickets (zero at launch, left zero); null: no split.
+    float* split_part;
+    int32_t* split_tickets;
+    int split_slots;
 };
+
+// The workspace share of that split: kGemmSplitSlots slots of kGemmSplitSlotBytes (two
+// SMs x 128 features x 256 rows of fp32) and two int32 tickets per slot.
+constexpr int kGemmSplitSlots = 96;
+constexpr size_t kGemmSplitSlotBytes = size_t(2) * 256 * 128 * sizeof(float);
+constexpr size_t kGemmSplitTicketBytes = size_t(2) * kGemmSplitSlots * sizeof(int32_t);
 
 // tcgen05 kernel a bf16 projection runs: 0 one SM per tile, 1 SM pairs on row
 // tiles, 2 SM pairs with swapped operands.

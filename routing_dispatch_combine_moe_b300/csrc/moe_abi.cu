@@ -149,7 +149,7 @@ int validate(const moe_config* c) {
 }
 
 struct Layout {
-    size_t status, near_ties, hist, drop_offsets, routed_offsets, elist, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
+    size_t status, near_ties, split_tickets, split_part, hist, drop_offsets, routed_offsets, elist, route_partial, topk_idx, topk_gate, counts_routed, counts_kept, offsets, rank_offsets,
         n_dropped, pos, row_src, drop_list, xperm, h, out, x_stage, y_stage;
     // deduplicated dispatch (cfg->dedup): scratch in the dispatch part, outputs in the forward part
     size_t dd_slots, dd_hist, dd_kept, dd_drop, dd_routed, dd_rank, dd_ndrop;
@@ -173,6 +173,7 @@ Layout layout(const moe_config* c) {
     };
     L.status = take(2 * sizeof(int32_t));  // the status word, then the dispatch scan's ticket
     L.near_ties = take(sizeof(int32_t));
+    L.split_tickets = take(bf16_experts(c) ? kGemmSplitTicketBytes : 0);
     L.hist = take(sizeof(int32_t) * size_t(N) * nblk);
     L.drop_offsets = take(sizeof(int32_t) * size_t(N));
     L.routed_offsets = take(sizeof(int32_t) * size_t(N + 1));
@@ -203,6 +204,7 @@ Layout layout(const moe_config* c) {
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
         L.h = take(split_h(c) ? 2 * 2 * R * size_t(c->F) : b * R * size_t(c->F));
         L.out = take((out_dtype(c) == MOE_F32 ? 4 : b) * R * size_t(c->d));
+        L.split_part = take(bf16_experts(c) ? kGemmSplitSlots * kGemmSplitSlotBytes : 0);
     } else {
         L.h = 0;
         L.out = L.xperm;
@@ -262,14 +264,16 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->n_near_ties = at<int32_t>(ws, L.near_ties);
 }
 
-// Standalone moe_expert_ffn(_fp8) workspace: the status word, then (FP8 hidden
-// activation) h's codes and row scales.
+// Standalone moe_expert_ffn(_fp8) workspace: the status word, the GEMM split's tickets
+// and partial slots (bf16 experts), then (FP8 hidden activation) h's codes and row scales.
 struct FfnLayout {
-    size_t hq, hscale, end;
+    size_t split_tickets, split_part, hq, hscale, end;
 };
 FfnLayout ffn_layout(const moe_config* c) {
     FfnLayout F{};
-    F.hq = kAlign;
+    F.split_tickets = kAlign;
+    F.split_part = align_up(F.split_tickets + (bf16_experts(c) ? kGemmSplitTicketBytes : 0));
+    F.hq = align_up(F.split_part + (bf16_experts(c) ? kGemmSplitSlots * kGemmSplitSlotBytes : 0));
     const size_t R = size_t(rows_cap(c));
     F.hscale = align_up(F.hq + (fp8_h(c) ? R * size_t(c->F) : 0));
     F.end = align_up(F.hscale + (fp8_h(c) ? sizeof(float) * R : 0));
@@ -384,8 +388,14 @@ inline size_t fp8_w2_scale_offset(const moe_config* c) {
 // e4m3 codes and W13 the FP8 weight buffer).
 int run_ffn(const moe_config* c, const void* xperm, const int32_t* offsets, const int32_t* counts, const void* W13,
             const void* W2, void* h, void* out, int32_t* status, cudaStream_t s, cudaEvent_t mid,
-            const float* xscale = nullptr, uint8_t* hq = nullptr, float* hscale = nullptr) {
+            const float* xscale = nullptr, uint8_t* hq = nullptr, float* hscale = nullptr,
+            float* split_part = nullptr, int32_t* split_tickets = nullptr) {
     FfnArgs a{};
+    if (bf16_experts(c) && split_part && split_tickets) {
+        a.split_part = split_part;
+        a.split_tickets = split_tickets;
+        a.split_slots = kGemmSplitSlots;
+    }
     if (fp8_gemm(c)) {
         a.in_fp8 = true;
         a.xscale = xscale;
@@ -453,8 +463,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     fill_view(c, ws, &v);
     // The router also counts each expert's assignments per dispatch block (the fused
     // route + count) and the near-tie tokens: one memset clears the status word, the
-    // near-tie count and that histogram, which follow each other at the start of the
-    // workspace.
+    // near-tie count, the expert GEMM split's tickets and that histogram, which follow
+    // each other at the start of the workspace.
     const size_t hist_end = L.hist + sizeof(int32_t) * size_t(n_experts(c)) *
                                          size_t(dispatch_blocks(int64_t(c->T) * n_slots(c)));
     cudaError_t e = cudaMemsetAsync(ws, 0, hist_end, s);
@@ -484,7 +494,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
         const int32_t* used = c->layout == MOE_LAYOUT_PADDED ? v.map.counts_kept : nullptr;
         const void* rows = fp8_gemm(c) ? static_cast<const void*>(v.xq) : v.xperm;
         if ((rc = run_ffn(c, rows, v.map.offsets, used, W13, W2, v.h, v.out, v.status, s, mid, v.xscale, v.hq,
-                          v.hscale)) != MOE_OK)
+                          v.hscale, bf16_experts(c) ? at<float>(ws, L.split_part) : nullptr,
+                          bf16_experts(c) ? at<int32_t>(ws, L.split_tickets) : nullptr)) != MOE_OK)
             return rc;
     } else if ((rc = record(events, n_events, 3, s)) != MOE_OK) {
         return rc;
@@ -654,11 +665,14 @@ int moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* offs
     if (!aligned16(xperm) || !aligned16(W13) || !aligned16(W2) || !aligned16(h) || !aligned16(out) ||
         !aligned16(ws))
         return MOE_ERR_ALIGN;
-    if (ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+    const FfnLayout FL = ffn_layout(cfg);
+    if (ws_bytes < FL.end) return MOE_ERR_WORKSPACE;
+    // the status word and the GEMM split's tickets
     int32_t* status = static_cast<int32_t*>(ws);
-    const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
-    return run_ffn(cfg, xperm, offsets, nullptr, W13, W2, h, out, status, stream, nullptr);
+    const cudaError_t e = cudaMemsetAsync(status, 0, FL.split_part, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status, split tickets)");
+    return run_ffn(cfg, xperm, offsets, nullptr, W13, W2, h, out, status, stream, nullptr, nullptr, nullptr, nullptr,
+                   at<float>(ws, FL.split_part), at<int32_t>(ws, FL.split_tickets));
 }
 
 size_t moe_fp8_weight_bytes(const moe_config* cfg) {
@@ -707,11 +721,13 @@ int moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* xq, const float* xs
         return MOE_ERR_ALIGN;
     const FfnLayout FL = ffn_layout(cfg);
     if (ws_bytes < FL.end) return MOE_ERR_WORKSPACE;
+    // the status word and the GEMM split's tickets
     int32_t* status = static_cast<int32_t*>(ws);
-    const cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    const cudaError_t e = cudaMemsetAsync(status, 0, FL.split_part, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status, split tickets)");
     return run_ffn(cfg, xq, offsets, nullptr, W13_fp8, W2, h, out, status, stream, nullptr, xscale,
-                   fp8_h(cfg) ? at<uint8_t>(ws, FL.hq) : nullptr, fp8_h(cfg) ? at<float>(ws, FL.hscale) : nullptr);
+                   fp8_h(cfg) ? at<uint8_t>(ws, FL.hq) : nullptr, fp8_h(cfg) ? at<float>(ws, FL.hscale) : nullptr,
+                   at<float>(ws, FL.split_part), at<int32_t>(ws, FL.split_tickets));
 }
 
 int moe_combine(const moe_config* cfg, const void* out, const float* topk_gate, const int32_t* pos, void* y,
@@ -801,6 +817,6 @@ const char* moe_ffn_kernel_name(const moe_config* cfg) {
     }
 }
 
-int moe_version(void) { return 200; }
+int moe_version(void) { return 201; }
 
 }  // extern "C"

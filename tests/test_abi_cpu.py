@@ -383,10 +383,13 @@ def test_fp8_h_validation_workspace_and_w2_bytes():
     # W2 buffer: N*d*F codes, the next 256-byte boundary, N*d fp32 scales
     assert abi.moe_fp8_w2_bytes(h8) == (8 * 128 * 64 + 255) // 256 * 256 + 4 * 8 * 128
     assert abi.moe_fp8_w2_bytes(g) == 0
-    # the FFN workspace holds h's codes and scales after the status word
+    # the FFN workspace: the status word, the GEMM split's tickets (two per slot) and fp32
+    # partial slots (2 SMs x 128 features x 256 rows each), then h's codes and scales
     rows = 64 * 2
-    assert abi.moe_ffn_workspace_bytes(h8) >= 256 + rows * 64 + rows * 4
-    assert abi.moe_ffn_workspace_bytes(g) == 256
+    split = 1024 + 96 * 2 * 128 * 256 * 4
+    assert abi.moe_ffn_workspace_bytes(h8) >= split + rows * 64 + rows * 4
+    assert abi.moe_ffn_workspace_bytes(g) == split
+    assert abi.moe_ffn_workspace_bytes(cfg(act="f32", expert="relu")) == 256  # FMA experts: no split
     v = abi.moe_workspace_view()
     base = 1 << 40
     n = abi.moe_workspace_bytes(h8)
