@@ -190,8 +190,13 @@ def fp8_row_bytes(d: int, per_row: bool = False) -> int:
     return d + 4 * (1 if per_row else (d + 127) // 128)
 
 
-def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, routed_rows: int = 0) -> dict:
+def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, routed_rows: int = 0,
+                active_experts: int | None = None) -> dict:
     """Algorithmic work per launch: flops of the formulas, bytes each kernel must move at least.
+
+    The expert GEMMs read the weights of the experts that hold at least one row
+    (`active_experts`, default all of them): an expert with no rows needs none of its
+    weights, and the kernels skip it.
 
     With the deduplicated dispatch the rows travel x -> send buffer -> expert rows: x is
     read once, each send row written once and read once, each expert row written once.
@@ -211,11 +216,12 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
     if f8g:  # x read once, each row written as codes + one scale
         dispatch = dispatch - rows * w.d * b + rows * fp8_row_bytes(w.d, per_row=True)
     up_in = rows * fp8_row_bytes(w.d, per_row=True) if f8g else rows * w.d * b
-    w13_bytes = w.n_experts * w.w13_rows * (w.d + 4) if f8g else w.n_experts * w.w13_rows * w.d * b
+    n_w = w.n_experts if active_experts is None else active_experts
+    w13_bytes = n_w * w.w13_rows * (w.d + 4) if f8g else n_w * w.w13_rows * w.d * b
     # FP8 hidden activation: the down stage also quantizes h (reads it in bf16, writes codes
     # + a scale per row) and then reads those and the e4m3 W2
     f8h = w.precision == "fp8_h"
-    w2_bytes = w.n_experts * w.d * (w.F + 4) if f8h else w.n_experts * w.d * w.F * b
+    w2_bytes = n_w * w.d * (w.F + 4) if f8h else n_w * w.d * w.F * b
     down_in = rows * h_cols * b + 2 * rows * (w.F + 4) if f8h else rows * h_cols * b
     return dict(
         route_flops=sizing.router_flops(w.T, w.d, w.E),
@@ -512,7 +518,8 @@ def run_ours(args, w, world, rank, local):
         fp8 = {"format": "e4m3 codes + one power-of-two scale per row, read as they are by the e4m3 up GEMM",
                "wire_bytes": rows * fp8_row_bytes(w.d, True), "bf16_wire_bytes": rows * w.d * 2,
                "ratio": fp8_row_bytes(w.d, True) / (w.d * 2)}
-    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0, routed_rows)
+    work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0, routed_rows,
+                       active_experts=int((kept > 0).sum()))
     peaks, peak_src = load_peaks()
     value = job_throughput(w.T, args.steps, world, max_ms / 1e3)
     dc_bytes = work["dispatch_bytes"] + work["combine_bytes"]

@@ -62,6 +62,10 @@ def test_algorithmic_work_of_the_bf16_and_fp8_layers():
     # actually reads are counted apart
     assert bf["combine_bytes"] == rows * d * 2 + T * d * 2
     assert bf["combine_bytes_moved"] == rows * d * 4 + T * d * 2
+    # experts without rows are skipped: only the active experts' weights count
+    six = bench.algorithmic(W["mixtral_bf16"], rows, out_bytes=4, h_cols=F, active_experts=6)
+    assert bf["up_bytes"] - six["up_bytes"] == 2 * 2 * F * d * 2 and bf["down_bytes"] - six["down_bytes"] == 2 * d * F * 2
+    assert six["up_flops"] == bf["up_flops"]
     # the DeepSeek-V3-shaped layer: x read, rows written, rows read, y written = 1057 MB
     ds = bench.algorithmic(W["dsv3_full"], 4096 * 8, out_bytes=4, h_cols=2048)
     assert ds["dispatch_bytes"] + ds["combine_bytes"] == 2 * (4096 + 32768) * 7168 * 2 == 1_056_964_608
