@@ -202,7 +202,8 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
     read once, each send row written once and read once, each expert row written once.
     With the FP8 dispatch each routed row is written as codes + scales, read back and
     written as a bf16 row. With the FP8 GEMM every row is written once as codes + its
-    scale (instead of a bf16 row) and the up projection reads those and the e4m3 weights.
+    scale (instead of a bf16 row) and the up projection reads those and the e4m3 weights;
+    with dedup too, the send rows are codes + one scale as well.
     """
     b = w.act_bytes
     up, down = sizing.expert_gemm_flops(rows, w.d, w.F, w.expert)
@@ -215,6 +216,8 @@ def algorithmic(w, rows: int, out_bytes: int, h_cols: int, rows_sent: int = 0, r
         dispatch += 2 * routed_rows * fp8_row_bytes(w.d)
     if f8g:  # x read once, each row written as codes + one scale
         dispatch = dispatch - rows * w.d * b + rows * fp8_row_bytes(w.d, per_row=True)
+        if w.dedup:  # the send rows written and read as codes + one scale each
+            dispatch += 2 * rows_sent * (fp8_row_bytes(w.d, per_row=True) - w.d * b)
     up_in = rows * fp8_row_bytes(w.d, per_row=True) if f8g else rows * w.d * b
     n_w = w.n_experts if active_experts is None else active_experts
     w13_bytes = n_w * w.w13_rows * (w.d + 4) if f8g else n_w * w.w13_rows * w.d * b
@@ -515,9 +518,13 @@ def run_ours(args, w, world, rank, local):
         if dedup:
             dedup["remote_send_bytes_fp8"] = int((dedup["rows_sent"] - int(send_counts[0])) * fp8_row_bytes(w.d))
     if w.dispatch_dtype == "fp8_gemm":
+        sent = dedup["rows_sent"] if dedup else rows  # with dedup the FP8 rows on the wire are the send rows
         fp8 = {"format": "e4m3 codes + one power-of-two scale per row, read as they are by the e4m3 up GEMM",
-               "wire_bytes": rows * fp8_row_bytes(w.d, True), "bf16_wire_bytes": rows * w.d * 2,
+               "wire_bytes": sent * fp8_row_bytes(w.d, True), "bf16_wire_bytes": sent * w.d * 2,
                "ratio": fp8_row_bytes(w.d, True) / (w.d * 2)}
+        if dedup:
+            dedup["remote_send_bytes_fp8"] = int((dedup["rows_sent"] - int(send_counts[0])) *
+                                                 fp8_row_bytes(w.d, True))
     work = algorithmic(w, rows, out_bytes, abi.hidden_cols(cfg), dedup["rows_sent"] if dedup else 0, routed_rows,
                        active_experts=int((kept > 0).sum()))
     peaks, peak_src = load_peaks()

@@ -117,7 +117,7 @@ typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t */
                               channel (moe_quantize_weights_fp8); h, W2 and the down projection stay
                               bf16. One scale per row, not per 128-element block, so that the GEMM can
                               apply it after the K loop. bf16 activations, ReLU or SwiGLU experts,
-                              d % 16 == 0, no dedup */
+                              d % 16 == 0; with dedup see moe_dispatch_dedup_fp8_gemm */
 
 /* Limits of this build. */
 #define MOE_MAX_K 16        /* experts per token, routed plus shared */
@@ -145,9 +145,9 @@ typedef struct moe_config {
     int32_t dedup;       /* 1: moe_layer_forward sends each token once per virtual rank (the
                           * deduplicated dispatch, see moe_dispatch_dedup) and fans the send rows
                           * out into the expert rows; D <= 16. 0: rows go straight from x. */
-    int32_t dispatch_dtype; /* MOE_DISPATCH_*; the FP8 formats need bf16 activations, and
-                             * MOE_DISPATCH_FP8_GEMM no dedup (with dedup, MOE_DISPATCH_FP8 sends
-                             * the deduplicated rows as FP8, see moe_dispatch_dedup_fp8) */
+    int32_t dispatch_dtype; /* MOE_DISPATCH_*; the FP8 formats need bf16 activations; with dedup
+                             * the deduplicated send rows travel in the FP8 format (see
+                             * moe_dispatch_dedup_fp8 and moe_dispatch_dedup_fp8_gemm) */
 } moe_config;
 
 /* Where the dispatch writes its routing map (all device int32 arrays). */
@@ -186,7 +186,7 @@ typedef struct moe_workspace_view {
                           * padding rows of out unwritten */
     moe_send_map send;   /* cfg->dedup only (NULL pointers otherwise) */
     void* xsend;         /* [T*D, d] act: the deduplicated send buffer (cfg->dedup only); with
-                          * MOE_DISPATCH_FP8 it holds the send rows' e4m3 codes [T*D, d] uint8 */
+                          * an FP8 dispatch dtype it holds the send rows' e4m3 codes [T*D, d] uint8 */
     uint8_t* xq;         /* [rows, d] e4m3 codes of the dispatched rows (MOE_DISPATCH_FP8: routed rows;
                           * MOE_DISPATCH_FP8_GEMM: all rows); with cfg->dedup and MOE_DISPATCH_FP8 the
                           * send rows' codes [T*D, d] (= xsend); NULL for MOE_DISPATCH_ACT */
@@ -199,6 +199,9 @@ typedef struct moe_workspace_view {
                            * largest selectable fp32 logits differ by less than 1e-6 of the larger
                            * magnitude (a near tie, where another valid rounding of the logits could
                            * select other experts) */
+    float* xsend_scale;  /* cfg->dedup with an FP8 dispatch dtype: the send rows' scales,
+                          * [T*D, ceil(d/128)] block scales (MOE_DISPATCH_FP8, = xscale) or [T*D]
+                          * row scales (MOE_DISPATCH_FP8_GEMM); NULL otherwise */
 } moe_workspace_view;
 
 /* ------------------------------------------------------------------ sizing */
@@ -310,6 +313,24 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
 int moe_dispatch_dedup_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
                            const moe_send_map* map, uint8_t* xsend_q, float* xsend_scale, void* xperm, void* ws,
                            size_t ws_bytes, moe_stream_t stream);
+
+/* The deduplicated dispatch in the FP8 GEMM's format, for cfg->dedup with
+ * MOE_DISPATCH_FP8_GEMM (the same pages and passages as moe_dispatch_dedup_fp8): the
+ * same send map, each send row the token's row quantized once by the row rule of
+ * moe_dispatch_fp8 (e4m3 codes and one power-of-two scale per row: d + 4 bytes per send
+ * row). The receiving side copies each kept routed assignment's send-row codes and scale
+ * into its expert row of xq / xscale, as they are; shared experts' rows are x quantized by
+ * the same rule. xq and xscale then equal what moe_dispatch_fp8 writes for the same map,
+ * and feed moe_expert_ffn_fp8.
+ *   x, topk_idx, pos, map, ws: as for moe_dispatch_dedup
+ *   xsend_q     [T*D, d] uint8 out: the send rows' codes (rows [0, send_offsets[D]) written)
+ *   xsend_scale [T*D] fp32 out: their row scales
+ *   xq          [rows, d] uint8 out, xscale [rows] fp32 out: the expert rows' codes and scales
+ *               (may be NULL when rows = moe_rows_capacity(cfg) is 0)
+ * MOE_ERR_ARG unless cfg->dedup and MOE_DISPATCH_FP8_GEMM. Bit-exact and deterministic. */
+int moe_dispatch_dedup_fp8_gemm(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
+                                const moe_send_map* map, uint8_t* xsend_q, float* xsend_scale, uint8_t* xq,
+                                float* xscale, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* FP8 dispatch of the rows a moe_dispatch with the same cfg mapped (its pos, row_src
  * and offsets).

@@ -68,7 +68,7 @@ class moe_send_map(ctypes.Structure):
 class moe_workspace_view(ctypes.Structure):
     _fields_ = [("status", _p), ("topk_idx", _p), ("topk_gate", _p), ("map", moe_dispatch_map),
                 ("xperm", _p), ("h", _p), ("out", _p), ("send", moe_send_map), ("xsend", _p), ("xq", _p),
-                ("xscale", _p), ("hq", _p), ("hscale", _p), ("n_near_ties", _p)]
+                ("xscale", _p), ("hq", _p), ("hscale", _p), ("n_near_ties", _p), ("xsend_scale", _p)]
 
 
 _SIGNATURES = {
@@ -97,6 +97,8 @@ _SIGNATURES = {
                                           _p, _p, _sz, _p]),
     "moe_dispatch_dedup_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p, ctypes.POINTER(moe_send_map),
                                               _p, _p, _p, _p, _sz, _p]),
+    "moe_dispatch_dedup_fp8_gemm": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, _p,
+                                                   ctypes.POINTER(moe_send_map), _p, _p, _p, _p, _p, _sz, _p]),
     "moe_dispatch_fp8": (ctypes.c_int, [ctypes.POINTER(moe_config), _p, _p, ctypes.POINTER(moe_dispatch_map), _p,
                                         _p, _p, _p, _sz, _p]),
     "moe_fp8_weight_bytes": (_sz, [ctypes.POINTER(moe_config)]),
@@ -268,6 +270,7 @@ class WorkspaceView:
     hq: int | None = None
     hscale: int | None = None
     n_near_ties: int | None = None
+    xsend_scale: int | None = None
 
 
 def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
@@ -279,7 +282,7 @@ def moe_workspace_get_view(cfg, ws: torch.Tensor) -> WorkspaceView:
     return WorkspaceView(v.status, v.topk_idx, v.topk_gate, m.counts_routed, m.counts_kept, m.offsets,
                          m.rank_offsets, m.pos, m.row_src, m.drop_list, m.n_dropped, v.xperm, v.h, v.out,
                          sm.send_counts, sm.send_offsets, sm.send_pos, sm.send_src, v.xsend, v.xq, v.xscale,
-                         v.hq, v.hscale, v.n_near_ties)
+                         v.hq, v.hscale, v.n_near_ties, v.xsend_scale)
 
 
 # ------------------------------------------------------------------ hot path
@@ -321,6 +324,16 @@ def moe_dispatch_dedup_fp8(cfg, x, topk_idx, pos, smap: moe_send_map, xsend_q, x
     _check(lib().moe_dispatch_dedup_fp8(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(pos), ctypes.byref(smap),
                                         _ptr(xsend_q), _ptr(xsend_scale), _ptr(xperm), _ptr(ws), ws.numel(),
                                         _stream(stream)), "moe_dispatch_dedup_fp8")
+
+
+def moe_dispatch_dedup_fp8_gemm(cfg, x, topk_idx, pos, smap: moe_send_map, xsend_q, xsend_scale, xq, xscale, ws,
+                                stream=None):
+    """Deduplicated send buffer as e4m3 codes + one scale per row; the fan-out copies them into
+    the expert rows' xq / xscale (the FP8 GEMM's input)."""
+    _check(lib().moe_dispatch_dedup_fp8_gemm(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(pos),
+                                             ctypes.byref(smap), _ptr(xsend_q), _ptr(xsend_scale), _ptr(xq),
+                                             _ptr(xscale), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_dispatch_dedup_fp8_gemm")
 
 
 def moe_dispatch_fp8(cfg, x, topk_idx, dmap: moe_dispatch_map, xq, xscale, xperm, ws, stream=None):

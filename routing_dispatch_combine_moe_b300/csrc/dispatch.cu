@@ -655,6 +655,14 @@ cudaError_t launch_dedup(const DedupArgs& a, cudaStream_t stream) {
     scatter_kernel<<<nblk, kDispatchBlock, 0, stream>>>(a.slots, A2, a.D, a.D, nblk, -1, a.hist, a.send_offsets,
                                                         a.drop_offsets, a.routed_offsets, nullptr, nullptr,
                                                         a.send_pos, a.send_src, nullptr);
+    if (a.fp8_rows) {
+        const cudaError_t e1 = launch_fp8_send_rows(a.x, a.send_pos, a.T, a.D, a.d, A2, static_cast<uint8_t*>(a.xsend),
+                                                    a.xsend_scale, a.status, stream);
+        if (e1 != cudaSuccess) return e1;
+        return launch_fp8_row_fanout(a.x, static_cast<const uint8_t*>(a.xsend), a.xsend_scale, a.topk_idx, a.pos,
+                                     a.send_pos, a.xq, a.xscale, a.T, a.K, a.E_routed, a.D, a.d, a.rows, A2,
+                                     a.status, stream);
+    }
     if (a.fp8) {
         const cudaError_t e1 = launch_fp8_send(a.x, a.slots, a.send_pos, a.T, a.D, a.d, A2,
                                                static_cast<uint8_t*>(a.xsend), a.xsend_scale, a.status, stream);

@@ -313,7 +313,86 @@ __global__ void __launch_bounds__(256) fanout_fp8_kernel(const uint4* __restrict
     }
 }
 
+// The deduplicated dispatch's receiving side with row-scaled FP8 send rows (the FP8
+// GEMM's format): one warp per token; each kept routed assignment's codes and row scale
+// are copied from the send row of (token, rank of its expert), and each shared expert's
+// row is x[t] quantized by the same row rule (shared experts are replicated: they read x).
+__global__ void __launch_bounds__(256) fanout_fp8_row_kernel(const uint4* __restrict__ x,
+                                                             const uint8_t* __restrict__ sq,
+                                                             const float* __restrict__ sscale,
+                                                             const int32_t* __restrict__ topk_idx,
+                                                             const int32_t* __restrict__ pos,
+                                                             const int32_t* __restrict__ send_pos,
+                                                             uint8_t* __restrict__ xq, float* __restrict__ xscale,
+                                                             int T, int K, int E_routed, int D, int d,
+                                                             int64_t max_rows, int64_t max_send, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int vpr = d / 8;  // 8-code pieces of a row; 16-byte bf16 pieces of x
+    int dst = -1, src = -1;  // src >= 0: send row; src == -2: x[t]
+    if (lane < K) {
+        const size_t a = size_t(t) * K + lane;
+        const int p = pos[a], e = topk_idx[a];
+        if (p >= 0 && p < max_rows) {
+            if (e >= 0 && e < E_routed) {
+                const int sr = send_pos[size_t(t) * D + e / (E_routed / D)];
+                if (sr >= 0 && sr < max_send) {
+                    dst = p;
+                    src = sr;
+                } else {
+                    set_status(status, MOE_DEV_ERR_INDEX);
+                }
+            } else {
+                dst = p;
+                src = -2;
+            }
+        } else if (p >= max_rows) {
+            set_status(status, MOE_DEV_ERR_INDEX);
+        }
+    }
+    const uint4* row = x + size_t(t) * vpr;
+    bool have_s = false;  // the row exponent of x[t], taken at its first shared slot
+    int s_x = 0;
+    for (int j = 0; j < K; ++j) {
+        const int dj = __shfl_sync(0xFFFFFFFFu, dst, j);
+        const int sj = __shfl_sync(0xFFFFFFFFu, src, j);
+        if (dj < 0) continue;
+        uint2* to = reinterpret_cast<uint2*>(xq + size_t(dj) * d);
+        if (sj == -2) {
+            if (!have_s) {
+                s_x = row_exponent(row, vpr, lane);
+                have_s = true;
+            }
+            for (int v = lane; v < vpr; v += 32) to[v] = e4m3_pack8(__ldg(row + v), s_x);
+            if (lane == 0) xscale[dj] = ldexpf(1.f, s_x);
+        } else {
+            const uint2* from = reinterpret_cast<const uint2*>(sq + size_t(sj) * d);
+            for (int v = lane; v < vpr; v += 32) to[v] = from[v];
+            if (lane == 0) xscale[dj] = sscale[sj];
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_fp8_send_rows(const void* x, const int32_t* send_pos, int T, int D, int d, int64_t max_send,
+                                 uint8_t* sq, float* sscale, int32_t* status, cudaStream_t stream) {
+    // the per-token row quantizer with the D send slots of each token as its destinations
+    gather_fp8_row_kernel<<<T, 128, 0, stream>>>(static_cast<const uint4*>(x), send_pos, T, D, d, max_send, sq,
+                                                  sscale, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_row_fanout(const void* x, const uint8_t* sq, const float* sscale, const int32_t* topk_idx,
+                                  const int32_t* pos, const int32_t* send_pos, uint8_t* xq, float* xscale, int T,
+                                  int K, int E_routed, int D, int d, int64_t max_rows, int64_t max_send,
+                                  int32_t* status, cudaStream_t stream) {
+    fanout_fp8_row_kernel<<<(T + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(x), sq, sscale, topk_idx, pos,
+                                                            send_pos, xq, xscale, T, K, E_routed, D, d, max_rows,
+                                                            max_send, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fp8_send(const void* x, const int32_t* slots, const int32_t* send_pos, int T, int D, int d,
                             int64_t max_send, uint8_t* xq, float* xscale, int32_t* status, cudaStream_t stream) {

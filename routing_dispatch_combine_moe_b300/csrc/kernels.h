@@ -97,8 +97,11 @@ struct DedupArgs {
     int32_t* send_pos;         // [T*D]
     int32_t* send_src;         // [T*D]
     void* xsend;               // [T*D, d] act, or (fp8) its e4m3 codes [T*D, d] uint8
-    float* xsend_scale;        // fp8: [T*D, ceil(d/128)] block scales of the send rows
+    float* xsend_scale;        // fp8: [T*D, ceil(d/128)] block scales of the send rows; fp8_rows: [T*D]
     bool fp8;                  // send rows as e4m3 + per-128 block scales; the fan-out dequantizes
+    bool fp8_rows;             // send rows as e4m3 + one scale per row; the fan-out copies codes + scale
+    uint8_t* xq;               // fp8_rows: [rows, d] the expert rows' codes (the FP8 GEMM's input) ...
+    float* xscale;             // ... and their row scales [rows]
     void* xperm;
     int32_t* status;
     // scratch
@@ -143,6 +146,16 @@ cudaError_t launch_fp8_fanout(const void* x, const uint8_t* xq, const float* xsc
                               const int32_t* pos, const int32_t* send_pos, void* xperm, int T, int K, int E_routed,
                               int D, int d, int64_t max_rows, int64_t max_send, int32_t* status,
                               cudaStream_t stream);
+// The same two legs in the FP8 GEMM's format: each send row quantized by the row rule
+// (codes [T*D, d], one scale per send row), and the fan-out copying each kept routed
+// assignment's codes and scale into xq [rows, d] / xscale [rows]; shared experts' rows are
+// x[t] quantized by the same rule.
+cudaError_t launch_fp8_send_rows(const void* x, const int32_t* send_pos, int T, int D, int d, int64_t max_send,
+                                 uint8_t* sq, float* sscale, int32_t* status, cudaStream_t stream);
+cudaError_t launch_fp8_row_fanout(const void* x, const uint8_t* sq, const float* sscale, const int32_t* topk_idx,
+                                  const int32_t* pos, const int32_t* send_pos, uint8_t* xq, float* xscale, int T,
+                                  int K, int E_routed, int D, int d, int64_t max_rows, int64_t max_send,
+                                  int32_t* status, cudaStream_t stream);
 // Row-scaled e4m3 codes [n_rows, d] and scales [n_rows] of a bf16 matrix [n_rows, d].
 cudaError_t launch_quantize_rows_fp8(const void* w, int64_t n_rows, int d, uint8_t* q, float* scale,
                                      cudaStream_t stream);

@@ -132,7 +132,6 @@ int validate(const moe_config* c) {
         c->dispatch_dtype != MOE_DISPATCH_FP8_GEMM)
         return MOE_ERR_ARG;
     if ((fp8_blocks(c) || fp8_gemm(c)) && c->act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-    if (fp8_gemm(c) && c->dedup) return MOE_ERR_UNSUPPORTED;  // dedup sends block-scaled FP8 rows only
     if (fp8_gemm(c) && c->expert_kind == MOE_EXPERT_IDENTITY) return MOE_ERR_UNSUPPORTED;
     if (fp8_gemm(c) && c->d % 16 != 0) return MOE_ERR_ALIGN;  // e4m3 rows of d bytes, 16-byte aligned
     // the FP8 hidden activation goes with the FP8 up projection (bf16 activations), h rows of F bytes
@@ -214,7 +213,10 @@ Layout layout(const moe_config* c) {
     L.send_pos = take(dd ? sizeof(int32_t) * TD : 0);
     L.send_src = take(dd ? sizeof(int32_t) * TD : 0);
     L.xsend = take(dd ? b * TD * size_t(c->d) : 0);  // with FP8: the send rows' e4m3 codes
-    L.xsend_scale = take(dd && fp8_blocks(c) ? sizeof(float) * TD * size_t((c->d + 127) / 128) : 0);
+    // the send rows' scales: per 128-element block, or (FP8 GEMM rows) one per row
+    L.xsend_scale = take(dd && fp8_blocks(c) ? sizeof(float) * TD * size_t((c->d + 127) / 128)
+                         : dd && fp8_gemm(c) ? sizeof(float) * TD
+                                             : 0);
     L.xq = take((fp8_blocks(c) && !dd) || fp8_gemm(c) ? R * size_t(c->d) : 0);
     L.xscale = take(fp8_blocks(c) && !dd ? sizeof(float) * R * size_t((c->d + 127) / 128)
                     : fp8_gemm(c) ? sizeof(float) * R
@@ -262,6 +264,7 @@ void fill_view(const moe_config* c, void* ws, moe_workspace_view* v) {
     v->hq = fp8_h(c) ? at<uint8_t>(ws, L.hq) : nullptr;
     v->hscale = fp8_h(c) ? at<float>(ws, L.hscale) : nullptr;
     v->n_near_ties = at<int32_t>(ws, L.near_ties);
+    v->xsend_scale = dd && f8 ? at<float>(ws, L.xsend_scale) : nullptr;
 }
 
 // Standalone moe_expert_ffn(_fp8) workspace: the status word, the GEMM split's tickets
@@ -323,8 +326,11 @@ int run_dispatch(const moe_config* c, const void* x, const int32_t* idx, const f
 }
 
 // Deduplicated send buffer + fan-out into xperm; the scratch lives in the dispatch part of ws.
+// xsend_scale: the send rows' scales with an FP8 dispatch dtype; xq, xscale: the expert
+// rows' codes and row scales with MOE_DISPATCH_FP8_GEMM (xperm is then not written).
 int run_dedup(const moe_config* c, const void* x, const int32_t* idx, const int32_t* pos, const moe_send_map* m,
-              void* xsend, void* xperm, void* ws, cudaStream_t s, float* xsend_scale = nullptr) {
+              void* xsend, void* xperm, void* ws, cudaStream_t s, float* xsend_scale = nullptr,
+              uint8_t* xq = nullptr, float* xscale = nullptr) {
     const Layout L = layout(c);
     DedupArgs a{};
     a.T = c->T; a.d = c->d; a.K = n_slots(c); a.E_routed = c->E; a.D = c->D;
@@ -340,6 +346,9 @@ int run_dedup(const moe_config* c, const void* x, const int32_t* idx, const int3
     a.xsend = xsend;
     a.xsend_scale = xsend_scale;
     a.fp8 = fp8_blocks(c);
+    a.fp8_rows = fp8_gemm(c);
+    a.xq = xq;
+    a.xscale = xscale;
     a.xperm = xperm;
     a.status = at<int32_t>(ws, L.status);
     a.slots = at<int32_t>(ws, L.dd_slots);
@@ -482,9 +491,8 @@ int forward(const moe_config* c, const void* x, const float* Wg, const float* bi
     if (f8 && !c->dedup &&
         (rc = run_fp8(c, x, v.topk_idx, &v.map, v.xq, v.xscale, fp8_gemm(c) ? nullptr : v.xperm, ws, s)) != MOE_OK)
         return rc;
-    if (c->dedup &&
-        (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s,
-                        fp8_blocks(c) ? at<float>(ws, L.xsend_scale) : nullptr)) != MOE_OK)
+    if (c->dedup && (rc = run_dedup(c, x, v.topk_idx, v.map.pos, &v.send, v.xsend, v.xperm, ws, s, v.xsend_scale,
+                                    fp8_gemm(c) ? v.xq : nullptr, fp8_gemm(c) ? v.xscale : nullptr)) != MOE_OK)
         return rc;
     if ((rc = record(events, n_events, 2, s)) != MOE_OK) return rc;
     if (c->expert_kind != MOE_EXPERT_IDENTITY) {
@@ -606,7 +614,7 @@ int moe_dispatch_dedup(const moe_config* cfg, const void* x, const int32_t* topk
                        moe_stream_t stream) {
     const int rc = validate(cfg);
     if (rc != MOE_OK) return rc;
-    if (!cfg->dedup || fp8_blocks(cfg)) return MOE_ERR_ARG;
+    if (!cfg->dedup || fp8_blocks(cfg) || fp8_gemm(cfg)) return MOE_ERR_ARG;
     if (!x || !topk_idx || !pos || !map || !ws || !map->send_counts || !map->send_offsets || !map->send_pos ||
         !map->send_src || !xsend || (!xperm && rows_cap(cfg) > 0))
         return MOE_ERR_ARG;
@@ -635,6 +643,25 @@ int moe_dispatch_dedup_fp8(const moe_config* cfg, const void* x, const int32_t* 
     const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
     return run_dedup(cfg, x, topk_idx, pos, map, xsend_q, xperm, ws, stream, xsend_scale);
+}
+
+int moe_dispatch_dedup_fp8_gemm(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* pos,
+                                const moe_send_map* map, uint8_t* xsend_q, float* xsend_scale, uint8_t* xq,
+                                float* xscale, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    const int rc = validate(cfg);
+    if (rc != MOE_OK) return rc;
+    if (!cfg->dedup || !fp8_gemm(cfg)) return MOE_ERR_ARG;
+    const bool rows = rows_cap(cfg) > 0;
+    if (!x || !topk_idx || !pos || !map || !ws || !map->send_counts || !map->send_offsets || !map->send_pos ||
+        !map->send_src || !xsend_q || !xsend_scale || (rows && (!xq || !xscale)))
+        return MOE_ERR_ARG;
+    if (!aligned16(x) || !aligned16(xsend_q) || !aligned4(xsend_scale) || (xq && !aligned16(xq)) ||
+        (xscale && !aligned4(xscale)) || !aligned4(topk_idx) || !aligned4(pos) || !aligned16(ws))
+        return MOE_ERR_ALIGN;
+    if (ws_bytes < layout(cfg).dispatch_end) return MOE_ERR_WORKSPACE;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(status)");
+    return run_dedup(cfg, x, topk_idx, pos, map, xsend_q, nullptr, ws, stream, xsend_scale, xq, xscale);
 }
 
 int moe_dispatch_fp8(const moe_config* cfg, const void* x, const int32_t* topk_idx, const moe_dispatch_map* map,
@@ -817,6 +844,6 @@ const char* moe_ffn_kernel_name(const moe_config* cfg) {
     }
 }
 
-int moe_version(void) { return 201; }
+int moe_version(void) { return 202; }
 
 }  // extern "C"

@@ -138,6 +138,11 @@ WORKLOADS: dict[str, Workload] = {
                  n_groups=8, topk_groups=4, dedup=True, dispatch_dtype="fp8",
                  note="the group-limited, deduplicated DeepSeek-V3 routing shape with the send rows as e4m3 "
                       "codes and per-128 power-of-two scales, dequantized by the receiving side's fan-out"),
+        Workload("dsv3_full_fp8_gemm_dedup", T=4096, d=7168, E=256, k=8, F=2048, act="bf16", expert="swiglu",
+                 D=8, n_groups=8, topk_groups=4, dedup=True, dispatch_dtype="fp8_gemm",
+                 note="the DeepSeek-V3-shaped full layer, group-limited to 4 of 8 groups, with the send rows "
+                      "deduplicated per rank and sent as row-scaled e4m3 codes that the receiving side hands "
+                      "to the FP8 up projection as they are"),
         Workload("dsv3_e32_slice", T=512, d=7168, E=32, k=8, F=2048, act="bf16", expert="swiglu",
                  note="an eighth of the DeepSeek-V3-shaped layer: the same d, F and k and the same 128 rows per "
                       "expert on average, with 32 experts (2.8 GB of weights), small enough for counter captures"),
@@ -147,7 +152,8 @@ WORKLOADS: dict[str, Workload] = {
 # Workload order as they are listed: small parity case first, headline second.
 WORKLOAD_ORDER = ["tiny_f32", "mixtral_bf16", "dsv3_route_only", "zipf_cf125", "dsv3_full", "dsv3_decode",
                   "dsv3_grouped_dedup", "mixtral_fp8_dispatch", "mixtral_fp8_gemm", "dsv3_decode_fp8_gemm",
-                  "dsv3_full_fp8_gemm", "mixtral_fp8_experts", "dsv3_grouped_dedup_fp8", "dsv3_e32_slice"]
+                  "dsv3_full_fp8_gemm", "mixtral_fp8_experts", "dsv3_grouped_dedup_fp8", "dsv3_full_fp8_gemm_dedup",
+                  "dsv3_e32_slice"]
 
 
 def scaled(w: Workload, **changes) -> Workload:

@@ -150,13 +150,21 @@ class StageBuffers:
                 self.xsend = torch.full((TD, w.d), 0xAB, dtype=torch.uint8, device=device)
                 self.xsend_scale = torch.full((TD, (w.d + 127) // 128), float("nan"), dtype=torch.float32,
                                               device=device)
+            elif w.dispatch_dtype == "fp8_gemm":  # e4m3 codes + one scale per send row
+                self.xsend = torch.full((TD, w.d), 0xAB, dtype=torch.uint8, device=device)
+                self.xsend_scale = torch.full((TD,), float("nan"), dtype=torch.float32, device=device)
             else:
                 self.xsend = torch.full((TD, w.d), float("nan"), dtype=w.torch_act, device=device)
 
     def smap(self):
         return abi.send_map(self.send_counts, self.send_offsets, self.send_pos, self.send_src)
 
-    def dedup(self, inp, topk_idx, pos, xperm):
+    def dedup(self, inp, topk_idx, pos, xperm, xq=None, xscale=None):
+        """The deduplicated dispatch into xperm, or (FP8 GEMM format) into xq / xscale."""
+        if self.cfg.dispatch_dtype == abi.MOE_DISPATCH_FP8_GEMM:
+            abi.moe_dispatch_dedup_fp8_gemm(self.cfg, inp["x"], topk_idx, pos, self.smap(), self.xsend,
+                                            self.xsend_scale, xq, xscale, self.ws_dispatch)
+            return
         if self.cfg.dispatch_dtype == abi.MOE_DISPATCH_FP8:
             abi.moe_dispatch_dedup_fp8(self.cfg, inp["x"], topk_idx, pos, self.smap(), self.xsend, self.xsend_scale,
                                        xperm, self.ws_dispatch)
@@ -454,6 +462,8 @@ def check_dedup(w, inp, bufs, st, d) -> dict:
     quantization of x), and the fanned-out expert rows equal to the direct gather's
     (FP8: to the direct FP8 dispatch's dequantized rows)."""
     fp8 = w.dispatch_dtype == "fp8"
+    if w.dispatch_dtype == "fp8_gemm":
+        return check_dedup_fp8_gemm(w, inp, bufs, st, d)
     direct = bufs.xperm.clone()
     if fp8:  # the direct FP8 dispatch of the same map: routed rows dequantized, shared rows from x
         direct = torch.full_like(bufs.xperm, float("nan"))
@@ -479,6 +489,36 @@ def check_dedup(w, inp, bufs, st, d) -> dict:
         assert torch.equal(bufs.xsend[:n], inp["x"][src_tok]), "send rows are not exact copies of x"
     held = torch.from_numpy(np.nonzero(d["row_src"] >= 0)[0]).to(fanned.device)  # padding rows are not sent
     assert torch.equal(fanned[held], direct[held]), "fanned-out rows differ from the direct dispatch's"
+    return s
+
+
+def check_dedup_fp8_gemm(w, inp, bufs, st, d) -> dict:
+    """Deduplicated dispatch in the FP8 GEMM's format: the send map bit-exact against the
+    oracle, each send row's codes and scale bit-exact against the oracle's row quantization
+    of its token, and the expert rows' codes and scales the fan-out writes equal to the
+    direct FP8 dispatch's of the same map (and so to the oracle's)."""
+    R = bufs.rows
+    dq = torch.full((R, w.d), 0xAB, dtype=torch.uint8, device=bufs.xq.device)
+    ds = torch.full((R,), float("nan"), dtype=torch.float32, device=bufs.xq.device)
+    abi.moe_dispatch_fp8(bufs.cfg, inp["x"], st["topk_idx"], bufs.dmap(), dq, ds, None, bufs.ws_dispatch)
+    fq = torch.full_like(dq, 0xCD)
+    fs = torch.full_like(ds, float("nan"))
+    bufs.dedup(inp, st["topk_idx"], bufs.pos, None, xq=fq, xscale=fs)
+    s = orc.dedup_send(cpu(st["topk_idx"]).numpy(), d["pos"], w.E, w.D)
+    torch.cuda.synchronize()
+    assert bufs.dispatch_status() == 0
+    np.testing.assert_array_equal(cpu(bufs.send_counts).numpy(), s["send_counts"])
+    np.testing.assert_array_equal(cpu(bufs.send_offsets).numpy(), s["send_offsets"])
+    np.testing.assert_array_equal(cpu(bufs.send_pos).numpy(), s["send_pos"])
+    n = s["n_send"]
+    np.testing.assert_array_equal(cpu(bufs.send_src).numpy()[:n], s["send_src"])
+    q = orc.quantize_fp8_rows(f64(inp["x"][torch.from_numpy(s["send_src"] // w.D).to(inp["x"].device)]))
+    np.testing.assert_array_equal(cpu(bufs.xsend).numpy()[:n], q["codes"])
+    np.testing.assert_array_equal(cpu(bufs.xsend_scale).numpy().astype(np.float64)[:n], q["scales"])
+    held = torch.from_numpy(np.nonzero(d["row_src"] >= 0)[0]).to(fq.device)
+    assert torch.equal(fq[held], dq[held]), "fanned-out codes differ from the direct FP8 dispatch's"
+    assert torch.equal(fs[held], ds[held]), "fanned-out row scales differ from the direct FP8 dispatch's"
+    compare_fp8_rows(w, fq, fs, d["row_src"], inp["x"])
     return s
 
 
@@ -647,7 +687,7 @@ class WorkspaceMap:
         self.out = None if not view.out else \
             ws[view.out - base:view.out - base + R * w.d * osz].view(odt).view(R, w.d)
         self.out_act = "f32" if odt == torch.float32 else "bf16"
-        if w.dispatch_dtype in ("fp8", "fp8_gemm") and not w.dedup:
+        if w.dispatch_dtype == "fp8_gemm" or (w.dispatch_dtype == "fp8" and not w.dedup):
             nb = (w.d + 127) // 128 if w.dispatch_dtype == "fp8" else 1
             self.xq = ws[view.xq - base:view.xq - base + R * w.d].view(R, w.d)
             self.xscale = ws[view.xscale - base:view.xscale - base + 4 * R * nb].view(torch.float32).view(R, nb)
@@ -659,11 +699,11 @@ class WorkspaceMap:
             self.send_offsets = i32(view.send_offsets, w.D + 1)
             self.send_pos = i32(view.send_pos, TD)
             self.send_src = i32(view.send_src, TD)
-            if w.dispatch_dtype == "fp8":  # codes [TD, d] and block scales [TD, nb] of the send rows
-                nb = (w.d + 127) // 128
+            if w.dispatch_dtype in ("fp8", "fp8_gemm"):  # codes [TD, d] and block or row scales of the send rows
+                nb = (w.d + 127) // 128 if w.dispatch_dtype == "fp8" else 1
                 self.xsend = ws[view.xsend - base:view.xsend - base + TD * w.d].view(TD, w.d)
-                self.xsend_scale = ws[view.xscale - base:view.xscale - base + 4 * TD * nb].view(torch.float32) \
-                    .view(TD, nb)
+                self.xsend_scale = ws[view.xsend_scale - base:view.xsend_scale - base + 4 * TD * nb] \
+                    .view(torch.float32).view(TD, nb)
             else:
                 self.xsend = ws[view.xsend - base:view.xsend - base + TD * w.d * esz].view(w.torch_act).view(TD, w.d)
 

@@ -300,6 +300,7 @@ def test_fp8_dispatch_validation_and_workspace():
     nd = abi.moe_workspace_bytes(ddf)
     assert abi.lib().moe_workspace_get_view(ctypes.byref(ddf), 1 << 40, nd, ctypes.byref(vd)) == 0
     assert vd.xq == vd.xsend and vd.xscale and vd.xscale >= vd.xsend + 64 * 4 * 128
+    assert vd.xsend_scale == vd.xscale
     m = abi.moe_send_map(*([A16] * 4))
     assert abi.lib().moe_dispatch_dedup(ctypes.byref(ddf), A16, A16, A16, ctypes.byref(m), A16, A16, A16, nd,
                                         None) == abi.MOE_ERR_ARG
@@ -309,6 +310,35 @@ def test_fp8_dispatch_validation_and_workspace():
                                             nd, None) == abi.MOE_ERR_ALIGN
     assert abi.lib().moe_dispatch_dedup_fp8(ctypes.byref(ddf), A16, A16, A16, ctypes.byref(m), A16, A16, A16, A16,
                                             abi.moe_dispatch_workspace_bytes(ddf) - 1, None) == abi.MOE_ERR_WORKSPACE
+    # with the FP8 GEMM's format the send rows carry one scale each and the fan-out fills
+    # the expert rows' codes and scales (xq, xscale), not xperm
+    ddg = cfg(D=4, dedup=True, dispatch_dtype="fp8_gemm")
+    assert abi.moe_validate_config(ddg) == abi.MOE_OK
+    assert abi.moe_kernels_per_forward(ddg) == abi.moe_kernels_per_forward(dd)
+    ng = abi.moe_workspace_bytes(ddg)
+    vg = abi.moe_workspace_view()
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(ddg), 1 << 40, ng, ctypes.byref(vg)) == 0
+    assert vg.xq and vg.xq != vg.xsend and vg.xscale - vg.xq >= 64 * 2 * 128      # expert rows' codes
+    assert vg.xsend_scale - vg.xsend >= 64 * 4 * 128                              # T*D send rows of d codes
+    assert (1 << 40) + ng - vg.xsend_scale >= 64 * 4 * 4                          # T*D row scales
+    vp = abi.moe_workspace_view()
+    assert abi.lib().moe_workspace_get_view(ctypes.byref(dd), 1 << 40, abi.moe_workspace_bytes(dd),
+                                            ctypes.byref(vp)) == 0
+    assert not vp.xsend_scale                                                     # bf16 send rows
+    lib = abi.lib()
+    dg = abi.moe_dispatch_workspace_bytes(ddg)
+    assert lib.moe_dispatch_dedup(ctypes.byref(ddg), A16, A16, A16, ctypes.byref(m), A16, A16, A16, dg,
+                                  None) == abi.MOE_ERR_ARG
+    assert lib.moe_dispatch_dedup_fp8(ctypes.byref(ddg), A16, A16, A16, ctypes.byref(m), A16, A16, A16, A16,
+                                      dg, None) == abi.MOE_ERR_ARG
+    assert lib.moe_dispatch_dedup_fp8_gemm(ctypes.byref(ddf), A16, A16, A16, ctypes.byref(m), A16, A16, A16, A16,
+                                           A16, dg, None) == abi.MOE_ERR_ARG     # block-scaled config
+    assert lib.moe_dispatch_dedup_fp8_gemm(ctypes.byref(ddg), A16, A16, A16, ctypes.byref(m), A16, A16, None, A16,
+                                           A16, dg, None) == abi.MOE_ERR_ARG     # no expert-row codes
+    assert lib.moe_dispatch_dedup_fp8_gemm(ctypes.byref(ddg), A16, A16, A16, ctypes.byref(m), A16, MIS, A16, A16,
+                                           A16, dg, None) == abi.MOE_ERR_ALIGN
+    assert lib.moe_dispatch_dedup_fp8_gemm(ctypes.byref(ddg), A16, A16, A16, ctypes.byref(m), A16, A16, A16, A16,
+                                           A16, dg - 1, None) == abi.MOE_ERR_WORKSPACE
     c = cfg()
     c.dispatch_dtype = 5
     assert abi.moe_validate_config(c) == abi.MOE_ERR_ARG
@@ -330,7 +360,6 @@ def test_fp8_gemm_validation_workspace_and_weight_bytes():
     assert abi.moe_validate_config(g) == abi.MOE_OK
     assert abi.moe_validate_config(cfg(dispatch_dtype="fp8_gemm", expert="relu")) == abi.MOE_OK
     assert abi.moe_validate_config(cfg(act="f32", dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
-    assert abi.moe_validate_config(cfg(D=4, dedup=True, dispatch_dtype="fp8_gemm")) == abi.MOE_ERR_UNSUPPORTED
     assert abi.moe_validate_config(cfg(F=0, expert="identity", dispatch_dtype="fp8_gemm")) == \
         abi.MOE_ERR_UNSUPPORTED
     assert abi.moe_validate_config(cfg(precision="split_h", dispatch_dtype="fp8_gemm")) == abi.MOE_OK

@@ -84,3 +84,6 @@ def test_algorithmic_work_of_the_bf16_and_fp8_layers():
     T2, d2, rows2, sent = 4096, 7168, 32768, 16000
     ddf = bench.algorithmic(W["dsv3_grouped_dedup_fp8"], rows2, out_bytes=2, h_cols=0, rows_sent=sent)
     assert ddf["dispatch_bytes"] == T2 * d2 * 2 + rows2 * d2 * 2 + 2 * sent * (d2 + 4 * 56)
+    # deduplicated send rows in the FP8 GEMM's format: codes + one scale, and so the expert rows
+    ddg = bench.algorithmic(W["dsv3_full_fp8_gemm_dedup"], rows2, out_bytes=4, h_cols=2048, rows_sent=sent)
+    assert ddg["dispatch_bytes"] == T2 * d2 * 2 + rows2 * (d2 + 4) + 2 * sent * (d2 + 4)

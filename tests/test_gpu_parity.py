@@ -17,6 +17,7 @@ from oracle import moe_oracle as orc
 from routing_dispatch_combine_moe_b300 import abi
 from routing_dispatch_combine_moe_b300 import workloads as wl
 from tests._gpu import (StageBuffers, WorkspaceMap, capacity_of, chain, check_chained_dispatch, check_close,
+                        compare_fp8_rows,
                         check_dispatch_of_oracle_routing, check_layer_close, check_near_tie_count,
                         check_combine, check_dedup, check_dispatch, check_ffn, check_fp8, check_route, cpu,
                         fp8_h_budget, fp8_h_layer_budget, gate_boundary_ties, half_ulp, oracle_dispatch,
@@ -44,6 +45,11 @@ REDUCED = {
     "grouped_dedup_fp8_swiglu": wl.Workload("grouped_dedup_fp8_swiglu", T=700, d=512, E=64, k=6, F=256,
                                             act="bf16", expert="swiglu", D=8, n_groups=8, topk_groups=3, dedup=True,
                                             capacity_factor="1", n_shared=1, dispatch_dtype="fp8"),
+    # row-scaled FP8 send rows handed to the FP8 GEMM: a shared expert (quantized from x on
+    # the receiving side) and drops
+    "grouped_dedup_fp8_gemm": wl.Workload("grouped_dedup_fp8_gemm", T=700, d=512, E=64, k=6, F=256, act="bf16",
+                                          expert="swiglu", D=8, n_groups=8, topk_groups=3, dedup=True,
+                                          capacity_factor="1", n_shared=1, dispatch_dtype="fp8_gemm"),
     "mixtral_fp8": wl.scaled(W["mixtral_fp8_dispatch"], T=512, d=1024, F=1536),
     "decode_fp8": wl.scaled(W["dsv3_decode"], d=1088, F=256, dispatch_dtype="fp8"),  # ragged last block
     "mixtral_fp8_gemm": wl.scaled(W["mixtral_fp8_gemm"], T=512, d=1024, F=1536),
@@ -118,7 +124,7 @@ def test_layer_forward_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", ["grouped_dedup", "grouped_dedup_swiglu", "grouped_dedup_fp8",
-                                  "grouped_dedup_fp8_swiglu"])
+                                  "grouped_dedup_fp8_swiglu", "grouped_dedup_fp8_gemm"])
 def test_dedup_forward_equals_the_direct_forward_bitwise(name):
     """The deduplicated dispatch changes where rows travel, not their values: the layer
     output is the same bits, and the send map in the workspace is the oracle's."""
@@ -375,6 +381,7 @@ FULL["mixtral_fp8_gemm"] = W["mixtral_fp8_gemm"]
 FULL["dsv3_decode_fp8_gemm"] = W["dsv3_decode_fp8_gemm"]
 FULL["mixtral_fp8_experts"] = W["mixtral_fp8_experts"]
 FULL["dsv3_grouped_dedup_fp8"] = W["dsv3_grouped_dedup_fp8"]
+FULL["dsv3_full_fp8_gemm_dedup"] = W["dsv3_full_fp8_gemm_dedup"]
 
 
 # Tokens whose y is compared element by element at full size: 256 on the DeepSeek-V3-shaped
@@ -411,6 +418,12 @@ def test_full_size_sampled(name):
             q = orc.quantize_fp8_blocks(f64(inp["x"][src[torch.from_numpy(rows).cuda()]]))
             np.testing.assert_array_equal(cpu(m.xsend).numpy()[rows], q["codes"])
             np.testing.assert_array_equal(cpu(m.xsend_scale).numpy().astype(np.float64)[rows], q["scales"])
+        elif w.dispatch_dtype == "fp8_gemm":  # codes and row scales of 64 sampled send rows
+            rows = np.random.default_rng(3).choice(s["n_send"], size=min(64, s["n_send"]), replace=False)
+            q = orc.quantize_fp8_rows(f64(inp["x"][src[torch.from_numpy(rows).cuda()]]))
+            np.testing.assert_array_equal(cpu(m.xsend).numpy()[rows], q["codes"])
+            np.testing.assert_array_equal(cpu(m.xsend_scale).numpy().astype(np.float64).reshape(-1)[rows],
+                                          q["scales"])
         else:
             assert torch.equal(m.xsend[:s["n_send"]], inp["x"][src])
         print(f"\n{name}: {s['n_send']} send rows, {s['n_send'] / w.T:.3f} ranks per token")
@@ -423,6 +436,11 @@ def test_full_size_sampled(name):
         q = orc.quantize_fp8_blocks(f64(inp["x"][torch.from_numpy(tok).cuda()]))
         np.testing.assert_array_equal(cpu(m.xq).numpy()[rows], q["codes"])
         np.testing.assert_array_equal(cpu(m.xscale).numpy().astype(np.float64)[rows], q["scales"])
+    if w.dispatch_dtype == "fp8_gemm" and how == "exact":
+        # the FP8 GEMM's input rows (with dedup: as the fan-out wrote them) on 64 sampled rows
+        rows = np.nonzero(d["row_src"] >= 0)[0]
+        rows = np.random.default_rng(1).choice(rows, size=min(64, rows.size), replace=False)
+        compare_fp8_rows(w, m.xq, m.xscale, d["row_src"], inp["x"], rows=rows)
     if w.expert == "identity" and w.dispatch_dtype == "act":
         assert torch.equal(y, inp["x"])
         return
@@ -470,8 +488,8 @@ def test_full_size_sampled(name):
     n_tok = SAMPLED_TOKENS if name == "dsv3_full" else SAMPLED_TOKENS_OTHERS
     if w.dispatch_dtype == "fp8_gemm" and w.expert != "identity":
         # the oracle quantizes every expert a sampled token uses (2F x d weights each, in
-        # float64): 8 tokens, 4 on the decode layer, whose tokens touch 9 of 257 experts each
-        n_tok = 4 if w.T <= 128 else 8
+        # float64): 8 tokens, 4 on the DeepSeek-V3-shaped layers (8 or 9 experts per token)
+        n_tok = 4 if (w.T <= 128 or w.E >= 256) else 8
     tokens = sorted(rng.choice(cand, size=min(n_tok, cand.size), replace=False).tolist())
     y_s, budget = _sampled_y(w, inp, dict(idx=r["idx_full"], G=r["G_full"]), d, tokens)
     err = check_layer_close(name, y[torch.as_tensor(tokens, device="cuda")], y_s, w.act, f"{name} sampled y",
