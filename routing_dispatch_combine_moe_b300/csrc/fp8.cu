@@ -367,8 +367,10 @@ __global__ void __launch_bounds__(256) fanout_fp8_row_kernel(const uint4* __rest
             for (int v = lane; v < vpr; v += 32) to[v] = e4m3_pack8(__ldg(row + v), s_x);
             if (lane == 0) xscale[dj] = ldexpf(1.f, s_x);
         } else {
-            const uint2* from = reinterpret_cast<const uint2*>(sq + size_t(sj) * d);
-            for (int v = lane; v < vpr; v += 32) to[v] = from[v];
+            // d % 16 == 0: both rows are whole 16-byte pieces
+            const uint4* from = reinterpret_cast<const uint4*>(sq + size_t(sj) * d);
+            uint4* to16 = reinterpret_cast<uint4*>(xq + size_t(dj) * d);
+            for (int v = lane; v < d / 16; v += 32) to16[v] = from[v];
             if (lane == 0) xscale[dj] = sscale[sj];
         }
     }
